@@ -1,0 +1,384 @@
+"""Plain, slow, float64 restatement of OSCAR's rotation, codec and decode attention.
+
+TEST INFRASTRUCTURE ONLY: only the tests, `__graft_entry__.smoke()` and the
+CPU-baseline leg of `bench.py` may import this module.  It shares no code,
+header, table or constant generator with the CUDA library and never imports
+it.  Every function is the plain definition or the pages' steps in the pages'
+order; numpy routines (matmul, eigh, sort) serve as single steps and nothing
+is blocked, fused or reordered beyond what the definition states.
+
+Sources (three web pages about the same paper, cited by title and section):
+  [GIST]  gist.science, "OSCAR: Offline Spectral Covariance-Aware Rotation for
+          2-bit KV Cache Quantization", Technical summary, sections 2.1 (theory),
+          2.2 A (offline calibration) and 2.2 B (online serving).
+  [ZAKER] myzaker.com article on OSCAR (Together AI / USYD / UIUC), parts
+          "OSCAR 把旋转对准 attention" (rotation) and
+          "从离线校准到在线推理的 pipeline" (token pool, demotion, decode).
+  [CSDN]  aicoding.csdn.net explainer of OSCAR / OScaR, section 三 (OSCAR):
+          三.1 (offline and inference stages).
+
+Readings where the pages are silent or garbled (the full list, with reasons,
+is kept with the design notes):
+  * Row-vector convention: a rotated key is k~ = k . R, with R = U . H . P.
+  * Eigenvectors ordered by descending eigenvalue; each column's sign is set so
+    that its largest-magnitude entry is positive (ties: lowest index).
+  * Hadamard is Sylvester's, normalised by 1/sqrt(d).
+  * Covariances are uncentred; C_S pools the rows of S.V with
+    S = row-softmax(Q K^T / sqrt(d)); the query covariance of a KV head pools
+    the queries of its whole GQA group.
+  * Clip: symmetric clamp to [-tau, tau] after rotation; tau is the
+    nearest-rank quantile (0.999) of |x . R| over a layer's calibration rows,
+    pooled over its KV heads (our procedure: parity unpinned beyond the
+    library agreeing with this function).
+  * One quantisation group = one token's 128 rotated channels of one KV head;
+    scale s = fp16((max - min) / 3), zero z = fp16(min) (round to nearest
+    even); code = clamp(rint((x - z) / s), 0, 3) with ties to even; s == 0
+    gives code 0.  Dequantised value: c * s + z.
+  * Four codes per byte, channel 4j+i in bits 2i..2i+1 of byte j.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+D_DEFAULT = 128
+PAGE_TOKENS = 16
+SINK_CAP = 64
+RECENT_CAP = 256
+# Page block of one (physical page, KV head): K half then V half; each half is
+# 16 tokens x 32 code bytes followed by 16 (scale, zero) fp16 pairs.
+CODE_BYTES = 32
+HALF_BYTES = PAGE_TOKENS * CODE_BYTES + PAGE_TOKENS * 4     # 576
+BLOCK_BYTES = 2 * HALF_BYTES                                # 1152
+
+
+# --------------------------------------------------------------------------
+# 1. rotation construction   [GIST] 2.1 and 2.2 A; [ZAKER] "OSCAR 把旋转对准 attention"
+# --------------------------------------------------------------------------
+
+def hadamard(d: int) -> np.ndarray:
+    """Orthonormal Sylvester Hadamard matrix: H[i][j] = (-1)^popcount(i & j) / sqrt(d).
+
+    [GIST] 2.2 A (H_Had spreads outlier energy across channels).
+    """
+    if d <= 0 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    h = np.empty((d, d), dtype=np.float64)
+    for i in range(d):
+        for j in range(d):
+            h[i, j] = -1.0 if bin(i & j).count("1") % 2 else 1.0
+    return h / math.sqrt(d)
+
+
+def bit_reverse(i: int, bits: int) -> int:
+    """i with its lowest `bits` bits in reverse order."""
+    r = 0
+    for _ in range(bits):
+        r = (r << 1) | (i & 1)
+        i >>= 1
+    return r
+
+
+def bit_reversal_matrix(d: int) -> np.ndarray:
+    """Permutation P_br with P[i][br(i)] = 1, so (x . P)[j] = x[br(j)].
+
+    [GIST] 2.2 A (P_br interleaves high- and low-variance channels).
+    """
+    bits = int(round(math.log2(d)))
+    p = np.zeros((d, d), dtype=np.float64)
+    for i in range(d):
+        p[i, bit_reverse(i, bits)] = 1.0
+    return p
+
+
+def query_covariance(q: np.ndarray) -> np.ndarray:
+    """C_Q = (1/N) sum_n q_n^T q_n over the N calibration query rows.   [GIST] 2.2 A."""
+    q = np.asarray(q, dtype=np.float64)
+    return q.T @ q / q.shape[0]
+
+
+def score_weighted_values(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """Rows of S . V with S = row-softmax(Q K^T / sqrt(d)): [N_q][d].  [GIST] 2.1, 2.2 A."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = q @ k.T / math.sqrt(q.shape[1])
+    s = s - s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p = p / p.sum(axis=1, keepdims=True)
+    return p @ v
+
+
+def value_covariance(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """C_S = (1/N) V^T S^T S V = (1/N) (S V)^T (S V).   [GIST] 2.1, 2.2 A."""
+    sv = score_weighted_values(q, k, v)
+    return sv.T @ sv / sv.shape[0]
+
+
+def eigenbasis(c: np.ndarray):
+    """(U, eigenvalues): columns of U are eigenvectors of the symmetric C.
+
+    Ordered by descending eigenvalue ("aligns channels with importance"),
+    each column's largest-|entry| made positive (ties: lowest index).
+    [GIST] 2.2 A (eigendecomposition gives U_Q / U_S).
+    """
+    c = np.asarray(c, dtype=np.float64)
+    w, u = np.linalg.eigh(c)
+    order = np.argsort(-w, kind="stable")
+    w = w[order]
+    u = u[:, order].copy()
+    for col in range(u.shape[1]):
+        j = int(np.argmax(np.abs(u[:, col])))
+        if u[j, col] < 0:
+            u[:, col] = -u[:, col]
+    return u, w
+
+
+def compose_rotation(u: np.ndarray) -> np.ndarray:
+    """R = U . H_Had . P_br.   [GIST] 2.2 A formula; [ZAKER] R = U . Hadamard . bit-reversal."""
+    d = u.shape[0]
+    return u @ hadamard(d) @ bit_reversal_matrix(d)
+
+
+def rotation_from_covariance(c: np.ndarray) -> np.ndarray:
+    u, _ = eigenbasis(c)
+    return compose_rotation(u)
+
+
+def clip_threshold(rotated: np.ndarray, quantile: float = 0.999) -> float:
+    """Nearest-rank `quantile` of |x| over every element of the rotated rows.
+
+    [GIST] 2.2 A (per-layer clip thresholds estimated from rotated calibration
+    activations; the procedure itself is this build's choice).
+    """
+    a = np.sort(np.abs(np.asarray(rotated, dtype=np.float64)).ravel())
+    rank = int(math.ceil(quantile * a.size))
+    rank = min(max(rank, 1), a.size)
+    return float(a[rank - 1])
+
+
+# --------------------------------------------------------------------------
+# 2. demotion codec   [ZAKER] pipeline part; [CSDN] 三.1 inference stage
+# --------------------------------------------------------------------------
+
+def rotate(x: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """x . R for row vectors x[..., d] (float64)."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(r, dtype=np.float64)
+
+
+def quantize(x_rot: np.ndarray, tau: float):
+    """Clip to [-tau, tau], then asymmetric 2-bit scale/zero quantisation per group.
+
+    x_rot[..., d]: one group per trailing vector.  Returns (codes uint8 in
+    0..3, scale float16, zero float16).  Codes are decided from the fp16
+    scale and zero that dequantisation will use.
+    [ZAKER] pipeline part (rotate, clip, quantize, pack; scale/zero point).
+    """
+    xc = np.clip(np.asarray(x_rot, dtype=np.float64), -tau, tau)
+    mn = xc.min(axis=-1)
+    mx = xc.max(axis=-1)
+    s16 = ((mx - mn) / 3.0).astype(np.float16)
+    z16 = mn.astype(np.float16)
+    s = s16.astype(np.float64)[..., None]
+    z = z16.astype(np.float64)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = (xc - z) / s
+        c = np.where(s > 0, np.clip(np.rint(u), 0, 3), 0)
+    return c.astype(np.uint8), s16, z16
+
+
+def dequantize(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """x^ = c * s + z (float64).   [ZAKER] pipeline part (scale/zero dequantisation)."""
+    return (codes.astype(np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
+            + np.asarray(zero, dtype=np.float64)[..., None])
+
+
+def demote(x: np.ndarray, r: np.ndarray, tau: float):
+    """Rotate -> clip -> quantise one or many token vectors x[..., d] with one R."""
+    return quantize(rotate(x, r), tau)
+
+
+def pack(codes: np.ndarray) -> np.ndarray:
+    """Four 2-bit codes per byte: byte j = c[4j] | c[4j+1]<<2 | c[4j+2]<<4 | c[4j+3]<<6.
+
+    [ZAKER] pipeline part ("every 4 two-bit values are packed into 1 byte").
+    """
+    c = np.asarray(codes, dtype=np.uint8)
+    c = c.reshape(c.shape[:-1] + (c.shape[-1] // 4, 4))
+    return (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
+
+
+def unpack(packed: np.ndarray) -> np.ndarray:
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.stack([(b >> (2 * i)) & 3 for i in range(4)], axis=-1)
+    return out.reshape(b.shape[:-1] + (b.shape[-1] * 4,)).astype(np.uint8)
+
+
+# --------------------------------------------------------------------------
+# 3. paged history layout (this build's format; the pages fix only "paged")
+# --------------------------------------------------------------------------
+
+def block_offset(page_id: int, kv_head: int, n_kv: int) -> int:
+    """Byte offset of the block of (physical page, KV head) inside the pool."""
+    return (int(page_id) * n_kv + int(kv_head)) * BLOCK_BYTES
+
+
+def token_offsets(slot: int, which: int):
+    """(code offset, scale offset) of a token slot within a block; which 0 = K, 1 = V."""
+    base = which * HALF_BYTES
+    return base + slot * CODE_BYTES, base + PAGE_TOKENS * CODE_BYTES + 4 * slot
+
+
+def store_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
+                  kv_head: int, which: int, packed: np.ndarray, scale16, zero16) -> None:
+    """Place one token's packed codes and (scale, zero) at history position `pos`.
+
+    The page is page_table[b][pos // 16], the slot pos % 16.   [GIST] 2.2 B
+    (paged KV cache).  `pool` is a flat uint8 array of n_pages * n_kv * 1152.
+    """
+    page = int(page_table[b, pos // PAGE_TOKENS])
+    base = block_offset(page, kv_head, n_kv)
+    co, so = token_offsets(pos % PAGE_TOKENS, which)
+    pool[base + co: base + co + CODE_BYTES] = packed
+    pair = np.array([scale16, zero16], dtype=np.float16).view(np.uint8)
+    pool[base + so: base + so + 4] = pair
+
+
+def load_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
+                 kv_head: int, which: int):
+    """(packed[32], scale float16, zero float16) stored for a history position."""
+    page = int(page_table[b, pos // PAGE_TOKENS])
+    base = block_offset(page, kv_head, n_kv)
+    co, so = token_offsets(pos % PAGE_TOKENS, which)
+    packed = pool[base + co: base + co + CODE_BYTES].copy()
+    sz = pool[base + so: base + so + 4].copy().view(np.float16)
+    return packed, sz[0], sz[1]
+
+
+def store_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
+                       pos0: int, packed: np.ndarray, scale16: np.ndarray,
+                       zero16: np.ndarray, which: int) -> None:
+    """store_history for tokens pos0 .. pos0+T-1 of all KV heads: packed[T][n_kv][32]."""
+    t_count = packed.shape[0]
+    pos = pos0 + np.arange(t_count)
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    slots = pos % PAGE_TOKENS
+    heads = np.arange(n_kv)
+    base = (pages[:, None] * n_kv + heads[None, :]) * BLOCK_BYTES          # [T][n_kv]
+    co = base + which * HALF_BYTES + slots[:, None] * CODE_BYTES
+    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slots[:, None]
+    idx = co[..., None] + np.arange(CODE_BYTES)
+    pool[idx] = packed
+    pair = np.stack([scale16, zero16], axis=-1).astype(np.float16).view(np.uint8)  # [T][n_kv][4]
+    pool[so[..., None] + np.arange(4)] = pair
+
+
+def load_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
+                      hist_len: int, which: int):
+    """(codes [T][n_kv][d] uint8, scale [T][n_kv] f16, zero [T][n_kv] f16) for positions < hist_len."""
+    pos = np.arange(hist_len)
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    slots = pos % PAGE_TOKENS
+    heads = np.arange(n_kv)
+    base = (pages[:, None] * n_kv + heads[None, :]) * BLOCK_BYTES
+    co = base + which * HALF_BYTES + slots[:, None] * CODE_BYTES
+    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slots[:, None]
+    packed = pool[co[..., None] + np.arange(CODE_BYTES)]
+    sz = pool[so[..., None] + np.arange(4)].copy().view(np.float16)      # [T][n_kv][2]
+    return unpack(packed), sz[..., 0], sz[..., 1]
+
+
+# --------------------------------------------------------------------------
+# 4. three-segment decode attention   [ZAKER] pipeline part; [GIST] 2.2 B
+# --------------------------------------------------------------------------
+
+def softmax_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray) -> np.ndarray:
+    """o = softmax(q . K^T / sqrt(d)) . V for one query row (float64)."""
+    q = np.asarray(q, dtype=np.float64)
+    if keys.shape[0] == 0:
+        return np.zeros(values.shape[1], dtype=np.float64)
+    s = np.asarray(keys, dtype=np.float64) @ q / math.sqrt(q.shape[0])
+    s = s - s.max()
+    p = np.exp(s)
+    return (p / p.sum()) @ np.asarray(values, dtype=np.float64)
+
+
+def decode_attention(q: np.ndarray, sink_k: np.ndarray, sink_v: np.ndarray,
+                     hist: dict, recent_k: np.ndarray, recent_v: np.ndarray,
+                     r_k: np.ndarray, r_v: np.ndarray) -> np.ndarray:
+    """Decode attention of one request over BF16 sink | INT2 history | BF16 recent.
+
+    q: [H_q][d]; sink_k/v: [Ls][H_kv][d]; recent_k/v: [Lr][H_kv][d] (logical
+    order; attention does not depend on it); hist: dict with codes_k/codes_v
+    [Lh][H_kv][d], scale_k/zero_k/scale_v/zero_v [Lh][H_kv]; r_k, r_v:
+    [H_kv][d][d].  Query head h reads KV head h // (H_q / H_kv).
+
+    The plain definition: every history token is dequantised and rotated back
+    with R^T, the three segments are concatenated and one softmax is taken.
+    [ZAKER] pipeline part (BF16 sink 64 | INT2 history | BF16 recent 256);
+    [GIST] 2.2 B (inverse rotation inside attention); [CSDN] 三.1.
+    """
+    n_q = q.shape[0]
+    n_kv = r_k.shape[0]
+    g = n_q // n_kv
+    out = np.zeros((n_q, q.shape[1]), dtype=np.float64)
+    for kv in range(n_kv):
+        k_hist = dequantize(hist["codes_k"][:, kv], hist["scale_k"][:, kv],
+                            hist["zero_k"][:, kv]) @ np.asarray(r_k[kv], dtype=np.float64).T
+        v_hist = dequantize(hist["codes_v"][:, kv], hist["scale_v"][:, kv],
+                            hist["zero_v"][:, kv]) @ np.asarray(r_v[kv], dtype=np.float64).T
+        keys = np.concatenate([np.asarray(sink_k[:, kv], dtype=np.float64), k_hist,
+                               np.asarray(recent_k[:, kv], dtype=np.float64)], axis=0)
+        vals = np.concatenate([np.asarray(sink_v[:, kv], dtype=np.float64), v_hist,
+                               np.asarray(recent_v[:, kv], dtype=np.float64)], axis=0)
+        for h in range(kv * g, (kv + 1) * g):
+            out[h] = softmax_attention(q[h], keys, vals)
+    return out
+
+
+def partial_state(q: np.ndarray, keys: np.ndarray, values: np.ndarray):
+    """(m, l, o) of one segment: m = max score, l = sum exp(s - m), o = sum exp(s - m) v.
+
+    An empty segment is (-inf, 0, 0).   [ZAKER] pipeline part (online softmax merge).
+    """
+    d = values.shape[1]
+    if keys.shape[0] == 0:
+        return -math.inf, 0.0, np.zeros(d)
+    s = np.asarray(keys, dtype=np.float64) @ np.asarray(q, dtype=np.float64) / math.sqrt(len(q))
+    m = float(s.max())
+    p = np.exp(s - m)
+    return m, float(p.sum()), p @ np.asarray(values, dtype=np.float64)
+
+
+def merge_states(states) -> np.ndarray:
+    """Online-softmax merge of segment states into the normalised output.
+
+    m = max m_i, l = sum l_i e^(m_i - m), o = sum o_i e^(m_i - m) / l; empty
+    segments (l = 0) are skipped and an all-empty merge gives zeros.
+    """
+    live = [(m, l, o) for (m, l, o) in states if l > 0]
+    if not live:
+        return np.zeros_like(states[0][2])
+    m = max(s[0] for s in live)
+    l = sum(s[1] * math.exp(s[0] - m) for s in live)
+    o = sum(s[2] * math.exp(s[0] - m) for s in live)
+    return o / l
+
+
+# --------------------------------------------------------------------------
+# 5. storage accounting   [ZAKER] "小模型也能守住高难推理"; [GIST] 4 (memory)
+# --------------------------------------------------------------------------
+
+def kv_bytes_per_history_token(n_kv: int, d: int = D_DEFAULT) -> int:
+    """Bytes per INT2 history token per layer: 2 (K,V) x n_kv x (d/4 codes + 4 s/z)."""
+    return 2 * n_kv * (d // 4 + 4)
+
+
+def effective_bits_per_element(ctx: int, d: int = D_DEFAULT,
+                               sink: int = SINK_CAP, recent: int = RECENT_CAP) -> float:
+    """Average stored bits per K/V element over a context of `ctx` tokens."""
+    bf16_tokens = min(ctx, sink + recent)
+    hist = ctx - bf16_tokens
+    bits = bf16_tokens * d * 16 + hist * (2 * d + 32)
+    return bits / (ctx * d)

@@ -1,0 +1,387 @@
+"""Pins of the float64 oracle against what the pages and mathematics fix.
+
+Every check here compares the oracle with something other than itself: values
+the pages print, hand-derived worked examples (tests/golden), closed forms,
+textbook special cases, invariants, or brute force on tiny inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from conftest import golden_lines
+
+
+def _orthogonal(d, seed):
+    # Orthogonal matrix from a QR factorisation (a different library routine
+    # from the eigensolver under test).
+    g = synth.generator(seed, 99)
+    q, r = np.linalg.qr(g.standard_normal((d, d)))
+    return q * np.sign(np.diag(r))
+
+
+# ---------------------------------------------------------------- Hadamard, P_br
+
+@pytest.mark.parametrize("d", [2, 4, 8, 16, 128])
+def test_hadamard_matches_sylvester_recursion(d):
+    h = np.array([[1.0]])
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    np.testing.assert_array_equal(O.hadamard(d), h / math.sqrt(d))
+    np.testing.assert_allclose(O.hadamard(d) @ O.hadamard(d), np.eye(d), atol=1e-14)
+
+
+def test_bit_reversal_golden_and_involution():
+    for line in golden_lines("bit_reversal.txt"):
+        d, rest = line.split(":")
+        d = int(d)
+        want = [int(x) for x in rest.split()]
+        p = O.bit_reversal_matrix(d)
+        got = [int(np.argmax(p[i])) for i in range(d)]
+        assert got == want
+    p = O.bit_reversal_matrix(128)
+    np.testing.assert_array_equal(p, p.T)
+    np.testing.assert_array_equal(p @ p, np.eye(128))
+
+
+# ---------------------------------------------------------------- eigenbasis, R
+
+def test_eigenbasis_of_diagonal_is_sorted_permutation():
+    diag = np.array([3.0, 7.0, 1.0, 5.0])
+    u, w = O.eigenbasis(np.diag(diag))
+    np.testing.assert_array_equal(w, [7.0, 5.0, 3.0, 1.0])
+    want = np.zeros((4, 4))
+    for col, row in enumerate([1, 3, 0, 2]):
+        want[row, col] = 1.0
+    np.testing.assert_array_equal(u, want)
+
+
+def test_eigenbasis_recovers_constructed_spectrum():
+    d = 128
+    q = _orthogonal(d, 1)
+    lam = np.linspace(400.0, 0.5, d) * (1 + 0.01 * np.arange(d) / d)  # distinct, gaps >= 1%
+    perm = synth.generator(2, 0).permutation(d)
+    c = q[:, perm] @ np.diag(lam[perm]) @ q[:, perm].T
+    u, w = O.eigenbasis(c)
+    np.testing.assert_allclose(w, lam, rtol=1e-12)
+    for k in range(d):
+        v = q[:, k].copy()
+        j = int(np.argmax(np.abs(v)))
+        v = v if v[j] > 0 else -v
+        np.testing.assert_allclose(u[:, k], v, atol=1e-10)
+    np.testing.assert_allclose(u.T @ u, np.eye(d), atol=1e-12)
+    np.testing.assert_allclose(c @ u, u * w, atol=1e-12 * np.linalg.norm(c))
+
+
+def test_rotation_of_diagonal_covariance_is_hadamard_then_bitreversal():
+    # Descending diagonal C gives U = I, so R must be H . P_br elementwise:
+    # R[i][j] = (-1)^popcount(i & br(j)) / sqrt(d).
+    d = 16
+    r = O.rotation_from_covariance(np.diag(np.arange(d, 0, -1, dtype=float)))
+    br = [int(x) for x in golden_lines("bit_reversal.txt")[1].split(":")[1].split()]
+    for i in range(d):
+        for j in range(d):
+            want = (-1.0) ** bin(i & br[j]).count("1") / 4.0
+            assert r[i, j] == pytest.approx(want, abs=1e-15)
+
+
+def test_rotation_is_orthogonal_and_composed_u_first():
+    d = 128
+    cal = synth.calibration_set(7, 0, 0, np.array([3, 40, 77, 100]), n_q=1024, n_k=256)
+    c = O.query_covariance(cal["q"])
+    r = O.rotation_from_covariance(c)
+    np.testing.assert_allclose(r @ r.T, np.eye(d), atol=1e-12)
+    np.testing.assert_allclose(r.T @ r, np.eye(d), atol=1e-12)
+    u, _ = O.eigenbasis(c)
+    hp = np.array([[(-1.0) ** bin(i & O.bit_reverse(j, 7)).count("1") for j in range(d)]
+                   for i in range(d)]) / math.sqrt(d)
+    np.testing.assert_allclose(r, u @ hp, atol=1e-13)
+
+
+# ---------------------------------------------------------------- covariances
+
+def test_query_covariance_brute_force():
+    g = synth.generator(3, 0)
+    q = g.standard_normal((5, 4))
+    want = np.zeros((4, 4))
+    for n in range(5):
+        for i in range(4):
+            for j in range(4):
+                want[i, j] += q[n, i] * q[n, j] / 5
+    np.testing.assert_allclose(O.query_covariance(q), want, atol=1e-15)
+
+
+def test_score_weighted_values_brute_force_and_one_hot():
+    g = synth.generator(4, 0)
+    d = 4
+    q = g.standard_normal((3, d))
+    k = g.standard_normal((5, d))
+    v = g.standard_normal((5, d))
+    want = np.zeros((3, d))
+    for n in range(3):
+        s = [sum(q[n, c] * k[t, c] for c in range(d)) / 2.0 for t in range(5)]
+        e = [math.exp(x) for x in s]
+        for t in range(5):
+            want[n] += e[t] / sum(e) * v[t]
+    np.testing.assert_allclose(O.score_weighted_values(q, k, v), want, atol=1e-14)
+    # S one-hot: each query matches exactly one key, so C_S = V_sel^T V_sel / N
+    d = 8
+    k = 100.0 * np.eye(d)
+    sel = np.array([2, 5, 5, 0])
+    q = 100.0 * np.eye(d)[sel]
+    v = g.standard_normal((d, d))
+    np.testing.assert_allclose(O.value_covariance(q, k, v), v[sel].T @ v[sel] / 4, atol=1e-12)
+
+
+def test_clip_threshold_nearest_rank():
+    g = synth.generator(5, 0)
+    x = np.arange(1, 1001, dtype=float) * g.choice([-1.0, 1.0], size=1000)
+    x = g.permutation(x).reshape(10, 100)
+    assert O.clip_threshold(x, 0.999) == 999.0
+    assert O.clip_threshold(x, 0.5) == 500.0
+    assert O.clip_threshold(x, 1.0) == 1000.0
+
+
+# ---------------------------------------------------------------- codec
+
+def test_fp16_rounding_golden():
+    for line in golden_lines("fp16_rounding.txt"):
+        val, bits = [s.strip() for s in line.split("->")]
+        got = np.array([float(val)]).astype(np.float16).view(np.uint16)[0]
+        assert got == int(bits, 16), line
+
+
+def test_pack_golden_and_round_trip():
+    for line in golden_lines("pack_bytes.txt"):
+        codes, byte = line.split("->")
+        c = np.array([int(x) for x in codes.split()], dtype=np.uint8)
+        assert O.pack(c)[0] == int(byte)
+    allb = np.arange(256, dtype=np.uint8)
+    np.testing.assert_array_equal(O.pack(O.unpack(allb[None, :])), allb[None, :])
+    c = synth.generator(6, 0).integers(0, 4, size=(7, 128)).astype(np.uint8)
+    np.testing.assert_array_equal(O.unpack(O.pack(c)), c)
+
+
+def _worked_cases():
+    d = 128
+    x = -2.0 + 0.5 * (np.arange(d) % 4)
+    shift = np.zeros((d, d))
+    for i in range(d):
+        shift[i, (i + 1) % d] = 1.0
+    return x, {"shift": (shift, 8.0), "clip": (np.eye(d), 1.5),
+               "bitrev": (O.bit_reversal_matrix(d), 8.0)}
+
+
+def test_quantize_worked_examples():
+    x, cases = _worked_cases()
+    for line in golden_lines("quantize_worked.txt"):
+        name, rest = line.split(":")
+        toks = rest.split()
+        want_bytes = []
+        for t in toks[2:]:
+            v, n = t.split("*")
+            want_bytes += [int(v)] * int(n)
+        r, tau = cases[name]
+        codes, s16, z16 = O.demote(x[None, :], r, tau)
+        assert s16.view(np.uint16)[0] == int(toks[0], 16), name
+        assert z16.view(np.uint16)[0] == int(toks[1], 16), name
+        np.testing.assert_array_equal(O.pack(codes)[0], want_bytes, err_msg=name)
+
+
+def test_quantize_invariants_brute_force():
+    g = synth.generator(8, 0)
+    x = g.standard_normal((64, 128)) * g.uniform(0.1, 30, size=(64, 1))
+    tau = 12.0
+    codes, s16, z16 = O.quantize(x, tau)
+    assert codes.max() <= 3
+    xc = np.clip(x, -tau, tau)
+    s = s16.astype(float)
+    z = z16.astype(float)
+    for r in range(64):
+        assert codes[r, np.argmin(xc[r])] == 0
+        assert codes[r, np.argmax(xc[r])] == 3
+        for j in range(128):
+            errs = [abs(xc[r, j] - (c * s[r] + z[r])) for c in range(4)]
+            best = int(np.argmin(errs))
+            if sorted(errs)[1] - sorted(errs)[0] > 1e-9 * s[r]:
+                assert codes[r, j] == best
+        xhat = codes[r] * s[r] + z[r]
+        assert np.max(np.abs(xhat - xc[r])) <= s[r] / 2 + 2e-3 * (abs(z[r]) + 3 * s[r])
+
+
+def test_constant_group_gives_zero_scale_and_codes():
+    codes, s16, z16 = O.quantize(np.full((1, 128), 1.25), 8.0)
+    assert s16[0] == 0 and z16[0] == np.float16(1.25)
+    assert not codes.any()
+    np.testing.assert_array_equal(O.dequantize(codes, s16, z16), np.full((1, 128), 1.25))
+
+
+# ---------------------------------------------------------------- paged layout
+
+def test_page_layout_offsets_and_round_trip():
+    # The block of (page 3, KV head 1) with 2 KV heads starts at (3*2+1)*1152;
+    # V half at +576; slot 5 codes at +5*32; its (scale, zero) at +512+4*5.
+    assert O.block_offset(3, 1, 2) == 8064
+    assert O.token_offsets(5, 1) == (576 + 160, 576 + 512 + 20)
+    assert O.token_offsets(0, 0) == (0, 512)
+    n_kv = 2
+    table, n_pages = synth.page_table(9, [37], n_extra_pages=1)
+    pool = np.zeros(n_pages * n_kv * O.BLOCK_BYTES, dtype=np.uint8)
+    g = synth.generator(9, 1)
+    packed = g.integers(0, 256, size=(37, n_kv, 32)).astype(np.uint8)
+    s = g.uniform(0.1, 2, size=(37, n_kv)).astype(np.float16)
+    z = g.uniform(-3, 0, size=(37, n_kv)).astype(np.float16)
+    O.store_history_bulk(pool, table, n_kv, 0, 0, packed, s, z, which=1)
+    for pos in (0, 15, 16, 36):
+        for h in range(n_kv):
+            pk, ss, zz = O.load_history(pool, table, n_kv, 0, pos, h, 1)
+            np.testing.assert_array_equal(pk, packed[pos, h])
+            assert ss == s[pos, h] and zz == z[pos, h]
+            page = table[0, pos // 16]
+            base = (page * n_kv + h) * 1152 + 576 + (pos % 16) * 32
+            np.testing.assert_array_equal(pool[base:base + 32], packed[pos, h])
+    codes, s2, z2 = O.load_history_bulk(pool, table, n_kv, 0, 37, 1)
+    np.testing.assert_array_equal(O.pack(codes), packed)
+    np.testing.assert_array_equal(s2, s)
+
+
+# ---------------------------------------------------------------- attention
+
+def test_softmax_scale_closed_form():
+    d = 128
+    q = np.zeros(d); q[0] = 4.0
+    keys = np.zeros((2, d)); keys[0, 0] = 2.0
+    vals = np.zeros((2, d)); vals[0, 1] = 1.0
+    w1 = 1.0 / (1.0 + math.exp(-8.0 / math.sqrt(128.0)))
+    o = O.softmax_attention(q, keys, vals)
+    assert o[1] == pytest.approx(w1, abs=1e-15)
+    assert np.count_nonzero(o) == 1
+
+
+def test_merge_equals_one_shot_softmax():
+    g = synth.generator(10, 0)
+    d = 8
+    q = g.standard_normal(d) * 3
+    keys = g.standard_normal((11, d)) * 3
+    vals = g.standard_normal((11, d))
+    one_shot = O.softmax_attention(q, keys, vals)
+    for cuts in ([0, 11], [0, 4, 11], [0, 1, 2, 7, 11], [0, 0, 5, 5, 11]):
+        states = [O.partial_state(q, keys[a:b], vals[a:b]) for a, b in zip(cuts, cuts[1:])]
+        np.testing.assert_allclose(O.merge_states(states), one_shot, atol=1e-13)
+    empty = O.partial_state(q, keys[:0], vals[:0])
+    assert empty[0] == -math.inf and empty[1] == 0.0
+    np.testing.assert_array_equal(O.merge_states([empty]), np.zeros(d))
+
+
+def test_attention_special_cases():
+    d = 16
+    g = synth.generator(11, 0)
+    q = g.standard_normal(d)
+    same = np.tile(g.standard_normal(d), (9, 1))
+    vals = g.standard_normal((9, d))
+    np.testing.assert_allclose(O.softmax_attention(q, same, vals), vals.mean(0), atol=1e-14)
+    keys = g.standard_normal((9, d))
+    keys[4] = 60.0 * q / np.linalg.norm(q) * math.sqrt(d)
+    np.testing.assert_allclose(O.softmax_attention(q, keys, vals), vals[4], atol=1e-12)
+
+
+def _tiny_state(seed, n_kv=2, g=2, d=128, ls=3, lh=21, lr=5, tau=6.0):
+    rng = synth.generator(seed, 0)
+    rk = np.stack([_orthogonal(d, seed * 10 + h) for h in range(n_kv)])
+    rv = np.stack([_orthogonal(d, seed * 10 + 5 + h) for h in range(n_kv)])
+    hk = rng.standard_normal((lh, n_kv, d)) * 3
+    hv = rng.standard_normal((lh, n_kv, d)) * 3
+    hist = {}
+    for name, x, r in (("k", hk, rk), ("v", hv, rv)):
+        codes = np.zeros((lh, n_kv, d), np.uint8)
+        sc = np.zeros((lh, n_kv), np.float16)
+        ze = np.zeros((lh, n_kv), np.float16)
+        for h in range(n_kv):
+            codes[:, h], sc[:, h], ze[:, h] = O.demote(x[:, h], r[h], tau)
+        hist["codes_" + name], hist["scale_" + name], hist["zero_" + name] = codes, sc, ze
+    st = dict(q=rng.standard_normal((n_kv * g, d)) * 2,
+              sink_k=rng.standard_normal((ls, n_kv, d)), sink_v=rng.standard_normal((ls, n_kv, d)),
+              recent_k=rng.standard_normal((lr, n_kv, d)), recent_v=rng.standard_normal((lr, n_kv, d)),
+              hist=hist, r_k=rk, r_v=rv)
+    return st
+
+
+def test_history_token_equals_same_token_in_bf16_segment():
+    # A dequantised history token, rotated back with R^T, must act exactly like
+    # the same vector stored unquantised: pins the inverse rotation's direction.
+    st = _tiny_state(12)
+    hist = st["hist"]
+    kv_keys = []
+    for name, r in (("k", st["r_k"]), ("v", st["r_v"])):
+        x = O.dequantize(hist["codes_" + name][-1:], hist["scale_" + name][-1:],
+                         hist["zero_" + name][-1:])            # [1][n_kv][d] rotated
+        kv_keys.append(np.einsum("thd,hed->the", x, r))        # x . R^T per head
+    a = O.decode_attention(st["q"], st["sink_k"], st["sink_v"], hist, st["recent_k"],
+                           st["recent_v"], st["r_k"], st["r_v"])
+    short = {k: v[:-1] for k, v in hist.items()}
+    b = O.decode_attention(st["q"], st["sink_k"], st["sink_v"], short,
+                           np.concatenate([st["recent_k"], kv_keys[0]]),
+                           np.concatenate([st["recent_v"], kv_keys[1]]), st["r_k"], st["r_v"])
+    np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_rotation_invariance_of_attention():
+    g = synth.generator(13, 0)
+    d = 128
+    r = _orthogonal(d, 13)
+    q = g.standard_normal(d)
+    keys = g.standard_normal((17, d))
+    vals = g.standard_normal((17, d))
+    plain = O.softmax_attention(q, keys, vals)
+    rotated = O.softmax_attention(q @ r, keys @ r, vals @ r) @ r.T
+    np.testing.assert_allclose(rotated, plain, atol=1e-12)
+
+
+def test_gqa_head_mapping_and_empty_segments():
+    d = 128
+    n_kv, g = 2, 3
+    z = lambda n: np.zeros((n, n_kv, d))
+    hist = {"codes_k": np.zeros((0, n_kv, d), np.uint8), "codes_v": np.zeros((0, n_kv, d), np.uint8),
+            "scale_k": np.zeros((0, n_kv), np.float16), "zero_k": np.zeros((0, n_kv), np.float16),
+            "scale_v": np.zeros((0, n_kv), np.float16), "zero_v": np.zeros((0, n_kv), np.float16)}
+    rv = z(4)
+    rv[:, 0] = 1.0
+    rv[:, 1] = 2.0
+    q = synth.generator(14, 0).standard_normal((n_kv * g, d))
+    eye = np.stack([np.eye(d)] * n_kv)
+    out = O.decode_attention(q, z(0), z(0), hist, synth.generator(14, 1).standard_normal((4, n_kv, d)),
+                             rv, eye, eye)
+    np.testing.assert_allclose(out[:g], 1.0, atol=1e-14)
+    np.testing.assert_allclose(out[g:], 2.0, atol=1e-14)
+
+
+def test_three_segments_equal_one_shot_over_concatenation():
+    st = _tiny_state(15)
+    hist = st["hist"]
+    out = O.decode_attention(st["q"], st["sink_k"], st["sink_v"], hist, st["recent_k"],
+                             st["recent_v"], st["r_k"], st["r_v"])
+    g = st["q"].shape[0] // st["r_k"].shape[0]
+    for h in range(st["q"].shape[0]):
+        kv = h // g
+        parts = []
+        parts.append(O.partial_state(st["q"][h], st["sink_k"][:, kv], st["sink_v"][:, kv]))
+        kh = O.dequantize(hist["codes_k"][:, kv], hist["scale_k"][:, kv], hist["zero_k"][:, kv])
+        vh = O.dequantize(hist["codes_v"][:, kv], hist["scale_v"][:, kv], hist["zero_v"][:, kv])
+        # history partial in the rotated domain: q.R_K against c*s+z, output rotated back once
+        m, l, o = O.partial_state(st["q"][h] @ st["r_k"][kv], kh, vh)
+        parts.append((m, l, o @ st["r_v"][kv].T))
+        parts.append(O.partial_state(st["q"][h], st["recent_k"][:, kv], st["recent_v"][:, kv]))
+        np.testing.assert_allclose(O.merge_states(parts), out[h], atol=1e-11)
+
+
+# ---------------------------------------------------------------- accounting
+
+def test_effective_bits_match_printed_values():
+    for line in golden_lines("effective_bits.txt"):
+        ctx, printed = line.split("->")
+        assert round(O.effective_bits_per_element(int(ctx)), 2) == float(printed)
+    # 576 B per history token-layer (8 KV heads) against 4096 B in BF16: 7.11x
+    assert O.kv_bytes_per_history_token(8) == 576
+    assert 4096 / O.kv_bytes_per_history_token(8) == pytest.approx(7.111, abs=1e-3)
