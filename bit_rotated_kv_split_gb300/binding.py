@@ -1,0 +1,150 @@
+"""ctypes binding of liboscar.so (include/oscar.h): argument marshalling only.
+
+Every function keeps the C name and forwards torch tensors as raw device or
+host pointers; all computation happens inside the library.  Importing this
+module loads the library and raises if it is missing - there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_double, c_float, c_int32, c_int64, c_size_t, c_void_p
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liboscar.so")
+
+OSCAR_OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE", 4: "CUDA",
+                5: "NO_CONVERGENCE", 6: "UNSUPPORTED"}
+DEV_PAGE_BOUNDS, DEV_LENGTH, DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+
+class OscarError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS_NAMES.get(status, "?"), status))
+
+
+class LayerDesc(ctypes.Structure):
+    """Mirror of `oscar_layer_desc`."""
+    _fields_ = [
+        ("batch", c_int32), ("n_q_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
+        ("sink_cap", c_int32), ("recent_cap", c_int32), ("max_pages_per_seq", c_int32),
+        ("max_hist", c_int32), ("n_pages", c_int64), ("tau_k", c_float), ("tau_v", c_float),
+        ("pages", c_void_p), ("page_table", c_void_p), ("hist_len", c_void_p),
+        ("sink_k", c_void_p), ("sink_v", c_void_p), ("sink_len", c_void_p),
+        ("recent_k", c_void_p), ("recent_v", c_void_p), ("recent_len", c_void_p),
+        ("recent_start", c_void_p), ("r_k", c_void_p), ("r_v", c_void_p), ("dev_status", c_void_p),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("liboscar.so is not built (%s); run bit_rotated_kv_split_gb300.build" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P = c_void_p
+    sig = {
+        "oscar_status_string": (ctypes.c_char_p, [c_int32]),
+        "oscar_abi_version": (c_int32, []),
+        "oscar_build_rotation": (c_int32, [P, c_int64, c_int32, P, P]),
+        "oscar_score_weighted_rows": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_double, P]),
+        "oscar_clip_threshold": (c_int32, [P, c_int64, c_int32, c_int32, P, c_double, P]),
+        "oscar_quantize_append": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
+                                            P, P, c_int32, P, P, P]),
+        "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
+                                             ctypes.POINTER(c_size_t), P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _check(fn, status):
+    if status != OSCAR_OK:
+        raise OscarError(fn, status)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def oscar_status_string(status: int) -> str:
+    return lib.oscar_status_string(status).decode()
+
+
+def oscar_abi_version() -> int:
+    return lib.oscar_abi_version()
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def oscar_build_rotation(x: np.ndarray):
+    """(R [d][d], eigenvalues [d]) from calibration rows x [n][d] (host float64)."""
+    x = _f64(x)
+    n, d = x.shape
+    r = np.empty((d, d), dtype=np.float64)
+    w = np.empty(d, dtype=np.float64)
+    _check("oscar_build_rotation", lib.oscar_build_rotation(x.ctypes.data, n, d, r.ctypes.data, w.ctypes.data))
+    return r, w
+
+
+def oscar_score_weighted_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float = None):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    d = q.shape[1]
+    out = np.empty((q.shape[0], d), dtype=np.float64)
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    _check("oscar_score_weighted_rows", lib.oscar_score_weighted_rows(
+        q.ctypes.data, q.shape[0], k.ctypes.data, v.ctypes.data, k.shape[0], d, scale, out.ctypes.data))
+    return out
+
+
+def oscar_clip_threshold(acts: np.ndarray, r: np.ndarray, quantile: float = 0.999) -> float:
+    """acts [n_heads][rows][d], r [n_heads][d][d] (host float64)."""
+    acts, r = _f64(acts), _f64(r)
+    h, rows, d = acts.shape
+    tau = c_double(0.0)
+    _check("oscar_clip_threshold", lib.oscar_clip_threshold(
+        acts.ctypes.data, rows, h, d, r.ctypes.data, quantile, ctypes.byref(tau)))
+    return tau.value
+
+
+def oscar_quantize_append(desc: LayerDesc, k_src, v_src, src_rows: int, row_stride: int, src_index,
+                          dst_req, dst_pos, n: int, new_k=None, new_v=None, stream=None) -> None:
+    _check("oscar_quantize_append", lib.oscar_quantize_append(
+        ctypes.byref(desc), _ptr(k_src), _ptr(v_src), int(src_rows), int(row_stride), _ptr(src_index),
+        _ptr(dst_req), _ptr(dst_pos), int(n), _ptr(new_k), _ptr(new_v), _stream(stream)))
+
+
+def oscar_decode_workspace_bytes(desc: LayerDesc) -> int:
+    size = c_size_t(0)
+    _check("oscar_decode_attention", lib.oscar_decode_attention(
+        ctypes.byref(desc), None, None, None, ctypes.byref(size), None))
+    return size.value
+
+
+def oscar_decode_attention(desc: LayerDesc, q, out, workspace, workspace_bytes: int = None,
+                           stream=None) -> None:
+    size = c_size_t(workspace.numel() * workspace.element_size() if workspace_bytes is None
+                    else workspace_bytes)
+    _check("oscar_decode_attention", lib.oscar_decode_attention(
+        ctypes.byref(desc), _ptr(q), _ptr(out), _ptr(workspace), ctypes.byref(size), _stream(stream)))

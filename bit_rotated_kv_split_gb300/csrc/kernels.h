@@ -1,0 +1,85 @@
+// Internal interface between the C-ABI layer (oscar_api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace oscar {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 16;
+constexpr int kBlockBytes = 1152;
+constexpr int kHalfBytes = 576;
+constexpr int kPartStride = 132;  // floats per (split, head) partial: m, l, pad, pad, o[128]
+
+// ---------------------------------------------------------------- demotion
+struct DemoteParams {
+  uint8_t* pages;
+  const int32_t* page_table;
+  int32_t* dev_status;
+  uint16_t* k_src;
+  uint16_t* v_src;
+  int64_t src_rows;
+  int64_t row_stride;
+  const int32_t* src_index;
+  const int32_t* dst_req;
+  const int32_t* dst_pos;
+  const uint16_t* new_k;
+  const uint16_t* new_v;
+  const float* r_k;
+  const float* r_v;
+  float tau_k, tau_v;
+  int32_t n, batch, n_kv, max_pages;
+  int64_t n_pages;
+};
+
+cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode
+struct DecodeParams {
+  // cache
+  const uint8_t* pages;
+  const int32_t* page_table;
+  const int32_t* hist_len;
+  const uint16_t* sink_k;
+  const uint16_t* sink_v;
+  const int32_t* sink_len;
+  const uint16_t* recent_k;
+  const uint16_t* recent_v;
+  const int32_t* recent_len;
+  const int32_t* recent_start;
+  const float* r_k;
+  const float* r_v;
+  int32_t* dev_status;
+  // io
+  const uint16_t* q;
+  float* out;
+  // workspace views
+  uint32_t* counters;   // [pairs]
+  uint32_t* qfrag;      // [pairs][NT][8][32][2]
+  float* qaux;          // [pairs][G][2]
+  float* partials;      // [pairs][n_splits][G][kPartStride]
+  // dims
+  int32_t batch, n_kv, group, sink_cap, recent_cap, max_pages;
+  int64_t n_pages;
+  int32_t max_hist;
+  // split plan
+  int32_t n_hist_splits, n_bf16_splits, pages_per_split, vpages_per_split;
+  // scale of the PV B operand (power of two) and its inverse times 2^24
+  float sigma_v, pv_unscale;
+};
+
+struct DecodePlan {
+  int32_t n_hist_splits, n_bf16_splits, pages_per_split, vpages_per_split;
+  size_t off_counters, off_qfrag, off_qaux, off_partials, total_bytes;
+};
+
+// Split plan and workspace layout for the current device; returns the
+// number of CTAs per SM the split kernel reaches, or <= 0 on a CUDA error.
+int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, int max_hist,
+                DecodePlan* plan, cudaError_t* err);
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace oscar

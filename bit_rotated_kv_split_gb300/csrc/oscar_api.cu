@@ -1,0 +1,173 @@
+// C-ABI entry points: host validation, split planning and kernel launches.
+// Every check runs before any launch; a rejected call launches nothing.
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.h"
+#include "oscar.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+oscar_status check_desc(const oscar_layer_desc* d, bool need_cache_segments) {
+  if (!d) return OSCAR_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->n_kv_heads < 1 || d->n_q_heads < 1 || d->head_dim != OSCAR_HEAD_DIM)
+    return OSCAR_ERR_INVALID_ARG;
+  if (d->n_q_heads % d->n_kv_heads) return OSCAR_ERR_INVALID_ARG;
+  if (d->sink_cap < 0 || d->recent_cap < 0 || d->sink_cap % OSCAR_PAGE_TOKENS ||
+      d->recent_cap % OSCAR_PAGE_TOKENS)
+    return OSCAR_ERR_INVALID_ARG;
+  if (d->max_pages_per_seq < 1 || d->n_pages < 1 || d->n_pages > INT32_MAX) return OSCAR_ERR_INVALID_ARG;
+  if (d->max_hist < 0 || int64_t(d->max_hist) > int64_t(d->max_pages_per_seq) * OSCAR_PAGE_TOKENS)
+    return OSCAR_ERR_INVALID_ARG;
+  // 2 tau / 3 must fit fp16 for the stored scale; tau > 0 and finite
+  if (!(d->tau_k > 0.f) || !(d->tau_v > 0.f) || !(d->tau_k <= 65504.f) || !(d->tau_v <= 65504.f))
+    return OSCAR_ERR_INVALID_ARG;
+  if (!d->pages || !d->page_table || !d->r_k || !d->r_v) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(d->pages, 128) || !aligned(d->r_k, 16) || !aligned(d->r_v, 16) ||
+      !aligned(d->page_table, 4))
+    return OSCAR_ERR_ALIGNMENT;
+  if (need_cache_segments) {
+    if (!d->hist_len || !d->sink_len || !d->recent_len || !d->recent_start)
+      return OSCAR_ERR_INVALID_ARG;
+    if ((d->sink_cap > 0 && (!d->sink_k || !d->sink_v)) ||
+        (d->recent_cap > 0 && (!d->recent_k || !d->recent_v)))
+      return OSCAR_ERR_INVALID_ARG;
+    if (!aligned(d->sink_k, 16) || !aligned(d->sink_v, 16) || !aligned(d->recent_k, 16) ||
+        !aligned(d->recent_v, 16))
+      return OSCAR_ERR_ALIGNMENT;
+  }
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" const char* oscar_status_string(oscar_status s) {
+  switch (s) {
+    case OSCAR_OK: return "ok";
+    case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+    case OSCAR_ERR_ALIGNMENT: return "misaligned pointer";
+    case OSCAR_ERR_WORKSPACE: return "workspace missing or too small";
+    case OSCAR_ERR_CUDA: return "CUDA error";
+    case OSCAR_ERR_NO_CONVERGENCE: return "eigensolver did not converge";
+    case OSCAR_ERR_UNSUPPORTED: return "unsupported configuration";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int32_t oscar_abi_version(void) { return OSCAR_ABI_VERSION; }
+
+extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint16_t* k_src,
+                                              uint16_t* v_src, int64_t src_rows,
+                                              int64_t row_stride,
+                                              const int32_t* src_index, const int32_t* dst_req,
+                                              const int32_t* dst_pos, int32_t n,
+                                              const uint16_t* new_k, const uint16_t* new_v,
+                                              void* stream) {
+  oscar_status st = check_desc(desc, false);
+  if (st != OSCAR_OK) return st;
+  if (n < 0) return OSCAR_ERR_INVALID_ARG;
+  if (n == 0) return OSCAR_OK;
+  if (!k_src || !v_src || !dst_req || !dst_pos || src_rows < 1) return OSCAR_ERR_INVALID_ARG;
+  if (!src_index && src_rows < n) return OSCAR_ERR_INVALID_ARG;
+  if ((new_k == nullptr) != (new_v == nullptr)) return OSCAR_ERR_INVALID_ARG;
+  if (row_stride < int64_t(desc->n_kv_heads) * OSCAR_HEAD_DIM || row_stride % 8)
+    return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(new_k, 16) || !aligned(new_v, 16) ||
+      !aligned(src_index, 4) || !aligned(dst_req, 4) || !aligned(dst_pos, 4))
+    return OSCAR_ERR_ALIGNMENT;
+  oscar::DemoteParams p{};
+  p.pages = desc->pages;
+  p.page_table = desc->page_table;
+  p.dev_status = desc->dev_status;
+  p.k_src = k_src;
+  p.v_src = v_src;
+  p.src_rows = src_rows;
+  p.row_stride = row_stride;
+  p.src_index = src_index;
+  p.dst_req = dst_req;
+  p.dst_pos = dst_pos;
+  p.new_k = new_k;
+  p.new_v = new_v;
+  p.r_k = desc->r_k;
+  p.r_v = desc->r_v;
+  p.tau_k = desc->tau_k;
+  p.tau_v = desc->tau_v;
+  p.n = n;
+  p.batch = desc->batch;
+  p.n_kv = desc->n_kv_heads;
+  p.max_pages = desc->max_pages_per_seq;
+  p.n_pages = desc->n_pages;
+  const cudaError_t e = oscar::launch_demote(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
+                                               float* out, void* workspace,
+                                               size_t* workspace_bytes, void* stream) {
+  oscar_status st = check_desc(desc, true);
+  if (st != OSCAR_OK) return st;
+  const int group = desc->n_q_heads / desc->n_kv_heads;
+  if (group != 4 && group != 8) return OSCAR_ERR_UNSUPPORTED;
+  if (!workspace_bytes) return OSCAR_ERR_INVALID_ARG;
+  oscar::DecodePlan plan{};
+  cudaError_t err = cudaSuccess;
+  if (oscar::plan_decode(desc->batch, desc->n_kv_heads, group, desc->sink_cap, desc->recent_cap,
+                         desc->max_hist, &plan, &err) <= 0)
+    return OSCAR_ERR_CUDA;
+  if (!workspace) {
+    *workspace_bytes = plan.total_bytes;
+    return OSCAR_OK;
+  }
+  if (*workspace_bytes < plan.total_bytes) return OSCAR_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return OSCAR_ERR_ALIGNMENT;
+  if (!q || !out) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16)) return OSCAR_ERR_ALIGNMENT;
+  if (int64_t(desc->batch) * desc->n_kv_heads > 65535 * 65535LL || desc->batch > 65535 ||
+      desc->n_kv_heads > 65535)
+    return OSCAR_ERR_UNSUPPORTED;
+
+  oscar::DecodeParams p{};
+  p.pages = desc->pages;
+  p.page_table = desc->page_table;
+  p.hist_len = desc->hist_len;
+  p.sink_k = desc->sink_k;
+  p.sink_v = desc->sink_v;
+  p.sink_len = desc->sink_len;
+  p.recent_k = desc->recent_k;
+  p.recent_v = desc->recent_v;
+  p.recent_len = desc->recent_len;
+  p.recent_start = desc->recent_start;
+  p.r_k = desc->r_k;
+  p.r_v = desc->r_v;
+  p.dev_status = desc->dev_status;
+  p.q = q;
+  p.out = out;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = reinterpret_cast<uint32_t*>(ws + plan.off_counters);
+  p.qfrag = reinterpret_cast<uint32_t*>(ws + plan.off_qfrag);
+  p.qaux = reinterpret_cast<float*>(ws + plan.off_qaux);
+  p.partials = reinterpret_cast<float*>(ws + plan.off_partials);
+  p.batch = desc->batch;
+  p.n_kv = desc->n_kv_heads;
+  p.group = group;
+  p.sink_cap = desc->sink_cap;
+  p.recent_cap = desc->recent_cap;
+  p.max_pages = desc->max_pages_per_seq;
+  p.n_pages = desc->n_pages;
+  p.max_hist = desc->max_hist;
+  p.n_hist_splits = plan.n_hist_splits;
+  p.n_bf16_splits = plan.n_bf16_splits;
+  p.pages_per_split = plan.pages_per_split;
+  p.vpages_per_split = plan.vpages_per_split;
+  // PV operand scale: p <= 2^8 and s_V <= 2 tau_v / 3 (x2 margin for fp16
+  // rounding), so p s_V sigma_v stays below 2^14 in fp16
+  int e = 0;
+  std::frexp(double(desc->tau_v) * (2.0 / 3.0) * 2.0 * 256.0, &e);
+  const int sig_exp = 14 - e;
+  p.sigma_v = std::ldexp(1.0f, sig_exp);
+  p.pv_unscale = std::ldexp(1.0f, 24 - sig_exp);
+  err = oscar::launch_decode(p, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

@@ -1,0 +1,223 @@
+/*
+ * oscar.h - C ABI of the OSCAR two-bit rotated KV-cache decode path for GB300
+ * (sm_103a).
+ *
+ * Method (three web pages about one paper, cited by title and section):
+ *   [GIST]  gist.science, "OSCAR: Offline Spectral Covariance-Aware Rotation
+ *           for 2-bit KV Cache Quantization", Technical summary 2.1, 2.2 A
+ *           (offline calibration), 2.2 B (online serving).
+ *   [ZAKER] myzaker.com OSCAR article, parts "OSCAR 把旋转对准 attention"
+ *           (rotation) and "从离线校准到在线推理的 pipeline" (token pool,
+ *           demotion kernel, INT2 decode, online-softmax merge).
+ *
+ * Conventions shared by every call:
+ *   - Row vectors: a rotated key is k~ = k . R with R = U . H_Had . P_br.
+ *   - head_dim d = 128, 16 tokens per page, one quantisation group per
+ *     (token, KV head, K|V) vector of 128 channels, fp16 scale and zero.
+ *   - bfloat16 data is passed as uint16_t bit patterns.
+ *   - All device memory is allocated and freed by the caller.  The library
+ *     keeps no state besides cached device attributes; calls on different
+ *     streams may run concurrently when they touch disjoint memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
+ *     calls are asynchronous; every argument is validated on the host before
+ *     any launch, and a rejected call launches nothing.
+ *   - Device-side faults the host cannot see in advance (page ids outside the
+ *     pool, lengths above their capacity, an expired bounded wait) never trap:
+ *     the kernel skips the offending access and ORs a bit into the optional
+ *     device status word `dev_status` (see OSCAR_DEV_*).
+ *   - No C++ exception crosses this boundary.
+ *
+ * Page pool layout (this library's format; the pages fix only "paged KV",
+ * "4 codes per byte" and "scale/zero point"):
+ *   pool = n_pages x n_kv_heads blocks of 1152 bytes, block (page p, head h)
+ *   at byte (p * n_kv_heads + h) * 1152.  A block is a K half then a V half,
+ *   576 bytes each:  16 tokens x 32 code bytes, then 16 (scale, zero) fp16
+ *   pairs.  Token slot t of a half: codes at 32 t, (scale, zero) at 512 + 4 t.
+ *   Code byte j of a token holds channels 4j..4j+3, channel 4j+i in bits
+ *   2i..2i+1; channels are in rotated order.  Logical history position x of
+ *   request b lives in page page_table[b][x / 16], slot x % 16.
+ */
+#ifndef OSCAR_H_
+#define OSCAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSCAR_ABI_VERSION 1
+
+#define OSCAR_HEAD_DIM 128
+#define OSCAR_PAGE_TOKENS 16
+#define OSCAR_BLOCK_BYTES 1152
+#define OSCAR_HALF_BYTES 576
+
+typedef int32_t oscar_status;
+enum {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID_ARG = 1,     /* null pointer, bad dimension or length     */
+  OSCAR_ERR_ALIGNMENT = 2,       /* a pointer misses its required alignment  */
+  OSCAR_ERR_WORKSPACE = 3,       /* workspace missing or too small            */
+  OSCAR_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed      */
+  OSCAR_ERR_NO_CONVERGENCE = 5,  /* the host eigensolver did not converge     */
+  OSCAR_ERR_UNSUPPORTED = 6      /* a valid but unimplemented configuration   */
+};
+
+/* Bits a kernel ORs into *dev_status (never cleared by the library). */
+#define OSCAR_DEV_PAGE_BOUNDS 0x1   /* a page id outside [0, n_pages): skipped  */
+#define OSCAR_DEV_LENGTH 0x2        /* a length above its capacity: clamped     */
+#define OSCAR_DEV_TIMEOUT 0x4       /* a bounded wait expired: work abandoned   */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* oscar_status_string(oscar_status s);
+
+/* OSCAR_ABI_VERSION of the loaded library. */
+int32_t oscar_abi_version(void);
+
+/*
+ * One attention layer's cache: a three-segment token pool, BF16 sink (64
+ * tokens) | INT2 history (paged) | BF16 recent window (256-slot ring).
+ * [ZAKER] pipeline part; [GIST] 2.2 B (hybrid-precision paged layout).
+ * Pointers are device pointers unless marked host.  The struct itself is
+ * read on the host during the call only; it may be reused or freed after.
+ */
+typedef struct oscar_layer_desc {
+  int32_t batch;              /* B >= 1                                        */
+  int32_t n_q_heads;          /* H_q, a multiple of n_kv_heads                */
+  int32_t n_kv_heads;         /* H_kv >= 1; GQA group g = H_q / H_kv in {4, 8} */
+  int32_t head_dim;           /* must be 128                                   */
+  int32_t sink_cap;           /* sink capacity in tokens (64 on the pages)     */
+  int32_t recent_cap;         /* recent ring capacity (256 on the pages)       */
+  int32_t max_pages_per_seq;  /* row length of page_table                      */
+  int32_t max_hist;           /* host upper bound on every hist_len[b]         */
+  int64_t n_pages;            /* physical pages in the pool                    */
+  float tau_k;                /* clip threshold of this layer's keys, > 0      */
+  float tau_v;                /* clip threshold of this layer's values, > 0    */
+  uint8_t* pages;             /* pool, 128-byte aligned (layout above)         */
+  const int32_t* page_table;  /* [B][max_pages_per_seq] physical page ids      */
+  const int32_t* hist_len;    /* [B] INT2 history length of each request       */
+  const uint16_t* sink_k;     /* [B][sink_cap][H_kv][d] bf16, 16-byte aligned  */
+  const uint16_t* sink_v;     /* same layout                                   */
+  const int32_t* sink_len;    /* [B] valid sink tokens (slots 0..len-1)        */
+  uint16_t* recent_k;         /* [B][recent_cap][H_kv][d] bf16 ring            */
+  uint16_t* recent_v;         /* same layout                                   */
+  const int32_t* recent_len;  /* [B] valid recent tokens                       */
+  const int32_t* recent_start;/* [B] ring slot of the oldest recent token      */
+  const float* r_k;           /* [H_kv][d][d] row-major R_K, k~ = k . R_K      */
+  const float* r_v;           /* [H_kv][d][d] row-major R_V                    */
+  int32_t* dev_status;        /* optional device word for OSCAR_DEV_* bits     */
+} oscar_layer_desc;
+
+/*
+ * oscar_build_rotation - the fixed rotation of one (layer, KV head) from
+ * calibration rows.  [GIST] 2.1 and 2.2 A; [ZAKER] "OSCAR 把旋转对准 attention".
+ *
+ *   C = x^T x / n over the n rows of x (host, row-major [n][d], float64):
+ *   post-RoPE queries of the KV head's query group for R_K (C_Q), or rows of
+ *   S.V (see oscar_score_weighted_rows) for R_V (C_S).  U = eigenvectors of C
+ *   by descending eigenvalue, each column's largest-|entry| made positive
+ *   (ties: lowest index).  r_out = U . H . P_br with the orthonormal Sylvester
+ *   Hadamard H and the bit-reversal permutation P_br.
+ *
+ *   d must be a power of two in [2, 1024]; n >= 1.  r_out (host, [d][d]
+ *   row-major) is written; eigvals_out (host, [d], nullable) receives the
+ *   eigenvalues in the same order.  Host-only, synchronous, thread-safe.
+ *   Returns OSCAR_ERR_NO_CONVERGENCE if the eigensolver does not converge.
+ */
+oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t d,
+                                  double* r_out, double* eigvals_out);
+
+/*
+ * oscar_score_weighted_rows - rows of S.V for the value covariance
+ * C_S = (1/N) V^T S^T S V.  [GIST] 2.1 and 2.2 A.
+ *
+ *   S = row-softmax(q k^T * scale) with q [n_q][d], k and v [n_k][d] (host,
+ *   row-major, float64); out [n_q][d] = S . v.  scale is normally 1/sqrt(d).
+ *   Host-only, synchronous.
+ */
+oscar_status oscar_score_weighted_rows(const double* q, int64_t n_q, const double* k,
+                                       const double* v, int64_t n_k, int32_t d,
+                                       double scale, double* out);
+
+/*
+ * oscar_clip_threshold - per-layer clip threshold from rotated calibration
+ * activations.  [GIST] 2.2 A (thresholds estimated from the rotated
+ * calibration activations); the estimator is this library's choice:
+ *
+ *   tau = nearest-rank `quantile` of |acts[h] . r[h]| over every element of
+ *   every head h < n_heads (acts [n_heads][rows][d], r [n_heads][d][d], host,
+ *   float64).  0 < quantile <= 1.  Writes *tau_out.  Host-only.
+ */
+oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_heads,
+                                  int32_t d, const double* r, double quantile,
+                                  double* tau_out);
+
+/*
+ * oscar_quantize_append - the fused demotion kernel: rotate, clip, quantise
+ * and pack tokens into INT2 history pages.  [ZAKER] pipeline part (the
+ * oldest recent token is rotated, clipped, quantised and packed into INT2
+ * history; 4 codes per byte; scale/zero point); [GIST] 2.2 B.
+ *
+ *   For item i < n and every KV head h: x = src row src_index[i] (identity if
+ *   src_index is NULL) of k_src / v_src, viewed as [src_rows][row_stride]
+ *   bf16 with head h at elements h*d .. h*d+d-1.  A source row outside
+ *   [0, src_rows), a request outside the batch or a position beyond the page
+ *   table skips the item and sets OSCAR_DEV_LENGTH; a page id outside the
+ *   pool skips it and sets OSCAR_DEV_PAGE_BOUNDS.  x~ = x . R[h] (fp32 accumulate),
+ *   clamped to [-tau, tau]; scale = fp16((max - min) / 3), zero = fp16(min);
+ *   code = clamp(rint((x~ - zero) / scale), 0, 3) (0 if scale is 0).  The
+ *   codes and (scale, zero) go to history position dst_pos[i] of request
+ *   dst_req[i] through desc->page_table.  K and V are both written.
+ *
+ *   new_k / new_v (nullable, both or neither): [n][H_kv][d] bf16 rows that
+ *   replace the demoted source rows after they have been read - the decode
+ *   step's "write the new token into the freed ring slot".  k_src / v_src
+ *   are written only then.
+ *
+ *   src_index, dst_req, dst_pos: device int32 [n].  k_src, v_src, new_k,
+ *   new_v: 16-byte aligned; row_stride a multiple of 8 and >= H_kv * d.
+ *   The caller owns lengths and page allocation: writing into a page that
+ *   another request also references is a caller error.  Items must name
+ *   distinct (request, position) pairs.  n = 0 is a no-op.  Async.
+ */
+oscar_status oscar_quantize_append(const oscar_layer_desc* desc,
+                                   uint16_t* k_src, uint16_t* v_src,
+                                   int64_t src_rows, int64_t row_stride,
+                                   const int32_t* src_index,
+                                   const int32_t* dst_req, const int32_t* dst_pos,
+                                   int32_t n, const uint16_t* new_k,
+                                   const uint16_t* new_v, void* stream);
+
+/*
+ * oscar_decode_attention - one decode step of attention for every request of
+ * the batch over BF16 sink | INT2 history | BF16 recent.  [ZAKER] pipeline
+ * part (INT2 kernel: unpack, scale/zero dequantisation, float accumulation;
+ * BF16 kernel for sink/recent; online-softmax merge); [GIST] 2.2 B (inverse
+ * rotation fused into the kernel with no extra memory traffic); [CSDN] the
+ * aicoding.csdn.net explainer, section 三.1 (load INT2, rotate back, attend).
+ *
+ *   q: [B][H_q][d] bf16 (16-byte aligned); out: [B][H_q][d] float32
+ *   (16-byte aligned), normalised softmax(q K^T / sqrt(d)) V over the valid
+ *   tokens of all three segments; query head j reads KV head j / g.
+ *   History keys/values are c * s + z rotated back with R^T; the kernel
+ *   computes this as (q . R_K) against c * s + z and one output rotation
+ *   . R_V^T per head, which is the same quantity.  A request with no valid
+ *   token gets zeros.
+ *
+ *   Workspace: call with workspace == NULL to receive the required size in
+ *   *workspace_bytes (depends on desc dims and the current device) and
+ *   return.  Otherwise workspace must be 256-byte aligned device memory of
+ *   at least that size, used by one call at a time (no initialisation
+ *   needed).  Async.
+ */
+oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
+                                    float* out, void* workspace, size_t* workspace_bytes,
+                                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H_ */

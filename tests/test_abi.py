@@ -1,0 +1,147 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared symbol,
+rejects bad arguments before any launch, and its host-side rotation routines
+agree with the oracle (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from conftest import ROOT
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "oscar.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\w[\w\s\*]*?\b(oscar_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    lib = ctypes.CDLL(built_lib)
+    names = _declared()
+    assert "oscar_decode_attention" in names and "oscar_quantize_append" in names
+    assert "oscar_build_rotation" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    assert B.oscar_abi_version() == 1
+    assert B.oscar_status_string(0) == "ok"
+    assert B.oscar_status_string(3).startswith("workspace")
+
+
+def _desc(**over):
+    from bit_rotated_kv_split_gb300.binding import LayerDesc
+    d = LayerDesc()
+    d.batch, d.n_q_heads, d.n_kv_heads, d.head_dim = 1, 4, 1, 128
+    d.sink_cap, d.recent_cap, d.max_pages_per_seq, d.max_hist = 64, 256, 8, 100
+    d.n_pages, d.tau_k, d.tau_v = 8, 10.0, 10.0
+    fake = 1 << 20   # 128-byte aligned fake addresses: never dereferenced on rejection
+    for name in ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
+                 "recent_v", "recent_len", "recent_start", "r_k", "r_v"):
+        setattr(d, name, fake)
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(head_dim=64), 1), (dict(batch=0), 1), (dict(n_q_heads=6, n_kv_heads=4), 1),
+    (dict(sink_cap=10), 1), (dict(tau_k=0.0), 1), (dict(tau_v=float("inf")), 1),
+    (dict(tau_k=float("nan")), 1), (dict(tau_v=70000.0), 1), (dict(max_hist=8 * 16 + 1), 1),
+    (dict(pages=0), 1), (dict(page_table=0), 1), (dict(hist_len=0), 1),
+    (dict(pages=(1 << 20) + 64), 2), (dict(r_k=(1 << 20) + 4), 2), (dict(sink_k=(1 << 20) + 2), 2),
+])
+def test_decode_rejects_bad_descriptors_before_launch(built_lib, over, status):
+    from bit_rotated_kv_split_gb300 import binding as B
+    size = ctypes.c_size_t(0)
+    got = B.lib.oscar_decode_attention(ctypes.byref(_desc(**over)), None, None, None,
+                                       ctypes.byref(size), None)
+    assert got == status
+
+
+def test_decode_unsupported_group(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    size = ctypes.c_size_t(0)
+    got = B.lib.oscar_decode_attention(ctypes.byref(_desc(n_q_heads=2)), None, None, None,
+                                       ctypes.byref(size), None)
+    assert got == 6
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), 1), (dict(k_src=0), 1), (dict(row_stride=100), 1), (dict(row_stride=64), 1),
+    (dict(src_rows=0), 1), (dict(src_rows=3), 1),
+    (dict(new_k=1 << 20), 1), (dict(k_src=(1 << 20) + 8), 2), (dict(dst_pos=(1 << 20) + 2), 2),
+])
+def test_quantize_append_rejects_bad_arguments(built_lib, kw, status):
+    from bit_rotated_kv_split_gb300 import binding as B
+    args = dict(k_src=1 << 20, v_src=1 << 20, src_rows=16, row_stride=128, src_index=None,
+                dst_req=1 << 20, dst_pos=1 << 20, n=4, new_k=None, new_v=None)
+    args.update(kw)
+    got = B.lib.oscar_quantize_append(ctypes.byref(_desc()), args["k_src"], args["v_src"],
+                                      args["src_rows"], args["row_stride"], args["src_index"],
+                                      args["dst_req"],
+                                      args["dst_pos"], args["n"], args["new_k"], args["new_v"], None)
+    assert got == status
+
+
+def test_quantize_append_zero_items_is_noop(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    assert B.lib.oscar_quantize_append(ctypes.byref(_desc()), None, None, 0, 0, None, None, None, 0,
+                                       None, None, None) == 0
+
+
+# ---------------------------------------------------------------- host rotation routines
+
+def test_build_rotation_matches_oracle(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    outl = synth.outlier_channels(31, 0, 1)
+    cal = synth.calibration_set(31, 0, 0, outl[0], n_q=2048, n_k=256)
+    r_lib, w_lib = B.oscar_build_rotation(cal["q"])
+    c = O.query_covariance(cal["q"])
+    u, w = O.eigenbasis(c)
+    assert np.min(np.abs(np.diff(w))) > 1e-7 * w[0]      # separated: U unique to ~1e-10
+    np.testing.assert_allclose(w_lib, w, rtol=1e-10, atol=1e-12 * w[0])
+    np.testing.assert_allclose(r_lib, O.compose_rotation(u), atol=1e-9)
+    np.testing.assert_allclose(r_lib @ r_lib.T, np.eye(128), atol=1e-12)
+
+
+def test_build_rotation_value_covariance_matches_oracle(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    # outlier-scaled calibration data makes S nearly one-hot and C_S rank
+    # deficient (eigenvectors not unique); plain N(0,1) data over 256 keys
+    # gives a full-rank C_S with separated eigenvalues, so U is unique
+    outl = synth.outlier_channels(32, 0, 1)
+    cal = synth.calibration_set(32, 0, 0, outl[0], n_q=512, n_k=256)
+    sv_lib = B.oscar_score_weighted_rows(cal["q"], cal["k"], cal["v"])
+    np.testing.assert_allclose(sv_lib, O.score_weighted_values(cal["q"], cal["k"], cal["v"]),
+                               rtol=1e-11, atol=1e-11)
+    g = synth.generator(32, 1)
+    q, k, v = g.standard_normal((2048, 128)) * 2, g.standard_normal((256, 128)), g.standard_normal((256, 128))
+    c = O.value_covariance(q, k, v)
+    _, w = O.eigenbasis(c)
+    assert np.min(np.abs(np.diff(w))) > 1e-7 * w[0]
+    r_lib, _ = B.oscar_build_rotation(B.oscar_score_weighted_rows(q, k, v))
+    np.testing.assert_allclose(r_lib, O.rotation_from_covariance(c), atol=1e-8)
+
+
+def test_build_rotation_rejects_bad_dims(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    x = np.ones((4, 12))
+    with pytest.raises(B.OscarError):
+        B.oscar_build_rotation(x)
+
+
+def test_clip_threshold_matches_oracle(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    g = synth.generator(33, 0)
+    acts = g.standard_normal((3, 200, 16)) * 4
+    r = np.stack([np.linalg.qr(g.standard_normal((16, 16)))[0] for _ in range(3)])
+    tau = B.oscar_clip_threshold(acts, r, 0.999)
+    ref = O.clip_threshold(np.stack([acts[h] @ r[h] for h in range(3)]), 0.999)
+    assert tau == pytest.approx(ref, rel=1e-14)

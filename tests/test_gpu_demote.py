@@ -1,0 +1,148 @@
+"""GPU parity of oscar_quantize_append (rotate, clip, quantise, pack, place).
+
+Codes, scales and zero points produced on the GPU are read back from the
+page pool with the oracle's reader and compared with the oracle's demotion of
+the same bf16 tokens under the same fp32 rotation, with the comparison rule in
+`harness.code_parity`.
+"""
+import numpy as np
+import pytest
+
+import harness as H
+import oracle as O
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(built_lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _pre_rounding(x_rot_clipped):
+    mn = x_rot_clipped.min(-1)
+    mx = x_rot_clipped.max(-1)
+    return (mx - mn) / 3.0, mn
+
+
+def _run(seed, n_tok, n_kv, positions=None, with_new=False):
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    from bit_rotated_kv_split_gb300.cache import LayerCache
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    xk = synth.activations(seed, (1, 0), n_tok, outl)
+    xv = synth.activations(seed, (1, 1), n_tok, outl)
+    g = synth.generator(seed, 5)
+    src_index = g.permutation(n_tok).astype(np.int32)
+    if positions is None:
+        positions = np.arange(n_tok)
+    hist = int(positions.max()) + 1
+    table, n_pages = synth.page_table(seed, [hist], n_extra_pages=0)
+    cache = LayerCache(1, n_kv * 4, n_kv, table.shape[1], n_pages, torch.from_numpy(rk32),
+                       torch.from_numpy(rv32), tau_k, tau_v)
+    cache.page_table.copy_(torch.from_numpy(table))
+    dev = torch.device("cuda")
+    k_src = torch.from_numpy(xk).to(torch.bfloat16).to(dev).contiguous()
+    v_src = torch.from_numpy(xv).to(torch.bfloat16).to(dev).contiguous()
+    si = torch.from_numpy(src_index).to(dev)
+    dr = torch.zeros(n_tok, dtype=torch.int32, device=dev)
+    dp = torch.from_numpy(positions.astype(np.int32)).to(dev)
+    new_k = new_v = None
+    if with_new:
+        nk = synth.activations(seed, (1, 2), n_tok, outl)
+        nv = synth.activations(seed, (1, 3), n_tok, outl)
+        new_k = torch.from_numpy(nk).to(torch.bfloat16).to(dev)
+        new_v = torch.from_numpy(nv).to(torch.bfloat16).to(dev)
+    B.oscar_quantize_append(cache.desc(hist), k_src.view(torch.uint16), v_src.view(torch.uint16),
+                            n_tok, n_kv * 128, si, dr, dp, n_tok,
+                            None if new_k is None else new_k.view(torch.uint16),
+                            None if new_v is None else new_v.view(torch.uint16))
+    torch.cuda.synchronize()
+    assert int(cache.dev_status.item()) == 0
+    pool = cache.pages.cpu().numpy()
+    res = {}
+    for which, x, r32, tau in ((0, xk, rk32, tau_k), (1, xv, rv32, tau_v)):
+        gc, gs, gz = O.load_history_bulk(pool, table, n_kv, 0, hist, which)
+        xs = x[src_index]                                  # token written to position i
+        gc, gs, gz = gc[positions], gs[positions], gz[positions]
+        xr = np.stack([np.clip(xs[:, h].astype(np.float64) @ r32[h].astype(np.float64), -tau, tau)
+                       for h in range(n_kv)], axis=1)
+        rc, rs, rz = H.demote_heads(xs, r32, tau)
+        pre_s, pre_z = _pre_rounding(xr)
+        res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z)
+    if with_new:
+        np.testing.assert_array_equal(k_src.float().cpu().numpy()[src_index], nk)
+        np.testing.assert_array_equal(v_src.float().cpu().numpy()[src_index], nv)
+    return res
+
+
+def test_demote_tiny_config_tokens():
+    res = _run(2001, 1728, 1)
+    print(res)
+
+
+def test_demote_eight_heads_scattered_positions():
+    g = synth.generator(3, 1)
+    pos = g.permutation(700)[:333]
+    res = _run(2002, 333, 8, positions=pos)
+    print(res)
+
+
+def test_demote_writes_new_token_into_freed_rows():
+    _run(2003, 64, 2, with_new=True)
+
+
+def test_append_then_decode_matches_oracle_steps():
+    """Decode steps: demote the oldest recent token into history, write the new
+    token into its ring slot, attend; the oracle replays the same steps with
+    its own demotion."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    sc = H.Scenario(2004, [1000, 700], n_kv=2, g=4)
+    cache, q = H.to_device(sc)
+    dev = q.device
+    steps = 5
+    outl = sc.outl
+    hist = [dict((k, v.copy()) for k, v in h.items()) for h in sc.hist]
+    recents = [list(zip(*sc.segments(b)[2:])) for b in range(sc.B)]
+    start = sc.recent_start.copy()
+    hist_len = sc.hist_len.copy()
+    for step in range(steps):
+        newk = synth.activations(sc.seed, (7, step, 0), sc.B, outl)
+        newv = synth.activations(sc.seed, (7, step, 1), sc.B, outl)
+        src = torch.tensor([b * 256 + int(start[b]) for b in range(sc.B)], dtype=torch.int32, device=dev)
+        dr = torch.arange(sc.B, dtype=torch.int32, device=dev)
+        dp = torch.from_numpy(hist_len.astype(np.int32)).to(dev)
+        B.oscar_quantize_append(cache.desc(int(hist_len.max()) + 1), cache.recent_k.view(torch.uint16),
+                                cache.recent_v.view(torch.uint16), sc.B * 256, sc.n_kv * 128, src,
+                                dr, dp, sc.B,
+                                torch.from_numpy(newk).to(torch.bfloat16).to(dev).view(torch.uint16),
+                                torch.from_numpy(newv).to(torch.bfloat16).to(dev).view(torch.uint16))
+        for b in range(sc.B):
+            ok, ov = recents[b].pop(0)
+            ck, sk, zk = H.demote_heads(ok[None], sc.rk32, sc.tau_k)
+            cv, sv, zv = H.demote_heads(ov[None], sc.rv32, sc.tau_v)
+            for name, arr in (("codes_k", ck), ("scale_k", sk), ("zero_k", zk), ("codes_v", cv),
+                              ("scale_v", sv), ("zero_v", zv)):
+                hist[b][name] = np.concatenate([hist[b][name], arr])
+            recents[b].append((newk[b], newv[b]))
+        hist_len += 1
+        start = (start + 1) % 256
+        cache.hist_len.copy_(torch.from_numpy(hist_len))
+        cache.recent_start.copy_(torch.from_numpy(start.astype(np.int32)))
+        cache.max_hist = int(hist_len.max())
+        out, status = H.run_decode(cache, q)
+        assert status == 0
+        ref = np.zeros_like(out)
+        for b in range(sc.B):
+            sk_, sv_, _, _ = sc.segments(b)
+            rk = np.stack([x[0] for x in recents[b]])
+            rv = np.stack([x[1] for x in recents[b]])
+            ref[b] = O.decode_attention(sc.q[b].astype(np.float64), sk_, sv_, hist[b], rk, rv,
+                                        sc.rk32.astype(np.float64), sc.rv32.astype(np.float64))
+        err = H.relative_error(out, ref)
+        assert err.max() <= 2e-3, (step, err.max())
