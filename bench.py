@@ -1,0 +1,534 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the OSCAR two-bit KV path on GB300.
+
+Workload (Qwen3-8B-shaped single layer): batch 1, 32 query heads, 8 KV heads
+(GQA 4), head_dim 128, context 100,000 tokens = 64 BF16 sink + 99,680 INT2
+history (16-token pages, fp16 scale/zero per 128-channel group) + 256 BF16
+recent.  Synthetic seeded data: N(0,1) with 4 outlier channels x20 per KV
+head; rotations and clip thresholds built by the library from 4096 seeded
+calibration queries and 2048 calibration keys/values per KV head.
+
+One step = the whole hot path once: oscar_quantize_append (the oldest recent
+token of every KV head is rotated, clipped, quantised, packed into history,
+and the new token written into the freed ring slot) + oscar_decode_attention
+(q pre-rotation, INT2 split-KV scan, BF16 sink/recent scan, merge and output
+rotation).  The step is replayed from a steady state (lengths do not advance,
+so every step does identical work).  Steps cycle over several independent
+copies of the layer cache whose total size exceeds 3x the L2 cache, so no
+step reads its inputs from L2 (inputs larger than L2; no flush needed).
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+
+`--impl reference` times the float64 CPU oracle on this host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import copy
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(workload="qwen3-8b-layer-decode-100k", batch=1, n_q_heads=32, n_kv_heads=8,
+                head_dim=128, ctx=100_000, sink=64, recent=256, page_tokens=16, group=128, seed=1002)
+METRIC = "decode-attn tokens/s at 100k ctx (1 layer, Qwen3-8B shape)"
+UNIT = "tokens/s"
+CACHE_TENSORS = ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
+                 "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
+    ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--reps", type=int, default=20, help=argparse.SUPPRESS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _split(ctx):
+    s = min(ctx, WORKLOAD["sink"])
+    r = min(ctx - s, WORKLOAD["recent"])
+    return s, ctx - s - r, r
+
+
+def bytes_per_decode():
+    """Algorithmic HBM bytes of one decode launch on the workload (per step)."""
+    w = WORKLOAD
+    _, hist, _ = _split(w["ctx"])
+    per_hist_token = w["n_kv_heads"] * 2 * (w["head_dim"] // 4 + 4)          # codes + s/z, K and V
+    bf16 = (w["sink"] + w["recent"]) * w["n_kv_heads"] * 2 * w["head_dim"] * 2
+    table = -(-hist // w["page_tokens"]) * 4
+    io = w["n_q_heads"] * w["head_dim"] * (2 + 4)
+    return hist * per_hist_token + bf16 + table + io
+
+
+def _config_json(extra=None):
+    w = WORKLOAD
+    s, h, r = _split(w["ctx"])
+    cfg = {"workload": w["workload"], "batch": w["batch"], "n_q_heads": w["n_q_heads"],
+           "n_kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"], "ctx": w["ctx"],
+           "sink_bf16": s, "history_int2": h, "recent_bf16": r, "page_tokens": w["page_tokens"],
+           "quant_group": w["group"], "parallelism": "replicas"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------- oracle leg
+
+def _oracle_sample_setup():
+    """Inputs of one KV head (4 query heads) of the workload for the oracle."""
+    import numpy as np
+    import oracle as O
+    import synth
+    w = WORKLOAD
+    seed = w["seed"]
+    outl = synth.outlier_channels(seed, 0, 1)
+    cal = synth.calibration_set(seed, 0, 0, outl[0], n_q=4096, n_k=2048)
+    rk = O.rotation_from_covariance(O.query_covariance(cal["q"]))
+    rv = O.rotation_from_covariance(O.value_covariance(cal["q"], cal["k"], cal["v"]))
+    tau_k = O.clip_threshold(cal["k"] @ rk)
+    tau_v = O.clip_threshold(cal["v"] @ rv)
+    s, h, r = _split(w["ctx"])
+    k = synth.activations(seed, (0, 0, 0), w["ctx"] + 1, outl).astype(np.float64)
+    v = synth.activations(seed, (0, 0, 1), w["ctx"] + 1, outl).astype(np.float64)
+    g = w["n_q_heads"] // w["n_kv_heads"]
+    q = synth.activations(seed, (0, 0, 2), 1, np.repeat(outl, g, axis=0))[0].astype(np.float64)
+    hist = {}
+    for name, x, rot, tau in (("k", k, rk, tau_k), ("v", v, rv, tau_v)):
+        c, sc, ze = O.demote(x[s:s + h - 1, 0], rot, tau)
+        hist["codes_" + name], hist["scale_" + name], hist["zero_" + name] = c[:, None], sc[:, None], ze[:, None]
+    return dict(O=O, np=np, q=q, k=k, v=v, rk=rk, rv=rv, tau_k=tau_k, tau_v=tau_v, hist=hist, s=s, h=h, r=r)
+
+
+def _oracle_step(st, n_hist=None):
+    """One decode step of one KV head, by the oracle: demote the oldest recent
+    token into history, then attend over sink | history | recent.  `n_hist`
+    limits the history to its first n_hist - 1 stored tokens plus the demoted
+    one (a bounded sample; cost is linear in the history length)."""
+    O, np = st["O"], st["np"]
+    s, h = st["s"], st["h"]
+    keep = (h - 1) if n_hist is None else max(0, min(h - 1, n_hist - 1))
+    ck, sk, zk = O.demote(st["k"][s + h - 1, 0][None], st["rk"], st["tau_k"])
+    cv, sv, zv = O.demote(st["v"][s + h - 1, 0][None], st["rv"], st["tau_v"])
+    old = st["hist"]
+    hist = {"codes_k": np.concatenate([old["codes_k"][:keep], ck[:, None]]),
+            "scale_k": np.concatenate([old["scale_k"][:keep], sk[:, None]]),
+            "zero_k": np.concatenate([old["zero_k"][:keep], zk[:, None]]),
+            "codes_v": np.concatenate([old["codes_v"][:keep], cv[:, None]]),
+            "scale_v": np.concatenate([old["scale_v"][:keep], sv[:, None]]),
+            "zero_v": np.concatenate([old["zero_v"][:keep], zv[:, None]])}
+    k, v = st["k"], st["v"]
+    return O.decode_attention(st["q"], k[:s], v[:s], hist, k[s + h:s + h + st["r"]],
+                              v[s + h:s + h + st["r"]], st["rk"][None], st["rv"][None])
+
+
+SAMPLE_DESC = ("one of the 8 KV heads (its 4 query heads) of a full decode step at 100k context "
+               "(demotion of 1 token + attention over 64 + 99,680 INT2 + 256 tokens); "
+               "step time extrapolated x8 to all KV heads")
+
+
+def cpu_baseline_worker(reps):
+    st = _oracle_sample_setup()
+    _oracle_step(st)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _oracle_step(st)
+    dt = (time.perf_counter() - t0) / reps
+    print(json.dumps({"sample_seconds": dt, "reps": reps}))
+
+
+def _single_thread_env():
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    return env
+
+
+def cpu_baseline(reps=20):
+    """The oracle timed on one host core in a fresh process (started before any GPU work)."""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
+                        "--reps", str(reps)], capture_output=True, text=True, env=_single_thread_env(),
+                       timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr[-400:]}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    step = res["sample_seconds"] * WORKLOAD["n_kv_heads"]
+    return {"value": WORKLOAD["batch"] / step, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": SAMPLE_DESC + "; %d timed repetitions" % res["reps"]}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    st = _oracle_sample_setup()
+    h = st["h"]
+    # size the per-step sample so that warm-up + timed steps take about 150 s
+    t1 = time.perf_counter()
+    _oracle_step(st)
+    full = time.perf_counter() - t1
+    n_hist = h
+    budget = 150.0 / max(args.steps + args.warmup, 1)
+    if full > budget:
+        n_hist = max(h // 64, int(h * budget / full))
+    frac = n_hist / h
+    for _ in range(args.warmup):
+        _oracle_step(st, n_hist)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(st, n_hist)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    step = dt * WORKLOAD["n_kv_heads"] / frac
+    value = WORKLOAD["batch"] / step
+    sample = SAMPLE_DESC if n_hist == h else (
+        SAMPLE_DESC + "; history cut to the first %d of %d tokens per step and scaled by %.2f"
+        % (n_hist, h, 1 / frac))
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config_json(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------- GPU leg
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons around the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _roofline_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def rotations_from_library(B):
+    """Per-head R_K, R_V and per-layer taus, built by the library's host routines."""
+    import numpy as np
+    import synth
+    w = WORKLOAD
+    seed, n_kv = w["seed"], w["n_kv_heads"]
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    rk, rv, ck, cv = [], [], [], []
+    for hh in range(n_kv):
+        cal = synth.calibration_set(seed, 0, hh, outl[hh], n_q=4096, n_k=2048)
+        rk.append(B.oscar_build_rotation(cal["q"])[0])
+        rv.append(B.oscar_build_rotation(B.oscar_score_weighted_rows(cal["q"], cal["k"], cal["v"]))[0])
+        ck.append(cal["k"])
+        cv.append(cal["v"])
+    rk32 = np.stack(rk).astype(np.float32)
+    rv32 = np.stack(rv).astype(np.float32)
+    tau_k = B.oscar_clip_threshold(np.stack(ck), rk32.astype(np.float64))
+    tau_v = B.oscar_clip_threshold(np.stack(cv), rv32.astype(np.float64))
+    return rk32, rv32, tau_k, tau_v, outl
+
+
+def build_layer(torch, B, dev, rot):
+    """One layer cache of the workload on `dev`, history filled by the library's own demotion."""
+    import synth
+    from bit_rotated_kv_split_gb300.cache import LayerCache
+    w = WORKLOAD
+    seed, n_kv, bsz = w["seed"], w["n_kv_heads"], w["batch"]
+    s, h, r = _split(w["ctx"])
+    rk, rv, tau_k, tau_v, outl = rot
+    table, n_pages = synth.page_table(seed, [h] * bsz, n_extra_pages=1)
+    cache = LayerCache(bsz, w["n_q_heads"], n_kv, table.shape[1], n_pages, torch.from_numpy(rk),
+                       torch.from_numpy(rv), tau_k, tau_v, device=dev)
+    cache.page_table.copy_(torch.from_numpy(table))
+    cache.max_hist = h
+    chunk = 32768
+    for b in range(bsz):
+        for t0 in range(0, h, chunk):
+            n = min(chunk, h - t0)
+            xk = synth.activations_device(seed, (0, b, 0, t0), n, outl, dev)
+            xv = synth.activations_device(seed, (0, b, 1, t0), n, outl, dev)
+            pos = torch.arange(t0, t0 + n, dtype=torch.int32, device=dev)
+            req = torch.full((n,), b, dtype=torch.int32, device=dev)
+            B.oscar_quantize_append(cache.desc(h), xk.view(torch.uint16), xv.view(torch.uint16), n,
+                                    n_kv * 128, None, req, pos, n)
+    sk = synth.activations_device(seed, (1, 0), bsz * w["sink"], outl, dev)
+    sv = synth.activations_device(seed, (1, 1), bsz * w["sink"], outl, dev)
+    rk_ = synth.activations_device(seed, (1, 2), bsz * w["recent"], outl, dev)
+    rv_ = synth.activations_device(seed, (1, 3), bsz * w["recent"], outl, dev)
+    cache.sink_k.copy_(sk.view(cache.sink_k.shape))
+    cache.sink_v.copy_(sv.view(cache.sink_v.shape))
+    cache.recent_k.copy_(rk_.view(cache.recent_k.shape))
+    cache.recent_v.copy_(rv_.view(cache.recent_v.shape))
+    cache.hist_len.fill_(h)
+    cache.sink_len.fill_(s)
+    cache.recent_len.fill_(r)
+    cache.recent_start.fill_(1)     # ring slot 0 holds the newest token after each step
+    torch.cuda.synchronize()
+    assert int(cache.dev_status.item()) == 0
+    return cache
+
+
+def clone_layer(layer):
+    c = copy.copy(layer)
+    for name in CACHE_TENSORS:
+        setattr(c, name, getattr(layer, name).clone())
+    return c
+
+
+def run_gpu(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.reps)          # before any GPU work in this process
+    import torch
+    import torch.distributed as dist
+    from bit_rotated_kv_split_gb300 import binding as B
+    import synth
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOAD
+    bsz, n_kv = w["batch"], w["n_kv_heads"]
+    s, h, r = _split(w["ctx"])
+
+    rot = rotations_from_library(B)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    layer0 = build_layer(torch, B, dev, rot)
+    per_layer = layer0.pages.numel() + 4 * (layer0.sink_k.numel() + layer0.recent_k.numel())
+    n_copies = max(2, math.ceil(3 * l2 / per_layer))
+    layers = [layer0] + [clone_layer(layer0) for _ in range(n_copies - 1)]
+    torch.cuda.synchronize()
+
+    qo = synth.outlier_channels(w["seed"], 0, n_kv).repeat(w["n_q_heads"] // n_kv, axis=0)
+    q = synth.activations_device(w["seed"], (2, 0), bsz, qo, dev).view(bsz, w["n_q_heads"], 128)
+    new_k = synth.activations_device(w["seed"], (2, 1), bsz, rot[4], dev)
+    new_v = synth.activations_device(w["seed"], (2, 2), bsz, rot[4], dev)
+    out = torch.empty((bsz, w["n_q_heads"], 128), dtype=torch.float32, device=dev)
+    src = torch.tensor([b * w["recent"] for b in range(bsz)], dtype=torch.int32, device=dev)
+    dst_req = torch.arange(bsz, dtype=torch.int32, device=dev)
+    dst_pos = torch.full((bsz,), h - 1, dtype=torch.int32, device=dev)
+    descs = [L.desc(h) for L in layers]
+    ws_bytes = B.oscar_decode_workspace_bytes(descs[0])
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def demote(i):
+        L = layers[i]
+        B.oscar_quantize_append(descs[i], L.recent_k.view(torch.uint16), L.recent_v.view(torch.uint16),
+                                bsz * w["recent"], n_kv * 128, src, dst_req, dst_pos, bsz,
+                                new_k.view(torch.uint16), new_v.view(torch.uint16))
+
+    def decode(i):
+        B.oscar_decode_attention(descs[i], q, out, ws, ws_bytes)
+
+    # CUDA graphs of each copy's two calls (host launch overhead out of the step)
+    stream = torch.cuda.Stream()
+    graphs = []
+    use_graphs = True
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(n_copies):
+                demote(i)
+                decode(i)
+            torch.cuda.synchronize()
+            for i in range(n_copies):
+                gd, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gd, stream=stream):
+                    demote(i)
+                with torch.cuda.graph(ga, stream=stream):
+                    decode(i)
+                graphs.append((gd, ga))
+    except Exception as exc:  # graph capture unavailable: launch directly
+        use_graphs = False
+        graphs = []
+        sys.stderr.write("graph capture failed (%s); timing direct launches\n" % exc)
+    torch.cuda.synchronize()
+
+    def step(i):
+        if use_graphs:
+            graphs[i][0].replay()
+        else:
+            demote(i)
+
+    def attend(i):
+        if use_graphs:
+            graphs[i][1].replay()
+        else:
+            decode(i)
+
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = Clocks(local)
+    with torch.cuda.stream(stream):
+        for k in range(W):
+            step(k % n_copies)
+            attend(k % n_copies)
+        torch.cuda.synchronize()
+        clocks.start()
+        t_pre = time.perf_counter()
+        pre = 0
+        while time.perf_counter() - t_pre < 1.0:      # same load before the timed region, for clock samples
+            for _ in range(50):
+                step(pre % n_copies)
+                attend(pre % n_copies)
+                pre += 1
+            torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in range(K):
+            i = k % n_copies
+            ev[k][0].record(stream)
+            step(i)
+            ev[k][1].record(stream)
+            attend(i)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        for k in range(min(K, 200)):
+            step(k % n_copies)
+            attend(k % n_copies)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    decode_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    demote_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    t_step = total_ms / K / 1e3
+    if world > 1:
+        tt = torch.tensor([t_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+    status = max(int(L.dev_status.item()) for L in layers)
+
+    # end to end through the public API with pinned host buffers
+    q_host = q.cpu().pin_memory()
+    nk_host = new_k.cpu().pin_memory()
+    nv_host = new_v.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    ke = min(K, 500)
+    with torch.cuda.stream(stream):
+        for k in range(5):
+            demote(k % n_copies)
+            decode(k % n_copies)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(ke):
+            i = k % n_copies
+            q.copy_(q_host, non_blocking=True)
+            new_k.copy_(nk_host, non_blocking=True)
+            new_v.copy_(nv_host, non_blocking=True)
+            demote(i)
+            decode(i)
+            out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3 / ke
+
+    if rank == 0:
+        peak, peak_kind = _roofline_peak()
+        nbytes = bytes_per_decode()
+        achieved = nbytes / (decode_ms / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": world * bsz / t_step, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int2/bf16 in, f32 accumulate",
+            "data": "synthetic",
+            "config": _config_json({"l2_policy": "inputs larger than L2: %d rotating layer caches of %.1f MB "
+                                                 "(%.0f MB > 3x L2 %.0f MB)" % (n_copies, per_layer / 1e6,
+                                                                                n_copies * per_layer / 1e6, l2 / 1e6),
+                                    "cuda_graphs": use_graphs}),
+            "decode_ms": decode_ms, "demote_ms": demote_ms,
+            "hbm_gbs_decode": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "split_kernel (oscar_decode_attention, one launch per step)",
+                         "algorithmic_bytes": nbytes, "peak_kind": peak_kind + " hbm_gbs"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * bsz / e2e_s, "unit": UNIT,
+                    "h2d_bytes_per_step": q.numel() * 2 + new_k.numel() * 2 + new_v.numel() * 2,
+                    "d2h_bytes_per_step": out.numel() * 4},
+            "gpu_launches": 2 * K,
+            "clocks": clk,
+            "device_status": status,
+            "host_wall_s": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.cpu_baseline_worker:
+        cpu_baseline_worker(args.reps)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -6,21 +6,27 @@
 // gist.science "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV
 // Cache Quantization", Technical summary 2.2 B: the inverse rotation is fused
 // into the attention kernel with no extra memory traffic.  Here it is applied
-// as q~ = q . R_K once per query head (prep kernel) and one o . R_V^T per head
-// after the history partials are merged, instead of rotating every token.
+// as q~ = q . R_K once per query head and one o . R_V^T per head after the
+// history partials are merged, instead of rotating every token.
 //
-// Launch 1 (prep, one CTA per (request, KV head)): q~ = q . R_K in fp32, split
-//   into fp16 hi + lo with a power-of-two scale and laid out as the B fragments
-//   of the QK tensor-core MMA; zeroes the merge tickets.
-// Launch 2 (split kernel, programmatic dependent launch): CTA (split, kv, b).
-//   Splits < n_hist_splits scan a range of INT2 pages; the rest scan the BF16
-//   sink/recent tokens.  Each of the 4 warps streams its own pages through a
-//   6-stage shared-memory ring filled by 1-D TMA bulk copies (one 1152-byte
-//   page block per stage, mbarrier completion, bounded waits) and keeps its
-//   own online-softmax state; the CTA merges its warps and writes one partial
-//   (m, l, o) per query head.  The last CTA of a (request, KV head) to finish
-//   (atomic ticket, no waiting) merges all partials, applies . R_V^T to the
-//   history part and writes the normalised output.
+// One launch.  CTA (split, kv, b) of W warps (16 for GQA 4, 12 for GQA 8; one
+// CTA per SM) owns a contiguous range of INT2 pages of one (request, KV head)
+// and a share of its BF16 sink/recent tokens:
+//   1. lane 0 of each warp starts 1-D TMA bulk copies of the warp's first
+//      pages (one 1152-byte page block per stage, a ring of stages per warp,
+//      mbarrier completion, bounded waits);
+//   2. meanwhile R_K arrives in shared memory by one TMA bulk transfer and
+//      the CTA computes q~ = q . R_K for the GQA group (fp32), then builds
+//      each lane's tensor-core B fragments from it;
+//   3. every warp streams its INT2 pages through its ring, keeping its own
+//      online-softmax state; then the warps owning the fewest pages scan the
+//      CTA's BF16 tokens (direct vector loads);
+//   4. the CTA merges its warps into two partials (m, l, o) per query head
+//      (history, rotated domain; BF16, original domain);
+//   5. the last CTA of the (request, KV head) to finish (atomic ticket, no
+//      waiting) merges all partials - loads kept in flight, R_V prefetched -
+//      applies . R_V^T to the history part and writes the normalised output,
+//      then resets the ticket.
 //
 // INT2 arithmetic on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
 //   QK: A = codes of 16 tokens x 128 channels, B = q~ (hi | lo columns), so
@@ -36,26 +42,52 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+// Tunables (compile-time): warps per CTA for GQA 4 / GQA 8, ring stages per
+// warp, and the number of independent accumulator chains of the QK MMA.
+#ifndef OSCAR_WARPS_G4
+#define OSCAR_WARPS_G4 16
+#endif
+#ifndef OSCAR_WARPS_G8
+#define OSCAR_WARPS_G8 12
+#endif
+#ifndef OSCAR_STAGES
+#define OSCAR_STAGES 6
+#endif
+#ifndef OSCAR_QK_CHAINS
+#define OSCAR_QK_CHAINS 2
+#endif
+
 namespace oscar {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 6;
+constexpr int kStages = OSCAR_STAGES;
+constexpr int kQkChains = OSCAR_QK_CHAINS;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (p <= 2^8)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kMaxSplits = 128;               // bounds the last CTA's merge scratch
 
 template <int G>
 struct Geo {
   static constexpr int NT = (2 * G + 7) / 8;          // column tiles holding hi | lo parts
   static constexpr int HS = G >= 8 ? G / 4 : 2;       // head slots per lane
   static constexpr int NTQ = (G + 7) / 8;             // BF16 QK column tiles
-  static constexpr size_t kStageBytes = size_t(kWarps) * kStages * kBlockBytes;
-  static constexpr size_t kBarBytes = size_t(kWarps) * kStages * 8;
-  static constexpr size_t kStateBytes = size_t(kWarps) * G * kPartStride * 4;
-  static constexpr size_t kSmem = kStageBytes + kBarBytes + kStateBytes + 16;
+  static constexpr int W = G <= 4 ? OSCAR_WARPS_G4 : OSCAR_WARPS_G8;  // warps per CTA
+  static constexpr int T = W * 32;
+  static constexpr size_t kStageBytes = size_t(W) * kStages * kBlockBytes;
+  // ring barriers + the R_K barrier, padded so the region after it stays
+  // 128-byte aligned (TMA destinations need at least 16)
+  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 1) * 8 + 127) / 128 * 128;
+  static constexpr size_t kStateBytes = size_t(W) * G * kPartStride * 4;   // per partial type
+  // prologue: R_K (64 KB) and the q~ scratch; epilogue: two warp-state sets
+  static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
+  static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G) * 4;
+  static constexpr size_t kUnion0 = kRotBytes + kQScratch;
+  static constexpr size_t kUnion = (kUnion0 > 2 * kStateBytes ? kUnion0 : 2 * kStateBytes);
+  static constexpr size_t kSmem = kStageBytes + kBarBytes + kUnion + 16;
+  static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
 // head owned by head slot hs of a lane with column group tig
@@ -91,104 +123,7 @@ __device__ __forceinline__ void flag(int32_t* st, int bit) {
   if (st) atomicOr(st, bit);
 }
 
-// ------------------------------------------------------------------ prep kernel
-
-template <int G>
-__global__ void __launch_bounds__(kThreads) prep_kernel(DecodeParams p) {
-  pdl_launch_dependents();
-  constexpr int NT = Geo<G>::NT;
-  __shared__ float qs[G][kHeadDim];
-  __shared__ float qt[G][kHeadDim];
-  __shared__ float red_max[G][kWarps], red_sum[G][kWarps];
-  __shared__ float sigma[G];
-  const int hkv = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int pair = b * p.n_kv + hkv;
-  const int lane = tid & 31, warp = tid >> 5;
-
-  for (int h = 0; h < G; ++h) {
-    const uint16_t v = p.q[(int64_t(b) * p.n_kv * G + hkv * G + h) * kHeadDim + tid];
-    qs[h][tid] = __uint_as_float(uint32_t(v) << 16);
-  }
-  if (tid == 0) p.counters[pair] = 0u;
-  __syncthreads();
-
-  // q~[h][j] = sum_i q[h][i] R_K[i][j]  (thread j, i ascending)
-  const float* r = p.r_k + int64_t(hkv) * kHeadDim * kHeadDim + tid;
-  float acc[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.f;
-  for (int i = 0; i < kHeadDim; ++i) {
-    const float rij = __ldg(r + i * kHeadDim);
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][i], rij, acc[h]);
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    qt[h][tid] = acc[h];
-    float mx = fabsf(acc[h]), sm = acc[h];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      sm += __shfl_xor_sync(kFull, sm, o);
-    }
-    if (lane == 0) {
-      red_max[h][warp] = mx;
-      red_sum[h][warp] = sm;
-    }
-  }
-  __syncthreads();
-  if (tid < G) {
-    float mx = 0.f, sm = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      mx = fmaxf(mx, red_max[tid][w]);
-      sm += red_sum[tid][w];
-    }
-    // power-of-two scale putting max|q~| in [2^13, 2^14): keeps the fp16 hi
-    // part normal and the lo part precise
-    int e = 0;
-    if (mx > 0.f) {
-      frexpf(mx, &e);            // mx in [2^(e-1), 2^e)
-      e = 14 - e;
-      e = max(-100, min(100, e));
-    }
-    const float sg = ldexpf(1.f, e);
-    sigma[tid] = sg;
-    const float scale = kLog2e * rsqrtf(float(kHeadDim));
-    p.qaux[(pair * G + tid) * 2 + 0] = ldexpf(1.f, 24 - e) * scale;  // 2^24/sigma * log2e/sqrt(d)
-    p.qaux[(pair * G + tid) * 2 + 1] = sm * scale;
-  }
-  __syncthreads();
-
-  // B fragments: [nt][j][lane][r]; column n = 8nt + gid is head n (hi part)
-  // for n < G, head n-G (lo part) for n < 2G, zero otherwise.  r = 0 holds
-  // channels (32tig + j, 32tig + j + 8), r = 1 (32tig + 16 + j, 32tig + 24 + j),
-  // each scaled by sigma * 4^-pos(j).
-  for (int idx = tid; idx < NT * 8 * 32; idx += kThreads) {
-    const int ln = idx & 31, j = (idx >> 5) & 7, nt = idx >> 8;
-    const int gid = ln >> 2, tig = ln & 3;
-    const int col = 8 * nt + gid;
-    uint32_t out[2] = {0u, 0u};
-    if (col < 2 * G) {
-      const int h = col < G ? col : col - G;
-      const bool lo = col >= G;
-      const float f = sigma[h] * ldexpf(1.f, -2 * code_pos(j));
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int c0 = 32 * tig + 16 * rr + j;
-        float v0 = qt[h][c0] * f, v1 = qt[h][c0 + 8] * f;
-        if (lo) {
-          v0 = split_lo(v0);
-          v1 = split_lo(v1);
-        }
-        out[rr] = pack_half2(v0, v1);
-      }
-    }
-    reinterpret_cast<uint2*>(p.qfrag)[(int64_t(pair) * NT * 8 + nt * 8 + j) * 32 + ln] =
-        make_uint2(out[0], out[1]);
-  }
-}
-
-// ------------------------------------------------------------------ INT2 page
+// ------------------------------------------------------------------ warp state and pages
 
 template <int G>
 struct WarpState {
@@ -265,7 +200,7 @@ struct WarpState {
   }
 };
 
-template <int G>
+template <int G, bool kTail>
 __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ pg, int ntok, int gid,
                                           int tig, const uint32_t (&qb)[Geo<G>::NT][8][2],
                                           const float (&unscale)[Geo<G>::HS],
@@ -284,10 +219,13 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ pg, int nt
   const uint32_t vsz0 = *reinterpret_cast<const uint32_t*>(pv + 512 + 4 * gid);
   const uint32_t vsz1 = *reinterpret_cast<const uint32_t*>(pv + 512 + 4 * (gid + 8));
 
-  // ---- scores: D[token][col] = 2^-24 sigma (q~ . c)
-  float d[NT][4];
+  // ---- scores: D[token][col] = 2^-24 sigma (q~ . c), k-steps spread over
+  // kQkChains independent accumulators to shorten the MMA dependency chain
+  float dc[kQkChains][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+  for (int ch = 0; ch < kQkChains; ++ch)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) dc[ch][nt][0] = dc[ch][nt][1] = dc[ch][nt][2] = dc[ch][nt][3] = 0.f;
   {
     const uint32_t w00 = kw0.x, w01 = kw0.y, w10 = kw1.x, w11 = kw1.y;
     const uint32_t s00 = w00 >> 6, s01 = w01 >> 6, s10 = w10 >> 6, s11 = w11 >> 6;
@@ -296,9 +234,20 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ pg, int nt
       const uint32_t a0 = code_pair(w00, s00, j), a1 = code_pair(w10, s10, j);
       const uint32_t a2 = code_pair(w01, s01, j), a3 = code_pair(w11, s11, j);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16(dc[j % kQkChains][nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
     }
   }
+  float d[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v = dc[0][nt][c];
+#pragma unroll
+      for (int ch = 1; ch < kQkChains; ++ch) v += dc[ch][nt][c];
+      d[nt][c] = v;
+    }
   float full[HS][2];
   if (G <= 4) {
 #pragma unroll
@@ -311,7 +260,7 @@ __device__ __forceinline__ void int2_page(const uint8_t* __restrict__ pg, int nt
       for (int c = 0; c < 4; ++c) full[2 * nt + (c & 1)][c >> 1] = d[nt][c] + d[nt + NT / 2][c];
   }
   const float2 kz0 = half2_to_float2(ksz0), kz1 = half2_to_float2(ksz1);
-  const bool ok0 = gid < ntok, ok1 = gid + 8 < ntok;
+  const bool ok0 = !kTail || gid < ntok, ok1 = !kTail || gid + 8 < ntok;
   float sc[HS][2];
 #pragma unroll
   for (int hs = 0; hs < HS; ++hs) {
@@ -484,95 +433,219 @@ __device__ __forceinline__ void store_warp_state(WarpState<G>& st, float* ws, in
   }
 }
 
+// ------------------------------------------------------------------ q~ and its fragments
+
+// q~ = q . R_K for the G query heads of (b, hkv), in fp32 with a fixed
+// summation order; R_K (64 KB) is brought into shared memory `rks` by one
+// TMA bulk transfer.  Per head a power-of-two scale sigma puts max|q~ sigma|
+// in [2^13, 2^14) so the fp16 hi part is normal and the lo part precise.
+// Leaves qt[G][128] (unscaled) at scratch + 5 G 128 and aux[G][4] =
+// (sigma, unscale, qz, -) at scratch + 6 G 128.
+template <int G>
+__device__ void rotate_query(const DecodeParams& p, int b, int hkv, float* rks, uint64_t* rbar,
+                             float* scratch) {
+  constexpr int T = Geo<G>::T;
+  float* qs = scratch;                 // [G][128]
+  float* part = qs + G * kHeadDim;     // [4][G][128]
+  float* qt = part + 4 * G * kHeadDim; // [G][128]
+  float* aux = qt + G * kHeadDim;      // [G][4]
+  float* red = aux + 4 * G;            // [G][4] partial max | [G][4] partial sum
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(rbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(rbar, uint32_t(Geo<G>::kRotBytes));
+    const float* rk = p.r_k + int64_t(hkv) * kHeadDim * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      bulk_copy_g2s(rks + c * (kHeadDim * kHeadDim / 4), rk + c * (kHeadDim * kHeadDim / 4),
+                    uint32_t(Geo<G>::kRotBytes / 4), rbar);
+  }
+  const uint16_t* qg = p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim;
+  for (int i = tid; i < G * kHeadDim; i += T) qs[i] = __uint_as_float(uint32_t(qg[i]) << 16);
+  __syncthreads();
+  if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
+  for (int task = tid; task < 4 * kHeadDim; task += T) {
+    const int ig = task / kHeadDim, j = task % kHeadDim;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i)
+        acc = fmaf(qs[h * kHeadDim + 32 * ig + i], rks[(32 * ig + i) * kHeadDim + j], acc);
+      part[(ig * G + h) * kHeadDim + j] = acc;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kHeadDim; idx += T) {
+    const float v = ((part[idx] + part[G * kHeadDim + idx]) + part[2 * G * kHeadDim + idx]) +
+                    part[3 * G * kHeadDim + idx];
+    qt[idx] = v;
+    float mx = fabsf(v), sm = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      sm += __shfl_xor_sync(kFull, sm, o);
+    }
+    if ((idx & 31) == 0) {
+      red[(idx >> 7) * 4 + ((idx >> 5) & 3)] = mx;
+      red[4 * G + (idx >> 7) * 4 + ((idx >> 5) & 3)] = sm;
+    }
+  }
+  __syncthreads();
+  if (tid < G) {
+    const float mx = fmaxf(fmaxf(red[tid * 4], red[tid * 4 + 1]), fmaxf(red[tid * 4 + 2], red[tid * 4 + 3]));
+    const float sm = ((red[4 * G + tid * 4] + red[4 * G + tid * 4 + 1]) + red[4 * G + tid * 4 + 2]) +
+                     red[4 * G + tid * 4 + 3];
+    int e = 0;
+    if (mx > 0.f) {
+      frexpf(mx, &e);              // mx in [2^(e-1), 2^e)
+      e = max(-100, min(100, 14 - e));
+    }
+    const float scale = kLog2e * rsqrtf(float(kHeadDim));
+    aux[tid * 4 + 0] = ldexpf(1.f, e);
+    aux[tid * 4 + 1] = ldexpf(1.f, 24 - e) * scale;   // 2^24 / sigma * log2(e) / sqrt(d)
+    aux[tid * 4 + 2] = sm * scale;
+  }
+  __syncthreads();
+}
+
+// Lane's B fragments of the QK MMA: column n = 8nt + gid is head n (hi part)
+// for n < G, head n-G (lo part) for n < 2G, zero otherwise; register r = 0
+// holds channels (32tig + j, 32tig + j + 8), r = 1 (32tig + 16 + j,
+// 32tig + 24 + j), each scaled by sigma 4^-pos(j).
+template <int G>
+__device__ __forceinline__ void query_fragments(const float* qt, const float* aux, int gid, int tig,
+                                                uint32_t (&qb)[Geo<G>::NT][8][2],
+                                                float (&unscale)[Geo<G>::HS],
+                                                float (&qz)[Geo<G>::HS]) {
+  constexpr int NT = Geo<G>::NT, HS = Geo<G>::HS;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = 8 * nt + gid;
+    const bool live = col < 2 * G;
+    const int h = col < G ? col : (live ? col - G : 0);
+    const bool lo = col >= G;
+    const float sg = aux[h * 4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float f = sg * ldexpf(1.f, -2 * code_pos(j));
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int c0 = 32 * tig + 16 * rr + j;
+        float v0 = qt[h * kHeadDim + c0] * f, v1 = qt[h * kHeadDim + c0 + 8] * f;
+        if (lo) {
+          v0 = split_lo(v0);
+          v1 = split_lo(v1);
+        }
+        qb[nt][j][rr] = live ? pack_half2(v0, v1) : 0u;
+      }
+    }
+  }
+#pragma unroll
+  for (int hs = 0; hs < HS; ++hs) {
+    const int h = slot_head<G>(tig, hs);
+    unscale[hs] = aux[h * 4 + 1];
+    qz[hs] = aux[h * 4 + 2];
+  }
+}
+
+// Page ids of a warp's pages, 32 at a time, one per lane (warp-collective).
+struct PidWindow {
+  int base = -1, v = -1;
+  __device__ __forceinline__ int get(int k, const int32_t* ptab, int first, int stride, int count,
+                                     int lane) {
+    const int b0 = k & ~31;
+    if (b0 != base) {
+      base = b0;
+      const int kk = b0 + lane;
+      v = kk < count ? __ldg(ptab + first + kk * stride) : -1;
+    }
+    return __shfl_sync(kFull, v, k & 31);
+  }
+};
+
 // ------------------------------------------------------------------ split kernel
 
 template <int G>
-__global__ void __launch_bounds__(kThreads) split_kernel(DecodeParams p) {
-  constexpr int NT = Geo<G>::NT, HS = Geo<G>::HS, NTQ = Geo<G>::NTQ;
+__global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
+  constexpr int NT = Geo<G>::NT, HS = Geo<G>::HS, NTQ = Geo<G>::NTQ, W = Geo<G>::W, T = Geo<G>::T;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stage = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<G>::kStageBytes);
-  float* wstate = reinterpret_cast<float*>(smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes);
-  int* s_last = reinterpret_cast<int*>(smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes +
-                                       Geo<G>::kStateBytes);
+  uint64_t* rbar = bars + W * kStages;
+  uint8_t* uni = smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes;
+  float* st_hist = reinterpret_cast<float*>(uni);
+  float* st_bf16 = st_hist + W * G * kPartStride;
+  float* rks = reinterpret_cast<float*>(uni);                         // prologue only
+  float* qscratch = reinterpret_cast<float*>(uni + Geo<G>::kRotBytes);
+  int* s_last = reinterpret_cast<int*>(uni + Geo<G>::kUnion);
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int pair = b * p.n_kv + hkv;
-  const int n_splits = p.n_hist_splits + p.n_bf16_splits;
+  const int n_splits = p.n_splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
 
-  WarpState<G> st;
-  st.init();
-  float* ws = wstate + warp * G * kPartStride;
+  // ---------------- INT2 page range of this CTA and warp
+  int hist = p.hist_len[b];
+  if (hist < 0 || hist > p.max_pages * kPage) {
+    if (tid == 0) flag(p.dev_status, 0x2);
+    hist = max(0, min(hist, p.max_pages * kPage));
+  }
+  const int n_pg = (hist + kPage - 1) / kPage;
+  if (n_pg > n_splits * p.pages_per_split && split == 0 && tid == 0)
+    flag(p.dev_status, 0x2);  // longer than the host bound max_hist: tail not read
+  const int pbeg = split * p.pages_per_split;
+  const int pend = min(pbeg + p.pages_per_split, n_pg);
+  const int first = pbeg + warp;
+  const int count = pend > first ? (pend - first + W - 1) / W : 0;
+  uint8_t* ring = stage + size_t(warp) * kStages * kBlockBytes;
+  uint64_t* bar = bars + warp * kStages;
+  const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
+  const uint8_t* pool = p.pages + int64_t(hkv) * kBlockBytes;
+  const int64_t page_stride = int64_t(p.n_kv) * kBlockBytes;
 
-  if (split < p.n_hist_splits) {
-    // ---------------- INT2 history pages [pbeg, pend)
-    int hist = p.hist_len[b];
-    if (hist < 0 || hist > p.max_pages * kPage) {
-      if (tid == 0) flag(p.dev_status, 0x2);
-      hist = max(0, min(hist, p.max_pages * kPage));
-    }
-    const int n_pg = (hist + kPage - 1) / kPage;
-    if (n_pg > p.n_hist_splits * p.pages_per_split && split == 0 && tid == 0)
-      flag(p.dev_status, 0x2);  // longer than the host bound max_hist: tail not read
-    const int pbeg = split * p.pages_per_split;
-    const int pend = min(pbeg + p.pages_per_split, n_pg);
-    const int first = pbeg + warp;
-    const int count = pend > first ? (pend - first + kWarps - 1) / kWarps : 0;
-    uint8_t* ring = stage + size_t(warp) * kStages * kBlockBytes;
-    uint64_t* bar = bars + warp * kStages;
-    const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
-    const uint8_t* pool = p.pages + int64_t(hkv) * kBlockBytes;
-    const int64_t page_stride = int64_t(p.n_kv) * kBlockBytes;
-
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bar + s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  PidWindow issue_ids, comp_ids;
+  auto issue = [&](int k) {  // warp-collective; lane 0 starts the copy
+    const int pid = issue_ids.get(k, ptab, first, W, count, lane);
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) mbar_init(bar + s, 1);
-      fence_mbar_init();
-    }
-    __syncwarp();
-    auto issue = [&](int k) {  // lane 0 only
-      const int pi = first + k * kWarps;
-      const int pid = ptab[pi];
       const int s = k % kStages;
       if (pid < 0 || pid >= p.n_pages) {
         // no copy: complete the stage's phase without bytes so the ring stays in step
         flag(p.dev_status, 0x1);
         mbar_arrive(bar + s);
-        return;
+      } else {
+        mbar_arrive_expect_tx(bar + s, kBlockBytes);
+        bulk_copy_g2s(ring + s * kBlockBytes, pool + int64_t(pid) * page_stride, kBlockBytes, bar + s);
       }
-      mbar_arrive_expect_tx(bar + s, kBlockBytes);
-      bulk_copy_g2s(ring + s * kBlockBytes, pool + int64_t(pid) * page_stride, kBlockBytes, bar + s);
-    };
-    if (lane == 0)
-      for (int k = 0; k < min(count, kStages); ++k) issue(k);
-
-    pdl_wait();  // q~ fragments and tickets come from the prep kernel
-    uint32_t qb[NT][8][2];
-    {
-      const uint2* src = reinterpret_cast<const uint2*>(p.qfrag) + int64_t(pair) * NT * 8 * 32;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint2 v = src[(nt * 8 + j) * 32 + lane];
-          qb[nt][j][0] = v.x;
-          qb[nt][j][1] = v.y;
-        }
     }
-    float unscale[HS], qz[HS];
-#pragma unroll
-    for (int hs = 0; hs < HS; ++hs) {
-      const int h = slot_head<G>(tig, hs);
-      unscale[hs] = p.qaux[(pair * G + h) * 2 + 0];
-      qz[hs] = p.qaux[(pair * G + h) * 2 + 1];
-    }
+  };
+  for (int k = 0; k < min(count, kStages); ++k) issue(k);
 
+  // ---------------- q~ (only CTAs that own pages need it)
+  uint32_t qb[NT][8][2];
+  float unscale[HS], qz[HS];
+  const bool any_pages = pend > pbeg;
+  if (any_pages) {
+    rotate_query<G>(p, b, hkv, rks, rbar, qscratch);
+    query_fragments<G>(qscratch + 5 * G * kHeadDim, qscratch + 6 * G * kHeadDim, gid, tig, qb, unscale, qz);
+  }
+  __syncthreads();   // prologue reads done before warp states overwrite the region
+
+  // ---------------- INT2 pages
+  {
+    WarpState<G> st;
+    st.init();
     bool timed_out = false;
     int k = 0;
     for (; k < count; ++k) {
-      const int pi = first + k * kWarps;
-      const int pid = ptab[pi];
+      const int pid = comp_ids.get(k, ptab, first, W, count, lane);
       const bool valid = pid >= 0 && pid < p.n_pages;
       const int s = k % kStages;
       if (!mbar_wait_bounded(bar + s, (k / kStages) & 1, kWaitLimitNs)) {
@@ -580,11 +653,15 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeParams p) {
         break;
       }
       if (valid) {
+        const int pi = first + k * W;
         const int ntok = min(kPage, hist - pi * kPage);
-        int2_page<G>(ring + s * kBlockBytes, ntok, gid, tig, qb, unscale, qz, p.sigma_v, st);
+        if (ntok == kPage)
+          int2_page<G, false>(ring + s * kBlockBytes, ntok, gid, tig, qb, unscale, qz, p.sigma_v, st);
+        else
+          int2_page<G, true>(ring + s * kBlockBytes, ntok, gid, tig, qb, unscale, qz, p.sigma_v, st);
       }
       __syncwarp();
-      if (lane == 0 && k + kStages < count) issue(k + kStages);
+      if (k + kStages < count) issue(k + kStages);
     }
     if (timed_out) {
       if (lane == 0) flag(p.dev_status, 0x4);
@@ -593,11 +670,11 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeParams p) {
       for (int kk = k; kk < min(count, k + kStages); ++kk)
         mbar_wait_bounded(bar + kk % kStages, (kk / kStages) & 1, kWaitLimitNs);
     }
-    store_warp_state<G, true>(st, ws, gid, tig, p.pv_unscale);
-  } else {
-    // ---------------- BF16 sink and recent tokens
-    pdl_wait();
-    const int bs = split - p.n_hist_splits;
+    store_warp_state<G, true>(st, st_hist + warp * G * kPartStride, gid, tig, p.pv_unscale);
+  }
+
+  // ---------------- BF16 sink / recent tokens owned by this CTA
+  {
     int sink_len = p.sink_len[b], rec_len = p.recent_len[b];
     const int rec_start = p.recent_start[b];
     if (sink_len < 0 || sink_len > p.sink_cap || rec_len < 0 || rec_len > p.recent_cap ||
@@ -607,16 +684,15 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeParams p) {
       rec_len = max(0, min(rec_len, p.recent_cap));
     }
     const int start = min(max(rec_start, 0), max(p.recent_cap - 1, 0));
-    const int sink_pages = p.sink_cap / kPage;
-    const int n_vp = sink_pages + p.recent_cap / kPage;
-    const int vbeg = bs * p.vpages_per_split;
-    const int vend = min(vbeg + p.vpages_per_split, n_vp);
+    const int n_vp = p.sink_cap / kPage + p.recent_cap / kPage;
     const int64_t hstride = int64_t(p.n_kv) * kHeadDim;
-
-    uint32_t qf[NTQ][8][2];
-    {
-      // B operand: column n is head n % G (heads duplicated when G < 8);
-      // r = 0 holds channels (32tig + 4j, +1), r = 1 (32tig + 4j + 2, +3)
+    WarpState<G> st;
+    st.init();
+    // virtual pages split, split + n_splits, ...; the k-th goes to warp
+    // W-1-(k % W): the last warps own the fewest INT2 pages
+    const int mine = split + (W - 1 - warp) * n_splits;
+    if (mine < n_vp) {
+      uint32_t qf[NTQ][8][2];
 #pragma unroll
       for (int nt = 0; nt < NTQ; ++nt) {
         const int h = (8 * nt + gid) % G;
@@ -630,53 +706,58 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeParams p) {
           qf[nt][2 * u + 1][1] = v.w;
         }
       }
-    }
-    auto row_of = [&](int u, bool kv, bool& ok) -> const uint16_t* {
-      if (u < p.sink_cap) {
-        ok = u < sink_len;
-        const uint16_t* base = kv ? p.sink_v : p.sink_k;
-        return base + (int64_t(b) * p.sink_cap + u) * hstride + int64_t(hkv) * kHeadDim;
+      auto row_of = [&](int u, bool kv, bool& ok) -> const uint16_t* {
+        if (u < p.sink_cap) {
+          ok = u < sink_len;
+          const uint16_t* base = kv ? p.sink_v : p.sink_k;
+          return base + (int64_t(b) * p.sink_cap + u) * hstride + int64_t(hkv) * kHeadDim;
+        }
+        const int i = u - p.sink_cap;
+        ok = i < rec_len;
+        const int slot = (start + i) % p.recent_cap;
+        const uint16_t* base = kv ? p.recent_v : p.recent_k;
+        return base + (int64_t(b) * p.recent_cap + slot) * hstride + int64_t(hkv) * kHeadDim;
+      };
+      for (int vp = mine; vp < n_vp; vp += W * n_splits) {
+        const int u0 = vp * kPage;
+        bool kok[2], vok[4];
+        const uint16_t* krow[2] = {row_of(u0 + gid, false, kok[0]), row_of(u0 + gid + 8, false, kok[1])};
+        const uint16_t* vrow[4] = {row_of(u0 + 2 * tig, true, vok[0]), row_of(u0 + 2 * tig + 1, true, vok[1]),
+                                   row_of(u0 + 2 * tig + 8, true, vok[2]),
+                                   row_of(u0 + 2 * tig + 9, true, vok[3])};
+        bf16_page<G>(krow, vrow, kok, vok, gid, tig, qf, st);
       }
-      const int i = u - p.sink_cap;
-      ok = i < rec_len;
-      const int slot = (start + i) % p.recent_cap;
-      const uint16_t* base = kv ? p.recent_v : p.recent_k;
-      return base + (int64_t(b) * p.recent_cap + slot) * hstride + int64_t(hkv) * kHeadDim;
-    };
-    for (int vp = vbeg + warp; vp < vend; vp += kWarps) {
-      const int u0 = vp * kPage;
-      bool kok[2], vok[4];
-      const uint16_t* krow[2] = {row_of(u0 + gid, false, kok[0]), row_of(u0 + gid + 8, false, kok[1])};
-      const uint16_t* vrow[4] = {row_of(u0 + 2 * tig, true, vok[0]), row_of(u0 + 2 * tig + 1, true, vok[1]),
-                                 row_of(u0 + 2 * tig + 8, true, vok[2]),
-                                 row_of(u0 + 2 * tig + 9, true, vok[3])};
-      bf16_page<G>(krow, vrow, kok, vok, gid, tig, qf, st);
     }
-    store_warp_state<G, false>(st, ws, gid, tig, 1.f);
+    store_warp_state<G, false>(st, st_bf16 + warp * G * kPartStride, gid, tig, 1.f);
   }
   __syncthreads();
 
-  // ---------------- CTA merge of the warps' states -> one partial per head
-  float* part = p.partials + (int64_t(pair) * n_splits + split) * G * kPartStride;
-  for (int h = 0; h < G; ++h) {
+  // ---------------- CTA merge of the warps -> one partial per head and type
+  float* part = p.partials + (int64_t(pair) * n_splits + split) * 2 * G * kPartStride;
+  for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
+    const int type = idx / (G * kHeadDim), h = (idx / kHeadDim) % G, c = idx % kHeadDim;
+    const float* src = type ? st_bf16 : st_hist;
     float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-      if (wstate[(w * G + h) * kPartStride + 1] > 0.f) mx = fmaxf(mx, wstate[(w * G + h) * kPartStride]);
+#pragma unroll 4
+    for (int w = 0; w < W; ++w) {
+      const float* s = src + (w * G + h) * kPartStride;
+      if (s[1] > 0.f) mx = fmaxf(mx, s[0]);
+    }
     float lsum = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float* s = wstate + (w * G + h) * kPartStride;
+#pragma unroll 4
+    for (int w = 0; w < W; ++w) {
+      const float* s = src + (w * G + h) * kPartStride;
       if (s[1] > 0.f) {
         const float f = exp2f(s[0] - mx);
         lsum = fmaf(s[1], f, lsum);
-        o = fmaf(s[4 + tid], f, o);
+        o = fmaf(s[4 + c], f, o);
       }
     }
-    part[h * kPartStride + 4 + tid] = o;
-    if (tid == 0) {
-      part[h * kPartStride + 0] = mx;
-      part[h * kPartStride + 1] = lsum;
+    float* dst = part + (type * G + h) * kPartStride;
+    dst[4 + c] = o;
+    if (c == 0) {
+      dst[0] = mx;
+      dst[1] = lsum;
     }
   }
 
@@ -691,80 +772,139 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DecodeParams p) {
   if (!*s_last) return;
   __threadfence();
 
-  const float* pp = p.partials + int64_t(pair) * n_splits * G * kPartStride;
-  float* oh = wstate;  // [G][128] merged history partial (rotated domain)
-  float mh[G], lh[G];
+  // R_V rows for the output rotation, fetched now so their latency overlaps
+  // the partial loads: thread -> (row c, quarter qq of the row)
+  constexpr int kRowSets = (4 * kHeadDim + T - 1) / T;
+  float4 rv[kRowSets][8];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float mx = -INFINITY;
-    for (int s = 0; s < p.n_hist_splits; ++s) {
-      const float* q = pp + (s * G + h) * kPartStride;
-      if (__ldcg(q + 1) > 0.f) mx = fmaxf(mx, __ldcg(q));
+  for (int rs = 0; rs < kRowSets; ++rs) {
+    const int task = tid + rs * T;
+    const int c = task >> 2, qq = task & 3;
+    if (c < kHeadDim) {
+      const float* row = p.r_v + (int64_t(hkv) * kHeadDim + c) * kHeadDim + 32 * qq;
+#pragma unroll
+      for (int k4 = 0; k4 < 8; ++k4) rv[rs][k4] = ldg_keep4(row + 4 * k4);
     }
-    float lsum = 0.f, o = 0.f;
-    for (int s = 0; s < p.n_hist_splits; ++s) {
-      const float* q = pp + (s * G + h) * kPartStride;
-      const float l = __ldcg(q + 1);
-      if (l > 0.f) {
-        const float f = exp2f(__ldcg(q) - mx);
-        lsum = fmaf(l, f, lsum);
-        o = fmaf(__ldcg(q + 4 + tid), f, o);
-      }
-    }
-    mh[h] = mx;
-    lh[h] = lsum;
-    oh[h * kHeadDim + tid] = o;
+  }
+
+  const float* pp = p.partials + int64_t(pair) * n_splits * 2 * G * kPartStride;
+  const int NP = n_splits * 2 * G;           // partial records of this pair
+  float* ms = reinterpret_cast<float*>(stage);
+  float* ls = ms + NP;
+  float* wt = ls + NP;
+  constexpr int SG = 4;
+  float* acc = wt + NP;                      // [2][SG][G][128]
+  float* oh = acc + 2 * SG * G * kHeadDim;   // [2][G][128]
+  float* hm = oh + 2 * G * kHeadDim;         // [G][2]: history factor, 1 / L
+  for (int i = tid; i < NP; i += T) {
+    ms[i] = __ldcg(pp + int64_t(i) * kPartStride);
+    ls[i] = __ldcg(pp + int64_t(i) * kPartStride + 1);
   }
   __syncthreads();
-  // history output back in the original basis: o[c] = sum_j o~[j] R_V[c][j]
-  float orot[G];
+  // weights: history partials relative to their own max (they are rotated
+  // after the sum); BF16 partials relative to the final max
+  if (warp < G) {
+    const int h = warp;
+    float mh = -INFINITY;
+    for (int s = lane; s < n_splits; s += 32) {
+      const int i = (s * 2 + 0) * G + h;
+      if (ls[i] > 0.f) mh = fmaxf(mh, ms[i]);
+    }
 #pragma unroll
-  for (int h = 0; h < G; ++h) orot[h] = 0.f;
-  {
-    const float4* rrow = reinterpret_cast<const float4*>(p.r_v + (int64_t(hkv) * kHeadDim + tid) * kHeadDim);
+    for (int o = 16; o > 0; o >>= 1) mh = fmaxf(mh, __shfl_xor_sync(kFull, mh, o));
+    float lh = 0.f;
+    for (int s = lane; s < n_splits; s += 32) {
+      const int i = (s * 2 + 0) * G + h;
+      const float w = ls[i] > 0.f ? exp2f(ms[i] - mh) : 0.f;
+      wt[i] = w;
+      lh = fmaf(ls[i], w, lh);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lh += __shfl_xor_sync(kFull, lh, o);
+    float m = lh > 0.f ? mh : -INFINITY;
+    for (int s = lane; s < n_splits; s += 32) {
+      const int i = (s * 2 + 1) * G + h;
+      if (ls[i] > 0.f) m = fmaxf(m, ms[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    float lt = 0.f;
+    for (int s = lane; s < n_splits; s += 32) {
+      const int i = (s * 2 + 1) * G + h;
+      const float w = ls[i] > 0.f ? exp2f(ms[i] - m) : 0.f;
+      wt[i] = w;
+      lt = fmaf(ls[i], w, lt);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(kFull, lt, o);
+    if (lane == 0) {
+      const float fh = lh > 0.f ? exp2f(mh - m) : 0.f;
+      const float l = fmaf(lh, fh, lt);
+      hm[h * 2 + 0] = fh;
+      hm[h * 2 + 1] = l > 0.f ? 1.f / l : 0.f;
+    }
+  }
+  __syncthreads();
+  // weighted sums of the partial outputs: task (type, h, c4, sg) sums splits
+  // s = sg, sg + SG, ... in order (float4 loads, all independent)
+  for (int task = tid; task < 2 * G * 32 * SG; task += T) {
+    const int sg = task % SG, c4 = (task / SG) % 32, h = (task / (SG * 32)) % G, type = task / (SG * 32 * G);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int j4 = 0; j4 < kHeadDim / 4; ++j4) {
-      const float4 r = __ldg(rrow + j4);
+    for (int s = sg; s < n_splits; s += SG) {
+      const int i = (s * 2 + type) * G + h;
+      const float w = wt[i];
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i) * kPartStride + 4) + c4);
+      a.x = fmaf(w, o.x, a.x);
+      a.y = fmaf(w, o.y, a.y);
+      a.z = fmaf(w, o.z, a.z);
+      a.w = fmaf(w, o.w, a.w);
+    }
+    reinterpret_cast<float4*>(acc + ((type * SG + sg) * G + h) * kHeadDim)[c4] = a;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
+    const int type = idx / (G * kHeadDim), hc = idx % (G * kHeadDim);
+    float v = 0.f;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float* o = oh + h * kHeadDim + 4 * j4;
-        orot[h] = fmaf(o[0], r.x, fmaf(o[1], r.y, fmaf(o[2], r.z, fmaf(o[3], r.w, orot[h]))));
+    for (int sg = 0; sg < SG; ++sg) v += acc[(type * SG + sg) * G * kHeadDim + hc];
+    oh[idx] = v;
+  }
+  __syncthreads();
+  // out[c] = (sum_j o~[j] R_V[c][j] * f_hist + o_bf16[c]) / L
+#pragma unroll
+  for (int rs = 0; rs < kRowSets; ++rs) {
+    const int task = tid + rs * T;
+    const int c = task >> 2, qq = task & 3;
+    const bool live = c < kHeadDim;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float d = 0.f;
+      if (live) {
+        const float4* o = reinterpret_cast<const float4*>(oh + h * kHeadDim + 32 * qq);
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 ov = o[k4];
+          d = fmaf(ov.x, rv[rs][k4].x, fmaf(ov.y, rv[rs][k4].y, fmaf(ov.z, rv[rs][k4].z, fmaf(ov.w, rv[rs][k4].w, d))));
+        }
+      }
+      d += __shfl_xor_sync(kFull, d, 1);
+      d += __shfl_xor_sync(kFull, d, 2);
+      if (live && qq == 0) {
+        const float v = fmaf(d, hm[h * 2], oh[G * kHeadDim + h * kHeadDim + c]) * hm[h * 2 + 1];
+        p.out[(int64_t(b) * p.n_kv * G + int64_t(hkv) * G + h) * kHeadDim + c] = v;
       }
     }
   }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float mx = lh[h] > 0.f ? mh[h] : -INFINITY;
-    for (int s = p.n_hist_splits; s < n_splits; ++s) {
-      const float* q = pp + (s * G + h) * kPartStride;
-      if (__ldcg(q + 1) > 0.f) mx = fmaxf(mx, __ldcg(q));
-    }
-    float lsum = 0.f, o = 0.f;
-    if (lh[h] > 0.f) {
-      const float f = exp2f(mh[h] - mx);
-      lsum = lh[h] * f;
-      o = orot[h] * f;
-    }
-    for (int s = p.n_hist_splits; s < n_splits; ++s) {
-      const float* q = pp + (s * G + h) * kPartStride;
-      const float l = __ldcg(q + 1);
-      if (l > 0.f) {
-        const float f = exp2f(__ldcg(q) - mx);
-        lsum = fmaf(l, f, lsum);
-        o = fmaf(__ldcg(q + 4 + tid), f, o);
-      }
-    }
-    p.out[(int64_t(b) * p.n_kv * G + hkv * G + h) * kHeadDim + tid] = lsum > 0.f ? o / lsum : 0.f;
-  }
+  if (tid == 0) p.counters[pair] = 0u;   // ready for the next call
 }
 
 template <int G>
 int occupancy() {
   int occ = 0;
-  cudaFuncSetAttribute(split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       int(Geo<G>::kSmem));
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<G>, kThreads,
-                                                    Geo<G>::kSmem) != cudaSuccess)
+  cudaFuncSetAttribute(split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Geo<G>::kSmem));
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<G>, Geo<G>::T, Geo<G>::kSmem) !=
+      cudaSuccess)
     return 0;
   return occ;
 }
@@ -774,20 +914,8 @@ cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Geo<G>::kSmem));
   if (e != cudaSuccess) return e;
-  prep_kernel<G><<<dim3(p.n_kv, p.batch), kThreads, 0, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_hist_splits + p.n_bf16_splits, p.n_kv, p.batch);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Geo<G>::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_kernel<G>, p);
+  split_kernel<G><<<dim3(p.n_splits, p.n_kv, p.batch), Geo<G>::T, Geo<G>::kSmem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -796,6 +924,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, int max_hist,
                 DecodePlan* plan, cudaError_t* err) {
+  (void)sink_cap;
+  (void)recent_cap;
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return 0;
@@ -818,39 +948,33 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
     }
     if (dev < 64) occ_cache[dev][gi] = occ;
   }
+  const int warps = group == 4 ? Geo<4>::W : Geo<8>::W;
   const int64_t slots = int64_t(sms) * occ;
   const int64_t pairs = int64_t(batch) * n_kv;
   const int pages_max = (max_hist + kPage - 1) / kPage;
-  const int n_vp = sink_cap / kPage + recent_cap / kPage;
-  int n_bf16 = (n_vp == 0) ? 0 : (pairs * 2 <= slots ? 2 : 1);
-  n_bf16 = min(n_bf16, n_vp);
-  int n_hist = 1, pps = max(pages_max, 1);
-  const int64_t avail = slots - pairs * n_bf16;
-  const int kOneWaveCap = 256;
-  if (avail >= pairs && pages_max > 0) {
-    const int per_pair = int(avail / pairs < 4096 ? avail / pairs : 4096);
-    const int p1 = (pages_max + per_pair - 1) / per_pair;
-    if (p1 <= kOneWaveCap) pps = max(p1, 1);
-    else pps = 128;
+  // one wave when every (request, KV head) can get whole SMs and each warp
+  // then streams at most 64 pages; otherwise 16 pages per warp and several
+  // waves balanced by the block scheduler
+  int pps;
+  const int64_t per_pair = slots / pairs;
+  if (per_pair >= 1 && (pages_max + per_pair - 1) / per_pair <= 64 * warps) {
+    pps = int((pages_max + per_pair - 1) / per_pair);
   } else {
-    pps = 128;
+    pps = 16 * warps;
   }
-  n_hist = max(1, (pages_max + pps - 1) / pps);
-  plan->n_hist_splits = n_hist;
-  plan->n_bf16_splits = n_bf16;
+  pps = max(pps, 1);
+  int n_splits = max(1, (pages_max + pps - 1) / pps);
+  if (n_splits > kMaxSplits) {
+    pps = (pages_max + kMaxSplits - 1) / kMaxSplits;
+    n_splits = (pages_max + pps - 1) / pps;
+  }
+  plan->n_splits = n_splits;
   plan->pages_per_split = pps;
-  plan->vpages_per_split = n_bf16 ? (n_vp + n_bf16 - 1) / n_bf16 : 0;
-  const int nt = (2 * group + 7) / 8;
-  const int n_splits = n_hist + n_bf16;
   size_t off = 0;
   plan->off_counters = off;
   off = align256(off + size_t(pairs) * 4);
-  plan->off_qfrag = off;
-  off = align256(off + size_t(pairs) * nt * 8 * 32 * 8);
-  plan->off_qaux = off;
-  off = align256(off + size_t(pairs) * group * 2 * 4);
   plan->off_partials = off;
-  off = align256(off + size_t(pairs) * n_splits * group * kPartStride * 4);
+  off = align256(off + size_t(pairs) * n_splits * 2 * group * kPartStride * 4);
   plan->total_bytes = off;
   *err = cudaSuccess;
   return occ;

@@ -56,23 +56,21 @@ struct DecodeParams {
   const uint16_t* q;
   float* out;
   // workspace views
-  uint32_t* counters;   // [pairs]
-  uint32_t* qfrag;      // [pairs][NT][8][32][2]
-  float* qaux;          // [pairs][G][2]
-  float* partials;      // [pairs][n_splits][G][kPartStride]
+  uint32_t* counters;   // [pairs] merge tickets (zero between calls)
+  float* partials;      // [pairs][n_splits][2][G][kPartStride]
   // dims
   int32_t batch, n_kv, group, sink_cap, recent_cap, max_pages;
   int64_t n_pages;
   int32_t max_hist;
   // split plan
-  int32_t n_hist_splits, n_bf16_splits, pages_per_split, vpages_per_split;
-  // scale of the PV B operand (power of two) and its inverse times 2^24
+  int32_t n_splits, pages_per_split;
+  // scale of the PV B operand (power of two) and 2^24 / sigma_v
   float sigma_v, pv_unscale;
 };
 
 struct DecodePlan {
-  int32_t n_hist_splits, n_bf16_splits, pages_per_split, vpages_per_split;
-  size_t off_counters, off_qfrag, off_qaux, off_partials, total_bytes;
+  int32_t n_splits, pages_per_split;
+  size_t off_counters, off_partials, total_bytes;
 };
 
 // Split plan and workspace layout for the current device; returns the

@@ -146,8 +146,6 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   p.out = out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = reinterpret_cast<uint32_t*>(ws + plan.off_counters);
-  p.qfrag = reinterpret_cast<uint32_t*>(ws + plan.off_qfrag);
-  p.qaux = reinterpret_cast<float*>(ws + plan.off_qaux);
   p.partials = reinterpret_cast<float*>(ws + plan.off_partials);
   p.batch = desc->batch;
   p.n_kv = desc->n_kv_heads;
@@ -157,10 +155,8 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   p.max_pages = desc->max_pages_per_seq;
   p.n_pages = desc->n_pages;
   p.max_hist = desc->max_hist;
-  p.n_hist_splits = plan.n_hist_splits;
-  p.n_bf16_splits = plan.n_bf16_splits;
+  p.n_splits = plan.n_splits;
   p.pages_per_split = plan.pages_per_split;
-  p.vpages_per_split = plan.vpages_per_split;
   // PV operand scale: p <= 2^8 and s_V <= 2 tau_v / 3 (x2 margin for fp16
   // rounding), so p s_V sigma_v stays below 2^14 in fp16
   int e = 0;

@@ -209,8 +209,10 @@ oscar_status oscar_quantize_append(const oscar_layer_desc* desc,
  *   Workspace: call with workspace == NULL to receive the required size in
  *   *workspace_bytes (depends on desc dims and the current device) and
  *   return.  Otherwise workspace must be 256-byte aligned device memory of
- *   at least that size, used by one call at a time (no initialisation
- *   needed).  Async.
+ *   at least that size, zero-filled before its first use (cudaMemset); each
+ *   call leaves it ready for the next one.  It holds per-call merge tickets
+ *   and split partials, so two calls in flight at the same time need two
+ *   workspaces.  Async.
  */
 oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
                                     float* out, void* workspace, size_t* workspace_bytes,

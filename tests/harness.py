@@ -216,7 +216,7 @@ def run_decode(cache, q, max_hist=None):
     from bit_rotated_kv_split_gb300 import binding as B
     desc = cache.desc(max_hist)
     nbytes = B.oscar_decode_workspace_bytes(desc)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     B.oscar_decode_attention(desc, q, out, ws)
     torch.cuda.synchronize()

@@ -122,3 +122,24 @@ def test_full_size_qwen3_8b_layer_100k():
     # configuration as the benchmark (plan depends only on dims and device)
     sc = H.Scenario(1002, [100_000], n_kv=8, g=4, cal=(4096, 2048))
     _check(sc)
+
+
+def test_workspace_is_reusable_across_calls():
+    # the merge tickets reset themselves: back-to-back calls on one workspace
+    # give identical outputs
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    sc = H.Scenario(19, [4000, 900], n_kv=2, g=4)
+    cache, q = H.to_device(sc)
+    desc = cache.desc()
+    ws = torch.zeros(B.oscar_decode_workspace_bytes(desc), dtype=torch.uint8, device=q.device)
+    outs = []
+    for _ in range(3):
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        B.oscar_decode_attention(desc, q, out, ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    err = H.relative_error(outs[0].cpu().numpy().astype(np.float64), sc.expected())
+    assert err.max() <= TOL
