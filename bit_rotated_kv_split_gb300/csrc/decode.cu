@@ -13,20 +13,20 @@
 // CTA per SM) owns a contiguous range of INT2 pages of one (request, KV head)
 // and a share of its BF16 sink/recent tokens:
 //   1. lane 0 of each warp starts 1-D TMA bulk copies of the warp's first
-//      pages (one 1152-byte page block per stage, a ring of stages per warp,
-//      mbarrier completion, bounded waits);
-//   2. meanwhile R_K arrives in shared memory by one TMA bulk transfer and
-//      the CTA computes q~ = q . R_K for the GQA group (fp32), then builds
-//      each lane's tensor-core B fragments from it;
+//      pages (one 1152-byte page block per stage, a ring of 6 (GQA 4) or 8
+//      (GQA 8) stages per warp, mbarrier completion, bounded waits);
+//   2. R_K arrives in shared memory by one TMA bulk transfer issued first;
+//      the CTA computes q~ = q . R_K for the GQA group (fp32) and builds the
+//      32 lanes' tensor-core B fragments once in shared memory;
 //   3. every warp streams its INT2 pages through its ring, keeping its own
 //      online-softmax state; then the warps owning the fewest pages scan the
 //      CTA's BF16 tokens (direct vector loads);
 //   4. the CTA merges its warps into two partials (m, l, o) per query head
-//      (history, rotated domain; BF16, original domain);
+//      (history and BF16) and rotates the history one back with R_V (staged
+//      by TMA during the scan), so every partial is in the original basis;
 //   5. the last CTA of the (request, KV head) to finish (atomic ticket, no
-//      waiting) merges all partials - loads kept in flight, R_V prefetched -
-//      applies . R_V^T to the history part and writes the normalised output,
-//      then resets the ticket.
+//      waiting) merges all partials (one warp per head, loads batched) and
+//      writes the normalised output, then resets the ticket.
 //
 // INT2 arithmetic on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
 //   QK: A = codes of 16 tokens x 128 channels, B = q~ (hi | lo columns), so
@@ -50,8 +50,11 @@
 #ifndef OSCAR_WARPS_G8
 #define OSCAR_WARPS_G8 12
 #endif
-#ifndef OSCAR_STAGES
-#define OSCAR_STAGES 6
+#ifndef OSCAR_STAGES_G4
+#define OSCAR_STAGES_G4 6
+#endif
+#ifndef OSCAR_STAGES_G8
+#define OSCAR_STAGES_G8 8
 #endif
 #ifndef OSCAR_QK_CHAINS
 #define OSCAR_QK_CHAINS 2
@@ -60,7 +63,6 @@
 namespace oscar {
 namespace {
 
-constexpr int kStages = OSCAR_STAGES;
 constexpr int kQkChains = OSCAR_QK_CHAINS;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (p <= 2^8)
@@ -75,19 +77,26 @@ struct Geo {
   static constexpr int NTQ = (G + 7) / 8;             // BF16 QK column tiles
   static constexpr int W = G <= 4 ? OSCAR_WARPS_G4 : OSCAR_WARPS_G8;  // warps per CTA
   static constexpr int T = W * 32;
+  static constexpr int kStages = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;   // ring stages per warp
   static constexpr size_t kStageBytes = size_t(W) * kStages * kBlockBytes;
-  // ring barriers + the R_K barrier, padded so the region after it stays
-  // 128-byte aligned (TMA destinations need at least 16)
-  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 1) * 8 + 127) / 128 * 128;
+  // ring barriers + the R_K and R_V barriers, padded so the region after it
+  // stays 128-byte aligned (TMA destinations need at least 16)
+  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 2) * 8 + 127) / 128 * 128;
   static constexpr size_t kStateBytes = size_t(W) * G * kPartStride * 4;   // per partial type
   // prologue: R_K (64 KB) and the q~ scratch; epilogue: two warp-state sets
   static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
-  static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G) * 4;
-  static constexpr size_t kUnion0 = kRotBytes + kQScratch;
-  static constexpr size_t kUnion = (kUnion0 > 2 * kStateBytes ? kUnion0 : 2 * kStateBytes);
+  static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G + 32 * NT * 16) * 4;
+  static constexpr size_t kUnion = kRotBytes + kQScratch;   // R_K then R_V | q~ scratch
   static constexpr size_t kSmem = kStageBytes + kBarBytes + kUnion + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+  // last-CTA merge scratch in the ring region: (max, sum), split weights,
+  // half sums and merged outputs
+  // each warp's ring slice holds its two warp states at the end
+  static_assert(2 * G * kPartStride * 4 <= kStages * kBlockBytes, "warp states in the ring slice");
+  // CTA merge scratch (after R_V in the union) and last-CTA scratch (ring)
+  static_assert((2 * G * W + 4 * G + G * kHeadDim) * 4 <= kQScratch, "CTA merge scratch");
+  static_assert((2 * G + 2 * G * 128 + 2 * G * kHeadDim) * 4 <= kStageBytes, "merge scratch");
 };
 
 // head owned by head slot hs of a lane with column group tig
@@ -435,46 +444,57 @@ __device__ __forceinline__ void store_warp_state(WarpState<G>& st, float* ws, in
 
 // ------------------------------------------------------------------ q~ and its fragments
 
-// q~ = q . R_K for the G query heads of (b, hkv), in fp32 with a fixed
-// summation order; R_K (64 KB) is brought into shared memory `rks` by one
-// TMA bulk transfer.  Per head a power-of-two scale sigma puts max|q~ sigma|
-// in [2^13, 2^14) so the fp16 hi part is normal and the lo part precise.
-// Leaves qt[G][128] (unscaled) at scratch + 5 G 128 and aux[G][4] =
-// (sigma, unscale, qz, -) at scratch + 6 G 128.
+// Shared-memory scratch of the prologue, in floats: qs[G][128] | part[4][G][128]
+// | qt[G][128] | aux[G][4] | red[2][G][4] | frag[32][NT*16] (u32).
 template <int G>
-__device__ void rotate_query(const DecodeParams& p, int b, int hkv, float* rks, uint64_t* rbar,
+struct QScratch {
+  static constexpr int kQs = 0, kPart = G * kHeadDim, kQt = 5 * G * kHeadDim, kAux = 6 * G * kHeadDim;
+  static constexpr int kRed = kAux + 4 * G, kFrag = kRed + 8 * G;
+  static constexpr int kFloats = kFrag + 32 * Geo<G>::NT * 16;
+  static_assert(kFrag % 4 == 0, "fragment rows are read as uint4");
+};
+
+// q~ = q . R_K for the G query heads of (b, hkv) in fp32 (fixed summation
+// order) from R_K and q already in shared memory (`rks` by a TMA issued at
+// kernel start, qs filled at kernel start).  Per head a power-of-two scale sigma puts max|q~ sigma| in
+// [2^13, 2^14) so the fp16 hi part is normal and the lo part precise.  The
+// 32 lanes' B fragments of the QK MMA are built once per CTA: column
+// n = 8nt + gid is head n (hi part) for n < G, head n-G (lo part) for
+// n < 2G, zero otherwise; register r = 0 holds channels (32tig + j,
+// 32tig + j + 8), r = 1 (32tig + 16 + j, 32tig + 24 + j), each scaled by
+// sigma 4^-pos(j).  aux[h] = (sigma, unscale, qz).
+template <int G>
+__device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float* rks, uint64_t* rbar,
                              float* scratch) {
-  constexpr int T = Geo<G>::T;
-  float* qs = scratch;                 // [G][128]
-  float* part = qs + G * kHeadDim;     // [4][G][128]
-  float* qt = part + 4 * G * kHeadDim; // [G][128]
-  float* aux = qt + G * kHeadDim;      // [G][4]
-  float* red = aux + 4 * G;            // [G][4] partial max | [G][4] partial sum
+  constexpr int T = Geo<G>::T, NT = Geo<G>::NT;
+  using S = QScratch<G>;
+  float* qs = scratch + S::kQs;
+  float* part = scratch + S::kPart;
+  float* qt = scratch + S::kQt;
+  float* aux = scratch + S::kAux;
+  float* red = scratch + S::kRed;
+  uint32_t* frag = reinterpret_cast<uint32_t*>(scratch + S::kFrag);
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    mbar_init(rbar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(rbar, uint32_t(Geo<G>::kRotBytes));
-    const float* rk = p.r_k + int64_t(hkv) * kHeadDim * kHeadDim;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      bulk_copy_g2s(rks + c * (kHeadDim * kHeadDim / 4), rk + c * (kHeadDim * kHeadDim / 4),
-                    uint32_t(Geo<G>::kRotBytes / 4), rbar);
-  }
-  const uint16_t* qg = p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim;
-  for (int i = tid; i < G * kHeadDim; i += T) qs[i] = __uint_as_float(uint32_t(qg[i]) << 16);
-  __syncthreads();
+  __syncthreads();   // qs was filled at kernel start
   if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
   for (int task = tid; task < 4 * kHeadDim; task += T) {
     const int ig = task / kHeadDim, j = task % kHeadDim;
+    float acc[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float acc = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i)
-        acc = fmaf(qs[h * kHeadDim + 32 * ig + i], rks[(32 * ig + i) * kHeadDim + j], acc);
-      part[(ig * G + h) * kHeadDim + j] = acc;
+    for (int h = 0; h < G; ++h) acc[h] = 0.f;
+#pragma unroll 2
+    for (int i4 = 0; i4 < 8; ++i4) {
+      const int i0 = 32 * ig + 4 * i4;
+      const float r0 = rks[(i0 + 0) * kHeadDim + j], r1 = rks[(i0 + 1) * kHeadDim + j];
+      const float r2 = rks[(i0 + 2) * kHeadDim + j], r3 = rks[(i0 + 3) * kHeadDim + j];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float4 qv = *reinterpret_cast<const float4*>(qs + h * kHeadDim + i0);
+        acc[h] = fmaf(qv.w, r3, fmaf(qv.z, r2, fmaf(qv.y, r1, fmaf(qv.x, r0, acc[h]))));
+      }
     }
+#pragma unroll
+    for (int h = 0; h < G; ++h) part[(ig * G + h) * kHeadDim + j] = acc[h];
   }
   __syncthreads();
   for (int idx = tid; idx < G * kHeadDim; idx += T) {
@@ -508,58 +528,39 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, float* rks, 
     aux[tid * 4 + 2] = sm * scale;
   }
   __syncthreads();
-}
-
-// Lane's B fragments of the QK MMA: column n = 8nt + gid is head n (hi part)
-// for n < G, head n-G (lo part) for n < 2G, zero otherwise; register r = 0
-// holds channels (32tig + j, 32tig + j + 8), r = 1 (32tig + 16 + j,
-// 32tig + 24 + j), each scaled by sigma 4^-pos(j).
-template <int G>
-__device__ __forceinline__ void query_fragments(const float* qt, const float* aux, int gid, int tig,
-                                                uint32_t (&qb)[Geo<G>::NT][8][2],
-                                                float (&unscale)[Geo<G>::HS],
-                                                float (&qz)[Geo<G>::HS]) {
-  constexpr int NT = Geo<G>::NT, HS = Geo<G>::HS;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int idx = tid; idx < 32 * NT * 16; idx += T) {
+    const int ln = idx / (NT * 16), rem = idx % (NT * 16);
+    const int nt = rem / 16, j = (rem / 2) % 8, rr = rem % 2;
+    const int gid = ln >> 2, tig = ln & 3;
     const int col = 8 * nt + gid;
-    const bool live = col < 2 * G;
-    const int h = col < G ? col : (live ? col - G : 0);
-    const bool lo = col >= G;
-    const float sg = aux[h * 4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float f = sg * ldexpf(1.f, -2 * code_pos(j));
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int c0 = 32 * tig + 16 * rr + j;
-        float v0 = qt[h * kHeadDim + c0] * f, v1 = qt[h * kHeadDim + c0 + 8] * f;
-        if (lo) {
-          v0 = split_lo(v0);
-          v1 = split_lo(v1);
-        }
-        qb[nt][j][rr] = live ? pack_half2(v0, v1) : 0u;
+    uint32_t v = 0u;
+    if (col < 2 * G) {
+      const int h = col < G ? col : col - G;
+      const float f = aux[h * 4] * __int_as_float((127 - 2 * code_pos(j)) << 23);   // sigma 4^-pos(j)
+      const int c0 = 32 * tig + 16 * rr + j;
+      float v0 = qt[h * kHeadDim + c0] * f, v1 = qt[h * kHeadDim + c0 + 8] * f;
+      if (col >= G) {
+        v0 = split_lo(v0);
+        v1 = split_lo(v1);
       }
+      v = pack_half2(v0, v1);
     }
+    frag[idx] = v;
   }
-#pragma unroll
-  for (int hs = 0; hs < HS; ++hs) {
-    const int h = slot_head<G>(tig, hs);
-    unscale[hs] = aux[h * 4 + 1];
-    qz[hs] = aux[h * 4 + 2];
-  }
+  __syncthreads();
 }
 
 // Page ids of a warp's pages, 32 at a time, one per lane (warp-collective).
+// `limit` bounds the page index (loads may run ahead of the history length).
 struct PidWindow {
   int base = -1, v = -1;
-  __device__ __forceinline__ int get(int k, const int32_t* ptab, int first, int stride, int count,
+  __device__ __forceinline__ int get(int k, const int32_t* ptab, int first, int stride, int limit,
                                      int lane) {
     const int b0 = k & ~31;
     if (b0 != base) {
       base = b0;
-      const int kk = b0 + lane;
-      v = kk < count ? __ldg(ptab + first + kk * stride) : -1;
+      const int pi = first + (b0 + lane) * stride;
+      v = pi < limit ? __ldg(ptab + pi) : -1;
     }
     return __shfl_sync(kFull, v, k & 31);
   }
@@ -570,10 +571,11 @@ struct PidWindow {
 template <int G>
 __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   constexpr int NT = Geo<G>::NT, HS = Geo<G>::HS, NTQ = Geo<G>::NTQ, W = Geo<G>::W, T = Geo<G>::T;
+  constexpr int kStages = Geo<G>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stage = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<G>::kStageBytes);
-  uint64_t* rbar = bars + W * kStages;
+  uint64_t* rbar = bars + W * kStages;       // R_K, then (last CTA) R_V
   uint8_t* uni = smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes;
   float* st_hist = reinterpret_cast<float*>(uni);
   float* st_bf16 = st_hist + W * G * kPartStride;
@@ -586,9 +588,35 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   const int n_splits = p.n_splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
+  const int pbeg = split * p.pages_per_split;
 
-  // ---------------- INT2 page range of this CTA and warp
+  // ---------------- R_K -> shared memory first: nothing it depends on
+  if (tid == 0 && pbeg < p.max_pages) {
+    mbar_init(rbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(rbar, uint32_t(Geo<G>::kRotBytes));
+    const float* rk = p.r_k + int64_t(hkv) * kHeadDim * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      bulk_copy_g2s(rks + c * (kHeadDim * kHeadDim / 4), rk + c * (kHeadDim * kHeadDim / 4),
+                    uint32_t(Geo<G>::kRotBytes / 4), rbar);
+  }
+
+  // ---------------- the query rows -> shared memory (used by the prologue)
+  if (pbeg < p.max_pages) {
+    const uint16_t* qg = p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim;
+    for (int i = tid; i < G * kHeadDim; i += T)
+      qscratch[QScratch<G>::kQs + i] = __uint_as_float(uint32_t(qg[i]) << 16);
+  }
+
+  // ---------------- INT2 page range of this CTA and warp (page ids are
+  // fetched together with the history length)
+  const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
+  const int first = pbeg + warp;
+  const int spec_end = min(pbeg + p.pages_per_split, p.max_pages);
+  PidWindow issue_ids, comp_ids;
   int hist = p.hist_len[b];
+  issue_ids.get(0, ptab, first, W, spec_end, lane);
   if (hist < 0 || hist > p.max_pages * kPage) {
     if (tid == 0) flag(p.dev_status, 0x2);
     hist = max(0, min(hist, p.max_pages * kPage));
@@ -596,13 +624,10 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   const int n_pg = (hist + kPage - 1) / kPage;
   if (n_pg > n_splits * p.pages_per_split && split == 0 && tid == 0)
     flag(p.dev_status, 0x2);  // longer than the host bound max_hist: tail not read
-  const int pbeg = split * p.pages_per_split;
   const int pend = min(pbeg + p.pages_per_split, n_pg);
-  const int first = pbeg + warp;
   const int count = pend > first ? (pend - first + W - 1) / W : 0;
   uint8_t* ring = stage + size_t(warp) * kStages * kBlockBytes;
   uint64_t* bar = bars + warp * kStages;
-  const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
   const uint8_t* pool = p.pages + int64_t(hkv) * kBlockBytes;
   const int64_t page_stride = int64_t(p.n_kv) * kBlockBytes;
 
@@ -611,9 +636,8 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     fence_mbar_init();
   }
   __syncwarp();
-  PidWindow issue_ids, comp_ids;
   auto issue = [&](int k) {  // warp-collective; lane 0 starts the copy
-    const int pid = issue_ids.get(k, ptab, first, W, count, lane);
+    const int pid = issue_ids.get(k, ptab, first, W, spec_end, lane);
     if (lane == 0) {
       const int s = k % kStages;
       if (pid < 0 || pid >= p.n_pages) {
@@ -628,15 +652,52 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   };
   for (int k = 0; k < min(count, kStages); ++k) issue(k);
 
-  // ---------------- q~ (only CTAs that own pages need it)
+  // ---------------- q~ and the lane's QK fragments
   uint32_t qb[NT][8][2];
   float unscale[HS], qz[HS];
   const bool any_pages = pend > pbeg;
   if (any_pages) {
     rotate_query<G>(p, b, hkv, rks, rbar, qscratch);
-    query_fragments<G>(qscratch + 5 * G * kHeadDim, qscratch + 6 * G * kHeadDim, gid, tig, qb, unscale, qz);
+    using S = QScratch<G>;
+    const uint4* fr = reinterpret_cast<const uint4*>(qscratch + S::kFrag) + lane * NT * 4;
+#pragma unroll
+    for (int i = 0; i < NT * 4; ++i) {
+      const uint4 v = fr[i];
+      const int e = 4 * i;
+      qb[e / 16][(e % 16) / 2][0] = v.x;
+      qb[e / 16][(e % 16) / 2][1] = v.y;
+      qb[(e + 2) / 16][((e + 2) % 16) / 2][0] = v.z;
+      qb[(e + 2) / 16][((e + 2) % 16) / 2][1] = v.w;
+    }
+#pragma unroll
+    for (int hs = 0; hs < HS; ++hs) {
+      const int h = slot_head<G>(tig, hs);
+      unscale[hs] = qscratch[S::kAux + h * 4 + 1];
+      qz[hs] = qscratch[S::kAux + h * 4 + 2];
+    }
+  } else if (tid == 0 && pbeg < p.max_pages) {
+    // R_K was requested: let it land before this region is reused
+    if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs)) flag(p.dev_status, 0x4);
   }
-  __syncthreads();   // prologue reads done before warp states overwrite the region
+  __syncthreads();   // prologue reads of R_K and the scratch are done
+
+  // R_V -> shared memory (replacing R_K) for this CTA's output rotation
+  float* rvs = rks;
+  uint64_t* vbar = rbar + 1;
+  if (tid == 0) {
+    fence_proxy_async_smem();
+    mbar_init(vbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(vbar, uint32_t(Geo<G>::kRotBytes));
+    const float* rv = p.r_v + int64_t(hkv) * kHeadDim * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      bulk_copy_g2s(rvs + c * (kHeadDim * kHeadDim / 4), rv + c * (kHeadDim * kHeadDim / 4),
+                    uint32_t(Geo<G>::kRotBytes / 4), vbar);
+  }
+  // each warp's states go into its own ring slice once its pages are done
+  float* my_state = reinterpret_cast<float*>(ring);
+  constexpr int kStateFloats = G * kPartStride;
 
   // ---------------- INT2 pages
   {
@@ -645,7 +706,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     bool timed_out = false;
     int k = 0;
     for (; k < count; ++k) {
-      const int pid = comp_ids.get(k, ptab, first, W, count, lane);
+      const int pid = comp_ids.get(k, ptab, first, W, spec_end, lane);
       const bool valid = pid >= 0 && pid < p.n_pages;
       const int s = k % kStages;
       if (!mbar_wait_bounded(bar + s, (k / kStages) & 1, kWaitLimitNs)) {
@@ -670,7 +731,8 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
       for (int kk = k; kk < min(count, k + kStages); ++kk)
         mbar_wait_bounded(bar + kk % kStages, (kk / kStages) & 1, kWaitLimitNs);
     }
-    store_warp_state<G, true>(st, st_hist + warp * G * kPartStride, gid, tig, p.pv_unscale);
+    __syncwarp();
+    store_warp_state<G, true>(st, my_state, gid, tig, p.pv_unscale);
   }
 
   // ---------------- BF16 sink / recent tokens owned by this CTA
@@ -728,173 +790,146 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
         bf16_page<G>(krow, vrow, kok, vok, gid, tig, qf, st);
       }
     }
-    store_warp_state<G, false>(st, st_bf16 + warp * G * kPartStride, gid, tig, 1.f);
+    store_warp_state<G, false>(st, my_state + kStateFloats, gid, tig, 1.f);
   }
   __syncthreads();
 
-  // ---------------- CTA merge of the warps -> one partial per head and type
+  // ---------------- CTA merge of the warps -> one partial per head and type;
+  // the history partial is rotated back with R_V here, so every partial is
+  // in the original basis
+  float* cw = qscratch;                       // [2][G][W] warp weights
+  float* cml = cw + 2 * G * W;                // [2][G][2] (m, l)
+  float* os = cml + 4 * G;                    // [G][128] merged history output (rotated basis)
+  const int slice = kStages * kBlockBytes / 4;   // floats between two warps' states
+  const float* states = reinterpret_cast<const float*>(stage);
+  if (tid < 2 * G) {
+    const int type = tid / G, h = tid % G;
+    const float* src = states + type * kStateFloats + h * kPartStride;
+    float mx = -INFINITY;
+    for (int w = 0; w < W; ++w)
+      if (src[w * slice + 1] > 0.f) mx = fmaxf(mx, src[w * slice]);
+    float lsum = 0.f;
+    for (int w = 0; w < W; ++w) {
+      const float l = src[w * slice + 1];
+      const float f = l > 0.f ? exp2f(src[w * slice] - mx) : 0.f;
+      cw[tid * W + w] = f;
+      lsum = fmaf(l, f, lsum);
+    }
+    cml[tid * 2] = mx;
+    cml[tid * 2 + 1] = lsum;
+  }
+  __syncthreads();
   float* part = p.partials + (int64_t(pair) * n_splits + split) * 2 * G * kPartStride;
   for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
-    const int type = idx / (G * kHeadDim), h = (idx / kHeadDim) % G, c = idx % kHeadDim;
-    const float* src = type ? st_bf16 : st_hist;
-    float mx = -INFINITY;
+    const int th = idx / kHeadDim, c = idx % kHeadDim;       // th = type * G + h
+    const float* src = states + (th / G) * kStateFloats + (th % G) * kPartStride + 4 + c;
+    float o = 0.f;
 #pragma unroll 4
-    for (int w = 0; w < W; ++w) {
-      const float* s = src + (w * G + h) * kPartStride;
-      if (s[1] > 0.f) mx = fmaxf(mx, s[0]);
+    for (int w = 0; w < W; ++w) o = fmaf(src[w * slice], cw[th * W + w], o);
+    if (th < G) {
+      os[idx] = o;
+    } else {
+      part[th * kPartStride + 4 + c] = o;
     }
-    float lsum = 0.f, o = 0.f;
-#pragma unroll 4
-    for (int w = 0; w < W; ++w) {
-      const float* s = src + (w * G + h) * kPartStride;
-      if (s[1] > 0.f) {
-        const float f = exp2f(s[0] - mx);
-        lsum = fmaf(s[1], f, lsum);
-        o = fmaf(s[4 + c], f, o);
-      }
-    }
-    float* dst = part + (type * G + h) * kPartStride;
-    dst[4 + c] = o;
     if (c == 0) {
-      dst[0] = mx;
-      dst[1] = lsum;
+      part[th * kPartStride + 0] = cml[th * 2];
+      part[th * kPartStride + 1] = cml[th * 2 + 1];
+    }
+  }
+  __syncthreads();
+  if (!mbar_wait_bounded(vbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
+  // history partial back in the original basis: o[c] = sum_j o~[j] R_V[c][j];
+  // thread (row c, quarter qq), chunk order rotated by the lane so the 32
+  // lanes of a load hit all 32 banks
+  for (int task = tid; task < 4 * kHeadDim; task += T) {
+    const int c = task >> 2, qq = task & 3;
+    const int rot = lane & 7;
+    const float* rrow = rvs + c * kHeadDim + 32 * qq;
+    float4 r[8];
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) r[k4] = reinterpret_cast<const float4*>(rrow)[(k4 + rot) & 7];
+#pragma unroll 1
+    for (int h = 0; h < G; ++h) {
+      const float4* o = reinterpret_cast<const float4*>(os + h * kHeadDim + 32 * qq);
+      float d = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < 8; ++k4) {
+        const float4 ov = o[(k4 + rot) & 7];
+        d = fmaf(ov.x, r[k4].x, fmaf(ov.y, r[k4].y, fmaf(ov.z, r[k4].z, fmaf(ov.w, r[k4].w, d))));
+      }
+      d += __shfl_xor_sync(kFull, d, 1);
+      d += __shfl_xor_sync(kFull, d, 2);
+      if (qq == 0) part[h * kPartStride + 4 + c] = d;
     }
   }
 
   // ---------------- ticket: the last CTA of this (request, KV head) merges
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
+    fence_acq_rel_gpu();
     const unsigned t = atomicAdd(p.counters + pair, 1u);
     *s_last = (t == unsigned(n_splits - 1)) ? 1 : 0;
   }
   __syncthreads();
   if (!*s_last) return;
-  __threadfence();
-
-  // R_V rows for the output rotation, fetched now so their latency overlaps
-  // the partial loads: thread -> (row c, quarter qq of the row)
-  constexpr int kRowSets = (4 * kHeadDim + T - 1) / T;
-  float4 rv[kRowSets][8];
-#pragma unroll
-  for (int rs = 0; rs < kRowSets; ++rs) {
-    const int task = tid + rs * T;
-    const int c = task >> 2, qq = task & 3;
-    if (c < kHeadDim) {
-      const float* row = p.r_v + (int64_t(hkv) * kHeadDim + c) * kHeadDim + 32 * qq;
-#pragma unroll
-      for (int k4 = 0; k4 < 8; ++k4) rv[rs][k4] = ldg_keep4(row + 4 * k4);
-    }
-  }
+  fence_acq_rel_gpu();
 
   const float* pp = p.partials + int64_t(pair) * n_splits * 2 * G * kPartStride;
-  const int NP = n_splits * 2 * G;           // partial records of this pair
-  float* ms = reinterpret_cast<float*>(stage);
-  float* ls = ms + NP;
-  float* wt = ls + NP;
-  constexpr int SG = 4;
-  float* acc = wt + NP;                      // [2][SG][G][128]
-  float* oh = acc + 2 * SG * G * kHeadDim;   // [2][G][128]
-  float* hm = oh + 2 * G * kHeadDim;         // [G][2]: history factor, 1 / L
-  for (int i = tid; i < NP; i += T) {
-    ms[i] = __ldcg(pp + int64_t(i) * kPartStride);
-    ls[i] = __ldcg(pp + int64_t(i) * kPartStride + 1);
+  const int NP = 2 * n_splits;                        // partials per head
+  float* ml = reinterpret_cast<float*>(stage);        // [G][2] (max, 1 / L)
+  float* wts = ml + 2 * G;                            // [G][2 * kMaxSplits] weights
+  float* oh = wts + G * 2 * kMaxSplits;               // [2][G][128] half sums
+  // weights per head over its 2 n_splits partials (split-major, type-minor)
+  for (int h = warp; h < G; h += W) {
+    float mx = -INFINITY;
+    for (int i = lane; i < NP; i += 32) {
+      const float* r = pp + int64_t(i * G + h) * kPartStride;
+      if (__ldcg(r + 1) > 0.f) mx = fmaxf(mx, __ldcg(r));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    float lsum = 0.f;
+    for (int i = lane; i < NP; i += 32) {
+      const float* r = pp + int64_t(i * G + h) * kPartStride;
+      const float l = __ldcg(r + 1);
+      const float f = l > 0.f ? exp2f(__ldcg(r) - mx) : 0.f;
+      wts[h * 2 * kMaxSplits + i] = f;
+      lsum = fmaf(l, f, lsum);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+    if (lane == 0) ml[h * 2 + 1] = lsum > 0.f ? 1.f / lsum : 0.f;
   }
   __syncthreads();
-  // weights: history partials relative to their own max (they are rotated
-  // after the sum); BF16 partials relative to the final max
-  if (warp < G) {
-    const int h = warp;
-    float mh = -INFINITY;
-    for (int s = lane; s < n_splits; s += 32) {
-      const int i = (s * 2 + 0) * G + h;
-      if (ls[i] > 0.f) mh = fmaxf(mh, ms[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mh = fmaxf(mh, __shfl_xor_sync(kFull, mh, o));
-    float lh = 0.f;
-    for (int s = lane; s < n_splits; s += 32) {
-      const int i = (s * 2 + 0) * G + h;
-      const float w = ls[i] > 0.f ? exp2f(ms[i] - mh) : 0.f;
-      wt[i] = w;
-      lh = fmaf(ls[i], w, lh);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lh += __shfl_xor_sync(kFull, lh, o);
-    float m = lh > 0.f ? mh : -INFINITY;
-    for (int s = lane; s < n_splits; s += 32) {
-      const int i = (s * 2 + 1) * G + h;
-      if (ls[i] > 0.f) m = fmaxf(m, ms[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    float lt = 0.f;
-    for (int s = lane; s < n_splits; s += 32) {
-      const int i = (s * 2 + 1) * G + h;
-      const float w = ls[i] > 0.f ? exp2f(ms[i] - m) : 0.f;
-      wt[i] = w;
-      lt = fmaf(ls[i], w, lt);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(kFull, lt, o);
-    if (lane == 0) {
-      const float fh = lh > 0.f ? exp2f(mh - m) : 0.f;
-      const float l = fmaf(lh, fh, lt);
-      hm[h * 2 + 0] = fh;
-      hm[h * 2 + 1] = l > 0.f ? 1.f / l : 0.f;
-    }
-  }
-  __syncthreads();
-  // weighted sums of the partial outputs: task (type, h, c4, sg) sums splits
-  // s = sg, sg + SG, ... in order (float4 loads, all independent)
-  for (int task = tid; task < 2 * G * 32 * SG; task += T) {
-    const int sg = task % SG, c4 = (task / SG) % 32, h = (task / (SG * 32)) % G, type = task / (SG * 32 * G);
+  // weighted sums: one warp per (half, head), lanes over channels (float4),
+  // loads of a batch issued together
+  for (int task = warp; task < 2 * G; task += W) {
+    const int half = task / G, h = task % G;
+    const int i0 = half ? NP / 2 : 0, i1 = half ? NP : NP / 2;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = sg; s < n_splits; s += SG) {
-      const int i = (s * 2 + type) * G + h;
-      const float w = wt[i];
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i) * kPartStride + 4) + c4);
-      a.x = fmaf(w, o.x, a.x);
-      a.y = fmaf(w, o.y, a.y);
-      a.z = fmaf(w, o.z, a.z);
-      a.w = fmaf(w, o.w, a.w);
-    }
-    reinterpret_cast<float4*>(acc + ((type * SG + sg) * G + h) * kHeadDim)[c4] = a;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
-    const int type = idx / (G * kHeadDim), hc = idx % (G * kHeadDim);
-    float v = 0.f;
+    for (int ib = i0; ib < i1; ib += 8) {
+      float4 v[8];
 #pragma unroll
-    for (int sg = 0; sg < SG; ++sg) v += acc[(type * SG + sg) * G * kHeadDim + hc];
-    oh[idx] = v;
-  }
-  __syncthreads();
-  // out[c] = (sum_j o~[j] R_V[c][j] * f_hist + o_bf16[c]) / L
+      for (int u = 0; u < 8; ++u)
+        if (ib + u < i1)
+          v[u] = __ldcg(reinterpret_cast<const float4*>(pp + int64_t((ib + u) * G + h) * kPartStride + 4) + lane);
 #pragma unroll
-  for (int rs = 0; rs < kRowSets; ++rs) {
-    const int task = tid + rs * T;
-    const int c = task >> 2, qq = task & 3;
-    const bool live = c < kHeadDim;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float d = 0.f;
-      if (live) {
-        const float4* o = reinterpret_cast<const float4*>(oh + h * kHeadDim + 32 * qq);
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 ov = o[k4];
-          d = fmaf(ov.x, rv[rs][k4].x, fmaf(ov.y, rv[rs][k4].y, fmaf(ov.z, rv[rs][k4].z, fmaf(ov.w, rv[rs][k4].w, d))));
+      for (int u = 0; u < 8; ++u)
+        if (ib + u < i1) {
+          const float f = wts[h * 2 * kMaxSplits + ib + u];
+          a.x = fmaf(f, v[u].x, a.x);
+          a.y = fmaf(f, v[u].y, a.y);
+          a.z = fmaf(f, v[u].z, a.z);
+          a.w = fmaf(f, v[u].w, a.w);
         }
-      }
-      d += __shfl_xor_sync(kFull, d, 1);
-      d += __shfl_xor_sync(kFull, d, 2);
-      if (live && qq == 0) {
-        const float v = fmaf(d, hm[h * 2], oh[G * kHeadDim + h * kHeadDim + c]) * hm[h * 2 + 1];
-        p.out[(int64_t(b) * p.n_kv * G + int64_t(hkv) * G + h) * kHeadDim + c] = v;
-      }
     }
+    reinterpret_cast<float4*>(oh + (half * G + h) * kHeadDim)[lane] = a;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kHeadDim; idx += T) {
+    const int h = idx / kHeadDim;
+    p.out[(int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim + idx] =
+        (oh[idx] + oh[G * kHeadDim + idx]) * ml[h * 2 + 1];
   }
   if (tid == 0) p.counters[pair] = 0u;   // ready for the next call
 }

@@ -41,25 +41,33 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   }
   __syncthreads();
 
-  // the item's source row, read before anything is written back into it
+  // indices first, then the source row and the destination page (two
+  // levels of independent loads, overlapping the R transfer)
   bool live = item < p.n;
   int64_t row = 0;
+  int bq = 0, pos = 0;
   if (live) {
     row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
-    if (row < 0 || row >= p.src_rows) {
+    bq = p.dst_req[item];
+    pos = p.dst_pos[item];
+    if (row < 0 || row >= p.src_rows || bq < 0 || bq >= p.batch || pos < 0 || pos / kPage >= p.max_pages) {
       if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x2);
       live = false;
     }
   }
   uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
   float xv[4] = {0.f, 0.f, 0.f, 0.f};
+  int64_t page = -1;
   if (live) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+    page = p.page_table[int64_t(bq) * p.max_pages + pos / kPage];
     xv[0] = bf16_lo(raw.x);
     xv[1] = bf16_hi(raw.x);
     xv[2] = bf16_lo(raw.y);
     xv[3] = bf16_hi(raw.y);
   }
+  // the source row may be overwritten by the new token only after every
+  // lane has read it
   __syncwarp();
   const uint16_t* fresh = which ? p.new_v : p.new_k;
   if (live && fresh) {
@@ -111,13 +119,6 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     byte |= uint32_t(code) << (2 * c);
   }
 
-  const int b = p.dst_req[item];
-  const int pos = p.dst_pos[item];
-  if (b < 0 || b >= p.batch || pos < 0 || pos / kPage >= p.max_pages) {
-    if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x2);
-    return;
-  }
-  const int64_t page = p.page_table[int64_t(b) * p.max_pages + pos / kPage];
   if (page < 0 || page >= p.n_pages) {
     if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
     return;
