@@ -380,10 +380,12 @@ def run_gpu(args):
     def decode(i):
         B.oscar_decode_attention(descs[i], q, out, ws, ws_bytes)
 
-    # CUDA graphs of each copy's two calls (host launch overhead out of the step)
+    # CUDA graphs: one per layer copy holding a whole step (demotion +
+    # decode), and two "kernel" graphs holding every copy's decode (resp.
+    # demotion) back to back, for the per-kernel durations
     stream = torch.cuda.Stream()
-    graphs = []
     use_graphs = True
+    g_step, g_decode, g_demote = [], None, None
     try:
         with torch.cuda.stream(stream):
             for i in range(n_copies):
@@ -391,68 +393,77 @@ def run_gpu(args):
                 decode(i)
             torch.cuda.synchronize()
             for i in range(n_copies):
-                gd, ga = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gd, stream=stream):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
                     demote(i)
-                with torch.cuda.graph(ga, stream=stream):
                     decode(i)
-                graphs.append((gd, ga))
+                g_step.append(g)
+            g_decode, g_demote = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_decode, stream=stream):
+                for i in range(n_copies):
+                    decode(i)
+            with torch.cuda.graph(g_demote, stream=stream):
+                for i in range(n_copies):
+                    demote(i)
     except Exception as exc:  # graph capture unavailable: launch directly
         use_graphs = False
-        graphs = []
         sys.stderr.write("graph capture failed (%s); timing direct launches\n" % exc)
     torch.cuda.synchronize()
 
-    def step(i):
+    def run_step(i):
         if use_graphs:
-            graphs[i][0].replay()
+            g_step[i].replay()
         else:
             demote(i)
-
-    def attend(i):
-        if use_graphs:
-            graphs[i][1].replay()
-        else:
             decode(i)
 
+    def run_all(graph, fn):
+        if use_graphs:
+            graph.replay()
+        else:
+            for i in range(n_copies):
+                fn(i)
+
     K, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = Clocks(local)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     with torch.cuda.stream(stream):
         for k in range(W):
-            step(k % n_copies)
-            attend(k % n_copies)
+            run_step(k % n_copies)
         torch.cuda.synchronize()
         clocks.start()
         t_pre = time.perf_counter()
         pre = 0
         while time.perf_counter() - t_pre < 1.0:      # same load before the timed region, for clock samples
             for _ in range(50):
-                step(pre % n_copies)
-                attend(pre % n_copies)
+                run_step(pre % n_copies)
                 pre += 1
             torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        ev[0].record(stream)
         for k in range(K):
-            i = k % n_copies
-            ev[k][0].record(stream)
-            step(i)
-            ev[k][1].record(stream)
-            attend(i)
-            ev[k][2].record(stream)
+            run_step(k % n_copies)
+        ev[1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-        for k in range(min(K, 200)):
-            step(k % n_copies)
-            attend(k % n_copies)
+        # per-kernel durations: every copy's decode (then demotion) back to
+        # back, repeated so that as many launches run as in the timed steps
+        reps = max(1, K // n_copies)
+        ev[2].record(stream)
+        for _ in range(reps):
+            run_all(g_decode, decode)
+        ev[3].record(stream)
+        for _ in range(reps):
+            run_all(g_demote, demote)
+        ev[4].record(stream)
         torch.cuda.synchronize()
         clk = clocks.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    decode_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
-    demote_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    total_ms = ev[0].elapsed_time(ev[1])
+    decode_ms = ev[2].elapsed_time(ev[3]) / (reps * n_copies)
+    demote_ms = ev[3].elapsed_time(ev[4]) / (reps * n_copies)
     t_step = total_ms / K / 1e3
     if world > 1:
         tt = torch.tensor([t_step], device=dev)
@@ -510,6 +521,8 @@ def run_gpu(args):
                     "h2d_bytes_per_step": q.numel() * 2 + new_k.numel() * 2 + new_v.numel() * 2,
                     "d2h_bytes_per_step": out.numel() * 4},
             "gpu_launches": 2 * K,
+            "kernel_timing": "decode_ms / demote_ms: %d back-to-back launches over the %d layer copies, "
+                             "CUDA events on the launching stream" % (reps * n_copies, n_copies),
             "clocks": clk,
             "device_status": status,
             "host_wall_s": wall,
