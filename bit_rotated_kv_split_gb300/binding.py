@@ -55,6 +55,7 @@ def _load():
                                             P, P, c_int32, P, P, P]),
         "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
                                              ctypes.POINTER(c_size_t), P]),
+        "oscar_decode_attention_static": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -148,3 +149,9 @@ def oscar_decode_attention(desc: LayerDesc, q, out, workspace, workspace_bytes: 
                     else workspace_bytes)
     _check("oscar_decode_attention", lib.oscar_decode_attention(
         ctypes.byref(desc), _ptr(q), _ptr(out), _ptr(workspace), ctypes.byref(size), _stream(stream)))
+
+
+def oscar_decode_attention_static(desc: LayerDesc, q, out, stream=None) -> None:
+    """Decode attention with the library's fixed workspace (no allocation by anyone)."""
+    _check("oscar_decode_attention_static", lib.oscar_decode_attention_static(
+        ctypes.byref(desc), _ptr(q), _ptr(out), _stream(stream)))

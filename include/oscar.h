@@ -218,6 +218,38 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
                                     float* out, void* workspace, size_t* workspace_bytes,
                                     void* stream);
 
+/*
+ * oscar_decode_attention_static - oscar_decode_attention for callers that
+ * cannot allocate device memory.  The paper has no counterpart: this is a
+ * deployment convenience of this library.
+ *
+ *   Some callers have no way to call cudaMalloc or to hand the library a
+ *   workspace: code embedded in a host framework that owns every device
+ *   allocation, or a latency-critical serving loop that forbids allocation
+ *   after start-up.  This entry point computes exactly what
+ *   oscar_decode_attention computes, but its workspace is a fixed array of
+ *   OSCAR_STATIC_WORKSPACE_BYTES inside the library, reserved on every GPU
+ *   that loads the library until the process exits.  It allocates nothing.
+ *
+ *   q, out and the cache are the caller's, as for oscar_decode_attention.
+ *   Returns OSCAR_ERR_WORKSPACE when the problem needs more workspace than
+ *   the fixed array holds (the size oscar_decode_attention reports for a
+ *   NULL workspace must not exceed OSCAR_STATIC_WORKSPACE_BYTES; about 0.65
+ *   MB for one 100k-token request with 8 KV heads and GQA 4).
+ *
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  Each call clears the part of the array that
+ *   must start at zero, on `stream`, then launches.  Every call shares the
+ *   one array and it keeps the last call's contents: calls whose work
+ *   overlaps on the GPU (different streams, or concurrent host threads
+ *   without stream ordering) race on it and must not be issued.
+ */
+#define OSCAR_STATIC_WORKSPACE_BYTES (8u << 20)
+
+oscar_status oscar_decode_attention_static(const oscar_layer_desc* desc, const uint16_t* q,
+                                           float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
