@@ -255,6 +255,27 @@ class Clocks:
                 "samples": len(rows)}
 
 
+def _profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "split_kernel_qwen3-8b-layer-decode-100k.md")
+    try:
+        text = open(prof).read()
+    except OSError:
+        return None
+    h = hashlib.sha256()
+    for f in ("decode.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "bit_rotated_kv_split_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != h.hexdigest():
+        return None
+    return int(m_bytes.group(1))
+
+
 def _roofline_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -513,7 +534,7 @@ def run_gpu(args):
             "decode_ms": decode_ms, "demote_ms": demote_ms,
             "hbm_gbs_decode": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": _profiled_traffic(),
                          "kernel": "split_kernel (oscar_decode_attention, one launch per step)",
                          "algorithmic_bytes": nbytes, "peak_kind": peak_kind + " hbm_gbs"},
             "cpu_baseline": cpu,
