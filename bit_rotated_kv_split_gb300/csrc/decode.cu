@@ -9,32 +9,37 @@
 // as q~ = q . R_K once per query head and one o . R_V^T per head and split,
 // instead of rotating every token.
 //
-// One launch; CTA (split, KV head, request) of 12 warps, one CTA per SM, owns
+// One launch; CTA (split, KV head, request) of 16 warps, one CTA per SM, owns
 // a contiguous range of INT2 pages of one (request, KV head) and a share of
 // its BF16 sink/recent tokens.  The INT2 pages are processed in tiles of 8
 // pages (128 tokens) by a warp-specialised tcgen05 pipeline:
-//   warp 8      producer: 1-D TMA bulk copies of the tile's 8 page blocks into
+//   warp 12     producer: 1-D TMA bulk copies of the tile's 8 page blocks into
 //               a ring of tile slots (mbarrier transaction counts);
-//   warps 0-3   K path, thread = token: unpack the token's 128 K codes into
-//               fp16 and store them in tensor memory (A of QK); after the QK
-//               MMA, read the scores back (one token, all heads per thread),
-//               online softmax, write p s_V (hi | lo fp16) to shared memory
-//               (B of PV);
+//   warps 8-11  K path, thread = token: unpack the token's 128 K codes into
+//               fp16 in tensor memory (A of QK); then lane 0 of warp 8 + j
+//               issues the QK MMAs of K-steps 2j, 2j+1 into accumulator j:
+//               D[token][col] = codes[token][k] . B_qk[k][col];
+//   warps 0-3   softmax, thread = token: sum the 4 accumulators, scores,
+//               online softmax with a running maximum per warp and head,
+//               p s_V (hi | lo fp16) into shared memory (B of PV);
 //   warps 4-7   V path, thread = channel: unpack the channel's codes of the
-//               tile's 128 tokens into fp16 in tensor memory (A of PV);
-//   warp 9      owns tensor memory and issues the MMAs from one lane:
-//               QK: D[token][col] = codes[token][k] . B_qk[k][col]
-//               PV: O[channel][col] += codes^T[channel][token] . P[token][col]
-//               (M = 128, N = 16, K = 16 per instruction, fp32 accumulate in
-//               tensor memory), completion signalled by tcgen05.commit;
-//   warps 10-11 the BF16 sink/recent tokens (mma.sync, bf16), concurrently.
-// The columns of B are the GQA heads' hi parts then lo parts (fp16 hi + lo
-// split of an fp32 value), so each MMA carries about fp32 precision.
-// A 2-bit code c at bit offset 2k of a 16-bit half is read as the fp16
-// subnormal c * 4^k * 2^-24 by one AND; the 4^k factors go into B and 2^-24
-// into the output scale.  The online-softmax maximum is raised lazily (only
-// when a score exceeds it by 2^8), and then the O accumulator in tensor
-// memory is rescaled in place.
+//               tile's 128 tokens into fp16 in tensor memory (A of PV); lane 0
+//               of warp 4 + j issues the PV MMAs of K-steps 2j, 2j+1 (the
+//               tokens of softmax warp j) into output accumulator j:
+//               O_j[channel][col] += codes^T[channel][token] . P[token][col];
+//   warps 14-15 the BF16 sink/recent tokens (mma.sync, bf16), concurrently;
+//   warp 13     owns the tensor-memory allocation.
+// MMAs are M = 128, N = 16, K = 16, fp16 in, fp32 accumulate in tensor
+// memory, completion signalled by tcgen05.commit.  They are issued from 8
+// threads because one thread issues only about one MMA per 50 cycles.  The
+// columns of B are the GQA heads' hi parts then lo parts (fp16 hi + lo split
+// of an fp32 value), so each MMA carries about fp32 precision.  A 2-bit code
+// c at bit offset 2k of a 16-bit half is read as the fp16 subnormal
+// c * 4^k * 2^-24 by one AND; the 4^k factors go into B and 2^-24 into the
+// output scale.  A softmax warp raises its maximum lazily (only when a score
+// exceeds it by 2^8); its output accumulator is then rescaled in place by
+// the V warps before the next PV MMAs.  The 4 accumulators are merged at the
+// end with their warps' maxima.
 //
 // Epilogue: the CTA rotates its history partial back with R_V (staged by TMA
 // during the scan) and writes it and its BF16 partial; the last CTA of the
@@ -56,7 +61,6 @@ namespace oscar {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (p <= 2^8)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSplits = 128;               // bounds the last CTA's merge scratch
@@ -65,14 +69,20 @@ constexpr int kTilePages = 8;
 constexpr int kTileTokens = kTilePages * kPage;           // 128
 constexpr int kTileBytes = kTilePages * kBlockBytes;      // 9216
 constexpr int kSlots = OSCAR_TILE_SLOTS;
-constexpr int kWarps = 12;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kBf16Warp = 10;
+// warp roles
+constexpr int kVWarp0 = 4, kKWarp0 = 8, kProducerWarp = 12, kTmemWarp = 13, kBf16Warp = 14;
 constexpr int kN = 16;                                      // MMA N: hi | lo columns
 constexpr uint32_t kIdesc = idesc_f16_f32(128, kN);
-// tensor-memory columns
-constexpr uint32_t kColAK = 0, kColAV = 128, kColQK = 256, kColPV = 288, kTmemCols = 512;
 constexpr int kBBytes = kN * kTileTokens * 2;               // one B operand tile (K = 128)
+// operand buffering: A_K and D_qk double, A_V triple, P quadruple, so the V
+// warps and the softmax can run ahead of the PV MMAs
+constexpr int kAvBufs = 3, kBpBufs = 4;
+// tensor-memory columns: A_K[2] | A_V[3] | D_qk[2][4 accumulators] | O[4 accumulators]
+constexpr uint32_t kColAK = 0, kColAV = 128, kColQK = kColAV + 64 * kAvBufs, kColPV = kColQK + 128,
+                   kTmemCols = 512;
+static_assert(kColPV + 4 * kN <= kTmemCols, "tensor memory columns");
 
 template <int G>
 struct Geo {
@@ -85,13 +95,14 @@ struct Geo {
   static constexpr size_t kQFloats = 6 * G * kHeadDim + 12 * G;
   static constexpr size_t kUnion = kRotBytes + kQFloats * 4;        // R_K then R_V | scratch
   static constexpr size_t kBf16State = size_t(2) * G * kPartStride * 4;
-  static constexpr int kBars = 2 * kSlots + 2 * 5 + 4;   // full, empty | ak qk bp av pv | x rk rv fin
+  // full, empty | ak qk_done qk_free | av | bp | pv | rs bqk rk rv fin
+  static constexpr int kBars = 2 * kSlots + 3 * 2 + kAvBufs + 2 * kBpBufs + 5;
   static constexpr size_t kBarBytes = (kBars * 8 + 127) / 128 * 128;
-  static constexpr size_t kMiscBytes = 1024;
+  static constexpr size_t kMiscBytes = 2048;
   static constexpr size_t oStage = 0;
   static constexpr size_t oBqk = oStage + kStageBytes;
   static constexpr size_t oBp = oBqk + kBBytes;
-  static constexpr size_t oUni = oBp + 2 * kBBytes;
+  static constexpr size_t oUni = oBp + kBpBufs * kBBytes;
   static constexpr size_t oBf16 = oUni + kUnion;
   static constexpr size_t oBars = (oBf16 + kBf16State + 127) / 128 * 128;
   static constexpr size_t oMisc = oBars + kBarBytes;
@@ -99,8 +110,8 @@ struct Geo {
   static_assert(kStageBytes % 128 == 0 && oBqk % 128 == 0 && oUni % 128 == 0, "TMA / UMMA operands aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   // CTA merge scratch after R_V in the union; last-CTA scratch in the ring
-  static_assert((G * kHeadDim + 4 * G) * 4 <= kQFloats * 4, "CTA merge scratch");
-  static_assert((2 * G + 2 * G * 128 + 2 * G * kHeadDim) * 4 <= kStageBytes, "merge scratch");
+  static_assert((G * kHeadDim + 8 * G) * 4 <= kQFloats * 4, "CTA merge scratch");
+  static_assert((2 * G + 2 * G * kMaxSplits + 2 * G * kHeadDim) * 4 <= kStageBytes, "merge scratch");
 };
 
 // head owned by head slot hs of a lane with column group tig (BF16 mma.sync)
@@ -143,17 +154,50 @@ __device__ __forceinline__ int b_offset(int n, int k) {
   return (k >> 4) * 512 + (n >> 3) * 256 + ((k >> 3) & 1) * 128 + (n & 7) * 16 + (k & 7) * 2;
 }
 
+// The first 2G columns (G = 4: 8, G = 8: 16) of one accumulator, this lane.
+template <int G>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[2 * G]) {
+  if constexpr (G == 4) {
+    tmem_ld8(taddr, r);
+  } else {
+    tmem_ld16(taddr, r);
+  }
+}
+template <int G>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[2 * G]) {
+  if constexpr (G == 4) {
+    tmem_st8(taddr, r);
+  } else {
+    tmem_st16(taddr, r);
+  }
+}
+
+// Unpacks 8 code words (16 codes each) into 64 fp16x2 TMEM columns of this
+// lane: column 8i + j = (code j, code j + 8) of word i, scaled 4^pos(j) 2^-24.
+__device__ __forceinline__ void codes_to_tmem(uint32_t taddr, const uint32_t (&wv)[8]) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t rr[32];
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const uint32_t w = wv[4 * half + ii], wsh = w >> 6;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) rr[8 * ii + j] = code_pair(w, wsh, j);
+    }
+    tmem_st32(taddr + 32u * half, rr);
+  }
+}
+
 // Bounded mbarrier wait that also ends early once another role aborted.
 struct Waiter {
   volatile int* abort_flag;
   int32_t* dev_status;
   __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) {
-    if (*abort_flag) return false;
     if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-      if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
       if (*abort_flag) return false;
+      if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
         flag(dev_status, 0x4);
@@ -363,7 +407,6 @@ __device__ __forceinline__ void store_warp_state(WarpState<G>& st, float* ws, in
     }
   }
 }
-
 // ------------------------------------------------------------------ q~ and the QK operand
 
 // Shared-memory scratch of the prologue, in floats: qs[G][128] | part[4][G][128]
@@ -389,7 +432,7 @@ constexpr uint32_t kPrologueBarrier = 1;
 // aux[h] = (sigma, 2^24 / sigma * log2(e) / sqrt(d), sum(q~) log2(e) / sqrt(d)).
 template <int G>
 __device__ void rotate_query(const float* rks, uint64_t* rbar, float* scratch, uint8_t* bqk,
-                             int32_t* dev_status) {
+                             uint64_t* bqk_ready, int32_t* dev_status) {
   constexpr int T = kPrologueThreads;
   using S = QScratch<G>;
   const float* qs = scratch + S::kQs;
@@ -467,6 +510,7 @@ __device__ void rotate_query(const float* rks, uint64_t* rbar, float* scratch, u
     *reinterpret_cast<uint32_t*>(bqk + b_offset(n, 2 * col)) = v;
   }
   fence_proxy_async_smem();
+  mbar_arrive(bqk_ready);   // the QK issuers wait for this
   named_barrier(kPrologueBarrier, T);
 }
 
@@ -488,11 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
   uint64_t* empty = full + kSlots;
   uint64_t* ak_full = empty + kSlots;
   uint64_t* qk_done = ak_full + 2;
-  uint64_t* bp_full = qk_done + 2;
-  uint64_t* av_full = bp_full + 2;
-  uint64_t* pv_done = av_full + 2;
-  uint64_t* xbar = pv_done + 2;
-  uint64_t* rbar = xbar + 1;
+  uint64_t* qk_free = qk_done + 2;
+  uint64_t* av_full = qk_free + 2;                // [kAvBufs]
+  uint64_t* bp_full = av_full + kAvBufs;          // [kBpBufs]
+  uint64_t* pv_done = bp_full + kBpBufs;          // [kBpBufs], PV of tile u -> u % kBpBufs
+  uint64_t* rsbar = pv_done + kBpBufs;
+  uint64_t* bqk_ready = rsbar + 1;
+  uint64_t* rbar = bqk_ready + 1;
   uint64_t* vbar = rbar + 1;
   uint64_t* fin = vbar + 1;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Gm::oMisc);
@@ -501,10 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
   int* s_last = reinterpret_cast<int*>(misc + 2);
   constexpr int kMaskWords = (kSlots + 3) / 4 * 4;
   uint32_t* tile_mask = misc + 4;                                    // [kSlots]
-  float* xchg = reinterpret_cast<float*>(misc + 4 + kMaskWords);     // [2][4 + 4G], 16-byte aligned
-  float* red_lz = xchg + 2 * (4 + 4 * G);                            // [4][2G] (l | zeta)
-  float* s_m = red_lz + 8 * G;                                       // [G]
-  static_assert(4 + kMaskWords + 2 * (4 + 4 * G) + 8 * G + G <= int(Gm::kMiscBytes / 4), "misc fits");
+  int* rs_flag = reinterpret_cast<int*>(misc + 4 + kMaskWords);      // [kBpBufs][4], 16-byte aligned
+  float* rs_f = reinterpret_cast<float*>(rs_flag + 4 * kBpBufs);     // [kBpBufs][4][G] rescale factors
+  float* st_m = rs_f + 4 * kBpBufs * G;                              // [4][G] softmax warps' maxima
+  float* st_l = st_m + 4 * G;                                        // [4][G] sums of p
+  float* st_z = st_l + 4 * G;                                        // [4][G] sums of p z_V
+  static_assert(4 + kMaskWords + 4 * kBpBufs + (4 * kBpBufs + 12) * G <= int(Gm::kMiscBytes / 4), "misc fits");
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int pair = b * p.n_kv + hkv;
@@ -517,19 +565,23 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 256);
+      mbar_init(empty + s, 384);                 // softmax, V and K warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(ak_full + i, 128);
-      mbar_init(qk_done + i, 1);
-      mbar_init(bp_full + i, 128);
-      mbar_init(av_full + i, 128);
-      mbar_init(pv_done + i, 1);
+      mbar_init(qk_done + i, 4);                 // one commit per QK issuer
+      mbar_init(qk_free + i, 128);
     }
-    mbar_init(xbar, 128);
+    for (int i = 0; i < kAvBufs; ++i) mbar_init(av_full + i, 128);
+    for (int i = 0; i < kBpBufs; ++i) {
+      mbar_init(bp_full + i, 128);
+      mbar_init(pv_done + i, 4);                 // one commit per PV issuer
+    }
+    mbar_init(rsbar, 128);
+    mbar_init(bqk_ready, kPrologueThreads);
     mbar_init(rbar, 1);
     mbar_init(vbar, 1);
-    mbar_init(fin, 1);
+    mbar_init(fin, 8);                           // every MMA issuer, once
     *abort_flag = 0;
     fence_mbar_init();
     if (pbeg < p.max_pages) {
@@ -541,13 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
                       uint32_t(Gm::kRotBytes / 4), rbar);
     }
   }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kTmemWarp) tmem_alloc(tmem_slot, kTmemCols);
   if (warp < 8 && pbeg < p.max_pages) {
     const uint16_t* qg = p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim;
     for (int i = tid; i < G * kHeadDim; i += kPrologueThreads)
       qscratch[QScratch<G>::kQs + i] = __uint_as_float(uint32_t(qg[i]) << 16);
     // P operand buffers: rows >= 2G stay zero
-    for (int i = tid; i < 2 * kBBytes / 16; i += kPrologueThreads)
+    for (int i = tid; i < kBpBufs * kBBytes / 16; i += kPrologueThreads)
       reinterpret_cast<uint4*>(bp)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -572,12 +624,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   Waiter wt{abort_flag, p.dev_status};
+  bool pv_final = false;   // V warps: the last PV products have landed
 
   if (warp < 8) {
     // ================= prologue: q~ and the QK operand (warps 0-7)
     float uns[G], qzh[G];
     if (n_tiles > 0) {
-      rotate_query<G>(rks, rbar, qscratch, bqk, p.dev_status);
+      rotate_query<G>(rks, rbar, qscratch, bqk, bqk_ready, p.dev_status);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         uns[h] = qscratch[QScratch<G>::kAux + h * 4 + 1];
@@ -599,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
     }
 
     if (warp < 4) {
-      // ================= K path and softmax: thread r = token r of a tile
+      // ================= softmax: thread r = token r of a tile
       const int r = tid;
       const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
       const int pg_in_tile = r >> 4, slot = r & 15;
@@ -612,42 +665,30 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
         l[h] = 0.f;
         z[h] = 0.f;
       }
-      uint32_t ksz_n = 0, vsz_n = 0, mask_n = 0;   // of the tile converted last
-      // K codes of tile t -> A_K[t % 2]; keeps the tile's scales for its softmax
-      auto convert = [&](int t) -> bool {
+      for (int t = 0; t < n_tiles; ++t) {
         const int s = t % kSlots;
-        if (!wt.wait(full + s, (t / kSlots) & 1)) return false;
+        if (!wt.wait(full + s, (t / kSlots) & 1)) break;
         const uint8_t* pg = stage + s * kTileBytes + pg_in_tile * kBlockBytes;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(pg + 32 * slot);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(pg + 32 * slot + 16);
-        ksz_n = *reinterpret_cast<const uint32_t*>(pg + 512 + 4 * slot);
-        vsz_n = *reinterpret_cast<const uint32_t*>(pg + kHalfBytes + 512 + 4 * slot);
-        mask_n = tile_mask[s];
-        const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint32_t col0 = lane_addr + kColAK + 64u * uint32_t(t & 1);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t rr[32];
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            const uint32_t w = wv[4 * half + wi], wsh = w >> 6;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) rr[8 * wi + j] = code_pair(w, wsh, j);
-          }
-          tmem_st32(col0 + 32u * half, rr);
-        }
-        tc_wait_st();
+        const uint32_t ksz = *reinterpret_cast<const uint32_t*>(pg + 512 + 4 * slot);
+        const uint32_t vsz = *reinterpret_cast<const uint32_t*>(pg + kHalfBytes + 512 + 4 * slot);
+        const uint32_t mask = tile_mask[s];
         mbar_arrive(empty + s);
-        tc_fence_before();
-        mbar_arrive(ak_full + (t & 1));
-        return true;
-      };
-      auto softmax = [&](int t, uint32_t ksz, uint32_t vsz, uint32_t mask) -> bool {
-        if (!wt.wait(qk_done + (t & 1), (t >> 1) & 1)) return false;
+        if (!wt.wait(qk_done + (t & 1), (t >> 1) & 1)) break;
         tc_fence_after();
-        uint32_t dr[16];
-        tmem_ld16(lane_addr + kColQK + 16u * uint32_t(t & 1), dr);
-        tc_wait_ld();
+        float dq[2 * G];
+        {
+          uint32_t dr[4][2 * G];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            tmem_ld_cols<G>(lane_addr + kColQK + uint32_t(64 * (t & 1) + kN * ch), dr[ch]);
+          tc_wait_ld();
+#pragma unroll
+          for (int n = 0; n < 2 * G; ++n)
+            dq[n] = (__uint_as_float(dr[0][n]) + __uint_as_float(dr[1][n])) +
+                    (__uint_as_float(dr[2][n]) + __uint_as_float(dr[3][n]));
+        }
+        tc_fence_before();
+        mbar_arrive(qk_free + (t & 1));
         const int pi = pbeg + kTilePages * t + pg_in_tile;
         const bool valid = ((mask >> pg_in_tile) & 1u) && pi * kPage + slot < hist;
         const float2 kz = half2_to_float2(ksz), vz = half2_to_float2(vsz);
@@ -655,61 +696,40 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
         bool need = false;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float full_d = __uint_as_float(dr[h]) + __uint_as_float(dr[G + h]);
-          sc[h] = valid ? fmaf(kz.x * full_d, uns[h], kz.y * qzh[h]) : -INFINITY;
+          sc[h] = valid ? fmaf(kz.x * (dq[h] + dq[G + h]), uns[h], kz.y * qzh[h]) : -INFINITY;
           need |= sc[h] > m[h] + kRescaleLog2;
         }
-        // lazy maximum: the 4 warps agree through one exchange per tile
-        float* xv = xchg + (t & 1) * (4 + 4 * G);
-        const bool vote = __any_sync(kFull, need);
-        if (lane == 0) reinterpret_cast<int*>(xv)[warp] = vote ? 1 : 0;
-        if (vote) {
+        // lazy maximum of this warp; an accumulator that already holds
+        // products of an older maximum is rescaled by the V warps
+        float f[G];
+        bool rescale = false;
+#pragma unroll
+        for (int h = 0; h < G; ++h) f[h] = 1.f;
+        if (__any_sync(kFull, need)) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             float wm = sc[h];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, o));
-            if (lane == h) xv[4 + warp * G + h] = wm;
-          }
-        }
-        mbar_arrive(xbar);
-        if (!wt.wait(xbar, t & 1)) return false;
-        const int4 votes = *reinterpret_cast<const int4*>(xv);
-        if (votes.x | votes.y | votes.z | votes.w) {
-          float f[G];
-          bool any_f = false;
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float nm = m[h];
-            if (votes.x) nm = fmaxf(nm, xv[4 + 0 * G + h]);
-            if (votes.y) nm = fmaxf(nm, xv[4 + 1 * G + h]);
-            if (votes.z) nm = fmaxf(nm, xv[4 + 2 * G + h]);
-            if (votes.w) nm = fmaxf(nm, xv[4 + 3 * G + h]);
-            f[h] = nm == m[h] ? 1.f : exp2f(m[h] - nm);
-            any_f |= nm != m[h];
-            m[h] = nm;
-            l[h] *= f[h];
-            z[h] *= f[h];
-          }
-          if (any_f && t > 0) {
-            // rescale O (row r) once every earlier PV product has landed
-            if (!wt.wait(pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1)) return false;
-            tc_fence_after();
-            uint32_t orow[16];
-            tmem_ld16(lane_addr + kColPV, orow);
-            tc_wait_ld();
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              orow[h] = __float_as_uint(__uint_as_float(orow[h]) * f[h]);
-              orow[G + h] = __float_as_uint(__uint_as_float(orow[G + h]) * f[h]);
+            const float nm = fmaxf(m[h], wm);
+            if (nm != m[h]) {
+              rescale |= m[h] != -INFINITY;
+              f[h] = exp2f(m[h] - nm);
+              l[h] *= f[h];
+              z[h] *= f[h];
+              m[h] = nm;
             }
-            tmem_st16(lane_addr + kColPV, orow);
-            tc_wait_st();
           }
         }
-        // probabilities -> P operand (hi | lo), K index of this token
-        if (t >= 2 && !wt.wait(pv_done + (t & 1), ((t - 2) >> 1) & 1)) return false;
-        uint8_t* pb = bp + (t & 1) * kBBytes;
+        // P operand buffer t % kBpBufs is free once PV of tile t - kBpBufs completed
+        const int pb_i = t % kBpBufs;
+        if (t >= kBpBufs && !wt.wait(pv_done + pb_i, ((t / kBpBufs) - 1) & 1)) break;
+        if (lane == 0) {
+          rs_flag[pb_i * 4 + warp] = (rescale && t > 0) ? 1 : 0;
+#pragma unroll
+          for (int h = 0; h < G; ++h) rs_f[(pb_i * 4 + warp) * G + h] = f[h];
+        }
+        uint8_t* pb = bp + pb_i * kBBytes;
         const float sv = vz.x * p.sigma_v * pos_scale;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -723,17 +743,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
           *reinterpret_cast<__half*>(pb + b_offset(G + h, kslot)) = lo;
         }
         fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bp_full + (t & 1));
-        return true;
-      };
-      bool ok = n_tiles > 0 ? convert(0) : true;
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        const uint32_t ksz = ksz_n, vsz = vsz_n, mask = mask_n;
-        if (t + 1 < n_tiles && !convert(t + 1)) break;
-        ok = softmax(t, ksz, vsz, mask);
+        mbar_arrive(bp_full + pb_i);
       }
-      // per-warp sums of l and zeta
+      // this warp's statistics
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float lv = l[h], zv = z[h];
@@ -742,58 +754,127 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
           lv += __shfl_xor_sync(kFull, lv, o);
           zv += __shfl_xor_sync(kFull, zv, o);
         }
-        if (lane == h) {
-          red_lz[warp * 2 * G + h] = lv;
-          red_lz[warp * 2 * G + G + h] = zv;
+        if (lane == 0) {
+          st_m[warp * G + h] = m[h];
+          st_l[warp * G + h] = lv;
+          st_z[warp * G + h] = zv;
         }
-        if (tid == 0) s_m[h] = m[h];
       }
     } else {
-      // ================= V path: thread c = channel c
-      const int c = tid - 128;
-      const uint32_t lane_addr = tmem + (uint32_t((warp & 3) * 32) << 16);
+      // ================= V path (thread c = channel c) and the PV MMAs
+      const int c = tid - 128, j = warp - kVWarp0;
+      const uint32_t lane_addr = tmem + (uint32_t(j * 32) << 16);
+      uint32_t rs_phase = 0;
+      // PV MMAs of tile u: rescale requested accumulators first
+      auto issue_pv = [&](int u) -> bool {
+        const int ub = u % kBpBufs;
+        if (!wt.wait(bp_full + ub, (u / kBpBufs) & 1)) return false;
+        const int4 fl = *reinterpret_cast<const int4*>(rs_flag + ub * 4);
+        if (fl.x | fl.y | fl.z | fl.w) {
+          if (u >= 1 && !wt.wait(pv_done + (u - 1) % kBpBufs, ((u - 1) / kBpBufs) & 1)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int fw = w == 0 ? fl.x : w == 1 ? fl.y : w == 2 ? fl.z : fl.w;
+            if (fw) {
+              const float* fr = rs_f + (ub * 4 + w) * G;
+              uint32_t o[2 * G];
+              tmem_ld_cols<G>(lane_addr + kColPV + uint32_t(kN * w), o);
+              tc_wait_ld();
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                o[h] = __float_as_uint(__uint_as_float(o[h]) * fr[h]);
+                o[G + h] = __float_as_uint(__uint_as_float(o[G + h]) * fr[h]);
+              }
+              tmem_st_cols<G>(lane_addr + kColPV + uint32_t(kN * w), o);
+            }
+          }
+          tc_wait_st();
+          tc_fence_before();
+          mbar_arrive(rsbar);
+          if (!wt.wait(rsbar, rs_phase & 1)) return false;
+          ++rs_phase;
+        }
+        int ok = 1;
+        if (lane == 0) {
+          ok = wt.wait(av_full + u % kAvBufs, (u / kAvBufs) & 1);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t a = tmem + kColAV + 64u * uint32_t(u % kAvBufs);
+            const uint32_t bb = smem_addr(bp) + uint32_t(ub) * kBBytes;
+#pragma unroll
+            for (int kk = 2 * j; kk < 2 * j + 2; ++kk)
+              umma_f16_ts(tmem + kColPV + uint32_t(kN * j), a + 8u * kk,
+                          smem_desc_kmajor(bb + 512u * kk, 128u, 256u), kIdesc, (u > 0 || (kk & 1)) ? 1u : 0u);
+            umma_commit(pv_done + ub);
+          }
+        }
+        return __shfl_sync(kFull, ok, 0) != 0;
+      };
       bool ok = true;
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % kSlots;
         if (!wt.wait(full + s, (t / kSlots) & 1)) { ok = false; break; }
-        if (t >= 2 && !wt.wait(pv_done + (t & 1), ((t - 2) >> 1) & 1)) { ok = false; break; }
+        // A_V buffer t % kAvBufs is free once PV of tile t - kAvBufs completed
+        if (t >= kAvBufs && !wt.wait(pv_done + (t - kAvBufs) % kBpBufs, ((t - kAvBufs) / kBpBufs) & 1)) {
+          ok = false;
+          break;
+        }
         const uint8_t* base = stage + s * kTileBytes + kHalfBytes + 4 * c;
         uint32_t wv[kTilePages];
 #pragma unroll
         for (int i = 0; i < kTilePages; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(base + i * kBlockBytes);
-        const uint32_t col0 = lane_addr + kColAV + 64u * uint32_t(t & 1);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t rr[32];
-#pragma unroll
-          for (int ii = 0; ii < 4; ++ii) {
-            const uint32_t w = wv[4 * half + ii], wsh = w >> 6;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) rr[8 * ii + j] = code_pair(w, wsh, j);
-          }
-          tmem_st32(col0 + 32u * half, rr);
-        }
+        codes_to_tmem(lane_addr + kColAV + 64u * uint32_t(t % kAvBufs), wv);
         tc_wait_st();
         mbar_arrive(empty + s);
         tc_fence_before();
-        mbar_arrive(av_full + (t & 1));
+        mbar_arrive(av_full + t % kAvBufs);
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
       }
-      // O row c: o~_h[c] = (hi + lo) * 2^24 / sigma_v (zeta added later)
-      float* os = qscratch;   // [G][128], read after the role barrier
-      if (n_tiles > 0 && ok &&
-          wt.wait(pv_done + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1)) {
-        tc_fence_after();
-        uint32_t orow[16];
-        tmem_ld16(lane_addr + kColPV, orow);
-        tc_wait_ld();
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          os[h * kHeadDim + c] = (__uint_as_float(orow[h]) + __uint_as_float(orow[G + h])) * p.pv_unscale;
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) os[h * kHeadDim + c] = 0.f;
-      }
+      if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
+      if (lane == 0) umma_commit(fin);
+      __syncwarp();
+      pv_final = n_tiles > 0 && ok && wt.wait(pv_done + (n_tiles - 1) % kBpBufs, ((n_tiles - 1) / kBpBufs) & 1);
     }
+  } else if (warp < kProducerWarp) {
+    // ================= K path (thread r = token r) and the QK MMAs
+    const int r = tid - 256, j = warp - kKWarp0;
+    const uint32_t lane_addr = tmem + (uint32_t(j * 32) << 16);
+    const int pg_in_tile = r >> 4, slot = r & 15;
+    int ok = 1;
+    if (n_tiles > 0 && lane == 0) ok = wt.wait(bqk_ready, 0);
+    ok = __shfl_sync(kFull, ok, 0);
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      const int s = t % kSlots;
+      if (!wt.wait(full + s, (t / kSlots) & 1)) break;
+      // A_K and D_qk buffers t % 2 are free once the softmax read tile t - 2
+      if (t >= 2 && !wt.wait(qk_free + (t & 1), ((t - 2) >> 1) & 1)) break;
+      const uint8_t* pg = stage + s * kTileBytes + pg_in_tile * kBlockBytes + 32 * slot;
+      const uint4 a0 = *reinterpret_cast<const uint4*>(pg);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(pg + 16);
+      const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      codes_to_tmem(lane_addr + kColAK + 64u * uint32_t(t & 1), wv);
+      tc_wait_st();
+      mbar_arrive(empty + s);
+      tc_fence_before();
+      mbar_arrive(ak_full + (t & 1));
+      if (lane == 0) {
+        ok = wt.wait(ak_full + (t & 1), (t >> 1) & 1);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t a = tmem + kColAK + 64u * uint32_t(t & 1);
+          const uint32_t d = tmem + kColQK + uint32_t(64 * (t & 1) + kN * j);
+          const uint32_t bq = smem_addr(bqk);
+#pragma unroll
+          for (int kk = 2 * j; kk < 2 * j + 2; ++kk)
+            umma_f16_ts(d, a + 8u * kk, smem_desc_kmajor(bq + 512u * kk, 128u, 256u), kIdesc, kk & 1);
+          umma_commit(qk_done + (t & 1));
+        }
+      }
+      ok = __shfl_sync(kFull, ok, 0);
+    }
+    if (lane == 0) umma_commit(fin);
+    __syncwarp();
   } else if (warp == kProducerWarp) {
     // ================= producer: 8 page blocks per tile, one lane per page
     int win_base = -1, win_pid = -1, issued = 0;
@@ -832,43 +913,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
       for (int t = max(0, issued - kSlots); t < issued; ++t)
         mbar_wait_bounded(full + t % kSlots, (t / kSlots) & 1, kWaitLimitNs);
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ================= MMA issue (one lane)
-    if (lane == 0) {
-      const uint32_t idesc = kIdesc;
-      const uint32_t bqk_addr = smem_addr(bqk), bp_addr = smem_addr(bp);
-      for (int t = 0; t <= n_tiles; ++t) {
-        if (t < n_tiles) {
-          if (!wt.wait(ak_full + (t & 1), (t >> 1) & 1)) break;
-          tc_fence_after();
-          const uint32_t a = tmem + kColAK + 64u * uint32_t(t & 1);
-          const uint32_t d = tmem + kColQK + 16u * uint32_t(t & 1);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f16_ts(d, a + 8u * kk, smem_desc_kmajor(bqk_addr + 512u * kk, 128u, 256u), idesc, kk > 0);
-          umma_commit(qk_done + (t & 1));
-        }
-        if (t >= 1) {
-          const int u = t - 1;
-          if (!wt.wait(av_full + (u & 1), (u >> 1) & 1)) break;
-          if (!wt.wait(bp_full + (u & 1), (u >> 1) & 1)) break;
-          tc_fence_after();
-          const uint32_t a = tmem + kColAV + 64u * uint32_t(u & 1);
-          const uint32_t bb = bp_addr + uint32_t(u & 1) * kBBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f16_ts(tmem + kColPV, a + 8u * kk, smem_desc_kmajor(bb + 512u * kk, 128u, 256u), idesc,
-                        (u > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(pv_done + (u & 1));
-        }
-      }
-      // every MMA issued has completed before tensor memory is released
-      umma_commit(fin);
-      mbar_wait_bounded(fin, 0, kWaitLimitNs);
-    }
-    __syncwarp();
-  } else {
-    // ================= BF16 sink / recent tokens (warps 10, 11)
+  } else if (warp >= kBf16Warp) {
+    // ================= BF16 sink / recent tokens (warps 14, 15)
     constexpr int NTQ = Gm::NTQ;
     const int bw = warp - kBf16Warp;
     int sink_len = p.sink_len[b], rec_len = p.recent_len[b];
@@ -929,43 +975,80 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
   // ================= all roles done
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
 
   float* part = p.partials + (int64_t(pair) * n_splits + split) * 2 * G * kPartStride;
   float* os = qscratch;                  // [G][128] o~ without zeta (history, rotated basis)
-  float* hz = qscratch + G * kHeadDim;   // [G][4]: m, l, zeta
-  // BF16 partial: merge of the two warps; history statistics
+  float* hz = qscratch + G * kHeadDim;   // [G][4]: zeta, BF16 weights f0, f1
+  // history: the 4 softmax warps' accumulators merged with their maxima
+  if (warp >= kVWarp0 && warp < kKWarp0) {
+    const int c = tid - 128;
+    const uint32_t lane_addr = tmem + (uint32_t((warp - kVWarp0) * 32) << 16);
+    float o[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) o[h] = 0.f;
+    if (pv_final) {
+      tc_fence_after();
+      uint32_t d[4][2 * G];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) tmem_ld_cols<G>(lane_addr + kColPV + uint32_t(kN * w), d[w]);
+      tc_wait_ld();
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          if (st_l[w * G + h] > 0.f) mx = fmaxf(mx, st_m[w * G + h]);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float e = st_l[w * G + h] > 0.f ? exp2f(st_m[w * G + h] - mx) : 0.f;
+          o[h] = fmaf(e, __uint_as_float(d[w][h]) + __uint_as_float(d[w][G + h]), o[h]);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) os[h * kHeadDim + c] = o[h] * p.pv_unscale;
+    tc_fence_before();
+  }
+  // history statistics and the BF16 partial's (m, l)
   if (tid < G) {
     const int h = tid;
-    const float* s0 = st_bf16 + h * kPartStride;
-    const float* s1 = st_bf16 + (G + h) * kPartStride;
-    const float m0 = s0[0], l0 = s0[1], m1 = s1[0], l1 = s1[1];
-    const float mx = l1 > 0.f ? (l0 > 0.f ? fmaxf(m0, m1) : m1) : m0;
-    const float f0 = l0 > 0.f ? exp2f(m0 - mx) : 0.f, f1 = l1 > 0.f ? exp2f(m1 - mx) : 0.f;
-    hz[G * 4 + h * 4 + 0] = f0;
-    hz[G * 4 + h * 4 + 1] = f1;
-    part[(G + h) * kPartStride + 0] = mx;
-    part[(G + h) * kPartStride + 1] = fmaf(l0, f0, l1 * f1);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (st_l[w * G + h] > 0.f) mx = fmaxf(mx, st_m[w * G + h]);
     float lsum = 0.f, zsum = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      lsum += red_lz[w * 2 * G + h];
-      zsum += red_lz[w * 2 * G + G + h];
+      const float e = st_l[w * G + h] > 0.f ? exp2f(st_m[w * G + h] - mx) : 0.f;
+      lsum = fmaf(e, st_l[w * G + h], lsum);
+      zsum = fmaf(e, st_z[w * G + h], zsum);
     }
     const bool any = n_tiles > 0 && lsum > 0.f;
-    part[h * kPartStride + 0] = any ? s_m[h] : -INFINITY;
+    part[h * kPartStride + 0] = any ? mx : -INFINITY;
     part[h * kPartStride + 1] = any ? lsum : 0.f;
-    hz[h * 4 + 2] = any ? zsum : 0.f;
+    hz[h * 4 + 0] = any ? zsum : 0.f;
+    const float* s0 = st_bf16 + h * kPartStride;
+    const float* s1 = st_bf16 + (G + h) * kPartStride;
+    const float m0 = s0[0], l0 = s0[1], m1 = s1[0], l1 = s1[1];
+    const float bx = l1 > 0.f ? (l0 > 0.f ? fmaxf(m0, m1) : m1) : m0;
+    const float f0 = l0 > 0.f ? exp2f(m0 - bx) : 0.f, f1 = l1 > 0.f ? exp2f(m1 - bx) : 0.f;
+    hz[h * 4 + 1] = f0;
+    hz[h * 4 + 2] = f1;
+    part[(G + h) * kPartStride + 0] = bx;
+    part[(G + h) * kPartStride + 1] = fmaf(l0, f0, l1 * f1);
   }
   __syncthreads();
+  if (warp == kTmemWarp) {
+    tc_fence_after();
+    if (lane == 0 && !mbar_wait_bounded(fin, 0, kWaitLimitNs)) flag(p.dev_status, 0x4);
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // BF16 partial: merge of the two warps
   for (int idx = tid; idx < G * kHeadDim; idx += T) {
     const int h = idx / kHeadDim, c = idx % kHeadDim;
     part[(G + h) * kPartStride + 4 + c] =
-        fmaf(hz[G * 4 + h * 4 + 0], st_bf16[h * kPartStride + 4 + c],
-             hz[G * 4 + h * 4 + 1] * st_bf16[(G + h) * kPartStride + 4 + c]);
+        fmaf(hz[h * 4 + 1], st_bf16[h * kPartStride + 4 + c], hz[h * 4 + 2] * st_bf16[(G + h) * kPartStride + 4 + c]);
   }
   if (n_tiles > 0) {
     if (!mbar_wait_bounded(vbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
@@ -993,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(DecodeParams p) {
           const float4 ov = o[(k4 + rot) & 7];
           d = fmaf(ov.x, rv[k4].x, fmaf(ov.y, rv[k4].y, fmaf(ov.z, rv[k4].z, fmaf(ov.w, rv[k4].w, d))));
         }
-        d = fmaf(hz[h * 4 + 2], rsum, d);
+        d = fmaf(hz[h * 4 + 0], rsum, d);
         d += __shfl_xor_sync(kFull, d, 1);
         d += __shfl_xor_sync(kFull, d, 2);
         if (qq == 0) part[h * kPartStride + 4 + c] = d;

@@ -13,6 +13,13 @@ constexpr int kBlockBytes = 1152;
 constexpr int kHalfBytes = 576;
 constexpr int kPartStride = 132;  // floats per (split, head) partial: m, l, pad, pad, o[128]
 
+// Lazy online-softmax maximum: a running maximum m is raised only when a
+// score (log2 units) exceeds it by more than this, so p = 2^(s - m) <= 2^this.
+#ifndef OSCAR_RESCALE_LOG2
+#define OSCAR_RESCALE_LOG2 8
+#endif
+constexpr int kRescaleLog2 = OSCAR_RESCALE_LOG2;
+
 // ---------------------------------------------------------------- demotion
 struct DemoteParams {
   uint8_t* pages;

@@ -157,10 +157,10 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   p.max_hist = desc->max_hist;
   p.n_splits = plan.n_splits;
   p.pages_per_split = plan.pages_per_split;
-  // PV operand scale: p <= 2^8 and s_V <= 2 tau_v / 3 (x2 margin for fp16
-  // rounding), so p s_V sigma_v stays below 2^14 in fp16
+  // PV operand scale: p <= 2^kRescaleLog2 and s_V <= 2 tau_v / 3 (x2 margin
+  // for fp16 rounding), so p s_V sigma_v stays below 2^14 in fp16
   int e = 0;
-  std::frexp(double(desc->tau_v) * (2.0 / 3.0) * 2.0 * 256.0, &e);
+  std::frexp(std::ldexp(double(desc->tau_v) * (2.0 / 3.0) * 2.0, oscar::kRescaleLog2), &e);
   const int sig_exp = 14 - e;
   p.sigma_v = std::ldexp(1.0f, sig_exp);
   p.pv_unscale = std::ldexp(1.0f, 24 - sig_exp);
