@@ -125,19 +125,7 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   }
   uint8_t* blk = p.pages + (page * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
   const int slot = pos % kPage;
-  if (which == 0) {
-    blk[32 * slot + lane] = uint8_t(byte);          // K: token-major, code byte `lane`
-  } else {
-    // V: channel-major words (channel c, slot s at bits 2s); other slots of
-    // the same words may be written concurrently, so clear and set atomically
-    uint32_t* words = reinterpret_cast<uint32_t*>(blk) + 4 * lane;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t code = (byte >> (2 * c)) & 3u;
-      atomicAnd(words + c, ~(3u << (2 * slot)));
-      atomicOr(words + c, code << (2 * slot));
-    }
-  }
+  blk[32 * slot + lane] = uint8_t(byte);
   if (lane == 0) {
     __half2 sz = __halves2half2(s16, z16);
     *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * slot) = sz;

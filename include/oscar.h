@@ -31,14 +31,11 @@
  * "4 codes per byte" and "scale/zero point"):
  *   pool = n_pages x n_kv_heads blocks of 1152 bytes, block (page p, head h)
  *   at byte (p * n_kv_heads + h) * 1152.  A block is a K half then a V half,
- *   576 bytes each; each half ends with 16 (scale, zero) fp16 pairs, token
- *   slot t at 512 + 4 t.  K codes are token-major: slot t's 32 code bytes at
- *   32 t, byte j holding channels 4j..4j+3 (channel 4j+i in bits 2i..2i+1).
- *   V codes are channel-major: 128 little-endian 32-bit words, word c at 4 c
- *   holding channel c of all 16 slots (slot t in bits 2t..2t+1).  Channels
- *   are in rotated order.  Logical history position x of request b lives in
- *   page page_table[b][x / 16], slot x % 16.  Fresh pages need no
- *   initialisation: demotion clears each code's bits before setting them.
+ *   576 bytes each:  16 tokens x 32 code bytes, then 16 (scale, zero) fp16
+ *   pairs.  Token slot t of a half: codes at 32 t, (scale, zero) at 512 + 4 t.
+ *   Code byte j of a token holds channels 4j..4j+3, channel 4j+i in bits
+ *   2i..2i+1; channels are in rotated order.  Logical history position x of
+ *   request b lives in page page_table[b][x / 16], slot x % 16.
  */
 #ifndef OSCAR_H_
 #define OSCAR_H_

@@ -216,16 +216,7 @@ def unpack(packed: np.ndarray) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# 3. paged history layout (this build's format; the pages fix only "paged",
-#    "4 codes per byte" and "scale/zero point")
-#
-# Block of one (physical page, KV head) = K half then V half, 576 bytes each.
-#   K half: token-major, 16 slots x 32 code bytes (byte j of a slot holds
-#           channels 4j..4j+3, channel 4j+i in bits 2i..2i+1).
-#   V half: channel-major, 128 little-endian 32-bit words; word c holds
-#           channel c of all 16 slots, slot s in bits 2s..2s+1 (so byte j of
-#           the word holds slots 4j..4j+3 of that channel).
-#   Each half ends with 16 (scale, zero) fp16 pairs, slot s at 512 + 4s.
+# 3. paged history layout (this build's format; the pages fix only "paged")
 # --------------------------------------------------------------------------
 
 def block_offset(page_id: int, kv_head: int, n_kv: int) -> int:
@@ -233,79 +224,69 @@ def block_offset(page_id: int, kv_head: int, n_kv: int) -> int:
     return (int(page_id) * n_kv + int(kv_head)) * BLOCK_BYTES
 
 
-def scale_offset(slot: int, which: int) -> int:
-    """Offset of a slot's (scale, zero) pair within a block; which 0 = K, 1 = V."""
-    return which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slot
+def token_offsets(slot: int, which: int):
+    """(code offset, scale offset) of a token slot within a block; which 0 = K, 1 = V."""
+    base = which * HALF_BYTES
+    return base + slot * CODE_BYTES, base + PAGE_TOKENS * CODE_BYTES + 4 * slot
 
 
-def code_location(slot: int, channel: int, which: int):
-    """(byte offset within the block, bit offset) of one code."""
-    if which == 0:
-        return slot * CODE_BYTES + channel // 4, 2 * (channel % 4)
-    return HALF_BYTES + 4 * channel + slot // 4, 2 * (slot % 4)
+def store_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
+                  kv_head: int, which: int, packed: np.ndarray, scale16, zero16) -> None:
+    """Place one token's packed codes and (scale, zero) at history position `pos`.
 
-
-def _positions(page_table, n_kv, b, pos):
-    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
-    base = (pages[:, None] * n_kv + np.arange(n_kv)[None, :]) * BLOCK_BYTES     # [T][n_kv]
-    return base, pos % PAGE_TOKENS
-
-
-def store_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos0: int,
-                       codes: np.ndarray, scale16: np.ndarray, zero16: np.ndarray, which: int) -> None:
-    """Place tokens pos0 .. pos0+T-1 of request b: codes [T][n_kv][d] (0..3), scale/zero [T][n_kv].
-
-    Position x lives in page page_table[b][x // 16], slot x % 16.  [GIST] 2.2 B
+    The page is page_table[b][pos // 16], the slot pos % 16.   [GIST] 2.2 B
     (paged KV cache).  `pool` is a flat uint8 array of n_pages * n_kv * 1152.
     """
-    codes = np.asarray(codes, dtype=np.uint8)
-    t_count, _, d = codes.shape
+    page = int(page_table[b, pos // PAGE_TOKENS])
+    base = block_offset(page, kv_head, n_kv)
+    co, so = token_offsets(pos % PAGE_TOKENS, which)
+    pool[base + co: base + co + CODE_BYTES] = packed
+    pair = np.array([scale16, zero16], dtype=np.float16).view(np.uint8)
+    pool[base + so: base + so + 4] = pair
+
+
+def load_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
+                 kv_head: int, which: int):
+    """(packed[32], scale float16, zero float16) stored for a history position."""
+    page = int(page_table[b, pos // PAGE_TOKENS])
+    base = block_offset(page, kv_head, n_kv)
+    co, so = token_offsets(pos % PAGE_TOKENS, which)
+    packed = pool[base + co: base + co + CODE_BYTES].copy()
+    sz = pool[base + so: base + so + 4].copy().view(np.float16)
+    return packed, sz[0], sz[1]
+
+
+def store_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
+                       pos0: int, packed: np.ndarray, scale16: np.ndarray,
+                       zero16: np.ndarray, which: int) -> None:
+    """store_history for tokens pos0 .. pos0+T-1 of all KV heads: packed[T][n_kv][32]."""
+    t_count = packed.shape[0]
     pos = pos0 + np.arange(t_count)
-    base, slots = _positions(page_table, n_kv, b, pos)
-    if which == 0:
-        idx = base + (slots * CODE_BYTES)[:, None]
-        pool[idx[..., None] + np.arange(d // 4)] = pack(codes)
-    else:
-        ch = np.arange(d)
-        byte = base[..., None] + HALF_BYTES + 4 * ch + (slots // 4)[:, None, None]     # [T][n_kv][d]
-        shift = (2 * (slots % 4)).astype(np.uint8)[:, None, None]
-        for t in range(t_count):          # slots of one page share bytes: one token at a time
-            cur = pool[byte[t]]
-            pool[byte[t]] = (cur & ~(np.uint8(3) << shift[t])) | (codes[t] << shift[t])
-    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + (4 * slots)[:, None]
-    pair = np.stack([scale16, zero16], axis=-1).astype(np.float16).view(np.uint8)    # [T][n_kv][4]
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    slots = pos % PAGE_TOKENS
+    heads = np.arange(n_kv)
+    base = (pages[:, None] * n_kv + heads[None, :]) * BLOCK_BYTES          # [T][n_kv]
+    co = base + which * HALF_BYTES + slots[:, None] * CODE_BYTES
+    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slots[:, None]
+    idx = co[..., None] + np.arange(CODE_BYTES)
+    pool[idx] = packed
+    pair = np.stack([scale16, zero16], axis=-1).astype(np.float16).view(np.uint8)  # [T][n_kv][4]
     pool[so[..., None] + np.arange(4)] = pair
 
 
 def load_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
-                      hist_len: int, which: int, d: int = D_DEFAULT):
+                      hist_len: int, which: int):
     """(codes [T][n_kv][d] uint8, scale [T][n_kv] f16, zero [T][n_kv] f16) for positions < hist_len."""
     pos = np.arange(hist_len)
-    base, slots = _positions(page_table, n_kv, b, pos)
-    if which == 0:
-        idx = base + (slots * CODE_BYTES)[:, None]
-        codes = unpack(pool[idx[..., None] + np.arange(d // 4)])
-    else:
-        ch = np.arange(d)
-        byte = base[..., None] + HALF_BYTES + 4 * ch + (slots // 4)[:, None, None]
-        shift = (2 * (slots % 4)).astype(np.uint8)[:, None, None]
-        codes = ((pool[byte] >> shift) & 3).astype(np.uint8)
-    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + (4 * slots)[:, None]
-    sz = pool[so[..., None] + np.arange(4)].copy().view(np.float16)        # [T][n_kv][2]
-    return codes, sz[..., 0], sz[..., 1]
-
-
-def store_history(pool, page_table, n_kv, b, pos, kv_head, which, codes, scale16, zero16) -> None:
-    """store_history_bulk for one token of one KV head: codes [d]."""
-    full_codes = np.zeros((1, n_kv, len(codes)), np.uint8)
-    sc = np.zeros((1, n_kv), np.float16)
-    ze = np.zeros((1, n_kv), np.float16)
-    old_c, old_s, old_z = load_history_bulk(pool, page_table, n_kv, b, pos + 1, which, len(codes))
-    full_codes[0] = old_c[pos]
-    sc[0], ze[0] = old_s[pos], old_z[pos]
-    full_codes[0, kv_head] = codes
-    sc[0, kv_head], ze[0, kv_head] = scale16, zero16
-    store_history_bulk(pool, page_table, n_kv, b, pos, full_codes, sc, ze, which)
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    slots = pos % PAGE_TOKENS
+    heads = np.arange(n_kv)
+    base = (pages[:, None] * n_kv + heads[None, :]) * BLOCK_BYTES
+    co = base + which * HALF_BYTES + slots[:, None] * CODE_BYTES
+    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slots[:, None]
+    packed = pool[co[..., None] + np.arange(CODE_BYTES)]
+    sz = pool[so[..., None] + np.arange(4)].copy().view(np.float16)      # [T][n_kv][2]
+    return unpack(packed), sz[..., 0], sz[..., 1]
 
 
 # --------------------------------------------------------------------------

@@ -96,8 +96,8 @@ class Scenario:
             cv, sv, zv = demote_heads(xv, self.rv32, self.tau_v)
             self.hist.append(dict(codes_k=ck, scale_k=sk, zero_k=zk, codes_v=cv, scale_v=sv, zero_v=zv))
             if hl:
-                O.store_history_bulk(self.pool, self.table, n_kv, b, 0, ck, sk, zk, 0)
-                O.store_history_bulk(self.pool, self.table, n_kv, b, 0, cv, sv, zv, 1)
+                O.store_history_bulk(self.pool, self.table, n_kv, b, 0, O.pack(ck), sk, zk, 0)
+                O.store_history_bulk(self.pool, self.table, n_kv, b, 0, O.pack(cv), sv, zv, 1)
 
     def segments(self, b):
         sl, hl, rl = int(self.sink_len[b]), int(self.hist_len[b]), int(self.recent_len[b])

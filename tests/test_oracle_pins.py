@@ -222,45 +222,29 @@ def test_constant_group_gives_zero_scale_and_codes():
 
 def test_page_layout_offsets_and_round_trip():
     # The block of (page 3, KV head 1) with 2 KV heads starts at (3*2+1)*1152;
-    # the V half at +576.  K codes are token-major: slot 5, channel 13 is byte
-    # 5*32 + 3, bits 2..3.  V codes are channel-major: channel 13, slot 5 is
-    # word 13 of the V half, byte 1 of that word, bits 2..3.  (scale, zero)
-    # of slot 5 sit at 512 + 20 within each half.
+    # V half at +576; slot 5 codes at +5*32; its (scale, zero) at +512+4*5.
     assert O.block_offset(3, 1, 2) == 8064
-    assert O.code_location(5, 13, 0) == (163, 2)
-    assert O.code_location(5, 13, 1) == (576 + 52 + 1, 2)
-    assert O.scale_offset(5, 1) == 576 + 512 + 20
-    assert O.scale_offset(0, 0) == 512
+    assert O.token_offsets(5, 1) == (576 + 160, 576 + 512 + 20)
+    assert O.token_offsets(0, 0) == (0, 512)
     n_kv = 2
     table, n_pages = synth.page_table(9, [37], n_extra_pages=1)
     pool = np.zeros(n_pages * n_kv * O.BLOCK_BYTES, dtype=np.uint8)
     g = synth.generator(9, 1)
-    codes = g.integers(0, 4, size=(37, n_kv, 128)).astype(np.uint8)
+    packed = g.integers(0, 256, size=(37, n_kv, 32)).astype(np.uint8)
     s = g.uniform(0.1, 2, size=(37, n_kv)).astype(np.float16)
     z = g.uniform(-3, 0, size=(37, n_kv)).astype(np.float16)
-    for which in (0, 1):
-        O.store_history_bulk(pool, table, n_kv, 0, 0, codes, s, z, which)
-        c2, s2, z2 = O.load_history_bulk(pool, table, n_kv, 0, 37, which)
-        np.testing.assert_array_equal(c2, codes)
-        np.testing.assert_array_equal(s2, s)
-        np.testing.assert_array_equal(z2, z)
-        for pos in (0, 15, 16, 36):
-            for h in range(n_kv):
-                base = (table[0, pos // 16] * n_kv + h) * 1152
-                for ch in (0, 13, 127):
-                    byte, bit = O.code_location(pos % 16, ch, which)
-                    assert (pool[base + byte] >> bit) & 3 == codes[pos, h, ch]
-    # byte-level golden of one V word: slots 0..3 of channel 0 hold codes
-    # 1, 2, 3, 0 -> byte 0 of word 0 is 0b00111001 = 57
-    pool2 = np.zeros(O.BLOCK_BYTES, dtype=np.uint8)
-    tab = np.zeros((1, 1), np.int32)
-    cc = np.zeros((4, 1, 128), np.uint8)
-    cc[:, 0, 0] = [1, 2, 3, 0]
-    O.store_history_bulk(pool2, tab, 1, 0, 0, cc, np.zeros((4, 1), np.float16), np.zeros((4, 1), np.float16), 1)
-    assert pool2[576] == 57 and not pool2[577:576 + 512].any()
-    # one-token store keeps the other slots of the shared words
-    O.store_history(pool2, tab, 1, 0, 2, 0, 1, np.full(128, 2, np.uint8), np.float16(1), np.float16(0))
-    assert pool2[576] == (1 | (2 << 2) | (2 << 4) | (0 << 6))
+    O.store_history_bulk(pool, table, n_kv, 0, 0, packed, s, z, which=1)
+    for pos in (0, 15, 16, 36):
+        for h in range(n_kv):
+            pk, ss, zz = O.load_history(pool, table, n_kv, 0, pos, h, 1)
+            np.testing.assert_array_equal(pk, packed[pos, h])
+            assert ss == s[pos, h] and zz == z[pos, h]
+            page = table[0, pos // 16]
+            base = (page * n_kv + h) * 1152 + 576 + (pos % 16) * 32
+            np.testing.assert_array_equal(pool[base:base + 32], packed[pos, h])
+    codes, s2, z2 = O.load_history_bulk(pool, table, n_kv, 0, 37, 1)
+    np.testing.assert_array_equal(O.pack(codes), packed)
+    np.testing.assert_array_equal(s2, s)
 
 
 # ---------------------------------------------------------------- attention
