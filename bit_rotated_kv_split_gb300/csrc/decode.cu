@@ -690,11 +690,14 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
                     uint32_t(Geo<G>::kRotBytes / 4), rbar);
   }
 
-  // ---------------- the query rows -> shared memory (used by the prologue)
-  if (pbeg < p.max_pages) {
+  uint16_t qv[(G * kHeadDim + T - 1) / T];
+  {
     const uint16_t* qg = p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim;
-    for (int i = tid; i < G * kHeadDim; i += T)
-      qscratch[QScratch<G>::kQs + i] = __uint_as_float(uint32_t(qg[i]) << 16);
+#pragma unroll
+    for (int i0 = 0; i0 < (G * kHeadDim + T - 1) / T; ++i0) {
+      const int i = tid + i0 * T;
+      qv[i0] = (pbeg < p.max_pages && i < G * kHeadDim) ? qg[i] : uint16_t(0);
+    }
   }
 
   // ---------------- INT2 page range of this CTA and warp.  The first pages
@@ -733,6 +736,16 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   const int spec_count = spec_end > first ? (spec_end - first + W - 1) / W : 0;
   const int issued0 = min(spec_count, kStages);
   for (int k = 0; k < issued0; ++k) issue(k, k);
+
+  // ---------------- the query rows -> shared memory (used by the prologue;
+  // requested before the page copies, stored after them)
+  if (pbeg < p.max_pages) {
+#pragma unroll
+    for (int i0 = 0; i0 < (G * kHeadDim + T - 1) / T; ++i0) {
+      const int i = tid + i0 * T;
+      if (i < G * kHeadDim) qscratch[QScratch<G>::kQs + i] = __uint_as_float(uint32_t(qv[i0]) << 16);
+    }
+  }
 
   if (hist < 0 || hist > p.max_pages * kPage) {
     if (tid == 0) flag(p.dev_status, 0x2);
@@ -930,43 +943,40 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   // ---------------- CTA merge of the warps -> one partial per head and type;
   // the history partial is rotated back with R_V here, so every partial is
   // in the original basis
-  float* cw = qscratch;                       // [2][G][W] warp weights
-  float* cml = cw + 2 * G * W;                // [2][G][2] (m, l)
-  float* os = cml + 4 * G;                    // [G][128] merged history output (rotated basis)
+  float* os = qscratch;                       // [G][128] merged history output (rotated basis)
   const int slice = kStages * kBlockBytes / 4;   // floats between two warps' states
   const float* states = reinterpret_cast<const float*>(stage);
-  if (tid < 2 * G) {
-    const int type = tid / G, h = tid % G;
-    const float* src = states + type * kStateFloats + h * kPartStride;
-    float mx = -INFINITY;
-    for (int w = 0; w < W; ++w)
-      if (src[w * slice + 1] > 0.f) mx = fmaxf(mx, src[w * slice]);
-    float lsum = 0.f;
-    for (int w = 0; w < W; ++w) {
-      const float l = src[w * slice + 1];
-      const float f = l > 0.f ? exp2f(src[w * slice] - mx) : 0.f;
-      cw[tid * W + w] = f;
-      lsum = fmaf(l, f, lsum);
-    }
-    cml[tid * 2] = mx;
-    cml[tid * 2 + 1] = lsum;
-  }
-  __syncthreads();
   float* part = p.partials + (int64_t(pair) * n_splits + split) * 2 * G * kPartStride;
+  // thread (type, head, channel): the warps' weights from their (m, l),
+  // read by all lanes of a warp at once (one (type, head) per warp)
   for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
     const int th = idx / kHeadDim, c = idx % kHeadDim;       // th = type * G + h
-    const float* src = states + (th / G) * kStateFloats + (th % G) * kPartStride + 4 + c;
-    float o = 0.f;
-#pragma unroll 4
-    for (int w = 0; w < W; ++w) o = fmaf(src[w * slice], cw[th * W + w], o);
+    const float* src = states + (th / G) * kStateFloats + (th % G) * kPartStride;
+    float mw[W], lw[W];
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      mw[w] = src[w * slice];
+      lw[w] = src[w * slice + 1];
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w)
+      if (lw[w] > 0.f) mx = fmaxf(mx, mw[w]);
+    float o = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float f = lw[w] > 0.f ? fast_exp2(mw[w] - mx) : 0.f;
+      lsum = fmaf(lw[w], f, lsum);
+      o = fmaf(src[w * slice + 4 + c], f, o);
+    }
     if (th < G) {
       os[idx] = o;
     } else {
       part[th * kPartStride + 4 + c] = o;
     }
     if (c == 0) {
-      part[th * kPartStride + 0] = cml[th * 2];
-      part[th * kPartStride + 1] = cml[th * 2 + 1];
+      part[th * kPartStride + 0] = mx;
+      part[th * kPartStride + 1] = lsum;
     }
   }
   __syncthreads();
@@ -1031,20 +1041,27 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
                  : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   for (int h = warp; h < G; h += W) {
-    float mx = -INFINITY;
-    for (int i = lane; i < NP; i += 32) {
-      const float* r = pp + int64_t(i * G + h) * kPartStride;
-      if (__ldcg(r + 1) > 0.f) mx = fmaxf(mx, __ldcg(r));
+    // (m, l) of partials lane, lane + 32, ... (NP <= 2 kMaxSplits = 8 x 32)
+    float2 ml[2 * kMaxSplits / 32];
+#pragma unroll
+    for (int u = 0; u < 2 * kMaxSplits / 32; ++u) {
+      const int i = lane + 32 * u;
+      ml[u] = i < NP ? __ldcg(reinterpret_cast<const float2*>(pp + int64_t(i * G + h) * kPartStride))
+                     : make_float2(-INFINITY, 0.f);
     }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 2 * kMaxSplits / 32; ++u)
+      if (ml[u].y > 0.f) mx = fmaxf(mx, ml[u].x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     float lsum = 0.f;
-    for (int i = lane; i < NP; i += 32) {
-      const float* r = pp + int64_t(i * G + h) * kPartStride;
-      const float l = __ldcg(r + 1);
-      const float f = l > 0.f ? exp2f(__ldcg(r) - mx) : 0.f;
-      wts[h * 2 * kMaxSplits + i] = f;
-      lsum = fmaf(l, f, lsum);
+#pragma unroll
+    for (int u = 0; u < 2 * kMaxSplits / 32; ++u) {
+      const int i = lane + 32 * u;
+      const float f = ml[u].y > 0.f ? exp2f(ml[u].x - mx) : 0.f;
+      if (i < NP) wts[h * 2 * kMaxSplits + i] = f;
+      lsum = fmaf(ml[u].y, f, lsum);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
