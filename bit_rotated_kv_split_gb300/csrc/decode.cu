@@ -77,6 +77,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMaxSplits = 128;               // bounds the last CTA's merge scratch
+constexpr int kBf16Warps = 2;                 // warps that scan the BF16 sink/recent tokens
+constexpr uint32_t kPrologueBarrier = 1;      // named barrier of the q~ prologue
 
 template <int G>
 struct Geo {
@@ -86,17 +88,20 @@ struct Geo {
   static constexpr int NTQ = (G + 7) / 8;             // BF16 QK column tiles
   static constexpr int W = G <= 4 ? OSCAR_WARPS_G4 : OSCAR_WARPS_G8;  // warps per CTA
   static constexpr int T = W * 32;
+  // the last kBf16Warps warps scan the BF16 tokens while the others build q~
+  static constexpr int PT = (W - kBf16Warps) * 32;
   static constexpr int kStages = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;   // ring stages per warp
   static constexpr size_t kStageBytes = size_t(W) * kStages * kBlockBytes;
   // ring barriers + the R_K and R_V barriers, padded so the region after it
   // stays 128-byte aligned (TMA destinations need at least 16)
-  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 2) * 8 + 127) / 128 * 128;
+  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 3) * 8 + 127) / 128 * 128;
   static constexpr size_t kStateBytes = size_t(W) * G * kPartStride * 4;   // per partial type
   // prologue: R_K (64 KB) and the q~ scratch; epilogue: two warp-state sets
   static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
   static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G + 32 * NH * 16) * 4;
   static constexpr size_t kUnion = kRotBytes + kQScratch;   // R_K then R_V | q~ scratch
-  static constexpr size_t kSmem = kStageBytes + kBarBytes + kUnion + 16;
+  static constexpr size_t kBf16State = size_t(kBf16Warps) * G * kPartStride * 4;
+  static constexpr size_t kSmem = kStageBytes + kBarBytes + kUnion + kBf16State + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   // last-CTA merge scratch in the ring region: (max, sum), split weights,
@@ -559,7 +564,7 @@ struct QScratch {
 template <int G>
 __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float* rks, uint64_t* rbar,
                              float* scratch) {
-  constexpr int T = Geo<G>::T, NH = Geo<G>::NH;
+  constexpr int T = Geo<G>::PT, NH = Geo<G>::NH;
   using S = QScratch<G>;
   float* qs = scratch + S::kQs;
   float* part = scratch + S::kPart;
@@ -568,7 +573,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
   float* red = scratch + S::kRed;
   uint32_t* frag = reinterpret_cast<uint32_t*>(scratch + S::kFrag);
   const int tid = threadIdx.x;
-  __syncthreads();   // qs was filled at kernel start
+  named_barrier(kPrologueBarrier, T);   // qs was filled at kernel start
   if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
   for (int task = tid; task < 4 * kHeadDim; task += T) {
     const int ig = task / kHeadDim, j = task % kHeadDim;
@@ -589,7 +594,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
 #pragma unroll
     for (int h = 0; h < G; ++h) part[(ig * G + h) * kHeadDim + j] = acc[h];
   }
-  __syncthreads();
+  named_barrier(kPrologueBarrier, T);
   for (int idx = tid; idx < G * kHeadDim; idx += T) {
     const float v = ((part[idx] + part[G * kHeadDim + idx]) + part[2 * G * kHeadDim + idx]) +
                     part[3 * G * kHeadDim + idx];
@@ -605,7 +610,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
       red[4 * G + (idx >> 7) * 4 + ((idx >> 5) & 3)] = sm;
     }
   }
-  __syncthreads();
+  named_barrier(kPrologueBarrier, T);
   if (tid < G) {
     const float mx = fmaxf(fmaxf(red[tid * 4], red[tid * 4 + 1]), fmaxf(red[tid * 4 + 2], red[tid * 4 + 3]));
     const float sm = ((red[4 * G + tid * 4] + red[4 * G + tid * 4 + 1]) + red[4 * G + tid * 4 + 2]) +
@@ -620,7 +625,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
     aux[tid * 4 + 1] = ldexpf(1.f, 24 - e) * scale;   // 2^24 / sigma * log2(e) / sqrt(d)
     aux[tid * 4 + 2] = sm * scale;
   }
-  __syncthreads();
+  named_barrier(kPrologueBarrier, T);
   for (int idx = tid; idx < 32 * NH * 16; idx += T) {
     const int ln = idx / (NH * 16), rem = idx % (NH * 16);
     const int nt = rem / 16, j = (rem / 2) % 8, rr = rem % 2;
@@ -635,7 +640,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
     }
     frag[idx] = pack_half2(v0, v1);
   }
-  __syncthreads();
+  named_barrier(kPrologueBarrier, T);
 }
 
 // Page ids of a warp's pages, 32 at a time, one per lane (warp-collective).
@@ -665,23 +670,29 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<G>::kStageBytes);
   uint64_t* rbar = bars + W * kStages;       // R_K, then (last CTA) R_V
   uint8_t* uni = smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes;
-  float* st_hist = reinterpret_cast<float*>(uni);
-  float* st_bf16 = st_hist + W * G * kPartStride;
   float* rks = reinterpret_cast<float*>(uni);                         // prologue only
   float* qscratch = reinterpret_cast<float*>(uni + Geo<G>::kRotBytes);
-  int* s_last = reinterpret_cast<int*>(uni + Geo<G>::kUnion);
+  float* st_bf16x = reinterpret_cast<float*>(uni + Geo<G>::kUnion);   // [kBf16Warps][G][kPartStride]
+  int* s_last = reinterpret_cast<int*>(uni + Geo<G>::kUnion + Geo<G>::kBf16State);
+  uint64_t* pro_done = bars + W * kStages + 2;   // q~ fragments ready (after R_K, R_V)
+  constexpr int PT = Geo<G>::PT;
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int pair = b * p.n_kv + hkv;
   const int n_splits = p.n_splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool bf16_warp = warp >= W - kBf16Warps;
   const int gid = lane >> 2, tig = lane & 3;
   const int pbeg = split * p.pages_per_split;
 
   // ---------------- R_K -> shared memory first: nothing it depends on
-  if (tid == 0 && pbeg < p.max_pages) {
+  if (tid == 0) {
     mbar_init(rbar, 1);
+    mbar_init(rbar + 1, 1);   // R_V
+    mbar_init(pro_done, 1);
     fence_mbar_init();
+  }
+  if (tid == 0 && pbeg < p.max_pages) {
     mbar_arrive_expect_tx(rbar, uint32_t(Geo<G>::kRotBytes));
     const float* rk = p.r_k + int64_t(hkv) * kHeadDim * kHeadDim;
 #pragma unroll
@@ -690,13 +701,13 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
                     uint32_t(Geo<G>::kRotBytes / 4), rbar);
   }
 
-  uint16_t qv[(G * kHeadDim + T - 1) / T];
+  uint16_t qv[(G * kHeadDim + PT - 1) / PT];
   {
     const uint16_t* qg = p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim;
 #pragma unroll
-    for (int i0 = 0; i0 < (G * kHeadDim + T - 1) / T; ++i0) {
-      const int i = tid + i0 * T;
-      qv[i0] = (pbeg < p.max_pages && i < G * kHeadDim) ? qg[i] : uint16_t(0);
+    for (int i0 = 0; i0 < (G * kHeadDim + PT - 1) / PT; ++i0) {
+      const int i = tid + i0 * PT;
+      qv[i0] = (pbeg < p.max_pages && !bf16_warp && i < G * kHeadDim) ? qg[i] : uint16_t(0);
     }
   }
 
@@ -737,12 +748,14 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   const int issued0 = min(spec_count, kStages);
   for (int k = 0; k < issued0; ++k) issue(k, k);
 
+  __syncthreads();   // the R_K / R_V / prologue barriers are initialised
+
   // ---------------- the query rows -> shared memory (used by the prologue;
   // requested before the page copies, stored after them)
-  if (pbeg < p.max_pages) {
+  if (pbeg < p.max_pages && !bf16_warp) {
 #pragma unroll
-    for (int i0 = 0; i0 < (G * kHeadDim + T - 1) / T; ++i0) {
-      const int i = tid + i0 * T;
+    for (int i0 = 0; i0 < (G * kHeadDim + PT - 1) / PT; ++i0) {
+      const int i = tid + i0 * PT;
       if (i < G * kHeadDim) qscratch[QScratch<G>::kQs + i] = __uint_as_float(uint32_t(qv[i0]) << 16);
     }
   }
@@ -757,13 +770,16 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   const int pend = min(pbeg + p.pages_per_split, n_pg);
   const int count = pend > first ? (pend - first + W - 1) / W : 0;
 
-  // ---------------- q~ and the lane's QK fragments
+  // ---------------- q~ and the lane's QK fragments (prologue warps); the
+  // BF16 warps scan the sink/recent tokens meanwhile and read the fragments
+  // once the prologue is done
   constexpr int NH = Geo<G>::NH;
   uint32_t qb[NH][8][2];
   float unscale[NH], qz[NH];
   const bool any_pages = pend > pbeg;
-  if (any_pages) {
-    rotate_query<G>(p, b, hkv, rks, rbar, qscratch);
+  float* rvs = rks;
+  uint64_t* vbar = rbar + 1;
+  auto load_fragments = [&]() {
     using S = QScratch<G>;
     const uint4* fr = reinterpret_cast<const uint4*>(qscratch + S::kFrag) + lane * NH * 4;
 #pragma unroll
@@ -781,27 +797,92 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
       unscale[nt] = qscratch[S::kAux + h * 4 + 1];
       qz[nt] = qscratch[S::kAux + h * 4 + 2];
     }
-  } else if (tid == 0 && pbeg < p.max_pages) {
-    // R_K was requested: let it land before this region is reused
-    if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs)) flag(p.dev_status, 0x4);
-  }
-  __syncthreads();   // prologue reads of R_K and the scratch are done
-
-  // R_V -> shared memory (replacing R_K) for this CTA's output rotation
-  float* rvs = rks;
-  uint64_t* vbar = rbar + 1;
-  if (tid == 0) {
-    fence_proxy_async_smem();
-    mbar_init(vbar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(vbar, uint32_t(Geo<G>::kRotBytes));
-    const float* rv = p.r_v + int64_t(hkv) * kHeadDim * kHeadDim;
+  };
+  if (!bf16_warp) {
+    if (any_pages) {
+      rotate_query<G>(p, b, hkv, rks, rbar, qscratch);
+      load_fragments();
+    } else if (tid == 0 && pbeg < p.max_pages) {
+      // R_K was requested: let it land before this region is reused
+      if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs)) flag(p.dev_status, 0x4);
+    }
+    named_barrier(kPrologueBarrier, PT);   // prologue reads of R_K are done
+    // R_V -> shared memory (replacing R_K) for this CTA's output rotation
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(vbar, uint32_t(Geo<G>::kRotBytes));
+      const float* rv = p.r_v + int64_t(hkv) * kHeadDim * kHeadDim;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      bulk_copy_g2s(rvs + c * (kHeadDim * kHeadDim / 4), rv + c * (kHeadDim * kHeadDim / 4),
-                    uint32_t(Geo<G>::kRotBytes / 4), vbar);
+      for (int c = 0; c < 4; ++c)
+        bulk_copy_g2s(rvs + c * (kHeadDim * kHeadDim / 4), rv + c * (kHeadDim * kHeadDim / 4),
+                      uint32_t(Geo<G>::kRotBytes / 4), vbar);
+      mbar_arrive(pro_done);
+    }
+  } else {
+    // ---------------- BF16 sink / recent tokens owned by this CTA: virtual
+    // pages split, split + n_splits, ...; the j-th goes to BF16 warp j % 2
+    int sink_len = p.sink_len[b], rec_len = p.recent_len[b];
+    const int rec_start = p.recent_start[b];
+    const int bw = warp - (W - kBf16Warps);
+    if (sink_len < 0 || sink_len > p.sink_cap || rec_len < 0 || rec_len > p.recent_cap ||
+        rec_start < 0 || rec_start >= max(p.recent_cap, 1)) {
+      if (bw == 0 && lane == 0) flag(p.dev_status, 0x2);
+      sink_len = max(0, min(sink_len, p.sink_cap));
+      rec_len = max(0, min(rec_len, p.recent_cap));
+    }
+    const int start = min(max(rec_start, 0), max(p.recent_cap - 1, 0));
+    const int n_vp = p.sink_cap / kPage + p.recent_cap / kPage;
+    const int64_t hstride = int64_t(p.n_kv) * kHeadDim;
+    WarpState<G> st;
+    st.init();
+    const int mine = split + bw * n_splits;
+    if (mine < n_vp) {
+      uint32_t qf[NTQ][8][2];
+#pragma unroll
+      for (int nt = 0; nt < NTQ; ++nt) {
+        const int h = (8 * nt + gid) % G;
+        const uint16_t* qrow = p.q + (int64_t(b) * p.n_kv * G + hkv * G + h) * kHeadDim + 32 * tig;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * u));
+          qf[nt][2 * u][0] = v.x;
+          qf[nt][2 * u][1] = v.y;
+          qf[nt][2 * u + 1][0] = v.z;
+          qf[nt][2 * u + 1][1] = v.w;
+        }
+      }
+      auto row_of = [&](int u, bool kv, bool& ok) -> const uint16_t* {
+        if (u < p.sink_cap) {
+          ok = u < sink_len;
+          const uint16_t* base = kv ? p.sink_v : p.sink_k;
+          return base + (int64_t(b) * p.sink_cap + u) * hstride + int64_t(hkv) * kHeadDim;
+        }
+        const int i = u - p.sink_cap;
+        ok = i < rec_len;
+        const int slot = (start + i) % p.recent_cap;
+        const uint16_t* base = kv ? p.recent_v : p.recent_k;
+        return base + (int64_t(b) * p.recent_cap + slot) * hstride + int64_t(hkv) * kHeadDim;
+      };
+      for (int vp = mine; vp < n_vp; vp += kBf16Warps * n_splits) {
+        const int u0 = vp * kPage;
+        bool kok[2], vok[4];
+        const uint16_t* krow[2] = {row_of(u0 + gid, false, kok[0]), row_of(u0 + gid + 8, false, kok[1])};
+        const uint16_t* vrow[4] = {row_of(u0 + 2 * tig, true, vok[0]), row_of(u0 + 2 * tig + 1, true, vok[1]),
+                                   row_of(u0 + 2 * tig + 8, true, vok[2]),
+                                   row_of(u0 + 2 * tig + 9, true, vok[3])};
+        bf16_page<G>(krow, vrow, kok, vok, gid, tig, qf, st);
+      }
+    }
+    store_warp_state<G, false>(st, st_bf16x + bw * G * kPartStride, gid, tig, 1.f);
+    if (any_pages) {
+      if (!mbar_wait_bounded(pro_done, 0, kWaitLimitNs)) {
+        if (lane == 0) flag(p.dev_status, 0x4);
+      } else {
+        load_fragments();
+      }
+    }
   }
-  // each warp's states go into its own ring slice once its pages are done
+  // each warp's INT2 state goes into its own ring slice once its pages are done
   float* my_state = reinterpret_cast<float*>(ring);
   constexpr int kStateFloats = G * kPartStride;
 
@@ -881,63 +962,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     store_hist_state<G>(st, my_state, gid, tig, p.pv_unscale);
   }
 
-  // ---------------- BF16 sink / recent tokens owned by this CTA
-  {
-    int sink_len = p.sink_len[b], rec_len = p.recent_len[b];
-    const int rec_start = p.recent_start[b];
-    if (sink_len < 0 || sink_len > p.sink_cap || rec_len < 0 || rec_len > p.recent_cap ||
-        rec_start < 0 || rec_start >= max(p.recent_cap, 1)) {
-      if (tid == 0) flag(p.dev_status, 0x2);
-      sink_len = max(0, min(sink_len, p.sink_cap));
-      rec_len = max(0, min(rec_len, p.recent_cap));
-    }
-    const int start = min(max(rec_start, 0), max(p.recent_cap - 1, 0));
-    const int n_vp = p.sink_cap / kPage + p.recent_cap / kPage;
-    const int64_t hstride = int64_t(p.n_kv) * kHeadDim;
-    WarpState<G> st;
-    st.init();
-    // virtual pages split, split + n_splits, ...; the k-th goes to warp
-    // W-1-(k % W): the last warps own the fewest INT2 pages
-    const int mine = split + (W - 1 - warp) * n_splits;
-    if (mine < n_vp) {
-      uint32_t qf[NTQ][8][2];
-#pragma unroll
-      for (int nt = 0; nt < NTQ; ++nt) {
-        const int h = (8 * nt + gid) % G;
-        const uint16_t* qrow = p.q + (int64_t(b) * p.n_kv * G + hkv * G + h) * kHeadDim + 32 * tig;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * u));
-          qf[nt][2 * u][0] = v.x;
-          qf[nt][2 * u][1] = v.y;
-          qf[nt][2 * u + 1][0] = v.z;
-          qf[nt][2 * u + 1][1] = v.w;
-        }
-      }
-      auto row_of = [&](int u, bool kv, bool& ok) -> const uint16_t* {
-        if (u < p.sink_cap) {
-          ok = u < sink_len;
-          const uint16_t* base = kv ? p.sink_v : p.sink_k;
-          return base + (int64_t(b) * p.sink_cap + u) * hstride + int64_t(hkv) * kHeadDim;
-        }
-        const int i = u - p.sink_cap;
-        ok = i < rec_len;
-        const int slot = (start + i) % p.recent_cap;
-        const uint16_t* base = kv ? p.recent_v : p.recent_k;
-        return base + (int64_t(b) * p.recent_cap + slot) * hstride + int64_t(hkv) * kHeadDim;
-      };
-      for (int vp = mine; vp < n_vp; vp += W * n_splits) {
-        const int u0 = vp * kPage;
-        bool kok[2], vok[4];
-        const uint16_t* krow[2] = {row_of(u0 + gid, false, kok[0]), row_of(u0 + gid + 8, false, kok[1])};
-        const uint16_t* vrow[4] = {row_of(u0 + 2 * tig, true, vok[0]), row_of(u0 + 2 * tig + 1, true, vok[1]),
-                                   row_of(u0 + 2 * tig + 8, true, vok[2]),
-                                   row_of(u0 + 2 * tig + 9, true, vok[3])};
-        bf16_page<G>(krow, vrow, kok, vok, gid, tig, qf, st);
-      }
-    }
-    store_warp_state<G, false>(st, my_state + kStateFloats, gid, tig, 1.f);
-  }
   __syncthreads();
 
   // ---------------- CTA merge of the warps -> one partial per head and type;
@@ -949,14 +973,19 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   float* part = p.partials + (int64_t(pair) * n_splits + split) * 2 * G * kPartStride;
   // thread (type, head, channel): the warps' weights from their (m, l),
   // read by all lanes of a warp at once (one (type, head) per warp)
+  // (history: the W warps' states in their ring slices; BF16: the BF16
+  // warps' states)
   for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
     const int th = idx / kHeadDim, c = idx % kHeadDim;       // th = type * G + h
-    const float* src = states + (th / G) * kStateFloats + (th % G) * kPartStride;
+    const bool hist_type = th < G;
+    const float* src = hist_type ? states + (th % G) * kPartStride : st_bf16x + (th % G) * kPartStride;
+    const int stride = hist_type ? slice : G * kPartStride;
+    const int nw = hist_type ? W : kBf16Warps;
     float mw[W], lw[W];
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      mw[w] = src[w * slice];
-      lw[w] = src[w * slice + 1];
+      mw[w] = w < nw ? src[w * stride] : -INFINITY;
+      lw[w] = w < nw ? src[w * stride + 1] : 0.f;
     }
     float mx = -INFINITY;
 #pragma unroll
@@ -965,9 +994,11 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     float o = 0.f, lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      const float f = lw[w] > 0.f ? fast_exp2(mw[w] - mx) : 0.f;
-      lsum = fmaf(lw[w], f, lsum);
-      o = fmaf(src[w * slice + 4 + c], f, o);
+      if (w < nw) {
+        const float f = lw[w] > 0.f ? fast_exp2(mw[w] - mx) : 0.f;
+        lsum = fmaf(lw[w], f, lsum);
+        o = fmaf(src[w * stride + 4 + c], f, o);
+      }
     }
     if (th < G) {
       os[idx] = o;
