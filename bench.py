@@ -18,8 +18,14 @@ copies of the layer cache whose total size exceeds 3x the L2 cache, so no
 step reads its inputs from L2 (inputs larger than L2; no flush needed).
 
   python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+  python bench.py --workload qwen3-4b-36layer-b28-100k | qwen3-32b-layer-b64-ragged-prefix |
+                  bulk-demote-128k-36layer
 
-`--impl reference` times the float64 CPU oracle on this host instead.
+`--impl reference` times the float64 CPU oracle on this host instead.  The
+other `--workload`s measure the larger stated workloads (one JSON line each):
+a 36-layer decode step of 28 requests at 100k context, a batch-64 GQA-8
+layer with ragged contexts and a shared 32k prefix, and the bulk demotion of
+a 128k-token prefill followed by batch-1 decode over it.
 """
 from __future__ import annotations
 
@@ -40,6 +46,19 @@ WORKLOAD = dict(workload="qwen3-8b-layer-decode-100k", batch=1, n_q_heads=32, n_
                 head_dim=128, ctx=100_000, sink=64, recent=256, page_tokens=16, group=128, seed=1002)
 METRIC = "decode-attn tokens/s at 100k ctx (1 layer, Qwen3-8B shape)"
 UNIT = "tokens/s"
+EXTRA_WORKLOADS = {
+    # 36-layer decode step: per layer one demotion per request + decode
+    "qwen3-4b-36layer-b28-100k": dict(batch=28, n_q_heads=32, n_kv_heads=8, ctx=100_000, layers=36,
+                                      seed=1003, distinct_layers=2),
+    # one GQA-8 layer, contexts U[8k, 128k], first 32k tokens a shared prefix
+    "qwen3-32b-layer-b64-ragged-prefix": dict(batch=64, n_q_heads=64, n_kv_heads=8, ctx_lo=8192,
+                                              ctx_hi=131_072, shared=32_768, layers=1, seed=1004,
+                                              distinct_layers=2),
+    # rotate-clip-quantise-pack of a 128k-token prefill (8 KV heads, 36
+    # layers), then batch-1 GQA-4 decode over the 128k history
+    "bulk-demote-128k-36layer": dict(batch=1, n_q_heads=32, n_kv_heads=8, ctx=131_072, layers=36,
+                                     seed=1005, distinct_layers=2),
+}
 CACHE_TENSORS = ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
                  "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status")
 
@@ -53,6 +72,8 @@ def _args():
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--reps", type=int, default=20, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD["workload"],
+                    choices=[WORKLOAD["workload"]] + sorted(EXTRA_WORKLOADS))
     return ap.parse_args()
 
 
@@ -553,6 +574,261 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------- larger stated workloads
+
+def _rotations_for(B, seed, n_kv, layer):
+    """R_K, R_V, tau_K, tau_V of one layer, built by the library from seeded calibration data."""
+    import numpy as np
+    import synth
+    outl = synth.outlier_channels(seed, layer, n_kv)
+    rk, rv, ck, cv = [], [], [], []
+    for hh in range(n_kv):
+        cal = synth.calibration_set(seed, layer, hh, outl[hh], n_q=4096, n_k=2048)
+        rk.append(B.oscar_build_rotation(cal["q"])[0])
+        rv.append(B.oscar_build_rotation(B.oscar_score_weighted_rows(cal["q"], cal["k"], cal["v"]))[0])
+        ck.append(cal["k"])
+        cv.append(cal["v"])
+    rk32 = np.stack(rk).astype(np.float32)
+    rv32 = np.stack(rv).astype(np.float32)
+    tau_k = B.oscar_clip_threshold(np.stack(ck), rk32.astype(np.float64))
+    tau_v = B.oscar_clip_threshold(np.stack(cv), rv32.astype(np.float64))
+    return rk32, rv32, tau_k, tau_v, outl
+
+
+def _build_batch_cache(torch, B, dev, rot, seed, layer, ctxs, n_q, n_kv, shared_hist=0):
+    """Layer cache for requests of contexts `ctxs`; history demoted by the library.
+
+    With `shared_hist`, the full history pages below it are one physical set
+    shared by every request (demoted once)."""
+    import synth
+    from bit_rotated_kv_split_gb300.cache import LayerCache
+    rk, rv, tau_k, tau_v, outl = rot
+    splits = [_split(c) for c in ctxs]
+    hist = [h for _, h, _ in splits]
+    table, n_pages = synth.page_table(seed + 100 * layer, hist, n_extra_pages=1, shared_prefix_tokens=shared_hist)
+    bsz = len(ctxs)
+    cache = LayerCache(bsz, n_q, n_kv, table.shape[1], n_pages, torch.from_numpy(rk), torch.from_numpy(rv),
+                       tau_k, tau_v, device=dev)
+    cache.page_table.copy_(torch.from_numpy(table))
+    cache.max_hist = max(hist)
+    n_shared_pages = 0
+    if shared_hist:
+        n_shared_pages = min(shared_hist // 16, max(h // 16 for h in hist))
+    shared_tok = [min(n_shared_pages, h // 16) * 16 for h in hist]
+    chunk = 32768
+    done_shared = 0
+    for b in range(bsz):
+        lo = shared_tok[b] if done_shared >= shared_tok[b] else done_shared
+        for t0 in range(lo, hist[b], chunk):
+            n = min(chunk, hist[b] - t0)
+            stream_b = 0 if t0 < shared_tok[b] else b
+            xk = synth.activations_device(seed, (layer, stream_b, 0, t0), n, outl, dev)
+            xv = synth.activations_device(seed, (layer, stream_b, 1, t0), n, outl, dev)
+            pos = torch.arange(t0, t0 + n, dtype=torch.int32, device=dev)
+            req = torch.full((n,), b, dtype=torch.int32, device=dev)
+            B.oscar_quantize_append(cache.desc(max(hist) + 16), xk.view(torch.uint16), xv.view(torch.uint16), n,
+                                    n_kv * 128, None, req, pos, n)
+        done_shared = max(done_shared, shared_tok[b])
+    cap_s, cap_r = WORKLOAD["sink"], WORKLOAD["recent"]
+    sk = synth.activations_device(seed, (layer, 1, 0), bsz * cap_s, outl, dev)
+    sv = synth.activations_device(seed, (layer, 1, 1), bsz * cap_s, outl, dev)
+    rk_ = synth.activations_device(seed, (layer, 1, 2), bsz * cap_r, outl, dev)
+    rv_ = synth.activations_device(seed, (layer, 1, 3), bsz * cap_r, outl, dev)
+    cache.sink_k.copy_(sk.view(cache.sink_k.shape))
+    cache.sink_v.copy_(sv.view(cache.sink_v.shape))
+    cache.recent_k.copy_(rk_.view(cache.recent_k.shape))
+    cache.recent_v.copy_(rv_.view(cache.recent_v.shape))
+    cache.hist_len.copy_(torch.tensor(hist, dtype=torch.int32))
+    cache.sink_len.copy_(torch.tensor([x for x, _, _ in splits], dtype=torch.int32))
+    cache.recent_len.copy_(torch.tensor([x for _, _, x in splits], dtype=torch.int32))
+    cache.recent_start.fill_(1)
+    torch.cuda.synchronize()
+    assert int(cache.dev_status.item()) == 0
+    unique_hist = n_shared_pages * 16 + sum(h - st for h, st in zip(hist, shared_tok))
+    return cache, hist, unique_hist
+
+
+def _decode_bytes(hist_tokens, ctx_tokens_bf16, n_q, n_kv, n_hist_pages):
+    per_hist_token = n_kv * 2 * (128 // 4 + 4)
+    return (hist_tokens * per_hist_token + ctx_tokens_bf16 * n_kv * 2 * 128 * 2 + n_hist_pages * 4
+            + n_q * 128 * 6)
+
+
+def run_extra(args):
+    import numpy as np
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    import synth
+    cfg = EXTRA_WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n_q, n_kv, seed, L, nd = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["seed"], cfg["layers"], cfg["distinct_layers"]
+    bsz = cfg["batch"]
+    K, W = args.steps, args.warmup
+    peak, peak_kind = _roofline_peak()
+    rots = [_rotations_for(B, seed, n_kv, i) for i in range(nd)]
+    stream = torch.cuda.Stream()
+    clocks = Clocks(0)
+    line = {"n_gpus": 1, "steps": K, "warmup": W, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int2/bf16 in, f32 accumulate", "data": "synthetic"}
+
+    if args.workload == "bulk-demote-128k-36layer":
+        ctx = cfg["ctx"]
+        s0, h, r0 = _split(ctx)
+        caches, srcs = [], []
+        for i in range(nd):
+            c, _, _ = _build_batch_cache(torch, B, dev, rots[i], seed, i, [ctx], n_q, n_kv)
+            caches.append(c)
+            srcs.append((synth.activations_device(seed, (50 + i, 0), ctx, rots[i][4], dev),
+                         synth.activations_device(seed, (50 + i, 1), ctx, rots[i][4], dev)))
+        idx = torch.arange(s0, s0 + h, dtype=torch.int32, device=dev)
+        req = torch.zeros(h, dtype=torch.int32, device=dev)
+        pos = torch.arange(h, dtype=torch.int32, device=dev)
+        descs = [c.desc(h) for c in caches]
+        q = synth.activations_device(seed, (60, 0), 1, rots[0][4].repeat(n_q // n_kv, axis=0), dev).view(1, n_q, 128)
+        out = torch.empty((1, n_q, 128), dtype=torch.float32, device=dev)
+        ws_bytes = B.oscar_decode_workspace_bytes(descs[0])
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+
+        def demote_layer(i):
+            xk, xv = srcs[i % nd]
+            B.oscar_quantize_append(descs[i % nd], xk.view(torch.uint16), xv.view(torch.uint16), ctx,
+                                    n_kv * 128, idx, req, pos, h)
+
+        def decode(i):
+            B.oscar_decode_attention(descs[i % nd], q, out, ws, ws_bytes)
+
+        with torch.cuda.stream(stream):
+            gd, gq = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            for i in range(2):
+                demote_layer(i)
+                decode(i)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(gd, stream=stream):
+                for i in range(L):
+                    demote_layer(i)
+            with torch.cuda.graph(gq, stream=stream):
+                for i in range(2 * nd):
+                    decode(i)
+            for _ in range(W):
+                gd.replay()
+                gq.replay()
+            torch.cuda.synchronize()
+            clocks.start()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            for _ in range(K):
+                gd.replay()
+            e[1].record(stream)
+            for _ in range(K):
+                gq.replay()
+            e[2].record(stream)
+            torch.cuda.synchronize()
+            clk = clocks.stop()
+        t_bulk = e[0].elapsed_time(e[1]) / 1e3 / K            # 36 layers
+        t_dec = e[1].elapsed_time(e[2]) / 1e3 / (K * 2 * nd)
+        bulk_bytes = L * h * n_kv * (2 * 128 * 2 + 2 * (128 // 4 + 4))
+        dec_bytes = _decode_bytes(h, s0 + r0, n_q, n_kv, -(-h // 16))
+        status = max(int(c.dev_status.item()) for c in caches)
+        line.update({
+            "metric": "bulk demotion GB/s (read + written) of a 128k-token prefill, 8 KV heads x 36 layers",
+            "value": bulk_bytes / t_bulk / 1e9, "unit": "GB/s", "ms_per_step": t_bulk * 1e3,
+            "config": {"workload": args.workload, "tokens": h, "n_kv_heads": n_kv, "head_dim": 128, "layers": L,
+                       "distinct_layers": nd, "l2_policy": "inputs larger than L2 (prefill buffers of %.0f MB per layer)"
+                       % (ctx * n_kv * 128 * 2 * 2 / 1e6)},
+            "roofline": {"bound": "hbm", "achieved": bulk_bytes / t_bulk / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": bulk_bytes / t_bulk / 1e9 / peak, "kernel": "demote_kernel (oscar_quantize_append)",
+                         "algorithmic_bytes": bulk_bytes, "peak_kind": peak_kind + " hbm_gbs"},
+            "decode_after": {"ms": t_dec * 1e3, "tokens_per_s": 1 / t_dec, "hbm_gbs": dec_bytes / t_dec / 1e9,
+                             "frac": dec_bytes / t_dec / 1e9 / peak, "algorithmic_bytes": dec_bytes,
+                             "context": ctx, "n_q_heads": n_q},
+            "gpu_launches": K * (L + 2 * nd), "clocks": clk, "device_status": status})
+        print(json.dumps(line))
+        return
+
+    # decode-step workloads
+    if "ctx" in cfg:
+        ctxs = [cfg["ctx"]] * bsz
+    else:
+        ctxs = [int(c) for c in synth.ragged_lengths(seed, bsz, cfg["ctx_lo"], cfg["ctx_hi"])]
+    shared_hist = cfg.get("shared", 0)
+    shared_hist = shared_hist - WORKLOAD["sink"] if shared_hist else 0
+    caches, uniq = [], 0
+    for i in range(nd):
+        c, hist, uniq = _build_batch_cache(torch, B, dev, rots[i], seed, i, ctxs, n_q, n_kv, shared_hist)
+        caches.append(c)
+    g = n_q // n_kv
+    q = synth.activations_device(seed, (70, 0), bsz, rots[0][4].repeat(g, axis=0), dev).view(bsz, n_q, 128)
+    new_k = synth.activations_device(seed, (70, 1), bsz, rots[0][4], dev)
+    new_v = synth.activations_device(seed, (70, 2), bsz, rots[0][4], dev)
+    out = torch.empty((bsz, n_q, 128), dtype=torch.float32, device=dev)
+    src = torch.tensor([b * WORKLOAD["recent"] for b in range(bsz)], dtype=torch.int32, device=dev)
+    dst_req = torch.arange(bsz, dtype=torch.int32, device=dev)
+    dst_pos = torch.tensor(hist, dtype=torch.int32, device=dev)        # private tail slot of each request
+    descs = [c.desc(max(hist) + 16) for c in caches]
+    ddescs = [c.desc(max(hist)) for c in caches]
+    ws_bytes = B.oscar_decode_workspace_bytes(ddescs[0])
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def demote(i):
+        c = caches[i % nd]
+        B.oscar_quantize_append(descs[i % nd], c.recent_k.view(torch.uint16), c.recent_v.view(torch.uint16),
+                                bsz * WORKLOAD["recent"], n_kv * 128, src, dst_req, dst_pos, bsz,
+                                new_k.view(torch.uint16), new_v.view(torch.uint16))
+
+    def decode(i):
+        B.oscar_decode_attention(ddescs[i % nd], q, out, ws, ws_bytes)
+
+    with torch.cuda.stream(stream):
+        for i in range(nd):
+            demote(i)
+            decode(i)
+        torch.cuda.synchronize()
+        g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=stream):
+            for i in range(L):
+                demote(i)
+                decode(i)
+        with torch.cuda.graph(g_dec, stream=stream):
+            for i in range(max(L, 2 * nd)):
+                decode(i)
+        for _ in range(W):
+            g_step.replay()
+        torch.cuda.synchronize()
+        clocks.start()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        for _ in range(K):
+            g_step.replay()
+        e[1].record(stream)
+        for _ in range(K):
+            g_dec.replay()
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+    t_step = e[0].elapsed_time(e[1]) / 1e3 / K
+    t_dec = e[1].elapsed_time(e[2]) / 1e3 / (K * max(L, 2 * nd))
+    bf16_tok = sum(sum(_split(c)[0::2]) for c in ctxs)
+    logical = _decode_bytes(sum(hist), bf16_tok, n_q * bsz, n_kv, sum(-(-h // 16) for h in hist))
+    unique = _decode_bytes(uniq, bf16_tok, n_q * bsz, n_kv, sum(-(-h // 16) for h in hist))
+    status = max(int(c.dev_status.item()) for c in caches)
+    metric = ("36-layer decode-step tokens/s (Qwen3-4B shape, batch 28, 100k ctx, 1 demotion per request-layer)"
+              if L > 1 else "decode tokens/s (Qwen3-32B layer, batch 64, ragged 8k-128k ctx, shared 32k prefix)")
+    line.update({
+        "metric": metric, "value": bsz / t_step, "unit": "tokens/s", "ms_per_step": t_step * 1e3,
+        "config": {"workload": args.workload, "batch": bsz, "n_q_heads": n_q, "n_kv_heads": n_kv, "head_dim": 128,
+                   "layers": L, "distinct_layers": nd, "ctx_min": min(ctxs), "ctx_max": max(ctxs),
+                   "ctx_mean": sum(ctxs) / bsz, "shared_prefix_tokens": cfg.get("shared", 0),
+                   "l2_policy": "inputs larger than L2 (each layer cache > 1 GB)", "cuda_graphs": True},
+        "decode_ms": t_dec * 1e3,
+        "roofline": {"bound": "hbm", "achieved": unique / t_dec / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": unique / t_dec / 1e9 / peak, "kernel": "split_kernel (oscar_decode_attention)",
+                     "algorithmic_bytes": unique, "logical_bytes": logical, "peak_kind": peak_kind + " hbm_gbs"},
+        "logical_gbs": logical / t_dec / 1e9,
+        "gpu_launches": K * 2 * L, "clocks": clk, "device_status": status})
+    print(json.dumps(line))
+
+
 def main():
     args = _args()
     if args.cpu_baseline_worker:
@@ -560,6 +836,9 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload != WORKLOAD["workload"]:
+        run_extra(args)
         return
     run_gpu(args)
 
