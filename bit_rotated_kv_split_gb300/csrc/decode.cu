@@ -1192,22 +1192,25 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
   const int64_t slots = int64_t(sms) * occ;
   const int64_t pairs = int64_t(batch) * n_kv;
   const int pages_max = (max_hist + kPage - 1) / kPage;
-  // one wave when every (request, KV head) can get whole SMs and each warp
-  // then streams at most 64 pages; otherwise 16 pages per warp and several
-  // waves balanced by the block scheduler
-  int pps;
-  const int64_t per_pair = slots / pairs;
-  if (per_pair >= 1 && (pages_max + per_pair - 1) / per_pair <= 64 * warps) {
-    pps = int((pages_max + per_pair - 1) / per_pair);
-  } else {
-    pps = 16 * warps;
+  // splits per (request, KV head): the count that minimises a simple model
+  // of the launch time, waves x (pages per warp x time per page + fixed
+  // per-CTA time), with the measured ~1 us per page per warp (GQA 4; ~1.5 us
+  // for GQA 8) and ~10 us of fixed prologue + merge latency per CTA
+  const double t_page = group == 4 ? 0.95 : 1.5, t_fixed = 10.0;
+  int n_splits = 1;
+  double best = 1e300;
+  for (int n = 1; n <= kMaxSplits; ++n) {
+    const int64_t pps_n = (pages_max + n - 1) / n;
+    if (n > 1 && (pages_max + pps_n - 1) / pps_n < n) break;   // no finer split exists
+    const int64_t waves = (pairs * n + slots - 1) / slots;
+    const double cost = double(waves) * (double((pps_n + warps - 1) / warps) * t_page + t_fixed);
+    if (cost < best * 0.999) {
+      best = cost;
+      n_splits = n;
+    }
   }
-  pps = max(pps, 1);
-  int n_splits = max(1, (pages_max + pps - 1) / pps);
-  if (n_splits > kMaxSplits) {
-    pps = (pages_max + kMaxSplits - 1) / kMaxSplits;
-    n_splits = (pages_max + pps - 1) / pps;
-  }
+  int pps = max(1, (pages_max + n_splits - 1) / n_splits);
+  n_splits = max(1, (pages_max + pps - 1) / pps);
   plan->n_splits = n_splits;
   plan->pages_per_split = pps;
   size_t off = 0;
