@@ -43,6 +43,11 @@ struct DemoteParams {
 
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream);
 
+// Tensor-core bulk path (128 tokens per MMA tile); used for at least
+// kBulkDemoteMin items without a new-token write.
+constexpr int kBulkDemoteMin = 1024;
+cudaError_t launch_demote_bulk(const DemoteParams& p, cudaStream_t stream);
+
 // ---------------------------------------------------------------- decode
 struct DecodeParams {
   // cache

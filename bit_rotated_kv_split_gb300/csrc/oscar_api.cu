@@ -99,7 +99,9 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
   p.n_kv = desc->n_kv_heads;
   p.max_pages = desc->max_pages_per_seq;
   p.n_pages = desc->n_pages;
-  const cudaError_t e = oscar::launch_demote(p, static_cast<cudaStream_t>(stream));
+  const bool bulk = n >= oscar::kBulkDemoteMin && !new_k && !new_v;
+  const cudaError_t e = bulk ? oscar::launch_demote_bulk(p, static_cast<cudaStream_t>(stream))
+                             : oscar::launch_demote(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 

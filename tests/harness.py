@@ -134,17 +134,21 @@ class Scenario:
         return sk, sv
 
 
-def rotation_error_bound(x: np.ndarray, r32: np.ndarray) -> np.ndarray:
-    """Bound on |fp32 x.R - exact x.R| per (token, head), maximised over channels.
+def rotation_error_bound(x: np.ndarray, r32: np.ndarray, terms_per_channel: int = 6) -> np.ndarray:
+    """Bound on |computed x.R - exact x.R| per (token, head), maximised over channels.
 
-    x [T][n_kv][d], r32 [n_kv][d][d].  The standard bound for a d-term dot
-    product accumulated in binary32: gamma_d * sum_i |x_i| |R_ij|, with
-    gamma_d = d u / (1 - d u) and u = 2^-24 (plus one rounding of the bf16
-    inputs, which are exact in binary32).
+    x [T][n_kv][d], r32 [n_kv][d][d].  The standard bound for an m-term dot
+    product accumulated in binary32: gamma_m * sum_i |x_i| |R_ij|, with
+    gamma_m = m u / (1 - m u), u = 2^-24 and m = terms_per_channel * d.  The
+    SIMT kernel sums d products; the tensor-core bulk kernel sums 2 d (R split
+    into hi + lo) in blocks of 16 whose internal addition is not specified to
+    round to nearest after each product, and was measured at up to 1.7x the
+    3 d binary32 bound on 1M token-heads; m = 6 d covers both.
     """
     t, n_kv, d = x.shape
     u = 2.0 ** -24
-    gamma = d * u / (1 - d * u)
+    m = terms_per_channel * d
+    gamma = m * u / (1 - m * u)
     out = np.empty((t, n_kv))
     for h in range(n_kv):
         out[:, h] = (np.abs(x[:, h].astype(np.float64)) @ np.abs(r32[h].astype(np.float64))).max(-1)
@@ -179,14 +183,22 @@ def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, r
         tol = 1e-5 * np.abs(pb)
         if err is not None:
             tol = np.maximum(tol, err[bad])
-        half_ulp = np.abs(np.spacing(g[bad])).astype(np.float64) / 2
-        ok = np.abs(gb - pb) <= tol + half_ulp
+        # the interval of values that round to g (asymmetric at a binade edge)
+        gh = g[bad]
+        lo_edge = gb - (gb - np.nextafter(gh, np.float16(-np.inf)).astype(np.float64)) / 2
+        hi_edge = gb + (np.nextafter(gh, np.float16(np.inf)).astype(np.float64) - gb) / 2
+        ok = (pb >= lo_edge - tol) & (pb <= hi_edge + tol)
+        half_ulp = np.maximum(hi_edge - gb, gb - lo_edge)
         if not np.all(ok):
             d_ulp = np.abs(g[bad].view(np.uint16).astype(np.int32) - r[bad].view(np.uint16).astype(np.int32))
+            idx = np.argwhere(bad)[~ok][:4]
             raise AssertionError("scale/zero differ beyond the rounding rule: %d of %d differ, "
-                                 "max ulp %d, max |gpu - pre| / tol %.3g"
+                                 "max ulp %d, max |gpu - pre| / tol %.3g; first (index, gpu, oracle, pre, tol): %s"
                                  % (int((~ok).sum()), int(bad.size), int(d_ulp.max()),
-                                    float((np.abs(gb - pb) / (tol + half_ulp)).max())))
+                                    float((np.abs(gb - pb) / (tol + half_ulp)).max()),
+                                    [(tuple(int(v) for v in i), float(g[tuple(i)]), float(r[tuple(i)]),
+                                      float(pre[tuple(i)]), float((tol + half_ulp)[~ok][n]))
+                                     for n, i in enumerate(idx)]))
         return int(bad.sum())
 
     n_s = fp16_ok(gpu_s, ref_s, pre_s, None if rot_err is None else 2.0 * rot_err / 3.0)
@@ -199,9 +211,11 @@ def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, r
     diff = gpu_codes != recomputed
     if diff.any():
         ud = u[diff]
+        # a rotated value known to within rot_err moves u by rot_err / s
+        slack = 0.0 if rot_err is None else np.broadcast_to((rot_err[..., None] / s), u.shape)[diff]
         near = np.zeros(ud.shape, bool)
         for bnd in (0.5, 1.5, 2.5):
-            near |= np.abs(ud - bnd) <= 1e-5 * bnd
+            near |= np.abs(ud - bnd) <= np.maximum(1e-5 * bnd, slack)
         assert near.all(), "%d codes differ away from a rounding boundary" % int((~near).sum())
     e2e = float(np.mean(gpu_codes != ref_codes))
     assert e2e <= 1e-4, "code mismatch fraction %g > 1e-4" % e2e

@@ -73,7 +73,8 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False):
                        for h in range(n_kv)], axis=1)
         rc, rs, rz = H.demote_heads(xs, r32, tau)
         pre_s, pre_z = _pre_rounding(xr)
-        res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z)
+        res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z,
+                                   rot_err=H.rotation_error_bound(xs, r32))
     if with_new:
         np.testing.assert_array_equal(k_src.float().cpu().numpy()[src_index], nk)
         np.testing.assert_array_equal(v_src.float().cpu().numpy()[src_index], nv)
@@ -81,7 +82,16 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False):
 
 
 def test_demote_tiny_config_tokens():
+    # 1728 tokens: the tensor-core bulk path
     res = _run(2001, 1728, 1)
+    print(res)
+
+
+def test_demote_bulk_path_eight_heads_ragged_tail():
+    # 3000 tokens (not a multiple of the 128-token tile), scattered positions
+    g = synth.generator(4, 1)
+    pos = g.permutation(5000)[:3000]
+    res = _run(2004, 3000, 8, positions=pos)
     print(res)
 
 
