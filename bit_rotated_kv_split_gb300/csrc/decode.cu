@@ -109,7 +109,7 @@ struct Geo {
   // each warp's ring slice holds its two warp states at the end
   static_assert(2 * G * kPartStride * 4 <= kStages * kBlockBytes, "warp states in the ring slice");
   // CTA merge scratch (after R_V in the union) and last-CTA scratch (ring)
-  static_assert((2 * G * W + 4 * G + G * kHeadDim) * 4 <= kQScratch, "CTA merge scratch");
+  static_assert((2 * G * kHeadDim + 6 * G) * 4 <= kQScratch, "CTA merge scratch");
   static_assert((G + 2 * G * kMaxSplits) * 4 + 16 * (T / (G * 32) > 0 ? T / (G * 32) : 1) * G * 32 + 16 <= kStageBytes,
                 "merge scratch");
 };
@@ -964,13 +964,15 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
 
   __syncthreads();
 
-  // ---------------- CTA merge of the warps -> one partial per head and type;
-  // the history partial is rotated back with R_V here, so every partial is
-  // in the original basis
+  // ---------------- CTA merge of the warps -> one partial per head: the
+  // history part is rotated back with R_V and joined with the BF16 part, so
+  // the CTA writes one (m, l, o) per head in the original basis
   float* os = qscratch;                       // [G][128] merged history output (rotated basis)
+  float* ob = os + G * kHeadDim;              // [G][128] merged BF16 output
+  float* cml = ob + G * kHeadDim;             // [2][G][2] (m, l) of history, BF16
   const int slice = kStages * kBlockBytes / 4;   // floats between two warps' states
   const float* states = reinterpret_cast<const float*>(stage);
-  float* part = p.partials + (int64_t(pair) * n_splits + split) * 2 * G * kPartStride;
+  float* part = p.partials + (int64_t(pair) * n_splits + split) * G * kPartStride;
   // thread (type, head, channel): the warps' weights from their (m, l),
   // read by all lanes of a warp at once (one (type, head) per warp)
   // (history: the W warps' states in their ring slices; BF16: the BF16
@@ -1000,21 +1002,28 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
         o = fmaf(src[w * stride + 4 + c], f, o);
       }
     }
-    if (th < G) {
-      os[idx] = o;
-    } else {
-      part[th * kPartStride + 4 + c] = o;
-    }
+    os[idx] = o;                                           // ob follows os
     if (c == 0) {
-      part[th * kPartStride + 0] = mx;
-      part[th * kPartStride + 1] = lsum;
+      cml[th * 2 + 0] = mx;
+      cml[th * 2 + 1] = lsum;
     }
   }
   __syncthreads();
   if (!mbar_wait_bounded(vbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
-  // history partial back in the original basis: o[c] = sum_j o~[j] R_V[c][j];
-  // thread (row c, quarter qq), chunk order rotated by the lane so the 32
-  // lanes of a load hit all 32 banks
+  // history partial back in the original basis, o[c] = sum_j o~[j] R_V[c][j],
+  // joined with the BF16 partial; thread (row c, quarter qq), chunk order
+  // rotated by the lane so the 32 lanes of a load hit all 32 banks
+  float* jw = cml + 4 * G;                    // [G][2] weights of the history and BF16 parts
+  if (tid < G) {
+    const float mh = cml[tid * 2], lh = cml[tid * 2 + 1], mb = cml[(G + tid) * 2], lb = cml[(G + tid) * 2 + 1];
+    const float mx = lh > 0.f ? (lb > 0.f ? fmaxf(mh, mb) : mh) : mb;
+    const float wh = lh > 0.f ? fast_exp2(mh - mx) : 0.f, wb = lb > 0.f ? fast_exp2(mb - mx) : 0.f;
+    jw[tid * 2] = wh;
+    jw[tid * 2 + 1] = wb;
+    part[tid * kPartStride + 0] = mx;
+    part[tid * kPartStride + 1] = fmaf(lh, wh, lb * wb);
+  }
+  __syncthreads();
   for (int task = tid; task < 4 * kHeadDim; task += T) {
     const int c = task >> 2, qq = task & 3;
     const int rot = lane & 7;
@@ -1033,7 +1042,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
       }
       d += __shfl_xor_sync(kFull, d, 1);
       d += __shfl_xor_sync(kFull, d, 2);
-      if (qq == 0) part[h * kPartStride + 4 + c] = d;
+      if (qq == 0) part[h * kPartStride + 4 + c] = fmaf(jw[h * 2], d, jw[h * 2 + 1] * ob[h * kHeadDim + c]);
     }
   }
 
@@ -1048,12 +1057,12 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   if (!*s_last) return;
   fence_acq_rel_gpu();
 
-  // Merge of the 2 n_splits partials of each head.  Thread (q, head h,
+  // Merge of the n_splits partials of each head.  Thread (q, head h,
   // channel quad c4) first requests its partial outputs i = q, q + Q, ...;
   // while they are in flight, warp h computes head h's weights, so the two
   // dependent global reads overlap.
-  const float* pp = p.partials + int64_t(pair) * n_splits * 2 * G * kPartStride;
-  const int NP = 2 * n_splits;                        // partials per head
+  const float* pp = p.partials + int64_t(pair) * n_splits * G * kPartStride;
+  const int NP = n_splits;                            // partials per head
   constexpr int HC = G * 32;                          // (head, channel quad) pairs
   constexpr int Q = T / HC > 0 ? T / HC : 1;          // partial subsets
   constexpr int kPre = 12;                            // outputs requested before the weights
@@ -1217,7 +1226,7 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
   plan->off_counters = off;
   off = align256(off + size_t(pairs) * 4);
   plan->off_partials = off;
-  off = align256(off + size_t(pairs) * n_splits * 2 * group * kPartStride * 4);
+  off = align256(off + size_t(pairs) * n_splits * group * kPartStride * 4);
   plan->total_bytes = off;
   *err = cudaSuccess;
   return occ;

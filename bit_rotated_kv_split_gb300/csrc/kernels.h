@@ -69,7 +69,7 @@ struct DecodeParams {
   float* out;
   // workspace views
   uint32_t* counters;   // [pairs] merge tickets (zero between calls)
-  float* partials;      // [pairs][n_splits][2][G][kPartStride]
+  float* partials;      // [pairs][n_splits][G][kPartStride]
   // dims
   int32_t batch, n_kv, group, sink_cap, recent_cap, max_pages;
   int64_t n_pages;

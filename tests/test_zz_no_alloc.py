@@ -45,13 +45,15 @@ def test_static_workspace_rejects_oversized_problems():
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
-    # 64 requests x 8 KV heads x GQA 8 at 128k tokens needs far more than the
-    # fixed array; the call must refuse before launching anything
+    # 1024 requests x 8 KV heads x GQA 8 at 128k tokens: at least one split
+    # partial per (request, query head) is far more than the fixed array; the
+    # call must refuse before launching anything
     r = torch.eye(128).repeat(8, 1, 1)
-    cache = LayerCache(64, 64, 8, 8192, 16, r, r, 4.0, 4.0)
+    cache = LayerCache(1024, 64, 8, 8192, 16, r, r, 4.0, 4.0, sink_cap=0, recent_cap=0)
     desc = cache.desc(131_072 - 320)
-    out = torch.empty((64, 64, 128), dtype=torch.float32, device="cuda")
-    q = torch.zeros((64, 64, 128), dtype=torch.bfloat16, device="cuda")
+    assert B.oscar_decode_workspace_bytes(desc) > (8 << 20)
+    out = torch.empty((1024, 64, 128), dtype=torch.float32, device="cuda")
+    q = torch.zeros((1024, 64, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(B.OscarError) as err:
         B.oscar_decode_attention_static(desc, q.view(torch.uint16), out)
     assert err.value.status == 3
