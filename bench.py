@@ -427,7 +427,7 @@ def run_gpu(args):
     # demotion) back to back, for the per-kernel durations
     stream = torch.cuda.Stream()
     use_graphs = True
-    g_step, g_decode, g_demote = [], None, None
+    g_step, g_chain, g_decode, g_demote = [], None, None, None
     try:
         with torch.cuda.stream(stream):
             for i in range(n_copies):
@@ -440,6 +440,13 @@ def run_gpu(args):
                     demote(i)
                     decode(i)
                 g_step.append(g)
+            # every copy's step in order, as a serving loop replays all layers
+            # (kernel to kernel edges are programmatic launches)
+            g_chain = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_chain, stream=stream):
+                for i in range(n_copies):
+                    demote(i)
+                    decode(i)
             g_decode, g_demote = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_decode, stream=stream):
                 for i in range(n_copies):
@@ -459,6 +466,17 @@ def run_gpu(args):
             demote(i)
             decode(i)
 
+    def run_steps(n):
+        """n steps over the layer copies 0, 1, ... in order (whole chains, then single steps)."""
+        if use_graphs:
+            for _ in range(n // n_copies):
+                g_chain.replay()
+            for k in range(n % n_copies):
+                g_step[k].replay()
+        else:
+            for k in range(n):
+                run_step(k % n_copies)
+
     def run_all(graph, fn):
         if use_graphs:
             graph.replay()
@@ -470,24 +488,21 @@ def run_gpu(args):
     clocks = Clocks(local)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     with torch.cuda.stream(stream):
-        for k in range(W):
-            run_step(k % n_copies)
+        run_steps(W)
         torch.cuda.synchronize()
         clocks.start()
         t_pre = time.perf_counter()
         pre = 0
         while time.perf_counter() - t_pre < 1.0:      # same load before the timed region, for clock samples
-            for _ in range(50):
-                run_step(pre % n_copies)
-                pre += 1
+            run_steps(7 * n_copies)
+            pre += 7 * n_copies
             torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         ev[0].record(stream)
-        for k in range(K):
-            run_step(k % n_copies)
+        run_steps(K)
         ev[1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0

@@ -41,6 +41,7 @@
 //   2^-24 factors are folded into the B operand (QK) or the output (PV).
 //   The contraction order of channels is free, so B is permuted to match.
 #include <cfloat>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -287,15 +288,18 @@ __device__ __forceinline__ void int2_qk(const uint8_t* __restrict__ pg, int gid,
 
 // Scores (log2 units) of the lane's two tokens of one page from its QK
 // accumulators and the tokens' K (scale, zero); -inf where not valid.
-template <int G>
+// kMasked = false: every token of the page is valid (no selects).
+template <int G, bool kMasked>
 __device__ __forceinline__ void int2_scores(const float (&d)[Geo<G>::NH][4], uint32_t ksz0, uint32_t ksz1,
                                             bool ok0, bool ok1, const float (&uns)[Geo<G>::NH],
                                             const float (&qz)[Geo<G>::NH], float (&sc)[Geo<G>::NH][2]) {
   const float2 kz0 = half2_to_float2(ksz0), kz1 = half2_to_float2(ksz1);
 #pragma unroll
   for (int nt = 0; nt < Geo<G>::NH; ++nt) {
-    sc[nt][0] = ok0 ? fmaf(kz0.x * (d[nt][0] + d[nt][1]), uns[nt], kz0.y * qz[nt]) : -INFINITY;
-    sc[nt][1] = ok1 ? fmaf(kz1.x * (d[nt][2] + d[nt][3]), uns[nt], kz1.y * qz[nt]) : -INFINITY;
+    const float s0 = fmaf(kz0.x * (d[nt][0] + d[nt][1]), uns[nt], kz0.y * qz[nt]);
+    const float s1 = fmaf(kz1.x * (d[nt][2] + d[nt][3]), uns[nt], kz1.y * qz[nt]);
+    sc[nt][0] = (!kMasked || ok0) ? s0 : -INFINITY;
+    sc[nt][1] = (!kMasked || ok1) ? s1 : -INFINITY;
   }
 }
 
@@ -337,19 +341,32 @@ __device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH]
 // Probabilities of one page -> PV B fragments: the lane packs (hi, lo) of
 // p s_V sigma_v for token gid (row gid, columns 2 tig, 2 tig + 1) and token
 // gid + 8; movmatrix transposes them into the B layout (rows = tokens).
-template <int G>
+// (kMasked = false: every token valid, so stale ring bytes never reach a
+// product and no select is needed.)
+template <int G, bool kMasked>
 __device__ __forceinline__ void int2_probs(const float (&sc)[Geo<G>::NH][2], uint32_t vsz0, uint32_t vsz1,
                                            bool ok0, bool ok1, float sigma_v, HistState<G>& st,
                                            uint32_t (&pb)[Geo<G>::NH][2]) {
   const float2 vz0 = half2_to_float2(vsz0), vz1 = half2_to_float2(vsz1);
+  const float sv0 = vz0.x * sigma_v, sv1 = vz1.x * sigma_v;
 #pragma unroll
   for (int nt = 0; nt < Geo<G>::NH; ++nt) {
-    const float p0 = ok0 ? fast_exp2(sc[nt][0] - st.m[nt]) : 0.f;
-    const float p1 = ok1 ? fast_exp2(sc[nt][1] - st.m[nt]) : 0.f;
-    st.l[nt] += p0 + p1;
-    st.z[nt] += (ok0 ? p0 * vz0.y : 0.f) + (ok1 ? p1 * vz1.y : 0.f);
-    const float q0 = ok0 ? p0 * vz0.x * sigma_v : 0.f;
-    const float q1 = ok1 ? p1 * vz1.x * sigma_v : 0.f;
+    float p0 = fast_exp2(sc[nt][0] - st.m[nt]);
+    float p1 = fast_exp2(sc[nt][1] - st.m[nt]);
+    float q0, q1;
+    if constexpr (kMasked) {
+      p0 = ok0 ? p0 : 0.f;
+      p1 = ok1 ? p1 : 0.f;
+      st.l[nt] += p0 + p1;
+      st.z[nt] += (ok0 ? p0 * vz0.y : 0.f) + (ok1 ? p1 * vz1.y : 0.f);
+      q0 = ok0 ? p0 * sv0 : 0.f;
+      q1 = ok1 ? p1 * sv1 : 0.f;
+    } else {
+      st.l[nt] += p0 + p1;
+      st.z[nt] = fmaf(p0, vz0.y, fmaf(p1, vz1.y, st.z[nt]));
+      q0 = p0 * sv0;
+      q1 = p1 * sv1;
+    }
     const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
     const __half l0 = __float2half_rn(q0 - __half2float(h0)), l1 = __float2half_rn(q1 - __half2float(h1));
     pb[nt][0] = movmatrix_trans(uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(l0)) << 16));
@@ -677,6 +694,8 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   uint64_t* pro_done = bars + W * kStages + 2;   // q~ fragments ready (after R_K, R_V)
   constexpr int PT = Geo<G>::PT;
 
+  pdl_wait();                 // the previous kernel's writes are visible
+  pdl_launch_dependents();
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int pair = b * p.n_kv + hkv;
   const int n_splits = p.n_splits;
@@ -901,6 +920,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     for (; k < count; k += kGroup) {
       const uint8_t* pg[kGroup];
       bool ok[kGroup][2];
+      bool all_full = true;        // warp-uniform
       int s_u = s_cur;
       uint32_t ph_u = phase;
 #pragma unroll
@@ -911,6 +931,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
         const bool valid = in && ((stage_ok >> s_u) & 1u);
         if (in && !valid && lane == 0) flag(p.dev_status, 0x1);
         const int ntok = valid ? tok_left - u * W * kPage : 0;
+        all_full = all_full && ntok >= kPage;
         ok[u][0] = gid < ntok;
         ok[u][1] = gid + 8 < ntok;
         if (++s_u == kStages) {
@@ -919,23 +940,34 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
         }
       }
       if (timed_out) break;
-      float sc[kGroup][NH][2];
+      // QK of the step's pages, one maximum update, probabilities and PV;
+      // steps whose tokens are all valid (every step but the history's last
+      // and a warp's odd tail page) take the select-free variant
+      auto step = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
+        float sc[kGroup][NH][2];
 #pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        float d[NH][4];
-        int2_qk<G>(pg[u], gid, tig, qb, d);
-        const uint32_t ksz0 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * gid);
-        const uint32_t ksz1 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * (gid + 8));
-        int2_scores<G>(d, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
-      }
-      int2_update_max<G, kGroup>(sc, st);
+        for (int u = 0; u < kGroup; ++u) {
+          float d[NH][4];
+          int2_qk<G>(pg[u], gid, tig, qb, d);
+          const uint32_t ksz0 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * gid);
+          const uint32_t ksz1 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * (gid + 8));
+          int2_scores<G, kMasked>(d, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
+        }
+        int2_update_max<G, kGroup>(sc, st);
 #pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        const uint32_t vsz0 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * gid);
-        const uint32_t vsz1 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * (gid + 8));
-        uint32_t pb[NH][2];
-        int2_probs<G>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
-        int2_pv<G>(pg[u], gid, tig, pb, st);
+        for (int u = 0; u < kGroup; ++u) {
+          const uint32_t vsz0 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * gid);
+          const uint32_t vsz1 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * (gid + 8));
+          uint32_t pb[NH][2];
+          int2_probs<G, kMasked>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
+          int2_pv<G>(pg[u], gid, tig, pb, st);
+        }
+      };
+      if (all_full) {
+        step(std::false_type{});
+      } else {
+        step(std::true_type{});
       }
       __syncwarp();
 #pragma unroll
@@ -1163,8 +1195,8 @@ cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Geo<G>::kSmem));
   if (e != cudaSuccess) return e;
-  split_kernel<G><<<dim3(p.n_splits, p.n_kv, p.batch), Geo<G>::T, Geo<G>::kSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(split_kernel<G>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T), Geo<G>::kSmem,
+                    stream, p);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -23,6 +23,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr size_t kSmem = kRotBytes + 16;
 
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
+  pdl_wait();                 // the previous kernel's writes are visible
+  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   float* rs = reinterpret_cast<float*>(smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kRotBytes);
@@ -140,8 +142,8 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream) {
   if (chunks > 0x7fffffff || int64_t(p.n_kv) * 2 > 65535) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(demote_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
-  demote_kernel<<<dim3(unsigned(chunks), unsigned(p.n_kv * 2)), kWarps * 32, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(demote_kernel, dim3(unsigned(chunks), unsigned(p.n_kv * 2)), dim3(kWarps * 32), kSmem,
+                    stream, p);
 }
 
 }  // namespace oscar

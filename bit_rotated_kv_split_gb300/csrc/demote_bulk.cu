@@ -78,6 +78,8 @@ struct Waiter {
 };
 
 __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p) {
+  pdl_wait();                 // the previous kernel's writes are visible
+  pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* bhi = smem + oBhi;
   uint8_t* blo = smem + oBlo;
@@ -290,8 +292,8 @@ cudaError_t launch_demote_bulk(const DemoteParams& p, cudaStream_t stream) {
   // one CTA per SM shared out over the (KV head, K|V) pairs
   const int64_t per_pair = int64_t(sms) / (2 * p.n_kv);
   const int64_t gx = per_pair < n_tiles ? (per_pair > 0 ? per_pair : 1) : n_tiles;
-  bulk_demote_kernel<<<dim3(unsigned(gx), unsigned(p.n_kv * 2)), kThreads, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(bulk_demote_kernel, dim3(unsigned(gx), unsigned(p.n_kv * 2)), dim3(kThreads), kSmem,
+                    stream, p);
 }
 
 }  // namespace oscar

@@ -20,6 +20,27 @@ constexpr int kPartStride = 132;  // floats per (split, head) partial: m, l, pad
 #endif
 constexpr int kRescaleLog2 = OSCAR_RESCALE_LOG2;
 
+// Every kernel launches with programmatic stream serialisation: its CTAs may
+// become resident while the kernel before it on the stream drains, and its
+// first instruction (griddepcontrol.wait) holds them until that kernel has
+// completed and its writes are visible, so results are those of plain stream
+// order; each kernel also allows the kernel after it to launch at once.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------- demotion
 struct DemoteParams {
   uint8_t* pages;
