@@ -105,14 +105,13 @@ struct Geo {
   static constexpr size_t kSmem = kStageBytes + kBarBytes + kUnion + kBf16State + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-  // last-CTA merge scratch in the ring region: (max, sum), split weights,
-  // half sums and merged outputs
   // each warp's ring slice holds its two warp states at the end
   static_assert(2 * G * kPartStride * 4 <= kStages * kBlockBytes, "warp states in the ring slice");
-  // CTA merge scratch (after R_V in the union) and last-CTA scratch (ring)
-  static_assert((2 * G * kHeadDim + 6 * G) * 4 <= kQScratch, "CTA merge scratch");
-  static_assert((G + 2 * G * kMaxSplits) * 4 + 16 * (T / (G * 32) > 0 ? T / (G * 32) : 1) * G * 32 + 16 <= kStageBytes,
-                "merge scratch");
+  // CTA merge scratch (after R_V in the union): merged outputs and weights
+  static_assert((2 * G * kHeadDim + 32 * G) * 4 <= kQScratch, "CTA merge scratch");
+  // ring region once the warp states are consumed: rotation quarters, then
+  // the last CTA's split weights
+  static_assert(4 * G * kHeadDim * 4 <= kStageBytes && G * kMaxSplits * 4 <= kStageBytes, "merge scratch");
 };
 
 // head owned by head slot hs of a lane with column group tig
@@ -998,84 +997,91 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
 
   // ---------------- CTA merge of the warps -> one partial per head: the
   // history part is rotated back with R_V and joined with the BF16 part, so
-  // the CTA writes one (m, l, o) per head in the original basis
+  // the CTA writes one (m, l, o) per head in the original basis.
+  // Warp h weighs head h's W history states (ring slices) and kBf16Warps
+  // BF16 states against their common maximum; lane i holds state i.
   float* os = qscratch;                       // [G][128] merged history output (rotated basis)
   float* ob = os + G * kHeadDim;              // [G][128] merged BF16 output
-  float* cml = ob + G * kHeadDim;             // [2][G][2] (m, l) of history, BF16
+  float* wts = ob + G * kHeadDim;             // [G][32] state weights
   const int slice = kStages * kBlockBytes / 4;   // floats between two warps' states
   const float* states = reinterpret_cast<const float*>(stage);
   float* part = p.partials + (int64_t(pair) * n_splits + split) * G * kPartStride;
-  // thread (type, head, channel): the warps' weights from their (m, l),
-  // read by all lanes of a warp at once (one (type, head) per warp)
-  // (history: the W warps' states in their ring slices; BF16: the BF16
-  // warps' states)
-  for (int idx = tid; idx < 2 * G * kHeadDim; idx += T) {
-    const int th = idx / kHeadDim, c = idx % kHeadDim;       // th = type * G + h
-    const bool hist_type = th < G;
-    const float* src = hist_type ? states + (th % G) * kPartStride : st_bf16x + (th % G) * kPartStride;
-    const int stride = hist_type ? slice : G * kPartStride;
-    const int nw = hist_type ? W : kBf16Warps;
-    float mw[W], lw[W];
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      mw[w] = w < nw ? src[w * stride] : -INFINITY;
-      lw[w] = w < nw ? src[w * stride + 1] : 0.f;
+  static_assert(W + kBf16Warps <= 32, "one lane per warp state");
+  static_assert(G <= W, "one warp per head");
+  if (warp < G) {
+    const int h = warp;
+    float m = -INFINITY, l = 0.f;
+    if (lane < W) {
+      m = states[lane * slice + h * kPartStride];
+      l = states[lane * slice + h * kPartStride + 1];
+    } else if (lane < W + kBf16Warps) {
+      m = st_bf16x[(lane - W) * G * kPartStride + h * kPartStride];
+      l = st_bf16x[(lane - W) * G * kPartStride + h * kPartStride + 1];
     }
-    float mx = -INFINITY;
+    float mx = l > 0.f ? m : -INFINITY;
 #pragma unroll
-    for (int w = 0; w < W; ++w)
-      if (lw[w] > 0.f) mx = fmaxf(mx, mw[w]);
-    float o = 0.f, lsum = 0.f;
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    const float f = l > 0.f ? fast_exp2(m - mx) : 0.f;
+    float lsum = l * f;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      if (w < nw) {
-        const float f = lw[w] > 0.f ? fast_exp2(mw[w] - mx) : 0.f;
-        lsum = fmaf(lw[w], f, lsum);
-        o = fmaf(src[w * stride + 4 + c], f, o);
-      }
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+    wts[h * 32 + lane] = f;
+    if (lane == 0) {
+      part[h * kPartStride + 0] = mx;
+      part[h * kPartStride + 1] = lsum;
     }
-    os[idx] = o;                                           // ob follows os
-    if (c == 0) {
-      cml[th * 2 + 0] = mx;
-      cml[th * 2 + 1] = lsum;
-    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kHeadDim; idx += T) {
+    const int h = idx / kHeadDim, c = idx % kHeadDim;
+    const float* wh = wts + h * 32;
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) o = fmaf(wh[w], states[w * slice + h * kPartStride + 4 + c], o);
+    float o2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kBf16Warps; ++w)
+      o2 = fmaf(wh[W + w], st_bf16x[w * G * kPartStride + h * kPartStride + 4 + c], o2);
+    os[idx] = o;
+    ob[idx] = o2;
   }
   __syncthreads();
   if (!mbar_wait_bounded(vbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
-  // history partial back in the original basis, o[c] = sum_j o~[j] R_V[c][j],
-  // joined with the BF16 partial; thread (row c, quarter qq), chunk order
-  // rotated by the lane so the 32 lanes of a load hit all 32 banks
-  float* jw = cml + 4 * G;                    // [G][2] weights of the history and BF16 parts
-  if (tid < G) {
-    const float mh = cml[tid * 2], lh = cml[tid * 2 + 1], mb = cml[(G + tid) * 2], lb = cml[(G + tid) * 2 + 1];
-    const float mx = lh > 0.f ? (lb > 0.f ? fmaxf(mh, mb) : mh) : mb;
-    const float wh = lh > 0.f ? fast_exp2(mh - mx) : 0.f, wb = lb > 0.f ? fast_exp2(mb - mx) : 0.f;
-    jw[tid * 2] = wh;
-    jw[tid * 2 + 1] = wb;
-    part[tid * kPartStride + 0] = mx;
-    part[tid * kPartStride + 1] = fmaf(lh, wh, lb * wb);
-  }
-  __syncthreads();
+  // history partial back in the original basis, o[c] = sum_j o~[j] R_V[c][j]:
+  // thread (row c, quarter qq of j), a warp holding 32 consecutive rows of
+  // one quarter; chunks are visited in a lane-rotated order so that the R_V
+  // reads of 8 lanes hit 8 bank groups and the o~ reads of a warp touch one
+  // 128-byte line; the quarters are summed through shared memory (the ring,
+  // whose warp states are consumed)
+  float* red4 = reinterpret_cast<float*>(stage);   // [4][G][128]
   for (int task = tid; task < 4 * kHeadDim; task += T) {
-    const int c = task >> 2, qq = task & 3;
+    const int c = task & (kHeadDim - 1), qq = task >> 7;
     const int rot = lane & 7;
-    const float* rrow = rvs + c * kHeadDim + 32 * qq;
+    const float4* rrow = reinterpret_cast<const float4*>(rvs + c * kHeadDim + 32 * qq);
     float4 r[8];
 #pragma unroll
-    for (int k4 = 0; k4 < 8; ++k4) r[k4] = reinterpret_cast<const float4*>(rrow)[(k4 + rot) & 7];
-#pragma unroll 1
+    for (int k4 = 0; k4 < 8; ++k4) r[k4] = rrow[(k4 + rot) & 7];
+    float d[G];
+#pragma unroll
     for (int h = 0; h < G; ++h) {
       const float4* o = reinterpret_cast<const float4*>(os + h * kHeadDim + 32 * qq);
-      float d = 0.f;
+      float acc = 0.f;
 #pragma unroll
       for (int k4 = 0; k4 < 8; ++k4) {
         const float4 ov = o[(k4 + rot) & 7];
-        d = fmaf(ov.x, r[k4].x, fmaf(ov.y, r[k4].y, fmaf(ov.z, r[k4].z, fmaf(ov.w, r[k4].w, d))));
+        acc = fmaf(ov.x, r[k4].x, fmaf(ov.y, r[k4].y, fmaf(ov.z, r[k4].z, fmaf(ov.w, r[k4].w, acc))));
       }
-      d += __shfl_xor_sync(kFull, d, 1);
-      d += __shfl_xor_sync(kFull, d, 2);
-      if (qq == 0) part[h * kPartStride + 4 + c] = fmaf(jw[h * 2], d, jw[h * 2 + 1] * ob[h * kHeadDim + c]);
+      d[h] = acc;
     }
+#pragma unroll
+    for (int h = 0; h < G; ++h) red4[(qq * G + h) * kHeadDim + c] = d[h];
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kHeadDim; idx += T) {
+    const int h = idx / kHeadDim, c = idx % kHeadDim;
+    const float d = (red4[(0 * G + h) * kHeadDim + c] + red4[(1 * G + h) * kHeadDim + c]) +
+                    (red4[(2 * G + h) * kHeadDim + c] + red4[(3 * G + h) * kHeadDim + c]);
+    part[h * kPartStride + 4 + c] = d + ob[idx];
   }
 
   // ---------------- ticket: the last CTA of this (request, KV head) merges
@@ -1089,95 +1095,66 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   if (!*s_last) return;
   fence_acq_rel_gpu();
 
-  // Merge of the n_splits partials of each head.  Thread (q, head h,
-  // channel quad c4) first requests its partial outputs i = q, q + Q, ...;
-  // while they are in flight, warp h computes head h's weights, so the two
-  // dependent global reads overlap.
-  const float* pp = p.partials + int64_t(pair) * n_splits * G * kPartStride;
-  const int NP = n_splits;                            // partials per head
-  constexpr int HC = G * 32;                          // (head, channel quad) pairs
-  constexpr int Q = T / HC > 0 ? T / HC : 1;          // partial subsets
-  constexpr int kPre = 12;                            // outputs requested before the weights
-  float* linv = reinterpret_cast<float*>(stage);      // [G] 1 / L
-  float* wts = linv + G;                              // [G][2 * kMaxSplits] weights
-  float4* red = reinterpret_cast<float4*>(wts + G * 2 * kMaxSplits);   // [Q][HC]
-  const int task = tid;
-  const int hc = task % HC, q = task / HC, hh = hc / 32, c4 = hc % 32;
-  const bool merger = task < HC * Q;
-  float4 pre[kPre];
+  // Merge of the n_splits partials: warp h merges head h on its own (lane =
+  // channel quad), requesting the first kPre partial outputs together with
+  // the (m, l) pairs so that both reads share one latency.
+  if (warp < G) {
+    const int h = warp, NP = n_splits;
+    const float* pp = p.partials + int64_t(pair) * n_splits * G * kPartStride;
+    auto o_of = [&](int i) {
+      return __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i * G + h) * kPartStride + 4) + lane);
+    };
+    constexpr int kPre = 24;
+    float4 pre[kPre];
 #pragma unroll
-  for (int j = 0; j < kPre; ++j) {
-    const int i = q + j * Q;
-    pre[j] = (merger && i < NP)
-                 ? __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i * G + hh) * kPartStride + 4) + c4)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int h = warp; h < G; h += W) {
-    // (m, l) of partials lane, lane + 32, ... (NP <= 2 kMaxSplits = 8 x 32)
-    float2 ml[2 * kMaxSplits / 32];
+    for (int j = 0; j < kPre; ++j) pre[j] = j < NP ? o_of(j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // (m, l) of partials lane, lane + 32, ... (NP <= kMaxSplits = 4 x 32)
+    float2 ml[kMaxSplits / 32];
 #pragma unroll
-    for (int u = 0; u < 2 * kMaxSplits / 32; ++u) {
+    for (int u = 0; u < kMaxSplits / 32; ++u) {
       const int i = lane + 32 * u;
       ml[u] = i < NP ? __ldcg(reinterpret_cast<const float2*>(pp + int64_t(i * G + h) * kPartStride))
                      : make_float2(-INFINITY, 0.f);
     }
     float mx = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < 2 * kMaxSplits / 32; ++u)
+    for (int u = 0; u < kMaxSplits / 32; ++u)
       if (ml[u].y > 0.f) mx = fmaxf(mx, ml[u].x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     float lsum = 0.f;
+    float* wh = reinterpret_cast<float*>(stage) + h * kMaxSplits;   // [G][kMaxSplits] weights
 #pragma unroll
-    for (int u = 0; u < 2 * kMaxSplits / 32; ++u) {
-      const int i = lane + 32 * u;
+    for (int u = 0; u < kMaxSplits / 32; ++u) {
       const float f = ml[u].y > 0.f ? exp2f(ml[u].x - mx) : 0.f;
-      if (i < NP) wts[h * 2 * kMaxSplits + i] = f;
+      wh[lane + 32 * u] = f;
       lsum = fmaf(ml[u].y, f, lsum);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
-    if (lane == 0) linv[h] = lsum > 0.f ? 1.f / lsum : 0.f;
-  }
-  __syncthreads();
-  if (merger) {
-    const float* wh = wts + hh * 2 * kMaxSplits;
+    __syncwarp();
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kPre; ++j) {
-      const int i = q + j * Q;
-      const float f = i < NP ? wh[i] : 0.f;
+      const float f = wh[j];   // 0 past NP
       a.x = fmaf(f, pre[j].x, a.x);
       a.y = fmaf(f, pre[j].y, a.y);
       a.z = fmaf(f, pre[j].z, a.z);
       a.w = fmaf(f, pre[j].w, a.w);
     }
-    for (int i = q + kPre * Q; i < NP; i += Q) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i * G + hh) * kPartStride + 4) + c4);
+    for (int i = kPre; i < NP; ++i) {
+      const float4 v = o_of(i);
       const float f = wh[i];
       a.x = fmaf(f, v.x, a.x);
       a.y = fmaf(f, v.y, a.y);
       a.z = fmaf(f, v.z, a.z);
       a.w = fmaf(f, v.w, a.w);
     }
-    red[q * HC + hc] = a;
-  }
-  __syncthreads();
-  for (int i = tid; i < HC; i += T) {
-    float4 a = red[i];
-#pragma unroll
-    for (int qq = 1; qq < Q; ++qq) {
-      const float4 v = red[qq * HC + i];
-      a.x += v.x;
-      a.y += v.y;
-      a.z += v.z;
-      a.w += v.w;
-    }
-    const float s = linv[i / 32];
-    reinterpret_cast<float4*>(p.out + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim)[i] =
+    const float s = lsum > 0.f ? 1.f / lsum : 0.f;
+    reinterpret_cast<float4*>(p.out + ((int64_t(b) * p.n_kv + hkv) * G + h) * kHeadDim)[lane] =
         make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+    if (h == 0 && lane == 0) p.counters[pair] = 0u;   // ready for the next call
   }
-  if (tid == 0) p.counters[pair] = 0u;   // ready for the next call
 }
 
 template <int G>
