@@ -60,20 +60,24 @@
 #ifndef OSCAR_STAGES_G8
 #define OSCAR_STAGES_G8 8
 #endif
-#ifndef OSCAR_QK_CHAINS
-#define OSCAR_QK_CHAINS 2
+#ifndef OSCAR_QK_CHAINS_G4
+#define OSCAR_QK_CHAINS_G4 2
+#endif
+#ifndef OSCAR_QK_CHAINS_G8
+#define OSCAR_QK_CHAINS_G8 1
 #endif
 // INT2 pages a warp processes per step (one online-softmax update per step)
-#ifndef OSCAR_GROUP
-#define OSCAR_GROUP 2
+// for GQA 4 / GQA 8
+#ifndef OSCAR_GROUP_G4
+#define OSCAR_GROUP_G4 4
+#endif
+#ifndef OSCAR_GROUP_G8
+#define OSCAR_GROUP_G8 3
 #endif
 
 namespace oscar {
 namespace {
 
-constexpr int kQkChains = OSCAR_QK_CHAINS;
-constexpr int kGroup = OSCAR_GROUP;
-static_assert(kGroup == 1 || kGroup == 2, "pages per step");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
@@ -92,6 +96,9 @@ struct Geo {
   // the last kBf16Warps warps scan the BF16 tokens while the others build q~
   static constexpr int PT = (W - kBf16Warps) * 32;
   static constexpr int kStages = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;   // ring stages per warp
+  static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : OSCAR_GROUP_G8;      // pages per step
+  static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
+  static_assert(kGroup >= 1 && kGroup < kStages, "a step leaves copies in flight");
   static constexpr size_t kStageBytes = size_t(W) * kStages * kBlockBytes;
   // ring barriers + the R_K and R_V barriers, padded so the region after it
   // stays 128-byte aligned (TMA destinations need at least 16)
@@ -257,7 +264,7 @@ struct HistState {
 template <int G>
 __device__ __forceinline__ void int2_qk(const uint8_t* __restrict__ pg, int gid, int tig,
                                         const uint32_t (&qb)[Geo<G>::NH][8][2], float (&d)[Geo<G>::NH][4]) {
-  constexpr int NH = Geo<G>::NH;
+  constexpr int NH = Geo<G>::NH, kQkChains = Geo<G>::kQkChains;
   const uint2 kw0 = *reinterpret_cast<const uint2*>(pg + 32 * gid + 8 * tig);
   const uint2 kw1 = *reinterpret_cast<const uint2*>(pg + 32 * (gid + 8) + 8 * tig);
   float dc[kQkChains][NH][4];
@@ -627,27 +634,28 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
     }
   }
   named_barrier(kPrologueBarrier, T);
+  // sigma = 2^e of head h, max|q~ sigma| in [2^13, 2^14): e from the exponent
+  // field of the head's maximum (the frexp exponent is that field - 126)
+  auto sigma_exp = [&](int h) {
+    const float mx = fmaxf(fmaxf(red[h * 4], red[h * 4 + 1]), fmaxf(red[h * 4 + 2], red[h * 4 + 3]));
+    const int e = mx > 0.f ? 14 - (((__float_as_int(mx) >> 23) & 255) - 126) : 0;
+    return max(-100, min(100, e));
+  };
   if (tid < G) {
-    const float mx = fmaxf(fmaxf(red[tid * 4], red[tid * 4 + 1]), fmaxf(red[tid * 4 + 2], red[tid * 4 + 3]));
     const float sm = ((red[4 * G + tid * 4] + red[4 * G + tid * 4 + 1]) + red[4 * G + tid * 4 + 2]) +
                      red[4 * G + tid * 4 + 3];
-    int e = 0;
-    if (mx > 0.f) {
-      frexpf(mx, &e);              // mx in [2^(e-1), 2^e)
-      e = max(-100, min(100, 14 - e));
-    }
+    const int e = sigma_exp(tid);
     const float scale = kLog2e * rsqrtf(float(kHeadDim));
-    aux[tid * 4 + 0] = ldexpf(1.f, e);
-    aux[tid * 4 + 1] = ldexpf(1.f, 24 - e) * scale;   // 2^24 / sigma * log2(e) / sqrt(d)
+    aux[tid * 4 + 0] = __int_as_float((127 + e) << 23);
+    aux[tid * 4 + 1] = __int_as_float((151 - e) << 23) * scale;   // 2^24 / sigma * log2(e) / sqrt(d)
     aux[tid * 4 + 2] = sm * scale;
   }
-  named_barrier(kPrologueBarrier, T);
   for (int idx = tid; idx < 32 * NH * 16; idx += T) {
     const int ln = idx / (NH * 16), rem = idx % (NH * 16);
     const int nt = rem / 16, j = (rem / 2) % 8, rr = rem % 2;
     const int gid = ln >> 2, tig = ln & 3;
     const int h = 4 * nt + gid / 2;
-    const float f = aux[h * 4] * __int_as_float((127 - 2 * code_pos(j)) << 23);   // sigma 4^-pos(j)
+    const float f = __int_as_float((127 + sigma_exp(h) - 2 * code_pos(j)) << 23);   // sigma 4^-pos(j)
     const int c0 = 32 * tig + 16 * rr + j;
     float v0 = qt[h * kHeadDim + c0] * f, v1 = qt[h * kHeadDim + c0 + 8] * f;
     if (gid & 1) {
@@ -904,6 +912,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   float* my_state = reinterpret_cast<float*>(ring);
   constexpr int kStateFloats = G * kPartStride;
 
+  constexpr int kGroup = Geo<G>::kGroup;
   // ---------------- INT2 pages, kGroup per step: QK of the step's pages,
   // one maximum update, then their probabilities and PV.  A page past the
   // warp's range or with an invalid id is computed on stale ring data with
