@@ -925,37 +925,58 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     int s_cur = 0;                 // ring stage of page k
     uint32_t phase = 0u;           // parity of page k's stage
     int tok_left = hist - first * kPage;   // history tokens from page k on
+    constexpr uint32_t kGroupBits = (1u << kGroup) - 1u, kRingBits = (1u << kStages) - 1u;
+    // page id of the first in-loop copy of lane u < kGroup (page kStages + u)
+    int pid_next = lane < kGroup && kStages + lane < count ? __ldg(ptab + first + (kStages + lane) * W) : -1;
     for (; k < count; k += kGroup) {
       const uint8_t* pg[kGroup];
-      bool ok[kGroup][2];
-      bool all_full = true;        // warp-uniform
+      // the step is full (warp-uniform) when its kGroup pages are in range,
+      // were copied, and hold kPage valid tokens each
+      uint32_t gmask = kGroupBits << s_cur;
+      gmask = (gmask | (gmask >> kStages)) & kRingBits;
+      const bool all_full = k + kGroup <= count && (stage_ok & gmask) == gmask &&
+                            tok_left - (kGroup - 1) * W * kPage >= kPage;
       int s_u = s_cur;
       uint32_t ph_u = phase;
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
-        const bool in = k + u < count;
         pg[u] = ring + s_u * kBlockBytes;
-        if (in && !mbar_wait_bounded(bar + s_u, ph_u, kWaitLimitNs)) timed_out = true;
-        const bool valid = in && ((stage_ok >> s_u) & 1u);
-        if (in && !valid && lane == 0) flag(p.dev_status, 0x1);
-        const int ntok = valid ? tok_left - u * W * kPage : 0;
-        all_full = all_full && ntok >= kPage;
-        ok[u][0] = gid < ntok;
-        ok[u][1] = gid + 8 < ntok;
+        if ((u == 0 || k + u < count) && !mbar_wait_bounded(bar + s_u, ph_u, kWaitLimitNs)) timed_out = true;
         if (++s_u == kStages) {
           s_u = 0;
           ph_u ^= 1u;
         }
       }
       if (timed_out) break;
+      // token validity of the lane's two tokens per page (masked steps only)
+      bool ok[kGroup][2];
+      if (!all_full) {
+        s_u = s_cur;
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          const bool in = k + u < count;
+          const bool valid = in && ((stage_ok >> s_u) & 1u);
+          if (in && !valid && lane == 0) flag(p.dev_status, 0x1);
+          const int ntok = valid ? tok_left - u * W * kPage : 0;
+          ok[u][0] = gid < ntok;
+          ok[u][1] = gid + 8 < ntok;
+          if (++s_u == kStages) s_u = 0;
+        }
+      }
       // QK of the step's pages, one maximum update, probabilities and PV;
       // steps whose tokens are all valid (every step but the history's last
-      // and a warp's odd tail page) take the select-free variant
+      // and a warp's tail) take the select-free variant; in the other, pages
+      // past the warp's range are skipped (warp-uniform branches)
       auto step = [&](auto masked) {
         constexpr bool kMasked = decltype(masked)::value;
         float sc[kGroup][NH][2];
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
+          if (kMasked && u > 0 && k + u >= count) {
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) sc[u][nt][0] = sc[u][nt][1] = -INFINITY;
+            continue;
+          }
           float d[NH][4];
           int2_qk<G>(pg[u], gid, tig, qb, d);
           const uint32_t ksz0 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * gid);
@@ -965,6 +986,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
         int2_update_max<G, kGroup>(sc, st);
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
+          if (kMasked && u > 0 && k + u >= count) continue;
           const uint32_t vsz0 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * gid);
           const uint32_t vsz1 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * (gid + 8));
           uint32_t pb[NH][2];
@@ -978,11 +1000,35 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
         step(std::true_type{});
       }
       __syncwarp();
-#pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        if (k + u + kStages < count) issue(k + u + kStages, s_cur);
-        if (++s_cur == kStages) {
-          s_cur = 0;
+      // the freed stages take pages k + kStages + u: lane u < kGroup starts
+      // the copy of page u (ids requested one step ahead), so the kGroup
+      // copies cost one pass of issue instructions
+      {
+        const int kk = k + kStages + lane;
+        const bool want = lane < kGroup && kk < count;
+        const int pid = pid_next;
+        pid_next = lane < kGroup && kk + kGroup < count ? __ldg(ptab + first + (kk + kGroup) * W) : -1;
+        const bool good = want && pid >= 0 && pid < p.n_pages;
+        int s = s_cur + lane;
+        if (s >= kStages) s -= kStages;
+        if (want) {
+          if (!good) {
+            mbar_arrive(bar + s);   // no copy: complete the phase without bytes
+          } else {
+            mbar_arrive_expect_tx(bar + s, kBlockBytes);
+            bulk_copy_g2s(ring + s * kBlockBytes, pool + int64_t(pid) * page_stride, kBlockBytes, bar + s);
+          }
+        }
+        const uint32_t want_bits = __ballot_sync(kFull, want) & kGroupBits;
+        const uint32_t good_bits = __ballot_sync(kFull, good) & kGroupBits;
+        auto to_stages = [&](uint32_t bits) {
+          const uint32_t r = bits << s_cur;
+          return (r | (r >> kStages)) & kRingBits;
+        };
+        stage_ok = (stage_ok & ~to_stages(want_bits)) | to_stages(good_bits);
+        s_cur += kGroup;
+        if (s_cur >= kStages) {
+          s_cur -= kStages;
           phase ^= 1u;
         }
       }
