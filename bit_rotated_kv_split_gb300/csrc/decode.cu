@@ -1139,38 +1139,45 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
     part[h * kPartStride + 4 + c] = d + ob[idx];
   }
 
-  // ---------------- ticket: the last CTA of this (request, KV head) merges
+  // ---------------- ticket: the last CTA of this (request, KV head) merges.
+  // The barrier orders the CTA's partial writes before thread 0's
+  // acquire-release add, which publishes them; in the last CTA the same add
+  // acquires the other CTAs' partials, and the barrier after it extends
+  // that to the merging warps.
   __syncthreads();
   if (tid == 0) {
-    fence_acq_rel_gpu();
-    const unsigned t = atomicAdd(p.counters + pair, 1u);
+    const unsigned t = atom_add_acq_rel_gpu(p.counters + pair, 1u);
     *s_last = (t == unsigned(n_splits - 1)) ? 1 : 0;
   }
   __syncthreads();
-  if (!*s_last) return;
-  fence_acq_rel_gpu();
+  if (!*s_last || warp >= G) return;
 
   // Merge of the n_splits partials: warp h merges head h on its own (lane =
-  // channel quad), requesting the first kPre partial outputs together with
-  // the (m, l) pairs so that both reads share one latency.
-  if (warp < G) {
+  // channel quad).  The first kPre partial outputs and the (m, l) pairs are
+  // requested back to back, so that all of them share one latency.
+  {
     const int h = warp, NP = n_splits;
     const float* pp = p.partials + int64_t(pair) * n_splits * G * kPartStride;
-    auto o_of = [&](int i) {
-      return __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i * G + h) * kPartStride + 4) + lane);
-    };
+    // the outputs first: the weights wait on the (m, l) loads issued last,
+    // by which time every load of the batch is in flight
     constexpr int kPre = 24;
     float4 pre[kPre];
 #pragma unroll
-    for (int j = 0; j < kPre; ++j) pre[j] = j < NP ? o_of(j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < kPre; ++j) {
+      pre[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      ld_cg_if(pre[j], pp + int64_t(j * G + h) * kPartStride + 4 + 4 * lane, j < NP);
+    }
     // (m, l) of partials lane, lane + 32, ... (NP <= kMaxSplits = 4 x 32)
     float2 ml[kMaxSplits / 32];
 #pragma unroll
     for (int u = 0; u < kMaxSplits / 32; ++u) {
       const int i = lane + 32 * u;
-      ml[u] = i < NP ? __ldcg(reinterpret_cast<const float2*>(pp + int64_t(i * G + h) * kPartStride))
-                     : make_float2(-INFINITY, 0.f);
+      ml[u] = make_float2(-INFINITY, 0.f);
+      ld_cg_if(ml[u], pp + int64_t(i * G + h) * kPartStride, i < NP);
     }
+    auto o_of = [&](int i) {
+      return __ldcg(reinterpret_cast<const float4*>(pp + int64_t(i * G + h) * kPartStride + 4) + lane);
+    };
     float mx = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kMaxSplits / 32; ++u)

@@ -88,6 +88,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Atomic add with acquire-release semantics at GPU scope (returns the old
+// value): publishes what happened before it in this CTA (barrier included)
+// and makes visible what other CTAs published before their own add.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// L2 loads issued in program order (volatile), each only when `ok` (the
+// destination keeps its value otherwise): a batch of them shares one
+// latency instead of being reordered behind the first use.
+__device__ __forceinline__ void ld_cg_if(float4& v, const float* p, bool ok) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t@q ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w)
+      : "l"(p), "r"(int(ok))
+      : "memory");
+}
+__device__ __forceinline__ void ld_cg_if(float2& v, const float* p, bool ok) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t@q ld.global.cg.v2.f32 {%0, %1}, [%2];\n\t}"
+               : "+f"(v.x), "+f"(v.y)
+               : "l"(p), "r"(int(ok))
+               : "memory");
+}
+
 // Release/acquire fence at GPU scope (publishes this CTA's prior writes when
 // issued after a CTA barrier, as in the standard "last block" pattern).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
