@@ -8,9 +8,14 @@
 // 2.2 B (paged cache).
 //
 // One CTA per (KV head, K|V, group of 4 items): the head's rotation R (64 KB)
-// is staged into shared memory by one TMA bulk copy, then each warp demotes
-// one item: lane l owns rotated channels 4l..4l+3 (one code byte),
-// x~_j = sum_i x_i R[i][j] in fp32 with i ascending, read from shared memory.
+// is staged into shared memory by four TMA bulk copies (one barrier per
+// quarter of its rows), then the CTA demotes its items one after another,
+// all four warps on each: warp w sums the inputs i in [32 w, 32 w + 32)
+// for every output, lane l owning rotated channels 4l..4l+3 (one code
+// byte); the four partial sums meet in shared memory, and warp 0 clips,
+// quantises and packs.  Splitting the inputs over the warps shortens the
+// dependent chain of a lone item (a decode step demotes one token per
+// request) from 128 to 32 steps.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -18,126 +23,150 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kItems = 4;                    // items per CTA
 constexpr uint32_t kRotBytes = kHeadDim * kHeadDim * 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr size_t kSmem = kRotBytes + 16;
+constexpr size_t kRedBytes = size_t(kWarps) * kHeadDim * 4;   // partial sums of one item
+constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
 
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   float* rs = reinterpret_cast<float*>(smem);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kRotBytes);
+  float* red = reinterpret_cast<float*>(smem + kRotBytes);       // [kWarps][128]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kRotBytes + kRedBytes);   // [4] R quarters
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int which = int(blockIdx.y & 1);     // 0 = K, 1 = V
   const int head = int(blockIdx.y >> 1);
-  const int item = int(blockIdx.x) * kWarps + warp;
   const float* rg = (which ? p.r_v : p.r_k) + int64_t(head) * kHeadDim * kHeadDim;
   if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+    for (int c = 0; c < 4; ++c) mbar_init(bar + c, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, kRotBytes);
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      bulk_copy_g2s(smem + c * (kRotBytes / 4), rg + c * (kRotBytes / 16), kRotBytes / 4, bar);
+    for (int c = 0; c < 4; ++c) {
+      mbar_arrive_expect_tx(bar + c, kRotBytes / 4);
+      bulk_copy_g2s(smem + c * (kRotBytes / 4), rg + c * (kRotBytes / 16), kRotBytes / 4, bar + c);
+    }
   }
   __syncthreads();
 
-  // indices first, then the source row and the destination page (two
-  // levels of independent loads, overlapping the R transfer)
-  bool live = item < p.n;
-  int64_t row = 0;
-  int bq = 0, pos = 0;
-  if (live) {
-    row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
-    bq = p.dst_req[item];
-    pos = p.dst_pos[item];
+  // every warp reads the items' indices and its quarter of each source row
+  // (two levels of independent loads, overlapping the R transfer)
+  const int item0 = int(blockIdx.x) * kItems;
+  bool live[kItems];
+  int64_t page[kItems];
+  int slot[kItems];
+  float xv[kItems];            // x_i, i = 32 warp + lane
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int item = item0 + it;
+    live[it] = item < p.n;
+    page[it] = -1;
+    slot[it] = 0;
+    xv[it] = 0.f;
+    if (!live[it]) continue;
+    const int64_t row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
+    const int bq = p.dst_req[item], pos = p.dst_pos[item];
     if (row < 0 || row >= p.src_rows || bq < 0 || bq >= p.batch || pos < 0 || pos / kPage >= p.max_pages) {
-      if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x2);
-      live = false;
+      if (warp == 0 && lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x2);
+      live[it] = false;
+      continue;
+    }
+    const uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
+    xv[it] = bf16_lo(uint32_t(src[32 * warp + lane]));
+    page[it] = p.page_table[int64_t(bq) * p.max_pages + pos / kPage];
+    slot[it] = pos % kPage;
+  }
+  // the source rows may be overwritten by the new tokens only after every
+  // warp has read its part of them
+  __syncthreads();
+  const uint16_t* fresh = which ? p.new_v : p.new_k;
+  if (fresh) {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+      if (!live[it]) continue;
+      const int item = item0 + it;
+      const int64_t row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
+      uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
+      src[32 * warp + lane] = fresh[(int64_t(item) * p.n_kv + head) * kHeadDim + 32 * warp + lane];
     }
   }
-  uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
-  float xv[4] = {0.f, 0.f, 0.f, 0.f};
-  int64_t page = -1;
-  if (live) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-    page = p.page_table[int64_t(bq) * p.max_pages + pos / kPage];
-    xv[0] = bf16_lo(raw.x);
-    xv[1] = bf16_hi(raw.x);
-    xv[2] = bf16_lo(raw.y);
-    xv[3] = bf16_hi(raw.y);
-  }
-  // the source row may be overwritten by the new token only after every
-  // lane has read it
-  __syncwarp();
-  const uint16_t* fresh = which ? p.new_v : p.new_k;
-  if (live && fresh) {
-    const uint2 nw = *reinterpret_cast<const uint2*>(
-        fresh + (int64_t(item) * p.n_kv + head) * kHeadDim + 4 * lane);
-    *reinterpret_cast<uint2*>(src + 4 * lane) = nw;
-  }
 
-  const bool ready = mbar_wait_bounded(bar, 0, kWaitLimitNs);
-  if (!ready) {
+  // warp w needs the rows 32 w .. 32 w + 31 of R: quarter w of the copy;
+  // on an expired wait the whole CTA leaves (after waiting, bounded, for
+  // the other quarters so that no copy lands after exit)
+  if (!__syncthreads_and(mbar_wait_bounded(bar + warp, 0, kWaitLimitNs))) {
     if (threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, 0x4);
+    for (int c = 0; c < 4; ++c) mbar_wait_bounded(bar + c, 0, kWaitLimitNs);
     return;
   }
-  if (!live) return;
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
-  const float4* r4 = reinterpret_cast<const float4*>(rs) + lane;
-#pragma unroll 8
-  for (int i = 0; i < kHeadDim; ++i) {
-    const float xi = __shfl_sync(0xffffffffu, xv[i & 3], i >> 2);
-    const float4 rr = r4[i * (kHeadDim / 4)];
-    a[0] = fmaf(xi, rr.x, a[0]);
-    a[1] = fmaf(xi, rr.y, a[1]);
-    a[2] = fmaf(xi, rr.z, a[2]);
-    a[3] = fmaf(xi, rr.w, a[3]);
-  }
-
   const float tau = which ? p.tau_v : p.tau_k;
-  float mn = INFINITY, mx = -INFINITY;
+  const float4* r4 = reinterpret_cast<const float4*>(rs) + lane;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    a[c] = fminf(fmaxf(a[c], -tau), tau);
-    mn = fminf(mn, a[c]);
-    mx = fmaxf(mx, a[c]);
-  }
+  for (int it = 0; it < kItems; ++it) {
+    if (!__syncthreads_or(live[it])) continue;   // uniform over the CTA
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const int i = 32 * warp + k;
+      const float xi = __shfl_sync(0xffffffffu, xv[it], k);
+      const float4 rr = r4[i * (kHeadDim / 4)];
+      a[0] = fmaf(xi, rr.x, a[0]);
+      a[1] = fmaf(xi, rr.y, a[1]);
+      a[2] = fmaf(xi, rr.z, a[2]);
+      a[3] = fmaf(xi, rr.w, a[3]);
+    }
+    *reinterpret_cast<float4*>(red + warp * kHeadDim + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
+    __syncthreads();
+    if (warp == 0 && live[it]) {
+      float v[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
-  const __half z16 = __float2half_rn(mn);
-  const float s = __half2float(s16);
-  const float z = __half2float(z16);
-  uint32_t byte = 0;
+      for (int c = 0; c < 4; ++c)
+        v[c] = (red[4 * lane + c] + red[kHeadDim + 4 * lane + c]) +
+               (red[2 * kHeadDim + 4 * lane + c] + red[3 * kHeadDim + 4 * lane + c]);
+      float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float code = 0.f;
-    if (s > 0.f) code = fminf(fmaxf(rintf(__fdiv_rn(a[c] - z, s)), 0.f), 3.f);
-    byte |= uint32_t(code) << (2 * c);
-  }
-
-  if (page < 0 || page >= p.n_pages) {
-    if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
-    return;
-  }
-  uint8_t* blk = p.pages + (page * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
-  const int slot = pos % kPage;
-  blk[32 * slot + lane] = uint8_t(byte);
-  if (lane == 0) {
-    __half2 sz = __halves2half2(s16, z16);
-    *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * slot) = sz;
+      for (int c = 0; c < 4; ++c) {
+        v[c] = fminf(fmaxf(v[c], -tau), tau);
+        mn = fminf(mn, v[c]);
+        mx = fmaxf(mx, v[c]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
+      const __half z16 = __float2half_rn(mn);
+      const float s = __half2float(s16);
+      const float z = __half2float(z16);
+      uint32_t byte = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float code = 0.f;
+        if (s > 0.f) code = fminf(fmaxf(rintf(__fdiv_rn(v[c] - z, s)), 0.f), 3.f);
+        byte |= uint32_t(code) << (2 * c);
+      }
+      if (page[it] < 0 || page[it] >= p.n_pages) {
+        if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
+      } else {
+        uint8_t* blk = p.pages + (page[it] * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
+        blk[32 * slot[it] + lane] = uint8_t(byte);
+        if (lane == 0) {
+          __half2 sz = __halves2half2(s16, z16);
+          *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * slot[it]) = sz;
+        }
+      }
+    }
+    __syncthreads();   // red is reused by the next item
   }
 }
 
 }  // namespace
 
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream) {
-  const int64_t chunks = (int64_t(p.n) + kWarps - 1) / kWarps;
+  const int64_t chunks = (int64_t(p.n) + kItems - 1) / kItems;
   if (chunks == 0) return cudaSuccess;
   if (chunks > 0x7fffffff || int64_t(p.n_kv) * 2 > 65535) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(demote_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
