@@ -43,6 +43,8 @@
 #include <cfloat>
 #include <type_traits>
 
+#include <cudaTypedefs.h>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -103,13 +105,14 @@ struct Geo {
   // ring barriers + the R_K and R_V barriers, padded so the region after it
   // stays 128-byte aligned (TMA destinations need at least 16)
   static constexpr size_t kBarBytes = ((size_t(W) * kStages + 3) * 8 + 127) / 128 * 128;
-  static constexpr size_t kStateBytes = size_t(W) * G * kPartStride * 4;   // per partial type
   // prologue: R_K (64 KB) and the q~ scratch; epilogue: two warp-state sets
   static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
   static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G + 32 * NH * 16) * 4;
   static constexpr size_t kUnion = kRotBytes + kQScratch;   // R_K then R_V | q~ scratch
   static constexpr size_t kBf16State = size_t(kBf16Warps) * G * kPartStride * 4;
-  static constexpr size_t kSmem = kStageBytes + kBarBytes + kUnion + kBf16State + 16;
+  // (+1 KB: the union starts at the next 1024-byte boundary, which the
+  // swizzled R_V boxes need)
+  static constexpr size_t kSmem = kStageBytes + kBarBytes + 1024 + kUnion + kBf16State + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   // each warp's ring slice holds its two warp states at the end
@@ -589,6 +592,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
                              float* scratch) {
   constexpr int T = Geo<G>::PT, NH = Geo<G>::NH;
   using S = QScratch<G>;
+  static_assert(S::kFloats * 4 <= Geo<G>::kQScratch, "prologue scratch");
   float* qs = scratch + S::kQs;
   float* part = scratch + S::kPart;
   float* qt = scratch + S::kQt;
@@ -686,7 +690,7 @@ struct PidWindow {
 // ------------------------------------------------------------------ split kernel
 
 template <int G>
-__global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NTQ = Geo<G>::NTQ, W = Geo<G>::W, T = Geo<G>::T;
   constexpr int kStages = Geo<G>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -694,6 +698,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<G>::kStageBytes);
   uint64_t* rbar = bars + W * kStages;       // R_K, then (last CTA) R_V
   uint8_t* uni = smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes;
+  uni += (1024u - (smem_addr(uni) & 1023u)) & 1023u;
   float* rks = reinterpret_cast<float*>(uni);                         // prologue only
   float* qscratch = reinterpret_cast<float*>(uni + Geo<G>::kRotBytes);
   float* st_bf16x = reinterpret_cast<float*>(uni + Geo<G>::kUnion);   // [kBf16Warps][G][kPartStride]
@@ -833,15 +838,15 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
       if (!mbar_wait_bounded(rbar, 0, kWaitLimitNs)) flag(p.dev_status, 0x4);
     }
     named_barrier(kPrologueBarrier, PT);   // prologue reads of R_K are done
-    // R_V -> shared memory (replacing R_K) for this CTA's output rotation
+    // R_V -> shared memory (replacing R_K) for this CTA's output rotation:
+    // box qq = columns 32 qq .. 32 qq + 31 of all 128 rows, 16-byte chunks
+    // of row c swizzled to chunk ^ (c & 7)
     if (tid == 0) {
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(vbar, uint32_t(Geo<G>::kRotBytes));
-      const float* rv = p.r_v + int64_t(hkv) * kHeadDim * kHeadDim;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        bulk_copy_g2s(rvs + c * (kHeadDim * kHeadDim / 4), rv + c * (kHeadDim * kHeadDim / 4),
-                      uint32_t(Geo<G>::kRotBytes / 4), vbar);
+      for (int qq = 0; qq < 4; ++qq)
+        tma_load_2d(rvs + qq * (kHeadDim * kHeadDim / 4), &p.tm_rv, 32 * qq, hkv * kHeadDim, vbar);
       mbar_arrive(pro_done);
     }
   } else {
@@ -910,7 +915,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   }
   // each warp's INT2 state goes into its own ring slice once its pages are done
   float* my_state = reinterpret_cast<float*>(ring);
-  constexpr int kStateFloats = G * kPartStride;
 
   constexpr int kGroup = Geo<G>::kGroup;
   // ---------------- INT2 pages, kGroup per step: QK of the step's pages,
@@ -1104,18 +1108,17 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
   if (!mbar_wait_bounded(vbar, 0, kWaitLimitNs) && tid == 0) flag(p.dev_status, 0x4);
   // history partial back in the original basis, o[c] = sum_j o~[j] R_V[c][j]:
   // thread (row c, quarter qq of j), a warp holding 32 consecutive rows of
-  // one quarter; chunks are visited in a lane-rotated order so that the R_V
-  // reads of 8 lanes hit 8 bank groups and the o~ reads of a warp touch one
-  // 128-byte line; the quarters are summed through shared memory (the ring,
-  // whose warp states are consumed)
+  // one quarter; the swizzled boxes put chunk k4 of 8 consecutive rows in 8
+  // bank groups while every lane reads the same o~ chunk (a broadcast); the
+  // quarters are summed through shared memory (the ring, whose warp states
+  // are consumed)
   float* red4 = reinterpret_cast<float*>(stage);   // [4][G][128]
   for (int task = tid; task < 4 * kHeadDim; task += T) {
     const int c = task & (kHeadDim - 1), qq = task >> 7;
-    const int rot = lane & 7;
-    const float4* rrow = reinterpret_cast<const float4*>(rvs + c * kHeadDim + 32 * qq);
+    const float4* rrow = reinterpret_cast<const float4*>(rvs + qq * (kHeadDim * kHeadDim / 4)) + 8 * c;
     float4 r[8];
 #pragma unroll
-    for (int k4 = 0; k4 < 8; ++k4) r[k4] = rrow[(k4 + rot) & 7];
+    for (int k4 = 0; k4 < 8; ++k4) r[k4] = rrow[k4 ^ (c & 7)];
     float d[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -1123,7 +1126,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(DecodeParams p) {
       float acc = 0.f;
 #pragma unroll
       for (int k4 = 0; k4 < 8; ++k4) {
-        const float4 ov = o[(k4 + rot) & 7];
+        const float4 ov = o[k4];
         acc = fmaf(ov.x, r[k4].x, fmaf(ov.y, r[k4].y, fmaf(ov.z, r[k4].z, fmaf(ov.w, r[k4].w, acc))));
       }
       d[h] = acc;
@@ -1241,6 +1244,26 @@ cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
+
+bool encode_rv_map(DecodeParams* p) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), cuuint64_t(p->n_kv) * kHeadDim};
+  const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 4};
+  const cuuint32_t box[2] = {32, cuuint32_t(kHeadDim)};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(&p->tm_rv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p->r_v), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, int max_hist,
                 DecodePlan* plan, cudaError_t* err) {

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace oscar {
@@ -99,7 +100,13 @@ struct DecodeParams {
   int32_t n_splits, pages_per_split;
   // scale of the PV B operand (power of two) and 2^24 / sigma_v
   float sigma_v, pv_unscale;
+  // R_V as a 2-D tensor (128 columns x n_kv * 128 rows of fp32) read in
+  // boxes of 32 columns x 128 rows with the 128-byte swizzle
+  CUtensorMap tm_rv;
 };
+
+// Fills p->tm_rv for p->r_v and p->n_kv; false if the driver refuses.
+bool encode_rv_map(DecodeParams* p);
 
 struct DecodePlan {
   int32_t n_splits, pages_per_split;

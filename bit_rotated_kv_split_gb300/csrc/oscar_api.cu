@@ -166,6 +166,7 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   const int sig_exp = 14 - e;
   p.sigma_v = std::ldexp(1.0f, sig_exp);
   p.pv_unscale = std::ldexp(1.0f, 24 - sig_exp);
+  if (!oscar::encode_rv_map(&p)) return OSCAR_ERR_CUDA;
   err = oscar::launch_decode(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }

@@ -34,6 +34,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 // Global -> shared bulk copy through the TMA engine; completion is counted
 // in bytes on `bar`.  dst, src 16-byte aligned, bytes a multiple of 16.
+// 2-D tiled TMA load of the box at element coordinates (x, y) of the tensor
+// map (a __grid_constant__ parameter) into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
                                               uint64_t* bar) {
   asm volatile(
