@@ -74,6 +74,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD["workload"],
                     choices=[WORKLOAD["workload"]] + sorted(EXTRA_WORKLOADS))
+    ap.add_argument("--rotation", default="oscar", choices=["oscar", "canalized32"],
+                    help="R_K/R_V of the default workload: the OSCAR eigenbasis rotation, or the OScaR "
+                         "block-diagonal one (Hadamard groups of 32 channels)")
     return ap.parse_args()
 
 
@@ -306,8 +309,9 @@ def _roofline_peak():
         return 6800.0, "fallback"
 
 
-def rotations_from_library(B):
-    """Per-head R_K, R_V and per-layer taus, built by the library's host routines."""
+def rotations_from_library(B, kind="oscar"):
+    """Per-head R_K, R_V and per-layer taus, built by the library's host routines
+    (kind "canalized32": the OScaR block-diagonal rotation for K and V)."""
     import numpy as np
     import synth
     w = WORKLOAD
@@ -316,8 +320,12 @@ def rotations_from_library(B):
     rk, rv, ck, cv = [], [], [], []
     for hh in range(n_kv):
         cal = synth.calibration_set(seed, 0, hh, outl[hh], n_q=4096, n_k=2048)
-        rk.append(B.oscar_build_rotation(cal["q"])[0])
-        rv.append(B.oscar_build_rotation(B.oscar_score_weighted_rows(cal["q"], cal["k"], cal["v"]))[0])
+        if kind == "canalized32":
+            rk.append(B.oscar_build_canalized_rotation(w["head_dim"], 32))
+            rv.append(B.oscar_build_canalized_rotation(w["head_dim"], 32))
+        else:
+            rk.append(B.oscar_build_rotation(cal["q"])[0])
+            rv.append(B.oscar_build_rotation(B.oscar_score_weighted_rows(cal["q"], cal["k"], cal["v"]))[0])
         ck.append(cal["k"])
         cv.append(cal["v"])
     rk32 = np.stack(rk).astype(np.float32)
@@ -393,7 +401,7 @@ def run_gpu(args):
     bsz, n_kv = w["batch"], w["n_kv_heads"]
     s, h, r = _split(w["ctx"])
 
-    rot = rotations_from_library(B)
+    rot = rotations_from_library(B, args.rotation)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     layer0 = build_layer(torch, B, dev, rot)
     per_layer = layer0.pages.numel() + 4 * (layer0.sink_k.numel() + layer0.recent_k.numel())
@@ -566,7 +574,7 @@ def run_gpu(args):
             "config": _config_json({"l2_policy": "inputs larger than L2: %d rotating layer caches of %.1f MB "
                                                  "(%.0f MB > 3x L2 %.0f MB)" % (n_copies, per_layer / 1e6,
                                                                                 n_copies * per_layer / 1e6, l2 / 1e6),
-                                    "cuda_graphs": use_graphs}),
+                                    "cuda_graphs": use_graphs, "rotation": args.rotation}),
             "decode_ms": decode_ms, "demote_ms": demote_ms,
             "hbm_gbs_decode": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -49,6 +49,7 @@ def _load():
         "oscar_status_string": (ctypes.c_char_p, [c_int32]),
         "oscar_abi_version": (c_int32, []),
         "oscar_build_rotation": (c_int32, [P, c_int64, c_int32, P, P]),
+        "oscar_build_canalized_rotation": (c_int32, [c_int32, c_int32, P]),
         "oscar_score_weighted_rows": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_double, P]),
         "oscar_clip_threshold": (c_int32, [P, c_int64, c_int32, c_int32, P, c_double, P]),
         "oscar_quantize_append": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
@@ -107,6 +108,13 @@ def oscar_build_rotation(x: np.ndarray):
     w = np.empty(d, dtype=np.float64)
     _check("oscar_build_rotation", lib.oscar_build_rotation(x.ctypes.data, n, d, r.ctypes.data, w.ctypes.data))
     return r, w
+
+
+def oscar_build_canalized_rotation(d: int, block: int):
+    """Block-diagonal OScaR rotation R [d][d] (host float64)."""
+    r = np.empty((d, d), dtype=np.float64)
+    _check("oscar_build_canalized_rotation", lib.oscar_build_canalized_rotation(d, block, r.ctypes.data))
+    return r
 
 
 def oscar_score_weighted_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float = None):

@@ -196,3 +196,21 @@ extern "C" oscar_status oscar_clip_threshold(const double* acts, int64_t rows, i
   *tau_out = mags[size_t(rank - 1)];
   return OSCAR_OK;
 }
+
+// OScaR variant ([CSDN] section 四.2): channels split into groups of `block`,
+// each rotated by the orthonormal Sylvester Hadamard of that size.
+extern "C" oscar_status oscar_build_canalized_rotation(int32_t d, int32_t block, double* r_out) {
+  if (!r_out || d < 1 || d > 1024 || !is_pow2(d) || block < 1 || block > d || !is_pow2(block))
+    return OSCAR_ERR_INVALID_ARG;
+  const double inv = 1.0 / std::sqrt(double(block));
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) {
+      double v = 0.0;
+      if (i / block == j / block) {
+        const int a = i % block, b = j % block;
+        v = (__builtin_popcount(unsigned(a & b)) & 1) ? -inv : inv;
+      }
+      r_out[size_t(i) * d + j] = v;
+    }
+  return OSCAR_OK;
+}

@@ -130,6 +130,20 @@ oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t d,
                                   double* r_out, double* eigvals_out);
 
 /*
+ * oscar_build_canalized_rotation - the block-diagonal rotation of the OScaR
+ * variant.  [CSDN] section 四.2 (channels split into groups, each rotated
+ * within the group; no inversion, no iteration).
+ *
+ *   r_out (host, [d][d] row-major, float64) = I_(d/block) (x) H_block, with
+ *   H_block the orthonormal Sylvester Hadamard of size block.  The variant's
+ *   per-token scaling is carried by the per-token (scale, zero) of this
+ *   codec, so the rotation is the whole difference; the demotion and decode
+ *   calls take it like any R.  d and block powers of two, 1 <= block <= d
+ *   <= 1024.  Host-only, synchronous, thread-safe.
+ */
+oscar_status oscar_build_canalized_rotation(int32_t d, int32_t block, double* r_out);
+
+/*
  * oscar_score_weighted_rows - rows of S.V for the value covariance
  * C_S = (1/N) V^T S^T S V.  [GIST] 2.1 and 2.2 A.
  *

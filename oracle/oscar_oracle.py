@@ -92,6 +92,25 @@ def bit_reversal_matrix(d: int) -> np.ndarray:
     return p
 
 
+def canalized_rotation(d: int, block: int) -> np.ndarray:
+    """Block-diagonal rotation of the OScaR variant: R = I_(d/block) (x) H_block.
+
+    [CSDN] section 四.2 (OScaR): the K/V channels are split into groups and
+    rotated within each group, with no matrix inversion and no iteration.
+    The pages name no in-group rotation; the plainest fixed orthogonal choice
+    is taken, the orthonormal Sylvester Hadamard of the group size.  The
+    variant's per-token scaling is already carried by this codec's per-token
+    (scale, zero) pair, so it adds nothing to R.
+    """
+    if d <= 0 or d & (d - 1) or block <= 0 or block & (block - 1) or block > d:
+        raise ValueError("d and block must be powers of two with block <= d")
+    r = np.zeros((d, d), dtype=np.float64)
+    hb = hadamard(block)
+    for g in range(d // block):
+        r[g * block:(g + 1) * block, g * block:(g + 1) * block] = hb
+    return r
+
+
 def query_covariance(q: np.ndarray) -> np.ndarray:
     """C_Q = (1/N) sum_n q_n^T q_n over the N calibration query rows.   [GIST] 2.2 A."""
     q = np.asarray(q, dtype=np.float64)

@@ -32,6 +32,22 @@ def rotations(seed: int, layer: int, n_kv: int, outl: np.ndarray, n_q: int = 409
     return rk32, rv32, tau_k, tau_v
 
 
+def canalized_rotations(seed: int, layer: int, n_kv: int, outl: np.ndarray, block: int,
+                        n_q: int = 1024, n_k: int = 512):
+    """The OScaR block-diagonal rotation for every KV head (K and V), as fp32,
+    with per-layer taus from the calibration rows rotated by it."""
+    r = O.canalized_rotation(128, block).astype(np.float32)
+    r32 = np.stack([r] * n_kv)
+    ck, cv = [], []
+    for h in range(n_kv):
+        cal = synth.calibration_set(seed, layer, h, outl[h], n_q=n_q, n_k=n_k)
+        ck.append(cal["k"] @ r.astype(np.float64))
+        cv.append(cal["v"] @ r.astype(np.float64))
+    tau_k = float(np.float32(O.clip_threshold(np.stack(ck))))
+    tau_v = float(np.float32(O.clip_threshold(np.stack(cv))))
+    return r32, r32.copy(), tau_k, tau_v
+
+
 def demote_heads(x: np.ndarray, r32: np.ndarray, tau: float):
     """Oracle demotion of x [T][n_kv][d] with per-head rotations: (codes, scale16, zero16)."""
     t, n_kv, d = x.shape

@@ -145,3 +145,13 @@ def test_clip_threshold_matches_oracle(built_lib):
     tau = B.oscar_clip_threshold(acts, r, 0.999)
     ref = O.clip_threshold(np.stack([acts[h] @ r[h] for h in range(3)]), 0.999)
     assert tau == pytest.approx(ref, rel=1e-14)
+
+
+def test_canalized_rotation_matches_oracle(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    for d, block in ((128, 32), (128, 128), (64, 8), (16, 1)):
+        np.testing.assert_array_equal(B.oscar_build_canalized_rotation(d, block), O.canalized_rotation(d, block))
+    for d, block in ((128, 48), (128, 256), (96, 32), (128, 0)):
+        with pytest.raises(B.OscarError) as err:
+            B.oscar_build_canalized_rotation(d, block)
+        assert err.value.status == 1

@@ -28,12 +28,15 @@ def _pre_rounding(x_rot_clipped):
     return (mx - mn) / 3.0, mn
 
 
-def _run(seed, n_tok, n_kv, positions=None, with_new=False):
+def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None):
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
     outl = synth.outlier_channels(seed, 0, n_kv)
-    rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    if canalized_block is None:
+        rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    else:
+        rk32, rv32, tau_k, tau_v = H.canalized_rotations(seed, 0, n_kv, outl, canalized_block)
     xk = synth.activations(seed, (1, 0), n_tok, outl)
     xv = synth.activations(seed, (1, 1), n_tok, outl)
     g = synth.generator(seed, 5)

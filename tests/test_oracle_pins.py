@@ -87,6 +87,41 @@ def test_rotation_of_diagonal_covariance_is_hadamard_then_bitreversal():
             assert r[i, j] == pytest.approx(want, abs=1e-15)
 
 
+def _fwht(v):
+    """Unnormalised fast Walsh-Hadamard transform by butterflies (Sylvester order)."""
+    v = np.array(v, dtype=np.float64)
+    h = 1
+    while h < v.size:
+        for i in range(0, v.size, 2 * h):
+            a, b = v[i:i + h].copy(), v[i + h:i + 2 * h].copy()
+            v[i:i + h], v[i + h:i + 2 * h] = a + b, a - b
+        h *= 2
+    return v
+
+
+def test_canalized_rotation_golden_and_blockwise_transform():
+    # [CSDN] section 4.2 (OScaR): rotation inside channel groups.  Golden for
+    # d = 4, groups of 2: two copies of [[1, 1], [1, -1]] / sqrt(2) on the diagonal
+    s = 1 / np.sqrt(2.0)
+    golden = np.array([[s, s, 0, 0], [s, -s, 0, 0], [0, 0, s, s], [0, 0, s, -s]])
+    np.testing.assert_array_equal(O.canalized_rotation(4, 2), golden)
+    # x . R equals, group by group, the butterfly transform (a different
+    # algorithm from the closed form) scaled by 1/sqrt(block)
+    x = synth.generator(31, 0).standard_normal((3, 128))
+    for block in (1, 8, 32, 128):
+        r = O.canalized_rotation(128, block)
+        want = np.concatenate([np.stack([_fwht(row[g:g + block]) for row in x]) for g in range(0, 128, block)],
+                              axis=1) / np.sqrt(block)
+        np.testing.assert_allclose(x @ r, want, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(r @ r.T, np.eye(128), rtol=0, atol=1e-12)
+        mask = np.kron(np.eye(128 // block), np.ones((block, block)))
+        assert np.all(r[mask == 0] == 0)
+    np.testing.assert_array_equal(O.canalized_rotation(128, 128), O.hadamard(128))
+    np.testing.assert_array_equal(O.canalized_rotation(16, 1), np.eye(16))
+    with pytest.raises(ValueError):
+        O.canalized_rotation(128, 48)
+
+
 def test_rotation_is_orthogonal_and_composed_u_first():
     d = 128
     cal = synth.calibration_set(7, 0, 0, np.array([3, 40, 77, 100]), n_q=1024, n_k=256)
