@@ -9,23 +9,27 @@
 // as q~ = q . R_K once per query head and one o . R_V^T per head after the
 // history partials are merged, instead of rotating every token.
 //
-// One launch.  CTA (split, kv, b) of W warps (16 for GQA 4, 12 for GQA 8; one
-// CTA per SM) owns a contiguous range of INT2 pages of one (request, KV head)
-// and a share of its BF16 sink/recent tokens:
-//   1. lane 0 of each warp starts 1-D TMA bulk copies of the warp's first
-//      pages (one 1152-byte page block per stage, a ring of 6 (GQA 4) or 8
-//      (GQA 8) stages per warp, mbarrier completion, bounded waits);
-//   2. R_K arrives in shared memory by one TMA bulk transfer issued first;
-//      the CTA computes q~ = q . R_K for the GQA group (fp32) and builds the
-//      32 lanes' tensor-core B fragments once in shared memory;
-//   3. every warp streams its INT2 pages through its ring, keeping its own
-//      online-softmax state; then the warps owning the fewest pages scan the
-//      CTA's BF16 tokens (direct vector loads);
-//   4. the CTA merges its warps into two partials (m, l, o) per query head
-//      (history and BF16) and rotates the history one back with R_V (staged
-//      by TMA during the scan), so every partial is in the original basis;
-//   5. the last CTA of the (request, KV head) to finish (atomic ticket, no
-//      waiting) merges all partials (one warp per head, loads batched) and
+// One launch (programmatic dependent launch: it waits for the previous
+// kernel's writes first and lets the next kernel become resident early).
+// CTA (split, kv, b) of W warps (16 for GQA 4, 12 for GQA 8; one CTA per SM)
+// owns a contiguous range of INT2 pages of one (request, KV head) and a
+// share of its BF16 sink/recent tokens:
+//   1. R_K is requested first (TMA bulk copy); lane 0 of each warp starts
+//      1-D TMA bulk copies of the warp's first pages (one 1152-byte page
+//      block per stage, a ring of 6 (GQA 4) or 8 (GQA 8) stages per warp,
+//      mbarrier completion, bounded waits);
+//   2. all warps but the last two compute q~ = q . R_K for the GQA group
+//      (fp32) and build the 32 lanes' tensor-core B fragments once in shared
+//      memory, while the last two scan the CTA's BF16 tokens;
+//   3. every warp streams its INT2 pages through its ring, 4 (GQA 4) or 3
+//      (GQA 8) per online-softmax step, keeping its own state; after a step
+//      its lanes start the copies of the freed stages together;
+//   4. one warp per head weighs the CTA's warp states against their common
+//      maximum; the history part is rotated back with R_V (four 2-D TMA
+//      copies with the 128-byte swizzle, issued after step 2) and joined
+//      with the BF16 part into one partial (m, l, o) per query head;
+//   5. the last CTA of the (request, KV head) to finish (acquire-release
+//      ticket, no waiting) merges all partials (one warp per head) and
 //      writes the normalised output, then resets the ticket.
 //
 // INT2 arithmetic on the tensor cores (mma.sync m16n8k16, fp32 accumulate):
@@ -102,10 +106,11 @@ struct Geo {
   static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
   static_assert(kGroup >= 1 && kGroup < kStages, "a step leaves copies in flight");
   static constexpr size_t kStageBytes = size_t(W) * kStages * kBlockBytes;
-  // ring barriers + the R_K and R_V barriers, padded so the region after it
-  // stays 128-byte aligned (TMA destinations need at least 16)
+  // ring barriers + the R_K, R_V and prologue-done barriers, padded so the
+  // region after it stays 128-byte aligned (TMA destinations need at least 16)
   static constexpr size_t kBarBytes = ((size_t(W) * kStages + 3) * 8 + 127) / 128 * 128;
-  // prologue: R_K (64 KB) and the q~ scratch; epilogue: two warp-state sets
+  // union: R_K (64 KB, prologue) then R_V (epilogue), followed by the q~
+  // scratch (prologue) that the CTA merge reuses
   static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
   static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G + 32 * NH * 16) * 4;
   static constexpr size_t kUnion = kRotBytes + kQScratch;   // R_K then R_V | q~ scratch
@@ -696,7 +701,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stage = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<G>::kStageBytes);
-  uint64_t* rbar = bars + W * kStages;       // R_K, then (last CTA) R_V
+  uint64_t* rbar = bars + W * kStages;       // R_K; rbar + 1: R_V
   uint8_t* uni = smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes;
   uni += (1024u - (smem_addr(uni) & 1023u)) & 1023u;
   float* rks = reinterpret_cast<float*>(uni);                         // prologue only

@@ -124,10 +124,6 @@ __device__ __forceinline__ void ld_cg_if(float2& v, const float* p, bool ok) {
                : "memory");
 }
 
-// Release/acquire fence at GPU scope (publishes this CTA's prior writes when
-// issued after a CTA barrier, as in the standard "last block" pattern).
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
 // Orders this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
