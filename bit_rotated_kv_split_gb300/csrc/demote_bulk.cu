@@ -22,8 +22,8 @@
 //   warps 0-3  read one token's 128 rotated values from tensor memory
 //              (thread = token = TMEM lane), clip, min/max, fp16 scale and
 //              zero point, codes, pack 32 bytes and store them in the page.
-// Operand and accumulator buffers are doubled so loading, MMA and the
-// epilogue of consecutive tiles overlap.  Every wait is bounded (1 s).
+// Operand, accumulator and metadata buffers are fourfold, so loading, MMA
+// and the epilogue of consecutive tiles overlap.  Every wait is bounded (1 s).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -36,10 +36,14 @@ constexpr int kMmaWarp = kEpiWarps + kLoadWarps;    // warp 8
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kOpBytes = kTile * kHeadDim * 2;      // one fp16 128 x 128 operand
 constexpr float kRScale = 16.f;
-constexpr size_t oBhi = 0, oBlo = kOpBytes, oA = 2 * size_t(kOpBytes), oMeta = 4 * size_t(kOpBytes);
-constexpr size_t oBars = oMeta + 2 * kTile * sizeof(int2);
-constexpr size_t kSmem = oBars + 128;
-constexpr uint32_t kCols = 256;                     // D[2] x 128 columns
+constexpr int kBufs = 4;                            // operand / accumulator / metadata buffers
+constexpr size_t oBhi = 0, oBlo = kOpBytes, oA = 2 * size_t(kOpBytes);
+constexpr size_t oMeta = oA + size_t(kBufs) * kOpBytes;
+constexpr size_t oBars = oMeta + size_t(kBufs) * kTile * sizeof(int2);
+constexpr size_t kSmem = oBars + (3 * kBufs + 2) * 8 + 16;
+constexpr uint32_t kCols = 128 * kBufs;             // D[kBufs] x 128 columns
+static_assert(kCols <= 512, "tensor memory columns");
+static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kFull = 0xffffffffu;
@@ -84,14 +88,14 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
   uint8_t* bhi = smem + oBhi;
   uint8_t* blo = smem + oBlo;
   uint8_t* abuf = smem + oA;
-  int2* meta = reinterpret_cast<int2*>(smem + oMeta);          // [2][128] (page, slot)
+  int2* meta = reinterpret_cast<int2*>(smem + oMeta);          // [kBufs][128] (page, slot)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + oBars);
-  uint64_t* a_full = bars;          // [2] loaders
-  uint64_t* mma_done = bars + 2;    // [2] commit
-  uint64_t* d_free = bars + 4;      // [2] epilogue
-  uint64_t* fin = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 7) + 1;
+  uint64_t* a_full = bars;                // [kBufs] loaders
+  uint64_t* mma_done = bars + kBufs;      // [kBufs] commit
+  uint64_t* d_free = bars + 2 * kBufs;    // [kBufs] epilogue
+  uint64_t* fin = bars + 3 * kBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kBufs + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kBufs + 1) + 1;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int which = int(blockIdx.y & 1), head = int(blockIdx.y >> 1);
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
   const int my_tiles = int(blockIdx.x) < n_tiles ? (n_tiles - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBufs; ++i) {
       mbar_init(a_full + i, kLoadWarps * 32);
       mbar_init(mma_done + i, 1);
       mbar_init(d_free + i, kEpiWarps * 32);
@@ -143,46 +147,60 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
     const int j = tid;
     const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
     for (int k = 0; k < my_tiles; ++k) {
-      const int buf = k & 1;
-      if (!wt.wait(a_full + buf, (k >> 1) & 1)) break;        // the loaders' page lookups
-      if (!wt.wait(mma_done + buf, (k >> 1) & 1)) break;
+      const int buf = k % kBufs;
+      const uint32_t par = (k / kBufs) & 1;
+      if (!wt.wait(a_full + buf, par)) break;        // the loaders' page lookups
+      if (!wt.wait(mma_done + buf, par)) break;
       tc_fence_after();
       const int2 m = meta[buf * kTile + j];
+      // D = 16 x~ (the operand scale), read as four 32-column loads behind one wait
       float v[kHeadDim];
       {
-        uint32_t r[32];
+        uint32_t r[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(lane_addr + uint32_t(buf * 128 + 32 * c), r);
-          tc_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + uint32_t(buf * 128 + 32 * c), r[c]);
+        tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[i]) * (1.f / kRScale);
-        }
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[c][i]);
       }
       tc_fence_before();
       mbar_arrive(d_free + buf);
       if (m.x < 0) continue;
-      float mn = INFINITY, mx = -INFINITY;
+      // clipping moves only the extremes: min and max of the clipped values
+      // are the clipped min and max, and a value beyond +-tau gets the code
+      // of the clipped extreme (0 or 3) through the final clamp
+      float mn = v[0], mx = v[0];
 #pragma unroll
-      for (int i = 0; i < kHeadDim; ++i) {
-        v[i] = fminf(fmaxf(v[i], -tau), tau);
+      for (int i = 1; i < kHeadDim; ++i) {
         mn = fminf(mn, v[i]);
         mx = fmaxf(mx, v[i]);
       }
+      mn = fminf(fmaxf(mn * (1.f / kRScale), -tau), tau);
+      mx = fminf(fmaxf(mx * (1.f / kRScale), -tau), tau);
       const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
       const __half z16 = __float2half_rn(mn);
       const float s = __half2float(s16), z = __half2float(z16);
+      // code = clamp(rint((x - z) / s), 0, 3) with x = D / 16: (x - z) / s by
+      // one FMA, clamped to [0, 3]; adding 1.5 * 2^23 rounds it to an
+      // integer held in the float's low bits (0x4B400000 + code), which are
+      // accumulated as bits * 4^i (mod 2^32) with the constant part of the
+      // sum removed once per word
       const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+      const float a16 = inv * (1.f / kRScale), nzi = -z * inv;
+      const float kMagic = 12582912.f;
+      constexpr uint32_t kBitsSum = 0x4B400000u * 0x55555555u;   // 0x4B400000 * sum_i 4^i (mod 2^32)
       uint32_t w[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         uint32_t word = 0u;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float code = fminf(fmaxf(rintf((v[16 * q + i] - z) * inv), 0.f), 3.f);
-          word |= uint32_t(code) << (2 * i);
+          const float t = fminf(fmaxf(fmaf(v[16 * q + i], a16, nzi), 0.f), 3.f);
+          word += __float_as_uint(t + kMagic) << (2 * i);
         }
-        w[q] = word;
+        w[q] = word - kBitsSum;
       }
       uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
       *reinterpret_cast<uint4*>(blk + 32 * m.y) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -194,10 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
     // ================= loaders: thread j = token j of the next tile
     const int j = tid - kEpiWarps * 32;
     for (int k = 0; k < my_tiles; ++k) {
-      const int buf = k & 1;
-      // operand, accumulator and metadata of buffer k % 2 are free once the
-      // epilogue of tile k - 2 has read them
-      if (k >= 2 && !wt.wait(d_free + buf, ((k - 2) >> 1) & 1)) break;
+      const int buf = k % kBufs;
+      // operand, accumulator and metadata of buffer k % kBufs are free once
+      // the epilogue of tile k - kBufs has read them
+      if (k >= kBufs && !wt.wait(d_free + buf, ((k - kBufs) / kBufs) & 1)) break;
       const int item = (int(blockIdx.x) + k * int(gridDim.x)) * kTile + j;
       bool live = item < p.n;
       int64_t row = 0;
@@ -247,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
     if (lane == 0) {
       const uint32_t bh = smem_addr(bhi), bl = smem_addr(blo);
       for (int k = 0; k < my_tiles; ++k) {
-        const int buf = k & 1;
-        if (!wt.wait(a_full + buf, (k >> 1) & 1)) break;
+        const int buf = k % kBufs;
+        if (!wt.wait(a_full + buf, (k / kBufs) & 1)) break;
         tc_fence_after();
         const uint32_t aa = smem_addr(abuf + buf * kOpBytes);
         const uint32_t d = tmem + uint32_t(buf * 128);
