@@ -704,7 +704,6 @@ def run_extra(args):
             caches.append(c)
             srcs.append((synth.activations_device(seed, (50 + i, 0), ctx, rots[i][4], dev),
                          synth.activations_device(seed, (50 + i, 1), ctx, rots[i][4], dev)))
-        idx = torch.arange(s0, s0 + h, dtype=torch.int32, device=dev)
         req = torch.zeros(h, dtype=torch.int32, device=dev)
         pos = torch.arange(h, dtype=torch.int32, device=dev)
         descs = [c.desc(h) for c in caches]
@@ -714,9 +713,11 @@ def run_extra(args):
         ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
 
         def demote_layer(i):
+            # the prefill buffers from their first history token (row s0):
+            # contiguous rows, no index
             xk, xv = srcs[i % nd]
-            B.oscar_quantize_append(descs[i % nd], xk.view(torch.uint16), xv.view(torch.uint16), ctx,
-                                    n_kv * 128, idx, req, pos, h)
+            B.oscar_quantize_append(descs[i % nd], xk[s0:].view(torch.uint16), xv[s0:].view(torch.uint16),
+                                    ctx - s0, n_kv * 128, None, req, pos, h)
 
         def decode(i):
             B.oscar_decode_attention(descs[i % nd], q, out, ws, ws_bytes)

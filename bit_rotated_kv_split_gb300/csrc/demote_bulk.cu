@@ -14,16 +14,24 @@
 // scaled by 16 and split into fp16 hi + lo parts (about 22 significant
 // bits), so D = x.(16 R)_hi + x.(16 R)_lo and x~ = D / 16.
 //
-// CTA (tile stride, KV head, K|V) of 9 warps, one CTA per SM:
-//   warps 4-7  load the next tile's 128 source rows (thread = token), convert
-//              to fp16 into the canonical K-major operand layout in shared
-//              memory, and look up each token's page;
-//   warp 8     issues the 16 MMAs of a tile from one lane;
-//   warps 0-3  read one token's 128 rotated values from tensor memory
-//              (thread = token = TMEM lane), clip, min/max, fp16 scale and
-//              zero point, codes, pack 32 bytes and store them in the page.
+// CTA (tile stride, KV head, K|V) of 13 warps, one CTA per SM:
+//   warps 8-11 bring a tile's 128 source rows into the A operand: with
+//              contiguous rows they convert the bf16 rows that 16 2-D TMA
+//              copies (8 columns x 128 rows each, one K column of 8 x 16-byte
+//              core matrices) put there to fp16 in place; with gathered rows
+//              each thread loads its token's row; they also look up each
+//              token's page;
+//   warp 12    issues the 16 MMAs of a tile from one lane;
+//   warp 13    starts the tile copies (contiguous rows) as buffers free up;
+//   warps 0-7  read half a token's 128 rotated values from tensor memory
+//              (warps w and w + 4 share the lane quadrant w % 4; thread =
+//              token = TMEM lane), meet on its min/max through shared memory,
+//              form the fp16 scale and zero point, and pack and store 16
+//              bytes of codes each.
 // Operand, accumulator and metadata buffers are fourfold, so loading, MMA
 // and the epilogue of consecutive tiles overlap.  Every wait is bounded (1 s).
+#include <cudaTypedefs.h>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -31,16 +39,18 @@ namespace oscar {
 namespace {
 
 constexpr int kTile = 128;                          // tokens per tile (MMA M)
-constexpr int kEpiWarps = 4, kLoadWarps = 4;
-constexpr int kMmaWarp = kEpiWarps + kLoadWarps;    // warp 8
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kEpiWarps = 8, kLoadWarps = 4;     // epilogue: two warps per TMEM lane quadrant
+constexpr int kMmaWarp = kEpiWarps + kLoadWarps;    // warp 12
+constexpr int kTmaWarp = kMmaWarp + 1;               // warp 13: source tile copies
+constexpr int kThreads = (kTmaWarp + 1) * 32;
 constexpr int kOpBytes = kTile * kHeadDim * 2;      // one fp16 128 x 128 operand
 constexpr float kRScale = 16.f;
 constexpr int kBufs = 4;                            // operand / accumulator / metadata buffers
 constexpr size_t oBhi = 0, oBlo = kOpBytes, oA = 2 * size_t(kOpBytes);
 constexpr size_t oMeta = oA + size_t(kBufs) * kOpBytes;
-constexpr size_t oBars = oMeta + size_t(kBufs) * kTile * sizeof(int2);
-constexpr size_t kSmem = oBars + (3 * kBufs + 2) * 8 + 16;
+constexpr size_t oXchg = oMeta + size_t(kBufs) * kTile * sizeof(int2);   // [2][2][128] (min, max)
+constexpr size_t oBars = oXchg + 2 * 2 * kTile * sizeof(float2);
+constexpr size_t kSmem = oBars + (4 * kBufs + 4) * 8 + 16;
 constexpr uint32_t kCols = 128 * kBufs;             // D[kBufs] x 128 columns
 static_assert(kCols <= 512, "tensor memory columns");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -51,10 +61,15 @@ constexpr uint32_t kFull = 0xffffffffu;
 // byte offset of (row, k) in a 128 x 128 fp16 operand, canonical K-major
 // layout without swizzle: 8 x 16-byte core matrices, 128 bytes between the
 // two K halves of a 16-wide K step (LBO), 256 bytes between 8-row groups
-// (SBO), 4096 bytes per K step
+// (SBO), 4096 bytes per K step (the B operand)
 __device__ __forceinline__ int op_offset(int row, int k) {
   return (k >> 4) * 4096 + (row >> 3) * 256 + ((k >> 3) & 1) * 128 + (row & 7) * 16 + (k & 7) * 2;
 }
+
+// the A operand: one 2 KB column of core matrices per 8 K values (the box
+// of one TMA copy), rows 16 bytes apart: LBO 2048, SBO 128, 4096 bytes per
+// K step
+__device__ __forceinline__ int a_offset(int row, int k) { return (k >> 3) * 2048 + row * 16 + (k & 7) * 2; }
 
 __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
@@ -81,7 +96,7 @@ struct Waiter {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p) {
+__global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_constant__ DemoteParams p) {
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -93,9 +108,12 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
   uint64_t* a_full = bars;                // [kBufs] loaders
   uint64_t* mma_done = bars + kBufs;      // [kBufs] commit
   uint64_t* d_free = bars + 2 * kBufs;    // [kBufs] epilogue
-  uint64_t* fin = bars + 3 * kBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kBufs + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kBufs + 1) + 1;
+  uint64_t* tma_full = bars + 3 * kBufs; // [kBufs] source tile copies
+  uint64_t* xfull = bars + 4 * kBufs;    // [2] epilogue halves' (min, max) exchange
+  uint64_t* fin = bars + 4 * kBufs + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * kBufs + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kBufs + 3) + 1;
+  float2* xchg = reinterpret_cast<float2*>(smem + oXchg);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int which = int(blockIdx.y & 1), head = int(blockIdx.y >> 1);
@@ -107,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
       mbar_init(a_full + i, kLoadWarps * 32);
       mbar_init(mma_done + i, 1);
       mbar_init(d_free + i, kEpiWarps * 32);
+      mbar_init(tma_full + i, 1);
     }
+    mbar_init(xfull, kEpiWarps * 32);
+    mbar_init(xfull + 1, kEpiWarps * 32);
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -143,9 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
   const float tau = which ? p.tau_v : p.tau_k;
 
   if (warp < kEpiWarps) {
-    // ================= epilogue: thread j = token j of the tile = TMEM lane j
-    const int j = tid;
-    const uint32_t lane_addr = tmem + (uint32_t(warp * 32) << 16);
+    // ================= epilogue: thread (token j = TMEM lane j, half hh):
+    // warps w and w + 4 read the lane quadrant w % 4, columns 64 hh .. 64 hh
+    // + 63 each, and meet on the token's min and max through shared memory
+    const int quad = warp & 3, hh = warp >> 2;
+    const int j = 32 * quad + lane;
+    const uint32_t lane_addr = tmem + (uint32_t(32 * quad) << 16);
     for (int k = 0; k < my_tiles; ++k) {
       const int buf = k % kBufs;
       const uint32_t par = (k / kBufs) & 1;
@@ -153,30 +177,37 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
       if (!wt.wait(mma_done + buf, par)) break;
       tc_fence_after();
       const int2 m = meta[buf * kTile + j];
-      // D = 16 x~ (the operand scale), read as four 32-column loads behind one wait
-      float v[kHeadDim];
+      // D = 16 x~ (the operand scale), two 32-column loads behind one wait
+      float v[kHeadDim / 2];
       {
-        uint32_t r[4][32];
+        uint32_t r[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + uint32_t(buf * 128 + 32 * c), r[c]);
+        for (int c = 0; c < 2; ++c) tmem_ld32(lane_addr + uint32_t(buf * 128 + 64 * hh + 32 * c), r[c]);
         tc_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[c][i]);
       }
       tc_fence_before();
       mbar_arrive(d_free + buf);
-      if (m.x < 0) continue;
       // clipping moves only the extremes: min and max of the clipped values
       // are the clipped min and max, and a value beyond +-tau gets the code
       // of the clipped extreme (0 or 3) through the final clamp
       float mn = v[0], mx = v[0];
 #pragma unroll
-      for (int i = 1; i < kHeadDim; ++i) {
+      for (int i = 1; i < kHeadDim / 2; ++i) {
         mn = fminf(mn, v[i]);
         mx = fmaxf(mx, v[i]);
       }
+      float2* xs = xchg + (k & 1) * 2 * kTile;
+      xs[hh * kTile + j] = make_float2(mn, mx);
+      mbar_arrive(xfull + (k & 1));
+      if (!wt.wait(xfull + (k & 1), (k >> 1) & 1)) break;
+      const float2 other = xs[(1 - hh) * kTile + j];
+      mn = fminf(mn, other.x);
+      mx = fmaxf(mx, other.y);
+      if (m.x < 0) continue;
       mn = fminf(fmaxf(mn * (1.f / kRScale), -tau), tau);
       mx = fminf(fmaxf(mx * (1.f / kRScale), -tau), tau);
       const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
@@ -191,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
       const float a16 = inv * (1.f / kRScale), nzi = -z * inv;
       const float kMagic = 12582912.f;
       constexpr uint32_t kBitsSum = 0x4B400000u * 0x55555555u;   // 0x4B400000 * sum_i 4^i (mod 2^32)
-      uint32_t w[8];
+      uint32_t w[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t word = 0u;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -203,35 +234,62 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
         w[q] = word - kBitsSum;
       }
       uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
-      *reinterpret_cast<uint4*>(blk + 32 * m.y) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(blk + 32 * m.y + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-      __half2 sz = __halves2half2(s16, z16);
-      *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * m.y) = sz;
+      *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (hh == 0) {
+        __half2 sz = __halves2half2(s16, z16);
+        *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * m.y) = sz;
+      }
     }
   } else if (warp < kMmaWarp) {
-    // ================= loaders: thread j = token j of the next tile
+    // ================= loaders: thread j = token j of the tile
     const int j = tid - kEpiWarps * 32;
+    // the token's indices (source row, request, position) are requested two
+    // tiles ahead and its page id one tile ahead, so neither dependent load
+    // waits in the tile loop
+    struct Idx {
+      bool live;
+      int64_t row;
+      int bq, pos;
+    };
+    auto load_idx = [&](int kt) {
+      const int item = (int(blockIdx.x) + kt * int(gridDim.x)) * kTile + j;
+      Idx r{item < p.n, 0, 0, 0};
+      if (r.live) {
+        r.row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
+        r.bq = p.dst_req[item];
+        r.pos = p.dst_pos[item];
+      }
+      return r;
+    };
+    auto check_and_look_up = [&](Idx& r) {
+      if (r.live && (r.row < 0 || r.row >= p.src_rows || r.bq < 0 || r.bq >= p.batch || r.pos < 0 ||
+                     r.pos / kPage >= p.max_pages)) {
+        if (p.dev_status) atomicOr(p.dev_status, 0x2);
+        r.live = false;
+      }
+      return r.live ? p.page_table[int64_t(r.bq) * p.max_pages + r.pos / kPage] : -1;
+    };
+    Idx nxt = my_tiles > 0 ? load_idx(0) : Idx{false, 0, 0, 0};
+    Idx nxt2 = my_tiles > 1 ? load_idx(1) : Idx{false, 0, 0, 0};
+    int nxt_pid = check_and_look_up(nxt);
     for (int k = 0; k < my_tiles; ++k) {
       const int buf = k % kBufs;
-      // operand, accumulator and metadata of buffer k % kBufs are free once
-      // the epilogue of tile k - kBufs has read them
-      if (k >= kBufs && !wt.wait(d_free + buf, ((k - kBufs) / kBufs) & 1)) break;
-      const int item = (int(blockIdx.x) + k * int(gridDim.x)) * kTile + j;
-      bool live = item < p.n;
-      int64_t row = 0;
-      int bq = 0, pos = 0;
+      // (TMA path: the copy warp waited for the buffer before its copies;
+      // here operand, accumulator and metadata of buffer k % kBufs are free
+      // once the epilogue of tile k - kBufs has read them)
+      if (!p.use_tma && k >= kBufs && !wt.wait(d_free + buf, ((k - kBufs) / kBufs) & 1)) break;
+      // this tile's token, then the pipeline moves on by one tile
+      bool live = nxt.live;
+      const int64_t row = nxt.row;
+      const int pos = nxt.pos;
+      const int pid = nxt_pid;
+      if (k + 1 < my_tiles) {
+        nxt = nxt2;
+        nxt_pid = check_and_look_up(nxt);
+      }
+      if (k + 2 < my_tiles) nxt2 = load_idx(k + 2);
       int page = -1;
       if (live) {
-        row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
-        bq = p.dst_req[item];
-        pos = p.dst_pos[item];
-        if (row < 0 || row >= p.src_rows || bq < 0 || bq >= p.batch || pos < 0 || pos / kPage >= p.max_pages) {
-          if (p.dev_status) atomicOr(p.dev_status, 0x2);
-          live = false;
-        }
-      }
-      if (live) {
-        const int pid = p.page_table[int64_t(bq) * p.max_pages + pos / kPage];
         if (pid < 0 || pid >= p.n_pages) {
           if (p.dev_status) atomicOr(p.dev_status, 0x1);
           live = false;
@@ -240,25 +298,57 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
         }
       }
       uint8_t* a = abuf + buf * kOpBytes;
-      const uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
+      if (p.use_tma) {
+        // bf16 -> fp16 in place, row j of every 8-column block
+        if (!wt.wait(tma_full + buf, (k / kBufs) & 1)) break;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 raw[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          raw[c] = live ? __ldg(reinterpret_cast<const uint4*>(src + 64 * half + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t wv[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+        for (int c = 0; c < kHeadDim / 8; ++c) {
+          uint4* q = reinterpret_cast<uint4*>(a + c * 2048 + j * 16);
+          const uint4 raw = *q;
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t h[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) h[e] = f16x2(sat16(bf16_lo(wv[e])), sat16(bf16_hi(wv[e])));
-          *reinterpret_cast<uint4*>(a + op_offset(j, 64 * half + 8 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *q = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      } else {
+        const uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 raw[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            raw[c] = live ? __ldg(reinterpret_cast<const uint4*>(src + 64 * half + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t wv[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = f16x2(sat16(bf16_lo(wv[e])), sat16(bf16_hi(wv[e])));
+            *reinterpret_cast<uint4*>(a + a_offset(j, 64 * half + 8 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
+          }
         }
       }
       meta[buf * kTile + j] = make_int2(live ? page : -1, pos % kPage);
       fence_proxy_async_smem();
       mbar_arrive(a_full + buf);
+    }
+  } else if (warp == kTmaWarp) {
+    // ================= source tile copies (TMA path): the 16 copies of
+    // tile k (one per 8 columns, lane c copies columns 8c .. 8c + 7) go out
+    // as soon as buffer k % kBufs is free
+    if (p.use_tma) {
+      for (int k = 0; k < my_tiles; ++k) {
+        const int b = k % kBufs;
+        if (k >= kBufs && !wt.wait(d_free + b, ((k - kBufs) / kBufs) & 1)) break;
+        if (lane == 0) mbar_arrive_expect_tx(tma_full + b, uint32_t(kOpBytes));
+        __syncwarp();
+        if (lane < kHeadDim / 8) {
+          const int row0 = (int(blockIdx.x) + k * int(gridDim.x)) * kTile;
+          tma_load_2d(abuf + b * kOpBytes + lane * 2048, &p.tm_src[which], head * kHeadDim + 8 * lane, row0,
+                      tma_full + b);
+        }
+      }
     }
   } else {
     // ================= MMA issue (one lane)
@@ -272,11 +362,11 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
         const uint32_t d = tmem + uint32_t(buf * 128);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 128u, 256u), smem_desc_kmajor(bh + 4096u * kk, 128u, 256u),
+          umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 2048u, 128u), smem_desc_kmajor(bh + 4096u * kk, 128u, 256u),
                       kIdesc, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 128u, 256u), smem_desc_kmajor(bl + 4096u * kk, 128u, 256u),
+          umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 2048u, 128u), smem_desc_kmajor(bl + 4096u * kk, 128u, 256u),
                       kIdesc, 1u);
         umma_commit(mma_done + buf);
       }
@@ -296,7 +386,40 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(DemoteParams p
 
 }  // namespace
 
-cudaError_t launch_demote_bulk(const DemoteParams& p, cudaStream_t stream) {
+// 2-D bf16 tensor maps over k_src / v_src (n_kv * 128 columns x src_rows
+// rows, row_stride elements apart) for the tile copies; false (gathered
+// rows instead) when the rows are indexed, the row pitch is not a multiple
+// of 16 bytes or the driver refuses
+bool encode_src_maps(DemoteParams* p) {
+  p->use_tma = 0;
+  if (p->src_index || (p->row_stride * 2) % 16 != 0 || p->src_rows < 1 || p->src_rows > (int64_t(1) << 31)) return false;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {cuuint64_t(p->n_kv) * kHeadDim, cuuint64_t(p->src_rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(p->row_stride) * 2};
+  const cuuint32_t box[2] = {8, cuuint32_t(kTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  const uint16_t* srcs[2] = {p->k_src, p->v_src};
+  for (int w = 0; w < 2; ++w)
+    if (encode(&p->tm_src[w], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(srcs[w]), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  p->use_tma = 1;
+  return true;
+}
+
+cudaError_t launch_demote_bulk(const DemoteParams& p_in, cudaStream_t stream) {
+  DemoteParams p = p_in;
+  encode_src_maps(&p);
   const int64_t n_tiles = (int64_t(p.n) + kTile - 1) / kTile;
   if (n_tiles == 0) return cudaSuccess;
   if (int64_t(p.n_kv) * 2 > 65535) return cudaErrorInvalidValue;

@@ -61,6 +61,11 @@ struct DemoteParams {
   float tau_k, tau_v;
   int32_t n, batch, n_kv, max_pages;
   int64_t n_pages;
+  // bulk path with contiguous source rows (no src_index): k_src / v_src as
+  // 2-D bf16 tensors (n_kv * 128 columns x src_rows rows) read in boxes of 8
+  // columns x 128 rows; use_tma = 0 means the rows are gathered by threads
+  CUtensorMap tm_src[2];
+  int32_t use_tma;
 };
 
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream);

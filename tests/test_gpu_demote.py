@@ -28,7 +28,7 @@ def _pre_rounding(x_rot_clipped):
     return (mx - mn) / 3.0, mn
 
 
-def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None):
+def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None, first_row=None):
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
@@ -41,6 +41,12 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
     xv = synth.activations(seed, (1, 1), n_tok, outl)
     g = synth.generator(seed, 5)
     src_index = g.permutation(n_tok).astype(np.int32)
+    if first_row is not None:
+        # contiguous rows: item i reads row first_row + i of the buffer (no
+        # index; the bulk kernel's tile copies)
+        src_index = np.arange(first_row, first_row + n_tok, dtype=np.int32)
+        xk = np.concatenate([synth.activations(seed, (1, 7), first_row, outl), xk])
+        xv = np.concatenate([synth.activations(seed, (1, 8), first_row, outl), xv])
     if positions is None:
         positions = np.arange(n_tok)
     hist = int(positions.max()) + 1
@@ -51,7 +57,7 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
     dev = torch.device("cuda")
     k_src = torch.from_numpy(xk).to(torch.bfloat16).to(dev).contiguous()
     v_src = torch.from_numpy(xv).to(torch.bfloat16).to(dev).contiguous()
-    si = torch.from_numpy(src_index).to(dev)
+    si = None if first_row is not None else torch.from_numpy(src_index).to(dev)
     dr = torch.zeros(n_tok, dtype=torch.int32, device=dev)
     dp = torch.from_numpy(positions.astype(np.int32)).to(dev)
     new_k = new_v = None
@@ -60,8 +66,10 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         nv = synth.activations(seed, (1, 3), n_tok, outl)
         new_k = torch.from_numpy(nk).to(torch.bfloat16).to(dev)
         new_v = torch.from_numpy(nv).to(torch.bfloat16).to(dev)
-    B.oscar_quantize_append(cache.desc(hist), k_src.view(torch.uint16), v_src.view(torch.uint16),
-                            n_tok, n_kv * 128, si, dr, dp, n_tok,
+    k_in = k_src[first_row:] if first_row is not None else k_src
+    v_in = v_src[first_row:] if first_row is not None else v_src
+    B.oscar_quantize_append(cache.desc(hist), k_in.view(torch.uint16), v_in.view(torch.uint16),
+                            k_in.shape[0], n_kv * 128, si, dr, dp, n_tok,
                             None if new_k is None else new_k.view(torch.uint16),
                             None if new_v is None else new_v.view(torch.uint16))
     torch.cuda.synchronize()
@@ -95,6 +103,15 @@ def test_demote_bulk_path_eight_heads_ragged_tail():
     g = synth.generator(4, 1)
     pos = g.permutation(5000)[:3000]
     res = _run(2004, 3000, 8, positions=pos)
+    print(res)
+
+
+def test_demote_bulk_path_contiguous_rows_ragged_tail():
+    # 3000 contiguous rows starting at row 77 of the buffer (no index), so
+    # the last 128-token tile is partial and the tile copies start mid-buffer
+    g = synth.generator(6, 1)
+    pos = g.permutation(4000)[:3000]
+    res = _run(2005, 3000, 4, positions=pos, first_row=77)
     print(res)
 
 

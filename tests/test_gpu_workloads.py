@@ -181,11 +181,12 @@ def test_bulk_demotion_128k_then_decode():
     cache.page_table.copy_(torch.from_numpy(table))
     k_src = torch.from_numpy(xk).to(torch.bfloat16).to(dev).contiguous()
     v_src = torch.from_numpy(xv).to(torch.bfloat16).to(dev).contiguous()
-    si = torch.arange(sl, sl + hl, dtype=torch.int32, device=dev)
+    # contiguous source rows (the prefill buffer from its first history
+    # token, no index): the tile-copy path of the bulk kernel
     dr = torch.zeros(hl, dtype=torch.int32, device=dev)
     dp = torch.arange(hl, dtype=torch.int32, device=dev)
-    B.oscar_quantize_append(cache.desc(hl), k_src.view(torch.uint16), v_src.view(torch.uint16), ctx,
-                            n_kv * 128, si, dr, dp, hl, None, None)
+    B.oscar_quantize_append(cache.desc(hl), k_src[sl:].view(torch.uint16), v_src[sl:].view(torch.uint16),
+                            ctx - sl, n_kv * 128, None, dr, dp, hl, None, None)
     torch.cuda.synchronize()
     assert int(cache.dev_status.item()) == 0
     # demotion parity on every token
