@@ -56,7 +56,6 @@ static_assert(kCols <= 512, "tensor memory columns");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr uint32_t kFull = 0xffffffffu;
 
 // byte offset of (row, k) in a 128 x 128 fp16 operand, canonical K-major
 // layout without swizzle: 8 x 16-byte core matrices, 128 bytes between the
@@ -76,7 +75,13 @@ __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ float sat16(float x) { return fminf(fmaxf(x, -65504.f), 65504.f); }
+// two floats -> fp16x2 (lo in the low half), rounded to nearest and
+// saturated to the finite fp16 range by the conversion itself
+__device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 struct Waiter {
   volatile int* abort_flag;
@@ -213,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
       const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
       const __half z16 = __float2half_rn(mn);
       const float s = __half2float(s16), z = __half2float(z16);
-      // code = clamp(rint((x - z) / s), 0, 3) with x = D / 16: (x - z) / s by
-      // one FMA, clamped to [0, 3]; adding 1.5 * 2^23 rounds it to an
-      // integer held in the float's low bits (0x4B400000 + code), which are
-      // accumulated as bits * 4^i (mod 2^32) with the constant part of the
-      // sum removed once per word
+      // code = clamp(rint((x - z) / s), 0, 3) with x = D / 16: one saturating
+      // FMA gives (x - z) / (3 s) clamped to [0, 1]; a second FMA scales by 3
+      // and adds 1.5 * 2^23, which rounds to an integer held in the float's
+      // low bits (0x4B400000 + code); the bits are accumulated as bits * 4^i
+      // (mod 2^32) and the constant part of the sum removed once per word
       const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-      const float a16 = inv * (1.f / kRScale), nzi = -z * inv;
+      const float a48 = inv * (1.f / (3.f * kRScale)), nzi3 = -z * inv * (1.f / 3.f);
       const float kMagic = 12582912.f;
       constexpr uint32_t kBitsSum = 0x4B400000u * 0x55555555u;   // 0x4B400000 * sum_i 4^i (mod 2^32)
       uint32_t w[4];
@@ -228,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
         uint32_t word = 0u;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float t = fminf(fmaxf(fmaf(v[16 * q + i], a16, nzi), 0.f), 3.f);
-          word += __float_as_uint(t + kMagic) << (2 * i);
+          const float t = __saturatef(fmaf(v[16 * q + i], a48, nzi3));
+          word += __float_as_uint(fmaf(t, 3.f, kMagic)) << (2 * i);
         }
         w[q] = word - kBitsSum;
       }
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
           const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t h[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) h[e] = f16x2(sat16(bf16_lo(wv[e])), sat16(bf16_hi(wv[e])));
+          for (int e = 0; e < 4; ++e) h[e] = f16x2_sat(bf16_lo(wv[e]), bf16_hi(wv[e]));
           *q = make_uint4(h[0], h[1], h[2], h[3]);
         }
       } else {
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
             const uint32_t wv[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
             uint32_t h[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = f16x2(sat16(bf16_lo(wv[e])), sat16(bf16_hi(wv[e])));
+            for (int e = 0; e < 4; ++e) h[e] = f16x2_sat(bf16_lo(wv[e]), bf16_hi(wv[e]));
             *reinterpret_cast<uint4*>(a + a_offset(j, 64 * half + 8 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
           }
         }
