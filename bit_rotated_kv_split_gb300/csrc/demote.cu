@@ -30,6 +30,14 @@ constexpr size_t kRedBytes = size_t(kWarps) * kHeadDim * 4;   // partial sums of
 constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
 
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
+  {
+    // L2 prefetch of this CTA's rotation (a hint that reads nothing, so it
+    // may precede the wait for the previous kernel)
+    const char* rg = reinterpret_cast<const char*>((blockIdx.y & 1 ? p.r_v : p.r_k) +
+                                                   int64_t(blockIdx.y >> 1) * kHeadDim * kHeadDim);
+    for (int i = threadIdx.x; i < int(kRotBytes / 128); i += kWarps * 32)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rg + 128 * i));
+  }
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
