@@ -711,8 +711,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   uint64_t* pro_done = bars + W * kStages + 2;   // q~ fragments ready (after R_K, R_V)
   constexpr int PT = Geo<G>::PT;
 
-  pdl_wait();                 // the previous kernel's writes are visible
-  pdl_launch_dependents();
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int pair = b * p.n_kv + hkv;
   const int n_splits = p.n_splits;
@@ -720,6 +718,29 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   const bool bf16_warp = warp >= W - kBf16Warps;
   const int gid = lane >> 2, tig = lane & 3;
   const int pbeg = split * p.pages_per_split;
+  // L2 prefetch of what the first phases read (R_K, this split's page-table
+  // entries, the query rows, the lengths): hints that read nothing, so they
+  // may precede the wait for the previous kernel
+  if (pbeg < p.max_pages) {
+    const char* rk = reinterpret_cast<const char*>(p.r_k + int64_t(hkv) * kHeadDim * kHeadDim);
+    for (int i = tid; i < kHeadDim * kHeadDim * 4 / 128; i += T)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rk + 128 * i));
+    if (warp == W - 1) {
+      const int32_t* row = p.page_table + int64_t(b) * p.max_pages + pbeg;
+      const int n = min(p.pages_per_split, p.max_pages - pbeg);
+      for (int i = 32 * lane; i < n; i += 32 * 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + i));
+      if (lane < 2 * G)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (int64_t(b) * p.n_kv * G + int64_t(hkv) * G) * kHeadDim + 64 * lane));
+      if (lane == 0) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.hist_len + b));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.sink_len + b));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.recent_len + b));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.recent_start + b));
+      }
+    }
+  }
+  pdl_wait();                 // the previous kernel's writes are visible
+  pdl_launch_dependents();
 
   // ---------------- R_K -> shared memory first: nothing it depends on
   if (tid == 0) {
