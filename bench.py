@@ -59,6 +59,9 @@ EXTRA_WORKLOADS = {
     "bulk-demote-128k-36layer": dict(batch=1, n_q_heads=32, n_kv_heads=8, ctx=131_072, layers=36,
                                      seed=1005, distinct_layers=2),
 }
+# calibration covariance on the device: C = X^T X / N over 2^20 bf16 rows of
+# 128 values (the C_Q / C_S accumulation of one KV head)
+CALIB_WORKLOAD = "calib-covariance-1m"
 CACHE_TENSORS = ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
                  "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status")
 
@@ -73,7 +76,7 @@ def _args():
     ap.add_argument("--reps", type=int, default=20, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD["workload"],
-                    choices=[WORKLOAD["workload"]] + sorted(EXTRA_WORKLOADS))
+                    choices=[WORKLOAD["workload"]] + sorted(EXTRA_WORKLOADS) + [CALIB_WORKLOAD])
     ap.add_argument("--rotation", default="oscar", choices=["oscar", "canalized32"],
                     help="R_K/R_V of the default workload: the OSCAR eigenbasis rotation, or the OScaR "
                          "block-diagonal one (Hadamard groups of 32 channels)")
@@ -853,6 +856,51 @@ def run_extra(args):
     print(json.dumps(line))
 
 
+def run_calibration(args):
+    """oscar_covariance over 2^20 seeded bf16 rows (256 MB, larger than L2): one
+    covariance per step, timed with CUDA events on the launching stream."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = 1 << 20
+    outl = synth.outlier_channels(1006, 0, 1)
+    x = synth.activations_device(1006, (70, 0), n, outl, dev).view(n, 128).contiguous()
+    c = torch.empty((128, 128), dtype=torch.float32, device=dev)
+    ws = torch.empty(B.oscar_covariance_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    K, W = args.steps, args.warmup
+    clocks = Clocks(0)
+    with torch.cuda.stream(stream):
+        for _ in range(max(W, 3)):
+            B.oscar_covariance(x, c, ws)
+        torch.cuda.synchronize()
+        clocks.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            B.oscar_covariance(x, c, ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+    t = e0.elapsed_time(e1) / K / 1e3
+    peak, peak_kind = _roofline_peak()
+    nbytes = n * 128 * 2
+    flops = 2.0 * n * 128 * 128
+    gbs = nbytes / t / 1e9
+    print(json.dumps({
+        "metric": "calibration covariance GB/s (2^20 bf16 rows of 128, C = X^T X / N)", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate", "data": "synthetic",
+        "config": {"workload": CALIB_WORKLOAD, "rows": n, "d": 128, "l2_policy": "input 256 MB > L2"},
+        "tflops": flops / t / 1e12,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "kernel": "covariance_partial_kernel (oscar_covariance)", "algorithmic_bytes": nbytes,
+                     "peak_kind": peak_kind + " hbm_gbs"},
+        "gpu_launches": 2 * K, "clocks": clk}))
+
+
 def main():
     args = _args()
     if args.cpu_baseline_worker:
@@ -860,6 +908,9 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload == CALIB_WORKLOAD:
+        run_calibration(args)
         return
     if args.workload != WORKLOAD["workload"]:
         run_extra(args)

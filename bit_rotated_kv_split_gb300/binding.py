@@ -50,6 +50,8 @@ def _load():
         "oscar_abi_version": (c_int32, []),
         "oscar_build_rotation": (c_int32, [P, c_int64, c_int32, P, P]),
         "oscar_build_canalized_rotation": (c_int32, [c_int32, c_int32, P]),
+        "oscar_build_rotation_from_covariance": (c_int32, [P, c_int32, P, P]),
+        "oscar_covariance": (c_int32, [P, c_int64, c_int32, c_int64, P, P, ctypes.POINTER(c_size_t), P]),
         "oscar_score_weighted_rows": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_double, P]),
         "oscar_clip_threshold": (c_int32, [P, c_int64, c_int32, c_int32, P, c_double, P]),
         "oscar_quantize_append": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
@@ -115,6 +117,31 @@ def oscar_build_canalized_rotation(d: int, block: int):
     r = np.empty((d, d), dtype=np.float64)
     _check("oscar_build_canalized_rotation", lib.oscar_build_canalized_rotation(d, block, r.ctypes.data))
     return r
+
+
+def oscar_build_rotation_from_covariance(c: np.ndarray):
+    """(R [d][d], eigenvalues [d]) from a covariance c [d][d] (host float64)."""
+    c = _f64(c)
+    d = c.shape[0]
+    r = np.empty((d, d), dtype=np.float64)
+    w = np.empty(d, dtype=np.float64)
+    _check("oscar_build_rotation_from_covariance",
+           lib.oscar_build_rotation_from_covariance(c.ctypes.data, d, r.ctypes.data, w.ctypes.data))
+    return r, w
+
+
+def oscar_covariance_workspace_bytes(n: int) -> int:
+    size = c_size_t(0)
+    _check("oscar_covariance", lib.oscar_covariance(None, int(n), 128, 128, None, None, ctypes.byref(size), None))
+    return size.value
+
+
+def oscar_covariance(x, c_out, workspace, stream=None) -> None:
+    """c_out [128][128] fp32 (device) = x^T x / n over the bf16 rows x [n][ld] (device)."""
+    n, ld = int(x.shape[0]), int(x.stride(0))
+    size = c_size_t(workspace.numel() * workspace.element_size())
+    _check("oscar_covariance", lib.oscar_covariance(_ptr(x), n, 128, ld, _ptr(c_out), _ptr(workspace),
+                                                    ctypes.byref(size), _stream(stream)))
 
 
 def oscar_score_weighted_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float = None):

@@ -120,8 +120,8 @@ struct Geo {
   static constexpr size_t kSmem = kStageBytes + kBarBytes + 1024 + kUnion + kBf16State + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-  // each warp's ring slice holds its two warp states at the end
-  static_assert(2 * G * kPartStride * 4 <= kStages * kBlockBytes, "warp states in the ring slice");
+  // each warp's ring slice holds its INT2 state once its pages are done
+  static_assert(G * kPartStride * 4 <= kStages * kBlockBytes, "warp state in the ring slice");
   // CTA merge scratch (after R_V in the union): merged outputs and weights
   static_assert((2 * G * kHeadDim + 32 * G) * 4 <= kQScratch, "CTA merge scratch");
   // ring region once the warp states are consumed: rotation quarters, then

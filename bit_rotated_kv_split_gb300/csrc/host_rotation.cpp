@@ -82,24 +82,10 @@ bool jacobi_eigen(std::vector<double>& a, int d, std::vector<double>& v, std::ve
 
 }  // namespace
 
-extern "C" oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t d, double* r_out,
-                                             double* eigvals_out) {
-  if (!x || !r_out || n < 1 || d < 2 || d > 1024 || !is_pow2(d)) return OSCAR_ERR_INVALID_ARG;
-  // C = x^T x / n (uncentred)
-  std::vector<double> c(size_t(d) * d, 0.0);
-  for (int64_t r = 0; r < n; ++r) {
-    const double* row = x + r * d;
-    for (int i = 0; i < d; ++i) {
-      const double xi = row[i];
-      double* ci = c.data() + size_t(i) * d;
-      for (int j = i; j < d; ++j) ci[j] += xi * row[j];
-    }
-  }
-  for (int i = 0; i < d; ++i)
-    for (int j = i; j < d; ++j) {
-      c[size_t(i) * d + j] /= double(n);
-      c[size_t(j) * d + i] = c[size_t(i) * d + j];
-    }
+namespace {
+
+// R = U . H . P from a symmetric covariance c[d][d] (destroyed).
+oscar_status rotation_from_cov(std::vector<double>& c, int d, double* r_out, double* eigvals_out) {
   std::vector<double> v, w;
   if (!jacobi_eigen(c, d, v, w)) return OSCAR_ERR_NO_CONVERGENCE;
   // order by descending eigenvalue; sign: largest-|entry| positive
@@ -137,6 +123,44 @@ extern "C" oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t
   for (int i = 0; i < d; ++i)
     for (int j = 0; j < d; ++j) r_out[size_t(i) * d + j] = uh[size_t(i) * d + bit_reverse(j, bits)];
   return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t d, double* r_out,
+                                             double* eigvals_out) {
+  if (!x || !r_out || n < 1 || d < 2 || d > 1024 || !is_pow2(d)) return OSCAR_ERR_INVALID_ARG;
+  // C = x^T x / n (uncentred)
+  std::vector<double> c(size_t(d) * d, 0.0);
+  for (int64_t r = 0; r < n; ++r) {
+    const double* row = x + r * d;
+    for (int i = 0; i < d; ++i) {
+      const double xi = row[i];
+      double* ci = c.data() + size_t(i) * d;
+      for (int j = i; j < d; ++j) ci[j] += xi * row[j];
+    }
+  }
+  for (int i = 0; i < d; ++i)
+    for (int j = i; j < d; ++j) {
+      c[size_t(i) * d + j] /= double(n);
+      c[size_t(j) * d + i] = c[size_t(i) * d + j];
+    }
+  return rotation_from_cov(c, d, r_out, eigvals_out);
+}
+
+// R from a covariance computed elsewhere (e.g. oscar_covariance on the
+// device): the symmetric part (c + c^T) / 2 is decomposed.
+extern "C" oscar_status oscar_build_rotation_from_covariance(const double* c, int32_t d, double* r_out,
+                                                             double* eigvals_out) {
+  if (!c || !r_out || d < 2 || d > 1024 || !is_pow2(d)) return OSCAR_ERR_INVALID_ARG;
+  std::vector<double> a(size_t(d) * d);
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) {
+      const double v = 0.5 * (c[size_t(i) * d + j] + c[size_t(j) * d + i]);
+      if (!std::isfinite(v)) return OSCAR_ERR_INVALID_ARG;
+      a[size_t(i) * d + j] = v;
+    }
+  return rotation_from_cov(a, d, r_out, eigvals_out);
 }
 
 extern "C" oscar_status oscar_score_weighted_rows(const double* q, int64_t n_q, const double* k,

@@ -125,4 +125,11 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- calibration
+// C = X^T X / n over n bf16 rows of 128 values (ld elements apart), split
+// over the rows into partials in `workspace`, added in a fixed order.
+size_t covariance_workspace_bytes(int64_t n);
+cudaError_t launch_covariance(const uint16_t* x, int64_t n, int64_t ld, float* c, void* workspace,
+                              cudaStream_t stream);
+
 }  // namespace oscar

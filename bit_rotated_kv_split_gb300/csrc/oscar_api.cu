@@ -170,3 +170,19 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   err = oscar::launch_decode(p, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
+
+// [GIST] 2.1 / 2.2 A: C_Q and C_S as one contraction over calibration rows.
+extern "C" oscar_status oscar_covariance(const uint16_t* x, int64_t n, int32_t d, int64_t ld, float* c_out,
+                                         void* workspace, size_t* workspace_bytes, void* stream) {
+  if (!workspace_bytes || n < 1 || d != 128 || ld < d) return OSCAR_ERR_INVALID_ARG;
+  const size_t need = oscar::covariance_workspace_bytes(n);
+  if (!workspace) {
+    *workspace_bytes = need;
+    return OSCAR_OK;
+  }
+  if (*workspace_bytes < need) return OSCAR_ERR_WORKSPACE;
+  if (!x || !c_out) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ld % 8) != 0 || !aligned(c_out, 16) || !aligned(workspace, 256)) return OSCAR_ERR_ALIGNMENT;
+  const cudaError_t err = oscar::launch_covariance(x, n, ld, c_out, workspace, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

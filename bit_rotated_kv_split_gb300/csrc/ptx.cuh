@@ -146,6 +146,15 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Four 8x8 b16 matrices from shared memory, transposed: lanes 8m..8m+7 give
+// the row addresses of matrix m; lane t receives rows 2 (t % 4), +1 of
+// column t / 4 of each matrix.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&d)[4], const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+               : "r"(smem_addr(row_addr)));
+}
+
 // D += A (16x16 bf16, row) * B (16x8 bf16, col), f32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {

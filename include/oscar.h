@@ -144,6 +144,34 @@ oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t d,
 oscar_status oscar_build_canalized_rotation(int32_t d, int32_t block, double* r_out);
 
 /*
+ * oscar_build_rotation_from_covariance - as oscar_build_rotation, from a
+ * covariance computed elsewhere (for instance by oscar_covariance on the
+ * device): c (host, [d][d] row-major, float64) is symmetrised as
+ * (c + c^T) / 2 and decomposed; r_out = U . H . P_br, eigvals_out (nullable)
+ * as in oscar_build_rotation.  OSCAR_ERR_INVALID_ARG for non-finite entries.
+ * Host-only, synchronous, thread-safe.
+ */
+oscar_status oscar_build_rotation_from_covariance(const double* c, int32_t d, double* r_out,
+                                                  double* eigvals_out);
+
+/*
+ * oscar_covariance - calibration covariance on the device.  [GIST] 2.1 and
+ * 2.2 A (C_Q = Q^T Q over calibration queries for R_K, C_S = (S V)^T (S V)
+ * for R_V, both divided by the number of rows).
+ *
+ *   c_out (device, [d][d] row-major, fp32) = X^T X / n over the n rows of x
+ *   (device, bf16, row r at x + r * ld, d = 128 values each).  Products of
+ *   bf16 values are exact in fp32; sums are fp32 over at most 2048 rows,
+ *   then over those partials in a fixed order (the result does not depend
+ *   on scheduling).  If workspace is NULL the required size is written to
+ *   *workspace_bytes and nothing runs; otherwise the call is asynchronous on
+ *   `stream`.  x 16-byte aligned, ld a multiple of 8, c_out 16-byte and the
+ *   workspace 256-byte aligned (OSCAR_ERR_ALIGNMENT); d must be 128.
+ */
+oscar_status oscar_covariance(const uint16_t* x, int64_t n, int32_t d, int64_t ld, float* c_out,
+                              void* workspace, size_t* workspace_bytes, void* stream);
+
+/*
  * oscar_score_weighted_rows - rows of S.V for the value covariance
  * C_S = (1/N) V^T S^T S V.  [GIST] 2.1 and 2.2 A.
  *

@@ -155,3 +155,32 @@ def test_canalized_rotation_matches_oracle(built_lib):
         with pytest.raises(B.OscarError) as err:
             B.oscar_build_canalized_rotation(d, block)
         assert err.value.status == 1
+
+
+def test_rotation_from_covariance_matches_row_builder(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    outl = synth.outlier_channels(41, 0, 1)
+    cal = synth.calibration_set(41, 0, 0, outl[0], n_q=2048, n_k=256)
+    r_rows, w_rows = B.oscar_build_rotation(cal["q"])
+    r_cov, w_cov = B.oscar_build_rotation_from_covariance(O.query_covariance(cal["q"]))
+    np.testing.assert_allclose(w_cov, w_rows, rtol=1e-12, atol=1e-12 * w_rows[0])
+    np.testing.assert_allclose(r_cov, r_rows, atol=1e-9)
+    bad = O.query_covariance(cal["q"])
+    bad[3, 5] = np.nan
+    with pytest.raises(B.OscarError) as err:
+        B.oscar_build_rotation_from_covariance(bad)
+    assert err.value.status == 1
+
+
+def test_covariance_rejects_bad_arguments(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    lib = B.lib
+    size = ctypes.c_size_t(0)
+    assert lib.oscar_covariance(None, 0, 128, 128, None, None, ctypes.byref(size), None) == 1
+    assert lib.oscar_covariance(None, 10, 64, 128, None, None, ctypes.byref(size), None) == 1
+    assert lib.oscar_covariance(None, 10, 128, 128, None, None, None, None) == 1
+    assert lib.oscar_covariance(None, 5000, 128, 128, None, None, ctypes.byref(size), None) == 0
+    assert size.value == 3 * 128 * 128 * 4
+    small = ctypes.c_size_t(size.value - 1)
+    assert lib.oscar_covariance(ctypes.c_void_p(256), 5000, 128, 128, ctypes.c_void_p(256), ctypes.c_void_p(256),
+                                ctypes.byref(small), None) == 3
