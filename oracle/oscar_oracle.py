@@ -35,6 +35,13 @@ is kept with the design notes):
     even); code = clamp(rint((x - z) / s), 0, 3) with ties to even; s == 0
     gives code 0.  Dequantised value: c * s + z.
   * Four codes per byte, channel 4j+i in bits 2i..2i+1 of byte j.
+  * Smaller quantisation groups (32 or 64 channels, K and V chosen apart):
+    group q of a token-head is the contiguous run of rotated channels
+    [q g, (q + 1) g), so the bit-reversal inside R decides which channels
+    share a group; each group has its own fp16 (scale, zero) by the rule
+    above.  With several groups the page stores a token's codes in a fixed
+    channel order of this build's format (`storage_channel`); one group per
+    token-head keeps channel order.
 """
 from __future__ import annotations
 
@@ -213,6 +220,37 @@ def dequantize(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.nda
             + np.asarray(zero, dtype=np.float64)[..., None])
 
 
+def quantize_groups(x_rot: np.ndarray, tau: float, group: int):
+    """`quantize` applied to each run of `group` consecutive rotated channels.
+
+    Returns (codes uint8 [..., d], scale float16 [..., d / group], zero
+    float16 [..., d / group]); group == d gives `quantize`'s values with a
+    trailing group axis of length 1.  [GIST] 2.2 A (bit-reversal balances the
+    dynamic range inside each quantisation group); [ZAKER] "OSCAR 把旋转对准
+    attention" (bit-reversal keeps an INT2 group from being ruled by a few
+    outlier channels).
+    """
+    x_rot = np.asarray(x_rot, dtype=np.float64)
+    d = x_rot.shape[-1]
+    if group <= 0 or d % group:
+        raise ValueError("group must divide the head dimension")
+    parts = [quantize(x_rot[..., q * group:(q + 1) * group], tau) for q in range(d // group)]
+    codes = np.concatenate([c for c, _, _ in parts], axis=-1)
+    scale = np.stack([s for _, s, _ in parts], axis=-1)
+    zero = np.stack([z for _, _, z in parts], axis=-1)
+    return codes, scale, zero
+
+
+def dequantize_groups(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """x^ = c * s_q + z_q with q the group of the channel (float64)."""
+    codes = np.asarray(codes)
+    ng = np.asarray(scale).shape[-1]
+    g = codes.shape[-1] // ng
+    s = np.repeat(np.asarray(scale, dtype=np.float64), g, axis=-1)
+    z = np.repeat(np.asarray(zero, dtype=np.float64), g, axis=-1)
+    return codes.astype(np.float64) * s + z
+
+
 def demote(x: np.ndarray, r: np.ndarray, tau: float):
     """Rotate -> clip -> quantise one or many token vectors x[..., d] with one R."""
     return quantize(rotate(x, r), tau)
@@ -308,6 +346,89 @@ def load_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: in
     return unpack(packed), sz[..., 0], sz[..., 1]
 
 
+# Grouped format.  A half (K or V) of a block with ng groups per token-head
+# holds 16 token rows of 32 code bytes, then 16 x ng (scale, zero) fp16
+# pairs, token-major: pair (slot, q) at 512 + 4 (slot ng + q).  One group per
+# token-head is exactly the format above.
+
+def half_bytes(ng: int) -> int:
+    """Bytes of one half of a block with ng quantisation groups per token-head."""
+    return PAGE_TOKENS * CODE_BYTES + PAGE_TOKENS * 4 * ng
+
+
+def block_bytes(ng_k: int, ng_v: int) -> int:
+    return half_bytes(ng_k) + half_bytes(ng_v)
+
+
+def storage_channel(which: int, ng: int, p: int) -> int:
+    """Rotated channel whose code sits at position p (byte p // 4, bits 2 (p % 4)).
+
+    This build's format; the pages fix none.  ng == 1: channel p.  ng > 1:
+    K (which 0): p = 32 t + 8 e + j (t, e < 4; j < 8) holds channel
+    (j // J) (128 / ng) + (j % J) 16 + 4 t + e with J = 8 / ng.
+    V (which 1): p = 16 a + 8 e + m (a < 8; e < 2; m < 8) holds channel
+    (m // M) (128 / ng) + (m % M) 16 + 2 a + e with M = 8 / ng.
+    Either way a channel's group is decided by j (K) or m (V) alone.
+    """
+    if ng == 1:
+        return p
+    gs = D_DEFAULT // ng
+    if which == 0:
+        t, e, j = p // 32, (p // 8) % 4, p % 8
+        jj = 8 // ng
+        return (j // jj) * gs + (j % jj) * 16 + 4 * t + e
+    a, e, m = p // 16, (p // 8) % 2, p % 8
+    mm = 8 // ng
+    return (m // mm) * gs + (m % mm) * 16 + 2 * a + e
+
+
+def storage_order(which: int, ng: int) -> np.ndarray:
+    """perm[p] = storage_channel(which, ng, p) for p < 128."""
+    return np.array([storage_channel(which, ng, p) for p in range(D_DEFAULT)], dtype=np.int64)
+
+
+def store_history_groups(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos0: int,
+                         codes: np.ndarray, scale16: np.ndarray, zero16: np.ndarray, which: int,
+                         ng_k: int, ng_v: int) -> None:
+    """Tokens pos0 .. pos0+T-1 of all KV heads into the grouped format.
+
+    codes [T][n_kv][128] in channel order, scale16 / zero16 [T][n_kv][ng].
+    """
+    ng = ng_k if which == 0 else ng_v
+    blk = block_bytes(ng_k, ng_v)
+    half0 = 0 if which == 0 else half_bytes(ng_k)
+    t_count = codes.shape[0]
+    pos = pos0 + np.arange(t_count)
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    slots = pos % PAGE_TOKENS
+    base = (pages[:, None] * n_kv + np.arange(n_kv)[None, :]) * blk + half0        # [T][n_kv]
+    packed = pack(np.asarray(codes)[..., storage_order(which, ng)])
+    co = base + slots[:, None] * CODE_BYTES
+    pool[co[..., None] + np.arange(CODE_BYTES)] = packed
+    pair = np.stack([scale16, zero16], axis=-1).astype(np.float16).view(np.uint8)   # [T][n_kv][4 ng]
+    so = base + PAGE_TOKENS * CODE_BYTES + 4 * ng * slots[:, None]
+    pool[so[..., None] + np.arange(4 * ng)] = pair.reshape(pair.shape[0], pair.shape[1], 4 * ng)
+
+
+def load_history_groups(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
+                        hist_len: int, which: int, ng_k: int, ng_v: int):
+    """(codes [T][n_kv][128] channel order, scale [T][n_kv][ng], zero [T][n_kv][ng])."""
+    ng = ng_k if which == 0 else ng_v
+    blk = block_bytes(ng_k, ng_v)
+    half0 = 0 if which == 0 else half_bytes(ng_k)
+    pos = np.arange(hist_len)
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    slots = pos % PAGE_TOKENS
+    base = (pages[:, None] * n_kv + np.arange(n_kv)[None, :]) * blk + half0
+    stored = unpack(pool[(base + slots[:, None] * CODE_BYTES)[..., None] + np.arange(CODE_BYTES)])
+    codes = np.empty_like(stored)
+    codes[..., storage_order(which, ng)] = stored
+    so = base + PAGE_TOKENS * CODE_BYTES + 4 * ng * slots[:, None]
+    sz = pool[so[..., None] + np.arange(4 * ng)].copy().view(np.float16)
+    sz = sz.reshape(sz.shape[0], sz.shape[1], ng, 2)
+    return codes, sz[..., 0], sz[..., 1]
+
+
 # --------------------------------------------------------------------------
 # 4. three-segment decode attention   [ZAKER] pipeline part; [GIST] 2.2 B
 # --------------------------------------------------------------------------
@@ -337,16 +458,21 @@ def decode_attention(q: np.ndarray, sink_k: np.ndarray, sink_v: np.ndarray,
     with R^T, the three segments are concatenated and one softmax is taken.
     [ZAKER] pipeline part (BF16 sink 64 | INT2 history | BF16 recent 256);
     [GIST] 2.2 B (inverse rotation inside attention); [CSDN] 三.1.
+    With several quantisation groups, scale_* / zero_* carry a trailing group
+    axis [Lh][H_kv][ng] and each channel uses its group's pair.
     """
     n_q = q.shape[0]
     n_kv = r_k.shape[0]
     g = n_q // n_kv
     out = np.zeros((n_q, q.shape[1]), dtype=np.float64)
+
+    def deq(which, kv):
+        c, s, z = hist["codes_" + which][:, kv], hist["scale_" + which][:, kv], hist["zero_" + which][:, kv]
+        return dequantize_groups(c, s, z) if np.ndim(s) == 2 else dequantize(c, s, z)
+
     for kv in range(n_kv):
-        k_hist = dequantize(hist["codes_k"][:, kv], hist["scale_k"][:, kv],
-                            hist["zero_k"][:, kv]) @ np.asarray(r_k[kv], dtype=np.float64).T
-        v_hist = dequantize(hist["codes_v"][:, kv], hist["scale_v"][:, kv],
-                            hist["zero_v"][:, kv]) @ np.asarray(r_v[kv], dtype=np.float64).T
+        k_hist = deq("k", kv) @ np.asarray(r_k[kv], dtype=np.float64).T
+        v_hist = deq("v", kv) @ np.asarray(r_v[kv], dtype=np.float64).T
         keys = np.concatenate([np.asarray(sink_k[:, kv], dtype=np.float64), k_hist,
                                np.asarray(recent_k[:, kv], dtype=np.float64)], axis=0)
         vals = np.concatenate([np.asarray(sink_v[:, kv], dtype=np.float64), v_hist,
@@ -389,15 +515,18 @@ def merge_states(states) -> np.ndarray:
 # 5. storage accounting   [ZAKER] "小模型也能守住高难推理"; [GIST] 4 (memory)
 # --------------------------------------------------------------------------
 
-def kv_bytes_per_history_token(n_kv: int, d: int = D_DEFAULT) -> int:
-    """Bytes per INT2 history token per layer: 2 (K,V) x n_kv x (d/4 codes + 4 s/z)."""
-    return 2 * n_kv * (d // 4 + 4)
+def kv_bytes_per_history_token(n_kv: int, d: int = D_DEFAULT, group_k: int = D_DEFAULT,
+                               group_v: int = D_DEFAULT) -> int:
+    """Bytes per INT2 history token per layer: n_kv x (K and V: d/4 codes + 4 per group)."""
+    return n_kv * (2 * (d // 4) + 4 * (d // group_k) + 4 * (d // group_v))
 
 
 def effective_bits_per_element(ctx: int, d: int = D_DEFAULT,
-                               sink: int = SINK_CAP, recent: int = RECENT_CAP) -> float:
-    """Average stored bits per K/V element over a context of `ctx` tokens."""
+                               sink: int = SINK_CAP, recent: int = RECENT_CAP,
+                               group: int = D_DEFAULT) -> float:
+    """Average stored bits per K (or V) element over a context of `ctx` tokens
+    (history: 2-bit codes plus a 32-bit (scale, zero) pair per group)."""
     bf16_tokens = min(ctx, sink + recent)
     hist = ctx - bf16_tokens
-    bits = bf16_tokens * d * 16 + hist * (2 * d + 32)
+    bits = bf16_tokens * d * 16 + hist * (2 * d + 32 * (d // group))
     return bits / (ctx * d)

@@ -420,3 +420,183 @@ def test_effective_bits_match_printed_values():
     # 576 B per history token-layer (8 KV heads) against 4096 B in BF16: 7.11x
     assert O.kv_bytes_per_history_token(8) == 576
     assert 4096 / O.kv_bytes_per_history_token(8) == pytest.approx(7.111, abs=1e-3)
+
+
+# ---------------------------------------------------------------- quantisation groups
+
+def test_quantize_groups_with_one_group_is_quantize():
+    g = synth.generator(7, 70)
+    x = g.standard_normal((9, 128)) * 2.0
+    c, s, z = O.quantize(x, 3.0)
+    cg, sg, zg = O.quantize_groups(x, 3.0, 128)
+    np.testing.assert_array_equal(cg, c)
+    np.testing.assert_array_equal(sg[..., 0].view(np.uint16), s.view(np.uint16))
+    np.testing.assert_array_equal(zg[..., 0].view(np.uint16), z.view(np.uint16))
+
+
+@pytest.mark.parametrize("group", [32, 64])
+def test_quantize_groups_arithmetic_progressions_closed_form(group):
+    # Group q holds a + k delta (k = 0..3 repeated) with a, delta exact in
+    # fp16 and every distance exact: codes are k, scale delta, zero a.
+    ng = 128 // group
+    a = np.array([-1.5, 0.25, 2.0, -0.125])[:ng]
+    delta = np.array([0.5, 0.125, 0.25, 1.0])[:ng]
+    k = np.tile(np.arange(4), group // 4)
+    x = np.concatenate([a[q] + delta[q] * k for q in range(ng)])
+    c, s, z = O.quantize_groups(x, 10.0, group)
+    np.testing.assert_array_equal(c, np.tile(k, ng))
+    np.testing.assert_array_equal(s.astype(np.float64), delta)
+    np.testing.assert_array_equal(z.astype(np.float64), a)
+
+
+@pytest.mark.parametrize("group", [32, 64])
+def test_quantize_groups_locality(group):
+    # A group's codes and (scale, zero) depend on its own channels only: an
+    # outlier planted in another group changes nothing in this one, while a
+    # single 128-channel group is changed by it.
+    g = synth.generator(8, 71)
+    x = g.standard_normal((5, 128))
+    y = x.copy()
+    y[:, 127] = 40.0
+    cx, sx, zx = O.quantize_groups(x, 50.0, group)
+    cy, sy, zy = O.quantize_groups(y, 50.0, group)
+    keep = 128 - group
+    np.testing.assert_array_equal(cx[:, :keep], cy[:, :keep])
+    np.testing.assert_array_equal(sx[:, :-1], sy[:, :-1])
+    np.testing.assert_array_equal(zx[:, :-1], zy[:, :-1])
+    assert not np.array_equal(O.quantize(x, 50.0)[1], O.quantize(y, 50.0)[1])
+    # dequantisation error within half a step of the channel's own group
+    xr = O.dequantize_groups(cy, sy, zy)
+    step = np.repeat(sy.astype(np.float64), group, axis=-1)
+    assert np.all(np.abs(xr - y) <= step / 2 + 1e-3 * step + 1e-12)
+
+
+def test_bit_reversal_balances_groups():
+    # The pages' stated purpose of P_br: with channels ordered by decreasing
+    # variance (an eigenbasis order), contiguous groups of 32 without P_br put
+    # all high-variance channels together; with P_br every group gets the
+    # same spread.  With one 128-channel group P_br only permutes the codes.
+    g = synth.generator(9, 72)
+    sd = 8.0 * 0.96 ** np.arange(128)
+    x = g.standard_normal((4000, 128)) * sd
+    xp = x @ O.bit_reversal_matrix(128)
+    _, s_plain, _ = O.quantize_groups(x, 1e4, 32)
+    _, s_br, _ = O.quantize_groups(xp, 1e4, 32)
+    ratio_plain = s_plain.astype(np.float64).mean(0).max() / s_plain.astype(np.float64).mean(0).min()
+    ratio_br = s_br.astype(np.float64).mean(0).max() / s_br.astype(np.float64).mean(0).min()
+    assert ratio_plain > 10.0 and ratio_br < 1.5
+    c1, s1, z1 = O.quantize(x[:50], 1e4)
+    c2, s2, z2 = O.quantize(xp[:50], 1e4)
+    np.testing.assert_array_equal(s1.view(np.uint16), s2.view(np.uint16))
+    np.testing.assert_array_equal(c1 @ O.bit_reversal_matrix(128), c2)
+
+
+def test_storage_channel_golden_and_permutation():
+    # hand-derived from the format definition (K: p = 32 t + 8 e + j,
+    # V: p = 16 a + 8 e + m)
+    assert O.storage_channel(0, 4, 51) == 54     # t 1, e 2, j 3: group 1, 16 + 4 + 2
+    assert O.storage_channel(0, 2, 51) == 54     # j 3 < 4: group 0, 48 + 4 + 2
+    assert O.storage_channel(0, 2, 6) == 96      # t 0, e 0, j 6: group 1, 64 + 32
+    assert O.storage_channel(1, 2, 61) == 87     # a 3, e 1, m 5: group 1, 64 + 16 + 7
+    assert O.storage_channel(1, 4, 15) == 113    # a 0, e 1, m 7: group 3, 96 + 16 + 1
+    for which in (0, 1):
+        assert list(O.storage_order(which, 1)) == list(range(128))
+        for ng in (2, 4):
+            assert sorted(O.storage_order(which, ng)) == list(range(128))
+
+
+@pytest.mark.parametrize("ng", [2, 4])
+def test_storage_order_makes_mma_operands_group_pure(ng):
+    # K: the 16 codes a tensor-core contraction step takes together sit at
+    # positions {32 t + 8 e + j : t, e < 4} for one j; V: a 16-row tile takes
+    # {16 a + 8 e + m : a < 8, e < 2} for one m.  Each such set must hold 16
+    # consecutive channels of one group.
+    gs = 128 // ng
+    for j in range(8):
+        ch = sorted(O.storage_channel(0, ng, 32 * t + 8 * e + j) for t in range(4) for e in range(4))
+        assert ch == list(range(ch[0], ch[0] + 16)) and ch[0] // gs == ch[-1] // gs
+    for m in range(8):
+        ch = sorted(O.storage_channel(1, ng, 16 * a + 8 * e + m) for a in range(8) for e in range(2))
+        assert ch == list(range(ch[0], ch[0] + 16)) and ch[0] // gs == ch[-1] // gs
+
+
+@pytest.mark.parametrize("ng_k,ng_v", [(1, 1), (2, 2), (4, 4), (4, 1), (1, 4)])
+def test_grouped_page_format_round_trip_and_offsets(ng_k, ng_v):
+    assert O.half_bytes(1) == 576 and O.half_bytes(2) == 640 and O.half_bytes(4) == 768
+    n_kv, n_pages = 2, 4
+    table = np.array([[3, 1, 0, 2]], np.int32)
+    pool = np.zeros(n_pages * n_kv * O.block_bytes(ng_k, ng_v), np.uint8)
+    g = synth.generator(10, 73)
+    t = 40
+    data = {}
+    for which, ng in ((0, ng_k), (1, ng_v)):
+        c = g.integers(0, 4, size=(t, n_kv, 128)).astype(np.uint8)
+        s = g.standard_normal((t, n_kv, ng)).astype(np.float16)
+        z = g.standard_normal((t, n_kv, ng)).astype(np.float16)
+        O.store_history_groups(pool, table, n_kv, 0, 0, c, s, z, which, ng_k, ng_v)
+        data[which] = (c, s, z)
+    for which in (0, 1):
+        c, s, z = O.load_history_groups(pool, table, n_kv, 0, t, which, ng_k, ng_v)
+        np.testing.assert_array_equal(c, data[which][0])
+        np.testing.assert_array_equal(s.view(np.uint16), data[which][1].view(np.uint16))
+        np.testing.assert_array_equal(z.view(np.uint16), data[which][2].view(np.uint16))
+    # one byte located by hand: token 21 (page 1, slot 5), KV head 1, V half;
+    # position p holds the code of channel storage_channel(1, ng_v, p)
+    blk = O.block_bytes(ng_k, ng_v)
+    base = (1 * n_kv + 1) * blk + O.half_bytes(ng_k) + 5 * 32
+    c_v = data[1][0]
+    for p in (0, 37, 127):
+        byte = pool[base + p // 4]
+        assert (byte >> (2 * (p % 4))) & 3 == c_v[21, 1, O.storage_channel(1, ng_v, p)]
+    so = (1 * n_kv + 1) * blk + O.half_bytes(ng_k) + 512 + 4 * (5 * ng_v + ng_v - 1)
+    pair = pool[so:so + 4].copy().view(np.float16)
+    assert pair[0] == data[1][1][21, 1, ng_v - 1] and pair[1] == data[1][2][21, 1, ng_v - 1]
+    if (ng_k, ng_v) == (1, 1):
+        # the grouped writer with one group is the original format
+        pool2 = np.zeros_like(pool)
+        for which in (0, 1):
+            c, s, z = data[which]
+            O.store_history_bulk(pool2, table, n_kv, 0, 0, O.pack(c), s[..., 0], z[..., 0], which)
+        np.testing.assert_array_equal(pool, pool2)
+
+
+def test_grouped_decode_reduces_to_plain_dequantisation():
+    # With ng groups whose (scale, zero) are all equal, grouped decode equals
+    # the one-group decode; with distinct pairs it equals the plain softmax
+    # over keys/values dequantised channel by channel.
+    g = synth.generator(11, 74)
+    n_kv, hq, lh = 2, 8, 30
+    r = np.stack([_orthogonal(128, 5), _orthogonal(128, 6)])
+    codes = g.integers(0, 4, size=(lh, n_kv, 128)).astype(np.uint8)
+    s1 = (np.abs(g.standard_normal((lh, n_kv))) * 0.3 + 0.05).astype(np.float16)
+    z1 = (g.standard_normal((lh, n_kv)) * 0.2).astype(np.float16)
+    q = g.standard_normal((hq, 128))
+    empty = np.zeros((0, n_kv, 128))
+    one = dict(codes_k=codes, scale_k=s1, zero_k=z1, codes_v=codes[::-1], scale_v=s1, zero_v=z1)
+    four = dict(codes_k=codes, scale_k=np.repeat(s1[..., None], 4, -1), zero_k=np.repeat(z1[..., None], 4, -1),
+                codes_v=codes[::-1], scale_v=np.repeat(s1[..., None], 4, -1), zero_v=np.repeat(z1[..., None], 4, -1))
+    a = O.decode_attention(q, empty, empty, one, empty, empty, r, r)
+    b = O.decode_attention(q, empty, empty, four, empty, empty, r, r)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+    s4 = (np.abs(g.standard_normal((lh, n_kv, 4))) * 0.3 + 0.05).astype(np.float16)
+    z4 = (g.standard_normal((lh, n_kv, 4)) * 0.2).astype(np.float16)
+    h = dict(codes_k=codes, scale_k=s4, zero_k=z4, codes_v=codes, scale_v=s4, zero_v=z4)
+    got = O.decode_attention(q, empty, empty, h, empty, empty, r, r)
+    for kv in range(n_kv):
+        deq = np.empty((lh, 128))
+        for t in range(lh):
+            for c in range(128):
+                deq[t, c] = codes[t, kv, c] * float(s4[t, kv, c // 32]) + float(z4[t, kv, c // 32])
+        keys = deq @ r[kv].T
+        for hh in range(kv * 4, kv * 4 + 4):
+            sc = keys @ q[hh] / math.sqrt(128)
+            p = np.exp(sc - sc.max())
+            np.testing.assert_allclose(got[hh], (p / p.sum()) @ keys, rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_storage_cost_closed_form():
+    # 2-bit codes plus one 32-bit (scale, zero) pair per group: 2 + 32 / g bits
+    assert O.effective_bits_per_element(10 ** 9, group=32) == pytest.approx(3.0, abs=1e-5)
+    assert O.effective_bits_per_element(10 ** 9, group=64) == pytest.approx(2.5, abs=1e-5)
+    assert O.kv_bytes_per_history_token(8, group_k=32, group_v=32) == 8 * (64 + 32)
+    assert O.kv_bytes_per_history_token(8) == 576
