@@ -37,6 +37,7 @@ class LayerDesc(ctypes.Structure):
         ("sink_k", c_void_p), ("sink_v", c_void_p), ("sink_len", c_void_p),
         ("recent_k", c_void_p), ("recent_v", c_void_p), ("recent_len", c_void_p),
         ("recent_start", c_void_p), ("r_k", c_void_p), ("r_v", c_void_p), ("dev_status", c_void_p),
+        ("quant_group_k", c_int32), ("quant_group_v", c_int32),
     ]
 
 
@@ -48,6 +49,7 @@ def _load():
     sig = {
         "oscar_status_string": (ctypes.c_char_p, [c_int32]),
         "oscar_abi_version": (c_int32, []),
+        "oscar_block_bytes": (c_int64, [c_int32, c_int32]),
         "oscar_build_rotation": (c_int32, [P, c_int64, c_int32, P, P]),
         "oscar_build_canalized_rotation": (c_int32, [c_int32, c_int32, P]),
         "oscar_build_rotation_from_covariance": (c_int32, [P, c_int32, P, P]),
@@ -96,6 +98,11 @@ def oscar_status_string(status: int) -> str:
 
 def oscar_abi_version() -> int:
     return lib.oscar_abi_version()
+
+
+def oscar_block_bytes(quant_group_k: int = 128, quant_group_v: int = 128) -> int:
+    """Bytes of one (page, KV head) block of the pool; 0 for an invalid group size."""
+    return lib.oscar_block_bytes(int(quant_group_k), int(quant_group_v))
 
 
 def _f64(a):

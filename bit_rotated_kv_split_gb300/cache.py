@@ -9,11 +9,10 @@ from __future__ import annotations
 
 import torch
 
-from .binding import LayerDesc
+from .binding import LayerDesc, oscar_block_bytes
 
 HEAD_DIM = 128
 PAGE_TOKENS = 16
-BLOCK_BYTES = 1152
 
 
 class LayerCache:
@@ -21,13 +20,18 @@ class LayerCache:
 
     def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, max_pages_per_seq: int,
                  n_pages: int, r_k: torch.Tensor, r_v: torch.Tensor, tau_k: float, tau_v: float,
-                 device="cuda", sink_cap: int = 64, recent_cap: int = 256):
+                 device="cuda", sink_cap: int = 64, recent_cap: int = 256, quant_group_k: int = 128,
+                 quant_group_v: int = 128):
         self.batch, self.n_q_heads, self.n_kv_heads = batch, n_q_heads, n_kv_heads
+        self.quant_group_k, self.quant_group_v = int(quant_group_k), int(quant_group_v)
+        self.block_bytes = oscar_block_bytes(self.quant_group_k, self.quant_group_v)
+        if self.block_bytes <= 0:
+            raise ValueError("quantisation group sizes must be 32, 64 or 128")
         self.sink_cap, self.recent_cap = sink_cap, recent_cap
         self.max_pages_per_seq, self.n_pages = max_pages_per_seq, n_pages
         self.tau_k, self.tau_v = float(tau_k), float(tau_v)
         dev = torch.device(device)
-        self.pages = torch.zeros(n_pages * n_kv_heads * BLOCK_BYTES, dtype=torch.uint8, device=dev)
+        self.pages = torch.zeros(n_pages * n_kv_heads * self.block_bytes, dtype=torch.uint8, device=dev)
         self.page_table = torch.full((batch, max_pages_per_seq), -1, dtype=torch.int32, device=dev)
         self.hist_len = torch.zeros(batch, dtype=torch.int32, device=dev)
         self.sink_len = torch.zeros(batch, dtype=torch.int32, device=dev)
@@ -53,6 +57,7 @@ class LayerCache:
         d.max_hist = self.max_hist if max_hist is None else int(max_hist)
         d.n_pages = self.n_pages
         d.tau_k, d.tau_v = self.tau_k, self.tau_v
+        d.quant_group_k, d.quant_group_v = self.quant_group_k, self.quant_group_v
         for name in ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
                      "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status"):
             setattr(d, name, getattr(self, name).data_ptr())

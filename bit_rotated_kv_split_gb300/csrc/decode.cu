@@ -91,7 +91,9 @@ constexpr int kMaxSplits = 128;               // bounds the last CTA's merge scr
 constexpr int kBf16Warps = 2;                 // warps that scan the BF16 sink/recent tokens
 constexpr uint32_t kPrologueBarrier = 1;      // named barrier of the q~ prologue
 
-template <int G>
+// NGK / NGV: quantisation groups per token-head of K / V (1, 2 or 4); they
+// fix the page block size and, through it, how many ring stages fit.
+template <int G, int NGK = 1, int NGV = 1>
 struct Geo {
   static constexpr int NT = (2 * G + 7) / 8;          // column tiles holding hi | lo parts
   static constexpr int HS = G >= 8 ? G / 4 : 2;       // BF16 head slots per lane
@@ -101,27 +103,35 @@ struct Geo {
   static constexpr int T = W * 32;
   // the last kBf16Warps warps scan the BF16 tokens while the others build q~
   static constexpr int PT = (W - kBf16Warps) * 32;
-  static constexpr int kStages = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;   // ring stages per warp
   static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : OSCAR_GROUP_G8;      // pages per step
   static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
-  static_assert(kGroup >= 1 && kGroup < kStages, "a step leaves copies in flight");
-  static constexpr size_t kStageBytes = size_t(W) * kStages * kBlockBytes;
-  // ring barriers + the R_K, R_V and prologue-done barriers, padded so the
-  // region after it stays 128-byte aligned (TMA destinations need at least 16)
-  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 3) * 8 + 127) / 128 * 128;
+  static constexpr int kBlock = block_bytes(NGK, NGV);   // one (page, KV head) block
+  static constexpr int kHalfK = half_bytes(NGK);         // offset of the V half
   // union: R_K (64 KB, prologue) then R_V (epilogue), followed by the q~
   // scratch (prologue) that the CTA merge reuses
   static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
-  static constexpr size_t kQScratch = (6 * G * kHeadDim + 12 * G + 32 * NH * 16) * 4;
+  static constexpr size_t kQScratch = (6 * G * kHeadDim + 16 * G + 32 * NH * 16) * 4;
   static constexpr size_t kUnion = kRotBytes + kQScratch;   // R_K then R_V | q~ scratch
   static constexpr size_t kBf16State = size_t(kBf16Warps) * G * kPartStride * 4;
+  // ring stages per warp: the tuned count, fewer when larger blocks (more
+  // quantisation groups) would not fit the 227 KB with everything else
+  static constexpr int kStagesTuned = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;
+  static constexpr int kStagesFit =
+      int((227 * 1024 - (1024 + kUnion + kBf16State + 16 + 1024)) / (size_t(W) * kBlock));
+  static constexpr int kStages = kStagesTuned < kStagesFit ? kStagesTuned : kStagesFit;
+  static_assert(kGroup >= 1 && kGroup < kStages, "a step leaves copies in flight");
+  static constexpr size_t kStageBytes = size_t(W) * kStages * kBlock;
+  // ring barriers + the R_K, R_V and prologue-done barriers, padded so the
+  // region after it stays 128-byte aligned (TMA destinations need at least 16)
+  static constexpr size_t kBarBytes = ((size_t(W) * kStages + 3) * 8 + 127) / 128 * 128;
+  static_assert(kBarBytes <= 1024, "barrier region within its budget");
   // (+1 KB: the union starts at the next 1024-byte boundary, which the
   // swizzled R_V boxes need)
   static constexpr size_t kSmem = kStageBytes + kBarBytes + 1024 + kUnion + kBf16State + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   // each warp's ring slice holds its INT2 state once its pages are done
-  static_assert(G * kPartStride * 4 <= kStages * kBlockBytes, "warp state in the ring slice");
+  static_assert(G * kPartStride * 4 <= kStages * kBlock, "warp state in the ring slice");
   // CTA merge scratch (after R_V in the union): merged outputs and weights
   static_assert((2 * G * kHeadDim + 32 * G) * 4 <= kQScratch, "CTA merge scratch");
   // ring region once the warp states are consumed: rotation quarters, then
@@ -250,11 +260,12 @@ struct WarpState {
 // INT2 state of a lane: heads 4 nt + tig (nt < G / 4), its tokens gid and
 // gid + 8 of each page; acc[nt][mt] holds output channels 16 gid + mt
 // (c < 2) and 16 gid + 8 + mt (c >= 2), columns hi (c even) and lo (c odd).
-template <int G>
+// z[nt][q]: the zero-point term sum p z_V of V group q.
+template <int G, int NGV>
 struct HistState {
   static constexpr int NH = Geo<G>::NH;
   float acc[NH][8][4];
-  float m[NH], l[NH], z[NH];
+  float m[NH], l[NH], z[NH][NGV];
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int nt = 0; nt < NH; ++nt) {
@@ -262,17 +273,21 @@ struct HistState {
       for (int mt = 0; mt < 8; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
       m[nt] = -INFINITY;
       l[nt] = 0.f;
-      z[nt] = 0.f;
+#pragma unroll
+      for (int q = 0; q < NGV; ++q) z[nt][q] = 0.f;
     }
   }
 };
 
-// QK of one INT2 page: d[nt] = 2^-24 sigma (q~ . c) of (token gid | gid + 8) x
-// (head 4 nt + tig hi, lo), K-steps spread over kQkChains accumulators.
-template <int G>
+// QK of one INT2 page: d[q][nt] = 2^-24 sigma (q~ . c) over K group q of
+// (token gid | gid + 8) x (head 4 nt + tig hi, lo).  With one group the
+// K-steps are spread over kQkChains accumulators; with NGK groups K-step j
+// reads group j / (8 / NGK) only (the page format's code order), so each
+// group has its own accumulator.
+template <int G, int NGK>
 __device__ __forceinline__ void int2_qk(const uint8_t* __restrict__ pg, int gid, int tig,
-                                        const uint32_t (&qb)[Geo<G>::NH][8][2], float (&d)[Geo<G>::NH][4]) {
-  constexpr int NH = Geo<G>::NH, kQkChains = Geo<G>::kQkChains;
+                                        const uint32_t (&qb)[Geo<G>::NH][8][2], float (&d)[NGK][Geo<G>::NH][4]) {
+  constexpr int NH = Geo<G>::NH, kQkChains = NGK > 1 ? NGK : Geo<G>::kQkChains;
   const uint2 kw0 = *reinterpret_cast<const uint2*>(pg + 32 * gid + 8 * tig);
   const uint2 kw1 = *reinterpret_cast<const uint2*>(pg + 32 * (gid + 8) + 8 * tig);
   float dc[kQkChains][NH][4];
@@ -287,31 +302,75 @@ __device__ __forceinline__ void int2_qk(const uint8_t* __restrict__ pg, int gid,
     const uint32_t a0 = code_pair(w00, s00, j), a1 = code_pair(w10, s10, j);
     const uint32_t a2 = code_pair(w01, s01, j), a3 = code_pair(w11, s11, j);
 #pragma unroll
-    for (int nt = 0; nt < NH; ++nt) mma_f16(dc[j % kQkChains][nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+    const int acc_i = NGK > 1 ? j / (8 / NGK) : j % kQkChains;
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) mma_f16(dc[acc_i][nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
   }
 #pragma unroll
   for (int nt = 0; nt < NH; ++nt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float v = dc[0][nt][c];
+      if constexpr (NGK > 1) {
 #pragma unroll
-      for (int ch = 1; ch < kQkChains; ++ch) v += dc[ch][nt][c];
-      d[nt][c] = v;
+        for (int q = 0; q < NGK; ++q) d[q][nt][c] = dc[q][nt][c];
+      } else {
+        float v = dc[0][nt][c];
+#pragma unroll
+        for (int ch = 1; ch < kQkChains; ++ch) v += dc[ch][nt][c];
+        d[0][nt][c] = v;
+      }
     }
+}
+
+// The NG (scale, zero) fp16 pairs of token slot t of a half (pairs start at
+// byte 512, token-major).
+template <int NG>
+__device__ __forceinline__ void load_sz(const uint8_t* half, int t, uint32_t (&sz)[NG]) {
+  const uint8_t* a = half + kCodeBytes + 4 * NG * t;
+  if constexpr (NG == 1) {
+    sz[0] = *reinterpret_cast<const uint32_t*>(a);
+  } else if constexpr (NG == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(a);
+    sz[0] = v.x;
+    sz[1] = v.y;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(a);
+    sz[0] = v.x;
+    sz[1] = v.y;
+    sz[2] = v.z;
+    sz[3] = v.w;
+  }
 }
 
 // Scores (log2 units) of the lane's two tokens of one page from its QK
 // accumulators and the tokens' K (scale, zero); -inf where not valid.
 // kMasked = false: every token of the page is valid (no selects).
-template <int G, bool kMasked>
-__device__ __forceinline__ void int2_scores(const float (&d)[Geo<G>::NH][4], uint32_t ksz0, uint32_t ksz1,
-                                            bool ok0, bool ok1, const float (&uns)[Geo<G>::NH],
-                                            const float (&qz)[Geo<G>::NH], float (&sc)[Geo<G>::NH][2]) {
-  const float2 kz0 = half2_to_float2(ksz0), kz1 = half2_to_float2(ksz1);
+// With NGK groups: score = unscale sum_q s_q (q~ . c)_q + sum_q z_q qz_q.
+template <int G, int NGK, bool kMasked>
+__device__ __forceinline__ void int2_scores(const float (&d)[NGK][Geo<G>::NH][4], const uint32_t (&ksz0)[NGK],
+                                            const uint32_t (&ksz1)[NGK], bool ok0, bool ok1,
+                                            const float (&uns)[Geo<G>::NH], const float (&qz)[Geo<G>::NH][NGK],
+                                            float (&sc)[Geo<G>::NH][2]) {
 #pragma unroll
   for (int nt = 0; nt < Geo<G>::NH; ++nt) {
-    const float s0 = fmaf(kz0.x * (d[nt][0] + d[nt][1]), uns[nt], kz0.y * qz[nt]);
-    const float s1 = fmaf(kz1.x * (d[nt][2] + d[nt][3]), uns[nt], kz1.y * qz[nt]);
+    float s0, s1;
+    if constexpr (NGK == 1) {
+      const float2 kz0 = half2_to_float2(ksz0[0]), kz1 = half2_to_float2(ksz1[0]);
+      s0 = fmaf(kz0.x * (d[0][nt][0] + d[0][nt][1]), uns[nt], kz0.y * qz[nt][0]);
+      s1 = fmaf(kz1.x * (d[0][nt][2] + d[0][nt][3]), uns[nt], kz1.y * qz[nt][0]);
+    } else {
+      float a0 = 0.f, a1 = 0.f, z0 = 0.f, z1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < NGK; ++q) {
+        const float2 kz0 = half2_to_float2(ksz0[q]), kz1 = half2_to_float2(ksz1[q]);
+        a0 = fmaf(kz0.x, d[q][nt][0] + d[q][nt][1], a0);
+        a1 = fmaf(kz1.x, d[q][nt][2] + d[q][nt][3], a1);
+        z0 = fmaf(kz0.y, qz[nt][q], z0);
+        z1 = fmaf(kz1.y, qz[nt][q], z1);
+      }
+      s0 = fmaf(a0, uns[nt], z0);
+      s1 = fmaf(a1, uns[nt], z1);
+    }
     sc[nt][0] = (!kMasked || ok0) ? s0 : -INFINITY;
     sc[nt][1] = (!kMasked || ok1) ? s1 : -INFINITY;
   }
@@ -319,8 +378,8 @@ __device__ __forceinline__ void int2_scores(const float (&d)[Geo<G>::NH][4], uin
 
 // Lazy online-softmax maximum over a step's scores: raised only when a score
 // exceeds it by 2^kRescaleLog2; the 8 lanes of a column group share a head.
-template <int G, int P>
-__device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH][2], HistState<G>& st) {
+template <int G, int NGV, int P>
+__device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH][2], HistState<G, NGV>& st) {
   constexpr int NH = Geo<G>::NH;
   bool need = false;
 #pragma unroll
@@ -340,7 +399,8 @@ __device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH]
       const float f = exp2f(st.m[nt] - pm);
       st.m[nt] = pm;
       st.l[nt] *= f;
-      st.z[nt] *= f;
+#pragma unroll
+      for (int q = 0; q < NGV; ++q) st.z[nt][q] *= f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         st.acc[nt][mt][0] *= f;
@@ -354,45 +414,57 @@ __device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH]
 
 // Probabilities of one page -> PV B fragments: the lane packs (hi, lo) of
 // p s_V sigma_v for token gid (row gid, columns 2 tig, 2 tig + 1) and token
-// gid + 8; movmatrix transposes them into the B layout (rows = tokens).
+// gid + 8; movmatrix transposes them into the B layout (rows = tokens).  With
+// NGV groups there is one operand per V group q (its own s_V), and the
+// zero-point term accumulates per group.
 // (kMasked = false: every token valid, so stale ring bytes never reach a
 // product and no select is needed.)
-template <int G, bool kMasked>
-__device__ __forceinline__ void int2_probs(const float (&sc)[Geo<G>::NH][2], uint32_t vsz0, uint32_t vsz1,
-                                           bool ok0, bool ok1, float sigma_v, HistState<G>& st,
-                                           uint32_t (&pb)[Geo<G>::NH][2]) {
-  const float2 vz0 = half2_to_float2(vsz0), vz1 = half2_to_float2(vsz1);
-  const float sv0 = vz0.x * sigma_v, sv1 = vz1.x * sigma_v;
+template <int G, int NGV, bool kMasked>
+__device__ __forceinline__ void int2_probs(const float (&sc)[Geo<G>::NH][2], const uint32_t (&vsz0)[NGV],
+                                           const uint32_t (&vsz1)[NGV], bool ok0, bool ok1, float sigma_v,
+                                           HistState<G, NGV>& st, uint32_t (&pb)[NGV][Geo<G>::NH][2]) {
+  float2 vz0[NGV], vz1[NGV];
+#pragma unroll
+  for (int q = 0; q < NGV; ++q) {
+    vz0[q] = half2_to_float2(vsz0[q]);
+    vz1[q] = half2_to_float2(vsz1[q]);
+  }
 #pragma unroll
   for (int nt = 0; nt < Geo<G>::NH; ++nt) {
     float p0 = fast_exp2(sc[nt][0] - st.m[nt]);
     float p1 = fast_exp2(sc[nt][1] - st.m[nt]);
-    float q0, q1;
     if constexpr (kMasked) {
       p0 = ok0 ? p0 : 0.f;
       p1 = ok1 ? p1 : 0.f;
-      st.l[nt] += p0 + p1;
-      st.z[nt] += (ok0 ? p0 * vz0.y : 0.f) + (ok1 ? p1 * vz1.y : 0.f);
-      q0 = ok0 ? p0 * sv0 : 0.f;
-      q1 = ok1 ? p1 * sv1 : 0.f;
-    } else {
-      st.l[nt] += p0 + p1;
-      st.z[nt] = fmaf(p0, vz0.y, fmaf(p1, vz1.y, st.z[nt]));
-      q0 = p0 * sv0;
-      q1 = p1 * sv1;
     }
-    const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
-    const __half l0 = __float2half_rn(q0 - __half2float(h0)), l1 = __float2half_rn(q1 - __half2float(h1));
-    pb[nt][0] = movmatrix_trans(uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(l0)) << 16));
-    pb[nt][1] = movmatrix_trans(uint32_t(__half_as_ushort(h1)) | (uint32_t(__half_as_ushort(l1)) << 16));
+    st.l[nt] += p0 + p1;
+#pragma unroll
+    for (int q = 0; q < NGV; ++q) {
+      float q0, q1;
+      if constexpr (kMasked) {
+        st.z[nt][q] += (ok0 ? p0 * vz0[q].y : 0.f) + (ok1 ? p1 * vz1[q].y : 0.f);
+        q0 = ok0 ? p0 * (vz0[q].x * sigma_v) : 0.f;
+        q1 = ok1 ? p1 * (vz1[q].x * sigma_v) : 0.f;
+      } else {
+        st.z[nt][q] = fmaf(p0, vz0[q].y, fmaf(p1, vz1[q].y, st.z[nt][q]));
+        q0 = p0 * (vz0[q].x * sigma_v);
+        q1 = p1 * (vz1[q].x * sigma_v);
+      }
+      const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
+      const __half l0 = __float2half_rn(q0 - __half2float(h0)), l1 = __float2half_rn(q1 - __half2float(h1));
+      pb[q][nt][0] = movmatrix_trans(uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(l0)) << 16));
+      pb[q][nt][1] = movmatrix_trans(uint32_t(__half_as_ushort(h1)) | (uint32_t(__half_as_ushort(l1)) << 16));
+    }
   }
 }
 
-// PV of one INT2 page: acc[nt][mt] += codes^T . P, channel 16 gid + mt (+8).
-template <int G>
+// PV of one INT2 page: acc[nt][mt] += codes^T . P, code positions 16 gid + mt
+// (+8); 16-row tile mt holds V group mt / (8 / NGV) (the page format's code
+// order) and takes that group's operand.  kHalfK: offset of the V half.
+template <int G, int NGV, int kHalfK>
 __device__ __forceinline__ void int2_pv(const uint8_t* __restrict__ pg, int gid, int tig,
-                                        const uint32_t (&pb)[Geo<G>::NH][2], HistState<G>& st) {
-  const uint8_t* pv = pg + kHalfBytes;
+                                        const uint32_t (&pb)[NGV][Geo<G>::NH][2], HistState<G, NGV>& st) {
+  const uint8_t* pv = pg + kHalfK;
   const uint32_t va = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 4 * gid);
   const uint32_t vb = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 32 + 4 * gid);
   const uint32_t vc = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 256 + 4 * gid);
@@ -404,29 +476,35 @@ __device__ __forceinline__ void int2_pv(const uint8_t* __restrict__ pg, int gid,
   for (int mt = 0; mt < 8; ++mt) {
     const uint32_t a0 = code_pair(x0l, y0l, mt), a1 = code_pair(x0h, y0h, mt);
     const uint32_t a2 = code_pair(x8l, y8l, mt), a3 = code_pair(x8h, y8h, mt);
+    const int q = mt / (8 / NGV);
 #pragma unroll
-    for (int nt = 0; nt < Geo<G>::NH; ++nt) mma_f16(st.acc[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+    for (int nt = 0; nt < Geo<G>::NH; ++nt) mma_f16(st.acc[nt][mt], a0, a1, a2, a3, pb[q][nt][0], pb[q][nt][1]);
   }
 }
 
 // INT2 warp state -> ws[h * kPartStride + (0, 1, 4 + channel)] in the
-// rotated basis: o~ = (hi + lo) 2^24 4^-pos(mt) / sigma_v + zeta.
-template <int G>
-__device__ __forceinline__ void store_hist_state(HistState<G>& st, float* ws, int gid, int tig, float pv_unscale) {
+// rotated basis: o~ = (hi + lo) 2^24 4^-pos(mt) / sigma_v + zeta_q, where
+// code position c = 16 gid + mt (+8) holds the page format's V channel.
+template <int G, int NGV>
+__device__ __forceinline__ void store_hist_state(HistState<G, NGV>& st, float* ws, int gid, int tig,
+                                                 float pv_unscale) {
   constexpr int NH = Geo<G>::NH;
 #pragma unroll
   for (int nt = 0; nt < NH; ++nt) {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       st.l[nt] += __shfl_xor_sync(kFull, st.l[nt], o);
-      st.z[nt] += __shfl_xor_sync(kFull, st.z[nt], o);
+#pragma unroll
+      for (int q = 0; q < NGV; ++q) st.z[nt][q] += __shfl_xor_sync(kFull, st.z[nt][q], o);
     }
     const int h = 4 * nt + tig;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const float f = pv_unscale * __int_as_float((127 - 2 * code_pos(mt)) << 23);
-      ws[h * kPartStride + 4 + 16 * gid + mt] = fmaf(st.acc[nt][mt][0] + st.acc[nt][mt][1], f, st.z[nt]);
-      ws[h * kPartStride + 4 + 16 * gid + 8 + mt] = fmaf(st.acc[nt][mt][2] + st.acc[nt][mt][3], f, st.z[nt]);
+      const float zq = st.z[nt][mt / (8 / NGV)];
+      const int c0 = storage_channel_v(NGV, 16 * gid + mt), c8 = storage_channel_v(NGV, 16 * gid + 8 + mt);
+      ws[h * kPartStride + 4 + c0] = fmaf(st.acc[nt][mt][0] + st.acc[nt][mt][1], f, zq);
+      ws[h * kPartStride + 4 + c8] = fmaf(st.acc[nt][mt][2] + st.acc[nt][mt][3], f, zq);
     }
     if (gid == 0) {
       ws[h * kPartStride + 0] = st.m[nt];
@@ -574,11 +652,11 @@ __device__ __forceinline__ void store_warp_state(WarpState<G>& st, float* ws, in
 // ------------------------------------------------------------------ q~ and its fragments
 
 // Shared-memory scratch of the prologue, in floats: qs[G][128] | part[4][G][128]
-// | qt[G][128] | aux[G][4] | red[2][G][4] | frag[32][NH*16] (u32).
+// | qt[G][128] | aux[G][8] | red[2][G][4] | frag[32][NH*16] (u32).
 template <int G>
 struct QScratch {
   static constexpr int kQs = 0, kPart = G * kHeadDim, kQt = 5 * G * kHeadDim, kAux = 6 * G * kHeadDim;
-  static constexpr int kRed = kAux + 4 * G, kFrag = kRed + 8 * G;
+  static constexpr int kRed = kAux + 8 * G, kFrag = kRed + 8 * G;
   static constexpr int kFloats = kFrag + 32 * Geo<G>::NH * 16;
   static_assert(kFrag % 4 == 0, "fragment rows are read as uint4");
 };
@@ -590,9 +668,11 @@ struct QScratch {
 // 32 lanes' B fragments of the QK MMA are built once per CTA: column
 // gid of column tile nt is the hi (gid even) or lo (gid odd) part of head
 // 4 nt + gid / 2; register r = 0 holds channels (32tig + j, 32tig + j + 8),
-// r = 1 (32tig + 16 + j, 32tig + 24 + j), each scaled by sigma 4^-pos(j).
-// aux[h] = (sigma, unscale, qz).
-template <int G>
+// r = 1 (32tig + 16 + j, 32tig + 24 + j), each scaled by sigma 4^-pos(j);
+// these are code positions, holding the page format's K channels for NGK
+// groups.  aux[h] = (sigma, unscale, qz[0 .. NGK-1]), qz[q] the scaled sum
+// of q~ over K group q.
+template <int G, int NGK>
 __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float* rks, uint64_t* rbar,
                              float* scratch) {
   constexpr int T = Geo<G>::PT, NH = Geo<G>::NH;
@@ -651,13 +731,22 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
     return max(-100, min(100, e));
   };
   if (tid < G) {
-    const float sm = ((red[4 * G + tid * 4] + red[4 * G + tid * 4 + 1]) + red[4 * G + tid * 4 + 2]) +
-                     red[4 * G + tid * 4 + 3];
+    // sums of q~ over 32-channel chunks; K group q spans chunks
+    // [q 4 / NGK, (q + 1) 4 / NGK)
+    const float* rs = red + 4 * G + tid * 4;
     const int e = sigma_exp(tid);
     const float scale = kLog2e * rsqrtf(float(kHeadDim));
-    aux[tid * 4 + 0] = __int_as_float((127 + e) << 23);
-    aux[tid * 4 + 1] = __int_as_float((151 - e) << 23) * scale;   // 2^24 / sigma * log2(e) / sqrt(d)
-    aux[tid * 4 + 2] = sm * scale;
+    aux[tid * 8 + 0] = __int_as_float((127 + e) << 23);
+    aux[tid * 8 + 1] = __int_as_float((151 - e) << 23) * scale;   // 2^24 / sigma * log2(e) / sqrt(d)
+    if constexpr (NGK == 1) {
+      aux[tid * 8 + 2] = (((rs[0] + rs[1]) + rs[2]) + rs[3]) * scale;
+    } else if constexpr (NGK == 2) {
+      aux[tid * 8 + 2] = (rs[0] + rs[1]) * scale;
+      aux[tid * 8 + 3] = (rs[2] + rs[3]) * scale;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) aux[tid * 8 + 2 + q] = rs[q] * scale;
+    }
   }
   for (int idx = tid; idx < 32 * NH * 16; idx += T) {
     const int ln = idx / (NH * 16), rem = idx % (NH * 16);
@@ -665,8 +754,9 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
     const int gid = ln >> 2, tig = ln & 3;
     const int h = 4 * nt + gid / 2;
     const float f = __int_as_float((127 + sigma_exp(h) - 2 * code_pos(j)) << 23);   // sigma 4^-pos(j)
-    const int c0 = 32 * tig + 16 * rr + j;
-    float v0 = qt[h * kHeadDim + c0] * f, v1 = qt[h * kHeadDim + c0 + 8] * f;
+    const int c0 = 32 * tig + 16 * rr + j;   // code position; +8: the pair's second
+    float v0 = qt[h * kHeadDim + storage_channel_k(NGK, c0)] * f;
+    float v1 = qt[h * kHeadDim + storage_channel_k(NGK, c0 + 8)] * f;
     if (gid & 1) {
       v0 = split_lo(v0);
       v1 = split_lo(v1);
@@ -694,15 +784,17 @@ struct PidWindow {
 
 // ------------------------------------------------------------------ split kernel
 
-template <int G>
+template <int G, int NGK, int NGV>
 __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_constant__ DecodeParams p) {
+  using Gm = Geo<G, NGK, NGV>;
   constexpr int NTQ = Geo<G>::NTQ, W = Geo<G>::W, T = Geo<G>::T;
-  constexpr int kStages = Geo<G>::kStages;
+  constexpr int kStages = Gm::kStages;
+  constexpr int kBlock = Gm::kBlock;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stage = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo<G>::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::kStageBytes);
   uint64_t* rbar = bars + W * kStages;       // R_K; rbar + 1: R_V
-  uint8_t* uni = smem + Geo<G>::kStageBytes + Geo<G>::kBarBytes;
+  uint8_t* uni = smem + Gm::kStageBytes + Gm::kBarBytes;
   uni += (1024u - (smem_addr(uni) & 1023u)) & 1023u;
   float* rks = reinterpret_cast<float*>(uni);                         // prologue only
   float* qscratch = reinterpret_cast<float*>(uni + Geo<G>::kRotBytes);
@@ -776,10 +868,10 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   const int spec_end = min(pbeg + p.pages_per_split, p.max_pages);
   PidWindow issue_ids;
   int hist = p.hist_len[b];
-  uint8_t* ring = stage + size_t(warp) * kStages * kBlockBytes;
+  uint8_t* ring = stage + size_t(warp) * kStages * kBlock;
   uint64_t* bar = bars + warp * kStages;
-  const uint8_t* pool = p.pages + int64_t(hkv) * kBlockBytes;
-  const int64_t page_stride = int64_t(p.n_kv) * kBlockBytes;
+  const uint8_t* pool = p.pages + int64_t(hkv) * kBlock;
+  const int64_t page_stride = int64_t(p.n_kv) * kBlock;
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar + s, 1);
     fence_mbar_init();
@@ -796,8 +888,8 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         // no copy: complete the stage's phase without bytes so the ring stays in step
         mbar_arrive(bar + s);
       } else {
-        mbar_arrive_expect_tx(bar + s, kBlockBytes);
-        bulk_copy_g2s(ring + s * kBlockBytes, pool + int64_t(pid) * page_stride, kBlockBytes, bar + s);
+        mbar_arrive_expect_tx(bar + s, kBlock);
+        bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid) * page_stride, kBlock, bar + s);
       }
     }
   };
@@ -832,7 +924,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // once the prologue is done
   constexpr int NH = Geo<G>::NH;
   uint32_t qb[NH][8][2];
-  float unscale[NH], qz[NH];
+  float unscale[NH], qz[NH][NGK];
   const bool any_pages = pend > pbeg;
   float* rvs = rks;
   uint64_t* vbar = rbar + 1;
@@ -851,13 +943,14 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
 #pragma unroll
     for (int nt = 0; nt < NH; ++nt) {
       const int h = 4 * nt + tig;
-      unscale[nt] = qscratch[S::kAux + h * 4 + 1];
-      qz[nt] = qscratch[S::kAux + h * 4 + 2];
+      unscale[nt] = qscratch[S::kAux + h * 8 + 1];
+#pragma unroll
+      for (int q = 0; q < NGK; ++q) qz[nt][q] = qscratch[S::kAux + h * 8 + 2 + q];
     }
   };
   if (!bf16_warp) {
     if (any_pages) {
-      rotate_query<G>(p, b, hkv, rks, rbar, qscratch);
+      rotate_query<G, NGK>(p, b, hkv, rks, rbar, qscratch);
       load_fragments();
     } else if (tid == 0 && pbeg < p.max_pages) {
       // R_K was requested: let it land before this region is reused
@@ -948,7 +1041,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // warp's range or with an invalid id is computed on stale ring data with
   // every token masked (uniform control flow, no effect on the result).
   {
-    HistState<G> st;
+    HistState<G, NGV> st;
     st.init();
     bool timed_out = false;
     int k = 0;
@@ -970,7 +1063,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
       uint32_t ph_u = phase;
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
-        pg[u] = ring + s_u * kBlockBytes;
+        pg[u] = ring + s_u * kBlock;
         if ((u == 0 || k + u < count) && !mbar_wait_bounded(bar + s_u, ph_u, kWaitLimitNs)) timed_out = true;
         if (++s_u == kStages) {
           s_u = 0;
@@ -1007,21 +1100,23 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
             for (int nt = 0; nt < NH; ++nt) sc[u][nt][0] = sc[u][nt][1] = -INFINITY;
             continue;
           }
-          float d[NH][4];
-          int2_qk<G>(pg[u], gid, tig, qb, d);
-          const uint32_t ksz0 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * gid);
-          const uint32_t ksz1 = *reinterpret_cast<const uint32_t*>(pg[u] + 512 + 4 * (gid + 8));
-          int2_scores<G, kMasked>(d, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
+          float d[NGK][NH][4];
+          int2_qk<G, NGK>(pg[u], gid, tig, qb, d);
+          uint32_t ksz0[NGK], ksz1[NGK];
+          load_sz<NGK>(pg[u], gid, ksz0);
+          load_sz<NGK>(pg[u], gid + 8, ksz1);
+          int2_scores<G, NGK, kMasked>(d, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
         }
-        int2_update_max<G, kGroup>(sc, st);
+        int2_update_max<G, NGV, kGroup>(sc, st);
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
           if (kMasked && u > 0 && k + u >= count) continue;
-          const uint32_t vsz0 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * gid);
-          const uint32_t vsz1 = *reinterpret_cast<const uint32_t*>(pg[u] + kHalfBytes + 512 + 4 * (gid + 8));
-          uint32_t pb[NH][2];
-          int2_probs<G, kMasked>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
-          int2_pv<G>(pg[u], gid, tig, pb, st);
+          uint32_t vsz0[NGV], vsz1[NGV];
+          load_sz<NGV>(pg[u] + Gm::kHalfK, gid, vsz0);
+          load_sz<NGV>(pg[u] + Gm::kHalfK, gid + 8, vsz1);
+          uint32_t pb[NGV][NH][2];
+          int2_probs<G, NGV, kMasked>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
+          int2_pv<G, NGV, Gm::kHalfK>(pg[u], gid, tig, pb, st);
         }
       };
       if (all_full) {
@@ -1045,8 +1140,8 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
           if (!good) {
             mbar_arrive(bar + s);   // no copy: complete the phase without bytes
           } else {
-            mbar_arrive_expect_tx(bar + s, kBlockBytes);
-            bulk_copy_g2s(ring + s * kBlockBytes, pool + int64_t(pid) * page_stride, kBlockBytes, bar + s);
+            mbar_arrive_expect_tx(bar + s, kBlock);
+            bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid) * page_stride, kBlock, bar + s);
           }
         }
         const uint32_t want_bits = __ballot_sync(kFull, want) & kGroupBits;
@@ -1075,7 +1170,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         mbar_wait_bounded(bar + kk % kStages, (kk / kStages) & 1, kWaitLimitNs);
     }
     __syncwarp();
-    store_hist_state<G>(st, my_state, gid, tig, p.pv_unscale);
+    store_hist_state<G, NGV>(st, my_state, gid, tig, p.pv_unscale);
   }
 
   __syncthreads();
@@ -1088,7 +1183,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   float* os = qscratch;                       // [G][128] merged history output (rotated basis)
   float* ob = os + G * kHeadDim;              // [G][128] merged BF16 output
   float* wts = ob + G * kHeadDim;             // [G][32] state weights
-  const int slice = kStages * kBlockBytes / 4;   // floats between two warps' states
+  const int slice = kStages * kBlock / 4;   // floats between two warps' states
   const float* states = reinterpret_cast<const float*>(stage);
   float* part = p.partials + (int64_t(pair) * n_splits + split) * G * kPartStride;
   static_assert(W + kBf16Warps <= 32, "one lane per warp state");
@@ -1248,23 +1343,43 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   }
 }
 
+// (every group variant also holds one CTA per SM: the planning uses the
+// one-group kernel)
 template <int G>
 int occupancy() {
   int occ = 0;
-  cudaFuncSetAttribute(split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Geo<G>::kSmem));
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<G>, Geo<G>::T, Geo<G>::kSmem) !=
+  cudaFuncSetAttribute(split_kernel<G, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       int(Geo<G>::kSmem));
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<G, 1, 1>, Geo<G>::T, Geo<G>::kSmem) !=
       cudaSuccess)
     return 0;
   return occ;
 }
 
-template <int G>
+template <int G, int NGK, int NGV>
 cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(Geo<G>::kSmem));
+  constexpr size_t smem = Geo<G, NGK, NGV>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(split_kernel<G, NGK, NGV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(split_kernel<G>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T), Geo<G>::kSmem,
+  return launch_pdl(split_kernel<G, NGK, NGV>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T), smem,
                     stream, p);
+}
+
+template <int G, int NGK>
+cudaError_t launch_gk(const DecodeParams& p, cudaStream_t stream) {
+  if (p.ng_v == 1) return launch_g<G, NGK, 1>(p, stream);
+  if (p.ng_v == 2) return launch_g<G, NGK, 2>(p, stream);
+  if (p.ng_v == 4) return launch_g<G, NGK, 4>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+template <int G>
+cudaError_t launch_gq(const DecodeParams& p, cudaStream_t stream) {
+  if (p.ng_k == 1) return launch_gk<G, 1>(p, stream);
+  if (p.ng_k == 2) return launch_gk<G, 2>(p, stream);
+  if (p.ng_k == 4) return launch_gk<G, 4>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1353,8 +1468,8 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  if (p.group == 4) return launch_g<4>(p, stream);
-  if (p.group == 8) return launch_g<8>(p, stream);
+  if (p.group == 4) return launch_gq<4>(p, stream);
+  if (p.group == 8) return launch_gq<8>(p, stream);
   return cudaErrorInvalidValue;
 }
 

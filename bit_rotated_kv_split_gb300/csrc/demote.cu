@@ -11,9 +11,10 @@
 // is staged into shared memory by four TMA bulk copies (one barrier per
 // quarter of its rows), then the CTA demotes its items one after another,
 // all four warps on each: warp w sums the inputs i in [32 w, 32 w + 32)
-// for every output, lane l owning rotated channels 4l..4l+3 (one code
-// byte); the four partial sums meet in shared memory, and warp 0 clips,
-// quantises and packs.  Splitting the inputs over the warps shortens the
+// for every output, lane l owning rotated channels 4l..4l+3; the four
+// partial sums meet in shared memory, and warp 0 clips, quantises (per
+// quantisation group) and packs, lane l forming code byte l of the page
+// format.  Splitting the inputs over the warps shortens the
 // dependent chain of a lone item (a decode step demotes one token per
 // request) from 128 to 32 steps.
 #include "kernels.h"
@@ -28,6 +29,76 @@ constexpr uint32_t kRotBytes = kHeadDim * kHeadDim * 4;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr size_t kRedBytes = size_t(kWarps) * kHeadDim * 4;   // partial sums of one item
 constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
+
+// Clip, quantise, pack and store one item from the four warps' partial sums
+// red[w][channel] (warp 0): lane l owns code byte l of the token row, i.e.
+// code positions 4 l .. 4 l + 3, which hold the rotated channels of the
+// page format's order for NG groups per token-head; each group's (min, max)
+// is reduced over the warp and gives its fp16 (scale, zero).
+template <int NG>
+__device__ __forceinline__ void finish_item(const DemoteParams& p, const float* red, int which, int head,
+                                            int64_t page, int slot, float tau, int lane) {
+  constexpr int kGs = kHeadDim / NG;
+  float v[4];
+  int grp[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = which ? storage_channel_v(NG, 4 * lane + c) : storage_channel_k(NG, 4 * lane + c);
+    v[c] = (red[ch] + red[kHeadDim + ch]) + (red[2 * kHeadDim + ch] + red[3 * kHeadDim + ch]);
+    v[c] = fminf(fmaxf(v[c], -tau), tau);
+    grp[c] = ch / kGs;
+  }
+  float s[NG], z[NG];
+  __half s16[NG], z16[NG];
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (grp[c] == q) {
+        mn = fminf(mn, v[c]);
+        mx = fmaxf(mx, v[c]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    s16[q] = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
+    z16[q] = __float2half_rn(mn);
+    s[q] = __half2float(s16[q]);
+    z[q] = __half2float(z16[q]);
+  }
+  uint32_t byte = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float sc = s[0], zc = z[0];
+#pragma unroll
+    for (int q = 1; q < NG; ++q) {
+      if (grp[c] == q) {
+        sc = s[q];
+        zc = z[q];
+      }
+    }
+    float code = 0.f;
+    if (sc > 0.f) code = fminf(fmaxf(rintf(__fdiv_rn(v[c] - zc, sc)), 0.f), 3.f);
+    byte |= uint32_t(code) << (2 * c);
+  }
+  if (page < 0 || page >= p.n_pages) {
+    if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
+    return;
+  }
+  uint8_t* blk = p.pages + (page * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v) + which * half_bytes(p.ng_k);
+  blk[32 * slot + lane] = uint8_t(byte);
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+    if (lane == q) {
+      __half2 sz = __halves2half2(s16[q], z16[q]);
+      *reinterpret_cast<__half2*>(blk + kCodeBytes + 4 * (slot * NG + q)) = sz;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   {
@@ -128,43 +199,13 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     *reinterpret_cast<float4*>(red + warp * kHeadDim + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
     __syncthreads();
     if (warp == 0 && live[it]) {
-      float v[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        v[c] = (red[4 * lane + c] + red[kHeadDim + 4 * lane + c]) +
-               (red[2 * kHeadDim + 4 * lane + c] + red[3 * kHeadDim + 4 * lane + c]);
-      float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        v[c] = fminf(fmaxf(v[c], -tau), tau);
-        mn = fminf(mn, v[c]);
-        mx = fmaxf(mx, v[c]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
-      const __half z16 = __float2half_rn(mn);
-      const float s = __half2float(s16);
-      const float z = __half2float(z16);
-      uint32_t byte = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float code = 0.f;
-        if (s > 0.f) code = fminf(fmaxf(rintf(__fdiv_rn(v[c] - z, s)), 0.f), 3.f);
-        byte |= uint32_t(code) << (2 * c);
-      }
-      if (page[it] < 0 || page[it] >= p.n_pages) {
-        if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
+      const int ng = which ? p.ng_v : p.ng_k;
+      if (ng == 4) {
+        finish_item<4>(p, red, which, head, page[it], slot[it], tau, lane);
+      } else if (ng == 2) {
+        finish_item<2>(p, red, which, head, page[it], slot[it], tau, lane);
       } else {
-        uint8_t* blk = p.pages + (page[it] * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
-        blk[32 * slot[it] + lane] = uint8_t(byte);
-        if (lane == 0) {
-          __half2 sz = __halves2half2(s16, z16);
-          *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * slot[it]) = sz;
-        }
+        finish_item<1>(p, red, which, head, page[it], slot[it], tau, lane);
       }
     }
     __syncthreads();   // red is reused by the next item

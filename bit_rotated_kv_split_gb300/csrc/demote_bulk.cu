@@ -48,8 +48,8 @@ constexpr float kRScale = 16.f;
 constexpr int kBufs = 4;                            // operand / accumulator / metadata buffers
 constexpr size_t oBhi = 0, oBlo = kOpBytes, oA = 2 * size_t(kOpBytes);
 constexpr size_t oMeta = oA + size_t(kBufs) * kOpBytes;
-constexpr size_t oXchg = oMeta + size_t(kBufs) * kTile * sizeof(int2);   // [2][2][128] (min, max)
-constexpr size_t oBars = oXchg + 2 * 2 * kTile * sizeof(float2);
+constexpr size_t oXchg = oMeta + size_t(kBufs) * kTile * sizeof(int2);   // [2][2][128][NG] (min, max)
+constexpr size_t oBars = oXchg + 2 * 2 * kTile * 4 * sizeof(float2);   // up to 4 groups
 constexpr size_t kSmem = oBars + (4 * kBufs + 4) * 8 + 16;
 constexpr uint32_t kCols = 128 * kBufs;             // D[kBufs] x 128 columns
 static_assert(kCols <= 512, "tensor memory columns");
@@ -101,6 +101,95 @@ struct Waiter {
   }
 };
 
+// Epilogue of one token-half: v[i] = 16 x~ at code position 64 hh + i, whose
+// quantisation group is ((64 hh + i) & 7) / (8 / NG) in the page format (K
+// and V alike).  The two halves of a token meet on each group's (min, max)
+// through shared memory; then the group's fp16 scale and zero point, the
+// codes (16 bytes) and, from half 0, the token's NG (scale, zero) pairs are
+// stored.  Returns false when the exchange wait expired.
+template <int NG>
+__device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&v)[kHeadDim / 2], float2* xchg,
+                                           uint64_t* xfull, Waiter& wt, int k, int hh, int j, int2 m, float tau,
+                                           int which, int head) {
+  constexpr int kSpan = 8 / NG;   // consecutive positions (mod 8) per group
+  // clipping moves only the extremes: min and max of the clipped values
+  // are the clipped min and max, and a value beyond +-tau gets the code
+  // of the clipped extreme (0 or 3) through the final clamp
+  float mn[NG], mx[NG];
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+    mn[q] = v[q * kSpan];
+    mx[q] = v[q * kSpan];
+  }
+#pragma unroll
+  for (int i = 0; i < kHeadDim / 2; ++i) {
+    const int q = (i & 7) / kSpan;
+    mn[q] = fminf(mn[q], v[i]);
+    mx[q] = fmaxf(mx[q], v[i]);
+  }
+  float2* xs = xchg + (k & 1) * 2 * kTile * NG;
+#pragma unroll
+  for (int q = 0; q < NG; ++q) xs[(hh * kTile + j) * NG + q] = make_float2(mn[q], mx[q]);
+  mbar_arrive(xfull + (k & 1));
+  if (!wt.wait(xfull + (k & 1), (k >> 1) & 1)) return false;
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+    const float2 other = xs[((1 - hh) * kTile + j) * NG + q];
+    mn[q] = fminf(mn[q], other.x);
+    mx[q] = fmaxf(mx[q], other.y);
+  }
+  if (m.x < 0) return true;
+  // code = clamp(rint((x - z) / s), 0, 3) with x = D / 16: one saturating
+  // FMA gives (x - z) / (3 s) clamped to [0, 1]; a second FMA scales by 3
+  // and adds 1.5 * 2^23, which rounds to an integer held in the float's
+  // low bits (0x4B400000 + code); the bits are accumulated as bits * 4^i
+  // (mod 2^32) and the constant part of the sum removed once per word
+  __half s16[NG], z16[NG];
+  float a48[NG], nzi3[NG];
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+    const float lo = fminf(fmaxf(mn[q] * (1.f / kRScale), -tau), tau);
+    const float hi = fminf(fmaxf(mx[q] * (1.f / kRScale), -tau), tau);
+    s16[q] = __float2half_rn(__fdiv_rn(hi - lo, 3.0f));
+    z16[q] = __float2half_rn(lo);
+    const float s = __half2float(s16[q]), z = __half2float(z16[q]);
+    const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+    a48[q] = inv * (1.f / (3.f * kRScale));
+    nzi3[q] = -z * inv * (1.f / 3.f);
+  }
+  const float kMagic = 12582912.f;
+  constexpr uint32_t kBitsSum = 0x4B400000u * 0x55555555u;   // 0x4B400000 * sum_i 4^i (mod 2^32)
+  uint32_t w[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint32_t word = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int q = (i & 7) / kSpan;
+      const float t = __saturatef(fmaf(v[16 * u + i], a48[q], nzi3[q]));
+      word += __float_as_uint(fmaf(t, 3.f, kMagic)) << (2 * i);
+    }
+    w[u] = word - kBitsSum;
+  }
+  uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v) + which * half_bytes(p.ng_k);
+  *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (hh == 0) {
+    uint32_t sz[NG];
+#pragma unroll
+    for (int q = 0; q < NG; ++q)
+      sz[q] = uint32_t(__half_as_ushort(s16[q])) | (uint32_t(__half_as_ushort(z16[q])) << 16);
+    uint8_t* dst = blk + kCodeBytes + 4 * NG * m.y;
+    if constexpr (NG == 1) {
+      *reinterpret_cast<uint32_t*>(dst) = sz[0];
+    } else if constexpr (NG == 2) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(sz[0], sz[1]);
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(sz[0], sz[1], sz[2], sz[3]);
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_constant__ DemoteParams p) {
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();
@@ -141,17 +230,21 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kCols);
   // B = (16 R)^T split into fp16 hi + lo: B[n][k] = 16 R[k][n]; thread (n,
   // half of k) writes 8 16-byte chunks of each part
+  // (column n of the product is code position n of the page format, so B
+  // takes column storage_channel(n) of R)
   if (tid < 2 * kTile) {
     const int n = tid & (kTile - 1), k0 = (tid >> 7) * 64;
-    const float* rg = (which ? p.r_v : p.r_k) + int64_t(head) * kHeadDim * kHeadDim;
+    const int ng = which ? p.ng_v : p.ng_k;
+    const int cn = which ? storage_channel_v(ng, n) : storage_channel_k(ng, n);
+    const float* rg = (which ? p.r_v : p.r_k) + int64_t(head) * kHeadDim * kHeadDim + cn;
 #pragma unroll 2
     for (int kc = 0; kc < 8; ++kc) {
       const int k = k0 + 8 * kc;
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float r0 = __ldg(rg + (k + 2 * e) * kHeadDim + n) * kRScale;
-        const float r1 = __ldg(rg + (k + 2 * e + 1) * kHeadDim + n) * kRScale;
+        const float r0 = __ldg(rg + (k + 2 * e) * kHeadDim) * kRScale;
+        const float r1 = __ldg(rg + (k + 2 * e + 1) * kHeadDim) * kRScale;
         const __half h0 = __float2half_rn(r0), h1 = __float2half_rn(r1);
         hi[e] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
         lo[e] = f16x2(r0 - __half2float(h0), r1 - __half2float(h1));
@@ -196,54 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
       }
       tc_fence_before();
       mbar_arrive(d_free + buf);
-      // clipping moves only the extremes: min and max of the clipped values
-      // are the clipped min and max, and a value beyond +-tau gets the code
-      // of the clipped extreme (0 or 3) through the final clamp
-      float mn = v[0], mx = v[0];
-#pragma unroll
-      for (int i = 1; i < kHeadDim / 2; ++i) {
-        mn = fminf(mn, v[i]);
-        mx = fmaxf(mx, v[i]);
-      }
-      float2* xs = xchg + (k & 1) * 2 * kTile;
-      xs[hh * kTile + j] = make_float2(mn, mx);
-      mbar_arrive(xfull + (k & 1));
-      if (!wt.wait(xfull + (k & 1), (k >> 1) & 1)) break;
-      const float2 other = xs[(1 - hh) * kTile + j];
-      mn = fminf(mn, other.x);
-      mx = fmaxf(mx, other.y);
-      if (m.x < 0) continue;
-      mn = fminf(fmaxf(mn * (1.f / kRScale), -tau), tau);
-      mx = fminf(fmaxf(mx * (1.f / kRScale), -tau), tau);
-      const __half s16 = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
-      const __half z16 = __float2half_rn(mn);
-      const float s = __half2float(s16), z = __half2float(z16);
-      // code = clamp(rint((x - z) / s), 0, 3) with x = D / 16: one saturating
-      // FMA gives (x - z) / (3 s) clamped to [0, 1]; a second FMA scales by 3
-      // and adds 1.5 * 2^23, which rounds to an integer held in the float's
-      // low bits (0x4B400000 + code); the bits are accumulated as bits * 4^i
-      // (mod 2^32) and the constant part of the sum removed once per word
-      const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-      const float a48 = inv * (1.f / (3.f * kRScale)), nzi3 = -z * inv * (1.f / 3.f);
-      const float kMagic = 12582912.f;
-      constexpr uint32_t kBitsSum = 0x4B400000u * 0x55555555u;   // 0x4B400000 * sum_i 4^i (mod 2^32)
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float t = __saturatef(fmaf(v[16 * q + i], a48, nzi3));
-          word += __float_as_uint(fmaf(t, 3.f, kMagic)) << (2 * i);
-        }
-        w[q] = word - kBitsSum;
-      }
-      uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * kBlockBytes + which * kHalfBytes;
-      *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
-      if (hh == 0) {
-        __half2 sz = __halves2half2(s16, z16);
-        *reinterpret_cast<__half2*>(blk + 32 * kPage + 4 * m.y) = sz;
-      }
+      const int ngw = which ? p.ng_v : p.ng_k;
+      const bool ok = ngw == 4   ? epi_finish<4>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head)
+                      : ngw == 2 ? epi_finish<2>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head)
+                                 : epi_finish<1>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head);
+      if (!ok) break;
     }
   } else if (warp < kMmaWarp) {
     // ================= loaders: thread j = token j of the tile

@@ -10,8 +10,27 @@ namespace oscar {
 
 constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
-constexpr int kBlockBytes = 1152;
-constexpr int kHalfBytes = 576;
+constexpr int kCodeBytes = 512;   // 16 token rows of 32 code bytes at the start of a half
+// A half with ng quantisation groups per token-head: the code rows, then
+// 16 x ng (scale, zero) fp16 pairs; a block is the K half then the V half.
+constexpr int half_bytes(int ng) { return kCodeBytes + 64 * ng; }
+constexpr int block_bytes(int ng_k, int ng_v) { return half_bytes(ng_k) + half_bytes(ng_v); }
+constexpr int kBlockBytes = block_bytes(1, 1);   // 1152: one group per token-head
+constexpr int kHalfBytes = half_bytes(1);        // 576
+
+// Rotated channel held by code position c of a token row with ng groups
+// (ng = 1: c itself).  K: c = 32 t + 8 e + j holds (j / J) g + (j % J) 16 +
+// 4 t + e; V: c = 16 a + 8 e + m holds (m / M) g + (m % M) 16 + 2 a + e, with
+// J = M = 8 / ng and g = 128 / ng, so one tensor-core K step (K) or one
+// 16-row tile (V) of the decode kernel reads one group.
+__host__ __device__ constexpr int storage_channel_k(int ng, int c) {
+  return ng == 1 ? c
+                 : ((c & 7) / (8 / ng)) * (kHeadDim / ng) + ((c & 7) % (8 / ng)) * 16 + 4 * (c >> 5) + ((c >> 3) & 3);
+}
+__host__ __device__ constexpr int storage_channel_v(int ng, int c) {
+  return ng == 1 ? c
+                 : ((c & 7) / (8 / ng)) * (kHeadDim / ng) + ((c & 7) % (8 / ng)) * 16 + 2 * (c >> 4) + ((c >> 3) & 1);
+}
 constexpr int kPartStride = 132;  // floats per (split, head) partial: m, l, pad, pad, o[128]
 
 // Lazy online-softmax maximum: a running maximum m is raised only when a
@@ -61,6 +80,7 @@ struct DemoteParams {
   float tau_k, tau_v;
   int32_t n, batch, n_kv, max_pages;
   int64_t n_pages;
+  int32_t ng_k, ng_v;   // quantisation groups per token-head (1, 2 or 4)
   // bulk path with contiguous source rows (no src_index): k_src / v_src as
   // 2-D bf16 tensors (n_kv * 128 columns x src_rows rows) read in boxes of 8
   // columns x 128 rows; use_tma = 0 means the rows are gathered by threads
@@ -99,6 +119,7 @@ struct DecodeParams {
   float* partials;      // [pairs][n_splits][G][kPartStride]
   // dims
   int32_t batch, n_kv, group, sink_cap, recent_cap, max_pages;
+  int32_t ng_k, ng_v;   // quantisation groups per token-head (1, 2 or 4)
   int64_t n_pages;
   int32_t max_hist;
   // split plan

@@ -10,6 +10,14 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// groups per token-head for a quantisation group size (0 = 128); 0 if invalid
+int groups_of(int32_t g) {
+  if (g == 0 || g == 128) return 1;
+  if (g == 64) return 2;
+  if (g == 32) return 4;
+  return 0;
+}
+
 oscar_status check_desc(const oscar_layer_desc* d, bool need_cache_segments) {
   if (!d) return OSCAR_ERR_INVALID_ARG;
   if (d->batch < 1 || d->n_kv_heads < 1 || d->n_q_heads < 1 || d->head_dim != OSCAR_HEAD_DIM)
@@ -25,6 +33,7 @@ oscar_status check_desc(const oscar_layer_desc* d, bool need_cache_segments) {
   if (!(d->tau_k > 0.f) || !(d->tau_v > 0.f) || !(d->tau_k <= 65504.f) || !(d->tau_v <= 65504.f))
     return OSCAR_ERR_INVALID_ARG;
   if (!d->pages || !d->page_table || !d->r_k || !d->r_v) return OSCAR_ERR_INVALID_ARG;
+  if (!groups_of(d->quant_group_k) || !groups_of(d->quant_group_v)) return OSCAR_ERR_INVALID_ARG;
   if (!aligned(d->pages, 128) || !aligned(d->r_k, 16) || !aligned(d->r_v, 16) ||
       !aligned(d->page_table, 4))
     return OSCAR_ERR_ALIGNMENT;
@@ -57,6 +66,11 @@ extern "C" const char* oscar_status_string(oscar_status s) {
 }
 
 extern "C" int32_t oscar_abi_version(void) { return OSCAR_ABI_VERSION; }
+
+extern "C" int64_t oscar_block_bytes(int32_t quant_group_k, int32_t quant_group_v) {
+  const int gk = groups_of(quant_group_k), gv = groups_of(quant_group_v);
+  return gk && gv ? int64_t(oscar::block_bytes(gk, gv)) : 0;
+}
 
 extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint16_t* k_src,
                                               uint16_t* v_src, int64_t src_rows,
@@ -99,6 +113,8 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
   p.n_kv = desc->n_kv_heads;
   p.max_pages = desc->max_pages_per_seq;
   p.n_pages = desc->n_pages;
+  p.ng_k = groups_of(desc->quant_group_k);
+  p.ng_v = groups_of(desc->quant_group_v);
   const bool bulk = n >= oscar::kBulkDemoteMin && !new_k && !new_v;
   const cudaError_t e = bulk ? oscar::launch_demote_bulk(p, static_cast<cudaStream_t>(stream))
                              : oscar::launch_demote(p, static_cast<cudaStream_t>(stream));
@@ -157,6 +173,8 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   p.max_pages = desc->max_pages_per_seq;
   p.n_pages = desc->n_pages;
   p.max_hist = desc->max_hist;
+  p.ng_k = groups_of(desc->quant_group_k);
+  p.ng_v = groups_of(desc->quant_group_v);
   p.n_splits = plan.n_splits;
   p.pages_per_split = plan.pages_per_split;
   // PV operand scale: p <= 2^kRescaleLog2 and s_V <= 2 tau_v / 3 (x2 margin

@@ -12,8 +12,13 @@
  *
  * Conventions shared by every call:
  *   - Row vectors: a rotated key is k~ = k . R with R = U . H_Had . P_br.
- *   - head_dim d = 128, 16 tokens per page, one quantisation group per
- *     (token, KV head, K|V) vector of 128 channels, fp16 scale and zero.
+ *   - head_dim d = 128, 16 tokens per page; a (token, KV head, K|V) vector
+ *     of 128 rotated channels is quantised in groups of g consecutive
+ *     channels (g = 128 by default; 64 or 32 per layer, for K and V apart,
+ *     see quant_group_k / quant_group_v), each with an fp16 scale and zero.
+ *     Smaller groups are where the bit-reversal P_br of R matters: it
+ *     interleaves high- and low-variance channels across the groups
+ *     ([GIST] 2.2 A; [ZAKER] "OSCAR 把旋转对准 attention").
  *   - bfloat16 data is passed as uint16_t bit patterns.
  *   - All device memory is allocated and freed by the caller.  The library
  *     keeps no state besides cached device attributes; calls on different
@@ -28,14 +33,21 @@
  *   - No C++ exception crosses this boundary.
  *
  * Page pool layout (this library's format; the pages fix only "paged KV",
- * "4 codes per byte" and "scale/zero point"):
- *   pool = n_pages x n_kv_heads blocks of 1152 bytes, block (page p, head h)
- *   at byte (p * n_kv_heads + h) * 1152.  A block is a K half then a V half,
- *   576 bytes each:  16 tokens x 32 code bytes, then 16 (scale, zero) fp16
- *   pairs.  Token slot t of a half: codes at 32 t, (scale, zero) at 512 + 4 t.
- *   Code byte j of a token holds channels 4j..4j+3, channel 4j+i in bits
- *   2i..2i+1; channels are in rotated order.  Logical history position x of
- *   request b lives in page page_table[b][x / 16], slot x % 16.
+ * "4 codes per byte" and "scale/zero point"), with G_K = 128 / g_K and
+ * G_V = 128 / g_V groups per vector:
+ *   half(G) = 512 + 64 G bytes: 16 tokens x 32 code bytes, then 16 x G
+ *   (scale, zero) fp16 pairs, token-major: pair (slot t, group q) at
+ *   512 + 4 (t G + q).  A block is a K half(G_K) then a V half(G_V) (1152
+ *   bytes with one group each, OSCAR_BLOCK_BYTES); block (page p, head h) at
+ *   byte (p * n_kv_heads + h) * block.  Token slot t of a half: codes at 32 t;
+ *   code position c (byte c / 4, bits 2 (c % 4)) holds rotated channel c
+ *   when G = 1.  When G > 1 it holds channel
+ *     K: c = 32 t + 8 e + j (t, e < 4, j < 8):  (j / J) g + (j % J) 16 + 4 t + e,
+ *     V: c = 16 a + 8 e + m (a < 8, e < 2, m < 8): (m / M) g + (m % M) 16 + 2 a + e,
+ *   with J = M = 8 / G, so that each tensor-core operand tile of the decode
+ *   kernel draws on one group.  Group q is rotated channels [q g, (q+1) g).
+ *   Logical history position x of request b lives in page
+ *   page_table[b][x / 16], slot x % 16.
  */
 #ifndef OSCAR_H_
 #define OSCAR_H_
@@ -47,7 +59,7 @@
 extern "C" {
 #endif
 
-#define OSCAR_ABI_VERSION 1
+#define OSCAR_ABI_VERSION 2
 
 #define OSCAR_HEAD_DIM 128
 #define OSCAR_PAGE_TOKENS 16
@@ -108,7 +120,13 @@ typedef struct oscar_layer_desc {
   const float* r_k;           /* [H_kv][d][d] row-major R_K, k~ = k . R_K      */
   const float* r_v;           /* [H_kv][d][d] row-major R_V                    */
   int32_t* dev_status;        /* optional device word for OSCAR_DEV_* bits     */
+  int32_t quant_group_k;      /* K quantisation group g_K: 32, 64 or 128 (0 = 128) */
+  int32_t quant_group_v;      /* V quantisation group g_V: 32, 64 or 128 (0 = 128) */
 } oscar_layer_desc;
+
+/* Bytes of one (page, KV head) block for groups g_k, g_v (0 = 128); 0 for
+ * any other value.  Host-only. */
+int64_t oscar_block_bytes(int32_t quant_group_k, int32_t quant_group_v);
 
 /*
  * oscar_build_rotation - the fixed rotation of one (layer, KV head) from
@@ -208,10 +226,12 @@ oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_he
  *   [0, src_rows), a request outside the batch or a position beyond the page
  *   table skips the item and sets OSCAR_DEV_LENGTH; a page id outside the
  *   pool skips it and sets OSCAR_DEV_PAGE_BOUNDS.  x~ = x . R[h] (fp32 accumulate),
- *   clamped to [-tau, tau]; scale = fp16((max - min) / 3), zero = fp16(min);
- *   code = clamp(rint((x~ - zero) / scale), 0, 3) (0 if scale is 0).  The
- *   codes and (scale, zero) go to history position dst_pos[i] of request
- *   dst_req[i] through desc->page_table.  K and V are both written.
+ *   clamped to [-tau, tau]; per group of g consecutive channels (g =
+ *   quant_group_k for K, quant_group_v for V) scale = fp16((max - min) / 3),
+ *   zero = fp16(min) over the group; code = clamp(rint((x~ - zero) / scale),
+ *   0, 3) (0 if scale is 0).  The codes and (scale, zero) pairs go to history
+ *   position dst_pos[i] of request dst_req[i] through desc->page_table, in the
+ *   pool layout above.  K and V are both written.
  *
  *   new_k / new_v (nullable, both or neither): [n][H_kv][d] bf16 rows that
  *   replace the demoted source rows after they have been read - the decode

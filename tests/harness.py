@@ -48,14 +48,25 @@ def canalized_rotations(seed: int, layer: int, n_kv: int, outl: np.ndarray, bloc
     return r32, r32.copy(), tau_k, tau_v
 
 
-def demote_heads(x: np.ndarray, r32: np.ndarray, tau: float):
-    """Oracle demotion of x [T][n_kv][d] with per-head rotations: (codes, scale16, zero16)."""
+def demote_heads(x: np.ndarray, r32: np.ndarray, tau: float, group: int = None):
+    """Oracle demotion of x [T][n_kv][d] with per-head rotations: (codes, scale16, zero16).
+
+    group None: one group per vector, scale/zero [T][n_kv]; group g: groups of
+    g channels, scale/zero [T][n_kv][d / g].
+    """
     t, n_kv, d = x.shape
     codes = np.zeros((t, n_kv, d), np.uint8)
-    s = np.zeros((t, n_kv), np.float16)
-    z = np.zeros((t, n_kv), np.float16)
+    if group is None:
+        s = np.zeros((t, n_kv), np.float16)
+        z = np.zeros((t, n_kv), np.float16)
+        for h in range(n_kv):
+            codes[:, h], s[:, h], z[:, h] = O.demote(x[:, h].astype(np.float64), r32[h].astype(np.float64), tau)
+        return codes, s, z
+    s = np.zeros((t, n_kv, d // group), np.float16)
+    z = np.zeros((t, n_kv, d // group), np.float16)
     for h in range(n_kv):
-        codes[:, h], s[:, h], z[:, h] = O.demote(x[:, h].astype(np.float64), r32[h].astype(np.float64), tau)
+        codes[:, h], s[:, h], z[:, h] = O.quantize_groups(
+            O.rotate(x[:, h].astype(np.float64), r32[h].astype(np.float64)), tau, group)
     return codes, s, z
 
 
@@ -64,8 +75,11 @@ class Scenario:
 
     def __init__(self, seed: int, ctxs, n_kv: int = 1, g: int = 4, shared_prefix_hist: int = 0,
                  cal=(1024, 512), ring_start=None, identity_pages: bool = False, rot=None,
-                 sink_cap: int = 64, recent_cap: int = 256):
+                 sink_cap: int = 64, recent_cap: int = 256, groups=(128, 128)):
         self.seed, self.ctxs, self.n_kv, self.g = seed, [int(c) for c in ctxs], n_kv, g
+        self.gk, self.gv = int(groups[0]), int(groups[1])
+        grouped = (self.gk, self.gv) != (D, D)
+        ngk, ngv = D // self.gk, D // self.gv
         self.B = len(self.ctxs)
         self.h_q = n_kv * g
         self.sink_cap, self.recent_cap = sink_cap, recent_cap
@@ -102,16 +116,19 @@ class Scenario:
         qo = np.repeat(self.outl, g, axis=0)
         self.q = np.stack([synth.activations(seed, (0, b, 2), 1, qo)[0] for b in range(self.B)])
         # oracle history codes and the page pool holding them
-        self.pool = np.zeros(self.n_pages * n_kv * O.BLOCK_BYTES, np.uint8)
+        self.pool = np.zeros(self.n_pages * n_kv * O.block_bytes(ngk, ngv), np.uint8)
         self.hist = []
         for b in range(self.B):
             sl, hl = int(self.sink_len[b]), int(self.hist_len[b])
             xk = self.k_tok[b][sl:sl + hl]
             xv = self.v_tok[b][sl:sl + hl]
-            ck, sk, zk = demote_heads(xk, self.rk32, self.tau_k)
-            cv, sv, zv = demote_heads(xv, self.rv32, self.tau_v)
+            ck, sk, zk = demote_heads(xk, self.rk32, self.tau_k, self.gk if grouped else None)
+            cv, sv, zv = demote_heads(xv, self.rv32, self.tau_v, self.gv if grouped else None)
             self.hist.append(dict(codes_k=ck, scale_k=sk, zero_k=zk, codes_v=cv, scale_v=sv, zero_v=zv))
-            if hl:
+            if hl and grouped:
+                O.store_history_groups(self.pool, self.table, n_kv, b, 0, ck, sk, zk, 0, ngk, ngv)
+                O.store_history_groups(self.pool, self.table, n_kv, b, 0, cv, sv, zv, 1, ngk, ngv)
+            elif hl:
                 O.store_history_bulk(self.pool, self.table, n_kv, b, 0, O.pack(ck), sk, zk, 0)
                 O.store_history_bulk(self.pool, self.table, n_kv, b, 0, O.pack(cv), sv, zv, 1)
 
@@ -228,7 +245,8 @@ def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, r
     if diff.any():
         ud = u[diff]
         # a rotated value known to within rot_err moves u by rot_err / s
-        slack = 0.0 if rot_err is None else np.broadcast_to((rot_err[..., None] / s), u.shape)[diff]
+        with np.errstate(divide="ignore", invalid="ignore"):   # s = 0 gives code 0 on both sides
+            slack = 0.0 if rot_err is None else np.broadcast_to((rot_err[..., None] / s), u.shape)[diff]
         near = np.zeros(ud.shape, bool)
         for bnd in (0.5, 1.5, 2.5):
             near |= np.abs(ud - bnd) <= np.maximum(1e-5 * bnd, slack)
@@ -252,7 +270,8 @@ def to_device(sc: Scenario):
     dev = torch.device("cuda")
     cache = LayerCache(sc.B, sc.h_q, sc.n_kv, sc.table.shape[1], sc.n_pages,
                        torch.from_numpy(sc.rk32), torch.from_numpy(sc.rv32), sc.tau_k, sc.tau_v,
-                       device=dev, sink_cap=sc.sink_cap, recent_cap=sc.recent_cap)
+                       device=dev, sink_cap=sc.sink_cap, recent_cap=sc.recent_cap,
+                       quant_group_k=getattr(sc, "gk", 128), quant_group_v=getattr(sc, "gv", 128))
     cache.pages.copy_(torch.from_numpy(sc.pool))
     cache.page_table.copy_(torch.from_numpy(sc.table))
     cache.hist_len.copy_(torch.from_numpy(sc.hist_len))

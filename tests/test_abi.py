@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol(built_lib):
 
 def test_version_and_status_strings(built_lib):
     from bit_rotated_kv_split_gb300 import binding as B
-    assert B.oscar_abi_version() == 1
+    assert B.oscar_abi_version() == 2
     assert B.oscar_status_string(0) == "ok"
     assert B.oscar_status_string(3).startswith("workspace")
 
@@ -56,6 +56,7 @@ def _desc(**over):
     (dict(tau_k=float("nan")), 1), (dict(tau_v=70000.0), 1), (dict(max_hist=8 * 16 + 1), 1),
     (dict(pages=0), 1), (dict(page_table=0), 1), (dict(hist_len=0), 1),
     (dict(pages=(1 << 20) + 64), 2), (dict(r_k=(1 << 20) + 4), 2), (dict(sink_k=(1 << 20) + 2), 2),
+    (dict(quant_group_k=16), 1), (dict(quant_group_v=96), 1), (dict(quant_group_k=-32), 1),
 ])
 def test_decode_rejects_bad_descriptors_before_launch(built_lib, over, status):
     from bit_rotated_kv_split_gb300 import binding as B
@@ -184,3 +185,24 @@ def test_covariance_rejects_bad_arguments(built_lib):
     small = ctypes.c_size_t(size.value - 1)
     assert lib.oscar_covariance(ctypes.c_void_p(256), 5000, 128, 128, ctypes.c_void_p(256), ctypes.c_void_p(256),
                                 ctypes.byref(small), None) == 3
+
+
+def test_block_bytes_match_the_format(built_lib):
+    # the library's block size equals the oracle's grouped format for every
+    # valid pair of group sizes (0 means 128), and 0 for anything else
+    from bit_rotated_kv_split_gb300 import binding as B
+    for gk in (0, 32, 64, 128):
+        for gv in (0, 32, 64, 128):
+            ngk, ngv = 128 // (gk or 128), 128 // (gv or 128)
+            assert B.oscar_block_bytes(gk, gv) == O.block_bytes(ngk, ngv)
+    assert B.oscar_block_bytes(128, 128) == 1152 == O.BLOCK_BYTES
+    for bad in (16, 48, 96, 256, -1):
+        assert B.oscar_block_bytes(bad, 128) == 0 and B.oscar_block_bytes(128, bad) == 0
+
+
+def test_append_rejects_bad_group_before_launch(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    fake = 1 << 20
+    got = B.lib.oscar_quantize_append(ctypes.byref(_desc(quant_group_v=48)), fake, fake, 4, 128, None,
+                                      fake, fake, 4, None, None, None)
+    assert got == 1

@@ -28,7 +28,8 @@ def _pre_rounding(x_rot_clipped):
     return (mx - mn) / 3.0, mn
 
 
-def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None, first_row=None):
+def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None, first_row=None,
+         groups=None):
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
@@ -51,8 +52,9 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         positions = np.arange(n_tok)
     hist = int(positions.max()) + 1
     table, n_pages = synth.page_table(seed, [hist], n_extra_pages=0)
+    gk, gv = groups if groups is not None else (128, 128)
     cache = LayerCache(1, n_kv * 4, n_kv, table.shape[1], n_pages, torch.from_numpy(rk32),
-                       torch.from_numpy(rv32), tau_k, tau_v)
+                       torch.from_numpy(rv32), tau_k, tau_v, quant_group_k=gk, quant_group_v=gv)
     cache.page_table.copy_(torch.from_numpy(table))
     dev = torch.device("cuda")
     k_src = torch.from_numpy(xk).to(torch.bfloat16).to(dev).contiguous()
@@ -76,16 +78,28 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
     assert int(cache.dev_status.item()) == 0
     pool = cache.pages.cpu().numpy()
     res = {}
-    for which, x, r32, tau in ((0, xk, rk32, tau_k), (1, xv, rv32, tau_v)):
-        gc, gs, gz = O.load_history_bulk(pool, table, n_kv, 0, hist, which)
+    for which, x, r32, tau, gsz in ((0, xk, rk32, tau_k, gk), (1, xv, rv32, tau_v, gv)):
         xs = x[src_index]                                  # token written to position i
-        gc, gs, gz = gc[positions], gs[positions], gz[positions]
         xr = np.stack([np.clip(xs[:, h].astype(np.float64) @ r32[h].astype(np.float64), -tau, tau)
                        for h in range(n_kv)], axis=1)
-        rc, rs, rz = H.demote_heads(xs, r32, tau)
-        pre_s, pre_z = _pre_rounding(xr)
-        res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z,
-                                   rot_err=H.rotation_error_bound(xs, r32))
+        rot_err = H.rotation_error_bound(xs, r32)
+        if groups is None:
+            gc, gs, gz = O.load_history_bulk(pool, table, n_kv, 0, hist, which)
+            gc, gs, gz = gc[positions], gs[positions], gz[positions]
+            rc, rs, rz = H.demote_heads(xs, r32, tau)
+            pre_s, pre_z = _pre_rounding(xr)
+            res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z, rot_err=rot_err)
+            continue
+        # groups: each group of gsz channels is compared as its own vector
+        ng = 128 // gsz
+        gc, gs, gz = O.load_history_groups(pool, table, n_kv, 0, hist, which, 128 // gk, 128 // gv)
+        gc, gs, gz = gc[positions], gs[positions], gz[positions]
+        rc, rs, rz = H.demote_heads(xs, r32, tau, gsz)
+        shp = (n_tok, n_kv, ng, gsz)
+        xg = xr.reshape(shp)
+        pre_s, pre_z = _pre_rounding(xg)
+        res[which] = H.code_parity(xg, gc.reshape(shp), gs, gz, rc.reshape(shp), rs, rz, pre_s, pre_z,
+                                   rot_err=np.repeat(rot_err[..., None], ng, axis=-1))
     if with_new:
         np.testing.assert_array_equal(k_src.float().cpu().numpy()[src_index], nk)
         np.testing.assert_array_equal(v_src.float().cpu().numpy()[src_index], nv)
