@@ -43,7 +43,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 WORKLOAD = dict(workload="qwen3-8b-layer-decode-100k", batch=1, n_q_heads=32, n_kv_heads=8,
-                head_dim=128, ctx=100_000, sink=64, recent=256, page_tokens=16, group=128, seed=1002)
+                head_dim=128, ctx=100_000, sink=64, recent=256, page_tokens=16, group_k=128, group_v=128,
+                seed=1002)
 METRIC = "decode-attn tokens/s at 100k ctx (1 layer, Qwen3-8B shape)"
 UNIT = "tokens/s"
 EXTRA_WORKLOADS = {
@@ -80,7 +81,12 @@ def _args():
     ap.add_argument("--rotation", default="oscar", choices=["oscar", "canalized32"],
                     help="R_K/R_V of the default workload: the OSCAR eigenbasis rotation, or the OScaR "
                          "block-diagonal one (Hadamard groups of 32 channels)")
-    return ap.parse_args()
+    ap.add_argument("--quant-group", default="128,128",
+                    choices=["%d,%d" % (a, b) for a in (32, 64, 128) for b in (32, 64, 128)],
+                    help="quantisation group sizes of K and V in the default workload (channels)")
+    args = ap.parse_args()
+    WORKLOAD["group_k"], WORKLOAD["group_v"] = (int(x) for x in args.quant_group.split(","))
+    return args
 
 
 def _split(ctx):
@@ -93,7 +99,8 @@ def bytes_per_decode():
     """Algorithmic HBM bytes of one decode launch on the workload (per step)."""
     w = WORKLOAD
     _, hist, _ = _split(w["ctx"])
-    per_hist_token = w["n_kv_heads"] * 2 * (w["head_dim"] // 4 + 4)          # codes + s/z, K and V
+    d = w["head_dim"]
+    per_hist_token = w["n_kv_heads"] * (2 * (d // 4) + 4 * (d // w["group_k"]) + 4 * (d // w["group_v"]))
     bf16 = (w["sink"] + w["recent"]) * w["n_kv_heads"] * 2 * w["head_dim"] * 2
     table = -(-hist // w["page_tokens"]) * 4
     io = w["n_q_heads"] * w["head_dim"] * (2 + 4)
@@ -106,7 +113,8 @@ def _config_json(extra=None):
     cfg = {"workload": w["workload"], "batch": w["batch"], "n_q_heads": w["n_q_heads"],
            "n_kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"], "ctx": w["ctx"],
            "sink_bf16": s, "history_int2": h, "recent_bf16": r, "page_tokens": w["page_tokens"],
-           "quant_group": w["group"], "parallelism": "replicas"}
+           "quant_group": w["group_k"] if w["group_k"] == w["group_v"] else "k%d/v%d" % (w["group_k"], w["group_v"]),
+           "parallelism": "replicas"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -134,9 +142,16 @@ def _oracle_sample_setup():
     q = synth.activations(seed, (0, 0, 2), 1, np.repeat(outl, g, axis=0))[0].astype(np.float64)
     hist = {}
     for name, x, rot, tau in (("k", k, rk, tau_k), ("v", v, rv, tau_v)):
-        c, sc, ze = O.demote(x[s:s + h - 1, 0], rot, tau)
+        c, sc, ze = _oracle_demote(O, x[s:s + h - 1, 0], rot, tau, w["group_" + name])
         hist["codes_" + name], hist["scale_" + name], hist["zero_" + name] = c[:, None], sc[:, None], ze[:, None]
     return dict(O=O, np=np, q=q, k=k, v=v, rk=rk, rv=rv, tau_k=tau_k, tau_v=tau_v, hist=hist, s=s, h=h, r=r)
+
+
+def _oracle_demote(O, x, r, tau, group):
+    """The oracle's demotion of rows x with one or several quantisation groups."""
+    if group == WORKLOAD["head_dim"]:
+        return O.demote(x, r, tau)
+    return O.quantize_groups(O.rotate(x, r), tau, group)
 
 
 def _oracle_step(st, n_hist=None):
@@ -147,8 +162,8 @@ def _oracle_step(st, n_hist=None):
     O, np = st["O"], st["np"]
     s, h = st["s"], st["h"]
     keep = (h - 1) if n_hist is None else max(0, min(h - 1, n_hist - 1))
-    ck, sk, zk = O.demote(st["k"][s + h - 1, 0][None], st["rk"], st["tau_k"])
-    cv, sv, zv = O.demote(st["v"][s + h - 1, 0][None], st["rv"], st["tau_v"])
+    ck, sk, zk = _oracle_demote(O, st["k"][s + h - 1, 0][None], st["rk"], st["tau_k"], WORKLOAD["group_k"])
+    cv, sv, zv = _oracle_demote(O, st["v"][s + h - 1, 0][None], st["rv"], st["tau_v"], WORKLOAD["group_v"])
     old = st["hist"]
     hist = {"codes_k": np.concatenate([old["codes_k"][:keep], ck[:, None]]),
             "scale_k": np.concatenate([old["scale_k"][:keep], sk[:, None]]),
@@ -186,7 +201,9 @@ def _single_thread_env():
 def cpu_baseline(reps=20):
     """The oracle timed on one host core in a fresh process (started before any GPU work)."""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
-                        "--reps", str(reps)], capture_output=True, text=True, env=_single_thread_env(),
+                        "--reps", str(reps), "--quant-group",
+                        "%d,%d" % (WORKLOAD["group_k"], WORKLOAD["group_v"])],
+                       capture_output=True, text=True, env=_single_thread_env(),
                        timeout=900)
     if r.returncode != 0:
         return {"error": r.stderr[-400:]}
@@ -287,6 +304,8 @@ def _profiled_traffic():
     taken on the current kernel sources (else None)."""
     import hashlib
     import re
+    if (WORKLOAD["group_k"], WORKLOAD["group_v"]) != (128, 128):
+        return None    # the summary covers the one-group kernel
     prof = os.path.join(ROOT, "profiles", "split_kernel_qwen3-8b-layer-decode-100k.md")
     try:
         text = open(prof).read()
@@ -348,7 +367,8 @@ def build_layer(torch, B, dev, rot):
     rk, rv, tau_k, tau_v, outl = rot
     table, n_pages = synth.page_table(seed, [h] * bsz, n_extra_pages=1)
     cache = LayerCache(bsz, w["n_q_heads"], n_kv, table.shape[1], n_pages, torch.from_numpy(rk),
-                       torch.from_numpy(rv), tau_k, tau_v, device=dev)
+                       torch.from_numpy(rv), tau_k, tau_v, device=dev, quant_group_k=w["group_k"],
+                       quant_group_v=w["group_v"])
     cache.page_table.copy_(torch.from_numpy(table))
     cache.max_hist = h
     chunk = 32768

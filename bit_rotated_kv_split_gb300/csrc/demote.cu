@@ -32,21 +32,23 @@ constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
 
 // Clip, quantise, pack and store one item from the four warps' partial sums
 // red[w][channel] (warp 0): lane l owns code byte l of the token row, i.e.
-// code positions 4 l .. 4 l + 3, which hold the rotated channels of the
-// page format's order for NG groups per token-head; each group's (min, max)
-// is reduced over the warp and gives its fp16 (scale, zero).
+// code positions 4 l + c (c < 4), which hold the rotated channels of the
+// page format's order for NG groups per token-head.  The group of position
+// 4 l + c is (4 (l & 1) + c) / (8 / NG) for K and V alike, so with c a
+// compile-time constant each code picks between two fixed groups by the
+// lane's parity.  Each group's (min, max) is reduced over the warp and
+// gives its fp16 (scale, zero).
 template <int NG>
 __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* red, int which, int head,
                                             int64_t page, int slot, float tau, int lane) {
-  constexpr int kGs = kHeadDim / NG;
+  constexpr int kSpan = 8 / NG;
+  const bool odd = lane & 1;
   float v[4];
-  int grp[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int ch = which ? storage_channel_v(NG, 4 * lane + c) : storage_channel_k(NG, 4 * lane + c);
     v[c] = (red[ch] + red[kHeadDim + ch]) + (red[2 * kHeadDim + ch] + red[3 * kHeadDim + ch]);
     v[c] = fminf(fmaxf(v[c], -tau), tau);
-    grp[c] = ch / kGs;
   }
   float s[NG], z[NG];
   __half s16[NG], z16[NG];
@@ -55,10 +57,9 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if (grp[c] == q) {
-        mn = fminf(mn, v[c]);
-        mx = fmaxf(mx, v[c]);
-      }
+      const bool in = odd ? ((4 + c) / kSpan == q) : (c / kSpan == q);
+      mn = in ? fminf(mn, v[c]) : mn;
+      mx = in ? fmaxf(mx, v[c]) : mx;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -73,14 +74,8 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
   uint32_t byte = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    float sc = s[0], zc = z[0];
-#pragma unroll
-    for (int q = 1; q < NG; ++q) {
-      if (grp[c] == q) {
-        sc = s[q];
-        zc = z[q];
-      }
-    }
+    const float sc = odd ? s[(4 + c) / kSpan] : s[c / kSpan];
+    const float zc = odd ? z[(4 + c) / kSpan] : z[c / kSpan];
     float code = 0.f;
     if (sc > 0.f) code = fminf(fmaxf(rintf(__fdiv_rn(v[c] - zc, sc)), 0.f), 3.f);
     byte |= uint32_t(code) << (2 * c);
@@ -91,15 +86,18 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
   }
   uint8_t* blk = p.pages + (page * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v) + which * half_bytes(p.ng_k);
   blk[32 * slot + lane] = uint8_t(byte);
+  if (lane < NG) {
+    __half2 sz = __halves2half2(s16[0], z16[0]);
 #pragma unroll
-  for (int q = 0; q < NG; ++q) {
-    if (lane == q) {
-      __half2 sz = __halves2half2(s16[q], z16[q]);
-      *reinterpret_cast<__half2*>(blk + kCodeBytes + 4 * (slot * NG + q)) = sz;
-    }
+    for (int q = 1; q < NG; ++q)
+      if (lane == q) sz = __halves2half2(s16[q], z16[q]);
+    *reinterpret_cast<__half2*>(blk + kCodeBytes + 4 * (slot * NG + lane)) = sz;
   }
 }
 
+// NGK / NGV: quantisation groups per token-head of K and V (template
+// arguments, so a kernel holds only the finishing code it uses).
+template <int NGK, int NGV>
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   {
     // L2 prefetch of this CTA's rotation (a hint that reads nothing, so it
@@ -199,13 +197,12 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     *reinterpret_cast<float4*>(red + warp * kHeadDim + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
     __syncthreads();
     if (warp == 0 && live[it]) {
-      const int ng = which ? p.ng_v : p.ng_k;
-      if (ng == 4) {
-        finish_item<4>(p, red, which, head, page[it], slot[it], tau, lane);
-      } else if (ng == 2) {
-        finish_item<2>(p, red, which, head, page[it], slot[it], tau, lane);
+      if constexpr (NGK == NGV) {
+        finish_item<NGK>(p, red, which, head, page[it], slot[it], tau, lane);
+      } else if (which) {
+        finish_item<NGV>(p, red, which, head, page[it], slot[it], tau, lane);
       } else {
-        finish_item<1>(p, red, which, head, page[it], slot[it], tau, lane);
+        finish_item<NGK>(p, red, which, head, page[it], slot[it], tau, lane);
       }
     }
     __syncthreads();   // red is reused by the next item
@@ -214,14 +211,35 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
 
 }  // namespace
 
+namespace {
+
+template <int NGK, int NGV>
+cudaError_t launch_ng(const DemoteParams& p, int64_t chunks, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(demote_kernel<NGK, NGV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kSmem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(demote_kernel<NGK, NGV>, dim3(unsigned(chunks), unsigned(p.n_kv * 2)), dim3(kWarps * 32),
+                    kSmem, stream, p);
+}
+
+template <int NGK>
+cudaError_t launch_ngk(const DemoteParams& p, int64_t chunks, cudaStream_t stream) {
+  if (p.ng_v == 1) return launch_ng<NGK, 1>(p, chunks, stream);
+  if (p.ng_v == 2) return launch_ng<NGK, 2>(p, chunks, stream);
+  if (p.ng_v == 4) return launch_ng<NGK, 4>(p, chunks, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream) {
   const int64_t chunks = (int64_t(p.n) + kItems - 1) / kItems;
   if (chunks == 0) return cudaSuccess;
   if (chunks > 0x7fffffff || int64_t(p.n_kv) * 2 > 65535) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(demote_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
-  if (e != cudaSuccess) return e;
-  return launch_pdl(demote_kernel, dim3(unsigned(chunks), unsigned(p.n_kv * 2)), dim3(kWarps * 32), kSmem,
-                    stream, p);
+  if (p.ng_k == 1) return launch_ngk<1>(p, chunks, stream);
+  if (p.ng_k == 2) return launch_ngk<2>(p, chunks, stream);
+  if (p.ng_k == 4) return launch_ngk<4>(p, chunks, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace oscar
