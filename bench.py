@@ -83,7 +83,7 @@ def _args():
                          "block-diagonal one (Hadamard groups of 32 channels)")
     ap.add_argument("--quant-group", default="128,128",
                     choices=["%d,%d" % (a, b) for a in (32, 64, 128) for b in (32, 64, 128)],
-                    help="quantisation group sizes of K and V in the default workload (channels)")
+                    help="quantisation group sizes of K and V (channels), for every GPU workload")
     args = ap.parse_args()
     WORKLOAD["group_k"], WORKLOAD["group_v"] = (int(x) for x in args.quant_group.split(","))
     return args
@@ -107,14 +107,18 @@ def bytes_per_decode():
     return hist * per_hist_token + bf16 + table + io
 
 
+def _group_label():
+    w = WORKLOAD
+    return w["group_k"] if w["group_k"] == w["group_v"] else "k%d/v%d" % (w["group_k"], w["group_v"])
+
+
 def _config_json(extra=None):
     w = WORKLOAD
     s, h, r = _split(w["ctx"])
     cfg = {"workload": w["workload"], "batch": w["batch"], "n_q_heads": w["n_q_heads"],
            "n_kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"], "ctx": w["ctx"],
            "sink_bf16": s, "history_int2": h, "recent_bf16": r, "page_tokens": w["page_tokens"],
-           "quant_group": w["group_k"] if w["group_k"] == w["group_v"] else "k%d/v%d" % (w["group_k"], w["group_v"]),
-           "parallelism": "replicas"}
+           "quant_group": _group_label(), "parallelism": "replicas"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -662,7 +666,8 @@ def _build_batch_cache(torch, B, dev, rot, seed, layer, ctxs, n_q, n_kv, shared_
     table, n_pages = synth.page_table(seed + 100 * layer, hist, n_extra_pages=1, shared_prefix_tokens=shared_hist)
     bsz = len(ctxs)
     cache = LayerCache(bsz, n_q, n_kv, table.shape[1], n_pages, torch.from_numpy(rk), torch.from_numpy(rv),
-                       tau_k, tau_v, device=dev)
+                       tau_k, tau_v, device=dev, quant_group_k=WORKLOAD["group_k"],
+                       quant_group_v=WORKLOAD["group_v"])
     cache.page_table.copy_(torch.from_numpy(table))
     cache.max_hist = max(hist)
     n_shared_pages = 0
@@ -702,8 +707,13 @@ def _build_batch_cache(torch, B, dev, rot, seed, layer, ctxs, n_q, n_kv, shared_
     return cache, hist, unique_hist
 
 
+def _hist_bytes_per_token(n_kv):
+    """INT2 history bytes of one token (K and V codes, one (scale, zero) per group)."""
+    return n_kv * (2 * (128 // 4) + 4 * (128 // WORKLOAD["group_k"]) + 4 * (128 // WORKLOAD["group_v"]))
+
+
 def _decode_bytes(hist_tokens, ctx_tokens_bf16, n_q, n_kv, n_hist_pages):
-    per_hist_token = n_kv * 2 * (128 // 4 + 4)
+    per_hist_token = _hist_bytes_per_token(n_kv)
     return (hist_tokens * per_hist_token + ctx_tokens_bf16 * n_kv * 2 * 128 * 2 + n_hist_pages * 4
             + n_q * 128 * 6)
 
@@ -782,13 +792,14 @@ def run_extra(args):
             clk = clocks.stop()
         t_bulk = e[0].elapsed_time(e[1]) / 1e3 / K            # 36 layers
         t_dec = e[1].elapsed_time(e[2]) / 1e3 / (K * 2 * nd)
-        bulk_bytes = L * h * n_kv * (2 * 128 * 2 + 2 * (128 // 4 + 4))
+        bulk_bytes = L * h * (n_kv * 2 * 128 * 2 + _hist_bytes_per_token(n_kv))
         dec_bytes = _decode_bytes(h, s0 + r0, n_q, n_kv, -(-h // 16))
         status = max(int(c.dev_status.item()) for c in caches)
         line.update({
             "metric": "bulk demotion GB/s (read + written) of a 128k-token prefill, 8 KV heads x 36 layers",
             "value": bulk_bytes / t_bulk / 1e9, "unit": "GB/s", "ms_per_step": t_bulk * 1e3,
             "config": {"workload": args.workload, "tokens": h, "n_kv_heads": n_kv, "head_dim": 128, "layers": L,
+                       "quant_group": _group_label(),
                        "distinct_layers": nd, "l2_policy": "inputs larger than L2 (prefill buffers of %.0f MB per layer)"
                        % (ctx * n_kv * 128 * 2 * 2 / 1e6)},
             "roofline": {"bound": "hbm", "achieved": bulk_bytes / t_bulk / 1e9, "peak": peak, "unit": "GB/s",
@@ -873,6 +884,7 @@ def run_extra(args):
         "metric": metric, "value": bsz / t_step, "unit": "tokens/s", "ms_per_step": t_step * 1e3,
         "config": {"workload": args.workload, "batch": bsz, "n_q_heads": n_q, "n_kv_heads": n_kv, "head_dim": 128,
                    "layers": L, "distinct_layers": nd, "ctx_min": min(ctxs), "ctx_max": max(ctxs),
+                   "quant_group": _group_label(),
                    "ctx_mean": sum(ctxs) / bsz, "shared_prefix_tokens": cfg.get("shared", 0),
                    "l2_policy": "inputs larger than L2 (each layer cache > 1 GB)", "cuda_graphs": True},
         "decode_ms": t_dec * 1e3,

@@ -103,7 +103,9 @@ struct Geo {
   static constexpr int T = W * 32;
   // the last kBf16Warps warps scan the BF16 tokens while the others build q~
   static constexpr int PT = (W - kBf16Warps) * 32;
-  static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : OSCAR_GROUP_G8;      // pages per step
+  // pages per step (GQA 8 with several quantisation groups: 2, which keeps
+  // its per-group state within the register budget)
+  static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : (NGK * NGV > 1 ? 2 : OSCAR_GROUP_G8);
   static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
   static constexpr int kBlock = block_bytes(NGK, NGV);   // one (page, KV head) block
   static constexpr int kHalfK = half_bytes(NGK);         // offset of the V half
@@ -279,15 +281,13 @@ struct HistState {
   }
 };
 
-// QK of one INT2 page: d[q][nt] = 2^-24 sigma (q~ . c) over K group q of
-// (token gid | gid + 8) x (head 4 nt + tig hi, lo).  With one group the
-// K-steps are spread over kQkChains accumulators; with NGK groups K-step j
-// reads group j / (8 / NGK) only (the page format's code order), so each
-// group has its own accumulator.
-template <int G, int NGK>
+// QK of one INT2 page (one K group): d[nt] = 2^-24 sigma (q~ . c) of (token
+// gid | gid + 8) x (head 4 nt + tig hi, lo), K-steps spread over kQkChains
+// accumulators.
+template <int G>
 __device__ __forceinline__ void int2_qk(const uint8_t* __restrict__ pg, int gid, int tig,
-                                        const uint32_t (&qb)[Geo<G>::NH][8][2], float (&d)[NGK][Geo<G>::NH][4]) {
-  constexpr int NH = Geo<G>::NH, kQkChains = NGK > 1 ? NGK : Geo<G>::kQkChains;
+                                        const uint32_t (&qb)[Geo<G>::NH][8][2], float (&d)[Geo<G>::NH][4]) {
+  constexpr int NH = Geo<G>::NH, kQkChains = Geo<G>::kQkChains;
   const uint2 kw0 = *reinterpret_cast<const uint2*>(pg + 32 * gid + 8 * tig);
   const uint2 kw1 = *reinterpret_cast<const uint2*>(pg + 32 * (gid + 8) + 8 * tig);
   float dc[kQkChains][NH][4];
@@ -302,24 +302,55 @@ __device__ __forceinline__ void int2_qk(const uint8_t* __restrict__ pg, int gid,
     const uint32_t a0 = code_pair(w00, s00, j), a1 = code_pair(w10, s10, j);
     const uint32_t a2 = code_pair(w01, s01, j), a3 = code_pair(w11, s11, j);
 #pragma unroll
-    const int acc_i = NGK > 1 ? j / (8 / NGK) : j % kQkChains;
-#pragma unroll
-    for (int nt = 0; nt < NH; ++nt) mma_f16(dc[acc_i][nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+    for (int nt = 0; nt < NH; ++nt) mma_f16(dc[j % kQkChains][nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
   }
 #pragma unroll
   for (int nt = 0; nt < NH; ++nt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if constexpr (NGK > 1) {
+      float v = dc[0][nt][c];
 #pragma unroll
-        for (int q = 0; q < NGK; ++q) d[q][nt][c] = dc[q][nt][c];
-      } else {
-        float v = dc[0][nt][c];
-#pragma unroll
-        for (int ch = 1; ch < kQkChains; ++ch) v += dc[ch][nt][c];
-        d[0][nt][c] = v;
-      }
+      for (int ch = 1; ch < kQkChains; ++ch) v += dc[ch][nt][c];
+      d[nt][c] = v;
     }
+}
+
+// QK of one INT2 page with NGK > 1 K groups, each group folded into the
+// score sums as soon as its K-steps are done (one live accumulator set):
+// a[nt][t] = sum_q s_q 2^-24 sigma (q~ . c)_q of token gid (t = 0) or
+// gid + 8 (t = 1).  The page format puts group q in K-steps q J .. q J + J - 1
+// (J = 8 / NGK); ksz0 / ksz1: the tokens' (scale, zero) pairs.
+template <int G, int NGK>
+__device__ __forceinline__ void int2_qk_groups(const uint8_t* __restrict__ pg, int gid, int tig,
+                                               const uint32_t (&qb)[Geo<G>::NH][8][2], const uint32_t (&ksz0)[NGK],
+                                               const uint32_t (&ksz1)[NGK], float (&a)[Geo<G>::NH][2]) {
+  constexpr int NH = Geo<G>::NH, J = 8 / NGK;
+  const uint2 kw0 = *reinterpret_cast<const uint2*>(pg + 32 * gid + 8 * tig);
+  const uint2 kw1 = *reinterpret_cast<const uint2*>(pg + 32 * (gid + 8) + 8 * tig);
+  const uint32_t w00 = kw0.x, w01 = kw0.y, w10 = kw1.x, w11 = kw1.y;
+  const uint32_t s00 = w00 >> 6, s01 = w01 >> 6, s10 = w10 >> 6, s11 = w11 >> 6;
+#pragma unroll
+  for (int nt = 0; nt < NH; ++nt) a[nt][0] = a[nt][1] = 0.f;
+#pragma unroll
+  for (int q = 0; q < NGK; ++q) {
+    float dq[NH][4];
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) dq[nt][0] = dq[nt][1] = dq[nt][2] = dq[nt][3] = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < J; ++jj) {
+      const int j = q * J + jj;
+      const uint32_t a0 = code_pair(w00, s00, j), a1 = code_pair(w10, s10, j);
+      const uint32_t a2 = code_pair(w01, s01, j), a3 = code_pair(w11, s11, j);
+#pragma unroll
+      for (int nt = 0; nt < NH; ++nt) mma_f16(dq[nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+    }
+    const float2 kz0 = half2_to_float2(ksz0[q]), kz1 = half2_to_float2(ksz1[q]);
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) {
+      a[nt][0] = fmaf(kz0.x, dq[nt][0] + dq[nt][1], a[nt][0]);
+      a[nt][1] = fmaf(kz1.x, dq[nt][2] + dq[nt][3], a[nt][1]);
+    }
+  }
 }
 
 // The NG (scale, zero) fp16 pairs of token slot t of a half (pairs start at
@@ -345,32 +376,39 @@ __device__ __forceinline__ void load_sz(const uint8_t* half, int t, uint32_t (&s
 // Scores (log2 units) of the lane's two tokens of one page from its QK
 // accumulators and the tokens' K (scale, zero); -inf where not valid.
 // kMasked = false: every token of the page is valid (no selects).
-// With NGK groups: score = unscale sum_q s_q (q~ . c)_q + sum_q z_q qz_q.
-template <int G, int NGK, bool kMasked>
-__device__ __forceinline__ void int2_scores(const float (&d)[NGK][Geo<G>::NH][4], const uint32_t (&ksz0)[NGK],
-                                            const uint32_t (&ksz1)[NGK], bool ok0, bool ok1,
-                                            const float (&uns)[Geo<G>::NH], const float (&qz)[Geo<G>::NH][NGK],
-                                            float (&sc)[Geo<G>::NH][2]) {
+// Scores (log2 units) of the lane's two tokens of one page from its QK
+// accumulators and the tokens' K (scale, zero); -inf where not valid.
+// kMasked = false: every token of the page is valid (no selects).
+template <int G, bool kMasked>
+__device__ __forceinline__ void int2_scores(const float (&d)[Geo<G>::NH][4], uint32_t ksz0, uint32_t ksz1,
+                                            bool ok0, bool ok1, const float (&uns)[Geo<G>::NH],
+                                            const float (&qz)[Geo<G>::NH][1], float (&sc)[Geo<G>::NH][2]) {
+  const float2 kz0 = half2_to_float2(ksz0), kz1 = half2_to_float2(ksz1);
 #pragma unroll
   for (int nt = 0; nt < Geo<G>::NH; ++nt) {
-    float s0, s1;
-    if constexpr (NGK == 1) {
-      const float2 kz0 = half2_to_float2(ksz0[0]), kz1 = half2_to_float2(ksz1[0]);
-      s0 = fmaf(kz0.x * (d[0][nt][0] + d[0][nt][1]), uns[nt], kz0.y * qz[nt][0]);
-      s1 = fmaf(kz1.x * (d[0][nt][2] + d[0][nt][3]), uns[nt], kz1.y * qz[nt][0]);
-    } else {
-      float a0 = 0.f, a1 = 0.f, z0 = 0.f, z1 = 0.f;
+    const float s0 = fmaf(kz0.x * (d[nt][0] + d[nt][1]), uns[nt], kz0.y * qz[nt][0]);
+    const float s1 = fmaf(kz1.x * (d[nt][2] + d[nt][3]), uns[nt], kz1.y * qz[nt][0]);
+    sc[nt][0] = (!kMasked || ok0) ? s0 : -INFINITY;
+    sc[nt][1] = (!kMasked || ok1) ? s1 : -INFINITY;
+  }
+}
+
+// With NGK > 1 groups: score = unscale sum_q s_q (q~ . c)_q + sum_q z_q qz_q,
+// from the folded sums of int2_qk_groups.
+template <int G, int NGK, bool kMasked>
+__device__ __forceinline__ void int2_scores_groups(const float (&a)[Geo<G>::NH][2], const uint32_t (&ksz0)[NGK],
+                                                   const uint32_t (&ksz1)[NGK], bool ok0, bool ok1,
+                                                   const float (&uns)[Geo<G>::NH],
+                                                   const float (&qz)[Geo<G>::NH][NGK], float (&sc)[Geo<G>::NH][2]) {
 #pragma unroll
-      for (int q = 0; q < NGK; ++q) {
-        const float2 kz0 = half2_to_float2(ksz0[q]), kz1 = half2_to_float2(ksz1[q]);
-        a0 = fmaf(kz0.x, d[q][nt][0] + d[q][nt][1], a0);
-        a1 = fmaf(kz1.x, d[q][nt][2] + d[q][nt][3], a1);
-        z0 = fmaf(kz0.y, qz[nt][q], z0);
-        z1 = fmaf(kz1.y, qz[nt][q], z1);
-      }
-      s0 = fmaf(a0, uns[nt], z0);
-      s1 = fmaf(a1, uns[nt], z1);
+  for (int nt = 0; nt < Geo<G>::NH; ++nt) {
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < NGK; ++q) {
+      z0 = fmaf(half2_to_float2(ksz0[q]).y, qz[nt][q], z0);
+      z1 = fmaf(half2_to_float2(ksz1[q]).y, qz[nt][q], z1);
     }
+    const float s0 = fmaf(a[nt][0], uns[nt], z0), s1 = fmaf(a[nt][1], uns[nt], z1);
     sc[nt][0] = (!kMasked || ok0) ? s0 : -INFINITY;
     sc[nt][1] = (!kMasked || ok1) ? s1 : -INFINITY;
   }
@@ -1035,7 +1073,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // each warp's INT2 state goes into its own ring slice once its pages are done
   float* my_state = reinterpret_cast<float*>(ring);
 
-  constexpr int kGroup = Geo<G>::kGroup;
+  constexpr int kGroup = Gm::kGroup;
   // ---------------- INT2 pages, kGroup per step: QK of the step's pages,
   // one maximum update, then their probabilities and PV.  A page past the
   // warp's range or with an invalid id is computed on stale ring data with
@@ -1100,12 +1138,18 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
             for (int nt = 0; nt < NH; ++nt) sc[u][nt][0] = sc[u][nt][1] = -INFINITY;
             continue;
           }
-          float d[NGK][NH][4];
-          int2_qk<G, NGK>(pg[u], gid, tig, qb, d);
           uint32_t ksz0[NGK], ksz1[NGK];
           load_sz<NGK>(pg[u], gid, ksz0);
           load_sz<NGK>(pg[u], gid + 8, ksz1);
-          int2_scores<G, NGK, kMasked>(d, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
+          if constexpr (NGK == 1) {
+            float d[NH][4];
+            int2_qk<G>(pg[u], gid, tig, qb, d);
+            int2_scores<G, kMasked>(d, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, sc[u]);
+          } else {
+            float a[NH][2];
+            int2_qk_groups<G, NGK>(pg[u], gid, tig, qb, ksz0, ksz1, a);
+            int2_scores_groups<G, NGK, kMasked>(a, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
+          }
         }
         int2_update_max<G, NGV, kGroup>(sc, st);
 #pragma unroll
