@@ -35,6 +35,12 @@ is kept with the design notes):
     even); code = clamp(rint((x - z) / s), 0, 3) with ties to even; s == 0
     gives code 0.  Dequantised value: c * s + z.
   * Four codes per byte, channel 4j+i in bits 2i..2i+1 of byte j.
+  * Lloyd-Max codebook: the group keeps its (scale, zero) from min and max;
+    the normalised value u = (x - z) / s in [0, 3] takes the index of the
+    nearest of four fp16 levels l_0 < l_1 < l_2 < l_3 fitted per layer (K and
+    V apart) by Lloyd's iteration on calibration values, ties to the lower
+    level; dequantised value z + s l[c].  Levels {0, 1, 2, 3} are the
+    uniform codec.
   * Smaller quantisation groups (32 or 64 channels, K and V chosen apart):
     group q of a token-head is the contiguous run of rotated channels
     [q g, (q + 1) g), so the bit-reversal inside R decides which channels
@@ -251,6 +257,77 @@ def dequantize_groups(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) ->
     return codes.astype(np.float64) * s + z
 
 
+def lloyd_max_levels(u: np.ndarray, iters: int = 100, init=(0.0, 1.0, 2.0, 3.0)) -> np.ndarray:
+    """Four-level Lloyd-Max quantiser of the samples u (float64).
+
+    Lloyd's iteration from `init`: thresholds at the midpoints of adjacent
+    levels; each level becomes the mean of the samples in its cell (u <=
+    t_1, t_1 < u <= t_2, ...; an empty cell keeps its level); stops after
+    `iters` rounds or when no level moves.  [ZAKER] "OSCAR 把旋转对准
+    attention" closing part (the code repo pairs the rotation with a
+    Lloyd-Max codebook).
+    """
+    u = np.sort(np.asarray(u, dtype=np.float64).ravel())
+    lv = np.array(init, dtype=np.float64)
+    for _ in range(iters):
+        t = (lv[:-1] + lv[1:]) / 2.0
+        cell = np.searchsorted(t, u, side="left")      # number of thresholds below u
+        new = lv.copy()
+        for k in range(4):
+            sel = u[cell == k]
+            if sel.size:
+                new[k] = sel.mean()
+        if np.array_equal(new, lv):
+            break
+        lv = new
+    return lv
+
+
+def normalised_values(x_rot: np.ndarray, tau: float) -> np.ndarray:
+    """u = (x - z) / s of every channel of rows with s > 0, with the codec's
+    fp16 (scale, zero) of one group per row (the calibration input of the
+    codebook fit)."""
+    xc = np.clip(np.asarray(x_rot, dtype=np.float64), -tau, tau)
+    _, s16, z16 = quantize(xc, tau)
+    s = s16.astype(np.float64)
+    z = z16.astype(np.float64)
+    keep = s > 0
+    return ((xc[keep] - z[keep][:, None]) / s[keep][:, None]).ravel()
+
+
+def fit_codebook(x: np.ndarray, r: np.ndarray, tau: float, iters: int = 100) -> np.ndarray:
+    """fp16 Lloyd-Max levels (as float16) of one layer from calibration rows
+    x [n][d] (rotated by r, clipped at tau, normalised per row)."""
+    lv = lloyd_max_levels(normalised_values(rotate(x, r), tau), iters)
+    return lv.astype(np.float16)
+
+
+def quantize_codebook(x_rot: np.ndarray, tau: float, levels):
+    """Clip, then (scale, zero) as in `quantize` and the nearest-level code.
+
+    code = number of thresholds t_k = (l_(k-1) + l_k) / 2 strictly below
+    u = (x - z) / s (so a tie takes the lower level); s == 0 gives code 0.
+    """
+    lv = np.asarray(levels, dtype=np.float16).astype(np.float64)
+    xc = np.clip(np.asarray(x_rot, dtype=np.float64), -tau, tau)
+    _, s16, z16 = quantize(xc, tau)
+    s = s16.astype(np.float64)[..., None]
+    z = z16.astype(np.float64)[..., None]
+    t = (lv[:-1] + lv[1:]) / 2.0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = (xc - z) / s
+        c = (u > t[0]).astype(np.uint8) + (u > t[1]) + (u > t[2])
+    c = np.where(s > 0, c, 0)
+    return c.astype(np.uint8), s16, z16
+
+
+def dequantize_codebook(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray, levels) -> np.ndarray:
+    """x^ = z + s l[c] (float64)."""
+    lv = np.asarray(levels, dtype=np.float16).astype(np.float64)
+    return (lv[np.asarray(codes)] * np.asarray(scale, dtype=np.float64)[..., None]
+            + np.asarray(zero, dtype=np.float64)[..., None])
+
+
 def demote(x: np.ndarray, r: np.ndarray, tau: float):
     """Rotate -> clip -> quantise one or many token vectors x[..., d] with one R."""
     return quantize(rotate(x, r), tau)
@@ -459,7 +536,9 @@ def decode_attention(q: np.ndarray, sink_k: np.ndarray, sink_v: np.ndarray,
     [ZAKER] pipeline part (BF16 sink 64 | INT2 history | BF16 recent 256);
     [GIST] 2.2 B (inverse rotation inside attention); [CSDN] 三.1.
     With several quantisation groups, scale_* / zero_* carry a trailing group
-    axis [Lh][H_kv][ng] and each channel uses its group's pair.
+    axis [Lh][H_kv][ng] and each channel uses its group's pair.  With a
+    Lloyd-Max codebook, hist also holds levels_k / levels_v (four fp16
+    levels each) and a history value is z + s l[c].
     """
     n_q = q.shape[0]
     n_kv = r_k.shape[0]
@@ -468,6 +547,8 @@ def decode_attention(q: np.ndarray, sink_k: np.ndarray, sink_v: np.ndarray,
 
     def deq(which, kv):
         c, s, z = hist["codes_" + which][:, kv], hist["scale_" + which][:, kv], hist["zero_" + which][:, kv]
+        if "levels_" + which in hist:
+            return dequantize_codebook(c, s, z, hist["levels_" + which])
         return dequantize_groups(c, s, z) if np.ndim(s) == 2 else dequantize(c, s, z)
 
     for kv in range(n_kv):

@@ -600,3 +600,83 @@ def test_grouped_storage_cost_closed_form():
     assert O.effective_bits_per_element(10 ** 9, group=64) == pytest.approx(2.5, abs=1e-5)
     assert O.kv_bytes_per_history_token(8, group_k=32, group_v=32) == 8 * (64 + 32)
     assert O.kv_bytes_per_history_token(8) == 576
+
+
+# ---------------------------------------------------------------- Lloyd-Max codebook
+
+def test_lloyd_max_uniform_density_closed_form():
+    # For a uniform density on [0, 3] the optimal 4-level quantiser has equal
+    # cells: levels (k + 1/2) 3 / 4.
+    u = (np.arange(240000) + 0.5) / 240000 * 3.0
+    np.testing.assert_allclose(O.lloyd_max_levels(u, 2000), [0.375, 1.125, 1.875, 2.625], atol=2e-5)
+
+
+def test_lloyd_max_gaussian_matches_max_1960():
+    norm = pytest.importorskip("scipy.stats").norm
+    want = {}
+    for line in golden_lines("lloyd_max_gaussian.txt"):
+        k, v = line.split(":")
+        want[k.strip()] = np.array([float(x) for x in v.split()])
+    g = norm.ppf((np.arange(400000) + 0.5) / 400000)
+    lv = O.lloyd_max_levels(g, 3000, init=(-1.5, -0.5, 0.5, 1.5))
+    np.testing.assert_allclose(lv, want["levels"], atol=6e-4)
+    np.testing.assert_allclose((lv[:-1] + lv[1:]) / 2, want["thresholds"], atol=6e-4)
+
+
+def test_lloyd_max_affine_equivariance_and_fixed_point():
+    g = synth.generator(12, 75)
+    u = np.concatenate([g.gamma(2.0, 0.4, 5000), 3.0 - g.gamma(3.0, 0.3, 3000)]).clip(0, 3)
+    lv = O.lloyd_max_levels(u, 500)
+    lv2 = O.lloyd_max_levels(2.5 * u - 1.0, 500, init=tuple(2.5 * np.array([0.0, 1.0, 2.0, 3.0]) - 1.0))
+    np.testing.assert_allclose(lv2, 2.5 * lv - 1.0, rtol=1e-9, atol=1e-9)
+    # centroid condition: every level is the mean of the samples nearest to it
+    near = np.argmin(np.abs(u[:, None] - lv[None, :]), axis=1)
+    for k in range(4):
+        if np.any(near == k):
+            assert abs(u[near == k].mean() - lv[k]) < 1e-9
+
+
+def test_codebook_code_is_nearest_level_brute_force():
+    g = synth.generator(13, 76)
+    x = g.standard_normal((200, 128)) * 1.5
+    levels = np.array([0.3, 1.05, 1.9, 2.75], np.float16)
+    c, s, z = O.quantize_codebook(x, 4.0, levels)
+    xc = np.clip(x, -4.0, 4.0)
+    lv = levels.astype(np.float64)
+    u = (xc - z.astype(np.float64)[:, None]) / s.astype(np.float64)[:, None]
+    want = np.argmin(np.abs(u[..., None] - lv), axis=-1)       # lowest index on a tie
+    np.testing.assert_array_equal(c, want)
+    # scale and zero are the uniform codec's; uniform levels give its codes
+    _, s0, z0 = O.quantize(x, 4.0)
+    np.testing.assert_array_equal(s.view(np.uint16), s0.view(np.uint16))
+    np.testing.assert_array_equal(z.view(np.uint16), z0.view(np.uint16))
+    cu, _, _ = O.quantize_codebook(x, 4.0, np.array([0, 1, 2, 3], np.float16))
+    np.testing.assert_array_equal(cu, O.quantize(x, 4.0)[0])    # no exact ties in this draw
+    # reconstruction error: within half the widest cell, in units of s
+    xr = O.dequantize_codebook(c, s, z, levels)
+    width = np.max(np.diff(np.concatenate([[0.0], (lv[:-1] + lv[1:]) / 2, [3.0]])))
+    assert np.all(np.abs(xr - xc) <= np.maximum(width, 2 * lv[0], ) * s.astype(np.float64)[:, None] + 1e-9)
+
+
+def test_codebook_decode_equals_plain_dequantisation():
+    g = synth.generator(14, 77)
+    n_kv, hq, lh = 1, 4, 25
+    r = _orthogonal(128, 7)[None]
+    codes = g.integers(0, 4, size=(lh, n_kv, 128)).astype(np.uint8)
+    s = (np.abs(g.standard_normal((lh, n_kv))) * 0.3 + 0.05).astype(np.float16)
+    z = (g.standard_normal((lh, n_kv)) * 0.2).astype(np.float16)
+    lk = np.array([0.2, 0.9, 2.1, 2.8], np.float16)
+    lvv = np.array([0.4, 1.2, 1.7, 2.6], np.float16)
+    q = g.standard_normal((hq, 128))
+    empty = np.zeros((0, n_kv, 128))
+    h = dict(codes_k=codes, scale_k=s, zero_k=z, codes_v=codes[::-1].copy(), scale_v=s[::-1].copy(),
+             zero_v=z[::-1].copy(), levels_k=lk, levels_v=lvv)
+    got = O.decode_attention(q, empty, empty, h, empty, empty, r, r)
+    keys = np.array([[float(z[t, 0]) + float(s[t, 0]) * float(lk[codes[t, 0, c]]) for c in range(128)]
+                     for t in range(lh)]) @ r[0].T
+    vals = np.array([[float(z[::-1][t, 0]) + float(s[::-1][t, 0]) * float(lvv[codes[::-1][t, 0, c]])
+                      for c in range(128)] for t in range(lh)]) @ r[0].T
+    for hh in range(hq):
+        sc = keys @ q[hh] / math.sqrt(128)
+        p = np.exp(sc - sc.max())
+        np.testing.assert_allclose(got[hh], (p / p.sum()) @ vals, rtol=1e-12, atol=1e-12)
