@@ -44,7 +44,7 @@ if ROOT not in sys.path:
 
 WORKLOAD = dict(workload="qwen3-8b-layer-decode-100k", batch=1, n_q_heads=32, n_kv_heads=8,
                 head_dim=128, ctx=100_000, sink=64, recent=256, page_tokens=16, group_k=128, group_v=128,
-                seed=1002)
+                codebook="uniform", seed=1002)
 METRIC = "decode-attn tokens/s at 100k ctx (1 layer, Qwen3-8B shape)"
 UNIT = "tokens/s"
 EXTRA_WORKLOADS = {
@@ -84,8 +84,16 @@ def _args():
     ap.add_argument("--quant-group", default="128,128",
                     choices=["%d,%d" % (a, b) for a in (32, 64, 128) for b in (32, 64, 128)],
                     help="quantisation group sizes of K and V (channels), for every GPU workload")
+    ap.add_argument("--codebook", default="uniform", choices=["uniform", "lloyd-max"],
+                    help="code levels: the uniform scale/zero grid, or per-layer Lloyd-Max levels fitted on "
+                         "the calibration rows (one quantisation group per vector)")
     args = ap.parse_args()
     WORKLOAD["group_k"], WORKLOAD["group_v"] = (int(x) for x in args.quant_group.split(","))
+    WORKLOAD["codebook"] = args.codebook
+    if args.codebook != "uniform" and (WORKLOAD["group_k"], WORKLOAD["group_v"]) != (128, 128):
+        ap.error("--codebook lloyd-max takes one quantisation group per vector")
+    if args.codebook != "uniform" and args.workload != WORKLOAD["workload"]:
+        ap.error("--codebook lloyd-max applies to the default workload")
     return args
 
 
@@ -118,7 +126,7 @@ def _config_json(extra=None):
     cfg = {"workload": w["workload"], "batch": w["batch"], "n_q_heads": w["n_q_heads"],
            "n_kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"], "ctx": w["ctx"],
            "sink_bf16": s, "history_int2": h, "recent_bf16": r, "page_tokens": w["page_tokens"],
-           "quant_group": _group_label(), "parallelism": "replicas"}
+           "quant_group": _group_label(), "codebook": w["codebook"], "parallelism": "replicas"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -145,14 +153,22 @@ def _oracle_sample_setup():
     g = w["n_q_heads"] // w["n_kv_heads"]
     q = synth.activations(seed, (0, 0, 2), 1, np.repeat(outl, g, axis=0))[0].astype(np.float64)
     hist = {}
+    if w["codebook"] != "uniform":
+        # the oracle's own Lloyd-Max fit on this head's calibration rows
+        hist["levels_k"] = O.fit_codebook(cal["k"], rk, tau_k)
+        hist["levels_v"] = O.fit_codebook(cal["v"], rv, tau_v)
     for name, x, rot, tau in (("k", k, rk, tau_k), ("v", v, rv, tau_v)):
-        c, sc, ze = _oracle_demote(O, x[s:s + h - 1, 0], rot, tau, w["group_" + name])
+        c, sc, ze = _oracle_demote(O, x[s:s + h - 1, 0], rot, tau, w["group_" + name],
+                                   hist.get("levels_" + name))
         hist["codes_" + name], hist["scale_" + name], hist["zero_" + name] = c[:, None], sc[:, None], ze[:, None]
     return dict(O=O, np=np, q=q, k=k, v=v, rk=rk, rv=rv, tau_k=tau_k, tau_v=tau_v, hist=hist, s=s, h=h, r=r)
 
 
-def _oracle_demote(O, x, r, tau, group):
-    """The oracle's demotion of rows x with one or several quantisation groups."""
+def _oracle_demote(O, x, r, tau, group, levels=None):
+    """The oracle's demotion of rows x with one or several quantisation groups,
+    or with codebook levels."""
+    if levels is not None:
+        return O.quantize_codebook(O.rotate(x, r), tau, levels)
     if group == WORKLOAD["head_dim"]:
         return O.demote(x, r, tau)
     return O.quantize_groups(O.rotate(x, r), tau, group)
@@ -166,15 +182,20 @@ def _oracle_step(st, n_hist=None):
     O, np = st["O"], st["np"]
     s, h = st["s"], st["h"]
     keep = (h - 1) if n_hist is None else max(0, min(h - 1, n_hist - 1))
-    ck, sk, zk = _oracle_demote(O, st["k"][s + h - 1, 0][None], st["rk"], st["tau_k"], WORKLOAD["group_k"])
-    cv, sv, zv = _oracle_demote(O, st["v"][s + h - 1, 0][None], st["rv"], st["tau_v"], WORKLOAD["group_v"])
     old = st["hist"]
+    ck, sk, zk = _oracle_demote(O, st["k"][s + h - 1, 0][None], st["rk"], st["tau_k"], WORKLOAD["group_k"],
+                                old.get("levels_k"))
+    cv, sv, zv = _oracle_demote(O, st["v"][s + h - 1, 0][None], st["rv"], st["tau_v"], WORKLOAD["group_v"],
+                                old.get("levels_v"))
     hist = {"codes_k": np.concatenate([old["codes_k"][:keep], ck[:, None]]),
             "scale_k": np.concatenate([old["scale_k"][:keep], sk[:, None]]),
             "zero_k": np.concatenate([old["zero_k"][:keep], zk[:, None]]),
             "codes_v": np.concatenate([old["codes_v"][:keep], cv[:, None]]),
             "scale_v": np.concatenate([old["scale_v"][:keep], sv[:, None]]),
             "zero_v": np.concatenate([old["zero_v"][:keep], zv[:, None]])}
+    for name in ("levels_k", "levels_v"):
+        if name in old:
+            hist[name] = old[name]
     k, v = st["k"], st["v"]
     return O.decode_attention(st["q"], k[:s], v[:s], hist, k[s + h:s + h + st["r"]],
                               v[s + h:s + h + st["r"]], st["rk"][None], st["rv"][None])
@@ -206,7 +227,7 @@ def cpu_baseline(reps=20):
     """The oracle timed on one host core in a fresh process (started before any GPU work)."""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
                         "--reps", str(reps), "--quant-group",
-                        "%d,%d" % (WORKLOAD["group_k"], WORKLOAD["group_v"])],
+                        "%d,%d" % (WORKLOAD["group_k"], WORKLOAD["group_v"]), "--codebook", WORKLOAD["codebook"]],
                        capture_output=True, text=True, env=_single_thread_env(),
                        timeout=900)
     if r.returncode != 0:
@@ -308,8 +329,8 @@ def _profiled_traffic():
     taken on the current kernel sources (else None)."""
     import hashlib
     import re
-    if (WORKLOAD["group_k"], WORKLOAD["group_v"]) != (128, 128):
-        return None    # the summary covers the one-group kernel
+    if (WORKLOAD["group_k"], WORKLOAD["group_v"]) != (128, 128) or WORKLOAD["codebook"] != "uniform":
+        return None    # the summary covers the one-group, uniform-level kernel
     prof = os.path.join(ROOT, "profiles", "split_kernel_qwen3-8b-layer-decode-100k.md")
     try:
         text = open(prof).read()
@@ -358,6 +379,13 @@ def rotations_from_library(B, kind="oscar"):
     rv32 = np.stack(rv).astype(np.float32)
     tau_k = B.oscar_clip_threshold(np.stack(ck), rk32.astype(np.float64))
     tau_v = B.oscar_clip_threshold(np.stack(cv), rv32.astype(np.float64))
+    if w["codebook"] != "uniform":
+        # Lloyd-Max levels of the layer from its heads' rotated calibration rows
+        eye = np.eye(w["head_dim"])
+        xk = np.concatenate([ck[i] @ rk32[i].astype(np.float64) for i in range(n_kv)])
+        xv = np.concatenate([cv[i] @ rv32[i].astype(np.float64) for i in range(n_kv)])
+        w["levels_k"] = [float(x) for x in B.oscar_fit_codebook(xk, eye, tau_k)]
+        w["levels_v"] = [float(x) for x in B.oscar_fit_codebook(xv, eye, tau_v)]
     return rk32, rv32, tau_k, tau_v, outl
 
 
@@ -372,7 +400,7 @@ def build_layer(torch, B, dev, rot):
     table, n_pages = synth.page_table(seed, [h] * bsz, n_extra_pages=1)
     cache = LayerCache(bsz, w["n_q_heads"], n_kv, table.shape[1], n_pages, torch.from_numpy(rk),
                        torch.from_numpy(rv), tau_k, tau_v, device=dev, quant_group_k=w["group_k"],
-                       quant_group_v=w["group_v"])
+                       quant_group_v=w["group_v"], levels_k=w.get("levels_k"), levels_v=w.get("levels_v"))
     cache.page_table.copy_(torch.from_numpy(table))
     cache.max_hist = h
     chunk = 32768

@@ -38,6 +38,7 @@ class LayerDesc(ctypes.Structure):
         ("recent_k", c_void_p), ("recent_v", c_void_p), ("recent_len", c_void_p),
         ("recent_start", c_void_p), ("r_k", c_void_p), ("r_v", c_void_p), ("dev_status", c_void_p),
         ("quant_group_k", c_int32), ("quant_group_v", c_int32),
+        ("codebook", c_int32), ("levels_k", c_float * 4), ("levels_v", c_float * 4),
     ]
 
 
@@ -56,6 +57,7 @@ def _load():
         "oscar_covariance": (c_int32, [P, c_int64, c_int32, c_int64, P, P, ctypes.POINTER(c_size_t), P]),
         "oscar_score_weighted_rows": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_double, P]),
         "oscar_clip_threshold": (c_int32, [P, c_int64, c_int32, c_int32, P, c_double, P]),
+        "oscar_fit_codebook": (c_int32, [P, c_int64, c_int32, P, c_double, c_int32, P]),
         "oscar_quantize_append": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
                                             P, P, c_int32, P, P, P]),
         "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
@@ -169,6 +171,16 @@ def oscar_clip_threshold(acts: np.ndarray, r: np.ndarray, quantile: float = 0.99
     _check("oscar_clip_threshold", lib.oscar_clip_threshold(
         acts.ctypes.data, rows, h, d, r.ctypes.data, quantile, ctypes.byref(tau)))
     return tau.value
+
+
+def oscar_fit_codebook(x: np.ndarray, r: np.ndarray, tau: float, iters: int = 100) -> np.ndarray:
+    """Four Lloyd-Max levels (float32 holding fp16 values) from calibration rows
+    x [n][d] rotated by r [d][d] and clipped at tau (host float64)."""
+    x, r = _f64(x), _f64(r)
+    out = np.empty(4, dtype=np.float32)
+    _check("oscar_fit_codebook", lib.oscar_fit_codebook(x.ctypes.data, x.shape[0], x.shape[1], r.ctypes.data,
+                                                        float(tau), int(iters), out.ctypes.data))
+    return out
 
 
 def oscar_quantize_append(desc: LayerDesc, k_src, v_src, src_rows: int, row_stride: int, src_index,

@@ -21,12 +21,17 @@ class LayerCache:
     def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, max_pages_per_seq: int,
                  n_pages: int, r_k: torch.Tensor, r_v: torch.Tensor, tau_k: float, tau_v: float,
                  device="cuda", sink_cap: int = 64, recent_cap: int = 256, quant_group_k: int = 128,
-                 quant_group_v: int = 128):
+                 quant_group_v: int = 128, levels_k=None, levels_v=None):
         self.batch, self.n_q_heads, self.n_kv_heads = batch, n_q_heads, n_kv_heads
         self.quant_group_k, self.quant_group_v = int(quant_group_k), int(quant_group_v)
         self.block_bytes = oscar_block_bytes(self.quant_group_k, self.quant_group_v)
         if self.block_bytes <= 0:
             raise ValueError("quantisation group sizes must be 32, 64 or 128")
+        # Lloyd-Max codebook levels (four fp16 values each) or None (uniform)
+        self.levels_k = None if levels_k is None else [float(x) for x in levels_k]
+        self.levels_v = None if levels_v is None else [float(x) for x in levels_v]
+        if (self.levels_k is None) != (self.levels_v is None):
+            raise ValueError("codebook levels for both K and V, or for neither")
         self.sink_cap, self.recent_cap = sink_cap, recent_cap
         self.max_pages_per_seq, self.n_pages = max_pages_per_seq, n_pages
         self.tau_k, self.tau_v = float(tau_k), float(tau_v)
@@ -58,6 +63,10 @@ class LayerCache:
         d.n_pages = self.n_pages
         d.tau_k, d.tau_v = self.tau_k, self.tau_v
         d.quant_group_k, d.quant_group_v = self.quant_group_k, self.quant_group_v
+        if self.levels_k is not None:
+            d.codebook = 1
+            for i in range(4):
+                d.levels_k[i], d.levels_v[i] = self.levels_k[i], self.levels_v[i]
         for name in ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
                      "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status"):
             setattr(d, name, getattr(self, name).data_ptr())

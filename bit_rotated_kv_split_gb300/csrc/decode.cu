@@ -93,7 +93,7 @@ constexpr uint32_t kPrologueBarrier = 1;      // named barrier of the q~ prologu
 
 // NGK / NGV: quantisation groups per token-head of K / V (1, 2 or 4); they
 // fix the page block size and, through it, how many ring stages fit.
-template <int G, int NGK = 1, int NGV = 1>
+template <int G, int NGK = 1, int NGV = 1, bool LV = false>
 struct Geo {
   static constexpr int NT = (2 * G + 7) / 8;          // column tiles holding hi | lo parts
   static constexpr int HS = G >= 8 ? G / 4 : 2;       // BF16 head slots per lane
@@ -103,9 +103,9 @@ struct Geo {
   static constexpr int T = W * 32;
   // the last kBf16Warps warps scan the BF16 tokens while the others build q~
   static constexpr int PT = (W - kBf16Warps) * 32;
-  // pages per step (GQA 8 with several quantisation groups: 2, which keeps
-  // its per-group state within the register budget)
-  static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : (NGK * NGV > 1 ? 2 : OSCAR_GROUP_G8);
+  // pages per step (GQA 8 with several quantisation groups or codebook
+  // levels: 2, which keeps the extra state within the register budget)
+  static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : (NGK * NGV > 1 || LV ? 2 : OSCAR_GROUP_G8);
   static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
   static constexpr int kBlock = block_bytes(NGK, NGV);   // one (page, KV head) block
   static constexpr int kHalfK = half_bytes(NGK);         // offset of the V half
@@ -551,6 +551,166 @@ __device__ __forceinline__ void store_hist_state(HistState<G, NGV>& st, float* w
   }
 }
 
+// ---------------------------------------------------------------- codebook levels
+// A code c = b0 + 2 b1 with level l[c] = l_0 + d1 c + a2 (2 b1) + b (b0 b1):
+// the three bit planes c, 2 b1 and b0 b1 are taken by single ANDs at the
+// positions code_pair uses (so they meet the same B fragments), with b0 b1
+// read from t = w & (w >> 1).
+
+__device__ __forceinline__ uint32_t plane_pair(uint32_t w, uint32_t wsh, int j, uint32_t m) {
+  return j < 5 ? (w & (m << (2 * j))) : (wsh & (m << (2 * (j - 3))));
+}
+
+// QK of one page with levels: e[nt][t] = sum over planes k = (c, 2 b1, b0 b1)
+// of coef[1 + k] 2^-24 sigma (q~ . plane_k) of token gid (t = 0) or gid + 8,
+// the planes taken one after another and folded (one live accumulator set).
+template <int G>
+__device__ __forceinline__ void int2_qk_levels(const uint8_t* __restrict__ pg, int gid, int tig,
+                                               const uint32_t (&qb)[Geo<G>::NH][8][2], const float* coef,
+                                               float (&e)[Geo<G>::NH][2]) {
+  constexpr int NH = Geo<G>::NH;
+  const uint2 kw0 = *reinterpret_cast<const uint2*>(pg + 32 * gid + 8 * tig);
+  const uint2 kw1 = *reinterpret_cast<const uint2*>(pg + 32 * (gid + 8) + 8 * tig);
+  const uint32_t w[4] = {kw0.x, kw1.x, kw0.y, kw1.y};   // a0, a1, a2, a3 sources
+#pragma unroll
+  for (int nt = 0; nt < NH; ++nt) e[nt][0] = e[nt][1] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    uint32_t src[4], sh[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      src[r] = k == 2 ? (w[r] & (w[r] >> 1)) : w[r];
+      sh[r] = src[r] >> 6;
+    }
+    const uint32_t m = k == 0 ? 0x00030003u : k == 1 ? 0x00020002u : 0x00010001u;
+    float d[NH][4];
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a0 = plane_pair(src[0], sh[0], j, m), a1 = plane_pair(src[1], sh[1], j, m);
+      const uint32_t a2 = plane_pair(src[2], sh[2], j, m), a3 = plane_pair(src[3], sh[3], j, m);
+#pragma unroll
+      for (int nt = 0; nt < NH; ++nt) mma_f16(d[nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt) {
+      e[nt][0] = fmaf(coef[1 + k], d[nt][0] + d[nt][1], e[nt][0]);
+      e[nt][1] = fmaf(coef[1 + k], d[nt][2] + d[nt][3], e[nt][1]);
+    }
+  }
+}
+
+// Scores with levels: q~ . k^ = s (d1 S_c + a2 S_2b1 + b S_b0b1) + (z + s l_0) sum q~.
+template <int G, bool kMasked>
+__device__ __forceinline__ void int2_scores_levels(const float (&e)[Geo<G>::NH][2], uint32_t ksz0, uint32_t ksz1,
+                                                   bool ok0, bool ok1, const float (&uns)[Geo<G>::NH],
+                                                   const float (&qz)[Geo<G>::NH][1], const float* coef,
+                                                   float (&sc)[Geo<G>::NH][2]) {
+  const float2 kz0 = half2_to_float2(ksz0), kz1 = half2_to_float2(ksz1);
+  const float z0 = fmaf(kz0.x, coef[0], kz0.y), z1 = fmaf(kz1.x, coef[0], kz1.y);
+#pragma unroll
+  for (int nt = 0; nt < Geo<G>::NH; ++nt) {
+    const float s0 = fmaf(kz0.x * e[nt][0], uns[nt], z0 * qz[nt][0]);
+    const float s1 = fmaf(kz1.x * e[nt][1], uns[nt], z1 * qz[nt][0]);
+    sc[nt][0] = (!kMasked || ok0) ? s0 : -INFINITY;
+    sc[nt][1] = (!kMasked || ok1) ? s1 : -INFINITY;
+  }
+}
+
+// Probabilities with levels: z[nt][0] += sum p z_V, z[nt][1] += sum p s_V (the
+// l_0 part), and one PV operand per plane k: p s_V sigma_v coef[1 + k].
+template <int G, bool kMasked>
+__device__ __forceinline__ void int2_probs_levels(const float (&sc)[Geo<G>::NH][2], uint32_t vsz0, uint32_t vsz1,
+                                                  bool ok0, bool ok1, float sigma_v, const float* coef,
+                                                  HistState<G, 2>& st, uint32_t (&pb)[3][Geo<G>::NH][2]) {
+  const float2 vz0 = half2_to_float2(vsz0), vz1 = half2_to_float2(vsz1);
+#pragma unroll
+  for (int nt = 0; nt < Geo<G>::NH; ++nt) {
+    float p0 = fast_exp2(sc[nt][0] - st.m[nt]);
+    float p1 = fast_exp2(sc[nt][1] - st.m[nt]);
+    if constexpr (kMasked) {
+      p0 = ok0 ? p0 : 0.f;
+      p1 = ok1 ? p1 : 0.f;
+    }
+    st.l[nt] += p0 + p1;
+    st.z[nt][0] = fmaf(p0, vz0.y, fmaf(p1, vz1.y, st.z[nt][0]));
+    st.z[nt][1] = fmaf(p0, vz0.x, fmaf(p1, vz1.x, st.z[nt][1]));
+    const float q0 = p0 * (vz0.x * sigma_v), q1 = p1 * (vz1.x * sigma_v);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const float r0 = q0 * coef[1 + k], r1 = q1 * coef[1 + k];
+      const __half h0 = __float2half_rn(r0), h1 = __float2half_rn(r1);
+      const __half l0 = __float2half_rn(r0 - __half2float(h0)), l1 = __float2half_rn(r1 - __half2float(h1));
+      pb[k][nt][0] = movmatrix_trans(uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(l0)) << 16));
+      pb[k][nt][1] = movmatrix_trans(uint32_t(__half_as_ushort(h1)) | (uint32_t(__half_as_ushort(l1)) << 16));
+    }
+  }
+}
+
+// PV with levels: acc += sum over planes of plane^T . pb[plane].
+template <int G>
+__device__ __forceinline__ void int2_pv_levels(const uint8_t* __restrict__ pg, int gid, int tig,
+                                               const uint32_t (&pb)[3][Geo<G>::NH][2], HistState<G, 2>& st) {
+  const uint8_t* pv = pg + kHalfBytes;
+  const uint32_t va = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 4 * gid);
+  const uint32_t vb = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 32 + 4 * gid);
+  const uint32_t vc = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 256 + 4 * gid);
+  const uint32_t vd = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 288 + 4 * gid);
+  const uint32_t x[4] = {prmt(va, vb, 0x5410), prmt(va, vb, 0x7632), prmt(vc, vd, 0x5410), prmt(vc, vd, 0x7632)};
+  uint32_t xs[4], t[4], ts[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    xs[r] = x[r] >> 6;
+    t[r] = x[r] & (x[r] >> 1);
+    ts[r] = t[r] >> 6;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    uint32_t a[3][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      a[0][r] = plane_pair(x[r], xs[r], mt, 0x00030003u);
+      a[1][r] = plane_pair(x[r], xs[r], mt, 0x00020002u);
+      a[2][r] = plane_pair(t[r], ts[r], mt, 0x00010001u);
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+      for (int nt = 0; nt < Geo<G>::NH; ++nt)
+        mma_f16(st.acc[nt][mt], a[k][0], a[k][1], a[k][2], a[k][3], pb[k][nt][0], pb[k][nt][1]);
+  }
+}
+
+// INT2 warp state with levels -> ws: o~ = (hi + lo) 2^24 4^-pos(mt) / sigma_v
+// + sum p z_V + l_0 sum p s_V.
+template <int G>
+__device__ __forceinline__ void store_hist_state_levels(HistState<G, 2>& st, float* ws, int gid, int tig,
+                                                        float pv_unscale, float l0) {
+  constexpr int NH = Geo<G>::NH;
+#pragma unroll
+  for (int nt = 0; nt < NH; ++nt) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      st.l[nt] += __shfl_xor_sync(kFull, st.l[nt], o);
+      st.z[nt][0] += __shfl_xor_sync(kFull, st.z[nt][0], o);
+      st.z[nt][1] += __shfl_xor_sync(kFull, st.z[nt][1], o);
+    }
+    const int h = 4 * nt + tig;
+    const float zt = fmaf(l0, st.z[nt][1], st.z[nt][0]);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const float f = pv_unscale * __int_as_float((127 - 2 * code_pos(mt)) << 23);
+      ws[h * kPartStride + 4 + 16 * gid + mt] = fmaf(st.acc[nt][mt][0] + st.acc[nt][mt][1], f, zt);
+      ws[h * kPartStride + 4 + 16 * gid + 8 + mt] = fmaf(st.acc[nt][mt][2] + st.acc[nt][mt][3], f, zt);
+    }
+    if (gid == 0) {
+      ws[h * kPartStride + 0] = st.m[nt];
+      ws[h * kPartStride + 1] = st.l[nt];
+    }
+  }
+}
+
 // ------------------------------------------------------------------ BF16 page
 
 template <int G>
@@ -822,9 +982,12 @@ struct PidWindow {
 
 // ------------------------------------------------------------------ split kernel
 
-template <int G, int NGK, int NGV>
+// kLevels: codebook levels (one quantisation group per vector only).
+template <int G, int NGK, int NGV, bool kLevels>
 __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_constant__ DecodeParams p) {
-  using Gm = Geo<G, NGK, NGV>;
+  using Gm = Geo<G, NGK, NGV, kLevels>;
+  static_assert(!kLevels || (NGK == 1 && NGV == 1), "codebook levels with one group per vector");
+  constexpr int NZ = kLevels ? 2 : NGV;   // zero-point sums per head
   constexpr int NTQ = Geo<G>::NTQ, W = Geo<G>::W, T = Geo<G>::T;
   constexpr int kStages = Gm::kStages;
   constexpr int kBlock = Gm::kBlock;
@@ -1079,7 +1242,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // warp's range or with an invalid id is computed on stale ring data with
   // every token masked (uniform control flow, no effect on the result).
   {
-    HistState<G, NGV> st;
+    HistState<G, NZ> st;
     st.init();
     bool timed_out = false;
     int k = 0;
@@ -1141,7 +1304,11 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
           uint32_t ksz0[NGK], ksz1[NGK];
           load_sz<NGK>(pg[u], gid, ksz0);
           load_sz<NGK>(pg[u], gid + 8, ksz1);
-          if constexpr (NGK == 1) {
+          if constexpr (kLevels) {
+            float e[NH][2];
+            int2_qk_levels<G>(pg[u], gid, tig, qb, p.coef_k, e);
+            int2_scores_levels<G, kMasked>(e, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, p.coef_k, sc[u]);
+          } else if constexpr (NGK == 1) {
             float d[NH][4];
             int2_qk<G>(pg[u], gid, tig, qb, d);
             int2_scores<G, kMasked>(d, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, sc[u]);
@@ -1151,16 +1318,22 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
             int2_scores_groups<G, NGK, kMasked>(a, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
           }
         }
-        int2_update_max<G, NGV, kGroup>(sc, st);
+        int2_update_max<G, NZ, kGroup>(sc, st);
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
           if (kMasked && u > 0 && k + u >= count) continue;
           uint32_t vsz0[NGV], vsz1[NGV];
           load_sz<NGV>(pg[u] + Gm::kHalfK, gid, vsz0);
           load_sz<NGV>(pg[u] + Gm::kHalfK, gid + 8, vsz1);
-          uint32_t pb[NGV][NH][2];
-          int2_probs<G, NGV, kMasked>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
-          int2_pv<G, NGV, Gm::kHalfK>(pg[u], gid, tig, pb, st);
+          if constexpr (kLevels) {
+            uint32_t pb[3][NH][2];
+            int2_probs_levels<G, kMasked>(sc[u], vsz0[0], vsz1[0], ok[u][0], ok[u][1], p.sigma_v, p.coef_v, st, pb);
+            int2_pv_levels<G>(pg[u], gid, tig, pb, st);
+          } else {
+            uint32_t pb[NGV][NH][2];
+            int2_probs<G, NGV, kMasked>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
+            int2_pv<G, NGV, Gm::kHalfK>(pg[u], gid, tig, pb, st);
+          }
         }
       };
       if (all_full) {
@@ -1214,7 +1387,11 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         mbar_wait_bounded(bar + kk % kStages, (kk / kStages) & 1, kWaitLimitNs);
     }
     __syncwarp();
-    store_hist_state<G, NGV>(st, my_state, gid, tig, p.pv_unscale);
+    if constexpr (kLevels) {
+      store_hist_state_levels<G>(st, my_state, gid, tig, p.pv_unscale, p.coef_v[0]);
+    } else {
+      store_hist_state<G, NGV>(st, my_state, gid, tig, p.pv_unscale);
+    }
   }
 
   __syncthreads();
@@ -1392,22 +1569,23 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
 template <int G>
 int occupancy() {
   int occ = 0;
-  cudaFuncSetAttribute(split_kernel<G, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(split_kernel<G, 1, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        int(Geo<G>::kSmem));
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<G, 1, 1>, Geo<G>::T, Geo<G>::kSmem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<G, 1, 1, false>, Geo<G>::T,
+                                                    Geo<G>::kSmem) !=
       cudaSuccess)
     return 0;
   return occ;
 }
 
-template <int G, int NGK, int NGV>
+template <int G, int NGK, int NGV, bool kLevels = false>
 cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
-  constexpr size_t smem = Geo<G, NGK, NGV>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(split_kernel<G, NGK, NGV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(smem));
+  constexpr size_t smem = Geo<G, NGK, NGV, kLevels>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(split_kernel<G, NGK, NGV, kLevels>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(split_kernel<G, NGK, NGV>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T), smem,
-                    stream, p);
+  return launch_pdl(split_kernel<G, NGK, NGV, kLevels>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T),
+                    smem, stream, p);
 }
 
 template <int G, int NGK>
@@ -1420,6 +1598,7 @@ cudaError_t launch_gk(const DecodeParams& p, cudaStream_t stream) {
 
 template <int G>
 cudaError_t launch_gq(const DecodeParams& p, cudaStream_t stream) {
+  if (p.codebook) return p.ng_k == 1 && p.ng_v == 1 ? launch_g<G, 1, 1, true>(p, stream) : cudaErrorInvalidValue;
   if (p.ng_k == 1) return launch_gk<G, 1>(p, stream);
   if (p.ng_k == 2) return launch_gk<G, 2>(p, stream);
   if (p.ng_k == 4) return launch_gk<G, 4>(p, stream);

@@ -37,10 +37,12 @@ constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
 // 4 l + c is (4 (l & 1) + c) / (8 / NG) for K and V alike, so with c a
 // compile-time constant each code picks between two fixed groups by the
 // lane's parity.  Each group's (min, max) is reduced over the warp and
-// gives its fp16 (scale, zero).
-template <int NG>
+// gives its fp16 (scale, zero).  kLevels: the code is the number of the
+// codebook thresholds `thr` strictly below u = (x - zero) / scale instead of
+// rint(u) clamped to [0, 3].
+template <int NG, bool kLevels>
 __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* red, int which, int head,
-                                            int64_t page, int slot, float tau, int lane) {
+                                            int64_t page, int slot, float tau, int lane, const float* thr) {
   constexpr int kSpan = 8 / NG;
   const bool odd = lane & 1;
   float v[4];
@@ -76,9 +78,16 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
   for (int c = 0; c < 4; ++c) {
     const float sc = odd ? s[(4 + c) / kSpan] : s[c / kSpan];
     const float zc = odd ? z[(4 + c) / kSpan] : z[c / kSpan];
-    float code = 0.f;
-    if (sc > 0.f) code = fminf(fmaxf(rintf(__fdiv_rn(v[c] - zc, sc)), 0.f), 3.f);
-    byte |= uint32_t(code) << (2 * c);
+    uint32_t code = 0u;
+    if (sc > 0.f) {
+      const float u = __fdiv_rn(v[c] - zc, sc);
+      if constexpr (kLevels) {
+        code = uint32_t(u > thr[0]) + uint32_t(u > thr[1]) + uint32_t(u > thr[2]);
+      } else {
+        code = uint32_t(fminf(fmaxf(rintf(u), 0.f), 3.f));
+      }
+    }
+    byte |= code << (2 * c);
   }
   if (page < 0 || page >= p.n_pages) {
     if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
@@ -97,7 +106,7 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
 
 // NGK / NGV: quantisation groups per token-head of K and V (template
 // arguments, so a kernel holds only the finishing code it uses).
-template <int NGK, int NGV>
+template <int NGK, int NGV, bool kLevels>
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   {
     // L2 prefetch of this CTA's rotation (a hint that reads nothing, so it
@@ -197,12 +206,13 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     *reinterpret_cast<float4*>(red + warp * kHeadDim + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
     __syncthreads();
     if (warp == 0 && live[it]) {
+      const float* thr = which ? p.thr_v : p.thr_k;
       if constexpr (NGK == NGV) {
-        finish_item<NGK>(p, red, which, head, page[it], slot[it], tau, lane);
+        finish_item<NGK, kLevels>(p, red, which, head, page[it], slot[it], tau, lane, thr);
       } else if (which) {
-        finish_item<NGV>(p, red, which, head, page[it], slot[it], tau, lane);
+        finish_item<NGV, kLevels>(p, red, which, head, page[it], slot[it], tau, lane, thr);
       } else {
-        finish_item<NGK>(p, red, which, head, page[it], slot[it], tau, lane);
+        finish_item<NGK, kLevels>(p, red, which, head, page[it], slot[it], tau, lane, thr);
       }
     }
     __syncthreads();   // red is reused by the next item
@@ -213,13 +223,13 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
 
 namespace {
 
-template <int NGK, int NGV>
+template <int NGK, int NGV, bool kLevels = false>
 cudaError_t launch_ng(const DemoteParams& p, int64_t chunks, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(demote_kernel<NGK, NGV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kSmem));
+  cudaError_t e = cudaFuncSetAttribute(demote_kernel<NGK, NGV, kLevels>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(demote_kernel<NGK, NGV>, dim3(unsigned(chunks), unsigned(p.n_kv * 2)), dim3(kWarps * 32),
-                    kSmem, stream, p);
+  return launch_pdl(demote_kernel<NGK, NGV, kLevels>, dim3(unsigned(chunks), unsigned(p.n_kv * 2)),
+                    dim3(kWarps * 32), kSmem, stream, p);
 }
 
 template <int NGK>
@@ -236,6 +246,9 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream) {
   const int64_t chunks = (int64_t(p.n) + kItems - 1) / kItems;
   if (chunks == 0) return cudaSuccess;
   if (chunks > 0x7fffffff || int64_t(p.n_kv) * 2 > 65535) return cudaErrorInvalidValue;
+  if (p.codebook) {   // one group per vector (checked by the caller)
+    return p.ng_k == 1 && p.ng_v == 1 ? launch_ng<1, 1, true>(p, chunks, stream) : cudaErrorInvalidValue;
+  }
   if (p.ng_k == 1) return launch_ngk<1>(p, chunks, stream);
   if (p.ng_k == 2) return launch_ngk<2>(p, chunks, stream);
   if (p.ng_k == 4) return launch_ngk<4>(p, chunks, stream);

@@ -106,11 +106,13 @@ struct Waiter {
 // and V alike).  The two halves of a token meet on each group's (min, max)
 // through shared memory; then the group's fp16 scale and zero point, the
 // codes (16 bytes) and, from half 0, the token's NG (scale, zero) pairs are
-// stored.  Returns false when the exchange wait expired.
-template <int NG>
+// stored.  kLevels (codebook): the code is the number of the thresholds thr
+// strictly below u = (x - zero) / scale, u formed with the reciprocal of the
+// scale.  Returns false when the exchange wait expired.
+template <int NG, bool kLevels>
 __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&v)[kHeadDim / 2], float2* xchg,
                                            uint64_t* xfull, Waiter& wt, int k, int hh, int j, int2 m, float tau,
-                                           int which, int head) {
+                                           int which, int head, const float* thr) {
   constexpr int kSpan = 8 / NG;   // consecutive positions (mod 8) per group
   // clipping moves only the extremes: min and max of the clipped values
   // are the clipped min and max, and a value beyond +-tau gets the code
@@ -145,7 +147,7 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
   // low bits (0x4B400000 + code); the bits are accumulated as bits * 4^i
   // (mod 2^32) and the constant part of the sum removed once per word
   __half s16[NG], z16[NG];
-  float a48[NG], nzi3[NG];
+  float a48[NG], nzi3[NG], a16[NG], nzi[NG];
 #pragma unroll
   for (int q = 0; q < NG; ++q) {
     const float lo = fminf(fmaxf(mn[q] * (1.f / kRScale), -tau), tau);
@@ -156,6 +158,8 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
     const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
     a48[q] = inv * (1.f / (3.f * kRScale));
     nzi3[q] = -z * inv * (1.f / 3.f);
+    a16[q] = inv * (1.f / kRScale);
+    nzi[q] = -z * inv;
   }
   const float kMagic = 12582912.f;
   constexpr uint32_t kBitsSum = 0x4B400000u * 0x55555555u;   // 0x4B400000 * sum_i 4^i (mod 2^32)
@@ -166,10 +170,16 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int q = (i & 7) / kSpan;
-      const float t = __saturatef(fmaf(v[16 * u + i], a48[q], nzi3[q]));
-      word += __float_as_uint(fmaf(t, 3.f, kMagic)) << (2 * i);
+      if constexpr (kLevels) {
+        // (scale 0: a16 = nzi = 0, so u = 0 and the code is 0)
+        const float un = fmaf(v[16 * u + i], a16[q], nzi[q]);
+        word |= (uint32_t(un > thr[0]) + uint32_t(un > thr[1]) + uint32_t(un > thr[2])) << (2 * i);
+      } else {
+        const float t = __saturatef(fmaf(v[16 * u + i], a48[q], nzi3[q]));
+        word += __float_as_uint(fmaf(t, 3.f, kMagic)) << (2 * i);
+      }
     }
-    w[u] = word - kBitsSum;
+    w[u] = kLevels ? word : word - kBitsSum;
   }
   uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v) + which * half_bytes(p.ng_k);
   *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -290,9 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
       tc_fence_before();
       mbar_arrive(d_free + buf);
       const int ngw = which ? p.ng_v : p.ng_k;
-      const bool ok = ngw == 4   ? epi_finish<4>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head)
-                      : ngw == 2 ? epi_finish<2>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head)
-                                 : epi_finish<1>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head);
+      const float* thr = which ? p.thr_v : p.thr_k;
+      const bool ok =
+          p.codebook ? epi_finish<1, true>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr)
+          : ngw == 4 ? epi_finish<4, false>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr)
+          : ngw == 2 ? epi_finish<2, false>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr)
+                     : epi_finish<1, false>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr);
       if (!ok) break;
     }
   } else if (warp < kMmaWarp) {

@@ -81,6 +81,10 @@ struct DemoteParams {
   int32_t n, batch, n_kv, max_pages;
   int64_t n_pages;
   int32_t ng_k, ng_v;   // quantisation groups per token-head (1, 2 or 4)
+  // codebook 1: code = number of thresholds (midpoints of adjacent levels)
+  // strictly below u = (x - zero) / scale; K then V
+  int32_t codebook;
+  float thr_k[3], thr_v[3];
   // bulk path with contiguous source rows (no src_index): k_src / v_src as
   // 2-D bf16 tensors (n_kv * 128 columns x src_rows rows) read in boxes of 8
   // columns x 128 rows; use_tma = 0 means the rows are gathered by threads
@@ -120,6 +124,11 @@ struct DecodeParams {
   // dims
   int32_t batch, n_kv, group, sink_cap, recent_cap, max_pages;
   int32_t ng_k, ng_v;   // quantisation groups per token-head (1, 2 or 4)
+  // codebook 1: a code's level is l[c] = l_0 + d1 c + a2 (2 b1) + b (b0 b1)
+  // over its bits c = b0 + 2 b1 (d1 = l_1 - l_0, a2 = (l_2 - 2 l_1 + l_0) / 2,
+  // b = l_3 - l_2 - l_1 + l_0); coef = {l_0, d1, a2, b} for K and for V
+  int32_t codebook;
+  float coef_k[4], coef_v[4];
   int64_t n_pages;
   int32_t max_hist;
   // split plan

@@ -3,12 +3,38 @@
 #include <cmath>
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 #include "oscar.h"
 
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// codebook levels: fp16 values, 0 <= l_0 < l_1 < l_2 < l_3 <= 3
+bool levels_ok(const float* l) {
+  for (int k = 0; k < 4; ++k) {
+    if (!std::isfinite(l[k]) || __half2float(__float2half_rn(l[k])) != l[k]) return false;
+    if (k > 0 && !(l[k] > l[k - 1])) return false;
+  }
+  return l[0] >= 0.f && l[3] <= 3.f;
+}
+
+int groups_of(int32_t g);
+
+// the codebook form of a descriptor needs one quantisation group per vector
+bool codebook_supported(const oscar_layer_desc* d) {
+  return d->codebook == 0 || (groups_of(d->quant_group_k) == 1 && groups_of(d->quant_group_v) == 1);
+}
+
+// level coefficients {l_0, d1, a2, b} of l[c] = l_0 + d1 c + a2 (2 b1) + b b0 b1
+void level_coef(const float* l, float* c) {
+  c[0] = l[0];
+  c[1] = l[1] - l[0];
+  c[2] = (l[2] - 2.f * l[1] + l[0]) * 0.5f;
+  c[3] = l[3] - l[2] - l[1] + l[0];
+}
 
 // groups per token-head for a quantisation group size (0 = 128); 0 if invalid
 int groups_of(int32_t g) {
@@ -34,6 +60,8 @@ oscar_status check_desc(const oscar_layer_desc* d, bool need_cache_segments) {
     return OSCAR_ERR_INVALID_ARG;
   if (!d->pages || !d->page_table || !d->r_k || !d->r_v) return OSCAR_ERR_INVALID_ARG;
   if (!groups_of(d->quant_group_k) || !groups_of(d->quant_group_v)) return OSCAR_ERR_INVALID_ARG;
+  if (d->codebook != 0 && d->codebook != 1) return OSCAR_ERR_INVALID_ARG;
+  if (d->codebook == 1 && (!levels_ok(d->levels_k) || !levels_ok(d->levels_v))) return OSCAR_ERR_INVALID_ARG;
   if (!aligned(d->pages, 128) || !aligned(d->r_k, 16) || !aligned(d->r_v, 16) ||
       !aligned(d->page_table, 4))
     return OSCAR_ERR_ALIGNMENT;
@@ -115,6 +143,14 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
   p.n_pages = desc->n_pages;
   p.ng_k = groups_of(desc->quant_group_k);
   p.ng_v = groups_of(desc->quant_group_v);
+  if (!codebook_supported(desc)) return OSCAR_ERR_UNSUPPORTED;
+  p.codebook = desc->codebook;
+  if (p.codebook) {
+    for (int k = 0; k < 3; ++k) {
+      p.thr_k[k] = (desc->levels_k[k] + desc->levels_k[k + 1]) * 0.5f;   // exact: fp16 inputs
+      p.thr_v[k] = (desc->levels_v[k] + desc->levels_v[k + 1]) * 0.5f;
+    }
+  }
   const bool bulk = n >= oscar::kBulkDemoteMin && !new_k && !new_v;
   const cudaError_t e = bulk ? oscar::launch_demote_bulk(p, static_cast<cudaStream_t>(stream))
                              : oscar::launch_demote(p, static_cast<cudaStream_t>(stream));
@@ -175,13 +211,21 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   p.max_hist = desc->max_hist;
   p.ng_k = groups_of(desc->quant_group_k);
   p.ng_v = groups_of(desc->quant_group_v);
+  if (!codebook_supported(desc)) return OSCAR_ERR_UNSUPPORTED;
+  p.codebook = desc->codebook;
+  if (p.codebook) {
+    level_coef(desc->levels_k, p.coef_k);
+    level_coef(desc->levels_v, p.coef_v);
+  }
   p.n_splits = plan.n_splits;
   p.pages_per_split = plan.pages_per_split;
   // PV operand scale: p <= 2^kRescaleLog2 and s_V <= 2 tau_v / 3 (x2 margin
   // for fp16 rounding), so p s_V sigma_v stays below 2^14 in fp16
   int e = 0;
   std::frexp(std::ldexp(double(desc->tau_v) * (2.0 / 3.0) * 2.0, oscar::kRescaleLog2), &e);
-  const int sig_exp = 14 - e;
+  // (codebook 1: the PV operands are p s_V times level coefficients of
+  // magnitude up to 3, so the scale is 8 times smaller)
+  const int sig_exp = 14 - e - (desc->codebook ? 3 : 0);
   p.sigma_v = std::ldexp(1.0f, sig_exp);
   p.pv_unscale = std::ldexp(1.0f, 24 - sig_exp);
   if (!oscar::encode_rv_map(&p)) return OSCAR_ERR_CUDA;

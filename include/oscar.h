@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define OSCAR_ABI_VERSION 2
+#define OSCAR_ABI_VERSION 3
 
 #define OSCAR_HEAD_DIM 128
 #define OSCAR_PAGE_TOKENS 16
@@ -122,7 +122,20 @@ typedef struct oscar_layer_desc {
   int32_t* dev_status;        /* optional device word for OSCAR_DEV_* bits     */
   int32_t quant_group_k;      /* K quantisation group g_K: 32, 64 or 128 (0 = 128) */
   int32_t quant_group_v;      /* V quantisation group g_V: 32, 64 or 128 (0 = 128) */
+  int32_t codebook;           /* 0: uniform levels 0..3; 1: levels_k / levels_v  */
+  float levels_k[4];          /* codebook 1: K levels l_0 < .. < l_3 (fp16 values) */
+  float levels_v[4];          /* codebook 1: V levels                          */
 } oscar_layer_desc;
+
+/*
+ * Codebook levels (desc->levels_k / levels_v, used when desc->codebook = 1):
+ * four fp16 values 0 <= l_0 < l_1 < l_2 < l_3 <= 3 in the normalised domain
+ * u = (x - zero) / scale, where the group's (scale, zero) are those of the
+ * uniform codec; a value dequantises to zero + scale * l[code].  Levels that
+ * are not fp16 values, not increasing or outside [0, 3] are rejected with
+ * OSCAR_ERR_INVALID_ARG.  Levels 0, 1, 2, 3 give the uniform codes except
+ * at exact ties u = 1.5 (lower level here, round-half-even there).
+ */
 
 /* Bytes of one (page, KV head) block for groups g_k, g_v (0 = 128); 0 for
  * any other value.  Host-only. */
@@ -215,6 +228,27 @@ oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_he
                                   double* tau_out);
 
 /*
+ * oscar_fit_codebook - the Lloyd-Max codebook of one layer's K or V from
+ * calibration rows.  [ZAKER] "OSCAR 把旋转对准 attention", closing part (the
+ * code repo combines the rotation with a Lloyd-Max codebook); the fit is this
+ * library's reading:
+ *
+ *   For every row of x [n][d] (host float64, d = 128) and its head's
+ *   rotation r [d][d]: x~ = clamp(x . r, -tau, tau); scale = fp16((max -
+ *   min) / 3), zero = fp16(min) (round to nearest even); rows with scale 0
+ *   are skipped; u = (x~ - zero) / scale for each channel.  Lloyd's iteration
+ *   over all u from levels {0, 1, 2, 3}: thresholds at the midpoints of
+ *   adjacent levels, each level the mean of the u in its cell (u <= t_1, t_1
+ *   < u <= t_2, ...; an empty cell keeps its level), at most `iters` rounds
+ *   or until no level moves.  levels_out[4] = the levels rounded to fp16 (as
+ *   float).  OSCAR_ERR_INVALID_ARG for bad sizes, tau <= 0, iters < 1, no
+ *   usable row, or fitted levels that are not strictly increasing in fp16.
+ *   Host-only, synchronous.
+ */
+oscar_status oscar_fit_codebook(const double* x, int64_t n, int32_t d, const double* r, double tau,
+                                int32_t iters, float* levels_out);
+
+/*
  * oscar_quantize_append - the fused demotion kernel: rotate, clip, quantise
  * and pack tokens into INT2 history pages.  [ZAKER] pipeline part (the
  * oldest recent token is rotated, clipped, quantised and packed into INT2
@@ -229,7 +263,11 @@ oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_he
  *   clamped to [-tau, tau]; per group of g consecutive channels (g =
  *   quant_group_k for K, quant_group_v for V) scale = fp16((max - min) / 3),
  *   zero = fp16(min) over the group; code = clamp(rint((x~ - zero) / scale),
- *   0, 3) (0 if scale is 0).  The codes and (scale, zero) pairs go to history
+ *   0, 3) (0 if scale is 0).  With desc->codebook == 1 (Lloyd-Max levels;
+ *   one group per vector only, else OSCAR_ERR_UNSUPPORTED) the code is
+ *   instead the number of thresholds (l_(k-1) + l_k) / 2 of levels_k / levels_v
+ *   strictly below u = (x~ - zero) / scale (the nearest level, ties to the
+ *   lower), 0 if scale is 0.  The codes and (scale, zero) pairs go to history
  *   position dst_pos[i] of request dst_req[i] through desc->page_table, in the
  *   pool layout above.  K and V are both written.
  *
@@ -263,7 +301,8 @@ oscar_status oscar_quantize_append(const oscar_layer_desc* desc,
  *   q: [B][H_q][d] bf16 (16-byte aligned); out: [B][H_q][d] float32
  *   (16-byte aligned), normalised softmax(q K^T / sqrt(d)) V over the valid
  *   tokens of all three segments; query head j reads KV head j / g.
- *   History keys/values are c * s + z rotated back with R^T; the kernel
+ *   History keys/values are c * s + z (codebook 0) or l[c] * s + z
+ *   (codebook 1) rotated back with R^T; the kernel
  *   computes this as (q . R_K) against c * s + z and one output rotation
  *   . R_V^T per head, which is the same quantity.  A request with no valid
  *   token gets zeros.

@@ -70,14 +70,28 @@ def demote_heads(x: np.ndarray, r32: np.ndarray, tau: float, group: int = None):
     return codes, s, z
 
 
+def demote_heads_codebook(x: np.ndarray, r32: np.ndarray, tau: float, levels):
+    """Oracle codebook demotion of x [T][n_kv][d]: (codes, scale16 [T][n_kv], zero16 [T][n_kv])."""
+    t, n_kv, d = x.shape
+    codes = np.zeros((t, n_kv, d), np.uint8)
+    s = np.zeros((t, n_kv), np.float16)
+    z = np.zeros((t, n_kv), np.float16)
+    for h in range(n_kv):
+        codes[:, h], s[:, h], z[:, h] = O.quantize_codebook(
+            O.rotate(x[:, h].astype(np.float64), r32[h].astype(np.float64)), tau, levels)
+    return codes, s, z
+
+
 class Scenario:
     """A seeded batch of three-segment caches with oracle expectations."""
 
     def __init__(self, seed: int, ctxs, n_kv: int = 1, g: int = 4, shared_prefix_hist: int = 0,
                  cal=(1024, 512), ring_start=None, identity_pages: bool = False, rot=None,
-                 sink_cap: int = 64, recent_cap: int = 256, groups=(128, 128)):
+                 sink_cap: int = 64, recent_cap: int = 256, groups=(128, 128), levels=None):
         self.seed, self.ctxs, self.n_kv, self.g = seed, [int(c) for c in ctxs], n_kv, g
         self.gk, self.gv = int(groups[0]), int(groups[1])
+        # levels: (levels_k, levels_v) of a Lloyd-Max codebook (fp16), or None
+        self.levels = None if levels is None else tuple(np.asarray(l, np.float16) for l in levels)
         grouped = (self.gk, self.gv) != (D, D)
         ngk, ngv = D // self.gk, D // self.gv
         self.B = len(self.ctxs)
@@ -122,9 +136,15 @@ class Scenario:
             sl, hl = int(self.sink_len[b]), int(self.hist_len[b])
             xk = self.k_tok[b][sl:sl + hl]
             xv = self.v_tok[b][sl:sl + hl]
-            ck, sk, zk = demote_heads(xk, self.rk32, self.tau_k, self.gk if grouped else None)
-            cv, sv, zv = demote_heads(xv, self.rv32, self.tau_v, self.gv if grouped else None)
+            if self.levels is not None:
+                ck, sk, zk = demote_heads_codebook(xk, self.rk32, self.tau_k, self.levels[0])
+                cv, sv, zv = demote_heads_codebook(xv, self.rv32, self.tau_v, self.levels[1])
+            else:
+                ck, sk, zk = demote_heads(xk, self.rk32, self.tau_k, self.gk if grouped else None)
+                cv, sv, zv = demote_heads(xv, self.rv32, self.tau_v, self.gv if grouped else None)
             self.hist.append(dict(codes_k=ck, scale_k=sk, zero_k=zk, codes_v=cv, scale_v=sv, zero_v=zv))
+            if self.levels is not None:
+                self.hist[-1]["levels_k"], self.hist[-1]["levels_v"] = self.levels
             if hl and grouped:
                 O.store_history_groups(self.pool, self.table, n_kv, b, 0, ck, sk, zk, 0, ngk, ngv)
                 O.store_history_groups(self.pool, self.table, n_kv, b, 0, cv, sv, zv, 1, ngk, ngv)
@@ -189,7 +209,7 @@ def rotation_error_bound(x: np.ndarray, r32: np.ndarray, terms_per_channel: int 
 
 
 def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, ref_s, ref_z,
-                pre_s: np.ndarray, pre_z: np.ndarray, rot_err=None):
+                pre_s: np.ndarray, pre_z: np.ndarray, rot_err=None, levels=None):
     """The demotion comparison rule.
 
     * scale/zero: fp16 bit-equal, or else the GPU's fp16 value is a rounding
@@ -201,7 +221,9 @@ def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, r
     * codes: recomputed from the GPU's own scale/zero and the oracle's float64
       rotated value; a GPU code may differ from that only when
       u = (x - z) / s lies within 1e-5 * b of a rounding boundary b in
-      {0.5, 1.5, 2.5}; end to end at most 1e-4 of the codes differ from the
+      {0.5, 1.5, 2.5} (with codebook `levels`: the midpoints of adjacent
+      levels, and codes are nearest-level indices); end to end at most 1e-4
+      of the codes (or 4 codes, in samples under 40,000) differ from the
       oracle's own.
     Returns a dict of counts; raises AssertionError on a violation.
     """
@@ -238,9 +260,15 @@ def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, r
     n_z = fp16_ok(gpu_z, ref_z, pre_z, rot_err)
     s = gpu_s.astype(np.float64)[..., None]
     z = gpu_z.astype(np.float64)[..., None]
+    bounds = (0.5, 1.5, 2.5)
     with np.errstate(divide="ignore", invalid="ignore"):
         u = (x_rot_clipped - z) / s
-        recomputed = np.where(s > 0, np.clip(np.rint(u), 0, 3), 0)
+        if levels is None:
+            recomputed = np.where(s > 0, np.clip(np.rint(u), 0, 3), 0)
+        else:
+            lv = np.asarray(levels, dtype=np.float16).astype(np.float64)
+            bounds = tuple((lv[:-1] + lv[1:]) / 2)
+            recomputed = np.where(s > 0, (u > bounds[0]).astype(int) + (u > bounds[1]) + (u > bounds[2]), 0)
     diff = gpu_codes != recomputed
     if diff.any():
         ud = u[diff]
@@ -248,11 +276,14 @@ def code_parity(x_rot_clipped: np.ndarray, gpu_codes, gpu_s, gpu_z, ref_codes, r
         with np.errstate(divide="ignore", invalid="ignore"):   # s = 0 gives code 0 on both sides
             slack = 0.0 if rot_err is None else np.broadcast_to((rot_err[..., None] / s), u.shape)[diff]
         near = np.zeros(ud.shape, bool)
-        for bnd in (0.5, 1.5, 2.5):
+        for bnd in bounds:
             near |= np.abs(ud - bnd) <= np.maximum(1e-5 * bnd, slack)
         assert near.all(), "%d codes differ away from a rounding boundary" % int((~near).sum())
-    e2e = float(np.mean(gpu_codes != ref_codes))
-    assert e2e <= 1e-4, "code mismatch fraction %g > 1e-4" % e2e
+    n_diff = int(np.sum(gpu_codes != ref_codes))
+    e2e = n_diff / max(gpu_codes.size, 1)
+    # (every differing code already passed the boundary rule above; this caps
+    # their number: 1e-4 of the codes, or 4 codes in a small sample)
+    assert n_diff <= max(1e-4 * gpu_codes.size, 4), "code mismatch fraction %g (%d codes)" % (e2e, n_diff)
     return dict(scale_diff=n_s, zero_diff=n_z, boundary_codes=int(diff.sum()), e2e_fraction=e2e)
 
 
@@ -271,7 +302,9 @@ def to_device(sc: Scenario):
     cache = LayerCache(sc.B, sc.h_q, sc.n_kv, sc.table.shape[1], sc.n_pages,
                        torch.from_numpy(sc.rk32), torch.from_numpy(sc.rv32), sc.tau_k, sc.tau_v,
                        device=dev, sink_cap=sc.sink_cap, recent_cap=sc.recent_cap,
-                       quant_group_k=getattr(sc, "gk", 128), quant_group_v=getattr(sc, "gv", 128))
+                       quant_group_k=getattr(sc, "gk", 128), quant_group_v=getattr(sc, "gv", 128),
+                       levels_k=None if getattr(sc, "levels", None) is None else sc.levels[0],
+                       levels_v=None if getattr(sc, "levels", None) is None else sc.levels[1])
     cache.pages.copy_(torch.from_numpy(sc.pool))
     cache.page_table.copy_(torch.from_numpy(sc.table))
     cache.hist_len.copy_(torch.from_numpy(sc.hist_len))

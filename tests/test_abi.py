@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol(built_lib):
 
 def test_version_and_status_strings(built_lib):
     from bit_rotated_kv_split_gb300 import binding as B
-    assert B.oscar_abi_version() == 2
+    assert B.oscar_abi_version() == 3
     assert B.oscar_status_string(0) == "ok"
     assert B.oscar_status_string(3).startswith("workspace")
 
@@ -206,3 +206,48 @@ def test_append_rejects_bad_group_before_launch(built_lib):
     got = B.lib.oscar_quantize_append(ctypes.byref(_desc(quant_group_v=48)), fake, fake, 4, 128, None,
                                       fake, fake, 4, None, None, None)
     assert got == 1
+
+
+def test_fit_codebook_matches_oracle(built_lib):
+    # the library's Lloyd-Max fit on seeded calibration rows equals the
+    # oracle's (fp16 levels; the float64 sums may differ in order only)
+    from bit_rotated_kv_split_gb300 import binding as B
+    outl = synth.outlier_channels(5, 0, 1)
+    cal = synth.calibration_set(5, 0, 0, outl[0], n_q=64, n_k=1500)
+    r = O.rotation_from_covariance(O.query_covariance(cal["k"]))
+    tau = O.clip_threshold(cal["k"] @ r)
+    want = O.fit_codebook(cal["k"], r, tau)
+    got = B.oscar_fit_codebook(cal["k"], r, tau)
+    ulp = np.abs(got.astype(np.float16).view(np.uint16).astype(int) - want.view(np.uint16).astype(int))
+    assert ulp.max() <= 1, (got, want)
+    assert np.all(np.diff(got) > 0) and got[0] > 0 and got[3] < 3
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(codebook=2), 1),
+    (dict(codebook=1, levels_k=(0.5, 0.25, 2.0, 2.5), levels_v=(0.5, 1.0, 2.0, 2.5)), 1),   # not increasing
+    (dict(codebook=1, levels_k=(0.1, 1.0, 2.0, 2.5), levels_v=(0.5, 1.0, 2.0, 2.5)), 1),    # 0.1 is no fp16 value
+    (dict(codebook=1, levels_k=(0.5, 1.0, 2.0, 3.5), levels_v=(0.5, 1.0, 2.0, 2.5)), 1),    # above 3
+])
+def test_decode_rejects_bad_codebook(built_lib, over, status):
+    from bit_rotated_kv_split_gb300 import binding as B
+    d = _desc()
+    for k, v in over.items():
+        if k.startswith("levels"):
+            for i in range(4):
+                getattr(d, k)[i] = v[i]
+        else:
+            setattr(d, k, v)
+    size = ctypes.c_size_t(0)
+    assert B.lib.oscar_decode_attention(ctypes.byref(d), None, None, None, ctypes.byref(size), None) == status
+
+
+def test_codebook_with_groups_is_unsupported(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    d = _desc(codebook=1, quant_group_k=32)
+    for i, v in enumerate((0.25, 1.0, 2.0, 2.75)):
+        d.levels_k[i] = v
+        d.levels_v[i] = v
+    fake = 1 << 20
+    got = B.lib.oscar_quantize_append(ctypes.byref(d), fake, fake, 4, 128, None, fake, fake, 4, None, None, None)
+    assert got == 6

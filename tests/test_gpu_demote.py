@@ -29,7 +29,7 @@ def _pre_rounding(x_rot_clipped):
 
 
 def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None, first_row=None,
-         groups=None):
+         groups=None, levels=None):
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
@@ -54,7 +54,9 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
     table, n_pages = synth.page_table(seed, [hist], n_extra_pages=0)
     gk, gv = groups if groups is not None else (128, 128)
     cache = LayerCache(1, n_kv * 4, n_kv, table.shape[1], n_pages, torch.from_numpy(rk32),
-                       torch.from_numpy(rv32), tau_k, tau_v, quant_group_k=gk, quant_group_v=gv)
+                       torch.from_numpy(rv32), tau_k, tau_v, quant_group_k=gk, quant_group_v=gv,
+                       levels_k=None if levels is None else levels[0],
+                       levels_v=None if levels is None else levels[1])
     cache.page_table.copy_(torch.from_numpy(table))
     dev = torch.device("cuda")
     k_src = torch.from_numpy(xk).to(torch.bfloat16).to(dev).contiguous()
@@ -86,9 +88,13 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         if groups is None:
             gc, gs, gz = O.load_history_bulk(pool, table, n_kv, 0, hist, which)
             gc, gs, gz = gc[positions], gs[positions], gz[positions]
-            rc, rs, rz = H.demote_heads(xs, r32, tau)
+            lv = None if levels is None else levels[which]
+            if lv is None:
+                rc, rs, rz = H.demote_heads(xs, r32, tau)
+            else:
+                rc, rs, rz = H.demote_heads_codebook(xs, r32, tau, lv)
             pre_s, pre_z = _pre_rounding(xr)
-            res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z, rot_err=rot_err)
+            res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z, rot_err=rot_err, levels=lv)
             continue
         # groups: each group of gsz channels is compared as its own vector
         ng = 128 // gsz
