@@ -602,14 +602,16 @@ def run_gpu(args):
 
     sh = stream.cuda_stream     # the stream handle, passed to the calls
 
+    in_bytes = inp.numel() * inp.element_size()
+    rk16 = [L.recent_k.view(torch.uint16) for L in layers]
+    rv16 = [L.recent_v.view(torch.uint16) for L in layers]
+    nk16, nv16 = nk_e.view(torch.uint16), nv_e.view(torch.uint16)
+
     def step_e2e(i):
-        L = layers[i]
-        inp.copy_(inp_host, non_blocking=True)
-        B.oscar_quantize_append(descs[i], L.recent_k.view(torch.uint16), L.recent_v.view(torch.uint16),
-                                bsz * w["recent"], n_kv * 128, src, dst_req, dst_pos, bsz,
-                                nk_e.view(torch.uint16), nv_e.view(torch.uint16), stream=sh)
-        B.oscar_decode_attention(descs[i], q_e, out, ws, ws_bytes, stream=sh)
-        out_host.copy_(out, non_blocking=True)
+        # one library call: H2D copy of the step's inputs, demotion, decode,
+        # D2H copy of the output
+        B.oscar_decode_step(descs[i], inp_host, inp, in_bytes, rk16[i], rv16[i], bsz * w["recent"], n_kv * 128,
+                            src, dst_req, dst_pos, bsz, nk16, nv16, q_e, out, ws, ws_bytes, out_host, stream=sh)
 
     ke = min(K, 500)
     with torch.cuda.stream(stream):

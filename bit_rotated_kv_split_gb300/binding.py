@@ -63,6 +63,8 @@ def _load():
         "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
                                              ctypes.POINTER(c_size_t), P]),
         "oscar_decode_attention_static": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P]),
+        "oscar_decode_step": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_size_t, P, P, c_int64, c_int64, P, P,
+                                        P, c_int32, P, P, P, P, P, c_size_t, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -203,6 +205,16 @@ def oscar_decode_attention(desc: LayerDesc, q, out, workspace, workspace_bytes: 
                     else workspace_bytes)
     _check("oscar_decode_attention", lib.oscar_decode_attention(
         ctypes.byref(desc), _ptr(q), _ptr(out), _ptr(workspace), ctypes.byref(size), _stream(stream)))
+
+
+def oscar_decode_step(desc: LayerDesc, host_in, dev_in, in_bytes: int, k_src, v_src, src_rows: int,
+                      row_stride: int, src_index, dst_req, dst_pos, n: int, new_k, new_v, q, out, workspace,
+                      workspace_bytes: int, host_out=None, stream=None) -> None:
+    """One decode step: H2D copy of the staged inputs, demotion, decode, D2H copy of the output."""
+    _check("oscar_decode_step", lib.oscar_decode_step(
+        ctypes.byref(desc), _ptr(host_in), _ptr(dev_in), int(in_bytes), _ptr(k_src), _ptr(v_src), int(src_rows),
+        int(row_stride), _ptr(src_index), _ptr(dst_req), _ptr(dst_pos), int(n), _ptr(new_k), _ptr(new_v),
+        _ptr(q), _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(host_out), _stream(stream)))
 
 
 def oscar_decode_attention_static(desc: LayerDesc, q, out, stream=None) -> None:

@@ -1581,8 +1581,7 @@ int occupancy() {
 template <int G, int NGK, int NGV, bool kLevels = false>
 cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
   constexpr size_t smem = Geo<G, NGK, NGV, kLevels>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(split_kernel<G, NGK, NGV, kLevels>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = set_smem_limit<split_kernel<G, NGK, NGV, kLevels>>(int(smem));
   if (e != cudaSuccess) return e;
   return launch_pdl(split_kernel<G, NGK, NGV, kLevels>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T),
                     smem, stream, p);

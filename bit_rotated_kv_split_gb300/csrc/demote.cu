@@ -225,8 +225,7 @@ namespace {
 
 template <int NGK, int NGV, bool kLevels = false>
 cudaError_t launch_ng(const DemoteParams& p, int64_t chunks, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(demote_kernel<NGK, NGV, kLevels>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+  cudaError_t e = set_smem_limit<demote_kernel<NGK, NGV, kLevels>>(int(kSmem));
   if (e != cudaSuccess) return e;
   return launch_pdl(demote_kernel<NGK, NGV, kLevels>, dim3(unsigned(chunks), unsigned(p.n_kv * 2)),
                     dim3(kWarps * 32), kSmem, stream, p);

@@ -496,7 +496,7 @@ cudaError_t launch_demote_bulk(const DemoteParams& p_in, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bulk_demote_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+  e = set_smem_limit<bulk_demote_kernel>(int(kSmem));
   if (e != cudaSuccess) return e;
   // one CTA per SM shared out over the (KV head, K|V) pairs
   const int64_t per_pair = int64_t(sms) / (2 * p.n_kv);

@@ -61,6 +61,20 @@ inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The kernel's dynamic shared-memory limit, set through the runtime once per
+// kernel and device (a call per launch would cost host time on every step).
+template <auto Kernel>
+inline cudaError_t set_smem_limit(int bytes) {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  return e;
+}
+
 // ---------------------------------------------------------------- demotion
 struct DemoteParams {
   uint8_t* pages;
@@ -154,6 +168,11 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
                 DecodePlan* plan, cudaError_t* err);
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- staging
+// Copies `bytes` from src to dst by a kernel in the launch chain; either side
+// may be pinned host memory that the device addresses directly.
+cudaError_t launch_stage(const void* src, void* dst, size_t bytes, cudaStream_t stream);
 
 // ---------------------------------------------------------------- calibration
 // C = X^T X / n over n bf16 rows of 128 values (ld elements apart), split

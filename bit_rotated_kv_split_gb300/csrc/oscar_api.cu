@@ -23,6 +23,16 @@ bool levels_ok(const float* l) {
 
 int groups_of(int32_t g);
 
+// pinned host memory that the current device addresses at the same pointer
+bool device_addressable_host(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();   // clear the error of an unregistered pointer
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 // the codebook form of a descriptor needs one quantisation group per vector
 bool codebook_supported(const oscar_layer_desc* d) {
   return d->codebook == 0 || (groups_of(d->quant_group_k) == 1 && groups_of(d->quant_group_v) == 1);
@@ -100,17 +110,22 @@ extern "C" int64_t oscar_block_bytes(int32_t quant_group_k, int32_t quant_group_
   return gk && gv ? int64_t(oscar::block_bytes(gk, gv)) : 0;
 }
 
-extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint16_t* k_src,
-                                              uint16_t* v_src, int64_t src_rows,
-                                              int64_t row_stride,
-                                              const int32_t* src_index, const int32_t* dst_req,
-                                              const int32_t* dst_pos, int32_t n,
-                                              const uint16_t* new_k, const uint16_t* new_v,
-                                              void* stream) {
+namespace {
+
+// Validates an append and fills its kernel parameters (no launch).  *empty:
+// n == 0, nothing to launch.
+oscar_status prepare_append(const oscar_layer_desc* desc, uint16_t* k_src, uint16_t* v_src, int64_t src_rows,
+                            int64_t row_stride, const int32_t* src_index, const int32_t* dst_req,
+                            const int32_t* dst_pos, int32_t n, const uint16_t* new_k, const uint16_t* new_v,
+                            oscar::DemoteParams* out, bool* empty) {
+  *empty = false;
   oscar_status st = check_desc(desc, false);
   if (st != OSCAR_OK) return st;
   if (n < 0) return OSCAR_ERR_INVALID_ARG;
-  if (n == 0) return OSCAR_OK;
+  if (n == 0) {
+    *empty = true;
+    return OSCAR_OK;
+  }
   if (!k_src || !v_src || !dst_req || !dst_pos || src_rows < 1) return OSCAR_ERR_INVALID_ARG;
   if (!src_index && src_rows < n) return OSCAR_ERR_INVALID_ARG;
   if ((new_k == nullptr) != (new_v == nullptr)) return OSCAR_ERR_INVALID_ARG;
@@ -151,15 +166,20 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
       p.thr_v[k] = (desc->levels_v[k] + desc->levels_v[k + 1]) * 0.5f;
     }
   }
-  const bool bulk = n >= oscar::kBulkDemoteMin && !new_k && !new_v;
-  const cudaError_t e = bulk ? oscar::launch_demote_bulk(p, static_cast<cudaStream_t>(stream))
-                             : oscar::launch_demote(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  *out = p;
+  return OSCAR_OK;
 }
 
-extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
-                                               float* out, void* workspace,
-                                               size_t* workspace_bytes, void* stream) {
+cudaError_t launch_append(const oscar::DemoteParams& p, cudaStream_t stream) {
+  const bool bulk = p.n >= oscar::kBulkDemoteMin && !p.new_k && !p.new_v;
+  return bulk ? oscar::launch_demote_bulk(p, stream) : oscar::launch_demote(p, stream);
+}
+
+// Validates a decode call and fills its kernel parameters (no launch).
+// *size_only: workspace was NULL and *workspace_bytes now holds the size.
+oscar_status prepare_decode(const oscar_layer_desc* desc, const uint16_t* q, float* out, void* workspace,
+                            size_t* workspace_bytes, oscar::DecodeParams* pout, bool* size_only) {
+  *size_only = false;
   oscar_status st = check_desc(desc, true);
   if (st != OSCAR_OK) return st;
   const int group = desc->n_q_heads / desc->n_kv_heads;
@@ -172,6 +192,7 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
     return OSCAR_ERR_CUDA;
   if (!workspace) {
     *workspace_bytes = plan.total_bytes;
+    *size_only = true;
     return OSCAR_OK;
   }
   if (*workspace_bytes < plan.total_bytes) return OSCAR_ERR_WORKSPACE;
@@ -229,8 +250,68 @@ extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, con
   p.sigma_v = std::ldexp(1.0f, sig_exp);
   p.pv_unscale = std::ldexp(1.0f, 24 - sig_exp);
   if (!oscar::encode_rv_map(&p)) return OSCAR_ERR_CUDA;
-  err = oscar::launch_decode(p, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  *pout = p;
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint16_t* k_src,
+                                              uint16_t* v_src, int64_t src_rows,
+                                              int64_t row_stride,
+                                              const int32_t* src_index, const int32_t* dst_req,
+                                              const int32_t* dst_pos, int32_t n,
+                                              const uint16_t* new_k, const uint16_t* new_v,
+                                              void* stream) {
+  oscar::DemoteParams p{};
+  bool empty = false;
+  const oscar_status st = prepare_append(desc, k_src, v_src, src_rows, row_stride, src_index, dst_req, dst_pos, n,
+                                         new_k, new_v, &p, &empty);
+  if (st != OSCAR_OK || empty) return st;
+  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
+                                               float* out, void* workspace,
+                                               size_t* workspace_bytes, void* stream) {
+  oscar::DecodeParams p{};
+  bool size_only = false;
+  const oscar_status st = prepare_decode(desc, q, out, workspace, workspace_bytes, &p, &size_only);
+  if (st != OSCAR_OK || size_only) return st;
+  return oscar::launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
+                                          size_t in_bytes, uint16_t* k_src, uint16_t* v_src, int64_t src_rows,
+                                          int64_t row_stride, const int32_t* src_index, const int32_t* dst_req,
+                                          const int32_t* dst_pos, int32_t n, const uint16_t* new_k,
+                                          const uint16_t* new_v, const uint16_t* q, float* out, void* workspace,
+                                          size_t workspace_bytes, float* host_out, void* stream) {
+  if ((in_bytes > 0) != (host_in != nullptr && dev_in != nullptr)) return OSCAR_ERR_INVALID_ARG;
+  if (!workspace) return OSCAR_ERR_WORKSPACE;
+  if ((in_bytes > 0 && !device_addressable_host(host_in)) || (host_out && !device_addressable_host(host_out)))
+    return OSCAR_ERR_INVALID_ARG;
+  oscar::DemoteParams pa{};
+  bool empty = false;
+  oscar_status st = prepare_append(desc, k_src, v_src, src_rows, row_stride, src_index, dst_req, dst_pos, n, new_k,
+                                   new_v, &pa, &empty);
+  if (st != OSCAR_OK) return st;
+  oscar::DecodeParams pd{};
+  bool size_only = false;
+  size_t ws_bytes = workspace_bytes;
+  st = prepare_decode(desc, q, out, workspace, &ws_bytes, &pd, &size_only);
+  if (st != OSCAR_OK) return st;
+  // the copies run as kernels in the launch chain, reading and writing the
+  // pinned host buffers directly
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in_bytes > 0 && oscar::launch_stage(host_in, dev_in, in_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (!empty && launch_append(pa, s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (oscar::launch_decode(pd, s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (host_out) {
+    const size_t out_bytes = size_t(desc->batch) * desc->n_q_heads * OSCAR_HEAD_DIM * sizeof(float);
+    if (oscar::launch_stage(out, host_out, out_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  }
+  return OSCAR_OK;
 }
 
 // [GIST] 2.1 / 2.2 A: C_Q and C_S as one contraction over calibration rows.

@@ -320,6 +320,37 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
                                     void* stream);
 
 /*
+ * oscar_decode_step - one decode step of a layer in one call, for a serving
+ * loop that holds the step's inputs in host memory: [ZAKER] pipeline part
+ * (demote the oldest recent token, write the new one, attend).
+ *
+ *   On `stream`, in this order: (1) if in_bytes > 0, copy in_bytes from
+ *   host_in (pinned host memory) to dev_in (device), the staging buffer
+ *   that q, new_k / new_v and the index arrays may point into; (2)
+ *   oscar_quantize_append with the given arguments (nothing when n = 0);
+ *   (3) oscar_decode_attention(desc, q, out, workspace, workspace_bytes);
+ *   (4) if host_out is not NULL, copy out ([B][H_q][d] float32) to host_out
+ *   (pinned host memory).  The results are those of the separate calls.
+ *   The two copies are kernels of the same launch chain: the GPU reads
+ *   host_in and writes host_out directly (GB300's coherent CPU-GPU link), so
+ *   both must be pinned host memory the device addresses at the same pointer
+ *   (cudaHostAlloc / cudaMallocHost on a system with unified addressing);
+ *   otherwise OSCAR_ERR_INVALID_ARG.  host_in is read anew on every call.
+ *   Every argument of (2) and (3) is validated before (1) is issued: a
+ *   rejected call copies and launches nothing.  in_bytes > 0 requires
+ *   host_in and dev_in (OSCAR_ERR_INVALID_ARG otherwise); workspace must be
+ *   given (OSCAR_ERR_WORKSPACE).  Async: host_out holds the output once the
+ *   stream reaches that point; host_in must not change before then.
+ */
+oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
+                               size_t in_bytes, uint16_t* k_src, uint16_t* v_src, int64_t src_rows,
+                               int64_t row_stride, const int32_t* src_index, const int32_t* dst_req,
+                               const int32_t* dst_pos, int32_t n, const uint16_t* new_k,
+                               const uint16_t* new_v, const uint16_t* q, float* out,
+                               void* workspace, size_t workspace_bytes, float* host_out,
+                               void* stream);
+
+/*
  * oscar_decode_attention_static - oscar_decode_attention for callers that
  * cannot allocate device memory.  The paper has no counterpart: this is a
  * deployment convenience of this library.

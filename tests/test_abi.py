@@ -251,3 +251,18 @@ def test_codebook_with_groups_is_unsupported(built_lib):
     fake = 1 << 20
     got = B.lib.oscar_quantize_append(ctypes.byref(d), fake, fake, 4, 128, None, fake, fake, 4, None, None, None)
     assert got == 6
+
+
+def test_decode_step_rejects_before_any_copy(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    fake = 1 << 20
+    args = lambda desc, host_in, dev_in, nbytes, ws: (  # noqa: E731
+        ctypes.byref(desc), host_in, dev_in, nbytes, fake, fake, 4, 128, None, fake, fake, 1, None, None,
+        fake, fake, ws, 1 << 20, None, None)
+    # staged bytes without both buffers
+    assert B.lib.oscar_decode_step(*args(_desc(), None, fake, 64, fake)) == 1
+    assert B.lib.oscar_decode_step(*args(_desc(), fake, None, 64, fake)) == 1
+    # no workspace
+    assert B.lib.oscar_decode_step(*args(_desc(), None, None, 0, None)) == 3
+    # a bad descriptor
+    assert B.lib.oscar_decode_step(*args(_desc(head_dim=64), None, None, 0, fake)) == 1

@@ -196,3 +196,45 @@ def test_append_then_decode_matches_oracle_steps():
                                         sc.rk32.astype(np.float64), sc.rv32.astype(np.float64))
         err = H.relative_error(out, ref)
         assert err.max() <= 2e-3, (step, err.max())
+
+
+def test_decode_step_equals_separate_calls():
+    """oscar_decode_step (staged H2D copy, demotion, decode, D2H copy) gives the
+    output of oscar_quantize_append + oscar_decode_attention bit for bit."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    sc = H.Scenario(2010, [1500, 900], n_kv=2, g=4)
+    outs = []
+    for fused in (False, True):
+        cache, q = H.to_device(sc)
+        dev = q.device
+        newk = synth.activations(sc.seed, (8, 0), sc.B, sc.outl)
+        newv = synth.activations(sc.seed, (8, 1), sc.B, sc.outl)
+        host = torch.cat([q.cpu().flatten(), torch.from_numpy(newk).to(torch.bfloat16).flatten(),
+                          torch.from_numpy(newv).to(torch.bfloat16).flatten()]).pin_memory()
+        stage = torch.empty(host.numel(), dtype=torch.bfloat16, device=dev)
+        nq, nk = q.numel(), newk.size
+        q_s, nk_s, nv_s = stage[:nq].view_as(q), stage[nq:nq + nk], stage[nq + nk:]
+        src = torch.tensor([b * 256 + int(sc.recent_start[b]) for b in range(sc.B)], dtype=torch.int32, device=dev)
+        dr = torch.arange(sc.B, dtype=torch.int32, device=dev)
+        dp = torch.from_numpy(sc.hist_len.astype(np.int32)).to(dev)
+        desc = cache.desc(int(sc.hist_len.max()) + 1)
+        nbytes = B.oscar_decode_workspace_bytes(desc)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        host_out = torch.zeros(q.shape, dtype=torch.float32).pin_memory()
+        args = (cache.recent_k.view(torch.uint16), cache.recent_v.view(torch.uint16), sc.B * 256, sc.n_kv * 128,
+                src, dr, dp, sc.B, nk_s.view(torch.uint16), nv_s.view(torch.uint16))
+        if fused:
+            B.oscar_decode_step(desc, host, stage, host.numel() * 2, *args, q_s, out, ws, nbytes, host_out)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(host_out.numpy(), out.cpu().numpy())
+        else:
+            stage.copy_(host)
+            B.oscar_quantize_append(desc, *args)
+            B.oscar_decode_attention(desc, q_s, out, ws, nbytes)
+            torch.cuda.synchronize()
+        assert int(cache.dev_status.item()) == 0
+        outs.append((out.cpu().numpy(), cache.pages.cpu().numpy(), cache.recent_k.float().cpu().numpy()))
+    for a, b in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(a, b)
