@@ -356,6 +356,16 @@ def _roofline_peak():
         return 6800.0, "fallback"
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over the ranks of the default
+    process group (gloo with CPU tensors, NCCL with CUDA tensors)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu().tolist()]
+
+
 def rotations_from_library(B, kind="oscar"):
     """Per-head R_K, R_V and per-layer taus, built by the library's host routines
     (kind "canalized32": the OScaR block-diagonal rotation for K and V)."""
@@ -585,15 +595,12 @@ def run_gpu(args):
     decode_ms = ev[2].elapsed_time(ev[3]) / (reps * n_copies)
     demote_ms = ev[3].elapsed_time(ev[4]) / (reps * n_copies)
     t_step = total_ms / K / 1e3
-    if world > 1:
-        tt = torch.tensor([t_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
     status = max(int(L.dev_status.item()) for L in layers)
 
-    # end to end through the public API with pinned host buffers: each step
-    # copies its inputs (q, new K, new V: one pinned staging buffer, one
-    # copy) to the device, demotes, decodes and reads the output back
+    # end to end through the public API with pinned host buffers: one
+    # oscar_decode_step per step brings its inputs (q, new K, new V: one
+    # pinned staging buffer) to the device, demotes, decodes and writes the
+    # output back to pinned host memory
     nq, nk = q.numel(), new_k.numel()
     inp = torch.empty(nq + 2 * nk, dtype=torch.bfloat16, device=dev)
     q_e, nk_e, nv_e = inp[:nq].view_as(q), inp[nq:nq + nk].view_as(new_k), inp[nq + nk:].view_as(new_v)
@@ -626,6 +633,9 @@ def run_gpu(args):
         e1.record(stream)
         torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3 / ke
+    if world > 1:
+        # the slowest rank sets the whole job's time
+        t_step, e2e_s = max_over_ranks([t_step, e2e_s], dev)
 
     if rank == 0:
         peak, peak_kind = _roofline_peak()
