@@ -238,3 +238,31 @@ def test_decode_step_equals_separate_calls():
         outs.append((out.cpu().numpy(), cache.pages.cpu().numpy(), cache.recent_k.float().cpu().numpy()))
     for a, b in zip(outs[0], outs[1]):
         np.testing.assert_array_equal(a, b)
+
+
+def test_decode_step_stages_odd_sizes_and_offsets():
+    """The staging copy of oscar_decode_step moves an odd number of bytes
+    between addresses off the 16-byte grid exactly (byte path) and leaves the
+    bytes around them alone; the decode result is unchanged (n = 0: no
+    demotion)."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    sc = H.Scenario(2011, [1200], n_kv=1, g=4)
+    cache, q = H.to_device(sc)
+    ref, _ = H.run_decode(cache, q)
+    g = synth.generator(2011, 9)
+    host = torch.from_numpy(g.integers(0, 256, size=1003).astype(np.uint8)).pin_memory()
+    dev = torch.zeros(1024, dtype=torch.uint8, device=q.device)
+    desc = cache.desc()
+    nbytes = B.oscar_decode_workspace_bytes(desc)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    for off_h, off_d, n in ((1, 3, 997), (16, 32, 960), (0, 0, 5)):
+        dev.zero_()
+        B.oscar_decode_step(desc, host.data_ptr() + off_h, dev.data_ptr() + off_d, n, None, None, 1, 128, None,
+                            None, None, 0, None, None, q, out, ws, nbytes, None)
+        torch.cuda.synchronize()
+        d = dev.cpu().numpy()
+        np.testing.assert_array_equal(d[off_d:off_d + n], host.numpy()[off_h:off_h + n])
+        assert not d[:off_d].any() and not d[off_d + n:].any()
+        np.testing.assert_array_equal(out.cpu().numpy(), ref.astype(np.float32))
