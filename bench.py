@@ -285,12 +285,17 @@ class Clocks:
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
+        import tempfile
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        # the raw samples go to a temporary file (OSCAR_CLOCKS_CSV keeps them
+        # at a chosen path); the JSON line carries their summary
+        self.path = os.environ.get("OSCAR_CLOCKS_CSV") or os.path.join(
+            tempfile.gettempdir(), "oscar_clocks_%d.csv" % os.getpid())
 
     def start(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        if os.path.dirname(self.path):
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
