@@ -329,6 +329,15 @@ class Clocks:
                 "samples": len(rows)}
 
 
+def _code_only(src):
+    """C++ source with comments removed and whitespace runs collapsed (string
+    and character literals kept), so that a comment edit leaves it unchanged."""
+    import re
+    tok = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|//[^\n]*|/\*.*?\*/', re.S)
+    out = tok.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", src)
+    return " ".join(out.split())
+
+
 def _profiled_traffic():
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel sources (else None)."""
@@ -343,8 +352,8 @@ def _profiled_traffic():
         return None
     h = hashlib.sha256()
     for f in ("decode.cu", "ptx.cuh", "kernels.h"):
-        with open(os.path.join(ROOT, "bit_rotated_kv_split_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_rotated_kv_split_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
     if not m_hash or not m_bytes or m_hash.group(1) != h.hexdigest():

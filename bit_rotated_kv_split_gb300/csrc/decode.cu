@@ -44,6 +44,18 @@
 //   subnormal c * 4^k * 2^-24 by a single AND (no conversion); the 4^k and
 //   2^-24 factors are folded into the B operand (QK) or the output (PV).
 //   The contraction order of channels is free, so B is permuted to match.
+//
+// Codec variants (template arguments; page block sizes and ring depths above
+// are those of one quantisation group per vector):
+//   - NGK / NGV > 1 quantisation groups: the page format stores codes so that
+//     K-step j reads K group j / (8 / NGK) and 16-row tile mt reads V group
+//     mt / (8 / NGV); QK folds each group's sum with its scale as soon as its
+//     K-steps are done, PV takes one p s_V operand per V group, and the
+//     zero-point terms are summed per group.
+//   - codebook levels: a level l[c] = l_0 + d1 c + a2 (2 b1) + b (b0 b1) of
+//     the code's bits, so QK and PV run over the three bit planes c, 2 b1 and
+//     b0 b1 (single ANDs at the same operand positions) with the level
+//     coefficients on the QK sums and on the PV operands.
 #include <cfloat>
 #include <type_traits>
 
