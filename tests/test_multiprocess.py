@@ -52,3 +52,24 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
     args = type("A", (), {"steps": 1, "warmup": 0, "gpus": 2})()
     bench.run_reference(args)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line():
+    # the reference arm (the oracle on one host core) prints one JSON line
+    # with the contract's keys; no GPU is touched
+    import json
+    import subprocess
+    import sys
+    from conftest import ROOT
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["config"]["workload"] == "qwen3-8b-layer-decode-100k"
