@@ -78,8 +78,10 @@ extern "C" oscar_status oscar_fit_codebook(const double* x, int64_t n, int32_t d
     for (int k = 0; k < 4; ++k) lv[k] = nl[k];
     if (same) break;
   }
+  // levels clamped to [0, 3] (the fp16 scale and zero can put u a rounding
+  // step outside it), then rounded to fp16
   for (int k = 0; k < 4; ++k) {
-    const double h = round_fp16(lv[k]);
+    const double h = round_fp16(std::min(std::max(lv[k], 0.0), 3.0));
     if (k > 0 && !(h > double(levels_out[k - 1]))) return OSCAR_ERR_INVALID_ARG;
     levels_out[k] = float(h);
   }

@@ -240,8 +240,8 @@ oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_he
  *   over all u from levels {0, 1, 2, 3}: thresholds at the midpoints of
  *   adjacent levels, each level the mean of the u in its cell (u <= t_1, t_1
  *   < u <= t_2, ...; an empty cell keeps its level), at most `iters` rounds
- *   or until no level moves.  levels_out[4] = the levels rounded to fp16 (as
- *   float).  OSCAR_ERR_INVALID_ARG for bad sizes, tau <= 0, iters < 1, no
+ *   or until no level moves.  levels_out[4] = the levels clamped to [0, 3]
+ *   and rounded to fp16 (as float).  OSCAR_ERR_INVALID_ARG for bad sizes, tau <= 0, iters < 1, no
  *   usable row, or fitted levels that are not strictly increasing in fp16.
  *   Host-only, synchronous.
  */

@@ -297,9 +297,11 @@ def normalised_values(x_rot: np.ndarray, tau: float) -> np.ndarray:
 
 def fit_codebook(x: np.ndarray, r: np.ndarray, tau: float, iters: int = 100) -> np.ndarray:
     """fp16 Lloyd-Max levels (as float16) of one layer from calibration rows
-    x [n][d] (rotated by r, clipped at tau, normalised per row)."""
+    x [n][d] (rotated by r, clipped at tau, normalised per row).  The levels
+    are clamped to [0, 3] before rounding (the fp16 scale and zero can put u
+    a rounding step outside it)."""
     lv = lloyd_max_levels(normalised_values(rotate(x, r), tau), iters)
-    return lv.astype(np.float16)
+    return np.clip(lv, 0.0, 3.0).astype(np.float16)
 
 
 def quantize_codebook(x_rot: np.ndarray, tau: float, levels):

@@ -680,3 +680,14 @@ def test_codebook_decode_equals_plain_dequantisation():
         sc = keys @ q[hh] / math.sqrt(128)
         p = np.exp(sc - sc.max())
         np.testing.assert_allclose(got[hh], (p / p.sum()) @ vals, rtol=1e-12, atol=1e-12)
+
+
+def test_fit_codebook_levels_stay_in_range_for_two_valued_rows():
+    # rows taking only their min and max: every u is 0 or 3 up to the fp16
+    # rounding of scale and zero; the two outer levels sit at the ends and
+    # stay inside [0, 3]
+    g = synth.generator(15, 78)
+    x = np.where(g.random((400, 128)) < 0.5, -1.2345, 2.71828) * (1 + 0.1 * g.random((400, 1)))
+    lv = O.fit_codebook(x, np.eye(128), 10.0).astype(np.float64)
+    assert lv[0] >= 0.0 and lv[3] <= 3.0
+    assert lv[0] == pytest.approx(0.0, abs=2e-3) and lv[3] == pytest.approx(3.0, abs=2e-3)
