@@ -641,14 +641,24 @@ __device__ __forceinline__ void int2_probs_levels(const float (&sc)[Geo<G>::NH][
   for (int nt = 0; nt < Geo<G>::NH; ++nt) {
     float p0 = fast_exp2(sc[nt][0] - st.m[nt]);
     float p1 = fast_exp2(sc[nt][1] - st.m[nt]);
+    float q0, q1;
     if constexpr (kMasked) {
+      // a masked token's (scale, zero) may be stale ring bytes: selects, not
+      // products with p = 0
       p0 = ok0 ? p0 : 0.f;
       p1 = ok1 ? p1 : 0.f;
+      st.l[nt] += p0 + p1;
+      st.z[nt][0] += (ok0 ? p0 * vz0.y : 0.f) + (ok1 ? p1 * vz1.y : 0.f);
+      st.z[nt][1] += (ok0 ? p0 * vz0.x : 0.f) + (ok1 ? p1 * vz1.x : 0.f);
+      q0 = ok0 ? p0 * (vz0.x * sigma_v) : 0.f;
+      q1 = ok1 ? p1 * (vz1.x * sigma_v) : 0.f;
+    } else {
+      st.l[nt] += p0 + p1;
+      st.z[nt][0] = fmaf(p0, vz0.y, fmaf(p1, vz1.y, st.z[nt][0]));
+      st.z[nt][1] = fmaf(p0, vz0.x, fmaf(p1, vz1.x, st.z[nt][1]));
+      q0 = p0 * (vz0.x * sigma_v);
+      q1 = p1 * (vz1.x * sigma_v);
     }
-    st.l[nt] += p0 + p1;
-    st.z[nt][0] = fmaf(p0, vz0.y, fmaf(p1, vz1.y, st.z[nt][0]));
-    st.z[nt][1] = fmaf(p0, vz0.x, fmaf(p1, vz1.x, st.z[nt][1]));
-    const float q0 = p0 * (vz0.x * sigma_v), q1 = p1 * (vz1.x * sigma_v);
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const float r0 = q0 * coef[1 + k], r1 = q1 * coef[1 + k];
