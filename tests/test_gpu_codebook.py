@@ -84,3 +84,29 @@ def test_decode_codebook_fixed_levels(levels):
     lv = np.array(levels, np.float16)
     sc = H.Scenario(4300, [3000, 1500], n_kv=2, g=4, levels=(lv, lv.copy()))
     _check(sc)
+
+
+@pytest.mark.parametrize("with_levels", [False, True])
+def test_masked_tail_slots_with_nan_bytes_do_not_leak(with_levels):
+    # token slots past the history length of a partial last page are masked;
+    # their (scale, zero) bytes are set to fp16 NaN and their codes to 0xFF,
+    # and the output must still match the oracle (selects, not p = 0 products)
+    import torch
+    levels = _levels(4400, 2) if with_levels else None
+    sc = H.Scenario(4400, [64 + 1000 + 256, 64 + 777 + 256], n_kv=2, g=4, levels=levels)
+    assert all(int(h) % 16 for h in sc.hist_len)
+    cache, q = H.to_device(sc)
+    pool = cache.pages.cpu().numpy().copy()
+    nan = np.array([0x7E00, 0x7E00], np.uint16).view(np.uint8)
+    for b in range(sc.B):
+        h = int(sc.hist_len[b])
+        page = int(sc.table[b, (h - 1) // 16])
+        for head in range(sc.n_kv):
+            base = (page * sc.n_kv + head) * O.BLOCK_BYTES
+            for half in (0, O.HALF_BYTES):
+                for slot in range(h % 16, 16):
+                    pool[base + half + 32 * slot: base + half + 32 * slot + 32] = 0xFF
+                    so = base + half + 512 + 4 * slot
+                    pool[so:so + 4] = nan
+    cache.pages.copy_(torch.from_numpy(pool))
+    _check(sc)
