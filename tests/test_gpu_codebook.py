@@ -1,7 +1,7 @@
 """GPU parity for the Lloyd-Max codebook (four fp16 levels per layer, K and V).
 
-The levels are fitted by the library's host routine on seeded calibration
-rows (checked against the oracle's fit on the CPU).  Demotion: both kernels
+The levels are the oracle's fit on seeded calibration rows (the library's
+own fit is checked against it on the CPU).  Demotion: both kernels
 write nearest-level codes with the uniform codec's (scale, zero); codes are
 compared with the oracle's by `harness.code_parity` with the codebook's
 thresholds as rounding boundaries.  Decode: the oracle quantises and packs
@@ -28,8 +28,8 @@ def _cuda(built_lib):
 
 
 def _levels(seed, n_kv=2):
-    """(levels_k, levels_v): the library's fit on seeded calibration rows."""
-    from bit_rotated_kv_split_gb300 import binding as B
+    """(levels_k, levels_v): the oracle's fit on seeded calibration rows (the
+    library's fit is checked against it on the CPU)."""
     outl = synth.outlier_channels(seed, 0, n_kv)
     rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
     xk = np.concatenate([synth.calibration_set(seed, 0, h, outl[h], n_q=64, n_k=512)["k"] @ rk32[h].astype(np.float64)
@@ -37,8 +37,8 @@ def _levels(seed, n_kv=2):
     xv = np.concatenate([synth.calibration_set(seed, 0, h, outl[h], n_q=64, n_k=512)["v"] @ rv32[h].astype(np.float64)
                          for h in range(n_kv)])
     eye = np.eye(128)
-    lk = B.oscar_fit_codebook(xk, eye, tau_k).astype(np.float16)
-    lv = B.oscar_fit_codebook(xv, eye, tau_v).astype(np.float16)
+    lk = O.fit_codebook(xk, eye, tau_k)
+    lv = O.fit_codebook(xv, eye, tau_v)
     assert not np.array_equal(lk.astype(np.float32), [0, 1, 2, 3])
     return lk, lv
 
