@@ -266,3 +266,28 @@ def test_decode_step_rejects_before_any_copy(built_lib):
     assert B.lib.oscar_decode_step(*args(_desc(), None, None, 0, None)) == 3
     # a bad descriptor
     assert B.lib.oscar_decode_step(*args(_desc(head_dim=64), None, None, 0, fake)) == 1
+
+
+def test_fit_codebook_arguments_and_single_round(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    g = synth.generator(6, 3)
+    x = g.standard_normal((300, 128))
+    eye = np.eye(128)
+    # one Lloyd round from {0, 1, 2, 3}: the cell means, as the oracle's
+    want = O.fit_codebook(x, eye, 3.0, iters=1)
+    got = B.oscar_fit_codebook(x, eye, 3.0, iters=1)
+    ulp = np.abs(got.astype(np.float16).view(np.uint16).astype(int) - want.view(np.uint16).astype(int))
+    assert ulp.max() <= 1
+    out = np.zeros(4, np.float32)
+    bad = [
+        (x.ctypes.data, 300, 64, eye.ctypes.data, 3.0, 10),     # d != 128
+        (x.ctypes.data, 0, 128, eye.ctypes.data, 3.0, 10),      # no rows
+        (x.ctypes.data, 300, 128, eye.ctypes.data, 0.0, 10),    # tau <= 0
+        (x.ctypes.data, 300, 128, eye.ctypes.data, 3.0, 0),     # iters < 1
+        (None, 300, 128, eye.ctypes.data, 3.0, 10),             # no rows pointer
+    ]
+    for a in bad:
+        assert B.lib.oscar_fit_codebook(*a, out.ctypes.data) == 1
+    # constant rows: every scale is 0, no usable row
+    c = np.ones((10, 128))
+    assert B.lib.oscar_fit_codebook(c.ctypes.data, 10, 128, eye.ctypes.data, 3.0, 10, out.ctypes.data) == 1
