@@ -73,3 +73,26 @@ def test_reference_arm_json_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["config"]["workload"] == "qwen3-8b-layer-decode-100k"
+
+
+def test_decode_bytes_match_the_oracle_accounting():
+    # the roofline's algorithmic bytes per decode launch: INT2 history at the
+    # oracle's per-token storage cost (codes + (scale, zero) per group), BF16
+    # sink and recent K/V, page-table entries, q in and the fp32 output
+    import bench
+    import oracle as O
+    w = bench.WORKLOAD
+    keep = (w["group_k"], w["group_v"])
+    try:
+        for gk, gv in ((128, 128), (64, 64), (32, 128), (32, 32)):
+            w["group_k"], w["group_v"] = gk, gv
+            s, h, r = bench._split(w["ctx"])
+            want = (h * O.kv_bytes_per_history_token(w["n_kv_heads"], group_k=gk, group_v=gv)
+                    + (s + r) * w["n_kv_heads"] * 2 * 128 * 2 + -(-h // 16) * 4
+                    + w["n_q_heads"] * 128 * (2 + 4))
+            assert bench.bytes_per_decode() == want
+            assert bench._hist_bytes_per_token(w["n_kv_heads"]) == O.kv_bytes_per_history_token(
+                w["n_kv_heads"], group_k=gk, group_v=gv)
+    finally:
+        w["group_k"], w["group_v"] = keep
+    assert bench.bytes_per_decode() == 58_775_896
