@@ -339,8 +339,9 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
  *   Every argument of (2) and (3) is validated before (1) is issued: a
  *   rejected call copies and launches nothing.  in_bytes > 0 requires
  *   host_in and dev_in (OSCAR_ERR_INVALID_ARG otherwise); workspace must be
- *   given (OSCAR_ERR_WORKSPACE).  Async: host_out holds the output once the
- *   stream reaches that point; host_in must not change before then.
+ *   given (OSCAR_ERR_WORKSPACE).  Async: host_in must not change until the
+ *   stream has passed step (1), and host_out holds the output once the
+ *   stream has passed step (4).
  */
 oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
                                size_t in_bytes, uint16_t* k_src, uint16_t* v_src, int64_t src_rows,
