@@ -63,6 +63,7 @@ EXTRA_WORKLOADS = {
 # calibration covariance on the device: C = X^T X / N over 2^20 bf16 rows of
 # 128 values (the C_Q / C_S accumulation of one KV head)
 CALIB_WORKLOAD = "calib-covariance-1m"
+RING_START = 1     # ring slot of the oldest recent token in the steady state
 CACHE_TENSORS = ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
                  "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status")
 
@@ -339,26 +340,25 @@ def _code_only(src):
 
 
 def _profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+    """DRAM bytes per decode launch from the committed ncu capture record
+    (profiles/split_kernel_qwen3-8b-layer-decode-100k.json, beside its
+    summary), if it was taken on the current kernel sources (else None)."""
     import hashlib
-    import re
     if (WORKLOAD["group_k"], WORKLOAD["group_v"]) != (128, 128) or WORKLOAD["codebook"] != "uniform":
-        return None    # the summary covers the one-group, uniform-level kernel
-    prof = os.path.join(ROOT, "profiles", "split_kernel_qwen3-8b-layer-decode-100k.md")
+        return None    # the capture covers the one-group, uniform-level kernel
+    prof = os.path.join(ROOT, "profiles", "split_kernel_qwen3-8b-layer-decode-100k.json")
     try:
-        text = open(prof).read()
-    except OSError:
+        with open(prof) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
     h = hashlib.sha256()
-    for f in ("decode.cu", "ptx.cuh", "kernels.h"):
+    for f in rec.get("source_files", []):
         with open(os.path.join(ROOT, "bit_rotated_kv_split_gb300", "csrc", f), encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
-    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    m_bytes = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != h.hexdigest():
+    if not rec.get("source_files") or rec.get("source_sha256") != h.hexdigest():
         return None
-    return int(m_bytes.group(1))
+    return int(rec["traffic_bytes_per_launch"])
 
 
 def _roofline_peak():
@@ -448,7 +448,11 @@ def build_layer(torch, B, dev, rot):
     cache.hist_len.fill_(h)
     cache.sink_len.fill_(s)
     cache.recent_len.fill_(r)
-    cache.recent_start.fill_(1)     # ring slot 0 holds the newest token after each step
+    # the oldest recent token sits in ring slot 1; every step demotes it and
+    # writes the new token into that slot.  Lengths and the ring start are
+    # not advanced, so each step does identical work (attention does not
+    # depend on where in the ring a token sits).
+    cache.recent_start.fill_(RING_START)
     torch.cuda.synchronize()
     assert int(cache.dev_status.item()) == 0
     return cache
@@ -493,7 +497,8 @@ def run_gpu(args):
     new_k = synth.activations_device(w["seed"], (2, 1), bsz, rot[4], dev)
     new_v = synth.activations_device(w["seed"], (2, 2), bsz, rot[4], dev)
     out = torch.empty((bsz, w["n_q_heads"], 128), dtype=torch.float32, device=dev)
-    src = torch.tensor([b * w["recent"] for b in range(bsz)], dtype=torch.int32, device=dev)
+    # ring row of each request's oldest recent token (the one a step demotes)
+    src = torch.tensor([b * w["recent"] + RING_START for b in range(bsz)], dtype=torch.int32, device=dev)
     dst_req = torch.arange(bsz, dtype=torch.int32, device=dev)
     dst_pos = torch.full((bsz,), h - 1, dtype=torch.int32, device=dev)
     descs = [L.desc(h) for L in layers]
@@ -754,7 +759,7 @@ def _build_batch_cache(torch, B, dev, rot, seed, layer, ctxs, n_q, n_kv, shared_
     cache.hist_len.copy_(torch.tensor(hist, dtype=torch.int32))
     cache.sink_len.copy_(torch.tensor([x for x, _, _ in splits], dtype=torch.int32))
     cache.recent_len.copy_(torch.tensor([x for _, _, x in splits], dtype=torch.int32))
-    cache.recent_start.fill_(1)
+    cache.recent_start.fill_(RING_START)
     torch.cuda.synchronize()
     assert int(cache.dev_status.item()) == 0
     unique_hist = n_shared_pages * 16 + sum(h - st for h, st in zip(hist, shared_tok))
@@ -882,7 +887,7 @@ def run_extra(args):
     new_k = synth.activations_device(seed, (70, 1), bsz, rots[0][4], dev)
     new_v = synth.activations_device(seed, (70, 2), bsz, rots[0][4], dev)
     out = torch.empty((bsz, n_q, 128), dtype=torch.float32, device=dev)
-    src = torch.tensor([b * WORKLOAD["recent"] for b in range(bsz)], dtype=torch.int32, device=dev)
+    src = torch.tensor([b * WORKLOAD["recent"] + RING_START for b in range(bsz)], dtype=torch.int32, device=dev)
     dst_req = torch.arange(bsz, dtype=torch.int32, device=dev)
     dst_pos = torch.tensor(hist, dtype=torch.int32, device=dev)        # private tail slot of each request
     descs = [c.desc(max(hist) + 16) for c in caches]

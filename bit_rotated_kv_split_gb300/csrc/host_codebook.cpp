@@ -80,10 +80,13 @@ extern "C" oscar_status oscar_fit_codebook(const double* x, int64_t n, int32_t d
   }
   // levels clamped to [0, 3] (the fp16 scale and zero can put u a rounding
   // step outside it), then rounded to fp16
+  // (built locally: levels_out is written only once all four are strictly
+  // increasing, so a rejected fit leaves it untouched)
+  float h[4];
   for (int k = 0; k < 4; ++k) {
-    const double h = round_fp16(std::min(std::max(lv[k], 0.0), 3.0));
-    if (k > 0 && !(h > double(levels_out[k - 1]))) return OSCAR_ERR_INVALID_ARG;
-    levels_out[k] = float(h);
+    h[k] = float(round_fp16(std::min(std::max(lv[k], 0.0), 3.0)));
+    if (k > 0 && !(h[k] > h[k - 1])) return OSCAR_ERR_INVALID_ARG;
   }
+  for (int k = 0; k < 4; ++k) levels_out[k] = h[k];
   return OSCAR_OK;
 }

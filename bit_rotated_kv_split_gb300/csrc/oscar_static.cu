@@ -4,8 +4,14 @@
 //
 // The workspace is one file-scope __device__ array of kStaticWorkspaceBytes.
 // Host code never uses the array's name as a device address (on the host it
-// names a host-side shadow); the device address is looked up once per device
-// with cudaGetSymbolAddress while that device is current, and cached.
+// names a host-side shadow); the device address is looked up with
+// cudaGetSymbolAddress while the device is current, once per device and
+// context: the lookup is repeated when the device's current context is not
+// the one the cached address belongs to (after cudaDeviceReset the module
+// is loaded again and the array may move).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "oscar.h"
@@ -19,17 +25,38 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 
 std::mutex g_mutex;
 void* g_ptr[kMaxDevices] = {nullptr};
+CUcontext g_ctx[kMaxDevices] = {nullptr};
 
-// Device address of g_static_workspace on the current device (first call on
-// a device performs the lookup).
+// The calling thread's current driver context (nullptr if none or if the
+// driver entry point is unavailable).
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 get = nullptr;
+  if (!get) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  }
+  CUcontext c = nullptr;
+  return get(&c) == CUDA_SUCCESS ? c : nullptr;
+}
+
+// Device address of g_static_workspace on the current device.  The first
+// call on a device (and the first after its context changed) performs the
+// lookup; later calls reuse it.
 oscar_status static_workspace(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OSCAR_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_ptr[dev]) {
+  const CUcontext ctx = current_context();
+  if (!g_ptr[dev] || !ctx || ctx != g_ctx[dev]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return OSCAR_ERR_CUDA;
     g_ptr[dev] = ptr;
+    // (the runtime made its primary context current during the lookup)
+    g_ctx[dev] = current_context();
   }
   *out = g_ptr[dev];
   return OSCAR_OK;

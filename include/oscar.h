@@ -371,8 +371,9 @@ oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in
  *   MB for one 100k-token request with 8 KV heads and GQA 4).
  *
  *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  Each call clears the part of the array that
+ *   (cudaGetSymbolAddress) with that device current, and so does the first
+ *   call after the device's context was replaced (cudaDeviceReset); make
+ *   those calls before any stream capture.  Each call clears the part of the array that
  *   must start at zero, on `stream`, then launches.  Every call shares the
  *   one array and it keeps the last call's contents: calls whose work
  *   overlaps on the GPU (different streams, or concurrent host threads

@@ -151,8 +151,8 @@ def value_covariance(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
 def eigenbasis(c: np.ndarray):
     """(U, eigenvalues): columns of U are eigenvectors of the symmetric C.
 
-    Ordered by descending eigenvalue ("aligns channels with importance"),
-    each column's largest-|entry| made positive (ties: lowest index).
+    Ordered by descending eigenvalue, so the strongest query directions come
+    first; each column's largest-|entry| made positive (ties: lowest index).
     [GIST] 2.2 A (eigendecomposition gives U_Q / U_S).
     """
     c = np.asarray(c, dtype=np.float64)
@@ -338,7 +338,7 @@ def demote(x: np.ndarray, r: np.ndarray, tau: float):
 def pack(codes: np.ndarray) -> np.ndarray:
     """Four 2-bit codes per byte: byte j = c[4j] | c[4j+1]<<2 | c[4j+2]<<4 | c[4j+3]<<6.
 
-    [ZAKER] pipeline part ("every 4 two-bit values are packed into 1 byte").
+    [ZAKER] pipeline part (the codes are packed four to a byte).
     """
     c = np.asarray(codes, dtype=np.uint8)
     c = c.reshape(c.shape[:-1] + (c.shape[-1] // 4, 4))

@@ -291,3 +291,16 @@ def test_fit_codebook_arguments_and_single_round(built_lib):
     # constant rows: every scale is 0, no usable row
     c = np.ones((10, 128))
     assert B.lib.oscar_fit_codebook(c.ctypes.data, 10, 128, eye.ctypes.data, 3.0, 10, out.ctypes.data) == 1
+
+
+def test_fit_codebook_leaves_output_untouched_when_levels_collapse(built_lib):
+    """Rows whose normalised values sit just below and just above u = 1.5
+    give two fitted levels that round to the same fp16 value: the fit is
+    rejected and the output buffer keeps its contents."""
+    from bit_rotated_kv_split_gb300 import binding as B
+    row = np.concatenate([[0.0, 3.0], np.full(63, 1.5 - 1e-4), np.full(63, 1.5 + 1e-4)])
+    x = np.tile(row, (20, 1))
+    eye = np.eye(128)
+    out = np.full(4, -7.0, np.float32)
+    assert B.lib.oscar_fit_codebook(x.ctypes.data, 20, 128, eye.ctypes.data, 3.0, 50, out.ctypes.data) == 1
+    np.testing.assert_array_equal(out, np.full(4, -7.0, np.float32))

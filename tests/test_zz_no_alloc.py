@@ -3,8 +3,8 @@
 oscar_decode_attention_static serves callers that cannot allocate device
 memory (a host framework that owns all allocations, or a serving loop that
 forbids allocating after start-up): it runs the same decode with a fixed
-workspace inside the library.  Two calls in a row must each match the
-regular entry point's output on the same inputs.  This file is collected
+workspace inside the library.  Two calls in a row must each give the
+regular entry point's output on the same inputs, bit for bit.  This file is collected
 last on purpose.
 """
 import numpy as np
@@ -24,20 +24,24 @@ def _cuda(built_lib):
 
 
 def test_static_workspace_matches_regular_entry_point_twice():
+    """Decode is deterministic (fixed-order reductions), so the fixed
+    workspace must give the regular entry point's output bit for bit, on
+    two calls in a row; both are also within the attention tolerance of the
+    float64 oracle."""
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     sc = H.Scenario(31, [3000, 800, 2049], n_kv=2, g=4)
     cache, q = H.to_device(sc)
     ref, status = H.run_decode(cache, q)
     assert status == 0
+    assert H.relative_error(ref, sc.expected()).max() <= TOL
     desc = cache.desc()
     for _ in range(2):
         out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=q.device)
         B.oscar_decode_attention_static(desc, q, out)
         torch.cuda.synchronize()
         got = out.cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(got))
-        assert H.relative_error(got, ref).max() <= TOL
+        np.testing.assert_array_equal(got, ref)
     assert int(cache.dev_status.item()) == 0
 
 
