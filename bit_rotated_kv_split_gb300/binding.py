@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "liboscar.so")
 
 OSCAR_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE", 4: "CUDA",
-                5: "NO_CONVERGENCE", 6: "UNSUPPORTED"}
+                5: "NO_CONVERGENCE", 6: "UNSUPPORTED", 7: "FILE"}
 DEV_PAGE_BOUNDS, DEV_LENGTH, DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 
@@ -58,6 +58,9 @@ def _load():
         "oscar_score_weighted_rows": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_double, P]),
         "oscar_clip_threshold": (c_int32, [P, c_int64, c_int32, c_int32, P, c_double, P]),
         "oscar_fit_codebook": (c_int32, [P, c_int64, c_int32, P, c_double, c_int32, P]),
+        "oscar_rotation_file_write": (c_int32, [ctypes.c_char_p, c_int32, c_int32, c_int32, P, P, P, P]),
+        "oscar_rotation_file_info": (c_int32, [ctypes.c_char_p, P, P, P]),
+        "oscar_rotation_file_read": (c_int32, [ctypes.c_char_p, c_int32, c_int32, c_int32, P, P, P, P]),
         "oscar_quantize_append": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
                                             P, P, c_int32, P, P, P]),
         "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
@@ -173,6 +176,31 @@ def oscar_clip_threshold(acts: np.ndarray, r: np.ndarray, quantile: float = 0.99
     _check("oscar_clip_threshold", lib.oscar_clip_threshold(
         acts.ctypes.data, rows, h, d, r.ctypes.data, quantile, ctypes.byref(tau)))
     return tau.value
+
+
+def oscar_rotation_file_write(path: str, r_k: np.ndarray, r_v: np.ndarray, tau_k, tau_v) -> None:
+    """r_k, r_v [n_layers][n_kv][d][d], tau_k, tau_v [n_layers] (stored as float32)."""
+    r_k = np.ascontiguousarray(r_k, dtype=np.float32)
+    r_v = np.ascontiguousarray(r_v, dtype=np.float32)
+    tk = np.ascontiguousarray(np.atleast_1d(tau_k), dtype=np.float32)
+    tv = np.ascontiguousarray(np.atleast_1d(tau_v), dtype=np.float32)
+    n_layers, n_kv, d = r_k.shape[0], r_k.shape[1], r_k.shape[2]
+    _check("oscar_rotation_file_write", lib.oscar_rotation_file_write(
+        os.fsencode(path), n_layers, n_kv, d, r_k.ctypes.data, r_v.ctypes.data, tk.ctypes.data, tv.ctypes.data))
+
+
+def oscar_rotation_file_read(path: str):
+    """(r_k, r_v [n_layers][n_kv][d][d] float32, tau_k, tau_v [n_layers] float32)."""
+    dims = [c_int32(0), c_int32(0), c_int32(0)]
+    _check("oscar_rotation_file_info", lib.oscar_rotation_file_info(os.fsencode(path), *[ctypes.byref(x) for x in dims]))
+    n_layers, n_kv, d = (x.value for x in dims)
+    r_k = np.empty((n_layers, n_kv, d, d), np.float32)
+    r_v = np.empty_like(r_k)
+    tk = np.empty(n_layers, np.float32)
+    tv = np.empty(n_layers, np.float32)
+    _check("oscar_rotation_file_read", lib.oscar_rotation_file_read(
+        os.fsencode(path), n_layers, n_kv, d, r_k.ctypes.data, r_v.ctypes.data, tk.ctypes.data, tv.ctypes.data))
+    return r_k, r_v, tk, tv
 
 
 def oscar_fit_codebook(x: np.ndarray, r: np.ndarray, tau: float, iters: int = 100) -> np.ndarray:

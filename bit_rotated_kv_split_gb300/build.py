@@ -64,7 +64,9 @@ def _compile(src: str, verbose: bool) -> str:
         if verbose:
             cmd += ["-Xptxas", "-v"]
     else:
-        cmd = [os.environ.get("CXX", "g++")] + CXX_FLAGS + ["-I", INCLUDE, "-c", src, "-o", obj]
+        # (the CUDA toolkit's headers: the header-only NVTX v3 ranges)
+        cuda_inc = os.path.join(os.path.dirname(os.path.dirname(_nvcc())), "include")
+        cmd = [os.environ.get("CXX", "g++")] + CXX_FLAGS + ["-I", INCLUDE, "-I", cuda_inc, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("compile failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))

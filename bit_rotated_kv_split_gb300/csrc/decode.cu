@@ -120,7 +120,6 @@ struct Geo {
   static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : (NGK * NGV > 1 || LV ? 2 : OSCAR_GROUP_G8);
   static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
   static constexpr int kBlock = block_bytes(NGK, NGV);   // one (page, KV head) block
-  static constexpr int kHalfK = half_bytes(NGK);         // offset of the V half
   // union: R_K (64 KB, prologue) then R_V (epilogue), followed by the q~
   // scratch (prologue) that the CTA merge reuses
   static constexpr size_t kRotBytes = size_t(kHeadDim) * kHeadDim * 4;
@@ -180,6 +179,17 @@ __device__ __forceinline__ int code_pos(int j) { return j < 5 ? j : j - 3; }
 
 __device__ __forceinline__ float split_lo(float x) {
   return x - __half2float(__float2half_rn(x));
+}
+
+// x as an fp16 (hi, lo) pair in one register, hi in the low half: hi = x
+// with its 13 low significand bits cleared (11 significant bits, exact in
+// fp16 within its normal range), lo = fp16(x - hi) (the difference is
+// exact), so hi + lo keeps about 22 bits of x.
+__device__ __forceinline__ uint32_t split_hi_lo(float x) {
+  const float hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x - hi), "f"(hi));
+  return r;
 }
 
 // 2^x by the ex2.approx instruction (relative error about 2^-22; results
@@ -365,24 +375,52 @@ __device__ __forceinline__ void int2_qk_groups(const uint8_t* __restrict__ pg, i
   }
 }
 
-// The NG (scale, zero) fp16 pairs of token slot t of a half (pairs start at
-// byte 512, token-major).
-template <int NG>
-__device__ __forceinline__ void load_sz(const uint8_t* half, int t, uint32_t (&sz)[NG]) {
-  const uint8_t* a = half + kCodeBytes + 4 * NG * t;
-  if constexpr (NG == 1) {
-    sz[0] = *reinterpret_cast<const uint32_t*>(a);
-  } else if constexpr (NG == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(a);
-    sz[0] = v.x;
-    sz[1] = v.y;
-  } else {
-    const uint4 v = *reinterpret_cast<const uint4*>(a);
-    sz[0] = v.x;
-    sz[1] = v.y;
-    sz[2] = v.z;
-    sz[3] = v.w;
+// The (scale, zero) fp16 pairs of token slot t of a page block: NGK K pairs
+// then NGV V pairs at kPairs + 4 (NGK + NGV) t.  load_pairs reads both sets
+// (one 8-byte load with one group each); load_group_pairs reads N pairs
+// from pair index `first` on.  The vector width of the loads is the largest
+// that every token slot's address allows: A words apart, with A the largest
+// power of two (at most 4) dividing both NGK + NGV and `first`.
+constexpr int pair_align(int n, int first) {
+  return (n % 4 == 0 && first % 4 == 0) ? 4 : (n % 2 == 0 && first % 2 == 0) ? 2 : 1;
+}
+
+template <int N, int A>
+__device__ __forceinline__ void load_words(const uint8_t* a, uint32_t (&w)[N]) {
+  constexpr int V = A < N ? A : (N % 4 == 0 ? 4 : N % 2 == 0 ? 2 : 1);
+  static_assert(N % V == 0, "vector width divides the word count");
+#pragma unroll
+  for (int i = 0; i < N / V; ++i) {
+    if constexpr (V == 4) {
+      const uint4 v = reinterpret_cast<const uint4*>(a)[i];
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    } else if constexpr (V == 2) {
+      const uint2 v = reinterpret_cast<const uint2*>(a)[i];
+      w[2 * i] = v.x;
+      w[2 * i + 1] = v.y;
+    } else {
+      w[i] = reinterpret_cast<const uint32_t*>(a)[i];
+    }
   }
+}
+
+template <int NGK, int NGV>
+__device__ __forceinline__ void load_pairs(const uint8_t* pg, int t, uint32_t (&ksz)[NGK], uint32_t (&vsz)[NGV]) {
+  constexpr int N = NGK + NGV;
+  uint32_t w[N];
+  load_words<N, pair_align(N, 0)>(pg + kPairs + 4 * N * t, w);
+#pragma unroll
+  for (int q = 0; q < NGK; ++q) ksz[q] = w[q];
+#pragma unroll
+  for (int q = 0; q < NGV; ++q) vsz[q] = w[NGK + q];
+}
+
+template <int NGK, int NGV, int kFirst, int N>
+__device__ __forceinline__ void load_group_pairs(const uint8_t* pg, int t, uint32_t (&sz)[N]) {
+  load_words<N, pair_align(NGK + NGV, kFirst)>(pg + kPairs + 4 * (NGK + NGV) * t + 4 * kFirst, sz);
 }
 
 // Scores (log2 units) of the lane's two tokens of one page from its QK
@@ -428,14 +466,18 @@ __device__ __forceinline__ void int2_scores_groups(const float (&a)[Geo<G>::NH][
 
 // Lazy online-softmax maximum over a step's scores: raised only when a score
 // exceeds it by 2^kRescaleLog2; the 8 lanes of a column group share a head.
+// The INT2 state keeps its maximum lowered by pv_log2 (st.m = max - pv_log2),
+// so that p = 2^(s - st.m) carries the PV operand scale 2^pv_log2 with it;
+// `lift` = kRescaleLog2 + pv_log2.
 template <int G, int NGV, int P>
-__device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH][2], HistState<G, NGV>& st) {
+__device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH][2], HistState<G, NGV>& st,
+                                                float pv_log2, float lift) {
   constexpr int NH = Geo<G>::NH;
   bool need = false;
 #pragma unroll
   for (int pg = 0; pg < P; ++pg)
 #pragma unroll
-    for (int nt = 0; nt < NH; ++nt) need |= fmaxf(sc[pg][nt][0], sc[pg][nt][1]) > st.m[nt] + float(kRescaleLog2);
+    for (int nt = 0; nt < NH; ++nt) need |= fmaxf(sc[pg][nt][0], sc[pg][nt][1]) > st.m[nt] + lift;
   if (!__any_sync(kFull, need)) return;
 #pragma unroll
   for (int nt = 0; nt < NH; ++nt) {
@@ -445,6 +487,7 @@ __device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH]
     pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 4));
     pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 8));
     pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 16));
+    pm -= pv_log2;
     if (pm > st.m[nt]) {
       const float f = exp2f(st.m[nt] - pm);
       st.m[nt] = pm;
@@ -463,15 +506,16 @@ __device__ __forceinline__ void int2_update_max(const float (&sc)[P][Geo<G>::NH]
 }
 
 // Probabilities of one page -> PV B fragments: the lane packs (hi, lo) of
-// p s_V sigma_v for token gid (row gid, columns 2 tig, 2 tig + 1) and token
-// gid + 8; movmatrix transposes them into the B layout (rows = tokens).  With
-// NGV groups there is one operand per V group q (its own s_V), and the
+// p s_V for token gid (row gid, columns 2 tig, 2 tig + 1) and token gid + 8,
+// with p = 2^(s - st.m) already carrying the operand scale 2^pv_log2;
+// movmatrix transposes them into the B layout (rows = tokens).  With NGV
+// groups there is one operand per V group q (its own s_V), and the
 // zero-point term accumulates per group.
 // (kMasked = false: every token valid, so stale ring bytes never reach a
 // product and no select is needed.)
 template <int G, int NGV, bool kMasked>
 __device__ __forceinline__ void int2_probs(const float (&sc)[Geo<G>::NH][2], const uint32_t (&vsz0)[NGV],
-                                           const uint32_t (&vsz1)[NGV], bool ok0, bool ok1, float sigma_v,
+                                           const uint32_t (&vsz1)[NGV], bool ok0, bool ok1,
                                            HistState<G, NGV>& st, uint32_t (&pb)[NGV][Geo<G>::NH][2]) {
   float2 vz0[NGV], vz1[NGV];
 #pragma unroll
@@ -493,34 +537,32 @@ __device__ __forceinline__ void int2_probs(const float (&sc)[Geo<G>::NH][2], con
       float q0, q1;
       if constexpr (kMasked) {
         st.z[nt][q] += (ok0 ? p0 * vz0[q].y : 0.f) + (ok1 ? p1 * vz1[q].y : 0.f);
-        q0 = ok0 ? p0 * (vz0[q].x * sigma_v) : 0.f;
-        q1 = ok1 ? p1 * (vz1[q].x * sigma_v) : 0.f;
+        q0 = ok0 ? p0 * vz0[q].x : 0.f;
+        q1 = ok1 ? p1 * vz1[q].x : 0.f;
       } else {
         st.z[nt][q] = fmaf(p0, vz0[q].y, fmaf(p1, vz1[q].y, st.z[nt][q]));
-        q0 = p0 * (vz0[q].x * sigma_v);
-        q1 = p1 * (vz1[q].x * sigma_v);
+        q0 = p0 * vz0[q].x;
+        q1 = p1 * vz1[q].x;
       }
-      const __half h0 = __float2half_rn(q0), h1 = __float2half_rn(q1);
-      const __half l0 = __float2half_rn(q0 - __half2float(h0)), l1 = __float2half_rn(q1 - __half2float(h1));
-      pb[q][nt][0] = movmatrix_trans(uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(l0)) << 16));
-      pb[q][nt][1] = movmatrix_trans(uint32_t(__half_as_ushort(h1)) | (uint32_t(__half_as_ushort(l1)) << 16));
+      pb[q][nt][0] = movmatrix_trans(split_hi_lo(q0));
+      pb[q][nt][1] = movmatrix_trans(split_hi_lo(q1));
     }
   }
 }
 
 // PV of one INT2 page: acc[nt][mt] += codes^T . P, code positions 16 gid + mt
 // (+8); 16-row tile mt holds V group mt / (8 / NGV) (the page format's code
-// order) and takes that group's operand.  kHalfK: offset of the V half.
-template <int G, int NGV, int kHalfK>
+// order) and takes that group's operand.  The V rows interleave slot pairs
+// by 16-bit halves, so the words at 64 a + 8 gid hold halves 2 gid and
+// 2 gid + 1 (code positions 16 gid .. 16 gid + 15) of tokens 2a and 2a + 1:
+// the lane's A operand rows, one 8-byte load per token pair.
+template <int G, int NGV>
 __device__ __forceinline__ void int2_pv(const uint8_t* __restrict__ pg, int gid, int tig,
                                         const uint32_t (&pb)[NGV][Geo<G>::NH][2], HistState<G, NGV>& st) {
-  const uint8_t* pv = pg + kHalfK;
-  const uint32_t va = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 4 * gid);
-  const uint32_t vb = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 32 + 4 * gid);
-  const uint32_t vc = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 256 + 4 * gid);
-  const uint32_t vd = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 288 + 4 * gid);
-  const uint32_t x0l = prmt(va, vb, 0x5410), x0h = prmt(va, vb, 0x7632);
-  const uint32_t x8l = prmt(vc, vd, 0x5410), x8h = prmt(vc, vd, 0x7632);
+  const uint8_t* pv = pg + kVCodes;
+  const uint2 w0 = *reinterpret_cast<const uint2*>(pv + 64 * tig + 8 * gid);
+  const uint2 w8 = *reinterpret_cast<const uint2*>(pv + 64 * (tig + 4) + 8 * gid);
+  const uint32_t x0l = w0.x, x0h = w0.y, x8l = w8.x, x8h = w8.y;
   const uint32_t y0l = x0l >> 6, y0h = x0h >> 6, y8l = x8l >> 6, y8h = x8h >> 6;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
@@ -533,8 +575,10 @@ __device__ __forceinline__ void int2_pv(const uint8_t* __restrict__ pg, int gid,
 }
 
 // INT2 warp state -> ws[h * kPartStride + (0, 1, 4 + channel)] in the
-// rotated basis: o~ = (hi + lo) 2^24 4^-pos(mt) / sigma_v + zeta_q, where
-// code position c = 16 gid + mt (+8) holds the page format's V channel.
+// rotated basis: o~ = (hi + lo) 2^24 4^-pos(mt) + zeta_q, where code position
+// c = 16 gid + mt (+8) holds the page format's V channel.  Every term of the
+// state carries the factor 2^pv_log2 and its maximum is lowered by pv_log2,
+// so (m, l, o~) is a softmax state like any other.
 template <int G, int NGV>
 __device__ __forceinline__ void store_hist_state(HistState<G, NGV>& st, float* ws, int gid, int tig,
                                                  float pv_unscale) {
@@ -631,10 +675,11 @@ __device__ __forceinline__ void int2_scores_levels(const float (&e)[Geo<G>::NH][
 }
 
 // Probabilities with levels: z[nt][0] += sum p z_V, z[nt][1] += sum p s_V (the
-// l_0 part), and one PV operand per plane k: p s_V sigma_v coef[1 + k].
+// l_0 part), and one PV operand per plane k: p s_V coef[1 + k] (p carries
+// the operand scale 2^pv_log2).
 template <int G, bool kMasked>
 __device__ __forceinline__ void int2_probs_levels(const float (&sc)[Geo<G>::NH][2], uint32_t vsz0, uint32_t vsz1,
-                                                  bool ok0, bool ok1, float sigma_v, const float* coef,
+                                                  bool ok0, bool ok1, const float* coef,
                                                   HistState<G, 2>& st, uint32_t (&pb)[3][Geo<G>::NH][2]) {
   const float2 vz0 = half2_to_float2(vsz0), vz1 = half2_to_float2(vsz1);
 #pragma unroll
@@ -650,22 +695,19 @@ __device__ __forceinline__ void int2_probs_levels(const float (&sc)[Geo<G>::NH][
       st.l[nt] += p0 + p1;
       st.z[nt][0] += (ok0 ? p0 * vz0.y : 0.f) + (ok1 ? p1 * vz1.y : 0.f);
       st.z[nt][1] += (ok0 ? p0 * vz0.x : 0.f) + (ok1 ? p1 * vz1.x : 0.f);
-      q0 = ok0 ? p0 * (vz0.x * sigma_v) : 0.f;
-      q1 = ok1 ? p1 * (vz1.x * sigma_v) : 0.f;
+      q0 = ok0 ? p0 * vz0.x : 0.f;
+      q1 = ok1 ? p1 * vz1.x : 0.f;
     } else {
       st.l[nt] += p0 + p1;
       st.z[nt][0] = fmaf(p0, vz0.y, fmaf(p1, vz1.y, st.z[nt][0]));
       st.z[nt][1] = fmaf(p0, vz0.x, fmaf(p1, vz1.x, st.z[nt][1]));
-      q0 = p0 * (vz0.x * sigma_v);
-      q1 = p1 * (vz1.x * sigma_v);
+      q0 = p0 * vz0.x;
+      q1 = p1 * vz1.x;
     }
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-      const float r0 = q0 * coef[1 + k], r1 = q1 * coef[1 + k];
-      const __half h0 = __float2half_rn(r0), h1 = __float2half_rn(r1);
-      const __half l0 = __float2half_rn(r0 - __half2float(h0)), l1 = __float2half_rn(r1 - __half2float(h1));
-      pb[k][nt][0] = movmatrix_trans(uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(l0)) << 16));
-      pb[k][nt][1] = movmatrix_trans(uint32_t(__half_as_ushort(h1)) | (uint32_t(__half_as_ushort(l1)) << 16));
+      pb[k][nt][0] = movmatrix_trans(split_hi_lo(q0 * coef[1 + k]));
+      pb[k][nt][1] = movmatrix_trans(split_hi_lo(q1 * coef[1 + k]));
     }
   }
 }
@@ -674,12 +716,10 @@ __device__ __forceinline__ void int2_probs_levels(const float (&sc)[Geo<G>::NH][
 template <int G>
 __device__ __forceinline__ void int2_pv_levels(const uint8_t* __restrict__ pg, int gid, int tig,
                                                const uint32_t (&pb)[3][Geo<G>::NH][2], HistState<G, 2>& st) {
-  const uint8_t* pv = pg + kHalfBytes;
-  const uint32_t va = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 4 * gid);
-  const uint32_t vb = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 32 + 4 * gid);
-  const uint32_t vc = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 256 + 4 * gid);
-  const uint32_t vd = *reinterpret_cast<const uint32_t*>(pv + 64 * tig + 288 + 4 * gid);
-  const uint32_t x[4] = {prmt(va, vb, 0x5410), prmt(va, vb, 0x7632), prmt(vc, vd, 0x5410), prmt(vc, vd, 0x7632)};
+  const uint8_t* pv = pg + kVCodes;
+  const uint2 w0 = *reinterpret_cast<const uint2*>(pv + 64 * tig + 8 * gid);
+  const uint2 w8 = *reinterpret_cast<const uint2*>(pv + 64 * (tig + 4) + 8 * gid);
+  const uint32_t x[4] = {w0.x, w0.y, w8.x, w8.y};
   uint32_t xs[4], t[4], ts[4];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -704,8 +744,8 @@ __device__ __forceinline__ void int2_pv_levels(const uint8_t* __restrict__ pg, i
   }
 }
 
-// INT2 warp state with levels -> ws: o~ = (hi + lo) 2^24 4^-pos(mt) / sigma_v
-// + sum p z_V + l_0 sum p s_V.
+// INT2 warp state with levels -> ws: o~ = (hi + lo) 2^24 4^-pos(mt)
+// + sum p z_V + l_0 sum p s_V (every term carries 2^pv_log2, as above).
 template <int G>
 __device__ __forceinline__ void store_hist_state_levels(HistState<G, 2>& st, float* ws, int gid, int tig,
                                                         float pv_unscale, float l0) {
@@ -816,7 +856,7 @@ __device__ __forceinline__ void bf16_page(const uint16_t* const (&krow)[2],
 // ------------------------------------------------------------------ warp -> smem state
 
 // kInt2: channel of (mt, c) is 16gid + mt (+8 for c >= 2), value scaled by
-// 2^24 4^-pos(mt) / sigma_v plus the zero-point term; BF16: 16gid + 2mt (+1).
+// 2^24 4^-pos(mt) plus the zero-point term; BF16: 16gid + 2mt (+1).
 template <int G, bool kInt2>
 __device__ __forceinline__ void store_warp_state(WarpState<G>& st, float* ws, int gid, int tig,
                                                  float pv_unscale) {
@@ -986,22 +1026,6 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
   named_barrier(kPrologueBarrier, T);
 }
 
-// Page ids of a warp's pages, 32 at a time, one per lane (warp-collective).
-// `limit` bounds the page index (loads may run ahead of the history length).
-struct PidWindow {
-  int base = -1, v = -1;
-  __device__ __forceinline__ int get(int k, const int32_t* ptab, int first, int stride, int limit,
-                                     int lane) {
-    const int b0 = k & ~31;
-    if (b0 != base) {
-      base = b0;
-      const int pi = first + (b0 + lane) * stride;
-      v = pi < limit ? __ldg(ptab + pi) : -1;
-    }
-    return __shfl_sync(kFull, v, k & 31);
-  }
-};
-
 // ------------------------------------------------------------------ split kernel
 
 // kLevels: codebook levels (one quantisation group per vector only).
@@ -1083,42 +1107,48 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     }
   }
 
-  // ---------------- INT2 page range of this CTA and warp.  The first pages
-  // are requested before the history length is known (pages past it are
-  // read but never used; out-of-range ids are never copied).
+  // ---------------- INT2 pages of this CTA: warp w first copies pages
+  // pbeg + kStages w + s (s < kStages) into its ring, requested before the
+  // history length is known (pages past it are read but never used; ids
+  // outside the pool are never copied).  The CTA's later pages are taken
+  // kGroup at a time from a shared counter as each warp frees its stages,
+  // so a warp whose pages arrive later takes fewer of them.
   const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
-  const int first = pbeg + warp;
   const int spec_end = min(pbeg + p.pages_per_split, p.max_pages);
-  PidWindow issue_ids;
   int hist = p.hist_len[b];
   uint8_t* ring = stage + size_t(warp) * kStages * kBlock;
   uint64_t* bar = bars + warp * kStages;
   const uint8_t* pool = p.pages + int64_t(hkv) * kBlock;
   const int64_t page_stride = int64_t(p.n_kv) * kBlock;
+  int* next_page = s_last + 1;   // the CTA's page counter
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar + s, 1);
     fence_mbar_init();
   }
   __syncwarp();
-  // stage s of the ring holds a copied (in-range) page while bit s is set
-  uint32_t stage_ok = 0u;
-  auto issue = [&](int k, int s) {  // warp-collective; lane 0 starts the copy
-    const int pid = issue_ids.get(k, ptab, first, W, spec_end, lane);
-    const bool good = pid >= 0 && pid < p.n_pages;
-    stage_ok = good ? (stage_ok | (1u << s)) : (stage_ok & ~(1u << s));
-    if (lane == 0) {
-      if (!good) {
+  // lane s < kStages describes ring stage s: the page index it holds (-1:
+  // none) and whether that page was copied (a valid id)
+  int ring_j = pbeg + kStages * warp + lane;
+  ring_j = lane < kStages && ring_j < spec_end ? ring_j : -1;
+  bool ring_ok = false;
+  {
+    const int pid = ring_j >= 0 ? __ldg(ptab + ring_j) : -1;
+    ring_ok = ring_j >= 0 && pid >= 0 && pid < p.n_pages;
+    if (ring_j >= 0) {
+      if (!ring_ok) {
         // no copy: complete the stage's phase without bytes so the ring stays in step
-        mbar_arrive(bar + s);
+        mbar_arrive(bar + lane);
       } else {
-        mbar_arrive_expect_tx(bar + s, kBlock);
-        bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid) * page_stride, kBlock, bar + s);
+        mbar_arrive_expect_tx(bar + lane, kBlock);
+        bulk_copy_g2s(ring + lane * kBlock, pool + int64_t(pid) * page_stride, kBlock, bar + lane);
       }
     }
-  };
-  const int spec_count = spec_end > first ? (spec_end - first + W - 1) / W : 0;
-  const int issued0 = min(spec_count, kStages);
-  for (int k = 0; k < issued0; ++k) issue(k, k);
+  }
+  // stages with an arrival not yet waited for (bit s), and the parity each
+  // stage's next completion has
+  uint32_t pending = __ballot_sync(kFull, ring_j >= 0) & ((1u << kStages) - 1u);
+  uint32_t parity = 0u;
+  if (tid == 0) *next_page = pbeg + kStages * W;
 
   __syncthreads();   // the R_K / R_V / prologue barriers are initialised
 
@@ -1140,7 +1170,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   if (n_pg > n_splits * p.pages_per_split && split == 0 && tid == 0)
     flag(p.dev_status, 0x2);  // longer than the host bound max_hist: tail not read
   const int pend = min(pbeg + p.pages_per_split, n_pg);
-  const int count = pend > first ? (pend - first + W - 1) / W : 0;
+  if (ring_j >= pend) ring_j = -1;   // past the history: copied, never used
 
   // ---------------- q~ and the lane's QK fragments (prologue warps); the
   // BF16 warps scan the sink/recent tokens meanwhile and read the fragments
@@ -1259,73 +1289,97 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   float* my_state = reinterpret_cast<float*>(ring);
 
   constexpr int kGroup = Gm::kGroup;
+  // K and V pairs of a token in one load, kept from QK to PV (one group
+  // each, GQA 4); the other variants load the V pairs again for PV, which
+  // keeps their register budget
+  constexpr bool kJointPairs = NGK == 1 && NGV == 1 && G <= 4;
   // ---------------- INT2 pages, kGroup per step: QK of the step's pages,
-  // one maximum update, then their probabilities and PV.  A page past the
-  // warp's range or with an invalid id is computed on stale ring data with
-  // every token masked (uniform control flow, no effect on the result).
+  // one maximum update, then their probabilities and PV.  The step consumes
+  // ring stages s_cur .. s_cur + kGroup - 1 (mod kStages) and refills them
+  // with the next kGroup pages of the CTA's counter.  Stages run dry in
+  // consumption order (the counter only grows), so the first empty stage of
+  // a step ends the warp's pages.  A page with an invalid id is computed on
+  // stale ring data with every token masked.
   {
     HistState<G, NZ> st;
     st.init();
+    const float lift = float(kRescaleLog2) + p.pv_log2;   // rescale test against st.m (see int2_update_max)
+    const int n_full = hist / kPage;                     // pages below it hold kPage valid tokens
     bool timed_out = false;
-    int k = 0;
-    int s_cur = 0;                 // ring stage of page k
-    uint32_t phase = 0u;           // parity of page k's stage
-    int tok_left = hist - first * kPage;   // history tokens from page k on
-    constexpr uint32_t kGroupBits = (1u << kGroup) - 1u, kRingBits = (1u << kStages) - 1u;
-    // page id of the first in-loop copy of lane u < kGroup (page kStages + u)
-    int pid_next = lane < kGroup && kStages + lane < count ? __ldg(ptab + first + (kStages + lane) * W) : -1;
-    for (; k < count; k += kGroup) {
+    int s_cur = 0;
+    // the next refill, one step ahead: its first page and lane u's page id
+    auto grab = [&]() {
+      int g = 0;
+      if (lane == 0) g = atomicAdd(next_page, kGroup);
+      return __shfl_sync(kFull, g, 0);
+    };
+    int g_next = grab();
+    int pid_next = lane < kGroup && g_next + lane < pend ? __ldg(ptab + g_next + lane) : -1;
+    while (true) {
+      int ju[kGroup];
       const uint8_t* pg[kGroup];
-      // the step is full (warp-uniform) when its kGroup pages are in range,
-      // were copied, and hold kPage valid tokens each
-      uint32_t gmask = kGroupBits << s_cur;
-      gmask = (gmask | (gmask >> kStages)) & kRingBits;
-      const bool all_full = k + kGroup <= count && (stage_ok & gmask) == gmask &&
-                            tok_left - (kGroup - 1) * W * kPage >= kPage;
-      int s_u = s_cur;
-      uint32_t ph_u = phase;
+      const uint32_t ok_bits = __ballot_sync(kFull, ring_ok);
+      bool all_full = true;
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
-        pg[u] = ring + s_u * kBlock;
-        if ((u == 0 || k + u < count) && !mbar_wait_bounded(bar + s_u, ph_u, kWaitLimitNs)) timed_out = true;
-        if (++s_u == kStages) {
-          s_u = 0;
-          ph_u ^= 1u;
+        int su = s_cur + u;
+        if (su >= kStages) su -= kStages;
+        ju[u] = __shfl_sync(kFull, ring_j, su);
+        pg[u] = ring + su * kBlock;
+        all_full = all_full && ju[u] >= 0 && ((ok_bits >> su) & 1u) && ju[u] < n_full;
+      }
+      if (ju[0] < 0) break;
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        int su = s_cur + u;
+        if (su >= kStages) su -= kStages;
+        if (ju[u] >= 0) {
+          if (!mbar_wait_bounded(bar + su, (parity >> su) & 1u, kWaitLimitNs)) {
+            timed_out = true;
+          } else {
+            pending &= ~(1u << su);
+            parity ^= 1u << su;
+          }
         }
       }
       if (timed_out) break;
       // token validity of the lane's two tokens per page (masked steps only)
       bool ok[kGroup][2];
       if (!all_full) {
-        s_u = s_cur;
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
-          const bool in = k + u < count;
-          const bool valid = in && ((stage_ok >> s_u) & 1u);
-          if (in && !valid && lane == 0) flag(p.dev_status, 0x1);
-          const int ntok = valid ? tok_left - u * W * kPage : 0;
+          int su = s_cur + u;
+          if (su >= kStages) su -= kStages;
+          const bool copied = (ok_bits >> su) & 1u;
+          if (ju[u] >= 0 && !copied && lane == 0) flag(p.dev_status, 0x1);
+          const int ntok = ju[u] >= 0 && copied ? hist - kPage * ju[u] : 0;
           ok[u][0] = gid < ntok;
           ok[u][1] = gid + 8 < ntok;
-          if (++s_u == kStages) s_u = 0;
         }
       }
       // QK of the step's pages, one maximum update, probabilities and PV;
       // steps whose tokens are all valid (every step but the history's last
-      // and a warp's tail) take the select-free variant; in the other, pages
-      // past the warp's range are skipped (warp-uniform branches)
+      // and a warp's last) take the select-free variant; in the other, empty
+      // stages are skipped (warp-uniform branches)
       auto step = [&](auto masked) {
         constexpr bool kMasked = decltype(masked)::value;
         float sc[kGroup][NH][2];
+        uint32_t vsz0[kGroup][NGV], vsz1[kGroup][NGV];   // the pages' V (scale, zero) pairs
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
-          if (kMasked && u > 0 && k + u >= count) {
+          if (kMasked && u > 0 && ju[u] < 0) {
 #pragma unroll
             for (int nt = 0; nt < NH; ++nt) sc[u][nt][0] = sc[u][nt][1] = -INFINITY;
             continue;
           }
           uint32_t ksz0[NGK], ksz1[NGK];
-          load_sz<NGK>(pg[u], gid, ksz0);
-          load_sz<NGK>(pg[u], gid + 8, ksz1);
+          if constexpr (kJointPairs) {
+            load_pairs<NGK, NGV>(pg[u], gid, ksz0, vsz0[u]);
+            load_pairs<NGK, NGV>(pg[u], gid + 8, ksz1, vsz1[u]);
+          } else {
+            load_group_pairs<NGK, NGV, 0>(pg[u], gid, ksz0);
+            load_group_pairs<NGK, NGV, 0>(pg[u], gid + 8, ksz1);
+          }
           if constexpr (kLevels) {
             float e[NH][2];
             int2_qk_levels<G>(pg[u], gid, tig, qb, p.coef_k, e);
@@ -1340,21 +1394,22 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
             int2_scores_groups<G, NGK, kMasked>(a, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
           }
         }
-        int2_update_max<G, NZ, kGroup>(sc, st);
+        int2_update_max<G, NZ, kGroup>(sc, st, p.pv_log2, lift);
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
-          if (kMasked && u > 0 && k + u >= count) continue;
-          uint32_t vsz0[NGV], vsz1[NGV];
-          load_sz<NGV>(pg[u] + Gm::kHalfK, gid, vsz0);
-          load_sz<NGV>(pg[u] + Gm::kHalfK, gid + 8, vsz1);
+          if (kMasked && u > 0 && ju[u] < 0) continue;
+          if constexpr (!kJointPairs) {
+            load_group_pairs<NGK, NGV, NGK>(pg[u], gid, vsz0[u]);
+            load_group_pairs<NGK, NGV, NGK>(pg[u], gid + 8, vsz1[u]);
+          }
           if constexpr (kLevels) {
             uint32_t pb[3][NH][2];
-            int2_probs_levels<G, kMasked>(sc[u], vsz0[0], vsz1[0], ok[u][0], ok[u][1], p.sigma_v, p.coef_v, st, pb);
+            int2_probs_levels<G, kMasked>(sc[u], vsz0[u][0], vsz1[u][0], ok[u][0], ok[u][1], p.coef_v, st, pb);
             int2_pv_levels<G>(pg[u], gid, tig, pb, st);
           } else {
             uint32_t pb[NGV][NH][2];
-            int2_probs<G, NGV, kMasked>(sc[u], vsz0, vsz1, ok[u][0], ok[u][1], p.sigma_v, st, pb);
-            int2_pv<G, NGV, Gm::kHalfK>(pg[u], gid, tig, pb, st);
+            int2_probs<G, NGV, kMasked>(sc[u], vsz0[u], vsz1[u], ok[u][0], ok[u][1], st, pb);
+            int2_pv<G, NGV>(pg[u], gid, tig, pb, st);
           }
         }
       };
@@ -1364,15 +1419,13 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         step(std::true_type{});
       }
       __syncwarp();
-      // the freed stages take pages k + kStages + u: lane u < kGroup starts
-      // the copy of page u (ids requested one step ahead), so the kGroup
-      // copies cost one pass of issue instructions
+      // the step's stages take the pages g_next .. g_next + kGroup - 1 (ids
+      // loaded one step ahead): lane u < kGroup starts the copy into stage
+      // s_cur + u, and the stage lanes learn their new page
       {
-        const int kk = k + kStages + lane;
-        const bool want = lane < kGroup && kk < count;
-        const int pid = pid_next;
-        pid_next = lane < kGroup && kk + kGroup < count ? __ldg(ptab + first + (kk + kGroup) * W) : -1;
-        const bool good = want && pid >= 0 && pid < p.n_pages;
+        const int jj = g_next + lane;
+        const bool want = lane < kGroup && jj < pend;
+        const bool good = want && pid_next >= 0 && pid_next < p.n_pages;
         int s = s_cur + lane;
         if (s >= kStages) s -= kStages;
         if (want) {
@@ -1380,34 +1433,31 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
             mbar_arrive(bar + s);   // no copy: complete the phase without bytes
           } else {
             mbar_arrive_expect_tx(bar + s, kBlock);
-            bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid) * page_stride, kBlock, bar + s);
+            bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid_next) * page_stride, kBlock, bar + s);
           }
         }
-        const uint32_t want_bits = __ballot_sync(kFull, want) & kGroupBits;
-        const uint32_t good_bits = __ballot_sync(kFull, good) & kGroupBits;
-        auto to_stages = [&](uint32_t bits) {
-          const uint32_t r = bits << s_cur;
-          return (r | (r >> kStages)) & kRingBits;
-        };
-        stage_ok = (stage_ok & ~to_stages(want_bits)) | to_stages(good_bits);
-        s_cur += kGroup;
-        if (s_cur >= kStages) {
-          s_cur -= kStages;
-          phase ^= 1u;
+        const uint32_t want_bits = __ballot_sync(kFull, want);
+        const uint32_t good_bits = __ballot_sync(kFull, good);
+        int ds = lane - s_cur;
+        if (ds < 0) ds += kStages;
+        if (lane < kStages && ds < kGroup) {
+          ring_j = (want_bits >> ds) & 1u ? g_next + ds : -1;
+          ring_ok = (good_bits >> ds) & 1u;
         }
+        const uint32_t r = (want_bits & ((1u << kGroup) - 1u)) << s_cur;
+        pending |= (r | (r >> kStages)) & ((1u << kStages) - 1u);
+        g_next = grab();
+        pid_next = lane < kGroup && g_next + lane < pend ? __ldg(ptab + g_next + lane) : -1;
+        s_cur += kGroup;
+        if (s_cur >= kStages) s_cur -= kStages;
       }
-      tok_left -= kGroup * W * kPage;
     }
     if (timed_out && lane == 0) flag(p.dev_status, 0x4);
     // copies still in flight (after a timeout, or requested speculatively
-    // past this warp's pages) land before the CTA's shared memory goes away;
-    // each wait is bounded
-    {
-      const int done = timed_out ? k : count;
-      const int req = max(min(count, k + kStages), issued0);
-      for (int kk = done; kk < req; ++kk)
-        mbar_wait_bounded(bar + kk % kStages, (kk / kStages) & 1, kWaitLimitNs);
-    }
+    // past the history) land before the CTA's shared memory goes away; each
+    // wait is bounded
+    for (int s = 0; s < kStages; ++s)
+      if ((pending >> s) & 1u) mbar_wait_bounded(bar + s, (parity >> s) & 1u, kWaitLimitNs);
     __syncwarp();
     if constexpr (kLevels) {
       store_hist_state_levels<G>(st, my_state, gid, tig, p.pv_unscale, p.coef_v[0]);

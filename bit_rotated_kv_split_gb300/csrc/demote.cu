@@ -93,14 +93,14 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
     if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
     return;
   }
-  uint8_t* blk = p.pages + (page * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v) + which * half_bytes(p.ng_k);
-  blk[32 * slot + lane] = uint8_t(byte);
+  uint8_t* blk = p.pages + (page * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v);
+  blk[which ? v_code_byte(slot, lane) : 32 * slot + lane] = uint8_t(byte);
   if (lane < NG) {
     __half2 sz = __halves2half2(s16[0], z16[0]);
 #pragma unroll
     for (int q = 1; q < NG; ++q)
       if (lane == q) sz = __halves2half2(s16[q], z16[q]);
-    *reinterpret_cast<__half2*>(blk + kCodeBytes + 4 * (slot * NG + lane)) = sz;
+    *reinterpret_cast<__half2*>(blk + pair_byte(p.ng_k, p.ng_v, slot, which, lane)) = sz;
   }
 }
 

@@ -181,21 +181,29 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
     }
     w[u] = kLevels ? word : word - kBitsSum;
   }
-  uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v) + which * half_bytes(p.ng_k);
-  *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
+  uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v);
+  if (which == 0) {
+    *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    // V rows interleave the two tokens of a slot pair by 16-bit halves: the
+    // eight halves 8 hh .. 8 hh + 7 of this token go 4 bytes apart
+    uint16_t* dst = reinterpret_cast<uint16_t*>(blk + v_code_byte(m.y, 16 * hh));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      dst[4 * u] = uint16_t(w[u] & 0xFFFFu);
+      dst[4 * u + 2] = uint16_t(w[u] >> 16);
+    }
+  }
   if (hh == 0) {
     uint32_t sz[NG];
 #pragma unroll
     for (int q = 0; q < NG; ++q)
       sz[q] = uint32_t(__half_as_ushort(s16[q])) | (uint32_t(__half_as_ushort(z16[q])) << 16);
-    uint8_t* dst = blk + kCodeBytes + 4 * NG * m.y;
-    if constexpr (NG == 1) {
-      *reinterpret_cast<uint32_t*>(dst) = sz[0];
-    } else if constexpr (NG == 2) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(sz[0], sz[1]);
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(sz[0], sz[1], sz[2], sz[3]);
-    }
+    // (4-byte stores: with K and V pairs side by side a token's pairs are
+    // only 4-byte aligned in general)
+    uint32_t* dst = reinterpret_cast<uint32_t*>(blk + pair_byte(p.ng_k, p.ng_v, m.y, which, 0));
+#pragma unroll
+    for (int q = 0; q < NG; ++q) dst[q] = sz[q];
   }
   return true;
 }

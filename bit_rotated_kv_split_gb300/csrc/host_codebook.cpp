@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "oscar.h"
+#include "trace.h"
 
 namespace {
 
@@ -36,6 +37,7 @@ double round_fp16(double x) {
 
 extern "C" oscar_status oscar_fit_codebook(const double* x, int64_t n, int32_t d, const double* r, double tau,
                                            int32_t iters, float* levels_out) {
+  OSCAR_TRACE_CALL();
   if (!x || !r || !levels_out || n < 1 || d != OSCAR_HEAD_DIM || !(tau > 0.0) || !std::isfinite(tau) || iters < 1)
     return OSCAR_ERR_INVALID_ARG;
   std::vector<double> u;

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "oscar.h"
+#include "trace.h"
 
 namespace {
 
@@ -129,6 +130,7 @@ oscar_status rotation_from_cov(std::vector<double>& c, int d, double* r_out, dou
 
 extern "C" oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t d, double* r_out,
                                              double* eigvals_out) {
+  OSCAR_TRACE_CALL();
   if (!x || !r_out || n < 1 || d < 2 || d > 1024 || !is_pow2(d)) return OSCAR_ERR_INVALID_ARG;
   // C = x^T x / n (uncentred)
   std::vector<double> c(size_t(d) * d, 0.0);
@@ -152,6 +154,7 @@ extern "C" oscar_status oscar_build_rotation(const double* x, int64_t n, int32_t
 // device): the symmetric part (c + c^T) / 2 is decomposed.
 extern "C" oscar_status oscar_build_rotation_from_covariance(const double* c, int32_t d, double* r_out,
                                                              double* eigvals_out) {
+  OSCAR_TRACE_CALL();
   if (!c || !r_out || d < 2 || d > 1024 || !is_pow2(d)) return OSCAR_ERR_INVALID_ARG;
   std::vector<double> a(size_t(d) * d);
   for (int i = 0; i < d; ++i)
@@ -166,6 +169,7 @@ extern "C" oscar_status oscar_build_rotation_from_covariance(const double* c, in
 extern "C" oscar_status oscar_score_weighted_rows(const double* q, int64_t n_q, const double* k,
                                                   const double* v, int64_t n_k, int32_t d,
                                                   double scale, double* out) {
+  OSCAR_TRACE_CALL();
   if (!q || !k || !v || !out || n_q < 1 || n_k < 1 || d < 1) return OSCAR_ERR_INVALID_ARG;
   std::vector<double> s(static_cast<size_t>(n_k));
   for (int64_t r = 0; r < n_q; ++r) {
@@ -197,6 +201,7 @@ extern "C" oscar_status oscar_score_weighted_rows(const double* q, int64_t n_q, 
 extern "C" oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_heads,
                                              int32_t d, const double* r, double quantile,
                                              double* tau_out) {
+  OSCAR_TRACE_CALL();
   if (!acts || !r || !tau_out || rows < 1 || n_heads < 1 || d < 1 || !(quantile > 0.0) ||
       quantile > 1.0)
     return OSCAR_ERR_INVALID_ARG;
@@ -224,6 +229,7 @@ extern "C" oscar_status oscar_clip_threshold(const double* acts, int64_t rows, i
 // OScaR variant ([CSDN] section 四.2): channels split into groups of `block`,
 // each rotated by the orthonormal Sylvester Hadamard of that size.
 extern "C" oscar_status oscar_build_canalized_rotation(int32_t d, int32_t block, double* r_out) {
+  OSCAR_TRACE_CALL();
   if (!r_out || d < 1 || d > 1024 || !is_pow2(d) || block < 1 || block > d || !is_pow2(block))
     return OSCAR_ERR_INVALID_ARG;
   const double inv = 1.0 / std::sqrt(double(block));

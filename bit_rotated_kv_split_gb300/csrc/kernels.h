@@ -10,13 +10,26 @@ namespace oscar {
 
 constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
-constexpr int kCodeBytes = 512;   // 16 token rows of 32 code bytes at the start of a half
-// A half with ng quantisation groups per token-head: the code rows, then
-// 16 x ng (scale, zero) fp16 pairs; a block is the K half then the V half.
-constexpr int half_bytes(int ng) { return kCodeBytes + 64 * ng; }
-constexpr int block_bytes(int ng_k, int ng_v) { return half_bytes(ng_k) + half_bytes(ng_v); }
+// Page block of one (physical page, KV head) with ng_k / ng_v quantisation
+// groups per K / V vector:
+//   [0, 512)     K code rows: token slot t, code byte l at 32 t + l;
+//   [512, 1024)  V code rows interleaved by token pair: token slot t, code
+//                byte l at 512 + 64 (t / 2) + 4 (l / 2) + 2 (t % 2) + l % 2,
+//                so the 32-bit word at 512 + 64 a + 4 h holds 16-bit half h
+//                (code positions 8h .. 8h+7) of slots 2a (low) and 2a + 1;
+//   [1024, ...)  per token slot t, its ng_k K (scale, zero) fp16 pairs and
+//                then its ng_v V pairs, at 1024 + 4 (ng_k + ng_v) t.
+constexpr int kCodeBytes = 512;   // 16 token rows of 32 code bytes (K, and V)
+constexpr int kVCodes = 512;      // offset of the V code rows
+constexpr int kPairs = 1024;      // offset of the (scale, zero) pairs
+constexpr int block_bytes(int ng_k, int ng_v) { return kPairs + 64 * (ng_k + ng_v); }
 constexpr int kBlockBytes = block_bytes(1, 1);   // 1152: one group per token-head
-constexpr int kHalfBytes = half_bytes(1);        // 576
+__host__ __device__ constexpr int v_code_byte(int t, int l) {
+  return kVCodes + 64 * (t >> 1) + 4 * (l >> 1) + 2 * (t & 1) + (l & 1);
+}
+__host__ __device__ constexpr int pair_byte(int ng_k, int ng_v, int t, int which, int q) {
+  return kPairs + 4 * (ng_k + ng_v) * t + 4 * (which ? ng_k : 0) + 4 * q;
+}
 
 // Rotated channel held by code position c of a token row with ng groups
 // (ng = 1: c itself).  K: c = 32 t + 8 e + j holds (j / J) g + (j % J) 16 +
@@ -147,8 +160,11 @@ struct DecodeParams {
   int32_t max_hist;
   // split plan
   int32_t n_splits, pages_per_split;
-  // scale of the PV B operand (power of two) and 2^24 / sigma_v
-  float sigma_v, pv_unscale;
+  // the PV B operand is p s_V 2^pv_log2 (an integer pv_log2 keeps it in the
+  // fp16 range): the INT2 states carry that factor in every term and keep
+  // their maximum lowered by pv_log2; pv_unscale = 2^24 undoes the codes'
+  // subnormal scale
+  float pv_log2, pv_unscale;
   // R_V as a 2-D tensor (128 columns x n_kv * 128 rows of fp32) read in
   // boxes of 32 columns x 128 rows with the 128-byte swizzle
   CUtensorMap tm_rv;

@@ -7,6 +7,7 @@
 
 #include "kernels.h"
 #include "oscar.h"
+#include "trace.h"
 
 namespace {
 
@@ -99,6 +100,7 @@ extern "C" const char* oscar_status_string(oscar_status s) {
     case OSCAR_ERR_CUDA: return "CUDA error";
     case OSCAR_ERR_NO_CONVERGENCE: return "eigensolver did not converge";
     case OSCAR_ERR_UNSUPPORTED: return "unsupported configuration";
+    case OSCAR_ERR_FILE: return "file missing, unreadable, truncated or damaged";
     default: return "unknown status";
   }
 }
@@ -241,14 +243,14 @@ oscar_status prepare_decode(const oscar_layer_desc* desc, const uint16_t* q, flo
   p.n_splits = plan.n_splits;
   p.pages_per_split = plan.pages_per_split;
   // PV operand scale: p <= 2^kRescaleLog2 and s_V <= 2 tau_v / 3 (x2 margin
-  // for fp16 rounding), so p s_V sigma_v stays below 2^14 in fp16
+  // for fp16 rounding), so p s_V 2^pv_log2 stays below 2^14 in fp16
   int e = 0;
   std::frexp(std::ldexp(double(desc->tau_v) * (2.0 / 3.0) * 2.0, oscar::kRescaleLog2), &e);
   // (codebook 1: the PV operands are p s_V times level coefficients of
   // magnitude up to 3, so the scale is 8 times smaller)
   const int sig_exp = 14 - e - (desc->codebook ? 3 : 0);
-  p.sigma_v = std::ldexp(1.0f, sig_exp);
-  p.pv_unscale = std::ldexp(1.0f, 24 - sig_exp);
+  p.pv_log2 = float(sig_exp);
+  p.pv_unscale = std::ldexp(1.0f, 24);
   if (!oscar::encode_rv_map(&p)) return OSCAR_ERR_CUDA;
   *pout = p;
   return OSCAR_OK;
@@ -263,6 +265,7 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
                                               const int32_t* dst_pos, int32_t n,
                                               const uint16_t* new_k, const uint16_t* new_v,
                                               void* stream) {
+  OSCAR_TRACE_CALL();
   oscar::DemoteParams p{};
   bool empty = false;
   const oscar_status st = prepare_append(desc, k_src, v_src, src_rows, row_stride, src_index, dst_req, dst_pos, n,
@@ -274,6 +277,7 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
 extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
                                                float* out, void* workspace,
                                                size_t* workspace_bytes, void* stream) {
+  OSCAR_TRACE_CALL();
   oscar::DecodeParams p{};
   bool size_only = false;
   const oscar_status st = prepare_decode(desc, q, out, workspace, workspace_bytes, &p, &size_only);
@@ -287,6 +291,7 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
                                           const int32_t* dst_pos, int32_t n, const uint16_t* new_k,
                                           const uint16_t* new_v, const uint16_t* q, float* out, void* workspace,
                                           size_t workspace_bytes, float* host_out, void* stream) {
+  OSCAR_TRACE_CALL();
   if ((in_bytes > 0) != (host_in != nullptr && dev_in != nullptr)) return OSCAR_ERR_INVALID_ARG;
   if (!workspace) return OSCAR_ERR_WORKSPACE;
   if ((in_bytes > 0 && !device_addressable_host(host_in)) || (host_out && !device_addressable_host(host_out)))
@@ -317,6 +322,7 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
 // [GIST] 2.1 / 2.2 A: C_Q and C_S as one contraction over calibration rows.
 extern "C" oscar_status oscar_covariance(const uint16_t* x, int64_t n, int32_t d, int64_t ld, float* c_out,
                                          void* workspace, size_t* workspace_bytes, void* stream) {
+  OSCAR_TRACE_CALL();
   if (!workspace_bytes || n < 1 || d != 128 || ld < d) return OSCAR_ERR_INVALID_ARG;
   const size_t need = oscar::covariance_workspace_bytes(n);
   if (!workspace) {

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "oscar.h"
+#include "trace.h"
 
 namespace {
 
@@ -68,6 +69,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 extern "C" oscar_status oscar_decode_attention_static(const oscar_layer_desc* desc, const uint16_t* q,
                                                       float* out, void* stream) {
+  OSCAR_TRACE_CALL();
   if (!desc) return OSCAR_ERR_INVALID_ARG;
   size_t need = 0;
   oscar_status st = oscar_decode_attention(desc, q, out, nullptr, &need, stream);

@@ -34,14 +34,18 @@
  *
  * Page pool layout (this library's format; the pages fix only "paged KV",
  * "4 codes per byte" and "scale/zero point"), with G_K = 128 / g_K and
- * G_V = 128 / g_V groups per vector:
- *   half(G) = 512 + 64 G bytes: 16 tokens x 32 code bytes, then 16 x G
- *   (scale, zero) fp16 pairs, token-major: pair (slot t, group q) at
- *   512 + 4 (t G + q).  A block is a K half(G_K) then a V half(G_V) (1152
- *   bytes with one group each, OSCAR_BLOCK_BYTES); block (page p, head h) at
- *   byte (p * n_kv_heads + h) * block.  Token slot t of a half: codes at 32 t;
- *   code position c (byte c / 4, bits 2 (c % 4)) holds rotated channel c
- *   when G = 1.  When G > 1 it holds channel
+ * G_V = 128 / g_V groups per vector.  A block of one (page p, KV head h)
+ * has 1024 + 64 (G_K + G_V) bytes (1152 with one group each,
+ * OSCAR_BLOCK_BYTES) and sits at byte (p * n_kv_heads + h) * block:
+ *   [0, 512)     K code rows: token slot t, code byte l at 32 t + l;
+ *   [512, 1024)  V code rows, the two tokens of a slot pair interleaved by
+ *                16-bit halves: token slot t, code byte l at
+ *                512 + 64 (t / 2) + 4 (l / 2) + 2 (t % 2) + (l % 2);
+ *   [1024, ...)  token slot t: its G_K K (scale, zero) fp16 pairs, then its
+ *                G_V V pairs, at 1024 + 4 (G_K + G_V) t.
+ *   Code byte l of a token row holds code positions 4l .. 4l+3 (bits
+ *   2 (c % 4)); position c holds rotated channel c when G = 1.  When G > 1
+ *   it holds channel
  *     K: c = 32 t + 8 e + j (t, e < 4, j < 8):  (j / J) g + (j % J) 16 + 4 t + e,
  *     V: c = 16 a + 8 e + m (a < 8, e < 2, m < 8): (m / M) g + (m % M) 16 + 2 a + e,
  *   with J = M = 8 / G, so that each tensor-core operand tile of the decode
@@ -59,12 +63,11 @@
 extern "C" {
 #endif
 
-#define OSCAR_ABI_VERSION 3
+#define OSCAR_ABI_VERSION 4
 
 #define OSCAR_HEAD_DIM 128
 #define OSCAR_PAGE_TOKENS 16
 #define OSCAR_BLOCK_BYTES 1152
-#define OSCAR_HALF_BYTES 576
 
 typedef int32_t oscar_status;
 enum {
@@ -74,7 +77,9 @@ enum {
   OSCAR_ERR_WORKSPACE = 3,       /* workspace missing or too small            */
   OSCAR_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed      */
   OSCAR_ERR_NO_CONVERGENCE = 5,  /* the host eigensolver did not converge     */
-  OSCAR_ERR_UNSUPPORTED = 6      /* a valid but unimplemented configuration   */
+  OSCAR_ERR_UNSUPPORTED = 6,     /* a valid but unimplemented configuration   */
+  OSCAR_ERR_FILE = 7             /* a file missing, unreadable, truncated or   */
+                                 /* failing its format or checksum check       */
 };
 
 /* Bits a kernel ORs into *dev_status (never cleared by the library). */
@@ -247,6 +252,29 @@ oscar_status oscar_clip_threshold(const double* acts, int64_t rows, int32_t n_he
  */
 oscar_status oscar_fit_codebook(const double* x, int64_t n, int32_t d, const double* r, double tau,
                                 int32_t iters, float* levels_out);
+
+/*
+ * Rotation files: a model's fixed rotations and clip thresholds, computed
+ * once offline, stored for serving start-up.  [ZAKER] closing part (the
+ * release ships a zoo of precomputed per-layer rotations); [GIST] 2.2 A
+ * (R and the thresholds are fixed per layer after calibration).
+ *
+ *   Layout (little-endian): "OSCARROT", u32 version 1, u32 n_layers, u32
+ *   n_kv_heads, u32 d; per layer f32 tau_k, f32 tau_v, R_K [n_kv][d][d] f32,
+ *   R_V [n_kv][d][d] f32; then the 64-bit FNV-1a hash of all bytes before it.
+ *   r_k / r_v (host) are [n_layers][n_kv][d][d] row-major, tau_k / tau_v
+ *   (host) [n_layers].  write creates or replaces the file; info reads the
+ *   dimensions; read checks the magic, version, dimensions (the caller's
+ *   must equal the file's, else OSCAR_ERR_INVALID_ARG), size and hash before
+ *   it writes any output.  OSCAR_ERR_FILE for an unreadable, truncated or
+ *   damaged file.  Host-only, synchronous.
+ */
+oscar_status oscar_rotation_file_write(const char* path, int32_t n_layers, int32_t n_kv_heads, int32_t d,
+                                       const float* r_k, const float* r_v, const float* tau_k,
+                                       const float* tau_v);
+oscar_status oscar_rotation_file_info(const char* path, int32_t* n_layers, int32_t* n_kv_heads, int32_t* d);
+oscar_status oscar_rotation_file_read(const char* path, int32_t n_layers, int32_t n_kv_heads, int32_t d,
+                                      float* r_k, float* r_v, float* tau_k, float* tau_v);
 
 /*
  * oscar_quantize_append - the fused demotion kernel: rotate, clip, quantise

@@ -59,11 +59,13 @@ D_DEFAULT = 128
 PAGE_TOKENS = 16
 SINK_CAP = 64
 RECENT_CAP = 256
-# Page block of one (physical page, KV head): K half then V half; each half is
-# 16 tokens x 32 code bytes followed by 16 (scale, zero) fp16 pairs.
+# Page block of one (physical page, KV head): 16 K code rows of 32 bytes, 16
+# V code rows of 32 bytes (interleaved by token pair), then the (scale, zero)
+# fp16 pairs of the 16 tokens (section 3).
 CODE_BYTES = 32
-HALF_BYTES = PAGE_TOKENS * CODE_BYTES + PAGE_TOKENS * 4     # 576
-BLOCK_BYTES = 2 * HALF_BYTES                                # 1152
+CODES_BYTES = PAGE_TOKENS * CODE_BYTES                      # 512 per K or V
+SZ_OFFSET = 2 * CODES_BYTES                                  # 1024
+BLOCK_BYTES = SZ_OFFSET + PAGE_TOKENS * 2 * 4                # 1152 (one group each)
 
 
 # --------------------------------------------------------------------------
@@ -354,89 +356,43 @@ def unpack(packed: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 # 3. paged history layout (this build's format; the pages fix only "paged")
 # --------------------------------------------------------------------------
+#
+# Block of one (physical page, KV head) with G_K groups per K vector and G_V
+# per V vector (1, 2 or 4 each), 1024 + 64 (G_K + G_V) bytes:
+#   K codes  [0, 512):     token slot t, code byte l at 32 t + l;
+#   V codes  [512, 1024):  token slot t, code byte l at
+#                          512 + 64 (t // 2) + 4 (l // 2) + 2 (t % 2) + (l % 2),
+#                          i.e. the two tokens of a slot pair alternate by
+#                          16-bit halves (8 codes each);
+#   pairs    [1024, ...):  token slot t holds its G_K K (scale, zero) fp16
+#                          pairs, then its G_V V pairs, at 1024 + 4 (G_K + G_V) t.
+# Code byte l of a token row holds code positions 4l .. 4l+3 (bits 2i..2i+1);
+# position p holds rotated channel storage_channel(which, G, p).
 
-def block_offset(page_id: int, kv_head: int, n_kv: int) -> int:
+
+def block_bytes(ng_k: int = 1, ng_v: int = 1) -> int:
+    """Bytes of one (page, KV head) block with ng_k / ng_v groups per vector."""
+    return SZ_OFFSET + PAGE_TOKENS * 4 * (ng_k + ng_v)
+
+
+def block_offset(page_id: int, kv_head: int, n_kv: int, ng_k: int = 1, ng_v: int = 1) -> int:
     """Byte offset of the block of (physical page, KV head) inside the pool."""
-    return (int(page_id) * n_kv + int(kv_head)) * BLOCK_BYTES
+    return (int(page_id) * n_kv + int(kv_head)) * block_bytes(ng_k, ng_v)
 
 
-def token_offsets(slot: int, which: int):
-    """(code offset, scale offset) of a token slot within a block; which 0 = K, 1 = V."""
-    base = which * HALF_BYTES
-    return base + slot * CODE_BYTES, base + PAGE_TOKENS * CODE_BYTES + 4 * slot
+def code_byte_offset(which: int, slot, byte):
+    """Offset within a block of code byte `byte` of token `slot`; which 0 = K, 1 = V."""
+    slot = np.asarray(slot)
+    byte = np.asarray(byte)
+    if which == 0:
+        return slot * CODE_BYTES + byte
+    return CODES_BYTES + 64 * (slot // 2) + 4 * (byte // 2) + 2 * (slot % 2) + (byte % 2)
 
 
-def store_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
-                  kv_head: int, which: int, packed: np.ndarray, scale16, zero16) -> None:
-    """Place one token's packed codes and (scale, zero) at history position `pos`.
-
-    The page is page_table[b][pos // 16], the slot pos % 16.   [GIST] 2.2 B
-    (paged KV cache).  `pool` is a flat uint8 array of n_pages * n_kv * 1152.
-    """
-    page = int(page_table[b, pos // PAGE_TOKENS])
-    base = block_offset(page, kv_head, n_kv)
-    co, so = token_offsets(pos % PAGE_TOKENS, which)
-    pool[base + co: base + co + CODE_BYTES] = packed
-    pair = np.array([scale16, zero16], dtype=np.float16).view(np.uint8)
-    pool[base + so: base + so + 4] = pair
-
-
-def load_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
-                 kv_head: int, which: int):
-    """(packed[32], scale float16, zero float16) stored for a history position."""
-    page = int(page_table[b, pos // PAGE_TOKENS])
-    base = block_offset(page, kv_head, n_kv)
-    co, so = token_offsets(pos % PAGE_TOKENS, which)
-    packed = pool[base + co: base + co + CODE_BYTES].copy()
-    sz = pool[base + so: base + so + 4].copy().view(np.float16)
-    return packed, sz[0], sz[1]
-
-
-def store_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
-                       pos0: int, packed: np.ndarray, scale16: np.ndarray,
-                       zero16: np.ndarray, which: int) -> None:
-    """store_history for tokens pos0 .. pos0+T-1 of all KV heads: packed[T][n_kv][32]."""
-    t_count = packed.shape[0]
-    pos = pos0 + np.arange(t_count)
-    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
-    slots = pos % PAGE_TOKENS
-    heads = np.arange(n_kv)
-    base = (pages[:, None] * n_kv + heads[None, :]) * BLOCK_BYTES          # [T][n_kv]
-    co = base + which * HALF_BYTES + slots[:, None] * CODE_BYTES
-    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slots[:, None]
-    idx = co[..., None] + np.arange(CODE_BYTES)
-    pool[idx] = packed
-    pair = np.stack([scale16, zero16], axis=-1).astype(np.float16).view(np.uint8)  # [T][n_kv][4]
-    pool[so[..., None] + np.arange(4)] = pair
-
-
-def load_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
-                      hist_len: int, which: int):
-    """(codes [T][n_kv][d] uint8, scale [T][n_kv] f16, zero [T][n_kv] f16) for positions < hist_len."""
-    pos = np.arange(hist_len)
-    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
-    slots = pos % PAGE_TOKENS
-    heads = np.arange(n_kv)
-    base = (pages[:, None] * n_kv + heads[None, :]) * BLOCK_BYTES
-    co = base + which * HALF_BYTES + slots[:, None] * CODE_BYTES
-    so = base + which * HALF_BYTES + PAGE_TOKENS * CODE_BYTES + 4 * slots[:, None]
-    packed = pool[co[..., None] + np.arange(CODE_BYTES)]
-    sz = pool[so[..., None] + np.arange(4)].copy().view(np.float16)      # [T][n_kv][2]
-    return unpack(packed), sz[..., 0], sz[..., 1]
-
-
-# Grouped format.  A half (K or V) of a block with ng groups per token-head
-# holds 16 token rows of 32 code bytes, then 16 x ng (scale, zero) fp16
-# pairs, token-major: pair (slot, q) at 512 + 4 (slot ng + q).  One group per
-# token-head is exactly the format above.
-
-def half_bytes(ng: int) -> int:
-    """Bytes of one half of a block with ng quantisation groups per token-head."""
-    return PAGE_TOKENS * CODE_BYTES + PAGE_TOKENS * 4 * ng
-
-
-def block_bytes(ng_k: int, ng_v: int) -> int:
-    return half_bytes(ng_k) + half_bytes(ng_v)
+def pair_offset(which: int, slot, q, ng_k: int = 1, ng_v: int = 1):
+    """Offset within a block of the (scale, zero) pair of group q of token `slot`."""
+    first = 0 if which == 0 else ng_k
+    return SZ_OFFSET + 4 * (ng_k + ng_v) * np.asarray(slot) + 4 * (first + np.asarray(q))
 
 
 def storage_channel(which: int, ng: int, p: int) -> int:
@@ -466,46 +422,83 @@ def storage_order(which: int, ng: int) -> np.ndarray:
     return np.array([storage_channel(which, ng, p) for p in range(D_DEFAULT)], dtype=np.int64)
 
 
+def _block_bases(page_table, n_kv, b, pos, ng_k, ng_v):
+    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
+    return (pages[:, None] * n_kv + np.arange(n_kv)[None, :]) * block_bytes(ng_k, ng_v)   # [T][n_kv]
+
+
 def store_history_groups(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos0: int,
                          codes: np.ndarray, scale16: np.ndarray, zero16: np.ndarray, which: int,
                          ng_k: int, ng_v: int) -> None:
-    """Tokens pos0 .. pos0+T-1 of all KV heads into the grouped format.
+    """Tokens pos0 .. pos0+T-1 of all KV heads (history positions of request b).
 
     codes [T][n_kv][128] in channel order, scale16 / zero16 [T][n_kv][ng].
+    The page is page_table[b][pos // 16], the slot pos % 16.  [GIST] 2.2 B
+    (paged KV cache).
     """
     ng = ng_k if which == 0 else ng_v
-    blk = block_bytes(ng_k, ng_v)
-    half0 = 0 if which == 0 else half_bytes(ng_k)
-    t_count = codes.shape[0]
-    pos = pos0 + np.arange(t_count)
-    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
-    slots = pos % PAGE_TOKENS
-    base = (pages[:, None] * n_kv + np.arange(n_kv)[None, :]) * blk + half0        # [T][n_kv]
-    packed = pack(np.asarray(codes)[..., storage_order(which, ng)])
-    co = base + slots[:, None] * CODE_BYTES
-    pool[co[..., None] + np.arange(CODE_BYTES)] = packed
-    pair = np.stack([scale16, zero16], axis=-1).astype(np.float16).view(np.uint8)   # [T][n_kv][4 ng]
-    so = base + PAGE_TOKENS * CODE_BYTES + 4 * ng * slots[:, None]
-    pool[so[..., None] + np.arange(4 * ng)] = pair.reshape(pair.shape[0], pair.shape[1], 4 * ng)
+    pos = pos0 + np.arange(np.asarray(codes).shape[0])
+    slots = (pos % PAGE_TOKENS)[:, None, None]
+    base = _block_bases(page_table, n_kv, b, pos, ng_k, ng_v)[..., None]
+    packed = pack(np.asarray(codes)[..., storage_order(which, ng)])              # [T][n_kv][32]
+    pool[base + code_byte_offset(which, slots, np.arange(CODE_BYTES))] = packed
+    pair = np.stack([np.asarray(scale16).reshape(packed.shape[0], n_kv, ng),
+                     np.asarray(zero16).reshape(packed.shape[0], n_kv, ng)], axis=-1)
+    pair = pair.astype(np.float16).view(np.uint8).reshape(packed.shape[0], n_kv, 4 * ng)
+    so = base + pair_offset(which, slots, 0, ng_k, ng_v)
+    pool[so + np.arange(4 * ng)] = pair
 
 
 def load_history_groups(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
                         hist_len: int, which: int, ng_k: int, ng_v: int):
     """(codes [T][n_kv][128] channel order, scale [T][n_kv][ng], zero [T][n_kv][ng])."""
     ng = ng_k if which == 0 else ng_v
-    blk = block_bytes(ng_k, ng_v)
-    half0 = 0 if which == 0 else half_bytes(ng_k)
     pos = np.arange(hist_len)
-    pages = page_table[b, pos // PAGE_TOKENS].astype(np.int64)
-    slots = pos % PAGE_TOKENS
-    base = (pages[:, None] * n_kv + np.arange(n_kv)[None, :]) * blk + half0
-    stored = unpack(pool[(base + slots[:, None] * CODE_BYTES)[..., None] + np.arange(CODE_BYTES)])
+    slots = (pos % PAGE_TOKENS)[:, None, None]
+    base = _block_bases(page_table, n_kv, b, pos, ng_k, ng_v)[..., None]
+    stored = unpack(pool[base + code_byte_offset(which, slots, np.arange(CODE_BYTES))])
     codes = np.empty_like(stored)
     codes[..., storage_order(which, ng)] = stored
-    so = base + PAGE_TOKENS * CODE_BYTES + 4 * ng * slots[:, None]
-    sz = pool[so[..., None] + np.arange(4 * ng)].copy().view(np.float16)
+    so = base + pair_offset(which, slots, 0, ng_k, ng_v)
+    sz = pool[so + np.arange(4 * ng)].copy().view(np.float16)
     sz = sz.reshape(sz.shape[0], sz.shape[1], ng, 2)
     return codes, sz[..., 0], sz[..., 1]
+
+
+def store_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
+                       pos0: int, packed: np.ndarray, scale16: np.ndarray,
+                       zero16: np.ndarray, which: int) -> None:
+    """One group per vector: packed[T][n_kv][32] codes, scale16 / zero16 [T][n_kv]."""
+    store_history_groups(pool, page_table, n_kv, b, pos0, unpack(packed), np.asarray(scale16)[..., None],
+                         np.asarray(zero16)[..., None], which, 1, 1)
+
+
+def load_history_bulk(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int,
+                      hist_len: int, which: int):
+    """(codes [T][n_kv][d] uint8, scale [T][n_kv] f16, zero [T][n_kv] f16) for positions < hist_len."""
+    codes, s, z = load_history_groups(pool, page_table, n_kv, b, hist_len, which, 1, 1)
+    return codes, s[..., 0], z[..., 0]
+
+
+def store_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
+                  kv_head: int, which: int, packed: np.ndarray, scale16, zero16) -> None:
+    """One token's packed codes [32] and (scale, zero) of one KV head at history position `pos`."""
+    base = block_offset(page_table[b, pos // PAGE_TOKENS], kv_head, n_kv)
+    slot = pos % PAGE_TOKENS
+    pool[base + code_byte_offset(which, slot, np.arange(CODE_BYTES))] = packed
+    so = base + int(pair_offset(which, slot, 0))
+    pool[so: so + 4] = np.array([scale16, zero16], dtype=np.float16).view(np.uint8)
+
+
+def load_history(pool: np.ndarray, page_table: np.ndarray, n_kv: int, b: int, pos: int,
+                 kv_head: int, which: int):
+    """(packed[32], scale float16, zero float16) stored for a history position."""
+    base = block_offset(page_table[b, pos // PAGE_TOKENS], kv_head, n_kv)
+    slot = pos % PAGE_TOKENS
+    packed = pool[base + code_byte_offset(which, slot, np.arange(CODE_BYTES))].copy()
+    so = base + int(pair_offset(which, slot, 0))
+    sz = pool[so: so + 4].copy().view(np.float16)
+    return packed, sz[0], sz[1]
 
 
 # --------------------------------------------------------------------------

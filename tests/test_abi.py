@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol(built_lib):
 
 def test_version_and_status_strings(built_lib):
     from bit_rotated_kv_split_gb300 import binding as B
-    assert B.oscar_abi_version() == 3
+    assert B.oscar_abi_version() == 4
     assert B.oscar_status_string(0) == "ok"
     assert B.oscar_status_string(3).startswith("workspace")
 
@@ -304,3 +304,78 @@ def test_fit_codebook_leaves_output_untouched_when_levels_collapse(built_lib):
     out = np.full(4, -7.0, np.float32)
     assert B.lib.oscar_fit_codebook(x.ctypes.data, 20, 128, eye.ctypes.data, 3.0, 50, out.ctypes.data) == 1
     np.testing.assert_array_equal(out, np.full(4, -7.0, np.float32))
+
+
+def test_calls_are_traced_as_nvtx_ranges(tmp_path):
+    """Every library call shows as one named NVTX range: a recording NVTX
+    injection library (tests/nvtx/record_ranges.c, built here with gcc)
+    sees a push named after each host call and a matching pop."""
+    import shutil
+    import subprocess
+    import sys
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    from bit_rotated_kv_split_gb300 import build as _b
+    lib_path = _b.ensure_built()
+    inj = tmp_path / "librecord.so"
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(_b._nvcc())), "include")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "nvtx", "record_ranges.c")
+    subprocess.run([gcc, "-shared", "-fPIC", "-O1", "-I", cuda_inc, src, "-o", str(inj)], check=True)
+    log = tmp_path / "ranges.txt"
+    code = (
+        "import ctypes, numpy as np\n"
+        "lib = ctypes.CDLL(%r)\n"
+        "x = np.random.default_rng(0).standard_normal((64, 8))\n"
+        "r = np.zeros((8, 8)); e = np.zeros(8)\n"
+        "assert lib.oscar_build_rotation(x.ctypes.data, ctypes.c_int64(64), 8, r.ctypes.data, e.ctypes.data) == 0\n"
+        "assert lib.oscar_build_canalized_rotation(8, 4, r.ctypes.data) == 0\n" % str(lib_path))
+    env = dict(os.environ, NVTX_INJECTION64_PATH=str(inj), OSCAR_NVTX_LOG=str(log))
+    subprocess.run([sys.executable, "-c", code], check=True, env=env)
+    lines = log.read_text().split("\n")
+    assert "push oscar_build_rotation" in lines and "push oscar_build_canalized_rotation" in lines
+    assert lines.count("pop") == sum(1 for ln in lines if ln.startswith("push "))
+
+
+def _q_orthogonal(g, d):
+    q, r = np.linalg.qr(g.standard_normal((d, d)))
+    return q * np.sign(np.diag(r))
+
+
+def test_rotation_file_round_trip_and_damage(tmp_path, built_lib):
+    """A rotation file written with the library reads back bit for bit; a
+    flipped byte, a cut-short file, a foreign file and a dimension mismatch
+    are refused before any output is written."""
+    from bit_rotated_kv_split_gb300 import binding as B
+    g = synth.generator(12, 1)
+    n_layers, n_kv, d = 3, 2, 128
+    rk = np.stack([np.stack([_q_orthogonal(g, d) for _ in range(n_kv)]) for _ in range(n_layers)]).astype(np.float32)
+    rv = np.stack([np.stack([_q_orthogonal(g, d) for _ in range(n_kv)]) for _ in range(n_layers)]).astype(np.float32)
+    tk = g.uniform(5, 20, n_layers).astype(np.float32)
+    tv = g.uniform(5, 20, n_layers).astype(np.float32)
+    path = str(tmp_path / "rot.bin")
+    B.oscar_rotation_file_write(path, rk, rv, tk, tv)
+    raw = open(path, "rb").read()
+    assert raw[:8] == b"OSCARROT" and len(raw) == 8 + 16 + n_layers * (8 + 8 * n_kv * d * d) + 8
+    assert np.frombuffer(raw[8:24], np.uint32).tolist() == [1, n_layers, n_kv, d]
+    got = B.oscar_rotation_file_read(path)
+    for a, b in zip(got, (rk, rv, tk, tv)):
+        np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+    # layer 1, KV head 0, R_K[5][7] sits at a fixed offset
+    off = 24 + (8 + 8 * n_kv * d * d) + 8 + 4 * (5 * d + 7)
+    assert np.frombuffer(raw[off:off + 4], np.float32)[0] == rk[1, 0, 5, 7]
+    out = np.full(n_layers, -1.0, np.float32)
+    big = np.zeros((n_layers, n_kv, d, d), np.float32)
+    damaged = [bytearray(raw), raw[:-9], b"NOTAROTATIONFILE" + raw[16:]]
+    damaged[0][1000] ^= 0x10
+    for i, bad in enumerate(damaged):
+        p = str(tmp_path / ("bad%d.bin" % i))
+        open(p, "wb").write(bytes(bad))
+        st = B.lib.oscar_rotation_file_read(os.fsencode(p), n_layers, n_kv, d, big.ctypes.data, big.ctypes.data,
+                                            out.ctypes.data, out.ctypes.data)
+        assert st == 7, (i, st)
+        assert np.all(out == -1.0) and not big.any()
+    assert B.lib.oscar_rotation_file_read(os.fsencode(path), n_layers, n_kv + 1, d, big.ctypes.data,
+                                          big.ctypes.data, out.ctypes.data, out.ctypes.data) == 1
+    assert B.lib.oscar_rotation_file_read(os.fsencode(str(tmp_path / "missing.bin")), n_layers, n_kv, d,
+                                          big.ctypes.data, big.ctypes.data, out.ctypes.data, out.ctypes.data) == 7

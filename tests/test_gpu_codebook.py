@@ -50,7 +50,7 @@ def test_demote_per_token_kernel_codebook():
 
 
 def test_demote_per_token_kernel_codebook_with_new_tokens():
-    _run(4002, 64, 2, with_new=True, levels=_levels(4002))
+    _run(4002, 512, 4, with_new=True, levels=_levels(4002, 4))
 
 
 def test_demote_bulk_gathered_rows_codebook():
@@ -103,10 +103,10 @@ def test_masked_tail_slots_with_nan_bytes_do_not_leak(with_levels):
         page = int(sc.table[b, (h - 1) // 16])
         for head in range(sc.n_kv):
             base = (page * sc.n_kv + head) * O.BLOCK_BYTES
-            for half in (0, O.HALF_BYTES):
+            for which in (0, 1):
                 for slot in range(h % 16, 16):
-                    pool[base + half + 32 * slot: base + half + 32 * slot + 32] = 0xFF
-                    so = base + half + 512 + 4 * slot
+                    pool[base + O.code_byte_offset(which, slot, np.arange(32))] = 0xFF
+                    so = base + int(O.pair_offset(which, slot, 0))
                     pool[so:so + 4] = nan
     cache.pages.copy_(torch.from_numpy(pool))
     _check(sc)

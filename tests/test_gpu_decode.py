@@ -143,3 +143,13 @@ def test_workspace_is_reusable_across_calls():
         assert torch.equal(o, outs[0])
     err = H.relative_error(outs[0].cpu().numpy().astype(np.float64), sc.expected())
     assert err.max() <= TOL
+
+
+@pytest.mark.parametrize("scales", [(2.0 ** -8, 2.0 ** -8, 1.0), (2.0 ** 8, 2.0 ** 8, 1.0),
+                                    (1.0, 2.0 ** 8, 2.0 ** -8), (2.0 ** 8, 2.0 ** -8, 2.0 ** 8)])
+def test_scaled_caches(scales):
+    """Keys, values and queries scaled by 2^-8 .. 2^8: the fp16 hi/lo splits of
+    q~ (per-head power-of-two scale) and of p s_V (scale from tau_v) and the
+    subnormal code operands keep the output within the bar."""
+    sc = H.Scenario(1013, [3000, 1500], n_kv=2, g=4, scales=scales)
+    _check(sc)

@@ -84,7 +84,6 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         xs = x[src_index]                                  # token written to position i
         xr = np.stack([np.clip(xs[:, h].astype(np.float64) @ r32[h].astype(np.float64), -tau, tau)
                        for h in range(n_kv)], axis=1)
-        rot_err = H.rotation_error_bound(xs, r32)
         if groups is None:
             gc, gs, gz = O.load_history_bulk(pool, table, n_kv, 0, hist, which)
             gc, gs, gz = gc[positions], gs[positions], gz[positions]
@@ -94,7 +93,7 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
             else:
                 rc, rs, rz = H.demote_heads_codebook(xs, r32, tau, lv)
             pre_s, pre_z = _pre_rounding(xr)
-            res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z, rot_err=rot_err, levels=lv)
+            res[which] = H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z, levels=lv)
             continue
         # groups: each group of gsz channels is compared as its own vector
         ng = 128 // gsz
@@ -104,8 +103,7 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         shp = (n_tok, n_kv, ng, gsz)
         xg = xr.reshape(shp)
         pre_s, pre_z = _pre_rounding(xg)
-        res[which] = H.code_parity(xg, gc.reshape(shp), gs, gz, rc.reshape(shp), rs, rz, pre_s, pre_z,
-                                   rot_err=np.repeat(rot_err[..., None], ng, axis=-1))
+        res[which] = H.code_parity(xg, gc.reshape(shp), gs, gz, rc.reshape(shp), rs, rz, pre_s, pre_z)
     if with_new:
         np.testing.assert_array_equal(k_src.float().cpu().numpy()[src_index], nk)
         np.testing.assert_array_equal(v_src.float().cpu().numpy()[src_index], nv)
@@ -143,7 +141,8 @@ def test_demote_eight_heads_scattered_positions():
 
 
 def test_demote_writes_new_token_into_freed_rows():
-    _run(2003, 64, 2, with_new=True)
+    # 512 tokens x 4 KV heads: enough codes for the 1e-4 bound on mismatches
+    _run(2003, 512, 4, with_new=True)
 
 
 def test_append_then_decode_matches_oracle_steps():
@@ -266,3 +265,110 @@ def test_decode_step_stages_odd_sizes_and_offsets():
         np.testing.assert_array_equal(d[off_d:off_d + n], host.numpy()[off_h:off_h + n])
         assert not d[:off_d].any() and not d[off_d + n:].any()
         np.testing.assert_array_equal(out.cpu().numpy(), ref.astype(np.float32))
+
+
+def _demote_rows(xk, xv, rk32, rv32, tau_k, tau_v, per_step, groups=(128, 128)):
+    """Demote the bf16 rows xk, xv [n][n_kv][128] to history positions 0..n-1
+    through one path: the tensor-core bulk kernel (one call, contiguous rows)
+    or the per-token kernel (calls of at most 1000 rows).  Returns the pool
+    and page table."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    from bit_rotated_kv_split_gb300.cache import LayerCache
+    n, n_kv = xk.shape[0], xk.shape[1]
+    table, n_pages = synth.page_table(77, [n], n_extra_pages=0)
+    cache = LayerCache(1, n_kv * 4, n_kv, table.shape[1], n_pages, torch.from_numpy(rk32), torch.from_numpy(rv32),
+                       tau_k, tau_v, quant_group_k=groups[0], quant_group_v=groups[1])
+    cache.page_table.copy_(torch.from_numpy(table))
+    dev = torch.device("cuda")
+    k_src = torch.from_numpy(xk).to(torch.bfloat16).to(dev).contiguous()
+    v_src = torch.from_numpy(xv).to(torch.bfloat16).to(dev).contiguous()
+    chunks = [(0, n)] if not per_step else [(a, min(a + 1000, n)) for a in range(0, n, 1000)]
+    for a, b in chunks:
+        m = b - a
+        assert per_step == (m < 1024)
+        dr = torch.zeros(m, dtype=torch.int32, device=dev)
+        dp = torch.arange(a, b, dtype=torch.int32, device=dev)
+        B.oscar_quantize_append(cache.desc(n), k_src[a:b].view(torch.uint16), v_src[a:b].view(torch.uint16), m,
+                                n_kv * 128, None, dr, dp, m, None, None)
+    torch.cuda.synchronize()
+    assert int(cache.dev_status.item()) == 0
+    return cache.pages.cpu().numpy(), table
+
+
+def _parity_of_pool(pool, table, xk, xv, rk32, rv32, tau_k, tau_v, groups=(128, 128)):
+    n, n_kv = xk.shape[0], xk.shape[1]
+    gk, gv = groups
+    out = {}
+    for which, x, r32, tau, gsz in ((0, xk, rk32, tau_k, gk), (1, xv, rv32, tau_v, gv)):
+        xr = np.stack([np.clip(x[:, h].astype(np.float64) @ r32[h].astype(np.float64), -tau, tau)
+                       for h in range(n_kv)], axis=1)
+        ng = 128 // gsz
+        if (gk, gv) == (128, 128):
+            gc, gs, gz = O.load_history_bulk(pool, table, n_kv, 0, n, which)
+            rc, rs, rz = H.demote_heads(x, r32, tau)
+            pre_s, pre_z = _pre_rounding(xr)
+            out[which] = (H.code_parity(xr, gc, gs, gz, rc, rs, rz, pre_s, pre_z), gc, gs, gz)
+            continue
+        gc, gs, gz = O.load_history_groups(pool, table, n_kv, 0, n, which, 128 // gk, 128 // gv)
+        rc, rs, rz = H.demote_heads(x, r32, tau, gsz)
+        shp = (n, n_kv, ng, gsz)
+        xg = xr.reshape(shp)
+        pre_s, pre_z = _pre_rounding(xg)
+        out[which] = (H.code_parity(xg, gc.reshape(shp), gs, gz, rc.reshape(shp), rs, rz, pre_s, pre_z),
+                      gc, gs, gz)
+    return out
+
+
+@pytest.mark.parametrize("groups", [(128, 128), (32, 64)])
+def test_same_tokens_through_both_paths(groups):
+    """The same 1500 tokens demoted by the tensor-core bulk kernel (one call
+    of 1500) and by the per-token kernel (calls of 1000 and 500) both meet
+    the code rule against the oracle; the two results differ, if at all,
+    only in codes the rule allows to differ."""
+    seed, n, n_kv = 2020, 1500, 4
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    xk = synth.activations(seed, (3, 0), n, outl)
+    xv = synth.activations(seed, (3, 1), n, outl)
+    res = {}
+    for per_step in (False, True):
+        pool, table = _demote_rows(xk, xv, rk32, rv32, tau_k, tau_v, per_step, groups)
+        res[per_step] = _parity_of_pool(pool, table, xk, xv, rk32, rv32, tau_k, tau_v, groups)
+    for which in (0, 1):
+        d = int(np.sum(res[False][which][1] != res[True][which][1]))
+        print("KV"[which], "codes differing between the paths:", d, res[False][which][0], res[True][which][0])
+        assert d <= 2 * 1e-4 * res[False][which][1].size
+
+
+@pytest.mark.parametrize("groups", [(128, 128), (32, 32)])
+def test_constant_groups_give_zero_scale_and_codes(groups):
+    """Token-head vectors whose (group of) rotated values is constant - the
+    zero vector, and vectors rotated far beyond +-tau so that the clip makes
+    every value equal - get scale 0 and all codes 0 in both demotion
+    kernels (bulk: 1100 tokens in one call; per-token: two calls)."""
+    seed, n, n_kv = 2021, 1100, 2
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    xk = synth.activations(seed, (4, 0), n, outl)
+    xv = synth.activations(seed, (4, 1), n, outl)
+    g = groups[0]
+    for x, r32, tau in ((xk, rk32, tau_k), (xv, rv32, tau_v)):
+        for h in range(n_kv):
+            rt = r32[h].astype(np.float64).T
+            x[0, h] = 0.0                                                  # the zero vector
+            x[1, h] = synth.to_bf16(np.full(128, 4.0 * tau) @ rt)         # all clipped to +tau
+            x[2, h] = synth.to_bf16(np.full(128, -4.0 * tau) @ rt)        # all clipped to -tau
+            target = np.concatenate([np.full(g, 4.0 * tau), np.linspace(-0.5, 0.5, 128 - g) * tau])
+            x[3, h] = synth.to_bf16(target @ rt)                          # first group clipped flat
+    for per_step in (False, True):
+        pool, table = _demote_rows(xk, xv, rk32, rv32, tau_k, tau_v, per_step, groups)
+        res = _parity_of_pool(pool, table, xk, xv, rk32, rv32, tau_k, tau_v, groups)
+        for which in (0, 1):
+            _, gc, gs, gz = res[which]
+            gs = np.asarray(gs, dtype=np.float64).reshape(n, n_kv, -1)
+            gcs = gc.reshape(n, n_kv, -1)
+            assert np.all(gs[0:3] == 0) and np.all(gcs[0:3] == 0)
+            assert np.all(gs[3, :, 0] == 0)
+            if g < 128:
+                assert np.all(gs[3, :, 1:] > 0)

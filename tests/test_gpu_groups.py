@@ -37,7 +37,7 @@ def test_demote_per_token_kernel_groups(groups):
 
 @pytest.mark.parametrize("groups", [(32, 32), (64, 128), (128, 64)])
 def test_demote_per_token_kernel_groups_with_new_tokens(groups):
-    _run(3002, 64, 2, with_new=True, groups=groups)
+    _run(3002, 512, 4, with_new=True, groups=groups)
 
 
 @pytest.mark.parametrize("groups", GROUPS)

@@ -256,11 +256,18 @@ def test_constant_group_gives_zero_scale_and_codes():
 # ---------------------------------------------------------------- paged layout
 
 def test_page_layout_offsets_and_round_trip():
-    # The block of (page 3, KV head 1) with 2 KV heads starts at (3*2+1)*1152;
-    # V half at +576; slot 5 codes at +5*32; its (scale, zero) at +512+4*5.
+    # The block of (page 3, KV head 1) with 2 KV heads starts at (3*2+1)*1152.
+    # K code byte l of slot t at 32 t + l; V code byte l of slot t at
+    # 512 + 64 (t // 2) + 4 (l // 2) + 2 (t % 2) + (l % 2); the (scale, zero)
+    # pairs of slot t at 1024 + 8 t (K) and 1024 + 8 t + 4 (V).
     assert O.block_offset(3, 1, 2) == 8064
-    assert O.token_offsets(5, 1) == (576 + 160, 576 + 512 + 20)
-    assert O.token_offsets(0, 0) == (0, 512)
+    assert O.block_bytes(1, 1) == O.BLOCK_BYTES == 1152
+    assert O.block_bytes(4, 2) == 1024 + 16 * 4 * 6
+    assert O.code_byte_offset(0, 5, 3) == 163
+    assert O.code_byte_offset(1, 5, 0) == 642 and O.code_byte_offset(1, 5, 3) == 647
+    assert O.code_byte_offset(1, 4, 3) == 512 + 128 + 4 + 1
+    assert O.pair_offset(0, 5, 0) == 1064 and O.pair_offset(1, 5, 0) == 1068
+    assert O.pair_offset(1, 5, 1, 4, 2) == 1024 + 24 * 5 + 4 * 5
     n_kv = 2
     table, n_pages = synth.page_table(9, [37], n_extra_pages=1)
     pool = np.zeros(n_pages * n_kv * O.BLOCK_BYTES, dtype=np.uint8)
@@ -274,12 +281,40 @@ def test_page_layout_offsets_and_round_trip():
             pk, ss, zz = O.load_history(pool, table, n_kv, 0, pos, h, 1)
             np.testing.assert_array_equal(pk, packed[pos, h])
             assert ss == s[pos, h] and zz == z[pos, h]
-            page = table[0, pos // 16]
-            base = (page * n_kv + h) * 1152 + 576 + (pos % 16) * 32
-            np.testing.assert_array_equal(pool[base:base + 32], packed[pos, h])
+            page, slot = table[0, pos // 16], pos % 16
+            base = (page * n_kv + h) * 1152
+            for l in range(32):
+                # V rows of a slot pair alternate by 16-bit halves
+                assert pool[base + 512 + 64 * (slot // 2) + 4 * (l // 2) + 2 * (slot % 2) + l % 2] == packed[pos, h, l]
+            sz = pool[base + 1024 + 8 * slot + 4: base + 1024 + 8 * slot + 8].copy().view(np.float16)
+            assert sz[0] == s[pos, h] and sz[1] == z[pos, h]
     codes, s2, z2 = O.load_history_bulk(pool, table, n_kv, 0, 37, 1)
     np.testing.assert_array_equal(O.pack(codes), packed)
     np.testing.assert_array_equal(s2, s)
+    # the K rows and pairs were never written
+    for pos in range(37):
+        pk, ss, zz = O.load_history(pool, table, n_kv, 0, pos, 0, 0)
+        assert not pk.any() and ss == 0 and zz == 0
+
+
+def test_decode_operand_words_of_the_v_rows():
+    # The 32-bit word at 512 + 64 a + 4 h of a block holds 16-bit half h of
+    # slot 2a's V row (low) and of slot 2a + 1's (high): eight code positions
+    # 8h .. 8h+7 of two consecutive tokens, as one tensor-core operand pair.
+    n_kv = 1
+    table = np.array([[0]], np.int32)
+    pool = np.zeros(O.BLOCK_BYTES, np.uint8)
+    g = synth.generator(9, 2)
+    codes = g.integers(0, 4, size=(16, 1, 128)).astype(np.uint8)
+    O.store_history_bulk(pool, table, n_kv, 0, 0, O.pack(codes), np.ones((16, 1), np.float16),
+                         np.zeros((16, 1), np.float16), 1)
+    for a in (0, 3, 7):
+        for h in (0, 9, 15):
+            w = int(pool[512 + 64 * a + 4 * h: 512 + 64 * a + 4 * h + 4].copy().view(np.uint32)[0])
+            for half, t in ((0, 2 * a), (1, 2 * a + 1)):
+                bits = (w >> (16 * half)) & 0xFFFF
+                for i in range(8):
+                    assert (bits >> (2 * i)) & 3 == codes[t, 0, 8 * h + i]
 
 
 # ---------------------------------------------------------------- attention
@@ -522,7 +557,7 @@ def test_storage_order_makes_mma_operands_group_pure(ng):
 
 @pytest.mark.parametrize("ng_k,ng_v", [(1, 1), (2, 2), (4, 4), (4, 1), (1, 4)])
 def test_grouped_page_format_round_trip_and_offsets(ng_k, ng_v):
-    assert O.half_bytes(1) == 576 and O.half_bytes(2) == 640 and O.half_bytes(4) == 768
+    assert O.block_bytes(1, 1) == 1152 and O.block_bytes(2, 2) == 1280 and O.block_bytes(4, 4) == 1536
     n_kv, n_pages = 2, 4
     table = np.array([[3, 1, 0, 2]], np.int32)
     pool = np.zeros(n_pages * n_kv * O.block_bytes(ng_k, ng_v), np.uint8)
@@ -540,17 +575,24 @@ def test_grouped_page_format_round_trip_and_offsets(ng_k, ng_v):
         np.testing.assert_array_equal(c, data[which][0])
         np.testing.assert_array_equal(s.view(np.uint16), data[which][1].view(np.uint16))
         np.testing.assert_array_equal(z.view(np.uint16), data[which][2].view(np.uint16))
-    # one byte located by hand: token 21 (page 1, slot 5), KV head 1, V half;
-    # position p holds the code of channel storage_channel(1, ng_v, p)
+    # bytes located by hand: token 21 (page 1, slot 5), KV head 1, V codes at
+    # 512 + 64 * 2 + 4 * (byte // 2) + 2 * 1 + byte % 2; position p (byte
+    # p // 4) holds the code of channel storage_channel(1, ng_v, p)
     blk = O.block_bytes(ng_k, ng_v)
-    base = (1 * n_kv + 1) * blk + O.half_bytes(ng_k) + 5 * 32
+    base = (1 * n_kv + 1) * blk
     c_v = data[1][0]
     for p in (0, 37, 127):
-        byte = pool[base + p // 4]
+        byte = pool[base + 512 + 128 + 4 * ((p // 4) // 2) + 2 + (p // 4) % 2]
         assert (byte >> (2 * (p % 4))) & 3 == c_v[21, 1, O.storage_channel(1, ng_v, p)]
-    so = (1 * n_kv + 1) * blk + O.half_bytes(ng_k) + 512 + 4 * (5 * ng_v + ng_v - 1)
+    # the last V pair of slot 5 sits after its ng_k K pairs and ng_v - 1 V pairs
+    so = base + 1024 + 4 * (ng_k + ng_v) * 5 + 4 * (ng_k + ng_v - 1)
     pair = pool[so:so + 4].copy().view(np.float16)
     assert pair[0] == data[1][1][21, 1, ng_v - 1] and pair[1] == data[1][2][21, 1, ng_v - 1]
+    # K code rows are plain token rows: token 21's byte 7 at 32 * 5 + 7
+    c_k = data[0][0]
+    byte = pool[base + 32 * 5 + 7]
+    for i in range(4):
+        assert (byte >> (2 * i)) & 3 == c_k[21, 1, O.storage_channel(0, ng_k, 28 + i)]
     if (ng_k, ng_v) == (1, 1):
         # the grouped writer with one group is the original format
         pool2 = np.zeros_like(pool)
