@@ -87,7 +87,7 @@
 // INT2 pages a warp processes per step (one online-softmax update per step)
 // for GQA 4 / GQA 8
 #ifndef OSCAR_GROUP_G4
-#define OSCAR_GROUP_G4 4
+#define OSCAR_GROUP_G4 3
 #endif
 #ifndef OSCAR_GROUP_G8
 #define OSCAR_GROUP_G8 3
@@ -117,7 +117,10 @@ struct Geo {
   static constexpr int PT = (W - kBf16Warps) * 32;
   // pages per step (GQA 8 with several quantisation groups or codebook
   // levels: 2, which keeps the extra state within the register budget)
-  static constexpr int kGroup = G <= 4 ? OSCAR_GROUP_G4 : (NGK * NGV > 1 || LV ? 2 : OSCAR_GROUP_G8);
+  // (larger blocks leave room for fewer stages: two pages per step where
+  // three would not give the ring two parts)
+  static constexpr int kGroup = G <= 4 ? (NGK * NGV >= 16 ? 2 : OSCAR_GROUP_G4)
+                                       : (NGK * NGV > 1 || LV ? 2 : OSCAR_GROUP_G8);
   static constexpr int kQkChains = G <= 4 ? OSCAR_QK_CHAINS_G4 : OSCAR_QK_CHAINS_G8;   // QK accumulators
   static constexpr int kBlock = block_bytes(NGK, NGV);   // one (page, KV head) block
   // union: R_K (64 KB, prologue) then R_V (epilogue), followed by the q~
@@ -128,11 +131,15 @@ struct Geo {
   static constexpr size_t kBf16State = size_t(kBf16Warps) * G * kPartStride * 4;
   // ring stages per warp: the tuned count, fewer when larger blocks (more
   // quantisation groups) would not fit the 227 KB with everything else
+  // the ring is kParts parts of kGroup stages: a step consumes one part
+  // while the others' copies are in flight
   static constexpr int kStagesTuned = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;
   static constexpr int kStagesFit =
       int((227 * 1024 - (1024 + kUnion + kBf16State + 16 + 1024)) / (size_t(W) * kBlock));
-  static constexpr int kStages = kStagesTuned < kStagesFit ? kStagesTuned : kStagesFit;
-  static_assert(kGroup >= 1 && kGroup < kStages, "a step leaves copies in flight");
+  static constexpr int kStagesMax = kStagesTuned < kStagesFit ? kStagesTuned : kStagesFit;
+  static constexpr int kParts = kStagesMax / kGroup;
+  static constexpr int kStages = kParts * kGroup;
+  static_assert(kGroup >= 1 && kParts >= 2, "a step leaves a part of the ring in flight");
   static constexpr size_t kStageBytes = size_t(W) * kStages * kBlock;
   // ring barriers + the R_K, R_V and prologue-done barriers, padded so the
   // region after it stays 128-byte aligned (TMA destinations need at least 16)
@@ -1036,6 +1043,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   constexpr int NZ = kLevels ? 2 : NGV;   // zero-point sums per head
   constexpr int NTQ = Geo<G>::NTQ, W = Geo<G>::W, T = Geo<G>::T;
   constexpr int kStages = Gm::kStages;
+  constexpr int kParts = Gm::kParts;
   constexpr int kBlock = Gm::kBlock;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stage = smem;
@@ -1110,9 +1118,10 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // ---------------- INT2 pages of this CTA: warp w first copies pages
   // pbeg + kStages w + s (s < kStages) into its ring, requested before the
   // history length is known (pages past it are read but never used; ids
-  // outside the pool are never copied).  The CTA's later pages are taken
-  // kGroup at a time from a shared counter as each warp frees its stages,
-  // so a warp whose pages arrive later takes fewer of them.
+  // outside the pool are never copied).  The ring is kParts parts of kGroup
+  // consecutive pages; once a step has consumed a part, the part takes the
+  // next kGroup pages of a CTA-wide counter, so a warp whose pages arrive
+  // later takes fewer of them.
   const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
   const int spec_end = min(pbeg + p.pages_per_split, p.max_pages);
   int hist = p.hist_len[b];
@@ -1126,16 +1135,15 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     fence_mbar_init();
   }
   __syncwarp();
-  // lane s < kStages describes ring stage s: the page index it holds (-1:
-  // none) and whether that page was copied (a valid id)
-  int ring_j = pbeg + kStages * warp + lane;
-  ring_j = lane < kStages && ring_j < spec_end ? ring_j : -1;
-  bool ring_ok = false;
+  // lane s < kStages copies the warp's s-th first page into stage s
+  uint32_t copied_bits, issued_bits;
   {
-    const int pid = ring_j >= 0 ? __ldg(ptab + ring_j) : -1;
-    ring_ok = ring_j >= 0 && pid >= 0 && pid < p.n_pages;
-    if (ring_j >= 0) {
-      if (!ring_ok) {
+    const int j = pbeg + kStages * warp + lane;
+    const bool in = lane < kStages && j < spec_end;
+    const int pid = in ? __ldg(ptab + j) : -1;
+    const bool ok = in && pid >= 0 && pid < p.n_pages;
+    if (in) {
+      if (!ok) {
         // no copy: complete the stage's phase without bytes so the ring stays in step
         mbar_arrive(bar + lane);
       } else {
@@ -1143,11 +1151,9 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         bulk_copy_g2s(ring + lane * kBlock, pool + int64_t(pid) * page_stride, kBlock, bar + lane);
       }
     }
+    copied_bits = __ballot_sync(kFull, ok);
+    issued_bits = __ballot_sync(kFull, in);
   }
-  // stages with an arrival not yet waited for (bit s), and the parity each
-  // stage's next completion has
-  uint32_t pending = __ballot_sync(kFull, ring_j >= 0) & ((1u << kStages) - 1u);
-  uint32_t parity = 0u;
   if (tid == 0) *next_page = pbeg + kStages * W;
 
   __syncthreads();   // the R_K / R_V / prologue barriers are initialised
@@ -1170,7 +1176,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   if (n_pg > n_splits * p.pages_per_split && split == 0 && tid == 0)
     flag(p.dev_status, 0x2);  // longer than the host bound max_hist: tail not read
   const int pend = min(pbeg + p.pages_per_split, n_pg);
-  if (ring_j >= pend) ring_j = -1;   // past the history: copied, never used
 
   // ---------------- q~ and the lane's QK fragments (prologue warps); the
   // BF16 warps scan the sink/recent tokens meanwhile and read the fragments
@@ -1293,20 +1298,31 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // each, GQA 4); the other variants load the V pairs again for PV, which
   // keeps their register budget
   constexpr bool kJointPairs = NGK == 1 && NGV == 1 && G <= 4;
-  // ---------------- INT2 pages, kGroup per step: QK of the step's pages,
-  // one maximum update, then their probabilities and PV.  The step consumes
-  // ring stages s_cur .. s_cur + kGroup - 1 (mod kStages) and refills them
-  // with the next kGroup pages of the CTA's counter.  Stages run dry in
-  // consumption order (the counter only grows), so the first empty stage of
-  // a step ends the warp's pages.  A page with an invalid id is computed on
-  // stale ring data with every token masked.
+  // ---------------- INT2 pages, one ring part (kGroup pages) per step: QK
+  // of the step's pages, one maximum update, then their probabilities and
+  // PV.  The loop body is unrolled over the kParts parts, so every stage
+  // index is a compile-time constant.  Parts run dry in consumption order
+  // (the counter only grows), so the first part past the history ends the
+  // warp's pages.  A page with an invalid id is computed on stale ring data
+  // with every token masked.
   {
     HistState<G, NZ> st;
     st.init();
     const float lift = float(kRescaleLog2) + p.pv_log2;   // rescale test against st.m (see int2_update_max)
     const int n_full = hist / kPage;                     // pages below it hold kPage valid tokens
-    bool timed_out = false;
-    int s_cur = 0;
+    constexpr uint32_t kPartBits = (1u << kGroup) - 1u;
+    // first page of each part and its copied pages (bit u: page base + u)
+    int base[kParts];
+    uint32_t good[kParts];
+#pragma unroll
+    for (int h = 0; h < kParts; ++h) {
+      base[h] = pbeg + kStages * warp + kGroup * h;
+      good[h] = (copied_bits >> (kGroup * h)) & kPartBits;
+    }
+    // stages whose arrival is not yet consumed, and each stage's parity
+    uint32_t pending = issued_bits & ((1u << kStages) - 1u);
+    uint32_t parity = 0u;
+    bool timed_out = false, done = false;
     // the next refill, one step ahead: its first page and lane u's page id
     auto grab = [&]() {
       int g = 0;
@@ -1315,141 +1331,130 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     };
     int g_next = grab();
     int pid_next = lane < kGroup && g_next + lane < pend ? __ldg(ptab + g_next + lane) : -1;
-    while (true) {
-      int ju[kGroup];
-      const uint8_t* pg[kGroup];
-      const uint32_t ok_bits = __ballot_sync(kFull, ring_ok);
-      bool all_full = true;
+    while (!done) {
 #pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        int su = s_cur + u;
-        if (su >= kStages) su -= kStages;
-        ju[u] = __shfl_sync(kFull, ring_j, su);
-        pg[u] = ring + su * kBlock;
-        all_full = all_full && ju[u] >= 0 && ((ok_bits >> su) & 1u) && ju[u] < n_full;
-      }
-      if (ju[0] < 0) break;
-#pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        int su = s_cur + u;
-        if (su >= kStages) su -= kStages;
-        if (ju[u] >= 0) {
-          if (!mbar_wait_bounded(bar + su, (parity >> su) & 1u, kWaitLimitNs)) {
-            timed_out = true;
-          } else {
-            pending &= ~(1u << su);
-            parity ^= 1u << su;
-          }
+      for (int h = 0; h < kParts; ++h) {
+        if (done) break;
+        const int j0 = base[h];
+        if (j0 >= pend) {
+          done = true;
+          break;
         }
-      }
-      if (timed_out) break;
-      // token validity of the lane's two tokens per page (masked steps only)
-      bool ok[kGroup][2];
-      if (!all_full) {
+        const int nv = min(kGroup, pend - j0);   // this part's pages within the history
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
-          int su = s_cur + u;
-          if (su >= kStages) su -= kStages;
-          const bool copied = (ok_bits >> su) & 1u;
-          if (ju[u] >= 0 && !copied && lane == 0) flag(p.dev_status, 0x1);
-          const int ntok = ju[u] >= 0 && copied ? hist - kPage * ju[u] : 0;
-          ok[u][0] = gid < ntok;
-          ok[u][1] = gid + 8 < ntok;
+          const int s = kGroup * h + u;
+          if (u == 0 || u < nv) {
+            if (!mbar_wait_bounded(bar + s, (parity >> s) & 1u, kWaitLimitNs)) {
+              timed_out = true;
+            } else {
+              pending &= ~(1u << s);
+              parity ^= 1u << s;
+            }
+          }
         }
-      }
-      // QK of the step's pages, one maximum update, probabilities and PV;
-      // steps whose tokens are all valid (every step but the history's last
-      // and a warp's last) take the select-free variant; in the other, empty
-      // stages are skipped (warp-uniform branches)
-      auto step = [&](auto masked) {
-        constexpr bool kMasked = decltype(masked)::value;
-        float sc[kGroup][NH][2];
-        uint32_t vsz0[kGroup][NGV], vsz1[kGroup][NGV];   // the pages' V (scale, zero) pairs
+        if (timed_out) {
+          done = true;
+          break;
+        }
+        const uint8_t* pg[kGroup];
 #pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-          if (kMasked && u > 0 && ju[u] < 0) {
+        for (int u = 0; u < kGroup; ++u) pg[u] = ring + (kGroup * h + u) * kBlock;
+        const bool all_full = nv == kGroup && good[h] == kPartBits && j0 + kGroup <= n_full;
+        // token validity of the lane's two tokens per page (masked steps only)
+        bool ok[kGroup][2];
+        if (!all_full) {
 #pragma unroll
-            for (int nt = 0; nt < NH; ++nt) sc[u][nt][0] = sc[u][nt][1] = -INFINITY;
-            continue;
-          }
-          uint32_t ksz0[NGK], ksz1[NGK];
-          if constexpr (kJointPairs) {
-            load_pairs<NGK, NGV>(pg[u], gid, ksz0, vsz0[u]);
-            load_pairs<NGK, NGV>(pg[u], gid + 8, ksz1, vsz1[u]);
-          } else {
-            load_group_pairs<NGK, NGV, 0>(pg[u], gid, ksz0);
-            load_group_pairs<NGK, NGV, 0>(pg[u], gid + 8, ksz1);
-          }
-          if constexpr (kLevels) {
-            float e[NH][2];
-            int2_qk_levels<G>(pg[u], gid, tig, qb, p.coef_k, e);
-            int2_scores_levels<G, kMasked>(e, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, p.coef_k, sc[u]);
-          } else if constexpr (NGK == 1) {
-            float d[NH][4];
-            int2_qk<G>(pg[u], gid, tig, qb, d);
-            int2_scores<G, kMasked>(d, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, sc[u]);
-          } else {
-            float a[NH][2];
-            int2_qk_groups<G, NGK>(pg[u], gid, tig, qb, ksz0, ksz1, a);
-            int2_scores_groups<G, NGK, kMasked>(a, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
+          for (int u = 0; u < kGroup; ++u) {
+            const bool copied = (good[h] >> u) & 1u;
+            if (u < nv && !copied && lane == 0) flag(p.dev_status, 0x1);
+            const int ntok = u < nv && copied ? hist - kPage * (j0 + u) : 0;
+            ok[u][0] = gid < ntok;
+            ok[u][1] = gid + 8 < ntok;
           }
         }
-        int2_update_max<G, NZ, kGroup>(sc, st, p.pv_log2, lift);
+        // QK of the step's pages, one maximum update, probabilities and PV;
+        // steps whose tokens are all valid (every step but the history's last)
+        // take the select-free variant; in the other, pages past the history
+        // are skipped (warp-uniform branches)
+        auto step = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
+          float sc[kGroup][NH][2];
+          uint32_t vsz0[kGroup][NGV], vsz1[kGroup][NGV];   // the pages' V (scale, zero) pairs
 #pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-          if (kMasked && u > 0 && ju[u] < 0) continue;
-          if constexpr (!kJointPairs) {
-            load_group_pairs<NGK, NGV, NGK>(pg[u], gid, vsz0[u]);
-            load_group_pairs<NGK, NGV, NGK>(pg[u], gid + 8, vsz1[u]);
+          for (int u = 0; u < kGroup; ++u) {
+            if (kMasked && u > 0 && u >= nv) {
+#pragma unroll
+              for (int nt = 0; nt < NH; ++nt) sc[u][nt][0] = sc[u][nt][1] = -INFINITY;
+              continue;
+            }
+            uint32_t ksz0[NGK], ksz1[NGK];
+            if constexpr (kJointPairs) {
+              load_pairs<NGK, NGV>(pg[u], gid, ksz0, vsz0[u]);
+              load_pairs<NGK, NGV>(pg[u], gid + 8, ksz1, vsz1[u]);
+            } else {
+              load_group_pairs<NGK, NGV, 0>(pg[u], gid, ksz0);
+              load_group_pairs<NGK, NGV, 0>(pg[u], gid + 8, ksz1);
+            }
+            if constexpr (kLevels) {
+              float e[NH][2];
+              int2_qk_levels<G>(pg[u], gid, tig, qb, p.coef_k, e);
+              int2_scores_levels<G, kMasked>(e, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, p.coef_k, sc[u]);
+            } else if constexpr (NGK == 1) {
+              float d[NH][4];
+              int2_qk<G>(pg[u], gid, tig, qb, d);
+              int2_scores<G, kMasked>(d, ksz0[0], ksz1[0], ok[u][0], ok[u][1], unscale, qz, sc[u]);
+            } else {
+              float a[NH][2];
+              int2_qk_groups<G, NGK>(pg[u], gid, tig, qb, ksz0, ksz1, a);
+              int2_scores_groups<G, NGK, kMasked>(a, ksz0, ksz1, ok[u][0], ok[u][1], unscale, qz, sc[u]);
+            }
           }
-          if constexpr (kLevels) {
-            uint32_t pb[3][NH][2];
-            int2_probs_levels<G, kMasked>(sc[u], vsz0[u][0], vsz1[u][0], ok[u][0], ok[u][1], p.coef_v, st, pb);
-            int2_pv_levels<G>(pg[u], gid, tig, pb, st);
-          } else {
-            uint32_t pb[NGV][NH][2];
-            int2_probs<G, NGV, kMasked>(sc[u], vsz0[u], vsz1[u], ok[u][0], ok[u][1], st, pb);
-            int2_pv<G, NGV>(pg[u], gid, tig, pb, st);
+          int2_update_max<G, NZ, kGroup>(sc, st, p.pv_log2, lift);
+#pragma unroll
+          for (int u = 0; u < kGroup; ++u) {
+            if (kMasked && u > 0 && u >= nv) continue;
+            if constexpr (!kJointPairs) {
+              load_group_pairs<NGK, NGV, NGK>(pg[u], gid, vsz0[u]);
+              load_group_pairs<NGK, NGV, NGK>(pg[u], gid + 8, vsz1[u]);
+            }
+            if constexpr (kLevels) {
+              uint32_t pb[3][NH][2];
+              int2_probs_levels<G, kMasked>(sc[u], vsz0[u][0], vsz1[u][0], ok[u][0], ok[u][1], p.coef_v, st, pb);
+              int2_pv_levels<G>(pg[u], gid, tig, pb, st);
+            } else {
+              uint32_t pb[NGV][NH][2];
+              int2_probs<G, NGV, kMasked>(sc[u], vsz0[u], vsz1[u], ok[u][0], ok[u][1], st, pb);
+              int2_pv<G, NGV>(pg[u], gid, tig, pb, st);
+            }
           }
+        };
+        if (all_full) {
+          step(std::false_type{});
+        } else {
+          step(std::true_type{});
         }
-      };
-      if (all_full) {
-        step(std::false_type{});
-      } else {
-        step(std::true_type{});
-      }
-      __syncwarp();
-      // the step's stages take the pages g_next .. g_next + kGroup - 1 (ids
-      // loaded one step ahead): lane u < kGroup starts the copy into stage
-      // s_cur + u, and the stage lanes learn their new page
-      {
-        const int jj = g_next + lane;
-        const bool want = lane < kGroup && jj < pend;
-        const bool good = want && pid_next >= 0 && pid_next < p.n_pages;
-        int s = s_cur + lane;
-        if (s >= kStages) s -= kStages;
-        if (want) {
-          if (!good) {
-            mbar_arrive(bar + s);   // no copy: complete the phase without bytes
-          } else {
-            mbar_arrive_expect_tx(bar + s, kBlock);
-            bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid_next) * page_stride, kBlock, bar + s);
+        __syncwarp();
+        // the part takes the pages g_next .. g_next + kGroup - 1 (ids loaded
+        // one step ahead): lane u < kGroup starts the copy into its stage
+        {
+          const bool want = lane < kGroup && g_next + lane < pend;
+          const bool good_id = want && pid_next >= 0 && pid_next < p.n_pages;
+          if (want) {
+            const int s = kGroup * h + lane;
+            if (!good_id) {
+              mbar_arrive(bar + s);   // no copy: complete the phase without bytes
+            } else {
+              mbar_arrive_expect_tx(bar + s, kBlock);
+              bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid_next) * page_stride, kBlock, bar + s);
+            }
           }
+          pending |= (__ballot_sync(kFull, want) & kPartBits) << (kGroup * h);
+          good[h] = __ballot_sync(kFull, good_id) & kPartBits;
+          base[h] = g_next;
+          g_next = grab();
+          pid_next = lane < kGroup && g_next + lane < pend ? __ldg(ptab + g_next + lane) : -1;
         }
-        const uint32_t want_bits = __ballot_sync(kFull, want);
-        const uint32_t good_bits = __ballot_sync(kFull, good);
-        int ds = lane - s_cur;
-        if (ds < 0) ds += kStages;
-        if (lane < kStages && ds < kGroup) {
-          ring_j = (want_bits >> ds) & 1u ? g_next + ds : -1;
-          ring_ok = (good_bits >> ds) & 1u;
-        }
-        const uint32_t r = (want_bits & ((1u << kGroup) - 1u)) << s_cur;
-        pending |= (r | (r >> kStages)) & ((1u << kStages) - 1u);
-        g_next = grab();
-        pid_next = lane < kGroup && g_next + lane < pend ? __ldg(ptab + g_next + lane) : -1;
-        s_cur += kGroup;
-        if (s_cur >= kStages) s_cur -= kStages;
       }
     }
     if (timed_out && lane == 0) flag(p.dev_status, 0x4);
