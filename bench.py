@@ -135,24 +135,24 @@ def _config_json(extra=None):
 
 # ---------------------------------------------------------------------------- oracle leg
 
-def _oracle_sample_setup():
+def _oracle_sample_setup(head=0):
     """Inputs of one KV head (4 query heads) of the workload for the oracle."""
     import numpy as np
     import oracle as O
     import synth
     w = WORKLOAD
     seed = w["seed"]
-    outl = synth.outlier_channels(seed, 0, 1)
-    cal = synth.calibration_set(seed, 0, 0, outl[0], n_q=4096, n_k=2048)
+    outl = synth.outlier_channels(seed, 0, w["n_kv_heads"])[head:head + 1]
+    cal = synth.calibration_set(seed, 0, head, outl[0], n_q=4096, n_k=2048)
     rk = O.rotation_from_covariance(O.query_covariance(cal["q"]))
     rv = O.rotation_from_covariance(O.value_covariance(cal["q"], cal["k"], cal["v"]))
     tau_k = O.clip_threshold(cal["k"] @ rk)
     tau_v = O.clip_threshold(cal["v"] @ rv)
     s, h, r = _split(w["ctx"])
-    k = synth.activations(seed, (0, 0, 0), w["ctx"] + 1, outl).astype(np.float64)
-    v = synth.activations(seed, (0, 0, 1), w["ctx"] + 1, outl).astype(np.float64)
+    k = synth.activations(seed, (0, head, 0), w["ctx"] + 1, outl).astype(np.float64)
+    v = synth.activations(seed, (0, head, 1), w["ctx"] + 1, outl).astype(np.float64)
     g = w["n_q_heads"] // w["n_kv_heads"]
-    q = synth.activations(seed, (0, 0, 2), 1, np.repeat(outl, g, axis=0))[0].astype(np.float64)
+    q = synth.activations(seed, (0, head, 2), 1, np.repeat(outl, g, axis=0))[0].astype(np.float64)
     hist = {}
     if w["codebook"] != "uniform":
         # the oracle's own Lloyd-Max fit on this head's calibration rows
@@ -214,7 +214,38 @@ def cpu_baseline_worker(reps):
     for _ in range(reps):
         _oracle_step(st)
     dt = (time.perf_counter() - t0) / reps
-    print(json.dumps({"sample_seconds": dt, "reps": reps}))
+    # one whole step, every KV head in full (no extrapolation)
+    heads = [st] + [_oracle_sample_setup(h) for h in range(1, WORKLOAD["n_kv_heads"])]
+    t1 = time.perf_counter()
+    for sh in heads:
+        _oracle_step(sh)
+    full = time.perf_counter() - t1
+    print(json.dumps({"sample_seconds": dt, "reps": reps, "full_step_seconds": full}))
+
+
+def _host_cpu():
+    """(model name, logical cores) of this host."""
+    import platform
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    name = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not name:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return name or platform.machine(), os.cpu_count()
 
 
 def _single_thread_env():
@@ -234,9 +265,16 @@ def cpu_baseline(reps=20):
     if r.returncode != 0:
         return {"error": r.stderr[-400:]}
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    step = res["sample_seconds"] * WORKLOAD["n_kv_heads"]
-    return {"value": WORKLOAD["batch"] / step, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": SAMPLE_DESC + "; %d timed repetitions" % res["reps"]}
+    model, n_cpu = _host_cpu()
+    full = res["full_step_seconds"]
+    return {"value": WORKLOAD["batch"] / full, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "one whole decode step at 100k context, all %d KV heads in full (demotion of 1 token and "
+                      "attention over 64 + 99,680 INT2 + 256 tokens per head), timed once"
+                      % WORKLOAD["n_kv_heads"],
+            "step_seconds": full,
+            "per_head_step_seconds": res["sample_seconds"],
+            "per_head_note": SAMPLE_DESC + "; %d timed repetitions" % res["reps"],
+            "host_cpu": model, "host_logical_cores": n_cpu}
 
 
 def run_reference(args):
@@ -267,12 +305,21 @@ def run_reference(args):
     sample = SAMPLE_DESC if n_hist == h else (
         SAMPLE_DESC + "; history cut to the first %d of %d tokens per step and scaled by %.2f"
         % (n_hist, h, 1 / frac))
+    model, n_cpu = _host_cpu()
+    # ms_per_step: what each timed step measured (one KV head, the history
+    # sample above); value: that time extrapolated to a whole step
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": _config_json(),
+            "extrapolation": {"measured_ms_per_sample_step": dt * 1e3,
+                              "factor": WORKLOAD["n_kv_heads"] / frac,
+                              "whole_step_ms": step * 1e3,
+                              "note": "each timed step runs one of the %d KV heads%s; value = batch / whole_step"
+                                      % (WORKLOAD["n_kv_heads"], "" if n_hist == h else
+                                         " over the first %d of %d history tokens" % (n_hist, h))},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host_cpu": model, "host_logical_cores": n_cpu},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

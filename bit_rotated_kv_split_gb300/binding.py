@@ -13,7 +13,9 @@ from ctypes import c_double, c_float, c_int32, c_int64, c_size_t, c_void_p
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "liboscar.so")
+# the in-tree library; OSCAR_LIBRARY names another build of it (a
+# verification build, for instance)
+LIB_PATH = os.environ.get("OSCAR_LIBRARY") or os.path.join(_PKG, "liboscar.so")
 
 OSCAR_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE", 4: "CUDA",
@@ -50,6 +52,7 @@ def _load():
     sig = {
         "oscar_status_string": (ctypes.c_char_p, [c_int32]),
         "oscar_abi_version": (c_int32, []),
+        "oscar_set_page_wait_limit": (c_int64, [c_int64]),
         "oscar_block_bytes": (c_int64, [c_int32, c_int32]),
         "oscar_build_rotation": (c_int32, [P, c_int64, c_int32, P, P]),
         "oscar_build_canalized_rotation": (c_int32, [c_int32, c_int32, P]),
@@ -105,6 +108,11 @@ def oscar_status_string(status: int) -> str:
 
 def oscar_abi_version() -> int:
     return lib.oscar_abi_version()
+
+
+def oscar_set_page_wait_limit(limit_ns: int) -> int:
+    """Limit of the decode kernel's waits for page copies (<= 0: the default, 1 s); returns the previous one."""
+    return int(lib.oscar_set_page_wait_limit(int(limit_ns)))
 
 
 def oscar_block_bytes(quant_group_k: int = 128, quant_group_v: int = 128) -> int:

@@ -57,10 +57,11 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, verbose: bool, build_dir: str = BUILD, defines=()) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     if src.endswith(".cu"):
-        cmd = [_nvcc()] + ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        cmd = ([_nvcc()] + ARCH + NVCC_FLAGS + ["-D" + d for d in defines] +
+               ["-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj])
         if verbose:
             cmd += ["-Xptxas", "-v"]
     else:
@@ -90,6 +91,21 @@ def build(verbose: bool = False, force: bool = False) -> str:
         raise RuntimeError("link failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
     os.replace(tmp, LIB)
     return LIB
+
+
+def build_variant(out_path: str, defines, build_dir: str) -> str:
+    """A separately named copy of the library compiled with extra -D
+    definitions (verification builds, such as the serial-copy decode the
+    race test compares with); returns out_path."""
+    os.makedirs(build_dir, exist_ok=True)
+    srcs = sources()
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        objs = list(ex.map(lambda s: _compile(s, False, build_dir, tuple(defines)), srcs))
+    cmd = [_nvcc()] + ARCH + ["-shared", "-o", out_path] + objs + ["-lstdc++"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
+    return out_path
 
 
 def ensure_built() -> str:

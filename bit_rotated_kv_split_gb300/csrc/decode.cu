@@ -84,6 +84,12 @@
 #ifndef OSCAR_QK_CHAINS_G8
 #define OSCAR_QK_CHAINS_G8 1
 #endif
+// 1: every page copy is waited for right after it is issued, so no copy
+// ever overlaps the computation (a verification build: its results must be
+// bit-identical to the default build's, which overlaps them)
+#ifndef OSCAR_SERIAL_COPIES
+#define OSCAR_SERIAL_COPIES 0
+#endif
 // INT2 pages a warp processes per step (one online-softmax update per step)
 // for GQA 4 / GQA 8
 #ifndef OSCAR_GROUP_G4
@@ -1120,8 +1126,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // history length is known (pages past it are read but never used; ids
   // outside the pool are never copied).  The ring is kParts parts of kGroup
   // consecutive pages; once a step has consumed a part, the part takes the
-  // next kGroup pages of a CTA-wide counter, so a warp whose pages arrive
-  // later takes fewer of them.
+  // warp's next kGroup pages.
   const int32_t* ptab = p.page_table + int64_t(b) * p.max_pages;
   const int spec_end = min(pbeg + p.pages_per_split, p.max_pages);
   int hist = p.hist_len[b];
@@ -1129,7 +1134,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   uint64_t* bar = bars + warp * kStages;
   const uint8_t* pool = p.pages + int64_t(hkv) * kBlock;
   const int64_t page_stride = int64_t(p.n_kv) * kBlock;
-  int* next_page = s_last + 1;   // the CTA's page counter
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar + s, 1);
     fence_mbar_init();
@@ -1153,8 +1157,11 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     }
     copied_bits = __ballot_sync(kFull, ok);
     issued_bits = __ballot_sync(kFull, in);
+    if (OSCAR_SERIAL_COPIES) {
+      if (in) mbar_wait_bounded(bar + lane, 0, kDrainWaitNs);
+      __syncwarp();
+    }
   }
-  if (tid == 0) *next_page = pbeg + kStages * W;
 
   __syncthreads();   // the R_K / R_V / prologue barriers are initialised
 
@@ -1301,9 +1308,8 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   // ---------------- INT2 pages, one ring part (kGroup pages) per step: QK
   // of the step's pages, one maximum update, then their probabilities and
   // PV.  The loop body is unrolled over the kParts parts, so every stage
-  // index is a compile-time constant.  Parts run dry in consumption order
-  // (the counter only grows), so the first part past the history ends the
-  // warp's pages.  A page with an invalid id is computed on stale ring data
+  // index is a compile-time constant.  A warp's pages only grow in
+  // consumption order, so the first part past the history ends them.  A page with an invalid id is computed on stale ring data
   // with every token masked.
   {
     HistState<G, NZ> st;
@@ -1324,13 +1330,16 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     uint32_t parity = 0u;
     bool timed_out = false, done = false;
     // the next refill, one step ahead: its first page and lane u's page id
-    auto grab = [&]() {
-      int g = 0;
-      if (lane == 0) g = atomicAdd(next_page, kGroup);
-      return __shfl_sync(kFull, g, 0);
-    };
+    // refill n of warp w takes pages pbeg + kStages W + (n W + w) kGroup
+    // onwards: a fixed schedule (the order of every sum is fixed, so results
+    // are bit-reproducible), in step with the initial fill
+    int n_refill = 0;
+    auto grab = [&]() { return pbeg + kStages * W + (n_refill++ * W + warp) * kGroup; };
     int g_next = grab();
     int pid_next = lane < kGroup && g_next + lane < pend ? __ldg(ptab + g_next + lane) : -1;
+    // the scan's time budget (page_wait_ns from its start): a warp past it
+    // gives up its remaining pages as if a copy had stalled
+    const uint64_t t_scan = global_timer_ns();
     while (!done) {
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
@@ -1340,12 +1349,17 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
           done = true;
           break;
         }
+        if (h == 0 && global_timer_ns() - t_scan > p.page_wait_ns) {   // once per ring cycle
+          timed_out = true;
+          done = true;
+          break;
+        }
         const int nv = min(kGroup, pend - j0);   // this part's pages within the history
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
           const int s = kGroup * h + u;
           if (u == 0 || u < nv) {
-            if (!mbar_wait_bounded(bar + s, (parity >> s) & 1u, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(bar + s, (parity >> s) & 1u, p.page_wait_ns)) {
               timed_out = true;
             } else {
               pending &= ~(1u << s);
@@ -1448,7 +1462,9 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
               mbar_arrive_expect_tx(bar + s, kBlock);
               bulk_copy_g2s(ring + s * kBlock, pool + int64_t(pid_next) * page_stride, kBlock, bar + s);
             }
+            if (OSCAR_SERIAL_COPIES) mbar_wait_bounded(bar + s, (parity >> s) & 1u, kDrainWaitNs);
           }
+          if (OSCAR_SERIAL_COPIES) __syncwarp();
           pending |= (__ballot_sync(kFull, want) & kPartBits) << (kGroup * h);
           good[h] = __ballot_sync(kFull, good_id) & kPartBits;
           base[h] = g_next;
@@ -1462,7 +1478,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     // past the history) land before the CTA's shared memory goes away; each
     // wait is bounded
     for (int s = 0; s < kStages; ++s)
-      if ((pending >> s) & 1u) mbar_wait_bounded(bar + s, (parity >> s) & 1u, kWaitLimitNs);
+      if ((pending >> s) & 1u) mbar_wait_bounded(bar + s, (parity >> s) & 1u, kDrainWaitNs);
     __syncwarp();
     if constexpr (kLevels) {
       store_hist_state_levels<G>(st, my_state, gid, tig, p.pv_unscale, p.coef_v[0]);

@@ -44,6 +44,10 @@ __host__ __device__ constexpr int storage_channel_v(int ng, int c) {
   return ng == 1 ? c
                  : ((c & 7) / (8 / ng)) * (kHeadDim / ng) + ((c & 7) % (8 / ng)) * 16 + 2 * (c >> 4) + ((c >> 3) & 1);
 }
+// Bounded waits: the default limit of every wait and the limit of the
+// waits that let copies already issued land before a CTA exits.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+constexpr uint64_t kDrainWaitNs = 1000000000ull;
 constexpr int kPartStride = 132;  // floats per (split, head) partial: m, l, pad, pad, o[128]
 
 // Lazy online-softmax maximum: a running maximum m is raised only when a
@@ -160,6 +164,11 @@ struct DecodeParams {
   int32_t max_hist;
   // split plan
   int32_t n_splits, pages_per_split;
+  // time budget of a warp's page scan, and the limit of each wait for a page
+  // copy: past either the warp gives up the rest of its pages
+  // (OSCAR_DEV_TIMEOUT); copies already issued are still waited for, each up
+  // to kDrainWaitNs, before the CTA exits
+  uint64_t page_wait_ns;
   // the PV B operand is p s_V 2^pv_log2 (an integer pv_log2 keeps it in the
   // fp16 range): the INT2 states carry that factor in every term and keep
   // their maximum lowered by pv_log2; pv_unscale = 2^24 undoes the codes'

@@ -1,5 +1,6 @@
 // C-ABI entry points: host validation, split planning and kernel launches.
 // Every check runs before any launch; a rejected call launches nothing.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -10,6 +11,9 @@
 #include "trace.h"
 
 namespace {
+
+// limit of the decode kernel's waits for page copies (oscar_set_page_wait_limit)
+std::atomic<int64_t> g_page_wait_ns{int64_t(oscar::kDefaultWaitNs)};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -106,6 +110,10 @@ extern "C" const char* oscar_status_string(oscar_status s) {
 }
 
 extern "C" int32_t oscar_abi_version(void) { return OSCAR_ABI_VERSION; }
+
+extern "C" int64_t oscar_set_page_wait_limit(int64_t limit_ns) {
+  return g_page_wait_ns.exchange(limit_ns > 0 ? limit_ns : int64_t(oscar::kDefaultWaitNs));
+}
 
 extern "C" int64_t oscar_block_bytes(int32_t quant_group_k, int32_t quant_group_v) {
   const int gk = groups_of(quant_group_k), gv = groups_of(quant_group_v);
@@ -242,6 +250,7 @@ oscar_status prepare_decode(const oscar_layer_desc* desc, const uint16_t* q, flo
   }
   p.n_splits = plan.n_splits;
   p.pages_per_split = plan.pages_per_split;
+  p.page_wait_ns = uint64_t(g_page_wait_ns.load());
   // PV operand scale: p <= 2^kRescaleLog2 and s_V <= 2 tau_v / 3 (x2 margin
   // for fp16 rounding), so p s_V 2^pv_log2 stays below 2^14 in fp16
   int e = 0;

@@ -87,13 +87,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Waits for phase `parity` of `bar` for at most about `limit_ns`; false on
-// expiry.  Each try suspends the warp instead of spinning on issue slots.
+// expiry.  Each try suspends the warp instead of spinning on issue slots
+// (for at most 1 ms, or the limit if that is shorter).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns) {
-  if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+  const uint32_t hint = limit_ns < 1000000ull ? uint32_t(limit_ns) : 1000000u;
+  if (mbar_try_wait_sleep(bar, parity, hint)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }

@@ -94,6 +94,20 @@ const char* oscar_status_string(oscar_status s);
 int32_t oscar_abi_version(void);
 
 /*
+ * oscar_set_page_wait_limit - the decode kernel's time budget for a warp's
+ * scan of its INT2 pages, which also bounds each wait for a page copy to
+ * land.  A warp past it gives up the rest of its pages, sets
+ * OSCAR_DEV_TIMEOUT in dev_status, and the call's output must not be used.
+ * limit_ns <= 0 restores the default (1 s, far beyond any scan).  Returns
+ * the previous limit.  Copies already issued are still waited for (up to
+ * 1 s each) before a CTA exits, and the workspace stays ready for the next
+ * call.  A stalled copy is the only way this path runs in normal use; a
+ * short limit makes it run on purpose (tests of the failure path).
+ * Process-wide, read when a decode call is issued.  Host-only.
+ */
+int64_t oscar_set_page_wait_limit(int64_t limit_ns);
+
+/*
  * One attention layer's cache: a three-segment token pool, BF16 sink (64
  * tokens) | INT2 history (paged) | BF16 recent window (256-slot ring).
  * [ZAKER] pipeline part; [GIST] 2.2 B (hybrid-precision paged layout).

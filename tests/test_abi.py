@@ -379,3 +379,13 @@ def test_rotation_file_round_trip_and_damage(tmp_path, built_lib):
                                           big.ctypes.data, out.ctypes.data, out.ctypes.data) == 1
     assert B.lib.oscar_rotation_file_read(os.fsencode(str(tmp_path / "missing.bin")), n_layers, n_kv, d,
                                           big.ctypes.data, big.ctypes.data, out.ctypes.data, out.ctypes.data) == 7
+
+
+def test_page_wait_limit_setting(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    prev = B.oscar_set_page_wait_limit(12345)
+    try:
+        assert B.oscar_set_page_wait_limit(0) == 12345          # 0 restores the default
+        assert B.oscar_set_page_wait_limit(-5) == 1_000_000_000
+    finally:
+        B.oscar_set_page_wait_limit(prev)

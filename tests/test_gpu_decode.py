@@ -153,3 +153,33 @@ def test_scaled_caches(scales):
     subnormal code operands keep the output within the bar."""
     sc = H.Scenario(1013, [3000, 1500], n_kv=2, g=4, scales=scales)
     _check(sc)
+
+
+def test_expired_page_waits_are_flagged_and_the_workspace_recovers():
+    """With the page-scan budget at 20 ns every warp gives up its pages at
+    its first step: the call returns, the timeout bit is set, and the copies
+    already issued land before the kernel exits.  With the default limit
+    restored, the next call on the same workspace gives the oracle's output."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    sc = H.Scenario(1002, [100_000], n_kv=8, g=4, cal=(1024, 512))
+    cache, q = H.to_device(sc)
+    desc = cache.desc()
+    nbytes = B.oscar_decode_workspace_bytes(desc)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    prev = B.oscar_set_page_wait_limit(20)
+    try:
+        for _ in range(2):
+            cache.dev_status.zero_()
+            B.oscar_decode_attention(desc, q, out, ws, nbytes)
+            torch.cuda.synchronize()
+            assert int(cache.dev_status.item()) == B.DEV_TIMEOUT
+    finally:
+        assert B.oscar_set_page_wait_limit(prev) == 20
+    cache.dev_status.zero_()
+    B.oscar_decode_attention(desc, q, out, ws, nbytes)
+    torch.cuda.synchronize()
+    assert int(cache.dev_status.item()) == 0
+    err = H.relative_error(out.cpu().numpy().astype(np.float64), sc.expected())
+    assert err.max() <= TOL

@@ -73,6 +73,13 @@ def test_reference_arm_json_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["config"]["workload"] == "qwen3-8b-layer-decode-100k"
+    # ms_per_step is what a timed step measured; the whole-step figure the
+    # value comes from is carried apart
+    ex = line["extrapolation"]
+    assert ex["measured_ms_per_sample_step"] == line["ms_per_step"]
+    assert abs(ex["whole_step_ms"] - ex["factor"] * line["ms_per_step"]) <= 1e-6 * ex["whole_step_ms"]
+    assert abs(line["value"] - 1e3 / ex["whole_step_ms"]) <= 1e-9 * line["value"]
+    assert line["cpu_baseline"]["host_logical_cores"] >= 1 and line["cpu_baseline"]["host_cpu"]
 
 
 def test_decode_bytes_match_the_oracle_accounting():
