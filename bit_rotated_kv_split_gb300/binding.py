@@ -58,6 +58,8 @@ def _load():
         "oscar_build_canalized_rotation": (c_int32, [c_int32, c_int32, P]),
         "oscar_build_rotation_from_covariance": (c_int32, [P, c_int32, P, P]),
         "oscar_covariance": (c_int32, [P, c_int64, c_int32, c_int64, P, P, ctypes.POINTER(c_size_t), P]),
+        "oscar_value_covariance": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_int64, P, P,
+                                             ctypes.POINTER(c_size_t), P]),
         "oscar_score_weighted_rows": (c_int32, [P, c_int64, P, P, c_int64, c_int32, c_double, P]),
         "oscar_clip_threshold": (c_int32, [P, c_int64, c_int32, c_int32, P, c_double, P]),
         "oscar_fit_codebook": (c_int32, [P, c_int64, c_int32, P, c_double, c_int32, P]),
@@ -164,6 +166,25 @@ def oscar_covariance(x, c_out, workspace, stream=None) -> None:
     size = c_size_t(workspace.numel() * workspace.element_size())
     _check("oscar_covariance", lib.oscar_covariance(_ptr(x), n, 128, ld, _ptr(c_out), _ptr(workspace),
                                                     ctypes.byref(size), _stream(stream)))
+
+
+def oscar_value_covariance_workspace_bytes(n_q: int) -> int:
+    size = c_size_t(0)
+    _check("oscar_value_covariance", lib.oscar_value_covariance(None, int(n_q), None, None, 1, 128, 128, None, None,
+                                                                ctypes.byref(size), None))
+    return size.value
+
+
+def oscar_value_covariance(q, k, v, c_out, workspace, stream=None) -> None:
+    """c_out [128][128] fp32 (device) = (S V)^T (S V) / n_q, S = softmax(q k^T / sqrt(128)),
+    over bf16 rows q [n_q][ld], k, v [n_k][ld] (device, one row stride)."""
+    n_q, n_k, ld = int(q.shape[0]), int(k.shape[0]), int(q.stride(0))
+    if int(k.stride(0)) != ld or int(v.stride(0)) != ld or int(v.shape[0]) != n_k:
+        raise ValueError("q, k and v must share one row stride; k and v one row count")
+    size = c_size_t(workspace.numel() * workspace.element_size())
+    _check("oscar_value_covariance", lib.oscar_value_covariance(
+        _ptr(q), n_q, _ptr(k), _ptr(v), n_k, 128, ld, _ptr(c_out), _ptr(workspace), ctypes.byref(size),
+        _stream(stream)))
 
 
 def oscar_score_weighted_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float = None):

@@ -9,10 +9,14 @@
 //
 // The rotation of 128 tokens is one 128 x 128 x 128 contraction,
 // D[token][j] = sum_i x[token][i] R[i][j], on tcgen05 (M = N = 128, K = 16
-// per instruction, fp32 accumulators in tensor memory).  x is bf16, exact in
-// fp16 within the fp16 range (larger magnitudes saturate at 65504); R is
-// scaled by 16 and split into fp16 hi + lo parts (about 22 significant
-// bits), so D = x.(16 R)_hi + x.(16 R)_lo and x~ = D / 16.
+// per instruction, fp32 accumulators in tensor memory).  x is bf16: each
+// token's row is scaled by a power of two 2^-e that puts its largest
+// magnitude in [2^14, 2^15), which makes every element of 8 significant
+// bits down to 2^-31 of that maximum exact in fp16 at any magnitude of the
+// row; R is scaled by 16 and split into fp16 hi + lo parts (about 22
+// significant bits), so D = x.(16 R)_hi + x.(16 R)_lo and x~ = 2^e D / 16.
+// (Scaling by a power of two commutes with the fp32 sums, so a row whose
+// elements were exact in fp16 unscaled gives the same D times 2^-e.)
 //
 // CTA (tile stride, KV head, K|V) of 13 warps, one CTA per SM:
 //   warps 8-11 bring a tile's 128 source rows into the A operand: with
@@ -101,19 +105,57 @@ struct Waiter {
   }
 };
 
-// Epilogue of one token-half: v[i] = 16 x~ at code position 64 hh + i, whose
+// The token's row scale 2^-e, from the largest magnitude bits mb (bf16,
+// sign cleared) over its 128 elements: e = (biased exponent) - 141, so the
+// scaled maximum lies in [2^14, 2^15); 0 for a zero row or one holding an
+// infinity or NaN; at least -126 (2^e stays a normal float; a subnormal
+// bf16 row scaled by 2^126 is still at least 2^-7).
+__device__ __forceinline__ int row_exponent(uint32_t mb) {
+  if (mb == 0u || mb >= 0x7F80u) return 0;
+  return max(int(mb >> 7) - 141, -126);
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }   // e in [-126, 127]
+
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint4 raw) {
+  acc = __vmaxu2(acc, raw.x & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, raw.y & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, raw.z & 0x7FFF7FFFu);
+  return __vmaxu2(acc, raw.w & 0x7FFF7FFFu);
+}
+
+// 8 bf16 times 2^-e -> 8 fp16 (exact products: a power of two)
+__device__ __forceinline__ uint4 to_f16_scaled(uint4 raw, float sc) {
+  const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t h[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = f16x2_sat(bf16_lo(wv[e]) * sc, bf16_hi(wv[e]) * sc);
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// Epilogue of one token-half: v[i] = 16 x~ 2^-e at code position 64 hh + i, whose
 // quantisation group is ((64 hh + i) & 7) / (8 / NG) in the page format (K
 // and V alike).  The two halves of a token meet on each group's (min, max)
 // through shared memory; then the group's fp16 scale and zero point, the
-// codes (16 bytes) and, from half 0, the token's NG (scale, zero) pairs are
-// stored.  kLevels (codebook): the code is the number of the thresholds thr
+// The row scale 2^e is folded into the extremes and the code
+// coefficients (exact: powers of two; a48 stays a normal float since a
+// nonzero fp16 scale needs a row maximum of at least 2^-26, e >= -40); a
+// row scaled down (e > 0) multiplies its values back first, so that no
+// coefficient can overflow.  kLevels (codebook): the code is the number of the thresholds thr
 // strictly below u = (x - zero) / scale, u formed with the reciprocal of the
 // scale.  Returns false when the exchange wait expired.
 template <int NG, bool kLevels>
-__device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&v)[kHeadDim / 2], float2* xchg,
+__device__ __forceinline__ bool epi_finish(const DemoteParams& p, float (&v)[kHeadDim / 2], float2* xchg,
                                            uint64_t* xfull, Waiter& wt, int k, int hh, int j, int2 m, float tau,
                                            int which, int head, const float* thr) {
   constexpr int kSpan = 8 / NG;   // consecutive positions (mod 8) per group
+  const int slot = m.y & (kPage - 1), e = (m.y >> 4) - 256;
+  float fold = pow2f(e);
+  if (e > 0) {
+#pragma unroll
+    for (int i = 0; i < kHeadDim / 2; ++i) v[i] *= fold;
+    fold = 1.f;
+  }
   // clipping moves only the extremes: min and max of the clipped values
   // are the clipped min and max, and a value beyond +-tau gets the code
   // of the clipped extreme (0 or 3) through the final clamp
@@ -150,15 +192,15 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
   float a48[NG], nzi3[NG], a16[NG], nzi[NG];
 #pragma unroll
   for (int q = 0; q < NG; ++q) {
-    const float lo = fminf(fmaxf(mn[q] * (1.f / kRScale), -tau), tau);
-    const float hi = fminf(fmaxf(mx[q] * (1.f / kRScale), -tau), tau);
+    const float lo = fminf(fmaxf(mn[q] * fold * (1.f / kRScale), -tau), tau);
+    const float hi = fminf(fmaxf(mx[q] * fold * (1.f / kRScale), -tau), tau);
     s16[q] = __float2half_rn(__fdiv_rn(hi - lo, 3.0f));
     z16[q] = __float2half_rn(lo);
     const float s = __half2float(s16[q]), z = __half2float(z16[q]);
     const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-    a48[q] = inv * (1.f / (3.f * kRScale));
+    a48[q] = inv * (1.f / (3.f * kRScale)) * fold;
     nzi3[q] = -z * inv * (1.f / 3.f);
-    a16[q] = inv * (1.f / kRScale);
+    a16[q] = inv * (1.f / kRScale) * fold;
     nzi[q] = -z * inv;
   }
   const float kMagic = 12582912.f;
@@ -183,11 +225,11 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
   }
   uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v);
   if (which == 0) {
-    *reinterpret_cast<uint4*>(blk + 32 * m.y + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(blk + 32 * slot + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
   } else {
     // V rows interleave the two tokens of a slot pair by 16-bit halves: the
     // eight halves 8 hh .. 8 hh + 7 of this token go 4 bytes apart
-    uint16_t* dst = reinterpret_cast<uint16_t*>(blk + v_code_byte(m.y, 16 * hh));
+    uint16_t* dst = reinterpret_cast<uint16_t*>(blk + v_code_byte(slot, 16 * hh));
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       dst[4 * u] = uint16_t(w[u] & 0xFFFFu);
@@ -201,7 +243,7 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, const float (&
       sz[q] = uint32_t(__half_as_ushort(s16[q])) | (uint32_t(__half_as_ushort(z16[q])) << 16);
     // (4-byte stores: with K and V pairs side by side a token's pairs are
     // only 4-byte aligned in general)
-    uint32_t* dst = reinterpret_cast<uint32_t*>(blk + pair_byte(p.ng_k, p.ng_v, m.y, which, 0));
+    uint32_t* dst = reinterpret_cast<uint32_t*>(blk + pair_byte(p.ng_k, p.ng_v, slot, which, 0));
 #pragma unroll
     for (int q = 0; q < NG; ++q) dst[q] = sz[q];
   }
@@ -374,38 +416,37 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
         }
       }
       uint8_t* a = abuf + buf * kOpBytes;
+      int row_e = 0;
       if (p.use_tma) {
-        // bf16 -> fp16 in place, row j of every 8-column block
+        // bf16 -> fp16 times the row scale in place, row j of every
+        // 8-column block (a first pass finds the row's largest magnitude)
         if (!wt.wait(tma_full + buf, (k / kBufs) & 1)) break;
+        uint32_t mb2 = 0u;
+#pragma unroll
+        for (int c = 0; c < kHeadDim / 8; ++c) mb2 = absmax_bf16x2(mb2, *reinterpret_cast<const uint4*>(a + c * 2048 + j * 16));
+        row_e = row_exponent(max(mb2 & 0xFFFFu, mb2 >> 16));
+        const float sc = pow2f(-row_e);
 #pragma unroll
         for (int c = 0; c < kHeadDim / 8; ++c) {
           uint4* q = reinterpret_cast<uint4*>(a + c * 2048 + j * 16);
-          const uint4 raw = *q;
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t h[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) h[e] = f16x2_sat(bf16_lo(wv[e]), bf16_hi(wv[e]));
-          *q = make_uint4(h[0], h[1], h[2], h[3]);
+          *q = to_f16_scaled(*q, sc);
         }
       } else {
         const uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
+        uint4 raw[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4 raw[8];
+        for (int c = 0; c < 16; ++c)
+          raw[c] = live ? __ldg(reinterpret_cast<const uint4*>(src + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t mb2 = 0u;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            raw[c] = live ? __ldg(reinterpret_cast<const uint4*>(src + 64 * half + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < 16; ++c) mb2 = absmax_bf16x2(mb2, raw[c]);
+        row_e = row_exponent(max(mb2 & 0xFFFFu, mb2 >> 16));
+        const float sc = pow2f(-row_e);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t wv[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-            uint32_t h[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = f16x2_sat(bf16_lo(wv[e]), bf16_hi(wv[e]));
-            *reinterpret_cast<uint4*>(a + a_offset(j, 64 * half + 8 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
-          }
-        }
+        for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(a + a_offset(j, 8 * c)) = to_f16_scaled(raw[c], sc);
       }
-      meta[buf * kTile + j] = make_int2(live ? page : -1, pos % kPage);
+      // (page, slot | (e + 256) << 4): the epilogue's store target and row scale
+      meta[buf * kTile + j] = make_int2(live ? page : -1, (pos % kPage) | ((row_e + 256) << 4));
       fence_proxy_async_smem();
       mbar_arrive(a_full + buf);
     }

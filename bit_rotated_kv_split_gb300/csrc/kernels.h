@@ -206,4 +206,11 @@ size_t covariance_workspace_bytes(int64_t n);
 cudaError_t launch_covariance(const uint16_t* x, int64_t n, int64_t ld, float* c, void* workspace,
                               cudaStream_t stream);
 
+// C_S = (S V)^T (S V) / n_q, S = row-softmax(Q K^T / sqrt(128)), over bf16
+// rows of q [n_q], k and v [n_k] (ld elements apart): the fp32 rows of S V,
+// then their covariance (partials added in a fixed order).
+size_t value_covariance_workspace_bytes(int64_t n_q);
+cudaError_t launch_value_covariance(const uint16_t* q, int64_t n_q, const uint16_t* k, const uint16_t* v,
+                                    int64_t n_k, int64_t ld, float* c, void* workspace, cudaStream_t stream);
+
 }  // namespace oscar

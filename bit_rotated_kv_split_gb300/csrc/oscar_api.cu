@@ -344,3 +344,24 @@ extern "C" oscar_status oscar_covariance(const uint16_t* x, int64_t n, int32_t d
   const cudaError_t err = oscar::launch_covariance(x, n, ld, c_out, workspace, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
+
+// [GIST] 2.1 / 2.2 A: C_S from calibration queries, keys and values.
+extern "C" oscar_status oscar_value_covariance(const uint16_t* q, int64_t n_q, const uint16_t* k, const uint16_t* v,
+                                               int64_t n_k, int32_t d, int64_t ld, float* c_out, void* workspace,
+                                               size_t* workspace_bytes, void* stream) {
+  OSCAR_TRACE_CALL();
+  if (!workspace_bytes || n_q < 1 || n_k < 1 || d != 128 || ld < d) return OSCAR_ERR_INVALID_ARG;
+  const size_t need = oscar::value_covariance_workspace_bytes(n_q);
+  if (!workspace) {
+    *workspace_bytes = need;
+    return OSCAR_OK;
+  }
+  if (*workspace_bytes < need) return OSCAR_ERR_WORKSPACE;
+  if (!q || !k || !v || !c_out) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || (ld % 8) != 0 || !aligned(c_out, 16) ||
+      !aligned(workspace, 256))
+    return OSCAR_ERR_ALIGNMENT;
+  const cudaError_t err =
+      oscar::launch_value_covariance(q, n_q, k, v, n_k, ld, c_out, workspace, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

@@ -222,6 +222,26 @@ oscar_status oscar_covariance(const uint16_t* x, int64_t n, int32_t d, int64_t l
                               void* workspace, size_t* workspace_bytes, void* stream);
 
 /*
+ * oscar_value_covariance - the score-weighted value covariance on the
+ * device.  [GIST] 2.1 and 2.2 A (C_S = (1/N) V^T S^T S V, S = row-softmax of
+ * the calibration scores).
+ *
+ *   c_out (device, [d][d] row-major, fp32) = (S V)^T (S V) / n_q with
+ *   S = row-softmax(q k^T / sqrt(d)), over device bf16 rows q [n_q], k and
+ *   v [n_k] (row r at base + r * ld, d = 128 values each).  The rows of S V
+ *   are formed in fp32 (exact bf16 products in Q K^T, an fp32 softmax, P
+ *   split into two bf16 parts against the bf16 values), then their
+ *   covariance as fp32 partials of 256 rows added in a fixed order.  If
+ *   workspace is NULL the required size is written to *workspace_bytes and
+ *   nothing runs; otherwise asynchronous on `stream`.  q, k, v 16-byte
+ *   aligned, ld a multiple of 8, c_out 16-byte and workspace 256-byte
+ *   aligned (OSCAR_ERR_ALIGNMENT); n_q, n_k >= 1 and d = 128.
+ */
+oscar_status oscar_value_covariance(const uint16_t* q, int64_t n_q, const uint16_t* k, const uint16_t* v,
+                                    int64_t n_k, int32_t d, int64_t ld, float* c_out, void* workspace,
+                                    size_t* workspace_bytes, void* stream);
+
+/*
  * oscar_score_weighted_rows - rows of S.V for the value covariance
  * C_S = (1/N) V^T S^T S V.  [GIST] 2.1 and 2.2 A.
  *
@@ -312,6 +332,12 @@ oscar_status oscar_rotation_file_read(const char* path, int32_t n_layers, int32_
  *   lower), 0 if scale is 0.  The codes and (scale, zero) pairs go to history
  *   position dst_pos[i] of request dst_req[i] through desc->page_table, in the
  *   pool layout above.  K and V are both written.
+ *
+ *   Any finite bf16 row is accepted at any magnitude: calls of n >= 1024
+ *   items (the tensor-core path) scale each token-head row by a power of two
+ *   before its fp16 operands are formed and scale the result back, so rows
+ *   beyond the fp16 range or below its normal range are rotated like any
+ *   other.  Rows holding an infinity or a NaN give unspecified codes.
  *
  *   new_k / new_v (nullable, both or neither): [n][H_kv][d] bf16 rows that
  *   replace the demoted source rows after they have been read - the decode

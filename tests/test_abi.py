@@ -187,6 +187,30 @@ def test_covariance_rejects_bad_arguments(built_lib):
                                 ctypes.byref(small), None) == 3
 
 
+def test_value_covariance_rejects_bad_arguments(built_lib):
+    from bit_rotated_kv_split_gb300 import binding as B
+    lib = B.lib
+    size = ctypes.c_size_t(0)
+    f = lib.oscar_value_covariance
+    assert f(None, 0, None, None, 1, 128, 128, None, None, ctypes.byref(size), None) == 1
+    assert f(None, 10, None, None, 0, 128, 128, None, None, ctypes.byref(size), None) == 1
+    assert f(None, 10, None, None, 1, 64, 128, None, None, ctypes.byref(size), None) == 1
+    assert f(None, 10, None, None, 1, 128, 100, None, None, ctypes.byref(size), None) == 1
+    assert f(None, 10, None, None, 1, 128, 128, None, None, None, None) == 1
+    # the S V rows (fp32, padded to 256 bytes) and one 128 x 128 fp32
+    # partial per 256 rows
+    assert f(None, 1000, None, None, 1, 128, 128, None, None, ctypes.byref(size), None) == 0
+    assert size.value == 1000 * 512 + 4 * 128 * 128 * 4
+    assert B.oscar_value_covariance_workspace_bytes(1000) == size.value
+    small = ctypes.c_size_t(size.value - 1)
+    a = ctypes.c_void_p(256)
+    assert f(a, 1000, a, a, 1, 128, 128, a, a, ctypes.byref(small), None) == 3
+    ok = ctypes.c_size_t(size.value)
+    # a row stride that is not a whole number of 16-byte units
+    assert f(a, 1000, a, a, 1, 128, 132, a, a, ctypes.byref(ok), None) == 2
+    assert f(ctypes.c_void_p(258), 1000, a, a, 1, 128, 128, a, a, ctypes.byref(ok), None) == 2
+
+
 def test_block_bytes_match_the_format(built_lib):
     # the library's block size equals the oracle's grouped format for every
     # valid pair of group sizes (0 means 128), and 0 for anything else

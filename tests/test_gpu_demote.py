@@ -29,7 +29,7 @@ def _pre_rounding(x_rot_clipped):
 
 
 def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None, first_row=None,
-         groups=None, levels=None):
+         groups=None, levels=None, scale=None):
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
@@ -40,6 +40,12 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         rk32, rv32, tau_k, tau_v = H.canalized_rotations(seed, 0, n_kv, outl, canalized_block)
     xk = synth.activations(seed, (1, 0), n_tok, outl)
     xv = synth.activations(seed, (1, 1), n_tok, outl)
+    if scale is not None:
+        # rows scaled by a power of two (still bf16 values), thresholds with
+        # them up to the largest the library accepts
+        xk = xk * np.float32(scale)
+        xv = xv * np.float32(scale)
+        tau_k, tau_v = min(tau_k * scale, 65504.0), min(tau_v * scale, 65504.0)
     g = synth.generator(seed, 5)
     src_index = g.permutation(n_tok).astype(np.int32)
     if first_row is not None:
@@ -339,6 +345,33 @@ def test_same_tokens_through_both_paths(groups):
         d = int(np.sum(res[False][which][1] != res[True][which][1]))
         print("KV"[which], "codes differing between the paths:", d, res[False][which][0], res[True][which][0])
         assert d <= 2 * 1e-4 * res[False][which][1].size
+
+
+@pytest.mark.parametrize("scale", [2.0 ** 12, 2.0 ** -20, 2.0 ** -60])
+def test_rows_far_from_unit_magnitude_through_both_paths(scale):
+    """Rows scaled by 2^12 (elements far beyond the fp16 range; thresholds
+    capped at 65504), by 2^-20 (most elements below fp16's normal range) and
+    by 2^-60 (every scale rounds to fp16 zero): the tensor-core kernel
+    (contiguous rows) and the per-token kernel both meet the code rule
+    against the oracle, which rotates the bf16 rows in float64."""
+    seed, n, n_kv = 2022, 1200, 2
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    xk = synth.activations(seed, (5, 0), n, outl) * np.float32(scale)
+    xv = synth.activations(seed, (5, 1), n, outl) * np.float32(scale)
+    tau_k, tau_v = min(tau_k * scale, 65504.0), min(tau_v * scale, 65504.0)
+    for per_step in (False, True):
+        pool, table = _demote_rows(xk, xv, rk32, rv32, tau_k, tau_v, per_step)
+        res = _parity_of_pool(pool, table, xk, xv, rk32, rv32, tau_k, tau_v)
+        print("per-step" if per_step else "bulk", res[0][0], res[1][0])
+
+
+@pytest.mark.parametrize("scale", [2.0 ** 12, 2.0 ** -20])
+def test_bulk_gathered_rows_far_from_unit_magnitude(scale):
+    # the tensor-core kernel's gathered-row loader (an index array)
+    g = synth.generator(7, 1)
+    pos = g.permutation(2500)[:2000]
+    print(_run(2023, 2000, 2, positions=pos, scale=scale))
 
 
 @pytest.mark.parametrize("groups", [(128, 128), (32, 32)])
