@@ -85,6 +85,9 @@ def _args():
     ap.add_argument("--quant-group", default="128,128",
                     choices=["%d,%d" % (a, b) for a in (32, 64, 128) for b in (32, 64, 128)],
                     help="quantisation group sizes of K and V (channels), for every GPU workload")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests of a --workload other than the default (0: the workload's own); a smaller "
+                         "batch of the same kernel, for profiler captures")
     ap.add_argument("--codebook", default="uniform", choices=["uniform", "lloyd-max"],
                     help="code levels: the uniform scale/zero grid, or per-layer Lloyd-Max levels fitted on "
                          "the calibration rows (one quantisation group per vector)")
@@ -833,7 +836,7 @@ def run_extra(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     n_q, n_kv, seed, L, nd = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["seed"], cfg["layers"], cfg["distinct_layers"]
-    bsz = cfg["batch"]
+    bsz = args.batch or cfg["batch"]
     K, W = args.steps, args.warmup
     peak, peak_kind = _roofline_peak()
     rots = [_rotations_for(B, seed, n_kv, i) for i in range(nd)]
@@ -984,15 +987,17 @@ def run_extra(args):
     logical = _decode_bytes(sum(hist), bf16_tok, n_q * bsz, n_kv, sum(-(-h // 16) for h in hist))
     unique = _decode_bytes(uniq, bf16_tok, n_q * bsz, n_kv, sum(-(-h // 16) for h in hist))
     status = max(int(c.dev_status.item()) for c in caches)
-    metric = ("36-layer decode-step tokens/s (Qwen3-4B shape, batch 28, 100k ctx, 1 demotion per request-layer)"
-              if L > 1 else "decode tokens/s (Qwen3-32B layer, batch 64, ragged 8k-128k ctx, shared 32k prefix)")
+    metric = ("36-layer decode-step tokens/s (Qwen3-4B shape, batch %d, 100k ctx, 1 demotion per request-layer)"
+              if L > 1 else "decode tokens/s (Qwen3-32B layer, batch %d, ragged 8k-128k ctx, shared 32k prefix)") % bsz
     line.update({
         "metric": metric, "value": bsz / t_step, "unit": "tokens/s", "ms_per_step": t_step * 1e3,
         "config": {"workload": args.workload, "batch": bsz, "n_q_heads": n_q, "n_kv_heads": n_kv, "head_dim": 128,
                    "layers": L, "distinct_layers": nd, "ctx_min": min(ctxs), "ctx_max": max(ctxs),
                    "quant_group": _group_label(),
                    "ctx_mean": sum(ctxs) / bsz, "shared_prefix_tokens": cfg.get("shared", 0),
-                   "l2_policy": "inputs larger than L2 (each layer cache > 1 GB)", "cuda_graphs": True},
+                   "l2_policy": "inputs %s than L2: %d distinct layer caches, each read %.0f MB per decode "
+                                "(unique) against 129 MB of L2" % ("larger" if unique > 129e6 else "NOT larger",
+                                                                    nd, unique / 1e6), "cuda_graphs": True},
         "decode_ms": t_dec * 1e3,
         "roofline": {"bound": "hbm", "achieved": unique / t_dec / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": unique / t_dec / 1e9 / peak, "kernel": "split_kernel (oscar_decode_attention)",

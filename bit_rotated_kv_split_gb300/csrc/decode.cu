@@ -1064,7 +1064,10 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   uint64_t* pro_done = bars + W * kStages + 2;   // q~ fragments ready (after R_K, R_V)
   constexpr int PT = Geo<G>::PT;
 
-  const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
+  // grid (KV head, request, split): CTAs start split-major, so the first
+  // splits of every request (full when its history reaches past them) go
+  // first and the shorter or empty later splits fill the last waves
+  const int split = blockIdx.z, hkv = blockIdx.x, b = blockIdx.y;
   const int pair = b * p.n_kv + hkv;
   const int n_splits = p.n_splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1676,7 +1679,7 @@ cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
   constexpr size_t smem = Geo<G, NGK, NGV, kLevels>::kSmem;
   cudaError_t e = set_smem_limit<split_kernel<G, NGK, NGV, kLevels>>(int(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(split_kernel<G, NGK, NGV, kLevels>, dim3(p.n_splits, p.n_kv, p.batch), dim3(Geo<G>::T),
+  return launch_pdl(split_kernel<G, NGK, NGV, kLevels>, dim3(p.n_kv, p.batch, p.n_splits), dim3(Geo<G>::T),
                     smem, stream, p);
 }
 

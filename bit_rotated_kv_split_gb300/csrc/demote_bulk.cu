@@ -182,7 +182,6 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, float (&v)[kHe
     mn[q] = fminf(mn[q], other.x);
     mx[q] = fmaxf(mx[q], other.y);
   }
-  if (m.x < 0) return true;
   // code = clamp(rint((x - z) / s), 0, 3) with x = D / 16: one saturating
   // FMA gives (x - z) / (3 s) clamped to [0, 1]; a second FMA scales by 3
   // and adds 1.5 * 2^23, which rounds to an integer held in the float's
@@ -223,12 +222,35 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, float (&v)[kHe
     }
     w[u] = kLevels ? word : word - kBitsSum;
   }
+  // V rows interleave the two tokens of a slot pair by 16-bit halves.  When
+  // the neighbouring lane (token j ^ 1 of the tile, same half hh) holds the
+  // other token of this token's slot pair in the same page - consecutive
+  // positions from an even one, as in a prefill - the two lanes trade half
+  // their codes and each stores 16 bytes of whole words; otherwise each
+  // lane stores its eight halves 4 bytes apart.  (Every lane takes part in
+  // the exchange, stored or not; lanes run in step here.)
+  const unsigned am = __activemask();
+  const int lane = int(threadIdx.x & 31);
+  const bool odd = lane & 1;
+  const int ppage = __shfl_xor_sync(am, m.x, 1), pslot = __shfl_xor_sync(am, slot, 1);
+  const bool paired = which == 1 && ((am >> (lane ^ 1)) & 1u) && m.x >= 0 && ppage == m.x &&
+                      (slot & 1) == int(odd) && (pslot ^ 1) == slot;
+  const uint32_t r0 = __shfl_xor_sync(am, odd ? w[0] : w[2], 1);
+  const uint32_t r1 = __shfl_xor_sync(am, odd ? w[1] : w[3], 1);
+  if (m.x < 0) return true;
   uint8_t* blk = p.pages + (int64_t(m.x) * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v);
   if (which == 0) {
     *reinterpret_cast<uint4*>(blk + 32 * slot + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if (paired) {
+    // word i of the pair's row = (even token's half i | odd token's half i);
+    // the even lane stores words 8 hh .. 8 hh + 3, the odd lane the next four
+    const uint4 v = odd ? make_uint4(prmt(r0, w[2], 0x5410), prmt(r0, w[2], 0x7632), prmt(r1, w[3], 0x5410),
+                                     prmt(r1, w[3], 0x7632))
+                        : make_uint4(prmt(w[0], r0, 0x5410), prmt(w[0], r0, 0x7632), prmt(w[1], r1, 0x5410),
+                                     prmt(w[1], r1, 0x7632));
+    *reinterpret_cast<uint4*>(blk + v_code_byte(slot & ~1, 16 * hh) + (odd ? 16 : 0)) = v;
   } else {
-    // V rows interleave the two tokens of a slot pair by 16-bit halves: the
-    // eight halves 8 hh .. 8 hh + 7 of this token go 4 bytes apart
+    // the eight halves 8 hh .. 8 hh + 7 of this token go 4 bytes apart
     uint16_t* dst = reinterpret_cast<uint16_t*>(blk + v_code_byte(slot, 16 * hh));
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
