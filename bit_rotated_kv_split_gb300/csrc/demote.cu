@@ -17,6 +17,7 @@
 // format.  Splitting the inputs over the warps shortens the
 // dependent chain of a lone item (a decode step demotes one token per
 // request) from 128 to 32 steps.
+#include "demote_math.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -43,8 +44,6 @@ constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
 template <int NG, bool kLevels>
 __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* red, int which, int head,
                                             int64_t page, int slot, float tau, int lane, const float* thr) {
-  constexpr int kSpan = 8 / NG;
-  const bool odd = lane & 1;
   float v[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -52,43 +51,8 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
     v[c] = (red[ch] + red[kHeadDim + ch]) + (red[2 * kHeadDim + ch] + red[3 * kHeadDim + ch]);
     v[c] = fminf(fmaxf(v[c], -tau), tau);
   }
-  float s[NG], z[NG];
   __half s16[NG], z16[NG];
-#pragma unroll
-  for (int q = 0; q < NG; ++q) {
-    float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const bool in = odd ? ((4 + c) / kSpan == q) : (c / kSpan == q);
-      mn = in ? fminf(mn, v[c]) : mn;
-      mx = in ? fmaxf(mx, v[c]) : mx;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    s16[q] = __float2half_rn(__fdiv_rn(mx - mn, 3.0f));
-    z16[q] = __float2half_rn(mn);
-    s[q] = __half2float(s16[q]);
-    z[q] = __half2float(z16[q]);
-  }
-  uint32_t byte = 0;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float sc = odd ? s[(4 + c) / kSpan] : s[c / kSpan];
-    const float zc = odd ? z[(4 + c) / kSpan] : z[c / kSpan];
-    uint32_t code = 0u;
-    if (sc > 0.f) {
-      const float u = __fdiv_rn(v[c] - zc, sc);
-      if constexpr (kLevels) {
-        code = uint32_t(u > thr[0]) + uint32_t(u > thr[1]) + uint32_t(u > thr[2]);
-      } else {
-        code = uint32_t(fminf(fmaxf(rintf(u), 0.f), 3.f));
-      }
-    }
-    byte |= code << (2 * c);
-  }
+  const uint32_t byte = quantize_lane<NG, kLevels>(v, lane, thr, s16, z16);
   if (page < 0 || page >= p.n_pages) {
     if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
     return;
