@@ -8,13 +8,11 @@ recent.  Synthetic seeded data: N(0,1) with 4 outlier channels x20 per KV
 head; rotations and clip thresholds built by the library from 4096 seeded
 calibration queries and 2048 calibration keys/values per KV head.
 
-One step = the whole hot path once: the oldest recent token of every KV
-head is rotated, clipped, quantised, packed into history and the new token
-written into the freed ring slot, then decode attention (q pre-rotation,
-INT2 split-KV scan, BF16 sink/recent scan, merge and output rotation).  By
-default the step is one kernel (oscar_decode_step_ring, the demotion inside
-the attention kernel); --step separate runs oscar_quantize_append +
-oscar_decode_attention.  The step is replayed from a steady state (lengths do not advance,
+One step = the whole hot path once: oscar_quantize_append (the oldest recent
+token of every KV head is rotated, clipped, quantised, packed into history,
+and the new token written into the freed ring slot) + oscar_decode_attention
+(q pre-rotation, INT2 split-KV scan, BF16 sink/recent scan, merge and output
+rotation).  The step is replayed from a steady state (lengths do not advance,
 so every step does identical work).  Steps cycle over several independent
 copies of the layer cache whose total size exceeds 3x the L2 cache, so no
 step reads its inputs from L2 (inputs larger than L2; no flush needed).
@@ -87,10 +85,6 @@ def _args():
     ap.add_argument("--quant-group", default="128,128",
                     choices=["%d,%d" % (a, b) for a in (32, 64, 128) for b in (32, 64, 128)],
                     help="quantisation group sizes of K and V (channels), for every GPU workload")
-    ap.add_argument("--step", default="ring", choices=["ring", "separate"],
-                    help="how the default workload's step runs: one kernel (oscar_decode_step_ring: demotion "
-                         "inside the attention kernel) or two (oscar_quantize_append + oscar_decode_attention); "
-                         "grouped and codebook layers always take two")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests of a --workload other than the default (0: the workload's own); a smaller "
                          "batch of the same kernel, for profiler captures")
@@ -570,49 +564,31 @@ def run_gpu(args):
     def decode(i):
         B.oscar_decode_attention(descs[i], q, out, ws, ws_bytes)
 
-    # one-kernel step: the same token moves (the newest ring slot's token is
-    # demoted into history position h - 1 and the slot takes the new token)
-    # inside the attention kernel
-    ring = args.step == "ring" and (w["group_k"], w["group_v"]) == (128, 128) and w["codebook"] == "uniform"
-
-    def ring_step(i):
-        B.oscar_decode_step_ring(descs[i], new_k.view(torch.uint16), new_v.view(torch.uint16), q, out, ws,
-                                 ws_bytes, stream=stream.cuda_stream)
-
-    def one_step(i):
-        if ring:
-            ring_step(i)
-        else:
-            demote(i)
-            decode(i)
-
-    # CUDA graphs: one per layer copy holding a whole step, and "kernel"
-    # graphs holding every copy's one-kernel step, decode and demotion back
-    # to back, for the per-kernel durations
+    # CUDA graphs: one per layer copy holding a whole step (demotion +
+    # decode), and two "kernel" graphs holding every copy's decode (resp.
+    # demotion) back to back, for the per-kernel durations
     stream = torch.cuda.Stream()
     use_graphs = True
     g_step, g_chain, g_decode, g_demote = [], None, None, None
     try:
         with torch.cuda.stream(stream):
             for i in range(n_copies):
-                one_step(i)
+                demote(i)
+                decode(i)
             torch.cuda.synchronize()
             for i in range(n_copies):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    one_step(i)
+                    demote(i)
+                    decode(i)
                 g_step.append(g)
             # every copy's step in order, as a serving loop replays all layers
             # (kernel to kernel edges are programmatic launches)
             g_chain = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_chain, stream=stream):
                 for i in range(n_copies):
-                    one_step(i)
-            if ring:
-                g_ring = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_ring, stream=stream):
-                    for i in range(n_copies):
-                        ring_step(i)
+                    demote(i)
+                    decode(i)
             g_decode, g_demote = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_decode, stream=stream):
                 for i in range(n_copies):
@@ -629,7 +605,8 @@ def run_gpu(args):
         if use_graphs:
             g_step[i].replay()
         else:
-            one_step(i)
+            demote(i)
+            decode(i)
 
     def run_steps(n):
         """n steps over the layer copies 0, 1, ... in order (whole chains, then single steps)."""
@@ -681,16 +658,11 @@ def run_gpu(args):
         for _ in range(reps):
             run_all(g_demote, demote)
         ev[4].record(stream)
-        if ring:
-            for _ in range(reps):
-                run_all(g_ring if use_graphs else None, ring_step)
-        ev[5].record(stream)
         torch.cuda.synchronize()
         clk = clocks.stop()
     total_ms = ev[0].elapsed_time(ev[1])
     decode_ms = ev[2].elapsed_time(ev[3]) / (reps * n_copies)
     demote_ms = ev[3].elapsed_time(ev[4]) / (reps * n_copies)
-    ring_ms = ev[4].elapsed_time(ev[5]) / (reps * n_copies) if ring else None
     t_step = total_ms / K / 1e3
     status = max(int(L.dev_status.item()) for L in layers)
 
@@ -713,15 +685,9 @@ def run_gpu(args):
 
     def step_e2e(i):
         # one library call: H2D copy of the step's inputs, demotion, decode,
-        # D2H copy of the output (the demotion inside the attention kernel
-        # when the step runs as one kernel)
-        if ring:
-            B.oscar_decode_step_ring(descs[i], nk16, nv16, q_e, out, ws, ws_bytes, host_in=inp_host, dev_in=inp,
-                                     in_bytes=in_bytes, host_out=out_host, stream=sh)
-        else:
-            B.oscar_decode_step(descs[i], inp_host, inp, in_bytes, rk16[i], rv16[i], bsz * w["recent"],
-                                n_kv * 128, src, dst_req, dst_pos, bsz, nk16, nv16, q_e, out, ws, ws_bytes,
-                                out_host, stream=sh)
+        # D2H copy of the output
+        B.oscar_decode_step(descs[i], inp_host, inp, in_bytes, rk16[i], rv16[i], bsz * w["recent"], n_kv * 128,
+                            src, dst_req, dst_pos, bsz, nk16, nv16, q_e, out, ws, ws_bytes, out_host, stream=sh)
 
     ke = min(K, 500)
     with torch.cuda.stream(stream):
@@ -743,12 +709,7 @@ def run_gpu(args):
     if rank == 0:
         peak, peak_kind = _roofline_peak()
         nbytes = bytes_per_decode()
-        # the one-kernel step also reads the displaced token's K and V rows and
-        # writes the ring rows and the demoted token (72 B) per (request, KV
-        # head); the new rows are read once, as the newest recent token
-        step_bytes = nbytes + bsz * n_kv * (2 * 256 + 2 * 256 + 72)
-        k_ms, k_bytes = (ring_ms, step_bytes) if ring else (decode_ms, nbytes)
-        achieved = k_bytes / (k_ms / 1e3) / 1e9
+        achieved = nbytes / (decode_ms / 1e3) / 1e9
         line = {
             "metric": METRIC, "value": world * bsz / t_step, "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": t_step * 1e3, "higher_is_better": True,
@@ -758,22 +719,19 @@ def run_gpu(args):
                                                  "(%.0f MB > 3x L2 %.0f MB)" % (n_copies, per_layer / 1e6,
                                                                                 n_copies * per_layer / 1e6, l2 / 1e6),
                                     "cuda_graphs": use_graphs, "rotation": args.rotation}),
-            "step": "one kernel (oscar_decode_step_ring)" if ring else
-                    "two kernels (oscar_quantize_append + oscar_decode_attention)",
-            "step_kernel_ms": ring_ms, "decode_ms": decode_ms, "demote_ms": demote_ms,
-            "hbm_gbs_decode": nbytes / (decode_ms / 1e3) / 1e9,
+            "decode_ms": decode_ms, "demote_ms": demote_ms,
+            "hbm_gbs_decode": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None if ring else _profiled_traffic(),
-                         "kernel": ("split_kernel, one-kernel step (oscar_decode_step_ring)" if ring else
-                                    "split_kernel (oscar_decode_attention, one launch per step)"),
-                         "algorithmic_bytes": k_bytes, "peak_kind": peak_kind + " hbm_gbs"},
+                         "frac": achieved / peak, "traffic": _profiled_traffic(),
+                         "kernel": "split_kernel (oscar_decode_attention, one launch per step)",
+                         "algorithmic_bytes": nbytes, "peak_kind": peak_kind + " hbm_gbs"},
             "cpu_baseline": cpu,
             "e2e": {"value": world * bsz / e2e_s, "unit": UNIT,
                     "h2d_bytes_per_step": q.numel() * 2 + new_k.numel() * 2 + new_v.numel() * 2,
                     "d2h_bytes_per_step": out.numel() * 4},
-            "gpu_launches": K if ring else 2 * K,
-            "kernel_timing": "step_kernel_ms / decode_ms / demote_ms: %d back-to-back launches each over the "
-                             "%d layer copies, CUDA events on the launching stream" % (reps * n_copies, n_copies),
+            "gpu_launches": 2 * K,
+            "kernel_timing": "decode_ms / demote_ms: %d back-to-back launches over the %d layer copies, "
+                             "CUDA events on the launching stream" % (reps * n_copies, n_copies),
             "clocks": clk,
             "device_status": status,
             "host_wall_s": wall,

@@ -71,8 +71,6 @@ def _load():
         "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
                                              ctypes.POINTER(c_size_t), P]),
         "oscar_decode_attention_static": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P]),
-        "oscar_decode_step_ring": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_size_t, P, P, P, P, P, c_size_t,
-                                             P, P]),
         "oscar_decode_step": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_size_t, P, P, c_int64, c_int64, P, P,
                                         P, c_int32, P, P, P, P, P, c_size_t, P, P]),
     }
@@ -274,16 +272,6 @@ def oscar_decode_step(desc: LayerDesc, host_in, dev_in, in_bytes: int, k_src, v_
         ctypes.byref(desc), _ptr(host_in), _ptr(dev_in), int(in_bytes), _ptr(k_src), _ptr(v_src), int(src_rows),
         int(row_stride), _ptr(src_index), _ptr(dst_req), _ptr(dst_pos), int(n), _ptr(new_k), _ptr(new_v),
         _ptr(q), _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(host_out), _stream(stream)))
-
-
-def oscar_decode_step_ring(desc: LayerDesc, new_k, new_v, q, out, workspace, workspace_bytes: int = None,
-                           host_in=None, dev_in=None, in_bytes: int = 0, host_out=None, stream=None) -> None:
-    """One decode step as one kernel: lengths already advanced; the newest recent slot takes
-    new_k / new_v after its previous token is demoted into history position hist_len - 1."""
-    ws = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
-    _check("oscar_decode_step_ring", lib.oscar_decode_step_ring(
-        ctypes.byref(desc), _ptr(host_in), _ptr(dev_in), int(in_bytes), _ptr(new_k), _ptr(new_v), _ptr(q),
-        _ptr(out), _ptr(workspace), int(ws), _ptr(host_out), _stream(stream)))
 
 
 def oscar_decode_attention_static(desc: LayerDesc, q, out, stream=None) -> None:

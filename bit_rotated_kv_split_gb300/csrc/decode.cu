@@ -61,7 +61,6 @@
 
 #include <cudaTypedefs.h>
 
-#include "demote_math.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -136,16 +135,13 @@ struct Geo {
   static constexpr size_t kQScratch = (6 * G * kHeadDim + 16 * G + 32 * NH * 16) * 4;
   static constexpr size_t kUnion = kRotBytes + kQScratch;   // R_K then R_V | q~ scratch
   static constexpr size_t kBf16State = size_t(kBf16Warps) * G * kPartStride * 4;
-  // last-CTA flag (+0), step demotion flag (+4), the demoted token's 64 code
-  // bytes (+16) and its K and V (scale, zero) pairs (+80)
-  static constexpr size_t kTail = 96;
   // ring stages per warp: the tuned count, fewer when larger blocks (more
   // quantisation groups) would not fit the 227 KB with everything else
   // the ring is kParts parts of kGroup stages: a step consumes one part
   // while the others' copies are in flight
   static constexpr int kStagesTuned = G <= 4 ? OSCAR_STAGES_G4 : OSCAR_STAGES_G8;
   static constexpr int kStagesFit =
-      int((227 * 1024 - (1024 + kUnion + kBf16State + kTail + 1024)) / (size_t(W) * kBlock));
+      int((227 * 1024 - (1024 + kUnion + kBf16State + 16 + 1024)) / (size_t(W) * kBlock));
   static constexpr int kStagesMax = kStagesTuned < kStagesFit ? kStagesTuned : kStagesFit;
   static constexpr int kParts = kStagesMax / kGroup;
   static constexpr int kStages = kParts * kGroup;
@@ -157,7 +153,7 @@ struct Geo {
   static_assert(kBarBytes <= 1024, "barrier region within its budget");
   // (+1 KB: the union starts at the next 1024-byte boundary, which the
   // swizzled R_V boxes need)
-  static constexpr size_t kSmem = kStageBytes + kBarBytes + 1024 + kUnion + kBf16State + kTail;
+  static constexpr size_t kSmem = kStageBytes + kBarBytes + 1024 + kUnion + kBf16State + 16;
   static_assert(kStageBytes % 128 == 0 && kBarBytes % 128 == 0, "TMA destinations must stay aligned");
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   // each warp's ring slice holds its INT2 state once its pages are done
@@ -926,112 +922,6 @@ __device__ __forceinline__ void store_warp_state(WarpState<G>& st, float* ws, in
   }
 }
 
-// ------------------------------------------------------------------ one-kernel decode step
-
-// R_V -> shared memory (replacing R_K) for the CTA's output rotation: box qq
-// = columns 32 qq .. 32 qq + 31 of all 128 rows, 16-byte chunks of row c
-// swizzled to chunk ^ (c & 7).  Issued by one thread once nothing reads R_K.
-__device__ __forceinline__ void request_rv(const DecodeParams& p, float* rvs, uint64_t* vbar, int hkv) {
-  fence_proxy_async_smem();
-  mbar_arrive_expect_tx(vbar, uint32_t(kHeadDim * kHeadDim * 4));
-#pragma unroll
-  for (int qq = 0; qq < 4; ++qq)
-    tma_load_2d(rvs + qq * (kHeadDim * kHeadDim / 4), &p.tm_rv, 32 * qq, hkv * kHeadDim, vbar);
-}
-
-// Warp-wide token moves of the one-kernel step for (request b, KV head hkv):
-// reads the K and V rows that ring slot `slot` held before the step, writes
-// the new token there, and with `demote` rotates, clips and quantises the
-// old token exactly as the per-token demotion kernel does (x . R as four
-// partial sums over 32 inputs each, added pairwise, then the shared
-// quantiser), stores it at slot `dslot` of pool page `pid`, and leaves its
-// code bytes and (scale, zero) pairs in dem_buf for the warp that scans
-// that page, raising dem_flag last.  R is read from shared memory: R_K as
-// the prologue staged it (row-major), then R_V in its four swizzled boxes
-// once vbar completes.  rv_gate counts the readers of R_K that are done (the
-// prologue and this warp): the second one requests R_V.
-__device__ __noinline__ void ring_step_token(const DecodeParams& p, int b, int hkv, int slot, bool demote,
-                                             int64_t pid, int dslot, const float* rs, uint64_t* rbar,
-                                             uint64_t* vbar, uint8_t* dem_buf, int* rv_gate,
-                                             volatile int* dem_flag) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t(b) * p.recent_cap + slot) * p.n_kv + hkv;
-  uint16_t* rk = p.recent_kw + row * kHeadDim;
-  uint16_t* rv = p.recent_vw + row * kHeadDim;
-  float x[2][4];   // lane l: x_(32 w + l)
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    x[0][w] = bf16_lo(uint32_t(rk[32 * w + lane]));
-    x[1][w] = bf16_lo(uint32_t(rv[32 * w + lane]));
-  }
-  __syncwarp();
-  const int64_t nrow = (int64_t(b) * p.n_kv + hkv) * kHeadDim;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    rk[32 * w + lane] = p.new_k[nrow + 32 * w + lane];
-    rv[32 * w + lane] = p.new_v[nrow + 32 * w + lane];
-  }
-  if (!demote) return;
-  const bool pid_ok = pid >= 0 && pid < p.n_pages;
-  uint8_t* blk = pid_ok ? p.pages_w + (pid * p.n_kv + hkv) * block_bytes(1, 1) : nullptr;
-  uint32_t* dem_pair = reinterpret_cast<uint32_t*>(dem_buf + 64);
-  const float4* r4 = reinterpret_cast<const float4*>(rs);
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    if (!mbar_wait_bounded(which ? vbar : rbar, 0, kWaitLimitNs) && lane == 0) flag(p.dev_status, 0x4);
-    float a[4][4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      a[w][0] = a[w][1] = a[w][2] = a[w][3] = 0.f;
-#pragma unroll 8
-      for (int k = 0; k < 32; ++k) {
-        const int i = 32 * w + k;
-        const float xi = __shfl_sync(0xffffffffu, x[which][w], k);
-        // R[i][4 lane .. 4 lane + 3]: R_K row-major; R_V box lane / 8, row i,
-        // 16-byte chunk (lane % 8) ^ (i % 8)
-        const float4 rr = which ? r4[(lane >> 3) * (kHeadDim * kHeadDim / 16) + 8 * i + ((lane & 7) ^ (i & 7))]
-                                : r4[i * (kHeadDim / 4) + lane];
-        a[w][0] = fmaf(xi, rr.x, a[w][0]);
-        a[w][1] = fmaf(xi, rr.y, a[w][1]);
-        a[w][2] = fmaf(xi, rr.z, a[w][2]);
-        a[w][3] = fmaf(xi, rr.w, a[w][3]);
-      }
-    }
-    if (which == 0) {
-      __syncwarp();   // every lane's reads of R_K are done
-      if (lane == 0) {
-        __threadfence_block();
-        if (atomicAdd(rv_gate, 1) + 1 == 2) {
-          __threadfence_block();
-          request_rv(p, const_cast<float*>(rs), vbar, hkv);
-        }
-      }
-    }
-    const float tau = which ? p.tau_v : p.tau_k;
-    float v[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      v[c] = (a[0][c] + a[1][c]) + (a[2][c] + a[3][c]);
-      v[c] = fminf(fmaxf(v[c], -tau), tau);
-    }
-    __half s16[1], z16[1];
-    const uint32_t byte = quantize_lane<1, false>(v, lane, nullptr, s16, z16);
-    const uint32_t pair = uint32_t(__half_as_ushort(s16[0])) | (uint32_t(__half_as_ushort(z16[0])) << 16);
-    dem_buf[32 * which + lane] = uint8_t(byte);
-    if (lane == 0) dem_pair[which] = pair;
-    if (blk) {
-      blk[which ? v_code_byte(dslot, lane) : 32 * dslot + lane] = uint8_t(byte);
-      if (lane == 0) *reinterpret_cast<uint32_t*>(blk + pair_byte(1, 1, dslot, which, 0)) = pair;
-    }
-  }
-  if (!pid_ok && lane == 0) flag(p.dev_status, 0x1);
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    *dem_flag = 1;
-  }
-}
-
 // ------------------------------------------------------------------ q~ and its fragments
 
 // Shared-memory scratch of the prologue, in floats: qs[G][128] | part[4][G][128]
@@ -1152,9 +1042,7 @@ __device__ void rotate_query(const DecodeParams& p, int b, int hkv, const float*
 // ------------------------------------------------------------------ split kernel
 
 // kLevels: codebook levels (one quantisation group per vector only).
-// kRing: the one-kernel decode step (DecodeParams::ring_step; built for the
-// one-group, uniform-level kernels)
-template <int G, int NGK, int NGV, bool kLevels, bool kRing = false>
+template <int G, int NGK, int NGV, bool kLevels>
 __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_constant__ DecodeParams p) {
   using Gm = Geo<G, NGK, NGV, kLevels>;
   static_assert(!kLevels || (NGK == 1 && NGV == 1), "codebook levels with one group per vector");
@@ -1173,9 +1061,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   float* qscratch = reinterpret_cast<float*>(uni + Geo<G>::kRotBytes);
   float* st_bf16x = reinterpret_cast<float*>(uni + Geo<G>::kUnion);   // [kBf16Warps][G][kPartStride]
   int* s_last = reinterpret_cast<int*>(uni + Geo<G>::kUnion + Geo<G>::kBf16State);
-  volatile int* dem_flag = s_last + 1;                                   // the step's demoted token is in dem_buf
-  int* rv_gate = s_last + 2;                                             // readers of R_K done (see request_rv)
-  uint8_t* dem_buf = uni + Geo<G>::kUnion + Geo<G>::kBf16State + 16;     // [2][32] code bytes, then [2] pairs
   uint64_t* pro_done = bars + W * kStages + 2;   // q~ fragments ready (after R_K, R_V)
   constexpr int PT = Geo<G>::PT;
 
@@ -1281,12 +1166,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     }
   }
 
-  if constexpr (kRing) {
-    if (tid == 0) {
-      *dem_flag = 0;
-      *rv_gate = 0;
-    }
-  }
   __syncthreads();   // the R_K / R_V / prologue barriers are initialised
 
   // ---------------- the query rows -> shared memory (used by the prologue;
@@ -1307,22 +1186,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
   if (n_pg > n_splits * p.pages_per_split && split == 0 && tid == 0)
     flag(p.dev_status, 0x2);  // longer than the host bound max_hist: tail not read
   const int pend = min(pbeg + p.pages_per_split, n_pg);
-
-  // ---------------- (kRing) the step's token moves, with the lengths already
-  // advanced: the new token is the newest recent token; when the ring is
-  // full and a history exists, the token its slot held is demoted into
-  // history position hist - 1 by the CTA whose range holds that page (else
-  // the first split writes the new token)
-  int rl = 0;
-  bool demote = false, dem_here = false, write_here = false;
-  int dem_page = -1;
-  if constexpr (kRing) {
-    rl = p.recent_len[b];
-    demote = hist >= 1 && rl == p.recent_cap && p.recent_cap > 0;
-    dem_page = demote ? (hist - 1) / kPage : -1;
-    dem_here = demote && dem_page >= pbeg && dem_page < pend;
-    write_here = rl >= 1 && rl <= p.recent_cap && (demote ? dem_here : split == 0);
-  }
 
   // ---------------- q~ and the lane's QK fragments (prologue warps); the
   // BF16 warps scan the sink/recent tokens meanwhile and read the fragments
@@ -1366,17 +1229,11 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     // box qq = columns 32 qq .. 32 qq + 31 of all 128 rows, 16-byte chunks
     // of row c swizzled to chunk ^ (c & 7)
     if (tid == 0) {
-      // (kRing, the CTA that demotes the step's token: its BF16 warp reads
-      // R_K too, and the later of the two requests R_V)
-      bool issue = true;
-      if constexpr (kRing) {
-        // (weights: 2 when no warp of this CTA demotes, else 1 + 1)
-        __threadfence_block();
-        const int add = dem_here ? 1 : 2;
-        issue = atomicAdd(rv_gate, add) + add == 2;
-        if (issue) __threadfence_block();
-      }
-      if (issue) request_rv(p, rvs, vbar, hkv);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(vbar, uint32_t(Geo<G>::kRotBytes));
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        tma_load_2d(rvs + qq * (kHeadDim * kHeadDim / 4), &p.tm_rv, 32 * qq, hkv * kHeadDim, vbar);
       mbar_arrive(pro_done);
     }
   } else {
@@ -1394,17 +1251,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
     const int start = min(max(rec_start, 0), max(p.recent_cap - 1, 0));
     const int n_vp = p.sink_cap / kPage + p.recent_cap / kPage;
     const int64_t hstride = int64_t(p.n_kv) * kHeadDim;
-    // (kRing) the newest recent token is the step's new token: every CTA
-    // reads it from new_k / new_v, so none waits for the ring write below
-    int new_u = -1;
-    if constexpr (kRing) {
-      if (rec_len >= 1) new_u = p.sink_cap + rec_len - 1;
-      if (bw == kBf16Warps - 1 && write_here) {
-        const int64_t pid = dem_here ? int64_t(ptab[dem_page]) : -1;
-        ring_step_token(p, b, hkv, (start + rec_len - 1) % p.recent_cap, dem_here, pid, (hist - 1) % kPage, rks,
-                        rbar, vbar, dem_buf, rv_gate, dem_flag);
-      }
-    }
     WarpState<G> st;
     st.init();
     const int mine = split + bw * n_splits;
@@ -1424,10 +1270,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         }
       }
       auto row_of = [&](int u, bool kv, bool& ok) -> const uint16_t* {
-        if (kRing && u == new_u) {
-          ok = true;
-          return (kv ? p.new_v : p.new_k) + (int64_t(b) * p.n_kv + hkv) * kHeadDim;
-        }
         if (u < p.sink_cap) {
           ok = u < sink_len;
           const uint16_t* base = kv ? p.sink_v : p.sink_k;
@@ -1535,10 +1377,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         const uint8_t* pg[kGroup];
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) pg[u] = ring + (kGroup * h + u) * kBlock;
-        // (kRing: the part holding the step's demoted token takes the masked
-        // path, which patches that token into the staged page)
-        const bool all_full = nv == kGroup && good[h] == kPartBits && j0 + kGroup <= n_full &&
-                              !(kRing && dem_here && dem_page >= j0 && dem_page < j0 + kGroup);
+        const bool all_full = nv == kGroup && good[h] == kPartBits && j0 + kGroup <= n_full;
         // token validity of the lane's two tokens per page (masked steps only)
         bool ok[kGroup][2];
         if (!all_full) {
@@ -1549,31 +1388,6 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
             const int ntok = u < nv && copied ? hist - kPage * (j0 + u) : 0;
             ok[u][0] = gid < ntok;
             ok[u][1] = gid + 8 < ntok;
-          }
-          if constexpr (kRing) {
-            const int u = dem_page - j0;
-            if (dem_here && u >= 0 && u < nv && ((good[h] >> u) & 1u)) {
-              // the step's demoted token into the staged page, once the
-              // demoting warp has left it in dem_buf (bounded wait)
-              const uint64_t t0 = global_timer_ns();
-              while (*dem_flag == 0) {
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                  if (lane == 0) flag(p.dev_status, 0x4);
-                  break;
-                }
-                __nanosleep(64);
-              }
-              __threadfence_block();
-              uint8_t* pgu = ring + (kGroup * h + u) * kBlock;
-              const int ds = (hist - 1) % kPage;
-              pgu[32 * ds + lane] = dem_buf[lane];
-              pgu[v_code_byte(ds, lane)] = dem_buf[32 + lane];
-              if (lane < 2)
-                *reinterpret_cast<uint32_t*>(pgu + pair_byte(1, 1, ds, lane, 0)) =
-                    reinterpret_cast<const uint32_t*>(dem_buf + 64)[lane];
-              fence_proxy_async_smem();   // before this stage is refilled by a copy
-              __syncwarp();
-            }
           }
         }
         // QK of the step's pages, one maximum update, probabilities and PV;
@@ -1860,17 +1674,12 @@ int occupancy() {
   return occ;
 }
 
-template <int G, int NGK, int NGV, bool kLevels = false, bool kRing = false>
+template <int G, int NGK, int NGV, bool kLevels = false>
 cudaError_t launch_g(const DecodeParams& p, cudaStream_t stream) {
-  if constexpr (NGK == 1 && NGV == 1 && !kLevels && !kRing) {
-    if (p.ring_step) return launch_g<G, 1, 1, false, true>(p, stream);
-  } else if constexpr (!kRing) {
-    if (p.ring_step) return cudaErrorInvalidValue;   // one group, uniform levels only
-  }
   constexpr size_t smem = Geo<G, NGK, NGV, kLevels>::kSmem;
-  cudaError_t e = set_smem_limit<split_kernel<G, NGK, NGV, kLevels, kRing>>(int(smem));
+  cudaError_t e = set_smem_limit<split_kernel<G, NGK, NGV, kLevels>>(int(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(split_kernel<G, NGK, NGV, kLevels, kRing>, dim3(p.n_kv, p.batch, p.n_splits), dim3(Geo<G>::T),
+  return launch_pdl(split_kernel<G, NGK, NGV, kLevels>, dim3(p.n_kv, p.batch, p.n_splits), dim3(Geo<G>::T),
                     smem, stream, p);
 }
 

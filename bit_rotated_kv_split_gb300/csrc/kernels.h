@@ -174,19 +174,6 @@ struct DecodeParams {
   // their maximum lowered by pv_log2; pv_unscale = 2^24 undoes the codes'
   // subnormal scale
   float pv_log2, pv_unscale;
-  // one-kernel decode step (ring_step = 1, one quantisation group, uniform
-  // levels): with the lengths already advanced, the new token new_k / new_v
-  // [B][H_kv][d] goes to the newest recent slot, whose previous token is
-  // demoted into history position hist_len - 1 first when the ring is full
-  // and a history exists; the writable views of the pool and the ring, and
-  // the clip thresholds, serve that
-  int32_t ring_step;
-  const uint16_t* new_k;
-  const uint16_t* new_v;
-  uint8_t* pages_w;
-  uint16_t* recent_kw;
-  uint16_t* recent_vw;
-  float tau_k, tau_v;
   // R_V as a 2-D tensor (128 columns x n_kv * 128 rows of fp32) read in
   // boxes of 32 columns x 128 rows with the 128-byte swizzle
   CUtensorMap tm_rv;

@@ -328,47 +328,6 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
   return OSCAR_OK;
 }
 
-// [ZAKER] pipeline part (demote the oldest recent token, write the new one,
-// attend) as one kernel, for the ring steady state.
-extern "C" oscar_status oscar_decode_step_ring(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
-                                               size_t in_bytes, const uint16_t* new_k, const uint16_t* new_v,
-                                               const uint16_t* q, float* out, void* workspace,
-                                               size_t workspace_bytes, float* host_out, void* stream) {
-  OSCAR_TRACE_CALL();
-  if ((in_bytes > 0) != (host_in != nullptr && dev_in != nullptr)) return OSCAR_ERR_INVALID_ARG;
-  if (!workspace) return OSCAR_ERR_WORKSPACE;
-  if ((in_bytes > 0 && !device_addressable_host(host_in)) || (host_out && !device_addressable_host(host_out)))
-    return OSCAR_ERR_INVALID_ARG;
-  if (!new_k || !new_v) return OSCAR_ERR_INVALID_ARG;
-  if (!aligned(new_k, 16) || !aligned(new_v, 16)) return OSCAR_ERR_ALIGNMENT;
-  oscar_status st = check_desc(desc, true);
-  if (st != OSCAR_OK) return st;
-  if (desc->recent_cap < 1 || groups_of(desc->quant_group_k) != 1 || groups_of(desc->quant_group_v) != 1 ||
-      desc->codebook)
-    return OSCAR_ERR_UNSUPPORTED;
-  oscar::DecodeParams pd{};
-  bool size_only = false;
-  size_t ws_bytes = workspace_bytes;
-  st = prepare_decode(desc, q, out, workspace, &ws_bytes, &pd, &size_only);
-  if (st != OSCAR_OK) return st;
-  pd.ring_step = 1;
-  pd.new_k = new_k;
-  pd.new_v = new_v;
-  pd.pages_w = desc->pages;
-  pd.recent_kw = desc->recent_k;
-  pd.recent_vw = desc->recent_v;
-  pd.tau_k = desc->tau_k;
-  pd.tau_v = desc->tau_v;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_bytes > 0 && oscar::launch_stage(host_in, dev_in, in_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
-  if (oscar::launch_decode(pd, s) != cudaSuccess) return OSCAR_ERR_CUDA;
-  if (host_out) {
-    const size_t out_bytes = size_t(desc->batch) * desc->n_q_heads * OSCAR_HEAD_DIM * sizeof(float);
-    if (oscar::launch_stage(out, host_out, out_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
-  }
-  return OSCAR_OK;
-}
-
 // [GIST] 2.1 / 2.2 A: C_Q and C_S as one contraction over calibration rows.
 extern "C" oscar_status oscar_covariance(const uint16_t* x, int64_t n, int32_t d, int64_t ld, float* c_out,
                                          void* workspace, size_t* workspace_bytes, void* stream) {

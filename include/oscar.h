@@ -420,43 +420,6 @@ oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in
                                void* stream);
 
 /*
- * oscar_decode_step_ring - one decode step of a layer in the steady state
- * of the token pool, as ONE kernel: [ZAKER] pipeline part (the oldest
- * recent-window token is demoted into INT2 history, the new token takes its
- * ring slot, attention over sink | history | recent), with the demotion
- * inside the attention kernel instead of a launch of its own.
- *
- *   The caller advances the lengths first (desc->hist_len, recent_len,
- *   recent_start describe the pool AFTER the step, as for the decode calls).
- *   For every request b with recent_len[b] >= 1, the new token (new_k /
- *   new_v [B][H_kv][d] bf16, 16-byte aligned) is the newest recent token:
- *   ring slot t = (recent_start[b] + recent_len[b] - 1) % recent_cap.  When
- *   recent_len[b] == recent_cap and hist_len[b] >= 1, the token that slot t
- *   held before the call is first demoted into history position
- *   hist_len[b] - 1 (rotate, clip, quantise, pack; the page must be private
- *   to b).  Slot t then holds the new token, and the output is attention over
- *   the advanced pool.  Requests with recent_len[b] == 0 get no write (their
- *   new token belongs to the sink, which the caller fills).
- *
- *   Equal bit for bit - pool bytes, ring rows and output - to
- *   oscar_quantize_append(src_index[b] = b * recent_cap + t, dst_req[b] = b,
- *   dst_pos[b] = hist_len[b] - 1, new rows new_k / new_v, for the requests
- *   that demote) followed by oscar_decode_attention on the same desc.
- *   One quantisation group per vector and uniform levels only
- *   (OSCAR_ERR_UNSUPPORTED otherwise); recent_cap >= 1.
- *
- *   host_in / dev_in / in_bytes and host_out work as in oscar_decode_step
- *   (optional staging of the step's inputs from pinned host memory and of
- *   the output back to it, as copy kernels in the same launch chain).
- *   Validation as oscar_decode_attention plus new_k / new_v (non-null,
- *   16-byte aligned); a rejected call copies and launches nothing.  Async.
- */
-oscar_status oscar_decode_step_ring(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
-                                    size_t in_bytes, const uint16_t* new_k, const uint16_t* new_v,
-                                    const uint16_t* q, float* out, void* workspace,
-                                    size_t workspace_bytes, float* host_out, void* stream);
-
-/*
  * oscar_decode_attention_static - oscar_decode_attention for callers that
  * cannot allocate device memory.  The paper has no counterpart: this is a
  * deployment convenience of this library.

@@ -66,20 +66,6 @@ def test_decode_rejects_bad_descriptors_before_launch(built_lib, over, status):
     assert got == status
 
 
-def test_ring_step_rejects_bad_arguments_before_launch(built_lib):
-    from bit_rotated_kv_split_gb300 import binding as B
-    f = B.lib.oscar_decode_step_ring
-    a = 1 << 20   # 16-byte aligned fake addresses: never dereferenced on rejection
-    ok = ctypes.byref(_desc())
-    assert f(ok, None, None, 0, a, a, a, a, None, 1 << 20, None, None) == 3      # no workspace
-    assert f(ok, None, None, 64, a, a, a, a, a, 1 << 20, None, None) == 1        # bytes without buffers
-    assert f(ok, None, None, 0, None, a, a, a, a, 1 << 20, None, None) == 1      # no new_k
-    assert f(ok, None, None, 0, a, a + 8, a, a, a, 1 << 20, None, None) == 2     # misaligned new_v
-    assert f(ctypes.byref(_desc(head_dim=64)), None, None, 0, a, a, a, a, a, 1 << 20, None, None) == 1
-    for over in (dict(quant_group_k=32), dict(quant_group_v=64), dict(recent_cap=0)):
-        assert f(ctypes.byref(_desc(**over)), None, None, 0, a, a, a, a, a, 1 << 20, None, None) == 6, over
-
-
 def test_decode_unsupported_group(built_lib):
     from bit_rotated_kv_split_gb300 import binding as B
     size = ctypes.c_size_t(0)
