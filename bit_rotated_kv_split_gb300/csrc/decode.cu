@@ -1654,8 +1654,10 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
       a.w = fmaf(f, v.w, a.w);
     }
     const float s = lsum > 0.f ? 1.f / lsum : 0.f;
-    reinterpret_cast<float4*>(p.out + ((int64_t(b) * p.n_kv + hkv) * G + h) * kHeadDim)[lane] =
-        make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+    const float4 res = make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+    const int64_t oi = ((int64_t(b) * p.n_kv + hkv) * G + h) * kHeadDim;
+    reinterpret_cast<float4*>(p.out + oi)[lane] = res;
+    if (p.out_host) reinterpret_cast<float4*>(p.out_host + oi)[lane] = res;   // over the CPU-GPU link
     if (h == 0 && lane == 0) p.counters[pair] = 0u;   // ready for the next call
   }
 }

@@ -79,6 +79,13 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
                                                    int64_t(blockIdx.y >> 1) * kHeadDim * kHeadDim);
     for (int i = threadIdx.x; i < int(kRotBytes / 128); i += kWarps * 32)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(rg + 128 * i));
+    // and the lines of this CTA's item indices (the first level of its
+    // dependent loads)
+    const int it0 = int(blockIdx.x) * kItems;
+    if (threadIdx.x < 3 && it0 < p.n) {
+      const int32_t* idx = threadIdx.x == 0 ? p.dst_req : threadIdx.x == 1 ? p.dst_pos : p.src_index;
+      if (idx) asm volatile("prefetch.global.L2 [%0];" ::"l"(idx + it0));
+    }
   }
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();

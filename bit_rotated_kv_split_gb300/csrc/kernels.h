@@ -149,6 +149,9 @@ struct DecodeParams {
   // io
   const uint16_t* q;
   float* out;
+  // optional second copy of the output in pinned host memory (16-byte
+  // aligned), written by the same stores that write `out`
+  float* out_host;
   // workspace views
   uint32_t* counters;   // [pairs] merge tickets (zero between calls)
   float* partials;      // [pairs][n_splits][G][kPartStride]

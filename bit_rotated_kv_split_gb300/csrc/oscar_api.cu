@@ -320,8 +320,12 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (in_bytes > 0 && oscar::launch_stage(host_in, dev_in, in_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
   if (!empty && launch_append(pa, s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  // a 16-byte aligned host_out is written by the decode kernel itself, with
+  // the same stores as `out`; otherwise a copy kernel follows it
+  const bool direct_out = host_out && aligned(host_out, 16);
+  if (direct_out) pd.out_host = host_out;
   if (oscar::launch_decode(pd, s) != cudaSuccess) return OSCAR_ERR_CUDA;
-  if (host_out) {
+  if (host_out && !direct_out) {
     const size_t out_bytes = size_t(desc->batch) * desc->n_q_heads * OSCAR_HEAD_DIM * sizeof(float);
     if (oscar::launch_stage(out, host_out, out_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
   }

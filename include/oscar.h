@@ -398,8 +398,10 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
  *   oscar_quantize_append with the given arguments (nothing when n = 0);
  *   (3) oscar_decode_attention(desc, q, out, workspace, workspace_bytes);
  *   (4) if host_out is not NULL, copy out ([B][H_q][d] float32) to host_out
- *   (pinned host memory).  The results are those of the separate calls.
- *   The two copies are kernels of the same launch chain: the GPU reads
+ *   (pinned host memory): when host_out is 16-byte aligned the decode kernel
+ *   of step (3) writes it with the same stores as `out`, else a copy kernel
+ *   follows.  The results are those of the separate calls.
+ *   The copies run in the same launch chain as kernels: the GPU reads
  *   host_in and writes host_out directly (GB300's coherent CPU-GPU link), so
  *   both must be pinned host memory the device addresses at the same pointer
  *   (cudaHostAlloc / cudaMallocHost on a system with unified addressing);

@@ -245,6 +245,30 @@ def test_decode_step_equals_separate_calls():
         np.testing.assert_array_equal(a, b)
 
 
+def test_decode_step_output_to_unaligned_host_buffer():
+    """host_out off the 16-byte grid: the output goes through the copy
+    kernel instead of the decode kernel's own stores; same bytes, and the
+    bytes around it untouched."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    sc = H.Scenario(2012, [1300, 700], n_kv=1, g=4)
+    cache, q = H.to_device(sc)
+    ref, _ = H.run_decode(cache, q)
+    desc = cache.desc()
+    nbytes = B.oscar_decode_workspace_bytes(desc)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    big = torch.zeros(q.numel() * 4 + 64, dtype=torch.uint8).pin_memory()
+    for off in (4, 16):
+        big.zero_()
+        B.oscar_decode_step(desc, None, None, 0, None, None, 1, 128, None, None, None, 0, None, None, q, out, ws,
+                            nbytes, big.data_ptr() + off)
+        torch.cuda.synchronize()
+        got = big.numpy()[off:off + q.numel() * 4].view(np.float32).reshape(q.shape)
+        np.testing.assert_array_equal(got, ref.astype(np.float32))
+        assert not big.numpy()[:off].any() and not big.numpy()[off + q.numel() * 4:].any()
+
+
 def test_decode_step_stages_odd_sizes_and_offsets():
     """The staging copy of oscar_decode_step moves an odd number of bytes
     between addresses off the 16-byte grid exactly (byte path) and leaves the
