@@ -1120,7 +1120,10 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
 #pragma unroll
     for (int i0 = 0; i0 < (G * kHeadDim + PT - 1) / PT; ++i0) {
       const int i = tid + i0 * PT;
-      qv[i0] = (pbeg < p.max_pages && !bf16_warp && i < G * kHeadDim) ? qg[i] : uint16_t(0);
+      // (q may sit in pinned host memory: cache-volatile loads)
+      qv[i0] = (pbeg < p.max_pages && !bf16_warp && i < G * kHeadDim)
+                   ? uint16_t(__ldcv(reinterpret_cast<const unsigned short*>(qg + i)))
+                   : uint16_t(0);
     }
   }
 
@@ -1262,7 +1265,7 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
         const uint16_t* qrow = p.q + (int64_t(b) * p.n_kv * G + hkv * G + h) * kHeadDim + 32 * tig;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + 8 * u));
+          const uint4 v = __ldcv(reinterpret_cast<const uint4*>(qrow + 8 * u));
           qf[nt][2 * u][0] = v.x;
           qf[nt][2 * u][1] = v.y;
           qf[nt][2 * u + 1][0] = v.z;

@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     slot[it] = 0;
     xv[it] = 0.f;
     if (!live[it]) continue;
-    const int64_t row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
-    const int bq = p.dst_req[item], pos = p.dst_pos[item];
+    // (the step's inputs may sit in pinned host memory, read over the
+    // CPU-GPU link: cache-volatile loads fetch them anew on every call)
+    const int64_t row = p.src_index ? int64_t(__ldcv(p.src_index + item)) : int64_t(item);
+    const int bq = __ldcv(p.dst_req + item), pos = __ldcv(p.dst_pos + item);
     if (row < 0 || row >= p.src_rows || bq < 0 || bq >= p.batch || pos < 0 || pos / kPage >= p.max_pages) {
       if (warp == 0 && lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x2);
       live[it] = false;
@@ -144,9 +146,11 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     for (int it = 0; it < kItems; ++it) {
       if (!live[it]) continue;
       const int item = item0 + it;
-      const int64_t row = p.src_index ? int64_t(p.src_index[item]) : int64_t(item);
+      const int64_t row = p.src_index ? int64_t(__ldcv(p.src_index + item)) : int64_t(item);
       uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
-      src[32 * warp + lane] = fresh[(int64_t(item) * p.n_kv + head) * kHeadDim + 32 * warp + lane];
+      src[32 * warp + lane] =
+          __ldcv(reinterpret_cast<const unsigned short*>(fresh) + (int64_t(item) * p.n_kv + head) * kHeadDim +
+                 32 * warp + lane);
     }
   }
 

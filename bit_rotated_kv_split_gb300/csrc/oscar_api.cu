@@ -315,10 +315,36 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
   size_t ws_bytes = workspace_bytes;
   st = prepare_decode(desc, q, out, workspace, &ws_bytes, &pd, &size_only);
   if (st != OSCAR_OK) return st;
-  // the copies run as kernels in the launch chain, reading and writing the
-  // pinned host buffers directly
+  // The step's inputs that lie in the staging range [dev_in, dev_in +
+  // in_bytes) are read by the kernels straight from the same offsets of
+  // host_in (cache-volatile loads over the CPU-GPU link), when the two
+  // buffers share their alignment modulo 16 bytes, the per-token demotion
+  // kernel runs, and the demotion's source rows lie outside the range;
+  // otherwise a copy kernel fills dev_in first.  Both run in the launch chain.
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_bytes > 0 && oscar::launch_stage(host_in, dev_in, in_bytes, s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(dev_in), hi = lo + in_bytes;
+  auto inside = [&](const void* ptr) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+    return ptr != nullptr && a >= lo && a < hi;
+  };
+  auto to_host = [&](const void* ptr) -> const void* {
+    return inside(ptr) ? static_cast<const uint8_t*>(host_in) + (reinterpret_cast<uintptr_t>(ptr) - lo) : ptr;
+  };
+  const bool bulk = !empty && pa.n >= oscar::kBulkDemoteMin && !pa.new_k && !pa.new_v;
+  const bool any_in = inside(q) || (!empty && (inside(pa.src_index) || inside(pa.dst_req) || inside(pa.dst_pos) ||
+                                               inside(pa.new_k) || inside(pa.new_v)));
+  const bool direct_in = in_bytes > 0 && any_in && ((lo ^ reinterpret_cast<uintptr_t>(host_in)) & 15) == 0 &&
+                         !bulk && !inside(pa.k_src) && !inside(pa.v_src);
+  if (direct_in) {
+    pd.q = static_cast<const uint16_t*>(to_host(pd.q));
+    pa.src_index = static_cast<const int32_t*>(to_host(pa.src_index));
+    pa.dst_req = static_cast<const int32_t*>(to_host(pa.dst_req));
+    pa.dst_pos = static_cast<const int32_t*>(to_host(pa.dst_pos));
+    pa.new_k = static_cast<const uint16_t*>(to_host(pa.new_k));
+    pa.new_v = static_cast<const uint16_t*>(to_host(pa.new_v));
+  } else if (in_bytes > 0 && oscar::launch_stage(host_in, dev_in, in_bytes, s) != cudaSuccess) {
+    return OSCAR_ERR_CUDA;
+  }
   if (!empty && launch_append(pa, s) != cudaSuccess) return OSCAR_ERR_CUDA;
   // a 16-byte aligned host_out is written by the decode kernel itself, with
   // the same stores as `out`; otherwise a copy kernel follows it

@@ -392,15 +392,21 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
  * loop that holds the step's inputs in host memory: [ZAKER] pipeline part
  * (demote the oldest recent token, write the new one, attend).
  *
- *   On `stream`, in this order: (1) if in_bytes > 0, copy in_bytes from
- *   host_in (pinned host memory) to dev_in (device), the staging buffer
- *   that q, new_k / new_v and the index arrays may point into; (2)
+ *   On `stream`, in this order: (1) if in_bytes > 0, bring in_bytes from
+ *   host_in (pinned host memory) to dev_in (device), the staging range that
+ *   q, new_k / new_v and the index arrays may point into; (2)
  *   oscar_quantize_append with the given arguments (nothing when n = 0);
  *   (3) oscar_decode_attention(desc, q, out, workspace, workspace_bytes);
  *   (4) if host_out is not NULL, copy out ([B][H_q][d] float32) to host_out
  *   (pinned host memory): when host_out is 16-byte aligned the decode kernel
  *   of step (3) writes it with the same stores as `out`, else a copy kernel
  *   follows.  The results are those of the separate calls.
+ *   Step (1) is not a copy when it need not be: if q or an argument of (2)
+ *   lies inside [dev_in, dev_in + in_bytes), host_in and dev_in are equal
+ *   modulo 16 bytes, the per-token demotion kernel runs (new rows given, or
+ *   n < 1024) and k_src / v_src lie outside that range, the kernels of (2)
+ *   and (3) read those inputs straight from the same offsets of host_in
+ *   and dev_in is left unwritten; otherwise a copy kernel fills dev_in.
  *   The copies run in the same launch chain as kernels: the GPU reads
  *   host_in and writes host_out directly (GB300's coherent CPU-GPU link), so
  *   both must be pinned host memory the device addresses at the same pointer
@@ -410,7 +416,7 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
  *   rejected call copies and launches nothing.  in_bytes > 0 requires
  *   host_in and dev_in (OSCAR_ERR_INVALID_ARG otherwise); workspace must be
  *   given (OSCAR_ERR_WORKSPACE).  Async: host_in must not change until the
- *   stream has passed step (1), and host_out holds the output once the
+ *   stream has passed step (3), and host_out holds the output once the
  *   stream has passed step (4).
  */
 oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
