@@ -21,6 +21,7 @@ OSCAR_OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "WORKSPACE", 4: "CUDA",
                 5: "NO_CONVERGENCE", 6: "UNSUPPORTED", 7: "FILE"}
 DEV_PAGE_BOUNDS, DEV_LENGTH, DEV_TIMEOUT = 0x1, 0x2, 0x4
+OSCAR_STEP_OVERLAP_PREVIOUS = 0x1     # oscar_decode_step flag
 
 
 class OscarError(RuntimeError):
@@ -68,11 +69,13 @@ def _load():
         "oscar_rotation_file_read": (c_int32, [ctypes.c_char_p, c_int32, c_int32, c_int32, P, P, P, P]),
         "oscar_quantize_append": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
                                             P, P, c_int32, P, P, P]),
+        "oscar_quantize_append_overlapped": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_int64, c_int64, P,
+                                                       P, P, c_int32, P, P, P]),
         "oscar_decode_attention": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P,
                                              ctypes.POINTER(c_size_t), P]),
         "oscar_decode_attention_static": (c_int32, [ctypes.POINTER(LayerDesc), P, P, P]),
         "oscar_decode_step": (c_int32, [ctypes.POINTER(LayerDesc), P, P, c_size_t, P, P, c_int64, c_int64, P, P,
-                                        P, c_int32, P, P, P, P, P, c_size_t, P, P]),
+                                        P, c_int32, P, P, P, P, P, c_size_t, P, ctypes.c_uint32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -249,6 +252,13 @@ def oscar_quantize_append(desc: LayerDesc, k_src, v_src, src_rows: int, row_stri
         _ptr(dst_req), _ptr(dst_pos), int(n), _ptr(new_k), _ptr(new_v), _stream(stream)))
 
 
+def oscar_quantize_append_overlapped(desc: LayerDesc, k_src, v_src, src_rows: int, row_stride: int, src_index,
+                                     dst_req, dst_pos, n: int, new_k=None, new_v=None, stream=None) -> None:
+    _check("oscar_quantize_append_overlapped", lib.oscar_quantize_append_overlapped(
+        ctypes.byref(desc), _ptr(k_src), _ptr(v_src), int(src_rows), int(row_stride), _ptr(src_index),
+        _ptr(dst_req), _ptr(dst_pos), int(n), _ptr(new_k), _ptr(new_v), _stream(stream)))
+
+
 def oscar_decode_workspace_bytes(desc: LayerDesc) -> int:
     size = c_size_t(0)
     _check("oscar_decode_attention", lib.oscar_decode_attention(
@@ -266,12 +276,13 @@ def oscar_decode_attention(desc: LayerDesc, q, out, workspace, workspace_bytes: 
 
 def oscar_decode_step(desc: LayerDesc, host_in, dev_in, in_bytes: int, k_src, v_src, src_rows: int,
                       row_stride: int, src_index, dst_req, dst_pos, n: int, new_k, new_v, q, out, workspace,
-                      workspace_bytes: int, host_out=None, stream=None) -> None:
-    """One decode step: H2D copy of the staged inputs, demotion, decode, D2H copy of the output."""
+                      workspace_bytes: int, host_out=None, stream=None, flags: int = 0) -> None:
+    """One decode step: H2D copy of the staged inputs, demotion, decode, D2H copy of the output.
+    flags: 0 or OSCAR_STEP_OVERLAP_PREVIOUS (the demotion overlaps the kernel before it)."""
     _check("oscar_decode_step", lib.oscar_decode_step(
         ctypes.byref(desc), _ptr(host_in), _ptr(dev_in), int(in_bytes), _ptr(k_src), _ptr(v_src), int(src_rows),
         int(row_stride), _ptr(src_index), _ptr(dst_req), _ptr(dst_pos), int(n), _ptr(new_k), _ptr(new_v),
-        _ptr(q), _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(host_out), _stream(stream)))
+        _ptr(q), _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(host_out), int(flags), _stream(stream)))
 
 
 def oscar_decode_attention_static(desc: LayerDesc, q, out, stream=None) -> None:

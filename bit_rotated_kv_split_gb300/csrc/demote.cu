@@ -41,9 +41,11 @@ constexpr size_t kSmem = kRotBytes + kRedBytes + 4 * 8;
 // gives its fp16 (scale, zero).  kLevels: the code is the number of the
 // codebook thresholds `thr` strictly below u = (x - zero) / scale instead of
 // rint(u) clamped to [0, 3].
+// (finish_codes forms lane l's code byte and, for lane q < NG, group q's
+// (scale, zero) pair; store_codes writes them to the page.)
 template <int NG, bool kLevels>
-__device__ __forceinline__ void finish_item(const DemoteParams& p, const float* red, int which, int head,
-                                            int64_t page, int slot, float tau, int lane, const float* thr) {
+__device__ __forceinline__ uint32_t finish_codes(const float* red, int which, float tau, int lane, const float* thr,
+                                                 uint32_t& pair) {
   float v[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -53,24 +55,33 @@ __device__ __forceinline__ void finish_item(const DemoteParams& p, const float* 
   }
   __half s16[NG], z16[NG];
   const uint32_t byte = quantize_lane<NG, kLevels>(v, lane, thr, s16, z16);
+  __half2 sz = __halves2half2(s16[0], z16[0]);
+#pragma unroll
+  for (int q = 1; q < NG; ++q)
+    if (lane == q) sz = __halves2half2(s16[q], z16[q]);
+  pair = *reinterpret_cast<uint32_t*>(&sz);
+  return byte;
+}
+
+__device__ __forceinline__ void store_codes(const DemoteParams& p, int ng, int which, int head, int64_t page,
+                                            int slot, int lane, uint32_t byte, uint32_t pair) {
   if (page < 0 || page >= p.n_pages) {
     if (lane == 0 && p.dev_status) atomicOr(p.dev_status, 0x1);
     return;
   }
   uint8_t* blk = p.pages + (page * p.n_kv + head) * block_bytes(p.ng_k, p.ng_v);
   blk[which ? v_code_byte(slot, lane) : 32 * slot + lane] = uint8_t(byte);
-  if (lane < NG) {
-    __half2 sz = __halves2half2(s16[0], z16[0]);
-#pragma unroll
-    for (int q = 1; q < NG; ++q)
-      if (lane == q) sz = __halves2half2(s16[q], z16[q]);
-    *reinterpret_cast<__half2*>(blk + pair_byte(p.ng_k, p.ng_v, slot, which, lane)) = sz;
-  }
+  if (lane < ng) *reinterpret_cast<uint32_t*>(blk + pair_byte(p.ng_k, p.ng_v, slot, which, lane)) = pair;
 }
 
 // NGK / NGV: quantisation groups per token-head of K and V (template
 // arguments, so a kernel holds only the finishing code it uses).
-template <int NGK, int NGV, bool kLevels>
+// kEarly (DemoteParams::early): the caller guarantees that the kernel just
+// before on the stream writes none of the rotation, the index arrays, the
+// page table and the source rows, so everything up to the codes runs before
+// the wait for that kernel; only the stores (the codes, and the new tokens
+// into the source rows) follow it.
+template <int NGK, int NGV, bool kLevels, bool kEarly = false>
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   {
     // L2 prefetch of this CTA's rotation (a hint that reads nothing, so it
@@ -87,8 +98,10 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
       if (idx) asm volatile("prefetch.global.L2 [%0];" ::"l"(idx + it0));
     }
   }
-  pdl_wait();                 // the previous kernel's writes are visible
-  pdl_launch_dependents();
+  if constexpr (!kEarly) {
+    pdl_wait();                 // the previous kernel's writes are visible
+    pdl_launch_dependents();
+  }
   extern __shared__ __align__(128) uint8_t smem[];
   float* rs = reinterpret_cast<float*>(smem);
   float* red = reinterpret_cast<float*>(smem + kRotBytes);       // [kWarps][128]
@@ -141,7 +154,8 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   // warp has read its part of them
   __syncthreads();
   const uint16_t* fresh = which ? p.new_v : p.new_k;
-  if (fresh) {
+  auto write_new_tokens = [&]() {
+    if (!fresh) return;
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
       if (!live[it]) continue;
@@ -152,7 +166,8 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
           __ldcv(reinterpret_cast<const unsigned short*>(fresh) + (int64_t(item) * p.n_kv + head) * kHeadDim +
                  32 * warp + lane);
     }
-  }
+  };
+  if constexpr (!kEarly) write_new_tokens();
 
   // warp w needs the rows 32 w .. 32 w + 31 of R: quarter w of the copy;
   // on an expired wait the whole CTA leaves (after waiting, bounded, for
@@ -160,10 +175,13 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   if (!__syncthreads_and(mbar_wait_bounded(bar + warp, 0, kWaitLimitNs))) {
     if (threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, 0x4);
     for (int c = 0; c < 4; ++c) mbar_wait_bounded(bar + c, 0, kWaitLimitNs);
+    if constexpr (kEarly) pdl_wait();   // the next kernel still follows the previous one
     return;
   }
   const float tau = which ? p.tau_v : p.tau_k;
   const float4* r4 = reinterpret_cast<const float4*>(rs) + lane;
+  const int ng = which ? NGV : NGK;
+  uint32_t code_byte[kItems], code_pair[kItems];   // warp 0 (kEarly: stored after the wait)
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     if (!__syncthreads_or(live[it])) continue;   // uniform over the CTA
@@ -180,17 +198,29 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     }
     *reinterpret_cast<float4*>(red + warp * kHeadDim + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
     __syncthreads();
+    code_byte[it] = code_pair[it] = 0u;
     if (warp == 0 && live[it]) {
       const float* thr = which ? p.thr_v : p.thr_k;
       if constexpr (NGK == NGV) {
-        finish_item<NGK, kLevels>(p, red, which, head, page[it], slot[it], tau, lane, thr);
+        code_byte[it] = finish_codes<NGK, kLevels>(red, which, tau, lane, thr, code_pair[it]);
       } else if (which) {
-        finish_item<NGV, kLevels>(p, red, which, head, page[it], slot[it], tau, lane, thr);
+        code_byte[it] = finish_codes<NGV, kLevels>(red, which, tau, lane, thr, code_pair[it]);
       } else {
-        finish_item<NGK, kLevels>(p, red, which, head, page[it], slot[it], tau, lane, thr);
+        code_byte[it] = finish_codes<NGK, kLevels>(red, which, tau, lane, thr, code_pair[it]);
       }
+      if constexpr (!kEarly) store_codes(p, ng, which, head, page[it], slot[it], lane, code_byte[it], code_pair[it]);
     }
     __syncthreads();   // red is reused by the next item
+  }
+  if constexpr (kEarly) {
+    pdl_wait();                 // the previous kernel is done: the stores may start
+    pdl_launch_dependents();
+    write_new_tokens();
+    if (warp == 0) {
+#pragma unroll
+      for (int it = 0; it < kItems; ++it)
+        if (live[it]) store_codes(p, ng, which, head, page[it], slot[it], lane, code_byte[it], code_pair[it]);
+    }
   }
 }
 
@@ -198,11 +228,14 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
 
 namespace {
 
-template <int NGK, int NGV, bool kLevels = false>
+template <int NGK, int NGV, bool kLevels = false, bool kEarly = false>
 cudaError_t launch_ng(const DemoteParams& p, int64_t chunks, cudaStream_t stream) {
-  cudaError_t e = set_smem_limit<demote_kernel<NGK, NGV, kLevels>>(int(kSmem));
+  if constexpr (!kEarly) {
+    if (p.early) return launch_ng<NGK, NGV, kLevels, true>(p, chunks, stream);
+  }
+  cudaError_t e = set_smem_limit<demote_kernel<NGK, NGV, kLevels, kEarly>>(int(kSmem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(demote_kernel<NGK, NGV, kLevels>, dim3(unsigned(chunks), unsigned(p.n_kv * 2)),
+  return launch_pdl(demote_kernel<NGK, NGV, kLevels, kEarly>, dim3(unsigned(chunks), unsigned(p.n_kv * 2)),
                     dim3(kWarps * 32), kSmem, stream, p);
 }
 

@@ -121,6 +121,10 @@ struct DemoteParams {
   // columns x 128 rows; use_tma = 0 means the rows are gathered by threads
   CUtensorMap tm_src[2];
   int32_t use_tma;
+  // per-token path: 1 = everything before the stores runs ahead of the wait
+  // for the previous kernel on the stream (that kernel writes nothing the
+  // demotion reads)
+  int32_t early;
 };
 
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream);

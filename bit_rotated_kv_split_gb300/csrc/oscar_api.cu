@@ -283,6 +283,21 @@ extern "C" oscar_status oscar_quantize_append(const oscar_layer_desc* desc, uint
   return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+extern "C" oscar_status oscar_quantize_append_overlapped(const oscar_layer_desc* desc, uint16_t* k_src,
+                                                         uint16_t* v_src, int64_t src_rows, int64_t row_stride,
+                                                         const int32_t* src_index, const int32_t* dst_req,
+                                                         const int32_t* dst_pos, int32_t n, const uint16_t* new_k,
+                                                         const uint16_t* new_v, void* stream) {
+  OSCAR_TRACE_CALL();
+  oscar::DemoteParams p{};
+  bool empty = false;
+  const oscar_status st = prepare_append(desc, k_src, v_src, src_rows, row_stride, src_index, dst_req, dst_pos, n,
+                                         new_k, new_v, &p, &empty);
+  if (st != OSCAR_OK || empty) return st;
+  p.early = 1;   // the tensor-core path ignores it and waits first
+  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
 extern "C" oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t* q,
                                                float* out, void* workspace,
                                                size_t* workspace_bytes, void* stream) {
@@ -299,8 +314,10 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
                                           int64_t row_stride, const int32_t* src_index, const int32_t* dst_req,
                                           const int32_t* dst_pos, int32_t n, const uint16_t* new_k,
                                           const uint16_t* new_v, const uint16_t* q, float* out, void* workspace,
-                                          size_t workspace_bytes, float* host_out, void* stream) {
+                                          size_t workspace_bytes, float* host_out, uint32_t flags,
+                                          void* stream) {
   OSCAR_TRACE_CALL();
+  if ((flags & ~OSCAR_STEP_OVERLAP_PREVIOUS) != 0) return OSCAR_ERR_INVALID_ARG;
   if ((in_bytes > 0) != (host_in != nullptr && dev_in != nullptr)) return OSCAR_ERR_INVALID_ARG;
   if (!workspace) return OSCAR_ERR_WORKSPACE;
   if ((in_bytes > 0 && !device_addressable_host(host_in)) || (host_out && !device_addressable_host(host_out)))
@@ -345,6 +362,10 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
   } else if (in_bytes > 0 && oscar::launch_stage(host_in, dev_in, in_bytes, s) != cudaSuccess) {
     return OSCAR_ERR_CUDA;
   }
+  // after a copy kernel of this call the demotion reads what it wrote: it
+  // waits first; otherwise the caller may let it overlap the kernel before
+  const bool staged = in_bytes > 0 && !direct_in;
+  if ((flags & OSCAR_STEP_OVERLAP_PREVIOUS) && !staged) pa.early = 1;
   if (!empty && launch_append(pa, s) != cudaSuccess) return OSCAR_ERR_CUDA;
   // a 16-byte aligned host_out is written by the decode kernel itself, with
   // the same stores as `out`; otherwise a copy kernel follows it

@@ -359,6 +359,36 @@ oscar_status oscar_quantize_append(const oscar_layer_desc* desc,
                                    const uint16_t* new_v, void* stream);
 
 /*
+ * oscar_quantize_append_overlapped - oscar_quantize_append whose reads and
+ * arithmetic run while the kernel before it on `stream` is still running.
+ * [ZAKER] pipeline part (demote the oldest recent token, write the new one):
+ * the same operation, the same arguments, bit for bit the same results.
+ *
+ *   The per-token kernel reads the rotations, the index arrays, the page
+ *   table and the source rows, rotates and quantises, and only then waits
+ *   for the previous kernel on the stream to finish; the code stores and
+ *   the new-token writes into k_src / v_src follow the wait.  This is for a
+ *   decode loop in which that previous kernel is the attention of the layer
+ *   before (oscar_decode_attention reads, never writes, the cache).
+ *   Precondition (the caller's): the kernel issued on `stream` just before
+ *   this call writes none of desc->r_k / r_v, desc->page_table, src_index,
+ *   dst_req, dst_pos, new_k, new_v and the source rows src_index names (it
+ *   may read them, and it may read or write anything else).  Kernels before
+ *   that one are complete: every kernel of this library waits for its
+ *   predecessor before it lets a successor start early, and other kernels
+ *   let none start early.  Calls that take the tensor-core path (n >= 1024,
+ *   no new rows) wait first, like oscar_quantize_append.  Argument checks
+ *   and error codes are those of oscar_quantize_append.  Async.
+ */
+oscar_status oscar_quantize_append_overlapped(const oscar_layer_desc* desc,
+                                              uint16_t* k_src, uint16_t* v_src,
+                                              int64_t src_rows, int64_t row_stride,
+                                              const int32_t* src_index,
+                                              const int32_t* dst_req, const int32_t* dst_pos,
+                                              int32_t n, const uint16_t* new_k,
+                                              const uint16_t* new_v, void* stream);
+
+/*
  * oscar_decode_attention - one decode step of attention for every request of
  * the batch over BF16 sink | INT2 history | BF16 recent.  [ZAKER] pipeline
  * part (INT2 kernel: unpack, scale/zero dequantisation, float accumulation;
@@ -418,14 +448,23 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
  *   given (OSCAR_ERR_WORKSPACE).  Async: host_in must not change until the
  *   stream has passed step (3), and host_out holds the output once the
  *   stream has passed step (4).
+ *
+ *   flags: 0, or OSCAR_STEP_OVERLAP_PREVIOUS: when no copy kernel of step
+ *   (1) runs, step (2) is oscar_quantize_append_overlapped (its reads and
+ *   arithmetic overlap the kernel before the call on `stream`), under that
+ *   function's precondition on that kernel; in a loop of oscar_decode_step
+ *   calls that kernel is the previous call's decode (or its output copy),
+ *   which qualifies as long as host_out and out overlap none of the inputs.
+ *   Other bits: OSCAR_ERR_INVALID_ARG.
  */
+#define OSCAR_STEP_OVERLAP_PREVIOUS 1u
 oscar_status oscar_decode_step(const oscar_layer_desc* desc, const void* host_in, void* dev_in,
                                size_t in_bytes, uint16_t* k_src, uint16_t* v_src, int64_t src_rows,
                                int64_t row_stride, const int32_t* src_index, const int32_t* dst_req,
                                const int32_t* dst_pos, int32_t n, const uint16_t* new_k,
                                const uint16_t* new_v, const uint16_t* q, float* out,
                                void* workspace, size_t workspace_bytes, float* host_out,
-                               void* stream);
+                               uint32_t flags, void* stream);
 
 /*
  * oscar_decode_attention_static - oscar_decode_attention for callers that

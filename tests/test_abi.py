@@ -282,7 +282,7 @@ def test_decode_step_rejects_before_any_copy(built_lib):
     fake = 1 << 20
     args = lambda desc, host_in, dev_in, nbytes, ws: (  # noqa: E731
         ctypes.byref(desc), host_in, dev_in, nbytes, fake, fake, 4, 128, None, fake, fake, 1, None, None,
-        fake, fake, ws, 1 << 20, None, None)
+        fake, fake, ws, 1 << 20, None, 0, None)
     # staged bytes without both buffers
     assert B.lib.oscar_decode_step(*args(_desc(), None, fake, 64, fake)) == 1
     assert B.lib.oscar_decode_step(*args(_desc(), fake, None, 64, fake)) == 1
@@ -290,6 +290,10 @@ def test_decode_step_rejects_before_any_copy(built_lib):
     assert B.lib.oscar_decode_step(*args(_desc(), None, None, 0, None)) == 3
     # a bad descriptor
     assert B.lib.oscar_decode_step(*args(_desc(head_dim=64), None, None, 0, fake)) == 1
+    # unknown flag bits
+    bad = list(args(_desc(), None, None, 0, fake))
+    bad[-2] = 2
+    assert B.lib.oscar_decode_step(*bad) == 1
 
 
 def test_fit_codebook_arguments_and_single_round(built_lib):

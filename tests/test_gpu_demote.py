@@ -203,6 +203,85 @@ def test_append_then_decode_matches_oracle_steps():
         assert err.max() <= 2e-3, (step, err.max())
 
 
+@pytest.mark.parametrize("n_layers", [1, 2])
+def test_overlapped_append_in_a_decode_chain(n_layers):
+    """oscar_quantize_append_overlapped reads and rotates while the previous
+    kernel (the attention of the layer before, or of the same layer one step
+    earlier) still runs.  A chain of steps launched back to back with no
+    host synchronisation gives the pages, rings and outputs of the same chain
+    with oscar_quantize_append bit for bit, and the last step's output of
+    layer 0 matches the oracle replaying the steps."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    steps = 4
+    base = H.Scenario(2013, [1100, 600], n_kv=2, g=4)
+    dev = torch.device("cuda", 0)
+    newk = [[synth.activations(base.seed, (10, s, i, 0), base.B, base.outl) for i in range(n_layers)]
+            for s in range(steps)]
+    newv = [[synth.activations(base.seed, (10, s, i, 1), base.B, base.outl) for i in range(n_layers)]
+            for s in range(steps)]
+    results = []
+    for overlapped in (False, True):
+        append = B.oscar_quantize_append_overlapped if overlapped else B.oscar_quantize_append
+        layers = [H.to_device(base) for _ in range(n_layers)]
+        q = layers[0][1]
+        # per-step lengths and ring starts, resident before the chain starts
+        hl = [torch.from_numpy((base.hist_len + s).astype(np.int32)).to(dev) for s in range(steps + 1)]
+        rs = [torch.from_numpy(((base.recent_start + s) % 256).astype(np.int32)).to(dev) for s in range(steps + 1)]
+        src = [torch.tensor([b * 256 + (int(base.recent_start[b]) + s) % 256 for b in range(base.B)],
+                            dtype=torch.int32, device=dev) for s in range(steps)]
+        dr = torch.arange(base.B, dtype=torch.int32, device=dev)
+        nk = [[torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in row] for row in newk]
+        nv = [[torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in row] for row in newv]
+        outs = [[torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(n_layers)]
+                for _ in range(steps)]
+        # one workspace per launch (the chain keeps several in flight)
+        wss = [torch.zeros(B.oscar_decode_workspace_bytes(layers[0][0].desc(int(base.hist_len.max()) + s + 1)),
+                           dtype=torch.uint8, device=dev) for s in range(steps) for _ in range(n_layers)]
+        torch.cuda.synchronize()
+        for s in range(steps):
+            for i, (cache, _) in enumerate(layers):
+                da = cache.desc(int(base.hist_len.max()) + s + 1)
+                da.hist_len, da.recent_start = hl[s].data_ptr(), rs[s].data_ptr()
+                dd = cache.desc(int(base.hist_len.max()) + s + 1)
+                dd.hist_len, dd.recent_start = hl[s + 1].data_ptr(), rs[s + 1].data_ptr()
+                append(da, cache.recent_k.view(torch.uint16), cache.recent_v.view(torch.uint16), base.B * 256,
+                       base.n_kv * 128, src[s], dr, hl[s], base.B, nk[s][i].view(torch.uint16),
+                       nv[s][i].view(torch.uint16))
+                ws = wss[s * n_layers + i]
+                B.oscar_decode_attention(dd, q, outs[s][i], ws, ws.numel())
+        torch.cuda.synchronize()
+        for cache, _ in layers:
+            assert int(cache.dev_status.item()) == 0
+        results.append([o.cpu().numpy() for row in outs for o in row] +
+                       [t.cpu().numpy() for cache, _ in layers
+                        for t in (cache.pages, cache.recent_k.view(torch.uint16), cache.recent_v.view(torch.uint16))])
+    for a, b in zip(*results):
+        np.testing.assert_array_equal(a, b)
+    # the oracle replays layer 0's steps with its own demotion
+    hist = [dict((k, v.copy()) for k, v in h.items()) for h in base.hist]
+    recents = [list(zip(*base.segments(b)[2:])) for b in range(base.B)]
+    for s in range(steps):
+        for b in range(base.B):
+            ok, ov = recents[b].pop(0)
+            ck, sk, zk = H.demote_heads(ok[None], base.rk32, base.tau_k)
+            cv, sv, zv = H.demote_heads(ov[None], base.rv32, base.tau_v)
+            for name, arr in (("codes_k", ck), ("scale_k", sk), ("zero_k", zk), ("codes_v", cv),
+                              ("scale_v", sv), ("zero_v", zv)):
+                hist[b][name] = np.concatenate([hist[b][name], arr])
+            recents[b].append((newk[s][0][b], newv[s][0][b]))
+    got = results[1][(steps - 1) * n_layers].astype(np.float64)
+    ref = np.zeros_like(got)
+    for b in range(base.B):
+        sk_, sv_, _, _ = base.segments(b)
+        rk = np.stack([x[0] for x in recents[b]])
+        rv = np.stack([x[1] for x in recents[b]])
+        ref[b] = O.decode_attention(base.q[b].astype(np.float64), sk_, sv_, hist[b], rk, rv,
+                                    base.rk32.astype(np.float64), base.rv32.astype(np.float64))
+    err = H.relative_error(got, ref)
+    assert err.max() <= 2e-3, err.max()
+
+
 def test_decode_step_equals_separate_calls():
     """oscar_decode_step (staged H2D copy, demotion, decode, D2H copy) gives the
     output of oscar_quantize_append + oscar_decode_attention bit for bit."""
@@ -242,6 +321,61 @@ def test_decode_step_equals_separate_calls():
         assert int(cache.dev_status.item()) == 0
         outs.append((out.cpu().numpy(), cache.pages.cpu().numpy(), cache.recent_k.float().cpu().numpy()))
     for a, b in zip(outs[0], outs[1]):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_decode_step_overlap_flag_in_a_chain():
+    """oscar_decode_step calls launched back to back over two layers, with
+    the inputs read straight from pinned host memory: with
+    OSCAR_STEP_OVERLAP_PREVIOUS (the demotion overlaps the previous call's
+    decode) the outputs, pages and rings equal those without it bit for bit."""
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    steps, n_layers = 3, 2
+    base = H.Scenario(2014, [900, 1400], n_kv=2, g=4)
+    dev = torch.device("cuda", 0)
+    results = []
+    for flags in (0, B.OSCAR_STEP_OVERLAP_PREVIOUS):
+        layers = [H.to_device(base) for _ in range(n_layers)]
+        q = layers[0][1]
+        hl = [torch.from_numpy((base.hist_len + s).astype(np.int32)).to(dev) for s in range(steps + 1)]
+        rs = [torch.from_numpy(((base.recent_start + s) % 256).astype(np.int32)).to(dev) for s in range(steps + 1)]
+        src = [torch.tensor([b * 256 + (int(base.recent_start[b]) + s) % 256 for b in range(base.B)],
+                            dtype=torch.int32, device=dev) for s in range(steps)]
+        dr = torch.arange(base.B, dtype=torch.int32, device=dev)
+        # per (step, layer): q, new K, new V in one pinned buffer and its staging range
+        nq, nk = q.numel(), base.B * base.n_kv * 128
+        hosts, stages = [], []
+        for s in range(steps):
+            for i in range(n_layers):
+                newk = synth.activations(base.seed, (11, s, i, 0), base.B, base.outl)
+                newv = synth.activations(base.seed, (11, s, i, 1), base.B, base.outl)
+                hosts.append(torch.cat([q.cpu().flatten(), torch.from_numpy(newk).to(torch.bfloat16).flatten(),
+                                        torch.from_numpy(newv).to(torch.bfloat16).flatten()]).pin_memory())
+                stages.append(torch.empty(nq + 2 * nk, dtype=torch.bfloat16, device=dev))
+        host_outs = [torch.zeros(q.shape, dtype=torch.float32).pin_memory() for _ in range(steps * n_layers)]
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        ws_bytes = B.oscar_decode_workspace_bytes(layers[0][0].desc(int(base.hist_len.max()) + steps))
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        for s in range(steps):
+            for i, (cache, _) in enumerate(layers):
+                k = s * n_layers + i
+                st = stages[k]
+                desc = cache.desc(int(base.hist_len.max()) + s + 1)
+                desc.hist_len, desc.recent_start = hl[s + 1].data_ptr(), rs[s + 1].data_ptr()
+                B.oscar_decode_step(desc, hosts[k], st, st.numel() * 2, cache.recent_k.view(torch.uint16),
+                                    cache.recent_v.view(torch.uint16), base.B * 256, base.n_kv * 128, src[s], dr,
+                                    hl[s], base.B, st[nq:nq + nk].view(torch.uint16),
+                                    st[nq + nk:].view(torch.uint16), st[:nq].view_as(q), out, ws, ws_bytes,
+                                    host_outs[k], flags=flags)
+        torch.cuda.synchronize()
+        for cache, _ in layers:
+            assert int(cache.dev_status.item()) == 0
+        results.append([h.numpy().copy() for h in host_outs] +
+                       [t.cpu().numpy() for cache, _ in layers
+                        for t in (cache.pages, cache.recent_k.view(torch.uint16), cache.recent_v.view(torch.uint16))])
+    for a, b in zip(*results):
         np.testing.assert_array_equal(a, b)
 
 
