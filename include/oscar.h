@@ -367,16 +367,18 @@ oscar_status oscar_quantize_append(const oscar_layer_desc* desc,
  *   The per-token kernel reads the rotations, the index arrays, the page
  *   table and the source rows, rotates and quantises, and only then waits
  *   for the previous kernel on the stream to finish; the code stores and
- *   the new-token writes into k_src / v_src follow the wait.  This is for a
- *   decode loop in which that previous kernel is the attention of the layer
- *   before (oscar_decode_attention reads, never writes, the cache).
- *   Precondition (the caller's): the kernel issued on `stream` just before
- *   this call writes none of desc->r_k / r_v, desc->page_table, src_index,
- *   dst_req, dst_pos, new_k, new_v and the source rows src_index names (it
- *   may read them, and it may read or write anything else).  Kernels before
- *   that one are complete: every kernel of this library waits for its
- *   predecessor before it lets a successor start early, and other kernels
- *   let none start early.  Calls that take the tensor-core path (n >= 1024,
+ *   the new-token writes into k_src / v_src (new_k / new_v are read only
+ *   then) follow the wait.  This is for a decode loop in which that previous
+ *   kernel is the projection that produces new_k / new_v, or the attention
+ *   of the layer before (oscar_decode_attention reads, never writes, the
+ *   cache).  Precondition (the caller's): the kernel issued on `stream` just
+ *   before this call writes none of desc->r_k / r_v, desc->page_table,
+ *   src_index, dst_req, dst_pos and the source rows src_index names (it may
+ *   read them, it may write new_k / new_v, and it may read or write anything
+ *   else).  The kernels before that one must be complete when it lets this
+ *   one start: true when it is a kernel of this library (each waits for its
+ *   predecessor before it lets a successor start early) or a kernel that
+ *   does not trigger its dependents early.  Calls that take the tensor-core path (n >= 1024,
  *   no new rows) wait first, like oscar_quantize_append.  Argument checks
  *   and error codes are those of oscar_quantize_append.  Async.
  */
