@@ -76,13 +76,16 @@ __device__ __forceinline__ void store_codes(const DemoteParams& p, int ng, int w
 
 // NGK / NGV: quantisation groups per token-head of K and V (template
 // arguments, so a kernel holds only the finishing code it uses).
-// kEarly (DemoteParams::early): the caller guarantees that the kernel just
-// before on the stream writes none of the rotation, the index arrays, the
-// page table and the source rows, so everything up to the codes runs before
-// the wait for that kernel; only the stores (the codes, and the new tokens
-// into the source rows) follow it.
+// kEarly (DemoteParams::early): the caller guarantees that the kernels that
+// may still run (the one just before on the stream, and the ones it lets
+// start early) write none of the rotation, the index arrays, the page table
+// and the source rows, so everything up to the codes runs before the wait
+// for that kernel; only the stores (the codes, and the new tokens into the
+// source rows) follow it.  The next kernel may start at once: it waits for
+// this one before it reads anything this one writes.
 template <int NGK, int NGV, bool kLevels, bool kEarly = false>
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
+  if constexpr (kEarly) pdl_launch_dependents();
   {
     // L2 prefetch of this CTA's rotation (a hint that reads nothing, so it
     // may precede the wait for the previous kernel)
@@ -214,7 +217,6 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   }
   if constexpr (kEarly) {
     pdl_wait();                 // the previous kernel is done: the stores may start
-    pdl_launch_dependents();
     write_new_tokens();
     if (warp == 0) {
 #pragma unroll

@@ -371,14 +371,18 @@ oscar_status oscar_quantize_append(const oscar_layer_desc* desc,
  *   then) follow the wait.  This is for a decode loop in which that previous
  *   kernel is the projection that produces new_k / new_v, or the attention
  *   of the layer before (oscar_decode_attention reads, never writes, the
- *   cache).  Precondition (the caller's): the kernel issued on `stream` just
- *   before this call writes none of desc->r_k / r_v, desc->page_table,
- *   src_index, dst_req, dst_pos and the source rows src_index names (it may
- *   read them, it may write new_k / new_v, and it may read or write anything
- *   else).  The kernels before that one must be complete when it lets this
- *   one start: true when it is a kernel of this library (each waits for its
- *   predecessor before it lets a successor start early) or a kernel that
- *   does not trigger its dependents early.  Calls that take the tensor-core path (n >= 1024,
+ *   cache).  Precondition (the caller's): no kernel that may still be
+ *   running when this one starts writes desc->r_k / r_v, desc->page_table,
+ *   src_index, dst_req, dst_pos or the source rows src_index names; new_k /
+ *   new_v and anything else may be written.  Those kernels are the one
+ *   issued on `stream` just before this call and, if that one lets its
+ *   successor start early, the ones still running at that point.  The other
+ *   kernels of this library let a successor start only after their own
+ *   wait, so after one of them only that kernel counts.  This kernel lets
+ *   its successor start at once (the successor's own wait still covers
+ *   everything this kernel and its predecessor write), so for a call after
+ *   it that reads before its wait, this call's predecessor counts too.
+ *   Calls that take the tensor-core path (n >= 1024,
  *   no new rows) wait first, like oscar_quantize_append.  Argument checks
  *   and error codes are those of oscar_quantize_append.  Async.
  */
