@@ -98,6 +98,11 @@
 #ifndef OSCAR_GROUP_G8
 #define OSCAR_GROUP_G8 3
 #endif
+// splits per (request, KV head): 0 = the planner's model; n > 0 forces n
+// (tuning builds)
+#ifndef OSCAR_PLAN_SPLITS
+#define OSCAR_PLAN_SPLITS 0
+#endif
 
 namespace oscar {
 namespace {
@@ -1776,6 +1781,7 @@ int plan_decode(int batch, int n_kv, int group, int sink_cap, int recent_cap, in
       n_splits = n;
     }
   }
+  if (OSCAR_PLAN_SPLITS > 0) n_splits = min(OSCAR_PLAN_SPLITS, kMaxSplits);
   int pps = max(1, (pages_max + n_splits - 1) / n_splits);
   n_splits = max(1, (pages_max + pps - 1) / pps);
   plan->n_splits = n_splits;
