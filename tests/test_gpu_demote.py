@@ -29,7 +29,7 @@ def _pre_rounding(x_rot_clipped):
 
 
 def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None, first_row=None,
-         groups=None, levels=None, scale=None):
+         groups=None, levels=None, scale=None, overlapped=False):
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     from bit_rotated_kv_split_gb300.cache import LayerCache
@@ -78,10 +78,11 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         new_v = torch.from_numpy(nv).to(torch.bfloat16).to(dev)
     k_in = k_src[first_row:] if first_row is not None else k_src
     v_in = v_src[first_row:] if first_row is not None else v_src
-    B.oscar_quantize_append(cache.desc(hist), k_in.view(torch.uint16), v_in.view(torch.uint16),
-                            k_in.shape[0], n_kv * 128, si, dr, dp, n_tok,
-                            None if new_k is None else new_k.view(torch.uint16),
-                            None if new_v is None else new_v.view(torch.uint16))
+    append = B.oscar_quantize_append_overlapped if overlapped else B.oscar_quantize_append
+    append(cache.desc(hist), k_in.view(torch.uint16), v_in.view(torch.uint16),
+           k_in.shape[0], n_kv * 128, si, dr, dp, n_tok,
+           None if new_k is None else new_k.view(torch.uint16),
+           None if new_v is None else new_v.view(torch.uint16))
     torch.cuda.synchronize()
     assert int(cache.dev_status.item()) == 0
     pool = cache.pages.cpu().numpy()
@@ -114,6 +115,31 @@ def _run(seed, n_tok, n_kv, positions=None, with_new=False, canalized_block=None
         np.testing.assert_array_equal(k_src.float().cpu().numpy()[src_index], nk)
         np.testing.assert_array_equal(v_src.float().cpu().numpy()[src_index], nv)
     return res
+
+
+def _lloyd_levels(seed, n_kv):
+    """(levels_k, levels_v): the oracle's Lloyd-Max fit on seeded calibration rows."""
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    rk32, rv32, tau_k, tau_v = H.rotations(seed, 0, n_kv, outl, n_q=1024, n_k=512)
+    out = []
+    for r32, tau, sub in ((rk32, tau_k, 0), (rv32, tau_v, 1)):
+        x = synth.activations(seed, (3, sub), 256, outl)
+        out.append(np.asarray(O.fit_codebook(x[:, 0].astype(np.float64), r32[0].astype(np.float64), tau),
+                              np.float16))
+    return tuple(out)
+
+
+@pytest.mark.parametrize("variant", ["uniform", "groups32", "groups64x128", "levels", "bulk"])
+def test_overlapped_entry_point_matches_oracle(variant):
+    """oscar_quantize_append_overlapped (every kernel form it instantiates,
+    and the tensor-core path it forwards to) under the same code rule."""
+    if variant == "bulk":
+        res = _run(2016, 1500, 2, overlapped=True)
+    else:
+        groups = {"groups32": (32, 32), "groups64x128": (64, 128)}.get(variant)
+        levels = _lloyd_levels(2015, 4) if variant == "levels" else None
+        res = _run(2015, 300, 4, with_new=True, groups=groups, levels=levels, overlapped=True)
+    print(res)
 
 
 def test_demote_tiny_config_tokens():
