@@ -81,8 +81,10 @@ __device__ __forceinline__ void store_codes(const DemoteParams& p, int ng, int w
 // start early) write none of the rotation, the index arrays, the page table
 // and the source rows, so everything up to the codes runs before the wait
 // for that kernel; only the stores (the codes, and the new tokens into the
-// source rows) follow it.  The next kernel may start at once: it waits for
-// this one before it reads anything this one writes.
+// source rows) follow it, and the loads of the new tokens unless
+// DemoteParams::early_rows says that kernel does not write them either.  The
+// next kernel may start at once: it waits for this one before it reads
+// anything this one writes.
 template <int NGK, int NGV, bool kLevels, bool kEarly = false>
 __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   if constexpr (kEarly) pdl_launch_dependents();
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   const int item0 = int(blockIdx.x) * kItems;
   bool live[kItems];
   int64_t page[kItems];
+  int64_t srow[kItems];        // the item's source row (the new token goes there)
   int slot[kItems];
   float xv[kItems];            // x_i, i = 32 warp + lane
 #pragma unroll
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
     const int item = item0 + it;
     live[it] = item < p.n;
     page[it] = -1;
+    srow[it] = 0;
     slot[it] = 0;
     xv[it] = 0.f;
     if (!live[it]) continue;
@@ -148,6 +152,7 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
       live[it] = false;
       continue;
     }
+    srow[it] = row;
     const uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
     xv[it] = bf16_lo(uint32_t(src[32 * warp + lane]));
     page[it] = p.page_table[int64_t(bq) * p.max_pages + pos / kPage];
@@ -157,20 +162,29 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   // warp has read its part of them
   __syncthreads();
   const uint16_t* fresh = which ? p.new_v : p.new_k;
-  auto write_new_tokens = [&]() {
+  uint16_t nv[kItems];         // the new tokens' elements 32 warp + lane
+  auto load_new_tokens = [&]() {
+#pragma unroll
+    for (int it = 0; it < kItems; ++it)
+      nv[it] = fresh && live[it]
+                   ? __ldcv(reinterpret_cast<const unsigned short*>(fresh) +
+                            (int64_t(item0 + it) * p.n_kv + head) * kHeadDim + 32 * warp + lane)
+                   : uint16_t(0);
+  };
+  auto store_new_tokens = [&]() {
     if (!fresh) return;
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
-      if (!live[it]) continue;
-      const int item = item0 + it;
-      const int64_t row = p.src_index ? int64_t(__ldcv(p.src_index + item)) : int64_t(item);
-      uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
-      src[32 * warp + lane] =
-          __ldcv(reinterpret_cast<const unsigned short*>(fresh) + (int64_t(item) * p.n_kv + head) * kHeadDim +
-                 32 * warp + lane);
+      uint16_t* dst = (which ? p.v_src : p.k_src) + srow[it] * p.row_stride + int64_t(head) * kHeadDim;
+      if (live[it]) dst[32 * warp + lane] = nv[it];
     }
   };
-  if constexpr (!kEarly) write_new_tokens();
+  if constexpr (!kEarly) {
+    load_new_tokens();
+    store_new_tokens();
+  } else if (p.early_rows) {
+    load_new_tokens();         // the caller's rows are final already
+  }
 
   // warp w needs the rows 32 w .. 32 w + 31 of R: quarter w of the copy;
   // on an expired wait the whole CTA leaves (after waiting, bounded, for
@@ -217,7 +231,8 @@ __global__ void __launch_bounds__(kWarps * 32) demote_kernel(DemoteParams p) {
   }
   if constexpr (kEarly) {
     pdl_wait();                 // the previous kernel is done: the stores may start
-    write_new_tokens();
+    if (!p.early_rows) load_new_tokens();
+    store_new_tokens();
     if (warp == 0) {
 #pragma unroll
       for (int it = 0; it < kItems; ++it)

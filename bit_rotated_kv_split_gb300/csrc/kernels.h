@@ -123,8 +123,9 @@ struct DemoteParams {
   int32_t use_tma;
   // per-token path: 1 = everything before the stores runs ahead of the wait
   // for the previous kernel on the stream (that kernel writes nothing the
-  // demotion reads)
-  int32_t early;
+  // demotion reads before it); early_rows: the new rows are read ahead of it
+  // too (that kernel does not write them either)
+  int32_t early, early_rows;
 };
 
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t stream);

@@ -365,7 +365,7 @@ extern "C" oscar_status oscar_decode_step(const oscar_layer_desc* desc, const vo
   // after a copy kernel of this call the demotion reads what it wrote: it
   // waits first; otherwise the caller may let it overlap the kernel before
   const bool staged = in_bytes > 0 && !direct_in;
-  if ((flags & OSCAR_STEP_OVERLAP_PREVIOUS) && !staged) pa.early = 1;
+  if ((flags & OSCAR_STEP_OVERLAP_PREVIOUS) && !staged) pa.early = pa.early_rows = 1;
   if (!empty && launch_append(pa, s) != cudaSuccess) return OSCAR_ERR_CUDA;
   // a 16-byte aligned host_out is written by the decode kernel itself, with
   // the same stores as `out`; otherwise a copy kernel follows it

@@ -458,9 +458,11 @@ oscar_status oscar_decode_attention(const oscar_layer_desc* desc, const uint16_t
  *   flags: 0, or OSCAR_STEP_OVERLAP_PREVIOUS: when no copy kernel of step
  *   (1) runs, step (2) is oscar_quantize_append_overlapped (its reads and
  *   arithmetic overlap the kernel before the call on `stream`), under that
- *   function's precondition on that kernel; in a loop of oscar_decode_step
- *   calls that kernel is the previous call's decode (or its output copy),
- *   which qualifies as long as host_out and out overlap none of the inputs.
+ *   function's precondition on that kernel, which here covers new_k / new_v
+ *   too (they are read before the wait as well); in a loop of
+ *   oscar_decode_step calls that kernel is the previous call's decode (or
+ *   its output copy), which qualifies as long as host_out and out overlap
+ *   none of the inputs.
  *   Other bits: OSCAR_ERR_INVALID_ARG.
  */
 #define OSCAR_STEP_OVERLAP_PREVIOUS 1u
