@@ -1100,6 +1100,34 @@ __global__ void __launch_bounds__(Geo<G>::T, 1) split_kernel(const __grid_consta
       }
     }
   }
+  if (bf16_warp) {
+    // the K and V rows of this warp's BF16 virtual pages (lane: token
+    // lane % 16, K or V, both 128-byte lines of the row); the ring start
+    // is read ahead of the wait only to place these hints, so a stale
+    // value costs nothing but useless lines
+    const int bw = warp - (W - kBf16Warps);
+    const int n_vp = p.sink_cap / kPage + p.recent_cap / kPage;
+    int start = 0;
+    if (p.recent_cap > 0) {
+      start = *reinterpret_cast<const volatile int32_t*>(p.recent_start + b) % p.recent_cap;
+      start += start < 0 ? p.recent_cap : 0;
+    }
+    const int64_t hstride = int64_t(p.n_kv) * kHeadDim;
+    for (int vp = split + bw * n_splits; vp < n_vp; vp += kBf16Warps * n_splits) {
+      const int u = vp * kPage + (lane & 15);
+      const bool kv = lane >= 16;
+      const uint16_t* a;
+      if (u < p.sink_cap) {
+        a = (kv ? p.sink_v : p.sink_k) + (int64_t(b) * p.sink_cap + u) * hstride;
+      } else {
+        const int slot = (start + u - p.sink_cap) % p.recent_cap;
+        a = (kv ? p.recent_v : p.recent_k) + (int64_t(b) * p.recent_cap + slot) * hstride;
+      }
+      a += int64_t(hkv) * kHeadDim;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 64));
+    }
+  }
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();
 
