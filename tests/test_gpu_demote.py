@@ -350,11 +350,14 @@ def test_decode_step_equals_separate_calls():
         np.testing.assert_array_equal(a, b)
 
 
-def test_decode_step_overlap_flag_in_a_chain():
-    """oscar_decode_step calls launched back to back over two layers, with
-    the inputs read straight from pinned host memory: with
+@pytest.mark.parametrize("staged", [False, True])
+def test_decode_step_overlap_flag_in_a_chain(staged):
+    """oscar_decode_step calls launched back to back over two layers: with
     OSCAR_STEP_OVERLAP_PREVIOUS (the demotion overlaps the previous call's
-    decode) the outputs, pages and rings equal those without it bit for bit."""
+    decode) the outputs, pages and rings equal those without it bit for bit,
+    both with the inputs read straight from pinned host memory and with them
+    staged by the copy kernel (host buffer off the device buffer's 16-byte
+    alignment), where the flag must leave the demotion waiting first."""
     import torch
     from bit_rotated_kv_split_gb300 import binding as B
     steps, n_layers = 3, 2
@@ -376,7 +379,8 @@ def test_decode_step_overlap_flag_in_a_chain():
             for i in range(n_layers):
                 newk = synth.activations(base.seed, (11, s, i, 0), base.B, base.outl)
                 newv = synth.activations(base.seed, (11, s, i, 1), base.B, base.outl)
-                hosts.append(torch.cat([q.cpu().flatten(), torch.from_numpy(newk).to(torch.bfloat16).flatten(),
+                pad = torch.zeros(4 if staged else 0, dtype=torch.bfloat16)   # 8 bytes: off the grid
+                hosts.append(torch.cat([pad, q.cpu().flatten(), torch.from_numpy(newk).to(torch.bfloat16).flatten(),
                                         torch.from_numpy(newv).to(torch.bfloat16).flatten()]).pin_memory())
                 stages.append(torch.empty(nq + 2 * nk, dtype=torch.bfloat16, device=dev))
         host_outs = [torch.zeros(q.shape, dtype=torch.float32).pin_memory() for _ in range(steps * n_layers)]
@@ -390,7 +394,8 @@ def test_decode_step_overlap_flag_in_a_chain():
                 st = stages[k]
                 desc = cache.desc(int(base.hist_len.max()) + s + 1)
                 desc.hist_len, desc.recent_start = hl[s + 1].data_ptr(), rs[s + 1].data_ptr()
-                B.oscar_decode_step(desc, hosts[k], st, st.numel() * 2, cache.recent_k.view(torch.uint16),
+                host_in = hosts[k].data_ptr() + (8 if staged else 0)
+                B.oscar_decode_step(desc, host_in, st, st.numel() * 2, cache.recent_k.view(torch.uint16),
                                     cache.recent_v.view(torch.uint16), base.B * 256, base.n_kv * 128, src[s], dr,
                                     hl[s], base.B, st[nq:nq + nk].view(torch.uint16),
                                     st[nq + nk:].view(torch.uint16), st[:nq].view_as(q), out, ws, ws_bytes,
