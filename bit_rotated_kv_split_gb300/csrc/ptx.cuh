@@ -157,6 +157,19 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&d)[4], const void* 
                : "r"(smem_addr(row_addr)));
 }
 
+// 16 bytes global -> shared, asynchronous (L2 only); src_bytes < 16 fills
+// the rest with zeros (0: no bytes are read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits until at most N of this thread's committed groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // D += A (16x16 bf16, row) * B (16x8 bf16, col), f32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -3,9 +3,10 @@ oracle, and the rotation built from it.
 
 [GIST] 2.1 and 2.2 A: C_Q = Q^T Q / N over calibration queries, C_S =
 (S V)^T (S V) / N.  The device computes fp32 sums of exact bf16 products
-(partials of at most 2048 rows, then the partials in chunk order), so each
-entry must lie within the summation bound gamma_m * sum_r |x_ri x_rj| / N of
-the oracle's value, m = 2048 + (number of partials) + 2.
+(partials of at most 2048 rows, then the partials in a fixed order of at
+most as many additions per path), so each entry must lie within the
+summation bound gamma_m * sum_r |x_ri x_rj| / N of the oracle's value,
+m = 2048 + (number of partials) + 2.
 """
 import numpy as np
 import pytest
