@@ -9,30 +9,26 @@
 //
 // The rotation of 128 tokens is one 128 x 128 x 128 contraction,
 // D[token][j] = sum_i x[token][i] R[i][j], on tcgen05 (M = N = 128, K = 16
-// per instruction, fp32 accumulators in tensor memory).  x is bf16: each
-// token's row is scaled by a power of two 2^-e that puts its largest
-// magnitude in [2^14, 2^15), which makes every element of 8 significant
-// bits down to 2^-31 of that maximum exact in fp16 at any magnitude of the
-// row; R is scaled by 16 and split into fp16 hi + lo parts (about 22
-// significant bits), so D = x.(16 R)_hi + x.(16 R)_lo and x~ = 2^e D / 16.
-// (Scaling by a power of two commutes with the fp32 sums, so a row whose
-// elements were exact in fp16 unscaled gives the same D times 2^-e.)
+// per instruction, fp32 accumulators in tensor memory).  x is bf16 and is
+// the A operand as it is (exact at any magnitude); R is scaled by 16 and
+// split into three bf16 parts, 16 R = r1 + r2 + r3 with r1 = bf16(16 R),
+// r2 = bf16(16 R - r1), r3 = bf16(16 R - r1 - r2) (about 24 significant
+// bits), so D = x.r3 + x.r2 + x.r1 (products exact in fp32, the smallest
+// parts first) and x~ = D / 16.
 //
-// CTA (tile stride, KV head, K|V) of 13 warps, one CTA per SM:
-//   warps 8-11 bring a tile's 128 source rows into the A operand: with
-//              contiguous rows they convert the bf16 rows that 16 2-D TMA
-//              copies (8 columns x 128 rows each, one K column of 8 x 16-byte
-//              core matrices) put there to fp16 in place; with gathered rows
-//              each thread loads its token's row; they also look up each
-//              token's page;
-//   warp 12    issues the 16 MMAs of a tile from one lane;
+// CTA (tile stride, KV head, K|V) of 14 warps, one CTA per SM:
+//   warps 8-11 look up each token's page; with gathered rows each thread
+//              also loads its token's row into the A operand (with
+//              contiguous rows 16 2-D TMA copies, 8 columns x 128 rows each,
+//              one K column of 8 x 16-byte core matrices, put it there);
+//   warp 12    issues the 24 MMAs of a tile from one lane;
 //   warp 13    starts the tile copies (contiguous rows) as buffers free up;
 //   warps 0-7  read half a token's 128 rotated values from tensor memory
 //              (warps w and w + 4 share the lane quadrant w % 4; thread =
 //              token = TMEM lane), meet on its min/max through shared memory,
 //              form the fp16 scale and zero point, and pack and store 16
 //              bytes of codes each.
-// Operand, accumulator and metadata buffers are fourfold, so loading, MMA
+// Operand, accumulator and metadata buffers are threefold, so loading, MMA
 // and the epilogue of consecutive tiles overlap.  Every wait is bounded (1 s).
 #include <cudaTypedefs.h>
 
@@ -47,18 +43,19 @@ constexpr int kEpiWarps = 8, kLoadWarps = 4;     // epilogue: two warps per TMEM
 constexpr int kMmaWarp = kEpiWarps + kLoadWarps;    // warp 12
 constexpr int kTmaWarp = kMmaWarp + 1;               // warp 13: source tile copies
 constexpr int kThreads = (kTmaWarp + 1) * 32;
-constexpr int kOpBytes = kTile * kHeadDim * 2;      // one fp16 128 x 128 operand
+constexpr int kOpBytes = kTile * kHeadDim * 2;      // one bf16 128 x 128 operand
 constexpr float kRScale = 16.f;
-constexpr int kBufs = 4;                            // operand / accumulator / metadata buffers
-constexpr size_t oBhi = 0, oBlo = kOpBytes, oA = 2 * size_t(kOpBytes);
+constexpr int kBParts = 3;                          // bf16 parts of 16 R
+constexpr int kBufs = 3;                            // operand / accumulator / metadata buffers
+constexpr size_t oB = 0, oA = size_t(kBParts) * kOpBytes;
 constexpr size_t oMeta = oA + size_t(kBufs) * kOpBytes;
 constexpr size_t oXchg = oMeta + size_t(kBufs) * kTile * sizeof(int2);   // [2][2][128][NG] (min, max)
 constexpr size_t oBars = oXchg + 2 * 2 * kTile * 4 * sizeof(float2);   // up to 4 groups
 constexpr size_t kSmem = oBars + (4 * kBufs + 4) * 8 + 16;
-constexpr uint32_t kCols = 128 * kBufs;             // D[kBufs] x 128 columns
-static_assert(kCols <= 512, "tensor memory columns");
+constexpr uint32_t kCols = 512;                     // allocation (a power of two) for D[kBufs] x 128
+static_assert(128 * kBufs <= kCols, "tensor memory columns");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-constexpr uint32_t kIdesc = idesc_f16_f32(128, 128);
+constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // byte offset of (row, k) in a 128 x 128 fp16 operand, canonical K-major
@@ -73,19 +70,6 @@ __device__ __forceinline__ int op_offset(int row, int k) {
 // of one TMA copy), rows 16 bytes apart: LBO 2048, SBO 128, 4096 bytes per
 // K step
 __device__ __forceinline__ int a_offset(int row, int k) { return (k >> 3) * 2048 + row * 16 + (k & 7) * 2; }
-
-__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// two floats -> fp16x2 (lo in the low half), rounded to nearest and
-// saturated to the finite fp16 range by the conversion itself
-__device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 struct Waiter {
   volatile int* abort_flag;
@@ -105,43 +89,11 @@ struct Waiter {
   }
 };
 
-// The token's row scale 2^-e, from the largest magnitude bits mb (bf16,
-// sign cleared) over its 128 elements: e = (biased exponent) - 141, so the
-// scaled maximum lies in [2^14, 2^15); 0 for a zero row or one holding an
-// infinity or NaN; at least -126 (2^e stays a normal float; a subnormal
-// bf16 row scaled by 2^126 is still at least 2^-7).
-__device__ __forceinline__ int row_exponent(uint32_t mb) {
-  if (mb == 0u || mb >= 0x7F80u) return 0;
-  return max(int(mb >> 7) - 141, -126);
-}
-
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }   // e in [-126, 127]
-
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint4 raw) {
-  acc = __vmaxu2(acc, raw.x & 0x7FFF7FFFu);
-  acc = __vmaxu2(acc, raw.y & 0x7FFF7FFFu);
-  acc = __vmaxu2(acc, raw.z & 0x7FFF7FFFu);
-  return __vmaxu2(acc, raw.w & 0x7FFF7FFFu);
-}
-
-// 8 bf16 times 2^-e -> 8 fp16 (exact products: a power of two)
-__device__ __forceinline__ uint4 to_f16_scaled(uint4 raw, float sc) {
-  const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t h[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) h[e] = f16x2_sat(bf16_lo(wv[e]) * sc, bf16_hi(wv[e]) * sc);
-  return make_uint4(h[0], h[1], h[2], h[3]);
-}
-
-// Epilogue of one token-half: v[i] = 16 x~ 2^-e at code position 64 hh + i, whose
+// Epilogue of one token-half: v[i] = 16 x~ at code position 64 hh + i, whose
 // quantisation group is ((64 hh + i) & 7) / (8 / NG) in the page format (K
 // and V alike).  The two halves of a token meet on each group's (min, max)
-// through shared memory; then the group's fp16 scale and zero point, the
-// The row scale 2^e is folded into the extremes and the code
-// coefficients (exact: powers of two; a48 stays a normal float since a
-// nonzero fp16 scale needs a row maximum of at least 2^-26, e >= -40); a
-// row scaled down (e > 0) multiplies its values back first, so that no
-// coefficient can overflow.  kLevels (codebook): the code is the number of the thresholds thr
+// through shared memory; then the group's fp16 scale and zero point and the
+// codes.  kLevels (codebook): the code is the number of the thresholds thr
 // strictly below u = (x - zero) / scale, u formed with the reciprocal of the
 // scale.  Returns false when the exchange wait expired.
 template <int NG, bool kLevels>
@@ -149,13 +101,7 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, float (&v)[kHe
                                            uint64_t* xfull, Waiter& wt, int k, int hh, int j, int2 m, float tau,
                                            int which, int head, const float* thr) {
   constexpr int kSpan = 8 / NG;   // consecutive positions (mod 8) per group
-  const int slot = m.y & (kPage - 1), e = (m.y >> 4) - 256;
-  float fold = pow2f(e);
-  if (e > 0) {
-#pragma unroll
-    for (int i = 0; i < kHeadDim / 2; ++i) v[i] *= fold;
-    fold = 1.f;
-  }
+  const int slot = m.y;
   // clipping moves only the extremes: min and max of the clipped values
   // are the clipped min and max, and a value beyond +-tau gets the code
   // of the clipped extreme (0 or 3) through the final clamp
@@ -191,15 +137,15 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, float (&v)[kHe
   float a48[NG], nzi3[NG], a16[NG], nzi[NG];
 #pragma unroll
   for (int q = 0; q < NG; ++q) {
-    const float lo = fminf(fmaxf(mn[q] * fold * (1.f / kRScale), -tau), tau);
-    const float hi = fminf(fmaxf(mx[q] * fold * (1.f / kRScale), -tau), tau);
+    const float lo = fminf(fmaxf(mn[q] * (1.f / kRScale), -tau), tau);
+    const float hi = fminf(fmaxf(mx[q] * (1.f / kRScale), -tau), tau);
     s16[q] = __float2half_rn(__fdiv_rn(hi - lo, 3.0f));
     z16[q] = __float2half_rn(lo);
     const float s = __half2float(s16[q]), z = __half2float(z16[q]);
     const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-    a48[q] = inv * (1.f / (3.f * kRScale)) * fold;
+    a48[q] = inv * (1.f / (3.f * kRScale));
     nzi3[q] = -z * inv * (1.f / 3.f);
-    a16[q] = inv * (1.f / kRScale) * fold;
+    a16[q] = inv * (1.f / kRScale);
     nzi[q] = -z * inv;
   }
   const float kMagic = 12582912.f;
@@ -276,8 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
   pdl_wait();                 // the previous kernel's writes are visible
   pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* bhi = smem + oBhi;
-  uint8_t* blo = smem + oBlo;
+  uint8_t* bparts = smem + oB;   // [kBParts] bf16 parts of (16 R)^T
   uint8_t* abuf = smem + oA;
   int2* meta = reinterpret_cast<int2*>(smem + oMeta);          // [kBufs][128] (page, slot)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + oBars);
@@ -310,10 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kCols);
-  // B = (16 R)^T split into fp16 hi + lo: B[n][k] = 16 R[k][n]; thread (n,
-  // half of k) writes 8 16-byte chunks of each part
-  // (column n of the product is code position n of the page format, so B
-  // takes column storage_channel(n) of R)
+  // B = (16 R)^T split into three bf16 parts: B[n][k] = 16 R[k][n] = r1 +
+  // r2 + r3, each part the bf16 rounding of what the previous ones leave
+  // (exact differences in fp32); thread (n, half of k) writes 8 16-byte
+  // chunks of each part (column n of the product is code position n of the
+  // page format, so B takes column storage_channel(n) of R)
   if (tid < 2 * kTile) {
     const int n = tid & (kTile - 1), k0 = (tid >> 7) * 64;
     const int ng = which ? p.ng_v : p.ng_k;
@@ -322,17 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
 #pragma unroll 2
     for (int kc = 0; kc < 8; ++kc) {
       const int k = k0 + 8 * kc;
-      uint32_t hi[4], lo[4];
+      uint32_t part[kBParts][4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float r0 = __ldg(rg + (k + 2 * e) * kHeadDim) * kRScale;
-        const float r1 = __ldg(rg + (k + 2 * e + 1) * kHeadDim) * kRScale;
-        const __half h0 = __float2half_rn(r0), h1 = __float2half_rn(r1);
-        hi[e] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
-        lo[e] = f16x2(r0 - __half2float(h0), r1 - __half2float(h1));
+        float r0 = __ldg(rg + (k + 2 * e) * kHeadDim) * kRScale;
+        float r1 = __ldg(rg + (k + 2 * e + 1) * kHeadDim) * kRScale;
+#pragma unroll
+        for (int t = 0; t < kBParts; ++t) {
+          part[t][e] = pack_bf162(r0, r1);
+          r0 -= bf16_lo(part[t][e]);
+          r1 -= bf16_hi(part[t][e]);
+        }
       }
-      *reinterpret_cast<uint4*>(bhi + op_offset(n, k)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(blo + op_offset(n, k)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+#pragma unroll
+      for (int t = 0; t < kBParts; ++t)
+        *reinterpret_cast<uint4*>(bparts + t * kOpBytes + op_offset(n, k)) =
+            make_uint4(part[t][0], part[t][1], part[t][2], part[t][3]);
     }
     fence_proxy_async_smem();
   }
@@ -438,37 +389,21 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
         }
       }
       uint8_t* a = abuf + buf * kOpBytes;
-      int row_e = 0;
       if (p.use_tma) {
-        // bf16 -> fp16 times the row scale in place, row j of every
-        // 8-column block (a first pass finds the row's largest magnitude)
+        // the tile copies put the bf16 rows in place: the operand is ready
+        // once they have landed
         if (!wt.wait(tma_full + buf, (k / kBufs) & 1)) break;
-        uint32_t mb2 = 0u;
-#pragma unroll
-        for (int c = 0; c < kHeadDim / 8; ++c) mb2 = absmax_bf16x2(mb2, *reinterpret_cast<const uint4*>(a + c * 2048 + j * 16));
-        row_e = row_exponent(max(mb2 & 0xFFFFu, mb2 >> 16));
-        const float sc = pow2f(-row_e);
-#pragma unroll
-        for (int c = 0; c < kHeadDim / 8; ++c) {
-          uint4* q = reinterpret_cast<uint4*>(a + c * 2048 + j * 16);
-          *q = to_f16_scaled(*q, sc);
-        }
       } else {
         const uint16_t* src = (which ? p.v_src : p.k_src) + row * p.row_stride + int64_t(head) * kHeadDim;
         uint4 raw[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           raw[c] = live ? __ldg(reinterpret_cast<const uint4*>(src + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
-        uint32_t mb2 = 0u;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) mb2 = absmax_bf16x2(mb2, raw[c]);
-        row_e = row_exponent(max(mb2 & 0xFFFFu, mb2 >> 16));
-        const float sc = pow2f(-row_e);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(a + a_offset(j, 8 * c)) = to_f16_scaled(raw[c], sc);
+        for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(a + a_offset(j, 8 * c)) = raw[c];
       }
-      // (page, slot | (e + 256) << 4): the epilogue's store target and row scale
-      meta[buf * kTile + j] = make_int2(live ? page : -1, (pos % kPage) | ((row_e + 256) << 4));
+      // (page, slot): the epilogue's store target
+      meta[buf * kTile + j] = make_int2(live ? page : -1, pos % kPage);
       fence_proxy_async_smem();
       mbar_arrive(a_full + buf);
     }
@@ -492,21 +427,21 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
   } else {
     // ================= MMA issue (one lane)
     if (lane == 0) {
-      const uint32_t bh = smem_addr(bhi), bl = smem_addr(blo);
+      const uint32_t bb = smem_addr(bparts);
       for (int k = 0; k < my_tiles; ++k) {
         const int buf = k % kBufs;
         if (!wt.wait(a_full + buf, (k / kBufs) & 1)) break;
         tc_fence_after();
         const uint32_t aa = smem_addr(abuf + buf * kOpBytes);
         const uint32_t d = tmem + uint32_t(buf * 128);
+        // the smallest part first: x.r3, then x.r2, then x.r1
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 2048u, 128u), smem_desc_kmajor(bh + 4096u * kk, 128u, 256u),
-                      kIdesc, kk > 0 ? 1u : 0u);
+        for (int t = kBParts - 1; t >= 0; --t)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 2048u, 128u), smem_desc_kmajor(bl + 4096u * kk, 128u, 256u),
-                      kIdesc, 1u);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_f16_ss(d, smem_desc_kmajor(aa + 4096u * kk, 2048u, 128u),
+                        smem_desc_kmajor(bb + uint32_t(t * kOpBytes) + 4096u * kk, 128u, 256u), kIdesc,
+                        (t < kBParts - 1 || kk > 0) ? 1u : 0u);
         umma_commit(mma_done + buf);
       }
       // every MMA issued has completed before tensor memory is released

@@ -274,6 +274,11 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr, uint32_t lb
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
   return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
+// The same with A and B both bf16 (the A and B format fields, bits 7-9 and
+// 10-12, set together: kind::f16 takes one type for both operands).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return idesc_f16_f32(m, n) | (1u << 7) | (1u << 10);
+}
 
 // D[tmem] (+)= A[smem desc] * B[smem desc], issued by one thread.
 __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

@@ -334,10 +334,10 @@ oscar_status oscar_rotation_file_read(const char* path, int32_t n_layers, int32_
  *   pool layout above.  K and V are both written.
  *
  *   Any finite bf16 row is accepted at any magnitude: calls of n >= 1024
- *   items (the tensor-core path) scale each token-head row by a power of two
- *   before its fp16 operands are formed and scale the result back, so rows
- *   beyond the fp16 range or below its normal range are rotated like any
- *   other.  Rows holding an infinity or a NaN give unspecified codes.
+ *   items (the tensor-core path) multiply the bf16 rows as they are by R
+ *   held as three bf16 parts (about 24 significant bits), with exact
+ *   products and fp32 sums, like the per-token path's fp32 arithmetic.
+ *   Rows holding an infinity or a NaN give unspecified codes.
  *
  *   new_k / new_v (nullable, both or neither): [n][H_kv][d] bf16 rows that
  *   replace the demoted source rows after they have been read - the decode
