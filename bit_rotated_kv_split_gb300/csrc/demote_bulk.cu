@@ -51,7 +51,7 @@ constexpr size_t oB = 0, oA = size_t(kBParts) * kOpBytes;
 constexpr size_t oMeta = oA + size_t(kBufs) * kOpBytes;
 constexpr size_t oXchg = oMeta + size_t(kBufs) * kTile * sizeof(int2);   // [2][2][128][NG] (min, max)
 constexpr size_t oBars = oXchg + 2 * 2 * kTile * 4 * sizeof(float2);   // up to 4 groups
-constexpr size_t kSmem = oBars + (4 * kBufs + 4) * 8 + 16;
+constexpr size_t kSmem = oBars + (4 * kBufs + 10) * 8 + 16;
 constexpr uint32_t kCols = 512;                     // allocation (a power of two) for D[kBufs] x 128
 static_assert(128 * kBufs <= kCols, "tensor memory columns");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
@@ -121,7 +121,7 @@ __device__ __forceinline__ bool epi_finish(const DemoteParams& p, float (&v)[kHe
 #pragma unroll
   for (int q = 0; q < NG; ++q) xs[(hh * kTile + j) * NG + q] = make_float2(mn[q], mx[q]);
   mbar_arrive(xfull + (k & 1));
-  if (!wt.wait(xfull + (k & 1), (k >> 1) & 1)) return false;
+  if (!wt.wait(xfull + (k & 1), (k >> 1) & 1)) return false;   // (the quadrant's two warps)
 #pragma unroll
   for (int q = 0; q < NG; ++q) {
     const float2 other = xs[((1 - hh) * kTile + j) * NG + q];
@@ -230,10 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
   uint64_t* mma_done = bars + kBufs;      // [kBufs] commit
   uint64_t* d_free = bars + 2 * kBufs;    // [kBufs] epilogue
   uint64_t* tma_full = bars + 3 * kBufs; // [kBufs] source tile copies
-  uint64_t* xfull = bars + 4 * kBufs;    // [2] epilogue halves' (min, max) exchange
-  uint64_t* fin = bars + 4 * kBufs + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * kBufs + 3);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kBufs + 3) + 1;
+  uint64_t* xfull = bars + 4 * kBufs;    // [4 quadrants][2] epilogue halves' (min, max) exchange
+  uint64_t* fin = bars + 4 * kBufs + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * kBufs + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kBufs + 9) + 1;
   float2* xchg = reinterpret_cast<float2*>(smem + oXchg);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -248,8 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
       mbar_init(d_free + i, kEpiWarps * 32);
       mbar_init(tma_full + i, 1);
     }
-    mbar_init(xfull, kEpiWarps * 32);
-    mbar_init(xfull + 1, kEpiWarps * 32);
+    for (int i = 0; i < 8; ++i) mbar_init(xfull + i, 2 * 32);   // warps w and w + 4
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -324,11 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) bulk_demote_kernel(const __grid_c
       mbar_arrive(d_free + buf);
       const int ngw = which ? p.ng_v : p.ng_k;
       const float* thr = which ? p.thr_v : p.thr_k;
+      uint64_t* xq = xfull + 2 * quad;   // this quadrant's exchange barriers
       const bool ok =
-          p.codebook ? epi_finish<1, true>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr)
-          : ngw == 4 ? epi_finish<4, false>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr)
-          : ngw == 2 ? epi_finish<2, false>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr)
-                     : epi_finish<1, false>(p, v, xchg, xfull, wt, k, hh, j, m, tau, which, head, thr);
+          p.codebook ? epi_finish<1, true>(p, v, xchg, xq, wt, k, hh, j, m, tau, which, head, thr)
+          : ngw == 4 ? epi_finish<4, false>(p, v, xchg, xq, wt, k, hh, j, m, tau, which, head, thr)
+          : ngw == 2 ? epi_finish<2, false>(p, v, xchg, xq, wt, k, hh, j, m, tau, which, head, thr)
+                     : epi_finish<1, false>(p, v, xchg, xq, wt, k, hh, j, m, tau, which, head, thr);
       if (!ok) break;
     }
   } else if (warp < kMmaWarp) {
