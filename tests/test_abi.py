@@ -79,22 +79,24 @@ def test_decode_unsupported_group(built_lib):
     (dict(src_rows=0), 1), (dict(src_rows=3), 1),
     (dict(new_k=1 << 20), 1), (dict(k_src=(1 << 20) + 8), 2), (dict(dst_pos=(1 << 20) + 2), 2),
 ])
-def test_quantize_append_rejects_bad_arguments(built_lib, kw, status):
+@pytest.mark.parametrize("entry", ["oscar_quantize_append", "oscar_quantize_append_overlapped"])
+def test_quantize_append_rejects_bad_arguments(built_lib, kw, status, entry):
     from bit_rotated_kv_split_gb300 import binding as B
     args = dict(k_src=1 << 20, v_src=1 << 20, src_rows=16, row_stride=128, src_index=None,
                 dst_req=1 << 20, dst_pos=1 << 20, n=4, new_k=None, new_v=None)
     args.update(kw)
-    got = B.lib.oscar_quantize_append(ctypes.byref(_desc()), args["k_src"], args["v_src"],
-                                      args["src_rows"], args["row_stride"], args["src_index"],
-                                      args["dst_req"],
-                                      args["dst_pos"], args["n"], args["new_k"], args["new_v"], None)
+    got = getattr(B.lib, entry)(ctypes.byref(_desc()), args["k_src"], args["v_src"],
+                                args["src_rows"], args["row_stride"], args["src_index"],
+                                args["dst_req"],
+                                args["dst_pos"], args["n"], args["new_k"], args["new_v"], None)
     assert got == status
 
 
-def test_quantize_append_zero_items_is_noop(built_lib):
+@pytest.mark.parametrize("entry", ["oscar_quantize_append", "oscar_quantize_append_overlapped"])
+def test_quantize_append_zero_items_is_noop(built_lib, entry):
     from bit_rotated_kv_split_gb300 import binding as B
-    assert B.lib.oscar_quantize_append(ctypes.byref(_desc()), None, None, 0, 0, None, None, None, 0,
-                                       None, None, None) == 0
+    assert getattr(B.lib, entry)(ctypes.byref(_desc()), None, None, 0, 0, None, None, None, 0,
+                                 None, None, None) == 0
 
 
 # ---------------------------------------------------------------- host rotation routines
