@@ -64,6 +64,7 @@ EXTRA_WORKLOADS = {
 # calibration covariance on the device: C = X^T X / N over 2^20 bf16 rows of
 # 128 values (the C_Q / C_S accumulation of one KV head)
 CALIB_WORKLOAD = "calib-covariance-1m"
+VCALIB_WORKLOAD = "calib-value-covariance-8kv"
 RING_START = 1     # ring slot of the oldest recent token in the steady state
 CACHE_TENSORS = ("pages", "page_table", "hist_len", "sink_k", "sink_v", "sink_len", "recent_k",
                  "recent_v", "recent_len", "recent_start", "r_k", "r_v", "dev_status")
@@ -79,7 +80,7 @@ def _args():
     ap.add_argument("--reps", type=int, default=20, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD["workload"],
-                    choices=[WORKLOAD["workload"]] + sorted(EXTRA_WORKLOADS) + [CALIB_WORKLOAD])
+                    choices=[WORKLOAD["workload"]] + sorted(EXTRA_WORKLOADS) + [CALIB_WORKLOAD, VCALIB_WORKLOAD])
     ap.add_argument("--rotation", default="oscar", choices=["oscar", "canalized32"],
                     help="R_K/R_V of the default workload: the OSCAR eigenbasis rotation, or the OScaR "
                          "block-diagonal one (Hadamard groups of 32 channels)")
@@ -1061,6 +1062,83 @@ def run_calibration(args):
         "gpu_launches": 2 * K, "clocks": clk}))
 
 
+def run_value_calibration(args):
+    """oscar_value_covariance for the 8 KV heads of one layer (4096 seeded
+    calibration queries and 2048 keys/values per head, the calibration sets
+    the default workload's rotations come from): one layer per step, the
+    heads on streams of their own that fork from and join the timed stream,
+    timed with CUDA events on that stream.  The roofline is the tensor pipe's
+    (the work is two dense contractions per head)."""
+    import numpy as np
+    import torch
+    from bit_rotated_kv_split_gb300 import binding as B
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    seed, n_kv, n_q, n_k = WORKLOAD["seed"], WORKLOAD["n_kv_heads"], 4096, 2048
+    outl = synth.outlier_channels(seed, 0, n_kv)
+    qs, ks, vs = [], [], []
+    for hh in range(n_kv):
+        cal = synth.calibration_set(seed, 0, hh, outl[hh], n_q=n_q, n_k=n_k)
+        qs.append(torch.from_numpy(np.ascontiguousarray(cal["q"])).to(torch.bfloat16).to(dev))
+        ks.append(torch.from_numpy(np.ascontiguousarray(cal["k"])).to(torch.bfloat16).to(dev))
+        vs.append(torch.from_numpy(np.ascontiguousarray(cal["v"])).to(torch.bfloat16).to(dev))
+    c = torch.empty((n_kv, 128, 128), dtype=torch.float32, device=dev)
+    # the heads are independent: one stream and one workspace per head, so
+    # their kernels run side by side (a head alone fills a fraction of the SMs)
+    wss = [torch.empty(B.oscar_value_covariance_workspace_bytes(n_q), dtype=torch.uint8, device=dev)
+           for _ in range(n_kv)]
+    stream = torch.cuda.Stream()
+    head_streams = [torch.cuda.Stream() for _ in range(n_kv)]
+    K, W = args.steps, args.warmup
+
+    def layer():
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        for hh in range(n_kv):
+            hs = head_streams[hh]
+            hs.wait_event(ev)
+            B.oscar_value_covariance(qs[hh], ks[hh], vs[hh], c[hh], wss[hh], stream=hs.cuda_stream)
+        for hs in head_streams:
+            done = torch.cuda.Event()
+            done.record(hs)
+            stream.wait_event(done)
+
+    clocks = Clocks(0)
+    with torch.cuda.stream(stream):
+        for _ in range(max(W, 3)):
+            layer()
+        torch.cuda.synchronize()
+        clocks.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            layer()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+    t = e0.elapsed_time(e1) / K / 1e3
+    # per head: Q K^T and S V (2 n_q n_k d each) and (S V)^T (S V) (2 n_q d^2)
+    flops = n_kv * (4.0 * n_q * n_k * 128 + 2.0 * n_q * 128 * 128)
+    tf = flops / t / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except (OSError, KeyError, ValueError):
+        peak, peak_kind = 1900.0, "fallback bf16"
+    print(json.dumps({
+        "metric": "score-weighted value covariance TFLOP/s (C_S = (S V)^T (S V) / N, 8 KV heads of one layer)",
+        "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": VCALIB_WORKLOAD, "n_kv_heads": n_kv, "calibration_queries": n_q,
+                   "calibration_keys": n_k, "d": 128, "l2_policy": "inputs 24 MB, L2-resident (compute-bound)"},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "kernel": "sv_rows_kernel + sv_covariance_kernel (oscar_value_covariance)",
+                     "algorithmic_flops": flops, "peak_kind": peak_kind},
+        "gpu_launches": 3 * n_kv * K, "clocks": clk}))
+
+
 def main():
     args = _args()
     if args.cpu_baseline_worker:
@@ -1071,6 +1149,9 @@ def main():
         return
     if args.workload == CALIB_WORKLOAD:
         run_calibration(args)
+        return
+    if args.workload == VCALIB_WORKLOAD:
+        run_value_calibration(args)
         return
     if args.workload != WORKLOAD["workload"]:
         run_extra(args)
